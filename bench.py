@@ -1,0 +1,344 @@
+#!/usr/bin/env python3
+"""Throughput of the fused 3x3 conv + epilogue on GB300.
+
+One step = one conv_epi_forward over the whole batch of the workload (conv +
+fused chain), inputs resident in HBM.  Default workload: x[128,16,256,256],
+Conv2d 16->64 (k3, s1, p0) with bias, min over channels, tanh, tanh
+(``c2_min_tanh2``), in the tf32 tensor-core mode.
+
+Prints ONE JSON line (rank 0).  Metric: TFLOP/s = 2*N*Cout*Ho*Wo*Cin*9 / time.
+  value      - whole-job TFLOP/s over the K timed steps (max over ranks)
+  e2e        - the same metric through conv_epi_forward_host, host buffers in
+               and out (pinned), copies inside the timed region
+  roofline   - the fused conv kernel against the tf32 tensor peak derived from
+               the measured bf16 peak (x 1.1/2.25, the nominal tf32:bf16 ratio)
+  cpu_baseline - the fp64 oracle on the host cores over a bounded sample
+  clocks     - nvidia-smi samples taken during the timed region
+
+``--impl reference`` times the oracle instead (the only reference this
+method has), on the same workload and metric, one bounded sample per step.
+
+Multi-GPU (torchrun): every rank runs its own full replica of the workload
+(weak scaling, no collective on the data path); value = all ranks' FLOPs /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "fused conv+epilogue TFLOP/s and % of GB300 TF32 dense peak (1 GPU)"
+TF32_PER_BF16 = 1.1 / 2.25        # nominal dense tf32 : bf16 tensor rates
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def conv_flops(wl) -> int:
+    """2 * N * Cout * Ho * Wo * Cin * 9 (multiply-adds counted twice)."""
+    return 2 * wl.N * wl.Cout * (wl.H - 2) * (wl.W - 2) * wl.Cin * 9
+
+
+def algorithmic_bytes(wl) -> int:
+    """x read once + filter + bias + chain parameters + the chain's output."""
+    n_out = {synth.KIND_MIN_TANH2: wl.N * (wl.H - 2) * (wl.W - 2),
+             synth.KIND_SCALE_MIN: wl.N * (wl.H - 2) * (wl.W - 2),
+             synth.KIND_MUL_LRELU_GELU: wl.N * wl.Cout * (wl.H - 2) * (wl.W - 2),
+             synth.KIND_GN_SCALE_POOL_CLAMP: wl.N * wl.Cout * ((wl.H - 2 - wl.pool_k) // wl.pool_k + 1) *
+             ((wl.W - 2 - wl.pool_k) // wl.pool_k + 1)}[wl.kind]
+    params = {synth.KIND_MUL_LRELU_GELU: 1, synth.KIND_GN_SCALE_POOL_CLAMP: 3}.get(wl.kind, 0)
+    return 4 * (wl.N * wl.Cin * wl.H * wl.W + wl.Cout * wl.Cin * 9 + wl.Cout * (1 + params) + n_out)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), d.get("hbm_gbs", FALLBACK_HBM_GBS), "measured"
+    return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            for k, nm in enumerate(names):
+                if len(r) > 5 + k and r[5 + k].lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.barrier(device_ids=[torch.cuda.current_device()])
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(wl, seconds: float, max_images: int):
+    """Time the fp64 oracle on whole images of the workload until ~seconds."""
+    import oracle
+    one = wl.with_batch(1)
+    t = synth.make_inputs(one, seed=0)
+    ch = oracle.chain_for(one, t)
+    cores = os.cpu_count() or 1
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(t.x, t.w, t.b, ch, nthreads=cores, want_index=False)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= max_images:
+            break
+    return conv_flops(one) * done / el / 1e12, el, done, cores
+
+
+def traffic_for(kernel_src_hash: str, workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("src_sha1") != kernel_src_hash:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def kernel_hash():
+    h = hashlib.sha1()
+    for name in ("tc.cu", "internal.h"):
+        with open(os.path.join(ROOT, "x3_conv2d_epilogue_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0, 1)
+    vals, t_all = [], 0.0
+    cores = os.cpu_count() or 1
+    for _ in range(args.steps):
+        v, el, done, cores = oracle_sample(wl, args.ref_seconds, 1 << 30)
+        vals.append(v)
+        t_all += el
+    value = float(np.mean(vals))
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
+            "config": {"workload": wl.name, "x": [wl.N, wl.Cin, wl.H, wl.W], "Cout": wl.Cout, "chain": wl.desc},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"whole images of {wl.name}, ~{args.ref_seconds:.0f} s per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c2_min_tanh2", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--mode", choices=["tf32", "fp32"], default="tf32")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length for cpu_baseline")
+    ap.add_argument("--ref-seconds", type=float, default=15.0, help="oracle sample length per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    wl = synth.WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, wl, world, rank)
+
+    import torch
+    import x3_conv2d_epilogue_gb300 as ce
+    torch.cuda.set_device(local)
+    mode = ce.MODE_TF32 if args.mode == "tf32" else ce.MODE_FP32
+
+    # inputs resident in HBM (same seeded recipe on every rank: weak scaling)
+    t = synth.make_inputs(wl, seed=0)
+    host = {k: getattr(t, k) for k in ("x", "w", "b", "mult", "gamma", "beta", "scale")}
+    dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in host.items()}
+    chan = dev["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else dev["scale"]
+    epi = ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan, lrelu_slope=wl.lrelu_slope, groups=wl.groups,
+                      eps=wl.eps, gamma=dev["gamma"], beta=dev["beta"], pool_k=wl.pool_k, clamp_lo=wl.clamp_lo,
+                      clamp_hi=wl.clamp_hi)
+    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode)
+    ce.conv_epi_reserve(h, epi)
+    shape = ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, epi, mode)
+    out = torch.empty(shape, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.Stream()
+    x_bytes = t.x.nbytes
+
+    def step():
+        ce.conv_epi_forward(h, dev["x"], dev["w"], dev["b"], epi, out, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    ce.conv_epi_sync(h, stream)
+    launches_per_step = ce.conv_epi_last_launch_count(h)
+
+    # ---- timed region: K steps, per-step CUDA events on the launching stream ----
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let the sampler start
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ce.conv_epi_sync(h, stream)
+    total_ms = t_begin.elapsed_time(t_end)
+    per = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(total_ms, world)
+    flops = conv_flops(wl)
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    kern_ms = float(np.mean(per))
+
+    # ---- end to end through the host-buffer entry point ----
+    pin = {k: (None if v is None else torch.from_numpy(v).pin_memory()) for k, v in host.items()}
+    chan_h = pin["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else pin["scale"]
+    epi_h = ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan_h, lrelu_slope=wl.lrelu_slope, groups=wl.groups,
+                        eps=wl.eps, gamma=pin["gamma"], beta=pin["beta"], pool_k=wl.pool_k, clamp_lo=wl.clamp_lo,
+                        clamp_hi=wl.clamp_hi)
+    out_h = torch.empty(shape, dtype=torch.float32).pin_memory()
+    ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)   # warm (allocates staging)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = flops * args.e2e_steps * world / e2e_s / 1e12
+    h2d = sum(v.nbytes for v in host.values() if v is not None)
+    d2h = out_h.numel() * 4
+
+    ce.conv_epi_destroy(h)
+
+    if rank != 0:
+        return 0
+
+    bf16, hbm, src = peaks()
+    tf32_peak = bf16 * TF32_PER_BF16
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, el, done, cores = oracle_sample(wl, args.cpu_seconds, wl.N)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{done} of {wl.N} images of {wl.name} ({el:.1f} s, fp64 direct loops)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.mode, "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": wl.name, "x": [wl.N, wl.Cin, wl.H, wl.W], "Cout": wl.Cout, "chain": wl.desc,
+                   "mode": args.mode, "l2": f"inputs larger than L2 ({x_bytes / 1e6:.0f} MB of x per step)",
+                   "per_gpu_batch": wl.N},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tf32_peak, "traffic": traffic_for(kernel_hash(), wl.name),
+                     "peak_source": f"{src} bf16 burst {bf16:.1f} x {TF32_PER_BF16:.4f}",
+                     "kernel": "conv_epi forward (prep + fused conv kernel)",
+                     "hbm_gbs": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm,
+                     "hbm_frac": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9 / hbm},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "kernel_ms": {"mean": kern_ms, "min": float(np.min(per)), "max": float(np.max(per))},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

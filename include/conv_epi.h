@@ -1,0 +1,159 @@
+/*
+ * conv_epi.h -- fused 3x3 Conv2d + epilogue for NVIDIA GB300 (sm_103a).
+ *
+ * One call computes, for an NCHW float32 input x[N][Cin][H][W], filter
+ * w[Cout][Cin][3][3] and bias b[Cout],
+ *
+ *     y[n,co,i,j] = b[co] + sum_{ci,kh,kw} w[co,ci,kh,kw] * x[n,ci,i+kh,j+kw]
+ *
+ * (kernel 3, stride 1, no padding: Ho = H-2, Wo = W-2) as an implicit GEMM
+ * with K = Cin*9, and applies one post-conv chain inside the GEMM epilogue.
+ * The full conv output y never reaches memory when the chain reduces it.
+ *
+ * The chains are the four models of the POPCORNBENCH kernel-writing
+ * transcripts (model Kimi-K2.6, level 2), problems
+ *   p25  min over channels (keepdim) -> tanh -> tanh       CONV_EPI_MIN_TANH2
+ *   p32  x scalar -> min over channels (keepdim)            CONV_EPI_SCALE_MIN
+ *   p54  x multiplier[C] -> LeakyReLU -> GELU (exact erf)   CONV_EPI_MUL_LRELU_GELU
+ *   p85  GroupNorm -> x scale[C] -> MaxPool(k) -> clamp     CONV_EPI_GN_SCALE_POOL_CLAMP
+ * Each page states its problem as a module built with the model's arguments
+ * whose forward(x) uses the module's parameters and returns the model's
+ * output; here the parameters travel in the arguments of conv_epi_forward.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, contiguous, row-major (NCHW), float32, and must start
+ *     on a 16-byte boundary.  "device pointer" means memory the current CUDA
+ *     device can read (cudaMalloc, torch CUDA tensors); "host pointer" means
+ *     ordinary (ideally pinned) host memory.
+ *   - The caller owns every tensor it passes; the library owns the handle and
+ *     its workspace (packed weights, GroupNorm partial sums, pooled max/min).
+ *   - Calls are asynchronous on the given stream unless stated otherwise and
+ *     return a status; no C++ exception crosses this boundary.
+ *   - There is no CPU fallback: without a usable sm_103a device, calls that
+ *     compute return CONV_EPI_ERR_CUDA or CONV_EPI_ERR_UNSUPPORTED.
+ */
+#ifndef CONV_EPI_H
+#define CONV_EPI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CONV_EPI_API __attribute__((visibility("default")))
+
+typedef struct conv_epi_handle_s *conv_epi_handle; /* opaque, library-owned */
+
+typedef enum {
+    CONV_EPI_OK = 0,
+    CONV_EPI_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad chain parameters */
+    CONV_EPI_ERR_UNSUPPORTED = 2,  /* shape/chain outside what the chosen mode implements */
+    CONV_EPI_ERR_ALIGNMENT = 3,    /* a tensor does not start on a 16-byte boundary */
+    CONV_EPI_ERR_CUDA = 4,         /* a CUDA runtime call failed (see conv_epi_last_cuda_error) */
+    CONV_EPI_ERR_TIMEOUT = 5,      /* a kernel gave up waiting on a pipeline barrier */
+    CONV_EPI_ERR_NO_MEMORY = 6,    /* workspace allocation failed */
+    CONV_EPI_ERR_DEVICE = 7        /* a kernel raised its own error flag */
+} conv_epi_status;
+
+/* Arithmetic of the convolution. */
+typedef enum {
+    CONV_EPI_MODE_TF32 = 0, /* 5th-gen tensor cores (tcgen05), tf32 operands, fp32 accumulate */
+    CONV_EPI_MODE_FP32 = 1  /* CUDA cores, fp32 fused multiply-add (strict-tolerance mode) */
+} conv_epi_mode;
+
+/* Problem description.  Kernel 3x3, stride 1, padding 0 are implied. */
+typedef struct {
+    int N, Cin, H, W, Cout; /* input [N][Cin][H][W], filter [Cout][Cin][3][3] */
+    int mode;               /* conv_epi_mode */
+} conv_epi_desc;
+
+typedef enum {
+    CONV_EPI_MIN_TANH2 = 1,          /* out[n,0,i,j] = tanh(tanh(min_c scalar*y[n,c,i,j]))   [N,1,Ho,Wo] */
+    CONV_EPI_SCALE_MIN = 2,          /* out[n,0,i,j] = min_c scalar*y[n,c,i,j]               [N,1,Ho,Wo] */
+    CONV_EPI_MUL_LRELU_GELU = 3,     /* t = y*chan_scale[c]; t = max(t,0)+slope*min(t,0);
+                                        out = 0.5 t (1 + erf(t/sqrt 2))                     [N,Cout,Ho,Wo] */
+    CONV_EPI_GN_SCALE_POOL_CLAMP = 4 /* z = ((y-mean_ng)*rstd_ng*gamma[c] + beta[c]) * chan_scale[c],
+                                        mean/biased var over (C/groups, Ho, Wo) of each (n, group),
+                                        rstd = 1/sqrt(var+eps); out = clamp(maxpool_k(z), lo, hi)
+                                        with stride k, floor mode                  [N,Cout,Hp,Wp] */
+} conv_epi_kind;
+
+/* Post-conv chain.  Parameter tensors are device pointers of Cout floats
+ * (host pointers for conv_epi_forward_host). */
+typedef struct {
+    int kind;                 /* conv_epi_kind */
+    float scalar;             /* MIN kinds: multiplier before the min (any sign; 1 = none) */
+    const float *chan_scale;  /* MUL_LRELU_GELU: multiplier[Cout]; GN kind: scale[Cout] after the norm */
+    float lrelu_slope;        /* MUL_LRELU_GELU: LeakyReLU negative slope (0.01 on the page) */
+    int groups;               /* GN: number of groups, divides Cout */
+    float eps;                /* GN: added to the variance inside the square root */
+    const float *gamma;       /* GN: weight[Cout] */
+    const float *beta;        /* GN: bias[Cout] */
+    int pool_k;               /* GN: max-pool kernel and stride (>= 1) */
+    float clamp_lo, clamp_hi; /* GN: clamp bounds after the pool (lo <= hi) */
+    int32_t *index_out;       /* optional device pointer, NULL to skip; same shape as out:
+                                 MIN kinds -> channel of the minimum (first on ties);
+                                 GN kind   -> window offset a*k+b of the pooled value
+                                              (first row-major on ties);
+                                 MUL_LRELU_GELU -> not produced (must be NULL).
+                                 Only CONV_EPI_MODE_FP32 produces indices. */
+} conv_epi_epilogue_desc;
+
+/* Output shape of a chain: shape[4] = {N, C, Ho', Wo'}.  Pure host call. */
+CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
+                                                   const conv_epi_epilogue_desc *epi,
+                                                   int64_t shape[4]);
+
+/* Create a handle for one problem size and mode on the current CUDA device.
+ * Validates the description and allocates the workspace every chain needs
+ * except the GN chain's pooled buffers, which are allocated on the first GN
+ * forward (conv_epi_reserve allocates them up front).  Synchronous. */
+CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi_handle *out);
+
+/* Allocate, ahead of the first forward, whatever workspace `epi` will need
+ * (so that forward itself never allocates, e.g. before graph capture). */
+CONV_EPI_API conv_epi_status conv_epi_reserve(conv_epi_handle h, const conv_epi_epilogue_desc *epi);
+
+/* Run conv + chain on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  x, w, b, the chain's parameter tensors and out are device
+ * pointers; out must hold conv_epi_output_shape() floats.  Asynchronous:
+ * argument errors are returned at once, device-side errors (a barrier wait
+ * that timed out) by conv_epi_sync(). */
+CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x, const float *w,
+                                              const float *b, const conv_epi_epilogue_desc *epi,
+                                              float *out, void *stream);
+
+/* Same computation from HOST buffers: copies x, w, b and the chain's
+ * parameters to library-owned device buffers on `stream`, runs the forward,
+ * copies the result back into host `out` and waits for the stream.  Every
+ * pointer (including those inside `epi`) is a host pointer. */
+CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const float *x, const float *w,
+                                                   const float *b, const conv_epi_epilogue_desc *epi,
+                                                   float *out, void *stream);
+
+/* Wait for `stream` and report any device-side error flag the library's
+ * kernels raised on this handle since the last call (then clear it). */
+CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream);
+
+/* Release the handle and its workspace (synchronises the device first). */
+CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h);
+
+/* Bytes of device workspace the handle holds now. */
+CONV_EPI_API size_t conv_epi_workspace_bytes(conv_epi_handle h);
+
+/* Number of kernel launches the last conv_epi_forward issued. */
+CONV_EPI_API int conv_epi_last_launch_count(conv_epi_handle h);
+
+/* Static strings; never NULL. */
+CONV_EPI_API const char *conv_epi_status_string(conv_epi_status s);
+CONV_EPI_API const char *conv_epi_last_cuda_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+CONV_EPI_API int conv_epi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CONV_EPI_H */

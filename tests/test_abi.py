@@ -1,0 +1,111 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+entry point the header declares, and its host-side validation answers
+without touching a device."""
+import ctypes as C
+import os
+
+import numpy as np
+import pytest
+
+import x3_conv2d_epilogue_gb300 as ce
+from x3_conv2d_epilogue_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ce.LIB_PATH):
+        _build.build()
+    return ce._lib()
+
+
+def test_header_declares_the_api():
+    names = ce.exported_symbols()
+    for must in ("conv_epi_create", "conv_epi_forward", "conv_epi_destroy", "conv_epi_forward_host",
+                 "conv_epi_output_shape", "conv_epi_status_string", "conv_epi_sync"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in ce.exported_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", ce.LIB_PATH], capture_output=True, text=True)
+    if out.returncode:
+        pytest.skip("nm not available")
+    names = {ln.split()[-1] for ln in out.stdout.splitlines() if ln.strip()}
+    assert names == set(ce.exported_symbols())
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert ce.conv_epi_status_string(s)
+    assert "unknown" in ce.conv_epi_status_string(99)
+    assert ce.conv_epi_version() >= 10000
+
+
+def shape(N, Cin, H, W, Cout, epi, mode=ce.MODE_TF32):
+    return ce.conv_epi_output_shape(N, Cin, H, W, Cout, epi, mode)
+
+
+def test_output_shapes(lib):
+    assert shape(2, 16, 32, 32, 64, ce.epilogue(ce.MIN_TANH2)) == (2, 1, 30, 30)
+    assert shape(128, 16, 256, 256, 64, ce.epilogue(ce.MIN_TANH2)) == (128, 1, 254, 254)
+    assert shape(64, 64, 256, 256, 128, ce.epilogue(ce.SCALE_MIN, scalar=2.0)) == (64, 1, 254, 254)
+    assert shape(64, 64, 256, 256, 64, ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=16)) == (64, 64, 254, 254)
+    gn = ce.epilogue(ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=16, pool_k=4)
+    assert shape(128, 8, 128, 128, 64, gn) == (128, 64, 31, 31)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(N=0), dict(Cin=0), dict(H=2), dict(W=1), dict(Cout=0), dict(mode=7),
+])
+def test_bad_descriptions_rejected(lib, bad):
+    d = dict(N=1, Cin=4, H=8, W=8, Cout=8, mode=ce.MODE_FP32)
+    d.update(bad)
+    with pytest.raises(ce.ConvEpiError) as ei:
+        ce.conv_epi_output_shape(d["N"], d["Cin"], d["H"], d["W"], d["Cout"], ce.epilogue(ce.MIN_TANH2), d["mode"])
+    assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("kw", [
+    dict(kind=9),
+    dict(kind=ce.MUL_LRELU_GELU),                                     # no multiplier
+    dict(kind=ce.MUL_LRELU_GELU, chan_scale=16, index_out=16),        # no index for this chain
+    dict(kind=ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16),       # no beta
+    dict(kind=ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=3),   # 3 does not divide 8
+    dict(kind=ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=2, pool_k=0),
+    dict(kind=ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=2, pool_k=7),  # > Ho
+    dict(kind=ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=2, clamp_lo=1, clamp_hi=0),
+    dict(kind=ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=2, eps=-1.0),
+    dict(kind=ce.SCALE_MIN, scalar=float("nan")),
+])
+def test_bad_chains_rejected(lib, kw):
+    kind = kw.pop("kind")
+    with pytest.raises(ce.ConvEpiError) as ei:
+        ce.conv_epi_output_shape(1, 4, 8, 8, 8, ce.epilogue(kind, **kw))
+    assert ei.value.status == 1
+
+
+def test_null_pointers_rejected(lib):
+    L = lib
+    assert L.conv_epi_create(None, None) == 1
+    assert L.conv_epi_forward(None, None, None, None, None, None, None) == 1
+    assert L.conv_epi_forward_host(None, None, None, None, None, None, None) == 1
+    assert L.conv_epi_destroy(None) == 1
+    assert L.conv_epi_sync(None, None) == 1
+    assert L.conv_epi_workspace_bytes(None) == 0
+    assert L.conv_epi_output_shape(None, None, None) == 1
+
+
+def test_create_without_device_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = C.c_void_p()
+    d = ce.Desc(1, 4, 8, 8, 8, ce.MODE_FP32)
+    st = lib.conv_epi_create(C.byref(d), C.byref(h))
+    assert st in (2, 4) and not h.value
+    assert isinstance(ce.conv_epi_status_string(st), str)

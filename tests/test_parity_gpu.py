@@ -1,0 +1,114 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, on
+the same seeded inputs, element by element.
+
+Small cases keep every workload's chain, channel counts and filter size but
+shrink N and H (and sometimes W) so the oracle finishes in seconds while the
+kernels still run several tiles and a ragged tail.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity_util import (check_fp32, check_index, check_tf32, gpu_run, min_index_gap, oracle_run,
+                         pool_index_gap)
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+SMALL = {
+    "pr1": W["pr1_min_tanh2"],
+    "c2s": W["c2_min_tanh2"].resized(N=2, H=21),                              # 19 output rows (odd tail)
+    "c2w": W["c2_min_tanh2"].resized(N=1, H=9, W=200),                        # ragged row width
+    "c3s": W["c3_mul_lrelu_gelu"].resized(N=2, H=11),
+    "c4s": W["c4_scale_min"].resized(N=1, H=12),
+    "c4neg": W["c4_scale_min"].resized(N=1, H=7, W=96, scalar=-1.5),          # max branch
+    "c5s": W["c5_gn_pool_clamp"].resized(N=2, H=42),                         # 40 rows: 10 bands, no tail
+    "c5t": W["c5_gn_pool_clamp"].resized(N=2, H=40),                         # 38 rows: 9 bands + 2 stat rows
+}
+FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
+
+
+def modes():
+    import x3_conv2d_epilogue_gb300 as ce
+    return {"fp32": ce.MODE_FP32, "tf32": ce.MODE_TF32}
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32"])
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_small_parity(case, mode):
+    wl = SMALL[case]
+    t = synth.make_inputs(wl, seed=0)
+    m = modes()[mode]
+    got, idx = gpu_run(wl, t, m, want_index=(mode == "fp32" and wl.kind != synth.KIND_MUL_LRELU_GELU))
+    ref, ref_idx = oracle_run(wl, t)
+    if mode == "fp32":
+        check_fp32(got, ref, case)
+    else:
+        check_tf32(got, ref, case)
+    if idx is not None:
+        y = oracle.conv3x3(t.x, t.w, t.b)
+        if wl.kind == synth.KIND_GN_SCALE_POOL_CLAMP:
+            sign = np.sign(t.gamma.astype(np.float64) * t.scale)[None, :].repeat(wl.N, 0)
+            gap = pool_index_gap(y, wl.pool_k, np.where(sign >= 0, 1.0, -1.0)) * np.abs(
+                (t.gamma.astype(np.float64) * t.scale))[None, :, None, None]
+        else:
+            gap = min_index_gap(y, wl.scalar)
+        check_index(idx, ref_idx, gap, case)
+
+
+@pytest.mark.parametrize("case", sorted(FP32_ONLY))
+def test_fp32_only_shapes(case):
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = FP32_ONLY[case]
+    t = synth.make_inputs(wl, seed=1)
+    got, idx = gpu_run(wl, t, ce.MODE_FP32, want_index=True)
+    ref, ref_idx = oracle_run(wl, t)
+    check_fp32(got, ref, case)
+    check_index(idx, ref_idx, min_index_gap(oracle.conv3x3(t.x, t.w, t.b), wl.scalar), case)
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32"])
+@pytest.mark.parametrize("case", ["pr1", "c4s", "c2s"])
+def test_integer_inputs_bit_exact(case, mode):
+    """Integer x, w, b with |v| <= 8: every product and partial sum is an
+    integer below 2^24 and every operand fits tf32, so the conv is exact in
+    both modes and the min chain's value must match to the last bit."""
+    wl = SMALL[case]
+    t = synth.make_integer_inputs(wl, seed=3)
+    got, _ = gpu_run(wl, t, modes()[mode])
+    y = oracle.conv3x3(t.x, t.w, t.b)
+    ref, _ = oracle.chain_min(y, wl.scalar, wl.kind == synth.KIND_MIN_TANH2)
+    if wl.kind == synth.KIND_SCALE_MIN:
+        np.testing.assert_array_equal(got.astype(np.float64), ref)
+    else:
+        # tanh(tanh(integer)): the fp32 tanhf of an exact argument
+        np.testing.assert_allclose(got, ref, rtol=0, atol=2e-7)
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32"])
+def test_delta_kernel_reproduces_input(mode):
+    """Centre-tap identity filter + per-channel chain with multiplier 1 and
+    slope 1: out = GELU(x cropped), to within the mode's tolerance."""
+    wl = W["c3_mul_lrelu_gelu"].resized(N=1, H=9, lrelu_slope=1.0)
+    t = synth.make_inputs(wl, seed=5)
+    t.w[:] = 0
+    for co in range(wl.Cout):
+        t.w[co, co % wl.Cin, 1, 1] = 1.0
+    t.b[:] = 0
+    t.mult[:] = 1.0
+    got, _ = gpu_run(wl, t, modes()[mode])
+    ref, _ = oracle_run(wl, t)
+    xc = t.x[:, np.arange(wl.Cout) % wl.Cin, 1:-1, 1:-1].astype(np.float64)
+    gelu = 0.5 * xc * (1 + np.vectorize(__import__("math").erf)(xc / np.sqrt(2)))
+    np.testing.assert_allclose(ref, gelu, rtol=1e-12, atol=1e-12)
+    (check_fp32 if mode == "fp32" else check_tf32)(got, ref, "delta")
+
+
+def test_repeated_forward_is_deterministic():
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = SMALL["c5t"]
+    t = synth.make_inputs(wl, seed=9)
+    a, _ = gpu_run(wl, t, ce.MODE_FP32, repeats=1)
+    b, _ = gpu_run(wl, t, ce.MODE_FP32, repeats=3)
+    np.testing.assert_array_equal(a, b)

@@ -1,0 +1,210 @@
+"""Python binding of libconv_epi: fused 3x3 Conv2d + epilogue on GB300.
+
+Argument marshalling only.  Every entry point has the name of the C function
+it calls (include/conv_epi.h) and takes torch CUDA tensors (or, for
+``conv_epi_forward_host``, numpy arrays / CPU tensors) in place of pointers.
+Every step of the computation runs in the library's CUDA kernels; there is no
+fallback: if ``libconv_epi.so`` is missing or the device is not sm_103a, the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libconv_epi.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "conv_epi.h")
+
+MODE_TF32, MODE_FP32 = 0, 1
+MIN_TANH2, SCALE_MIN, MUL_LRELU_GELU, GN_SCALE_POOL_CLAMP = 1, 2, 3, 4
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CUDA", 5: "TIMEOUT",
+          6: "NO_MEMORY", 7: "DEVICE"}
+
+
+class ConvEpiError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib().conv_epi_status_string(status).decode()
+        if status == 4:
+            msg += " -- " + _lib().conv_epi_last_cuda_error().decode()
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({msg})")
+
+
+class Desc(C.Structure):
+    _fields_ = [("N", C.c_int), ("Cin", C.c_int), ("H", C.c_int), ("W", C.c_int), ("Cout", C.c_int),
+                ("mode", C.c_int)]
+
+
+class EpilogueDesc(C.Structure):
+    _fields_ = [
+        ("kind", C.c_int),
+        ("scalar", C.c_float),
+        ("chan_scale", C.c_void_p),
+        ("lrelu_slope", C.c_float),
+        ("groups", C.c_int),
+        ("eps", C.c_float),
+        ("gamma", C.c_void_p),
+        ("beta", C.c_void_p),
+        ("pool_k", C.c_int),
+        ("clamp_lo", C.c_float),
+        ("clamp_hi", C.c_float),
+        ("index_out", C.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_L = None
+
+
+def _lib():
+    global _L
+    with _lock:
+        if _L is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built: run __graft_entry__.build() "
+                                   "(the CUDA path has no fallback)")
+            L = C.CDLL(LIB_PATH)
+            P, I = C.c_void_p, C.c_int
+            L.conv_epi_status_string.restype = C.c_char_p
+            L.conv_epi_status_string.argtypes = [I]
+            L.conv_epi_last_cuda_error.restype = C.c_char_p
+            L.conv_epi_output_shape.argtypes = [C.POINTER(Desc), C.POINTER(EpilogueDesc), P]
+            L.conv_epi_create.argtypes = [C.POINTER(Desc), C.POINTER(P)]
+            L.conv_epi_reserve.argtypes = [P, C.POINTER(EpilogueDesc)]
+            L.conv_epi_forward.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
+            L.conv_epi_forward_host.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
+            L.conv_epi_sync.argtypes = [P, P]
+            L.conv_epi_destroy.argtypes = [P]
+            L.conv_epi_workspace_bytes.argtypes = [P]
+            L.conv_epi_workspace_bytes.restype = C.c_size_t
+            L.conv_epi_last_launch_count.argtypes = [P]
+            L.conv_epi_version.restype = I
+            _L = L
+    return _L
+
+
+def exported_symbols():
+    """Names the header declares as CONV_EPI_API entry points."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"CONV_EPI_API\s+[\w\s\*]*?\b(conv_epi_\w+)\s*\(", text)))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    if hasattr(t, "ctypes"):
+        return t.ctypes.data
+    return int(t)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(st, where):
+    if st:
+        raise ConvEpiError(st, where)
+
+
+def epilogue(kind, scalar=1.0, chan_scale=None, lrelu_slope=0.01, groups=16, eps=1e-5, gamma=None, beta=None,
+             pool_k=4, clamp_lo=0.0, clamp_hi=1.0, index_out=None):
+    """Build a conv_epi_epilogue_desc; tensors are kept alive on the object."""
+    e = EpilogueDesc(kind, scalar, _ptr(chan_scale), lrelu_slope, groups, eps, _ptr(gamma), _ptr(beta), pool_k,
+                     clamp_lo, clamp_hi, _ptr(index_out))
+    e._keep = (chan_scale, gamma, beta, index_out)
+    return e
+
+
+def conv_epi_output_shape(N, Cin, H, W, Cout, epi, mode=MODE_TF32):
+    import numpy as np
+    s = np.zeros(4, dtype=np.int64)
+    d = Desc(N, Cin, H, W, Cout, mode)
+    _check(_lib().conv_epi_output_shape(C.byref(d), C.byref(epi), s.ctypes.data), "conv_epi_output_shape")
+    return tuple(int(v) for v in s)
+
+
+def conv_epi_create(N, Cin, H, W, Cout, mode=MODE_TF32):
+    h = C.c_void_p()
+    d = Desc(N, Cin, H, W, Cout, mode)
+    _check(_lib().conv_epi_create(C.byref(d), C.byref(h)), "conv_epi_create")
+    return h
+
+
+def conv_epi_reserve(h, epi):
+    _check(_lib().conv_epi_reserve(h, C.byref(epi)), "conv_epi_reserve")
+
+
+def conv_epi_forward(h, x, w, b, epi, out, stream=None):
+    _check(_lib().conv_epi_forward(h, _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out), _stream(stream)),
+           "conv_epi_forward")
+    return out
+
+
+def conv_epi_forward_host(h, x, w, b, epi, out, stream=None):
+    _check(_lib().conv_epi_forward_host(h, _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out), _stream(stream)),
+           "conv_epi_forward_host")
+    return out
+
+
+def conv_epi_sync(h, stream=None):
+    _check(_lib().conv_epi_sync(h, _stream(stream)), "conv_epi_sync")
+
+
+def conv_epi_destroy(h):
+    _check(_lib().conv_epi_destroy(h), "conv_epi_destroy")
+
+
+def conv_epi_workspace_bytes(h):
+    return _lib().conv_epi_workspace_bytes(h)
+
+
+def conv_epi_last_launch_count(h):
+    return _lib().conv_epi_last_launch_count(h)
+
+
+def conv_epi_version():
+    return _lib().conv_epi_version()
+
+
+def conv_epi_status_string(status):
+    return _lib().conv_epi_status_string(status).decode()
+
+
+class ConvEpi:
+    """Owns one handle; ``forward`` allocates the output with torch."""
+
+    def __init__(self, N, Cin, H, W, Cout, mode=MODE_TF32):
+        self.dims = (N, Cin, H, W, Cout)
+        self.mode = mode
+        self.h = conv_epi_create(N, Cin, H, W, Cout, mode)
+
+    def output_shape(self, epi):
+        return conv_epi_output_shape(*self.dims, epi, self.mode)
+
+    def forward(self, x, w, b, epi, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(self.output_shape(epi), device=x.device, dtype=torch.float32)
+        return conv_epi_forward(self.h, x, w, b, epi, out, stream)
+
+    def close(self):
+        if self.h:
+            conv_epi_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,304 @@
+// api.cu -- the C ABI of libconv_epi: argument validation, workspace
+// ownership, dispatch to the tf32 tensor-core path or the fp32 CUDA-core
+// path, host-buffer forward and device error reporting.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+thread_local char g_cuda_err[512] = "no CUDA error recorded";
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+conv_epi_status check_desc(const conv_epi_desc *d) {
+    if (!d) return CONV_EPI_ERR_INVALID_ARG;
+    if (d->N < 1 || d->Cin < 1 || d->Cout < 1 || d->H < 3 || d->W < 3) return CONV_EPI_ERR_INVALID_ARG;
+    if (d->mode != CONV_EPI_MODE_TF32 && d->mode != CONV_EPI_MODE_FP32) return CONV_EPI_ERR_INVALID_ARG;
+    // element counts and offsets are kept in 64-bit, but every single tensor
+    // must stay below 2^31 elements
+    const int64_t nx = (int64_t)d->N * d->Cin * d->H * d->W;
+    const int64_t ny = (int64_t)d->N * d->Cout * (d->H - 2) * (d->W - 2);
+    if (nx >= (1ll << 31) || ny >= (1ll << 31)) return CONV_EPI_ERR_UNSUPPORTED;
+    return CONV_EPI_OK;
+}
+
+// Validates the chain description itself (not its pointers' alignment).
+conv_epi_status check_epi(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
+    if (!e) return CONV_EPI_ERR_INVALID_ARG;
+    const int Ho = d.H - 2, Wo = d.W - 2;
+    switch (e->kind) {
+    case CONV_EPI_MIN_TANH2:
+    case CONV_EPI_SCALE_MIN:
+        if (!isfinite(e->scalar)) return CONV_EPI_ERR_INVALID_ARG;
+        return CONV_EPI_OK;
+    case CONV_EPI_MUL_LRELU_GELU:
+        if (!e->chan_scale || !isfinite(e->lrelu_slope)) return CONV_EPI_ERR_INVALID_ARG;
+        if (e->index_out) return CONV_EPI_ERR_INVALID_ARG;  // this chain has no index output
+        return CONV_EPI_OK;
+    case CONV_EPI_GN_SCALE_POOL_CLAMP:
+        if (!e->chan_scale || !e->gamma || !e->beta) return CONV_EPI_ERR_INVALID_ARG;
+        if (e->groups < 1 || d.Cout % e->groups != 0) return CONV_EPI_ERR_INVALID_ARG;
+        if (e->pool_k < 1 || e->pool_k > Ho || e->pool_k > Wo) return CONV_EPI_ERR_INVALID_ARG;
+        if (!(e->eps >= 0.0f) || !isfinite(e->eps)) return CONV_EPI_ERR_INVALID_ARG;
+        if (!(e->clamp_lo <= e->clamp_hi)) return CONV_EPI_ERR_INVALID_ARG;
+        return CONV_EPI_OK;
+    default:
+        return CONV_EPI_ERR_INVALID_ARG;
+    }
+}
+
+int pool_out(int n, int k) { return (n - k) / k + 1; }
+
+void shape_of(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, int64_t s[4]) {
+    const int Ho = d.H - 2, Wo = d.W - 2;
+    s[0] = d.N;
+    if (e.kind == CONV_EPI_MIN_TANH2 || e.kind == CONV_EPI_SCALE_MIN) {
+        s[1] = 1, s[2] = Ho, s[3] = Wo;
+    } else if (e.kind == CONV_EPI_MUL_LRELU_GELU) {
+        s[1] = d.Cout, s[2] = Ho, s[3] = Wo;
+    } else {
+        s[1] = d.Cout, s[2] = pool_out(Ho, e.pool_k), s[3] = pool_out(Wo, e.pool_k);
+    }
+}
+
+conv_epi_status check_mode_support(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
+    if (d.mode == CONV_EPI_MODE_FP32)
+        return e ? conv_epi::simt_supported(d, *e) : CONV_EPI_OK;
+    return conv_epi::tc_supported(d, e);
+}
+
+conv_epi_status forward_checks(conv_epi_handle h, const float *x, const float *w, const float *b,
+                               const conv_epi_epilogue_desc *e, const float *out) {
+    if (!h || !x || !w || !b || !out || !e) return CONV_EPI_ERR_INVALID_ARG;
+    conv_epi_status st = check_epi(h->d, e);
+    if (st) return st;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(out)) return CONV_EPI_ERR_ALIGNMENT;
+    if (e->index_out && (reinterpret_cast<uintptr_t>(e->index_out) & 3u)) return CONV_EPI_ERR_ALIGNMENT;
+    if (e->index_out && h->d.mode != CONV_EPI_MODE_FP32) return CONV_EPI_ERR_UNSUPPORTED;
+    return check_mode_support(h->d, e);
+}
+
+}  // namespace
+
+namespace conv_epi {
+
+conv_epi_status cuda_fail(cudaError_t e, const char *what) {
+    snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+    (void)cudaGetLastError();  // clear a sticky-free error so later calls can proceed
+    return e == cudaErrorMemoryAllocation ? CONV_EPI_ERR_NO_MEMORY : CONV_EPI_ERR_CUDA;
+}
+
+conv_epi_status ensure_gn_workspace(conv_epi_handle h, int pool_k, int groups, int units) {
+    const conv_epi_desc &d = h->d;
+    if (h->gn_mem && h->gn_pool_k == pool_k && h->gn_groups == groups && h->gn_units == units)
+        return CONV_EPI_OK;
+    const int Hp = pool_out(h->Ho, pool_k), Wp = pool_out(h->Wo, pool_k);
+    const size_t npool = (size_t)d.N * d.Cout * Hp * Wp;
+    const size_t npart = (size_t)d.N * units * groups * 2;
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    const size_t bytes = 2 * up(npool * sizeof(float)) + 2 * up(npool * sizeof(int32_t)) + up(npart * sizeof(double));
+    if (h->gn_mem && bytes <= h->gn_bytes) {
+        // reuse the larger buffer
+    } else {
+        if (h->gn_mem) {
+            CE_CUDA(cudaDeviceSynchronize());
+            CE_CUDA(cudaFree(h->gn_mem));
+            h->gn_mem = nullptr, h->gn_bytes = 0;
+        }
+        CE_CUDA(cudaMalloc(&h->gn_mem, bytes));
+        h->gn_bytes = bytes;
+    }
+    char *p = static_cast<char *>(h->gn_mem);
+    h->gn.pmax = reinterpret_cast<float *>(p), p += up(npool * sizeof(float));
+    h->gn.pmin = reinterpret_cast<float *>(p), p += up(npool * sizeof(float));
+    h->gn.amax = reinterpret_cast<int32_t *>(p), p += up(npool * sizeof(int32_t));
+    h->gn.amin = reinterpret_cast<int32_t *>(p), p += up(npool * sizeof(int32_t));
+    h->gn.part = reinterpret_cast<double *>(p);
+    h->gn.units = units, h->gn.Hp = Hp, h->gn.Wp = Wp;
+    h->gn_pool_k = pool_k, h->gn_groups = groups, h->gn_units = units;
+    return CONV_EPI_OK;
+}
+
+}  // namespace conv_epi
+
+extern "C" {
+
+CONV_EPI_API const char *conv_epi_status_string(conv_epi_status s) {
+    switch (s) {
+    case CONV_EPI_OK: return "ok";
+    case CONV_EPI_ERR_INVALID_ARG: return "invalid argument";
+    case CONV_EPI_ERR_UNSUPPORTED: return "unsupported shape, chain or device for this mode";
+    case CONV_EPI_ERR_ALIGNMENT: return "tensor not aligned to 16 bytes";
+    case CONV_EPI_ERR_CUDA: return "CUDA runtime error";
+    case CONV_EPI_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case CONV_EPI_ERR_NO_MEMORY: return "out of device memory";
+    case CONV_EPI_ERR_DEVICE: return "kernel raised an error flag";
+    }
+    return "unknown status";
+}
+
+CONV_EPI_API const char *conv_epi_last_cuda_error(void) { return g_cuda_err; }
+
+CONV_EPI_API int conv_epi_version(void) { return 10000; }
+
+CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc, const conv_epi_epilogue_desc *epi,
+                                                   int64_t shape[4]) {
+    if (!shape) return CONV_EPI_ERR_INVALID_ARG;
+    conv_epi_status st = check_desc(desc);
+    if (st) return st;
+    if ((st = check_epi(*desc, epi))) return st;
+    shape_of(*desc, *epi, shape);
+    return CONV_EPI_OK;
+}
+
+CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi_handle *out) {
+    if (!out) return CONV_EPI_ERR_INVALID_ARG;
+    *out = nullptr;
+    conv_epi_status st = check_desc(desc);
+    if (st) return st;
+    if ((st = check_mode_support(*desc, nullptr))) return st;
+    int dev = 0;
+    CE_CUDA(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    CE_CUDA(cudaGetDeviceProperties(&prop, dev));
+    // every kernel of this library is built for sm_103a only
+    if (!(prop.major == 10 && prop.minor == 3)) return CONV_EPI_ERR_UNSUPPORTED;
+    conv_epi_handle h = new (std::nothrow) conv_epi_handle_s();
+    if (!h) return CONV_EPI_ERR_NO_MEMORY;
+    h->d = *desc;
+    h->Ho = desc->H - 2, h->Wo = desc->W - 2;
+    h->device = dev;
+    h->sm_count = prop.multiProcessorCount;
+    h->cc_major = prop.major, h->cc_minor = prop.minor;
+    cudaError_t e = cudaMalloc(&h->dev_err, 256);
+    if (e == cudaSuccess) e = cudaMemset(h->dev_err, 0, 256);
+    if (e == cudaSuccess && desc->mode == CONV_EPI_MODE_TF32) {
+        h->wpack_bytes = conv_epi::tc_wpack_bytes(*desc);
+        e = cudaMalloc(&h->wpack, h->wpack_bytes);
+    }
+    if (e != cudaSuccess) {
+        st = conv_epi::cuda_fail(e, "conv_epi_create workspace");
+        cudaFree(h->dev_err);
+        cudaFree(h->wpack);
+        delete h;
+        return st;
+    }
+    *out = h;
+    return CONV_EPI_OK;
+}
+
+CONV_EPI_API conv_epi_status conv_epi_reserve(conv_epi_handle h, const conv_epi_epilogue_desc *epi) {
+    if (!h) return CONV_EPI_ERR_INVALID_ARG;
+    conv_epi_status st = check_epi(h->d, epi);
+    if (st) return st;
+    if ((st = check_mode_support(h->d, epi))) return st;
+    if (epi->kind != CONV_EPI_GN_SCALE_POOL_CLAMP) return CONV_EPI_OK;
+    const int units = h->d.mode == CONV_EPI_MODE_FP32 ? conv_epi::simt_gn_units(h->d, h->Ho, epi->pool_k)
+                                                      : conv_epi::tc_gn_units(h->d, h->Ho, epi->pool_k);
+    CE_CUDA(cudaSetDevice(h->device));
+    return conv_epi::ensure_gn_workspace(h, epi->pool_k, epi->groups, units);
+}
+
+CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
+                                              const conv_epi_epilogue_desc *epi, float *out, void *stream) {
+    conv_epi_status st = forward_checks(h, x, w, b, epi, out);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->last_launches = 0;
+    if (epi->kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
+        if ((st = conv_epi_reserve(h, epi))) return st;
+    }
+    if (h->d.mode == CONV_EPI_MODE_FP32) return conv_epi::simt_forward(h, x, w, b, *epi, out, s);
+    return conv_epi::tc_forward(h, x, w, b, *epi, out, s);
+}
+
+CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const float *x, const float *w,
+                                                   const float *b, const conv_epi_epilogue_desc *epi, float *out,
+                                                   void *stream) {
+    if (!h || !x || !w || !b || !epi || !out) return CONV_EPI_ERR_INVALID_ARG;
+    conv_epi_status st = check_epi(h->d, epi);
+    if (st) return st;
+    const conv_epi_desc &d = h->d;
+    int64_t shp[4];
+    shape_of(d, *epi, shp);
+    const size_t nx = (size_t)d.N * d.Cin * d.H * d.W, nw = (size_t)d.Cout * d.Cin * 9, nc = (size_t)d.Cout;
+    const size_t no = (size_t)(shp[0] * shp[1] * shp[2] * shp[3]);
+    auto up = [](size_t v) { return (v + 63) & ~(size_t)63; };  // 256-byte steps of floats
+    const size_t need = sizeof(float) * (up(nx) + up(nw) + 4 * up(nc) + up(no)) + sizeof(int32_t) * up(no);
+    CE_CUDA(cudaSetDevice(h->device));
+    if (need > h->stage_bytes) {
+        if (h->stage) {
+            CE_CUDA(cudaDeviceSynchronize());
+            CE_CUDA(cudaFree(h->stage));
+            h->stage = nullptr, h->stage_bytes = 0;
+        }
+        CE_CUDA(cudaMalloc(&h->stage, need));
+        h->stage_bytes = need;
+    }
+    float *dx = static_cast<float *>(h->stage);
+    float *dw = dx + up(nx), *db = dw + up(nw), *dp0 = db + up(nc), *dp1 = dp0 + up(nc), *dp2 = dp1 + up(nc);
+    float *dout = dp2 + up(nc);
+    int32_t *didx = reinterpret_cast<int32_t *>(dout + up(no));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CE_CUDA(cudaMemcpyAsync(dx, x, nx * sizeof(float), cudaMemcpyHostToDevice, s));
+    CE_CUDA(cudaMemcpyAsync(dw, w, nw * sizeof(float), cudaMemcpyHostToDevice, s));
+    CE_CUDA(cudaMemcpyAsync(db, b, nc * sizeof(float), cudaMemcpyHostToDevice, s));
+    conv_epi_epilogue_desc de = *epi;
+    if (epi->chan_scale) {
+        CE_CUDA(cudaMemcpyAsync(dp0, epi->chan_scale, nc * sizeof(float), cudaMemcpyHostToDevice, s));
+        de.chan_scale = dp0;
+    }
+    if (epi->gamma) {
+        CE_CUDA(cudaMemcpyAsync(dp1, epi->gamma, nc * sizeof(float), cudaMemcpyHostToDevice, s));
+        de.gamma = dp1;
+    }
+    if (epi->beta) {
+        CE_CUDA(cudaMemcpyAsync(dp2, epi->beta, nc * sizeof(float), cudaMemcpyHostToDevice, s));
+        de.beta = dp2;
+    }
+    if (epi->index_out) de.index_out = didx;
+    st = conv_epi_forward(h, dx, dw, db, &de, dout, stream);
+    if (st) return st;
+    CE_CUDA(cudaMemcpyAsync(out, dout, no * sizeof(float), cudaMemcpyDeviceToHost, s));
+    if (epi->index_out)
+        CE_CUDA(cudaMemcpyAsync(epi->index_out, didx, no * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    return conv_epi_sync(h, stream);
+}
+
+CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream) {
+    if (!h) return CONV_EPI_ERR_INVALID_ARG;
+    CE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    unsigned word = 0;
+    CE_CUDA(cudaMemcpy(&word, h->dev_err, sizeof word, cudaMemcpyDeviceToHost));
+    if (word) {
+        CE_CUDA(cudaMemset(h->dev_err, 0, sizeof word));
+        return (word & conv_epi::ERRBIT_TIMEOUT) ? CONV_EPI_ERR_TIMEOUT : CONV_EPI_ERR_DEVICE;
+    }
+    return CONV_EPI_OK;
+}
+
+CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
+    if (!h) return CONV_EPI_ERR_INVALID_ARG;
+    cudaSetDevice(h->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaFree(h->dev_err);
+    cudaFree(h->wpack);
+    cudaFree(h->gn_mem);
+    cudaFree(h->stage);
+    delete h;
+    return e == cudaSuccess ? CONV_EPI_OK : conv_epi::cuda_fail(e, "conv_epi_destroy");
+}
+
+CONV_EPI_API size_t conv_epi_workspace_bytes(conv_epi_handle h) {
+    if (!h) return 0;
+    return 256 + h->wpack_bytes + h->gn_bytes + h->stage_bytes;
+}
+
+CONV_EPI_API int conv_epi_last_launch_count(conv_epi_handle h) { return h ? h->last_launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// internal.h -- declarations shared by the translation units of libconv_epi.
+// Nothing here is visible through the C ABI (include/conv_epi.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/conv_epi.h"
+
+namespace conv_epi {
+
+// Device error word bits (ORed by kernels into handle->dev_err[0]).
+enum : unsigned {
+    ERRBIT_TIMEOUT = 1u,  // a bounded barrier wait ran out
+    ERRBIT_BOUNDS = 2u,   // a kernel's own bounds check refused an access
+    ERRBIT_TMEM = 4u,     // tensor-memory allocation returned an unexpected address
+};
+
+// Where the bounded waits give up (nanoseconds of %globaltimer).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// GroupNorm-chain workspace, written by either conv path and read by the
+// finalize kernel.  For each (n, c, ph, pw) of the pooled output:
+//   pmax / pmin : max / min of y = conv + bias over the k x k window;
+//   amax / amin : window offset a*k+b of the first max / min (fp32 mode only);
+// and for each (n, unit, group) the partial sums of y and y^2 (double) over
+// the rows/cols the unit covered.
+struct GnWork {
+    float *pmax = nullptr, *pmin = nullptr;
+    int32_t *amax = nullptr, *amin = nullptr;
+    double *part = nullptr;  // [N][units][groups][2]
+    int units = 0;           // partial-sum slots per image
+    int Hp = 0, Wp = 0;
+};
+
+}  // namespace conv_epi
+
+struct conv_epi_handle_s {
+    conv_epi_desc d{};
+    int Ho = 0, Wo = 0;
+    int device = 0;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    unsigned *dev_err = nullptr;  // device error word
+
+    // packed tf32 weights for the tensor-core path
+    float *wpack = nullptr;
+    size_t wpack_bytes = 0;
+
+    // GroupNorm workspace (allocated on demand / by conv_epi_reserve)
+    void *gn_mem = nullptr;
+    size_t gn_bytes = 0;
+    int gn_pool_k = 0, gn_groups = 0, gn_units = 0;
+    conv_epi::GnWork gn;
+
+    // device staging for conv_epi_forward_host
+    void *stage = nullptr;
+    size_t stage_bytes = 0;
+
+    int last_launches = 0;
+};
+
+namespace conv_epi {
+
+// records a failing CUDA call for conv_epi_last_cuda_error()
+conv_epi_status cuda_fail(cudaError_t e, const char *what);
+#define CE_CUDA(call)                                             \
+    do {                                                          \
+        cudaError_t e_ = (call);                                  \
+        if (e_ != cudaSuccess) return conv_epi::cuda_fail(e_, #call); \
+    } while (0)
+
+// GN workspace sizing shared by the two conv paths (units = partial-sum slots
+// per image, a function of the path's tiling).
+conv_epi_status ensure_gn_workspace(conv_epi_handle h, int pool_k, int groups, int units);
+
+// fp32 CUDA-core path (simt.cu)
+conv_epi_status simt_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc &e);
+int simt_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
+conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
+                             const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
+
+// tcgen05 tf32 path (tc.cu)
+conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e);
+size_t tc_wpack_bytes(const conv_epi_desc &d);
+int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
+conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
+                           const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
+
+// GroupNorm finalize (gn.cu): pooled max/min + statistics -> output
+conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, float *out,
+                            cudaStream_t s);
+
+}  // namespace conv_epi

@@ -1,0 +1,387 @@
+// simt.cu -- fp32 CUDA-core path (CONV_EPI_MODE_FP32, the strict-tolerance
+// mode): a direct 3x3 convolution with the post-conv chain fused into the
+// same kernel, so the full conv output is written only by the per-channel
+// chain (MUL_LRELU_GELU), whose output is the full tensor anyway.
+//
+// Prior art: the p54 page (POPCORNBENCH Kimi-K2.6, level-2 problem 54), in
+// its fused direct-conv design, stages a haloed input tile and a few output
+// channels' filters in shared memory and has each thread accumulate outputs
+// over (c_in, kh, kw).  Here a CTA owns one output row (or one pooling band
+// of rows) of one image and every output channel, so the channel reductions
+// of the min chains and the pooling of the GroupNorm chain finish on chip.
+//
+// Work decomposition (one CTA):
+//   threads  = PG pixel groups x CS channel slots (<= 256)
+//   a thread = 4 consecutive output pixels x 16 output channels per pass
+//   a pass   = CS*16 channels; passes loop until Cout is covered
+//   staging  = 16 input channels x 3 input rows x (PG*4 + 4) columns of x,
+//              and the matching 16 x 9 x (CS*16) filter taps, in shared memory
+#include <float.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace conv_epi {
+namespace {
+
+constexpr int kCI = 16;  // input channels staged per step
+constexpr int kCO = 16;  // output channels per thread per pass
+constexpr int kPX = 4;   // consecutive output pixels per thread
+
+struct SimtArgs {
+    const float *x, *w, *b;
+    int N, Cin, H, W, Cout, Ho, Wo;
+    int PG, CS;          // thread layout
+    int units;           // CTAs per image
+    int ntiles;          // pixel tiles of PG*4 columns along a row
+    float scalar;        // MIN kinds
+    const float *chan_scale;
+    float slope;
+    int groups, Hp, Wp;  // GN
+    float *out;
+    int32_t *idx;
+    GnWork gn;
+};
+
+__device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erff(t * 0.70710678118654752f)); }
+
+// KIND: conv_epi_kind; PK: pool kernel (GN only; 1, 2 or 4, dividing kPX)
+template <int KIND, int PK>
+__global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
+    extern __shared__ float4 smem_f4[];
+    float *sm = reinterpret_cast<float *>(smem_f4);
+    const int tid = threadIdx.x;
+    const int PG = a.PG, CS = a.CS;
+    const int tx = tid % PG, ty = tid / PG;
+    const int TW = PG * kPX, XW = TW + 4, COP = CS * kCO;
+    float *xs = sm;                  // [kCI][3][XW]
+    float *ws = sm + kCI * 3 * XW;   // [kCI][9][COP]
+    const int n = blockIdx.x / a.units;
+    const int u = blockIdx.x % a.units;
+    constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
+    constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
+    const int r0 = kGN ? u * PK : u;
+    const int r1 = kGN ? min(r0 + PK, a.Ho) : u + 1;
+    // min kinds: +1 tracks the minimum of y (scalar > 0), -1 the maximum (scalar < 0)
+    const int sgn = a.scalar > 0.0f ? 1 : (a.scalar < 0.0f ? -1 : 0);
+
+    // GroupNorm per-CTA group partial sums, in a fixed summation order
+    __shared__ double gpart[2 * 64];
+    if (kGN) {
+        for (int i = tid; i < 2 * 64; i += blockDim.x) gpart[i] = 0.0;
+    }
+
+    for (int t = 0; t < a.ntiles; ++t) {
+        const int wo0 = t * TW;
+        float best[kPX];
+        int bidx[kPX];
+#pragma unroll
+        for (int p = 0; p < kPX; ++p) best[p] = 0.0f, bidx[p] = -1;
+
+        for (int cobase = 0; cobase < a.Cout; cobase += COP) {
+            const int co0 = cobase + ty * kCO;
+            constexpr int WPT = kGN ? kPX / PK : 1;  // pooling windows per thread
+            float gs[kCO], gss[kCO];
+            float pmx[kCO][WPT], pmn[kCO][WPT];
+            int amx[kCO][WPT], amn[kCO][WPT];
+            if (kGN) {
+#pragma unroll
+                for (int c = 0; c < kCO; ++c) {
+                    gs[c] = 0.0f, gss[c] = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < WPT; ++j) pmx[c][j] = -FLT_MAX, pmn[c][j] = FLT_MAX, amx[c][j] = -1, amn[c][j] = -1;
+                }
+            }
+            for (int r = r0; r < r1; ++r) {
+                float acc[kCO][kPX];
+#pragma unroll
+                for (int c = 0; c < kCO; ++c) {
+                    const float bv = (co0 + c < a.Cout) ? __ldg(&a.b[co0 + c]) : 0.0f;
+#pragma unroll
+                    for (int p = 0; p < kPX; ++p) acc[c][p] = bv;
+                }
+                for (int ci0 = 0; ci0 < a.Cin; ci0 += kCI) {
+                    __syncthreads();
+                    for (int i = tid; i < kCI * 3 * XW; i += blockDim.x) {
+                        const int col = i % XW, rr = (i / XW) % 3, ci = i / (3 * XW);
+                        const int gci = ci0 + ci, gw = wo0 + col;
+                        float v = 0.0f;
+                        if (gci < a.Cin && gw < a.W)
+                            v = __ldg(&a.x[(((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw]);
+                        xs[i] = v;
+                    }
+                    for (int i = tid; i < kCI * 9 * COP; i += blockDim.x) {
+                        const int col = i % COP, tap = (i / COP) % 9, ci = i / (9 * COP);
+                        const int gci = ci0 + ci, gco = cobase + col;
+                        float v = 0.0f;
+                        if (gci < a.Cin && gco < a.Cout) v = __ldg(&a.w[((size_t)gco * a.Cin + gci) * 9 + tap]);
+                        ws[i] = v;
+                    }
+                    __syncthreads();
+                    const int nci = min(kCI, a.Cin - ci0);
+                    for (int ci = 0; ci < nci; ++ci) {
+#pragma unroll
+                        for (int kh = 0; kh < 3; ++kh) {
+                            const float *xr = xs + (ci * 3 + kh) * XW + tx * kPX;
+                            const float4 xa = *reinterpret_cast<const float4 *>(xr);
+                            const float2 xb = *reinterpret_cast<const float2 *>(xr + 4);
+                            const float xv[6] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y};
+#pragma unroll
+                            for (int kw = 0; kw < 3; ++kw) {
+                                const float4 *wr = reinterpret_cast<const float4 *>(ws + (ci * 9 + kh * 3 + kw) * COP + ty * kCO);
+                                float wv[kCO];
+#pragma unroll
+                                for (int q = 0; q < kCO / 4; ++q) {
+                                    const float4 f = wr[q];
+                                    wv[4 * q] = f.x, wv[4 * q + 1] = f.y, wv[4 * q + 2] = f.z, wv[4 * q + 3] = f.w;
+                                }
+#pragma unroll
+                                for (int c = 0; c < kCO; ++c)
+#pragma unroll
+                                    for (int p = 0; p < kPX; ++p) acc[c][p] = fmaf(wv[c], xv[p + kw], acc[c][p]);
+                            }
+                        }
+                    }
+                }
+
+                // ---- fold this row into the chain ----
+                const int wbase = wo0 + tx * kPX;
+                if (kMin) {
+#pragma unroll
+                    for (int c = 0; c < kCO; ++c) {
+                        if (co0 + c >= a.Cout) break;
+#pragma unroll
+                        for (int p = 0; p < kPX; ++p) {
+                            const float v = acc[c][p];
+                            const bool better = sgn >= 0 ? v < best[p] : v > best[p];
+                            if (bidx[p] < 0 || better) best[p] = v, bidx[p] = co0 + c;
+                        }
+                    }
+                } else if (KIND == CONV_EPI_MUL_LRELU_GELU) {
+                    if (wbase < a.Wo) {
+#pragma unroll
+                        for (int c = 0; c < kCO; ++c) {
+                            const int co = co0 + c;
+                            if (co >= a.Cout) break;
+                            const float m = __ldg(&a.chan_scale[co]);
+                            float o[kPX];
+#pragma unroll
+                            for (int p = 0; p < kPX; ++p) {
+                                float v = acc[c][p] * m;
+                                v = v > 0.0f ? v : a.slope * v;
+                                o[p] = gelu_erf(v);
+                            }
+                            float *dst = a.out + (((size_t)n * a.Cout + co) * a.Ho + r) * a.Wo + wbase;
+                            if (wbase + kPX <= a.Wo && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+                                reinterpret_cast<float2 *>(dst)[0] = make_float2(o[0], o[1]);
+                                reinterpret_cast<float2 *>(dst)[1] = make_float2(o[2], o[3]);
+                            } else {
+#pragma unroll
+                                for (int p = 0; p < kPX; ++p)
+                                    if (wbase + p < a.Wo) dst[p] = o[p];
+                            }
+                        }
+                    }
+                } else if (kGN) {
+                    const bool prow = r < a.Hp * PK;
+#pragma unroll
+                    for (int c = 0; c < kCO; ++c) {
+                        if (co0 + c >= a.Cout) break;
+#pragma unroll
+                        for (int p = 0; p < kPX; ++p) {
+                            const int wo = wbase + p;
+                            if (wo >= a.Wo) continue;
+                            const float v = acc[c][p];
+                            gs[c] += v;
+                            gss[c] = fmaf(v, v, gss[c]);
+                            if (prow && wo < a.Wp * PK) {
+                                const int j = p / PK;
+                                const int off = (r - r0) * PK + (p % PK);
+                                if (amx[c][j] < 0 || v > pmx[c][j]) pmx[c][j] = v, amx[c][j] = off;
+                                if (amn[c][j] < 0 || v < pmn[c][j]) pmn[c][j] = v, amn[c][j] = off;
+                            }
+                        }
+                    }
+                }
+            }  // rows
+
+            if (kGN) {
+                // pooled max/min of this band (a full band only: u < Hp)
+                if (u < a.Hp) {
+#pragma unroll
+                    for (int c = 0; c < kCO; ++c) {
+                        const int co = co0 + c;
+                        if (co >= a.Cout) break;
+#pragma unroll
+                        for (int j = 0; j < WPT; ++j) {
+                            const int pw = (wo0 + tx * kPX) / PK + j;
+                            if (pw >= a.Wp) continue;
+                            const size_t o = (((size_t)n * a.Cout + co) * a.Hp + u) * a.Wp + pw;
+                            a.gn.pmax[o] = pmx[c][j];
+                            a.gn.pmin[o] = pmn[c][j];
+                            a.gn.amax[o] = amx[c][j];
+                            a.gn.amin[o] = amn[c][j];
+                        }
+                    }
+                }
+                // statistics: per-thread channel sums -> shared memory -> fixed-order group sums
+                __syncthreads();
+                float *S = sm, *SS = sm + COP * PG;  // [COP][PG] each
+#pragma unroll
+                for (int c = 0; c < kCO; ++c) {
+                    S[(ty * kCO + c) * PG + tx] = gs[c];
+                    SS[(ty * kCO + c) * PG + tx] = gss[c];
+                }
+                __syncthreads();
+                const int cpg = a.Cout / a.groups;
+                for (int g = tid; g < a.groups; g += blockDim.x) {
+                    const int c_lo = max(cobase, g * cpg), c_hi = min(min(cobase + COP, a.Cout), (g + 1) * cpg);
+                    double s = 0.0, ss = 0.0;
+                    for (int co = c_lo; co < c_hi; ++co)
+                        for (int q = 0; q < PG; ++q) s += S[(co - cobase) * PG + q], ss += SS[(co - cobase) * PG + q];
+                    gpart[2 * g] += s;
+                    gpart[2 * g + 1] += ss;
+                }
+            }
+        }  // channel passes
+
+        if (kMin) {
+            // combine the CS channel slots: lowest value, then lowest channel
+            __syncthreads();
+            float *rv = sm;
+            int *ri = reinterpret_cast<int *>(sm + CS * TW);
+#pragma unroll
+            for (int p = 0; p < kPX; ++p) rv[ty * TW + tx * kPX + p] = best[p], ri[ty * TW + tx * kPX + p] = bidx[p];
+            __syncthreads();
+            for (int col = tid; col < TW; col += blockDim.x) {
+                const int wo = wo0 + col;
+                if (wo >= a.Wo) continue;
+                float bv = 0.0f;
+                int bi = -1;
+                for (int s = 0; s < CS; ++s) {
+                    const float v = rv[s * TW + col];
+                    const int i = ri[s * TW + col];
+                    if (i < 0) continue;
+                    const bool better = sgn >= 0 ? v < bv : v > bv;
+                    if (bi < 0 || better || (v == bv && i < bi)) bv = v, bi = i;
+                }
+                float o = sgn == 0 ? 0.0f * bv : a.scalar * bv;
+                if (KIND == CONV_EPI_MIN_TANH2) o = tanhf(tanhf(o));
+                const size_t oi = ((size_t)n * a.Ho + r0) * a.Wo + wo;
+                a.out[oi] = o;
+                if (a.idx) a.idx[oi] = sgn == 0 ? 0 : bi;
+            }
+        }
+    }  // pixel tiles
+
+    if (kGN) {
+        __syncthreads();
+        for (int g = tid; g < a.groups; g += blockDim.x) {
+            double *dst = a.gn.part + (((size_t)n * a.units + u) * a.groups + g) * 2;
+            dst[0] = gpart[2 * g];
+            dst[1] = gpart[2 * g + 1];
+        }
+    }
+}
+
+int pow2ceil(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+struct Layout {
+    int PG, CS, TW, XW, COP, ntiles;
+    size_t smem;
+};
+
+Layout layout_for(const conv_epi_desc &d, int Wo) {
+    Layout L;
+    L.PG = pow2ceil((Wo + kPX - 1) / kPX);
+    if (L.PG > 64) L.PG = 64;
+    const int cg = (d.Cout + kCO - 1) / kCO;
+    L.CS = 256 / L.PG;
+    if (L.CS > cg) L.CS = cg;
+    L.TW = L.PG * kPX, L.XW = L.TW + 4, L.COP = L.CS * kCO;
+    L.ntiles = (Wo + L.TW - 1) / L.TW;
+    const size_t stage = (size_t)(kCI * 3 * L.XW + kCI * 9 * L.COP) * sizeof(float);
+    const size_t red_min = (size_t)2 * L.CS * L.TW * sizeof(float);
+    const size_t red_gn = (size_t)2 * L.COP * L.PG * sizeof(float);
+    L.smem = stage;
+    if (red_min > L.smem) L.smem = red_min;
+    if (red_gn > L.smem) L.smem = red_gn;
+    return L;
+}
+
+template <int KIND, int PK>
+conv_epi_status launch(const SimtArgs &a, const Layout &L, int grid, cudaStream_t s) {
+    auto k = simt_conv_epi<KIND, PK>;
+    CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem));
+    k<<<grid, L.PG * L.CS, L.smem, s>>>(a);
+    CE_CUDA(cudaGetLastError());
+    return CONV_EPI_OK;
+}
+
+}  // namespace
+
+conv_epi_status simt_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
+    (void)d;
+    if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
+        if (!(e.pool_k == 1 || e.pool_k == 2 || e.pool_k == 4)) return CONV_EPI_ERR_UNSUPPORTED;
+        if (e.groups > 64) return CONV_EPI_ERR_UNSUPPORTED;
+    }
+    return CONV_EPI_OK;
+}
+
+int simt_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
+    (void)d;
+    return (Ho + pool_k - 1) / pool_k;
+}
+
+conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
+                             const conv_epi_epilogue_desc &e, float *out, cudaStream_t s) {
+    const conv_epi_desc &d = h->d;
+    const Layout L = layout_for(d, h->Wo);
+    SimtArgs a{};
+    a.x = x, a.w = w, a.b = b;
+    a.N = d.N, a.Cin = d.Cin, a.H = d.H, a.W = d.W, a.Cout = d.Cout, a.Ho = h->Ho, a.Wo = h->Wo;
+    a.PG = L.PG, a.CS = L.CS, a.ntiles = L.ntiles;
+    a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.slope = e.lrelu_slope;
+    a.groups = e.groups;
+    a.out = out, a.idx = e.index_out;
+    conv_epi_status st;
+    switch (e.kind) {
+    case CONV_EPI_MIN_TANH2:
+        a.units = h->Ho;
+        st = launch<CONV_EPI_MIN_TANH2, 1>(a, L, d.N * a.units, s);
+        break;
+    case CONV_EPI_SCALE_MIN:
+        a.units = h->Ho;
+        st = launch<CONV_EPI_SCALE_MIN, 1>(a, L, d.N * a.units, s);
+        break;
+    case CONV_EPI_MUL_LRELU_GELU:
+        a.units = h->Ho;
+        st = launch<CONV_EPI_MUL_LRELU_GELU, 1>(a, L, d.N * a.units, s);
+        break;
+    case CONV_EPI_GN_SCALE_POOL_CLAMP: {
+        a.units = simt_gn_units(d, h->Ho, e.pool_k);
+        a.gn = h->gn;
+        a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
+        if (h->gn.units != a.units) return CONV_EPI_ERR_INVALID_ARG;
+        if (e.pool_k == 4) st = launch<CONV_EPI_GN_SCALE_POOL_CLAMP, 4>(a, L, d.N * a.units, s);
+        else if (e.pool_k == 2) st = launch<CONV_EPI_GN_SCALE_POOL_CLAMP, 2>(a, L, d.N * a.units, s);
+        else st = launch<CONV_EPI_GN_SCALE_POOL_CLAMP, 1>(a, L, d.N * a.units, s);
+        if (st) return st;
+        h->last_launches = 1;
+        st = gn_finalize(h, e, out, s);
+        if (st == CONV_EPI_OK) h->last_launches = 2;
+        return st;
+    }
+    default:
+        return CONV_EPI_ERR_INVALID_ARG;
+    }
+    if (st == CONV_EPI_OK) h->last_launches = 1;
+    return st;
+}
+
+}  // namespace conv_epi
