@@ -225,11 +225,15 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=15.0, help="oracle sample length per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     wl = synth.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.with_batch(args.batch)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, wl, world, rank)
@@ -288,21 +292,23 @@ def main(argv=None):
     kern_ms = float(np.mean(per))
 
     # ---- end to end through the host-buffer entry point ----
-    pin = {k: (None if v is None else torch.from_numpy(v).pin_memory()) for k, v in host.items()}
-    chan_h = pin["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else pin["scale"]
-    epi_h = ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan_h, lrelu_slope=wl.lrelu_slope, groups=wl.groups,
-                        eps=wl.eps, gamma=pin["gamma"], beta=pin["beta"], pool_k=wl.pool_k, clamp_lo=wl.clamp_lo,
-                        clamp_hi=wl.clamp_hi)
-    out_h = torch.empty(shape, dtype=torch.float32).pin_memory()
-    ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)   # warm (allocates staging)
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = flops * args.e2e_steps * world / e2e_s / 1e12
-    h2d = sum(v.nbytes for v in host.values() if v is not None)
-    d2h = out_h.numel() * 4
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (None if v is None else torch.from_numpy(v).pin_memory()) for k, v in host.items()}
+        chan_h = pin["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else pin["scale"]
+        epi_h = ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan_h, lrelu_slope=wl.lrelu_slope,
+                            groups=wl.groups, eps=wl.eps, gamma=pin["gamma"], beta=pin["beta"], pool_k=wl.pool_k,
+                            clamp_lo=wl.clamp_lo, clamp_hi=wl.clamp_hi)
+        out_h = torch.empty(shape, dtype=torch.float32).pin_memory()
+        ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)   # warm (allocates staging)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+        h2d = sum(v.nbytes for v in host.values() if v is not None)
+        e2e = {"value": flops * args.e2e_steps * world / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * 4}
 
     ce.conv_epi_destroy(h)
 
@@ -331,7 +337,7 @@ def main(argv=None):
                      "hbm_gbs": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm,
                      "hbm_frac": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9 / hbm},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "kernel_ms": {"mean": kern_ms, "min": float(np.min(per)), "max": float(np.max(per))},
