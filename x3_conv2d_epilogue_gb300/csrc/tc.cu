@@ -54,7 +54,7 @@ constexpr int kConvWarp0 = 2, kConvWarps = 6, kConvThreads = kConvWarps * 32;
 constexpr int kEpiWarp0 = 8, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;     // columns per accumulator buffer
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kStgPitch = 17;       // epilogue transpose staging pitch (floats)
 
@@ -68,6 +68,9 @@ struct TcArgs {
     uint32_t p_magic;  // ceil(2^32 / P), exact division for q < 2^16
     int chunks, units_per_img, total_units, stages;
     uint32_t a_bytes, b_bytes, stage_bytes, scratch_off;
+    int resident;          // 1: every filter chunk stays in shared memory for the whole kernel
+    uint32_t stage0_off;   // byte offset of stage 0 (after the resident filter, if any)
+    uint32_t b_off;        // byte offset of B inside a stage (0 when the filter is resident)
     uint32_t a_kw_stride, a_lbo, a_plane_bytes;
     uint32_t idesc;
     float scalar;
@@ -111,6 +114,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
+}
+// 4-byte asynchronous global->shared copy; src_bytes = 0 writes zero
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ uint32_t f32_to_tf32(float f) {
@@ -222,12 +234,14 @@ struct Bars {
     __device__ uint32_t acc_full(int ab) const { return base + 8u * (3 * stages + ab); }
     __device__ uint32_t acc_empty(int ab) const { return base + 8u * (3 * stages + 2 + ab); }
     __device__ uint32_t final_bar() const { return base + 8u * (3 * stages + 4); }
-    static constexpr int count(int stages) { return 3 * stages + 5; }
+    __device__ uint32_t wres() const { return base + 8u * (3 * stages + 5); }
+    static constexpr int count(int stages) { return 3 * stages + 6; }
 };
 
 __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint32_t tmem, volatile int *abort_flag) {
     int it = 0, j = 0;
     bool ok = true;
+    if (a.resident) ok = wait_bar(bars.wres(), 0, abort_flag, a.err);
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x, ++j) {
         const int ab = j & 1;
         if (!wait_bar(bars.acc_empty(ab), ((j >> 1) & 1) ^ 1, abort_flag, a.err)) {
@@ -239,12 +253,15 @@ __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint
         for (int c = 0; c < a.chunks; ++c, ++it) {
             const int s = it % a.stages;
             const uint32_t ph = (it / a.stages) & 1;
-            if (!wait_bar(bars.full_w(s), ph, abort_flag, a.err) || !wait_bar(bars.full_x(s), ph, abort_flag, a.err)) {
+            if ((!a.resident && !wait_bar(bars.full_w(s), ph, abort_flag, a.err)) ||
+                !wait_bar(bars.full_x(s), ph, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t A0 = sbase + s * a.stage_bytes, B0 = A0 + a.a_bytes;
+            const uint32_t S0 = sbase + a.stage0_off + s * a.stage_bytes;
+            const uint32_t A0 = a.resident ? sbase + c * a.a_bytes : S0;
+            const uint32_t B0 = S0 + a.b_off;
             for (int u = 0; u < a.U; ++u) {
                 for (int sk = 0; sk <= a.S + 1; ++sk) {
 #pragma unroll
@@ -267,6 +284,16 @@ __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint
 }
 
 __device__ void weight_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
+    const char *wsrc = reinterpret_cast<const char *>(a.wpack);
+    if (a.resident) {
+        // the whole packed filter, once
+        const uint32_t total = a.chunks * a.a_bytes;
+        mbar_arrive_expect_tx(bars.wres(), total);
+        for (uint32_t off = 0; off < total; off += 16384u)
+            bulk_g2s(sbase + off, wsrc + off, min(16384u, total - off), bars.wres());
+        wait_bar(bars.wres(), 0, abort_flag, a.err, false);
+        return;
+    }
     int it = 0;
     int last_par[kMaxStages];
     bool issued[kMaxStages];
@@ -280,8 +307,8 @@ __device__ void weight_role(const TcArgs &a, uint32_t sbase, const Bars &bars, v
                 ok = false;
                 break;
             }
-            const uint32_t dst = sbase + s * a.stage_bytes;
-            const char *src = reinterpret_cast<const char *>(a.wpack) + (size_t)c * a.a_bytes;
+            const uint32_t dst = sbase + a.stage0_off + s * a.stage_bytes;
+            const char *src = wsrc + (size_t)c * a.a_bytes;
             mbar_arrive_expect_tx(bars.full_w(s), a.a_bytes);
             for (uint32_t off = 0; off < a.a_bytes; off += 16384u) {
                 const uint32_t n = min(16384u, a.a_bytes - off);
@@ -295,11 +322,19 @@ __device__ void weight_role(const TcArgs &a, uint32_t sbase, const Bars &bars, v
         if (issued[s]) wait_bar(bars.full_w(s), last_par[s], abort_flag, a.err, false);
 }
 
-__device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
+// Converter warps: x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] -> B plane
+// [ci4][q][4] of stage s, with 4-byte asynchronous copies (element f of the
+// plane, f = (jg*PL + q)*4 + e, comes from channel 8c+4jg+e at position q;
+// consecutive lanes write consecutive 4-byte words, so the shared-memory side
+// is conflict-free and the global side reads 32-byte runs of 4 channels).
+// Positions outside the image (rows >= H, columns >= W, the tail) are zero.
+// Two chunks are kept in flight per thread: the copies of chunk `it` are
+// issued before the thread waits for those of chunk `it-1` and signals them.
+__device__ void converter_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
     const int t = threadIdx.x - kConvWarp0 * 32;
     const size_t HW = (size_t)a.H * a.W;
-    const int items = 2 * a.PL;  // (ci4 group, position)
-    int it = 0;
+    const int words = 8 * a.PL;
+    int it = 0, pending = -1;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
         const int n = unit / a.units_per_img;
@@ -311,44 +346,33 @@ __device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars,
                 ok = false;
                 break;
             }
-            float4 *Bp = reinterpret_cast<float4 *>(smem + s * a.stage_bytes + a.a_bytes);
+            const uint32_t B0 = sbase + a.stage0_off + s * a.stage_bytes + a.b_off;
             const float *xc = a.x + ((size_t)n * a.Cin + 8 * c) * HW;
-            constexpr int UNR = 4;
-            for (int i0 = t; i0 < items; i0 += kConvThreads * UNR) {
-                float v[UNR][4];
-                int dst[UNR];
-#pragma unroll
-                for (int k = 0; k < UNR; ++k) {
-                    const int i = i0 + k * kConvThreads;
-                    dst[k] = -1;
-                    v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.0f;
-                    if (i < items) {
-                        const int jg = i >= a.PL ? 1 : 0;
-                        const int q = i - jg * a.PL;
-                        const int rr = __umulhi((uint32_t)q, a.p_magic);
-                        const int w = q - rr * a.P;
-                        const int h = r0 + rr;
-                        dst[k] = jg * a.PL + q;
-                        if (h < a.H && w < a.W) {
-                            const float *src = xc + (size_t)(4 * jg) * HW + (size_t)h * a.W + w;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) v[k][e] = __ldg(src + e * HW);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < UNR; ++k) {
-                    if (dst[k] >= 0) {
-                        uint4 o;
-                        o.x = f32_to_tf32(v[k][0]), o.y = f32_to_tf32(v[k][1]);
-                        o.z = f32_to_tf32(v[k][2]), o.w = f32_to_tf32(v[k][3]);
-                        reinterpret_cast<uint4 *>(Bp)[dst[k]] = o;
-                    }
-                }
+            for (int f = t; f < words; f += kConvThreads) {
+                const int e = f & 3;
+                const int i = f >> 2;
+                const int jg = i >= a.PL ? 1 : 0;
+                const int q = i - jg * a.PL;
+                const int rr = __umulhi((uint32_t)q, a.p_magic);
+                const int w = q - rr * a.P;
+                const int h = r0 + rr;
+                const bool valid = h < a.H && w < a.W;
+                const float *src = valid ? xc + (size_t)(4 * jg + e) * HW + (size_t)h * a.W + w : a.x;
+                cp_async4(B0 + 4u * f, src, valid ? 4u : 0u);
             }
-            fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
-            mbar_arrive(bars.full_x(s));
+            cp_async_commit();
+            if (pending >= 0) {
+                cp_async_wait<1>();       // the previous chunk's copies have landed
+                fence_proxy_async_smem();  // ... and are visible to the tensor core
+                mbar_arrive(bars.full_x(pending));
+            }
+            pending = s;
         }
+    }
+    if (pending >= 0) {
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        if (ok) mbar_arrive(bars.full_x(pending));
     }
 }
 
@@ -409,8 +433,9 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
         if (epi_bar_any(!ok)) break;  // all epilogue warps leave together
         tc_fence_after();
 
-        // GN per-thread state (registers): pooled max/min per window, sums
-        constexpr int kMaxWin = 16;  // windows per thread: chunks/2 * (16 / pool_k) <= 16 (checked on host)
+        // GN per-thread state (registers): pooled max/min of this thread's
+        // 4-column windows (4 per 16-column chunk, at most 4 chunks: P <= 128)
+        constexpr int kMaxWin = 16;
         float pmx[kMaxWin], pmn[kMaxWin];
         float ls = 0.0f, lss = 0.0f;
         if (kGN) {
@@ -419,7 +444,34 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
         }
 
         for (int u = 0; u < a.U; ++u) {
-            const int row = r0 + u * a.S + slot;
+            const int row = r0 + u * a.S + slot;  // the same for the whole warp
+            if constexpr (kGN) {
+#pragma unroll
+                for (int kc = 0; kc < kMaxWin / 4; ++kc) {
+                    const int cc = hc + 2 * kc;
+                    if (cc >= nchunks) break;
+                    const int col0 = cc * 16;
+                    float v[16];
+                    tmem_ld16(tmem + lane_off + ab * kAccStride + u * a.ucol + col0, v);
+                    if (row < a.Ho) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            v[i] += bias;
+                            if (col0 + i < a.Wo) {
+                                ls += v[i];
+                                lss = fmaf(v[i], v[i], lss);
+                            }
+                        }
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            const float mx = fmaxf(fmaxf(v[4 * wi], v[4 * wi + 1]), fmaxf(v[4 * wi + 2], v[4 * wi + 3]));
+                            const float mn = fminf(fminf(v[4 * wi], v[4 * wi + 1]), fminf(v[4 * wi + 2], v[4 * wi + 3]));
+                            pmx[4 * kc + wi] = fmaxf(pmx[4 * kc + wi], mx);
+                            pmn[4 * kc + wi] = fminf(pmn[4 * kc + wi], mn);
+                        }
+                    }
+                }
+            } else {
             for (int cc = hc; cc < nchunks; cc += 2) {
                 const int col0 = cc * 16;
                 float v[16];
@@ -448,28 +500,8 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
                         }
                     }
                     __syncwarp();
-                } else if (kGN) {
-                    if (row < a.Ho) {
-                        const int wk = (cc >> 1) * (16 / a.pool_k);  // this thread's window slot base
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (col0 + i < a.Wo) {
-                                ls += v[i];
-                                lss = fmaf(v[i], v[i], lss);
-                            }
-                        }
-                        for (int wi = 0; wi < 16 / a.pool_k; ++wi) {
-                            float mx = -INFINITY, mn = INFINITY;
-                            for (int i = 0; i < a.pool_k; ++i) {
-                                mx = fmaxf(mx, v[wi * a.pool_k + i]);
-                                mn = fminf(mn, v[wi * a.pool_k + i]);
-                            }
-#pragma unroll
-                            for (int k = 0; k < kMaxWin; ++k)
-                                if (k == wk + wi) pmx[k] = fmaxf(pmx[k], mx), pmn[k] = fminf(pmn[k], mn);
-                        }
-                    }
                 }
+            }
             }
         }
         // tensor memory of this unit is no longer needed
@@ -494,7 +526,6 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
             epi_bar();
         } else if (kGN) {
             // pool: combine the two row slots (S == 2) through shared memory
-            const int wpt = (nchunks / 2 + (hc < (nchunks & 1) ? 1 : 0)) * (16 / a.pool_k);
             float *xg = scratch;                                  // [8 warps][32 lanes][kMaxWin][2]
             float *st = scratch + kEpiWarps * 32 * kMaxWin * 2;   // [8 warps][32 lanes][2]
             st[(ew * 32 + lane) * 2] = ls;
@@ -506,23 +537,20 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
             }
             epi_bar();
             if (slot == 0 && ru < a.Hp) {
-                // lanes of slot 0 combine with the matching lane of slot 1 (quadrant + 4/S... )
+                const int ew1 = hc * 4 + qd + 2;  // warp holding the same channel in row slot 1
 #pragma unroll
                 for (int k = 0; k < kMaxWin; ++k) {
-                    if (k >= wpt) break;
+                    const int cc = hc + 2 * (k / 4);
+                    const int pw = cc * 4 + (k % 4);
+                    if (cc >= nchunks || pw >= a.Wp) continue;
                     float mx = pmx[k], mn = pmn[k];
                     if (a.S == 2) {
-                        const int ew1 = hc * 4 + qd + 2;  // same channel, row slot 1
                         mx = fmaxf(mx, xg[((ew1 * 32 + lane) * kMaxWin + k) * 2]);
                         mn = fminf(mn, xg[((ew1 * 32 + lane) * kMaxWin + k) * 2 + 1]);
                     }
-                    const int cc = hc + 2 * (k / (16 / a.pool_k));
-                    const int pw = cc * (16 / a.pool_k) + k % (16 / a.pool_k);
-                    if (pw < a.Wp) {
-                        const size_t o = (((size_t)n * a.Cout + co) * a.Hp + ru) * a.Wp + pw;
-                        a.gn.pmax[o] = mx;
-                        a.gn.pmin[o] = mn;
-                    }
+                    const size_t o = (((size_t)n * a.Cout + co) * a.Hp + ru) * a.Wp + pw;
+                    a.gn.pmax[o] = mx;
+                    a.gn.pmin[o] = mn;
                 }
             }
             // statistics: fixed-order sum per group
@@ -552,9 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const TcArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
     Bars bars;
-    bars.base = sbase + a.stages * a.stage_bytes;
+    bars.base = sbase + a.stage0_off + a.stages * a.stage_bytes;
     bars.stages = a.stages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + a.stages * a.stage_bytes + 8 * Bars::count(a.stages));
+    uint32_t *tmem_slot =
+        reinterpret_cast<uint32_t *>(smem + a.stage0_off + a.stages * a.stage_bytes + 8 * Bars::count(a.stages));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *scratch = reinterpret_cast<float *>(smem + a.scratch_off);
 
@@ -569,6 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const TcArgs a) {
             mbar_init(bars.acc_empty(ab), kEpiWarps);
         }
         mbar_init(bars.final_bar(), 1);
+        mbar_init(bars.wres(), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -589,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const TcArgs a) {
         if (lane == 0) weight_role(a, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
-        converter_role(a, smem, bars, abort_flag);
+        converter_role(a, sbase, bars, abort_flag);
     } else {
         epilogue_role<KIND>(a, scratch, bars, tmem, abort_flag);
     }
@@ -631,8 +661,8 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
 // ----------------------------------------------------------- planning ----
 struct Plan {
     int S, P, U, RU, Rin, PL, chunks, ucol;
-    uint32_t a_bytes, b_bytes, stage_bytes, scratch_bytes, scratch_off;
-    int stages;
+    uint32_t a_bytes, b_bytes, stage_bytes, scratch_bytes, scratch_off, stage0_off, b_off;
+    int stages, resident;
     size_t smem;
 };
 
@@ -649,6 +679,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     return 0;
 }
 
+// Shared memory: [resident filter][stages x (A? + B)][mbarriers][tmem slot, abort][scratch]
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (!(d.Cout == 64 || d.Cout == 128)) return false;
     if (d.Cin % 8 != 0 || d.W % 4 != 0 || d.W > 256 || d.H < 3) return false;
@@ -663,14 +694,30 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (pl.PL >= (1 << 16)) return false;
     pl.a_bytes = 3u * 2u * (2 * pl.S + 1) * d.Cout * 16u;
     pl.b_bytes = 2u * pl.PL * 16u;
-    pl.stage_bytes = (pl.a_bytes + pl.b_bytes + 1023u) & ~1023u;
     pl.scratch_bytes = scratch_bytes_for(kind, pl.U, pl.P);
-    const uint32_t fixed = 8u * Bars::count(kMaxStages) + 16u;
+    auto fits = [&](int st, uint32_t stage, uint32_t res) {
+        const size_t bars_end = (size_t)res + (size_t)st * stage + 8u * Bars::count(st) + 8u;
+        return ((bars_end + 15) & ~(size_t)15) + pl.scratch_bytes <= (size_t)kSmemLimit;
+    };
+    // keep the whole filter resident when it leaves room for at least 3 stages of B
+    const uint32_t res_bytes = (pl.chunks * pl.a_bytes + 1023u) & ~1023u;
+    const uint32_t b_stage = (pl.b_bytes + 1023u) & ~1023u;
+    if (fits(3, b_stage, res_bytes)) {
+        pl.resident = 1;
+        pl.stage_bytes = b_stage;
+        pl.stage0_off = res_bytes;
+        pl.b_off = 0;
+    } else {
+        pl.resident = 0;
+        pl.stage_bytes = (pl.a_bytes + pl.b_bytes + 1023u) & ~1023u;
+        pl.stage0_off = 0;
+        pl.b_off = pl.a_bytes;
+    }
     int st = kMaxStages;
-    while (st >= 2 && (size_t)st * pl.stage_bytes + fixed + pl.scratch_bytes + 1024 > (size_t)kSmemLimit) --st;
+    while (st >= 2 && !fits(st, pl.stage_bytes, pl.stage0_off)) --st;
     if (st < 2) return false;
     pl.stages = st;
-    pl.scratch_off = ((uint32_t)st * pl.stage_bytes + 8u * Bars::count(st) + 8u + 15u) & ~15u;
+    pl.scratch_off = (pl.stage0_off + (uint32_t)st * pl.stage_bytes + 8u * Bars::count(st) + 8u + 15u) & ~15u;
     pl.smem = pl.scratch_off + pl.scratch_bytes;
     return true;
 }
@@ -698,10 +745,9 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
     const int kind = e ? e->kind : CONV_EPI_MIN_TANH2;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     if (e && e->kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
-        // one pooling band per unit; windows must not straddle 16-column chunks
-        if (pl.RU != e->pool_k || 16 % e->pool_k != 0) return CONV_EPI_ERR_UNSUPPORTED;
-        const int nchunks = pl.P / 16;
-        if ((nchunks + 1) / 2 * (16 / e->pool_k) > 16) return CONV_EPI_ERR_UNSUPPORTED;
+        // the epilogue pools 4x4 windows over one band of 4 rows per unit,
+        // with at most 4 sixteen-column chunks per epilogue warp
+        if (e->pool_k != 4 || pl.RU != 4 || pl.P > 128 || pl.S != 2) return CONV_EPI_ERR_UNSUPPORTED;
     }
     return CONV_EPI_OK;
 }
@@ -740,6 +786,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.total_units = d.N * a.units_per_img;
     a.stages = pl.stages;
     a.a_bytes = pl.a_bytes, a.b_bytes = pl.b_bytes, a.stage_bytes = pl.stage_bytes, a.scratch_off = pl.scratch_off;
+    a.resident = pl.resident, a.stage0_off = pl.stage0_off, a.b_off = pl.b_off;
     a.a_plane_bytes = (uint32_t)d.Cout * 16u;
     a.a_lbo = (uint32_t)(2 * pl.S + 1) * a.a_plane_bytes;
     a.a_kw_stride = 2u * a.a_lbo;
