@@ -50,8 +50,20 @@ namespace conv_epi {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 2, kConvWarps = 6, kConvThreads = kConvWarps * 32;
-constexpr int kEpiWarp0 = 8, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
+// Warp roles per chain: the min chains need 4 epilogue warps, the per-channel
+// and GroupNorm chains 8; the converters take the warps in between.
+template <int KIND>
+struct Roles {
+    static constexpr bool kMinKind = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
+    static constexpr int kEpiWarps = kMinKind ? 4 : 8;
+    static constexpr int kEpiWarp0 = 16 - kEpiWarps;  // a multiple of 4 (tensor-memory quadrants)
+    static constexpr int kConvWarp0 = 2;
+    static constexpr int kConvWarps = kEpiWarp0 - kConvWarp0;
+    static constexpr int kConvThreads = kConvWarps * 32;
+    static constexpr int kEpiThreads = kEpiWarps * 32;
+    static constexpr int kColGroups = kEpiWarps / 4;  // epilogue warps per quadrant
+    static constexpr int kNBMax = kMinKind ? 2 : 3;   // 4x4 blocks per converter thread per chunk
+};
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;     // columns per accumulator buffer
 constexpr int kMaxStages = 6;
@@ -115,24 +127,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
-// 4-byte asynchronous global->shared copy; src_bytes = 0 writes zero
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ uint32_t f32_to_tf32(float f) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
     return r;
 }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
+template <int NT>
+__device__ __forceinline__ void epi_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
 // barrier over the epilogue warps that also ORs a flag across them, so they
 // all take the same branch after it
+template <int NT>
 __device__ __forceinline__ bool epi_bar_any(bool v) {
     uint32_t r;
     asm volatile(
@@ -141,7 +148,7 @@ __device__ __forceinline__ bool epi_bar_any(bool v) {
         "bar.red.or.pred p, 1, %2, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v), "n"(kEpiThreads)
+        : "r"((uint32_t)v), "n"(NT)
         : "memory");
     return r != 0;
 }
@@ -323,56 +330,95 @@ __device__ void weight_role(const TcArgs &a, uint32_t sbase, const Bars &bars, v
 }
 
 // Converter warps: x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] -> B plane
-// [ci4][q][4] of stage s, with 4-byte asynchronous copies (element f of the
-// plane, f = (jg*PL + q)*4 + e, comes from channel 8c+4jg+e at position q;
-// consecutive lanes write consecutive 4-byte words, so the shared-memory side
-// is conflict-free and the global side reads 32-byte runs of 4 channels).
-// Positions outside the image (rows >= H, columns >= W, the tail) are zero.
-// Two chunks are kept in flight per thread: the copies of chunk `it` are
-// issued before the thread waits for those of chunk `it-1` and signals them.
-__device__ void converter_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
-    const int t = threadIdx.x - kConvWarp0 * 32;
+// [ci4][q][4] of a stage.  Work item = one 4x4 block: 4 consecutive positions
+// (one 16-byte global load per channel) x 4 channels; a register transpose
+// turns it into 4 position rows of 16 bytes, rounded to tf32.  The rows are
+// stored in a per-thread rotated order so that the 8 threads of a store phase
+// hit 8 different bank groups.  Positions outside the image are zero.
+// Registers hold two chunks: the loads of chunk it+1 are in flight while the
+// thread waits for its stage and stores chunk it.
+template <int NB>
+struct ConvRegs {
+    float4 v[NB][4];
+    int row[NB];  // first B-plane row of the block (jg*PL + q), -1 when absent
+};
+
+__device__ __forceinline__ float pick(const float4 &v, int p) {
+    return p == 0 ? v.x : (p == 1 ? v.y : (p == 2 ? v.z : v.w));
+}
+
+template <int NT, int NB>
+__device__ __forceinline__ void conv_issue(const TcArgs &a, ConvRegs<NB> &r, int t, int flat) {
+    const int unit = blockIdx.x + (flat / a.chunks) * gridDim.x;
+    const int c = flat % a.chunks;
+    const int n = unit / a.units_per_img;
+    const int r0 = (unit % a.units_per_img) * a.RU;
     const size_t HW = (size_t)a.H * a.W;
-    const int words = 8 * a.PL;
-    int it = 0, pending = -1;
-    bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
-        const int n = unit / a.units_per_img;
-        const int r0 = (unit % a.units_per_img) * a.RU;
-        for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int s = it % a.stages;
-            const uint32_t ph = (it / a.stages) & 1;
-            if (!wait_bar(bars.empty(s), ph ^ 1, abort_flag, a.err)) {
-                ok = false;
-                break;
+    const int qpp = a.PL >> 2;  // 4-position groups per ci4 plane
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+        const int b = t + k * NT;
+        r.row[k] = -1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r.v[k][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (b < 2 * qpp) {
+            const int jg = b >= qpp ? 1 : 0;
+            const int q = 4 * (b - jg * qpp);
+            const int rr = __umulhi((uint32_t)q, a.p_magic);
+            const int w = q - rr * a.P;
+            const int h = r0 + rr;
+            r.row[k] = jg * a.PL + q;
+            if (h < a.H && w < a.W) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    a.x + (((size_t)n * a.Cin + 8 * c + 4 * jg) * HW + (size_t)h * a.W + w));
+#pragma unroll
+                for (int e = 0; e < 4; ++e) r.v[k][e] = __ldg(src + e * (HW >> 2));
             }
-            const uint32_t B0 = sbase + a.stage0_off + s * a.stage_bytes + a.b_off;
-            const float *xc = a.x + ((size_t)n * a.Cin + 8 * c) * HW;
-            for (int f = t; f < words; f += kConvThreads) {
-                const int e = f & 3;
-                const int i = f >> 2;
-                const int jg = i >= a.PL ? 1 : 0;
-                const int q = i - jg * a.PL;
-                const int rr = __umulhi((uint32_t)q, a.p_magic);
-                const int w = q - rr * a.P;
-                const int h = r0 + rr;
-                const bool valid = h < a.H && w < a.W;
-                const float *src = valid ? xc + (size_t)(4 * jg + e) * HW + (size_t)h * a.W + w : a.x;
-                cp_async4(B0 + 4u * f, src, valid ? 4u : 0u);
-            }
-            cp_async_commit();
-            if (pending >= 0) {
-                cp_async_wait<1>();       // the previous chunk's copies have landed
-                fence_proxy_async_smem();  // ... and are visible to the tensor core
-                mbar_arrive(bars.full_x(pending));
-            }
-            pending = s;
         }
     }
-    if (pending >= 0) {
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        if (ok) mbar_arrive(bars.full_x(pending));
+}
+
+template <int NB>
+__device__ __forceinline__ void conv_store(const TcArgs &a, const ConvRegs<NB> &r, uint8_t *plane) {
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+        if (r.row[k] < 0) continue;
+        const int rot = (r.row[k] >> 3) & 3;  // (position group / 2) mod 4
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int p = (i + rot) & 3;
+            uint4 o;
+            o.x = f32_to_tf32(pick(r.v[k][0], p));
+            o.y = f32_to_tf32(pick(r.v[k][1], p));
+            o.z = f32_to_tf32(pick(r.v[k][2], p));
+            o.w = f32_to_tf32(pick(r.v[k][3], p));
+            reinterpret_cast<uint4 *>(plane)[r.row[k] + p] = o;
+        }
+    }
+}
+
+template <int NT, int NB>
+__device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag,
+                               int t) {
+    const int my_units = a.total_units > (int)blockIdx.x ? (a.total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_units * a.chunks;
+    ConvRegs<NB> ra, rb;
+    auto finish = [&](const ConvRegs<NB> &r, int it) -> bool {
+        const int s = it % a.stages;
+        const uint32_t ph = (it / a.stages) & 1;
+        if (!wait_bar(bars.empty(s), ph ^ 1, abort_flag, a.err)) return false;
+        conv_store<NB>(a, r, smem + a.stage0_off + s * a.stage_bytes + a.b_off);
+        fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
+        mbar_arrive(bars.full_x(s));
+        return true;
+    };
+    if (total > 0) conv_issue<NT, NB>(a, ra, t, 0);
+    for (int it = 0; it < total; it += 2) {
+        if (it + 1 < total) conv_issue<NT, NB>(a, rb, t, it + 1);
+        if (!finish(ra, it)) return;
+        if (it + 1 >= total) break;
+        if (it + 2 < total) conv_issue<NT, NB>(a, ra, t, it + 2);
+        if (!finish(rb, it + 1)) return;
     }
 }
 
@@ -408,11 +454,13 @@ __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + e
 template <int KIND>
 __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars, uint32_t tmem,
                               volatile int *abort_flag) {
+    using R = Roles<KIND>;
+    constexpr int NH = R::kColGroups;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ew = warp - kEpiWarp0;  // 0..7
-    const int et = threadIdx.x - kEpiWarp0 * 32;
+    const int ew = warp - R::kEpiWarp0;
+    const int et = threadIdx.x - R::kEpiWarp0 * 32;
     const int qd = warp & 3;          // tensor-memory lane quadrant
-    const int hc = ew >> 2;           // which 16-column chunks (even / odd)
+    const int hc = ew >> 2;           // which 16-column chunks: cc = hc, hc + NH, ...
     const int L = qd * 32 + lane;     // accumulator row
     const int slot = L / a.Cout, co = L % a.Cout;
     const float bias = __ldg(&a.b[co]);
@@ -430,7 +478,7 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
         const int r0 = ru * a.RU;
         const int ab = j & 1;
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
-        if (epi_bar_any(!ok)) break;  // all epilogue warps leave together
+        if (epi_bar_any<R::kEpiThreads>(!ok)) break;  // all epilogue warps leave together
         tc_fence_after();
 
         // GN per-thread state (registers): pooled max/min of this thread's
@@ -448,7 +496,7 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
             if constexpr (kGN) {
 #pragma unroll
                 for (int kc = 0; kc < kMaxWin / 4; ++kc) {
-                    const int cc = hc + 2 * kc;
+                    const int cc = hc + NH * kc;
                     if (cc >= nchunks) break;
                     const int col0 = cc * 16;
                     float v[16];
@@ -472,7 +520,7 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
                     }
                 }
             } else {
-            for (int cc = hc; cc < nchunks; cc += 2) {
+            for (int cc = hc; cc < nchunks; cc += NH) {
                 const int col0 = cc * 16;
                 float v[16];
                 tmem_ld16(tmem + lane_off + ab * kAccStride + u * a.ucol + col0, v);
@@ -510,9 +558,9 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
         if (lane == 0) mbar_arrive(bars.acc_empty(ab));
 
         if (kMin) {
-            epi_bar();
+            epi_bar<R::kEpiThreads>();
             const int qps = 4 / a.S;  // quadrants per slot
-            for (int idx = et; idx < a.U * a.S * a.P; idx += kEpiThreads) {
+            for (int idx = et; idx < a.U * a.S * a.P; idx += R::kEpiThreads) {
                 const int u = idx / (a.S * a.P), rem = idx % (a.S * a.P);
                 const int s = rem / a.P, col = rem % a.P;
                 const int row = r0 + u * a.S + s;
@@ -523,11 +571,11 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
                 if (KIND == CONV_EPI_MIN_TANH2) o = tanhf(tanhf(o));
                 a.out[((size_t)n * a.Ho + row) * a.Wo + col] = o;
             }
-            epi_bar();
+            epi_bar<R::kEpiThreads>();
         } else if (kGN) {
             // pool: combine the two row slots (S == 2) through shared memory
             float *xg = scratch;                                  // [8 warps][32 lanes][kMaxWin][2]
-            float *st = scratch + kEpiWarps * 32 * kMaxWin * 2;   // [8 warps][32 lanes][2]
+            float *st = scratch + R::kEpiWarps * 32 * kMaxWin * 2;  // [8 warps][32 lanes][2]
             st[(ew * 32 + lane) * 2] = ls;
             st[(ew * 32 + lane) * 2 + 1] = lss;
 #pragma unroll
@@ -535,12 +583,12 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
                 xg[((ew * 32 + lane) * kMaxWin + k) * 2] = pmx[k];
                 xg[((ew * 32 + lane) * kMaxWin + k) * 2 + 1] = pmn[k];
             }
-            epi_bar();
+            epi_bar<R::kEpiThreads>();
             if (slot == 0 && ru < a.Hp) {
                 const int ew1 = hc * 4 + qd + 2;  // warp holding the same channel in row slot 1
 #pragma unroll
                 for (int k = 0; k < kMaxWin; ++k) {
-                    const int cc = hc + 2 * (k / 4);
+                    const int cc = hc + NH * (k / 4);
                     const int pw = cc * 4 + (k % 4);
                     if (cc >= nchunks || pw >= a.Wp) continue;
                     float mx = pmx[k], mn = pmn[k];
@@ -555,7 +603,7 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
             }
             // statistics: fixed-order sum per group
             const int cpg = a.Cout / a.groups;
-            for (int g = et; g < a.groups; g += kEpiThreads) {
+            for (int g = et; g < a.groups; g += R::kEpiThreads) {
                 double s0 = 0.0, s1 = 0.0;
                 for (int s = 0; s < a.S; ++s)
                     for (int h2 = 0; h2 < 2; ++h2)
@@ -569,7 +617,7 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
                 dst[0] = s0;
                 dst[1] = s1;
             }
-            epi_bar();
+            epi_bar<R::kEpiThreads>();
         }
     }
 }
@@ -590,12 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const TcArgs a) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(bars.full_w(s), 1);
-            mbar_init(bars.full_x(s), kConvThreads);
+            mbar_init(bars.full_x(s), Roles<KIND>::kConvThreads);
             mbar_init(bars.empty(s), 1);
         }
         for (int ab = 0; ab < 2; ++ab) {
             mbar_init(bars.acc_full(ab), 1);
-            mbar_init(bars.acc_empty(ab), kEpiWarps);
+            mbar_init(bars.acc_empty(ab), Roles<KIND>::kEpiWarps);
         }
         mbar_init(bars.final_bar(), 1);
         mbar_init(bars.wres(), 1);
@@ -618,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const TcArgs a) {
     } else if (warp == 1) {
         if (lane == 0) weight_role(a, sbase, bars, abort_flag);
         __syncwarp();
-    } else if (warp < kEpiWarp0) {
-        converter_role(a, sbase, bars, abort_flag);
+    } else if (warp < Roles<KIND>::kEpiWarp0) {
+        converter_role<Roles<KIND>::kConvThreads, Roles<KIND>::kNBMax>(
+            a, smem, bars, abort_flag, threadIdx.x - Roles<KIND>::kConvWarp0 * 32);
     } else {
         epilogue_role<KIND>(a, scratch, bars, tmem, abort_flag);
     }
@@ -672,11 +721,24 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_SCALE_MIN:
         return (uint32_t)(U * 4 * P * sizeof(float));
     case CONV_EPI_MUL_LRELU_GELU:
-        return (uint32_t)(kEpiWarps * 32 * kStgPitch * sizeof(float));
-    case CONV_EPI_GN_SCALE_POOL_CLAMP:
-        return (uint32_t)((kEpiWarps * 32 * 16 * 2 + kEpiWarps * 32 * 2) * sizeof(float));
+        return (uint32_t)(Roles<CONV_EPI_MUL_LRELU_GELU>::kEpiWarps * 32 * kStgPitch * sizeof(float));
+    case CONV_EPI_GN_SCALE_POOL_CLAMP: {
+        constexpr int ew = Roles<CONV_EPI_GN_SCALE_POOL_CLAMP>::kEpiWarps;
+        return (uint32_t)((ew * 32 * 16 * 2 + ew * 32 * 2) * sizeof(float));
+    }
     }
     return 0;
+}
+
+int conv_threads_for(int kind) {
+    switch (kind) {
+    case CONV_EPI_MIN_TANH2: return Roles<CONV_EPI_MIN_TANH2>::kConvThreads * Roles<CONV_EPI_MIN_TANH2>::kNBMax;
+    case CONV_EPI_SCALE_MIN: return Roles<CONV_EPI_SCALE_MIN>::kConvThreads * Roles<CONV_EPI_SCALE_MIN>::kNBMax;
+    case CONV_EPI_MUL_LRELU_GELU:
+        return Roles<CONV_EPI_MUL_LRELU_GELU>::kConvThreads * Roles<CONV_EPI_MUL_LRELU_GELU>::kNBMax;
+    default:
+        return Roles<CONV_EPI_GN_SCALE_POOL_CLAMP>::kConvThreads * Roles<CONV_EPI_GN_SCALE_POOL_CLAMP>::kNBMax;
+    }
 }
 
 // Shared memory: [resident filter][stages x (A? + B)][mbarriers][tmem slot, abort][scratch]
@@ -692,6 +754,8 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.PL = (pl.Rin * pl.P + 4 + 7) / 8 * 8;
     pl.chunks = d.Cin / 8;
     if (pl.PL >= (1 << 16)) return false;
+    // every 4x4 block of a chunk's B plane has a converter slot
+    if (pl.PL / 2 > conv_threads_for(kind)) return false;
     pl.a_bytes = 3u * 2u * (2 * pl.S + 1) * d.Cout * 16u;
     pl.b_bytes = 2u * pl.PL * 16u;
     pl.scratch_bytes = scratch_bytes_for(kind, pl.U, pl.P);
