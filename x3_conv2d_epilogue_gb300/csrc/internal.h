@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/conv_epi.h"
+#include "conv_epi.h"
 
 namespace conv_epi {
 

@@ -14,13 +14,16 @@
 // Operands in shared memory, both "K-major, no swizzle" with a 16-byte row:
 //   B (positions x 8 channels): plane[ci4][q][4 floats] -- position rows are
 //      16 bytes apart, so a tap shift of kh*P + kw positions is a plain
-//      (16-byte aligned) change of the descriptor's start address.  NCHW has
-//      positions contiguous per channel, so converter warps transpose the
-//      input tile on the way in (global -> registers -> shared), rounding to
-//      tf32 (round-to-nearest) as they go.
-//   A (128 rows x 8 channels): packed filter planes, loaded by the bulk-copy
-//      engine (cp.async.bulk) from a buffer the prep kernel writes each call.
+//      (16-byte aligned) change of the descriptor's start address.
+//   A (128 rows x 8 channels): packed filter planes (bulk copy engine).
 // Accumulators live in tensor memory (128 lanes x 512 columns, fp32).
+//
+// Input path.  The TMA engine loads each raw NCHW tile (8 channels x the
+// unit's input rows x W) into a ring of staging buffers, zero-filling rows past
+// the image.  Converter warps transpose a staged tile shared->shared into the
+// B plane (4x4 register transposes, tf32 round-to-nearest), so their
+// proxy fence before handing the plane to the tensor core covers only short
+// shared-memory stores -- never global loads in flight.
 //
 // Row slots.  The MMA's M is 128.  With Cout = 128 a tile is one output row
 // per accumulator.  With Cout = 64 the 128 accumulator lanes hold TWO output
@@ -32,17 +35,20 @@
 //
 // One CTA per SM (persistent), 16 warps:
 //   warp 0      tensor-memory allocator + single-thread MMA issuer
-//   warp 1      filter producer (bulk copies into the stage ring)
-//   warps 2-7   converters (input tile -> B plane)
+//   warp 1      filter producer (bulk copies, or one resident load)
+//   warp 2      input-tile producer (TMA tensor loads into the staging ring)
+//   warps 3-7   converters (staged tile -> B plane)
 //   warps 8-15  epilogue (tensor memory -> chain -> global), two warps per
-//               32-lane quadrant, alternating 16-column chunks
-// Stages: a ring of (A, B) buffers with full/empty mbarriers; two
-// accumulator buffers in tensor memory so the epilogue of one unit overlaps
-// the main loop of the next.  Every wait is bounded (2 s of %globaltimer);
-// on expiry the kernel raises an error bit, drains what it has in flight and
-// returns, so the context stays usable.
+//               32-lane quadrant, alternating column chunks
+// Rings (mbarrier full/empty pairs): filter stages, B planes, staged tiles;
+// two accumulator buffers in tensor memory so the epilogue of one unit
+// overlaps the main loop of the next.  Every wait is bounded (2 s of
+// %globaltimer); on expiry the kernel raises an error bit, drains what it has
+// in flight and returns, so the context stays usable.
+#include <cuda.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "internal.h"
 
@@ -50,45 +56,34 @@ namespace conv_epi {
 namespace {
 
 constexpr int kThreads = 512;
-// Warp roles per chain: the min chains need 4 epilogue warps, the per-channel
-// and GroupNorm chains 8; the converters take the warps in between.
-template <int KIND>
-struct Roles {
-    static constexpr bool kMinKind = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
-    static constexpr int kEpiWarps = kMinKind ? 4 : 8;
-    static constexpr int kEpiWarp0 = 16 - kEpiWarps;  // a multiple of 4 (tensor-memory quadrants)
-    static constexpr int kConvWarp0 = 2;
-    static constexpr int kConvWarps = kEpiWarp0 - kConvWarp0;
-    static constexpr int kConvThreads = kConvWarps * 32;
-    static constexpr int kEpiThreads = kEpiWarps * 32;
-    static constexpr int kColGroups = kEpiWarps / 4;  // epilogue warps per quadrant
-    static constexpr int kNBMax = kMinKind ? 2 : 3;   // 4x4 blocks per converter thread per chunk
-};
+constexpr int kConvWarp0 = 3, kConvWarps = 5, kConvThreads = kConvWarps * 32;
+constexpr int kEpiWarp0 = 8, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;     // columns per accumulator buffer
-constexpr int kMaxStages = 6;
+constexpr int kMaxRing = 4;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
-constexpr int kStgPitch = 17;       // epilogue transpose staging pitch (floats)
+constexpr int kStgPitch = 18;       // per-channel epilogue staging pitch (floats, even: float2 rows)
+constexpr int kPoolPitch = 33;      // GroupNorm pooled tile pitch (floats)
 
-struct TcArgs {
+struct TcArgs {  // 64-byte aligned through CUtensorMap
+    CUtensorMap xmap;  // x as a 4-D tensor (W, H, Cin, N); box (W, Rin, 8, 1)
     const float *x, *b, *wpack;
     float *out;
     unsigned *err;
     int N, Cin, H, W, Cout, Ho, Wo;
-    int S, P, U, RU, PL;
-    int ucol;          // tensor-memory columns between the unit's accumulators (multiple of 32)
-    uint32_t p_magic;  // ceil(2^32 / P), exact division for q < 2^16
-    int chunks, units_per_img, total_units, stages;
-    uint32_t a_bytes, b_bytes, stage_bytes, scratch_off;
-    int resident;          // 1: every filter chunk stays in shared memory for the whole kernel
-    uint32_t stage0_off;   // byte offset of stage 0 (after the resident filter, if any)
-    uint32_t b_off;        // byte offset of B inside a stage (0 when the filter is resident)
+    int S, P, U, RU, Rin, PL, ucol;
+    uint32_t p_magic;  // ceil(2^32 / P): exact q / P for q < 2^16
+    int chunks, units_per_img, total_units;
+    int resident;      // 1: the whole packed filter stays in shared memory
+    int na, nb, nr;    // ring depths: filter stages (streaming), B planes, staged tiles
+    uint32_t a_bytes, b_bytes, raw_bytes, raw_tx;  // raw_tx: exact bytes of one staged tile
+    uint32_t a_off, b_off, raw_off, bar_off, scratch_off;
     uint32_t a_kw_stride, a_lbo, a_plane_bytes;
     uint32_t idesc;
     float scalar;
     const float *chan_scale;
     float slope;
-    int groups, pool_k, Hp, Wp;
+    int groups, Hp, Wp;
     GnWork gn;
 };
 
@@ -127,19 +122,27 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// 4-D tiled TMA load; coordinates innermost first
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ uint32_t f32_to_tf32(float f) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
     return r;
 }
-template <int NT>
-__device__ __forceinline__ void epi_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
 // barrier over the epilogue warps that also ORs a flag across them, so they
 // all take the same branch after it
-template <int NT>
 __device__ __forceinline__ bool epi_bar_any(bool v) {
     uint32_t r;
     asm volatile(
@@ -148,7 +151,7 @@ __device__ __forceinline__ bool epi_bar_any(bool v) {
         "bar.red.or.pred p, 1, %2, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v), "n"(NT)
+        : "r"((uint32_t)v), "n"(kEpiThreads)
         : "memory");
     return r != 0;
 }
@@ -183,24 +186,39 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-// 32 lanes x 16 consecutive 32-bit columns; wait folded in so that no use of
-// the registers can be scheduled before the load has landed
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+// 32 lanes x 16 consecutive 32-bit columns.  Issue and wait are split so
+// that the next load overlaps work on the current registers; the wait names
+// the destination registers so no use can be scheduled before it.
+struct Frag16 {
     uint32_t r[16];
+};
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, Frag16 &f) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "=r"(f.r[0]), "=r"(f.r[1]), "=r"(f.r[2]), "=r"(f.r[3]), "=r"(f.r[4]), "=r"(f.r[5]), "=r"(f.r[6]),
+          "=r"(f.r[7]), "=r"(f.r[8]), "=r"(f.r[9]), "=r"(f.r[10]), "=r"(f.r[11]), "=r"(f.r[12]), "=r"(f.r[13]),
+          "=r"(f.r[14]), "=r"(f.r[15])
         : "r"(taddr)
         : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(Frag16 &f) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15])
+                 : "+r"(f.r[0]), "+r"(f.r[1]), "+r"(f.r[2]), "+r"(f.r[3]), "+r"(f.r[4]), "+r"(f.r[5]),
+                   "+r"(f.r[6]), "+r"(f.r[7]), "+r"(f.r[8]), "+r"(f.r[9]), "+r"(f.r[10]), "+r"(f.r[11]),
+                   "+r"(f.r[12]), "+r"(f.r[13]), "+r"(f.r[14]), "+r"(f.r[15])
                  :
                  : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait2(Frag16 &f, Frag16 &g) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(f.r[0]), "+r"(f.r[1]), "+r"(f.r[2]), "+r"(f.r[3]), "+r"(f.r[4]), "+r"(f.r[5]),
+                   "+r"(f.r[6]), "+r"(f.r[7]), "+r"(f.r[8]), "+r"(f.r[9]), "+r"(f.r[10]), "+r"(f.r[11]),
+                   "+r"(f.r[12]), "+r"(f.r[13]), "+r"(f.r[14]), "+r"(f.r[15]), "+r"(g.r[0]), "+r"(g.r[1]),
+                   "+r"(g.r[2]), "+r"(g.r[3]), "+r"(g.r[4]), "+r"(g.r[5]), "+r"(g.r[6]), "+r"(g.r[7]),
+                   "+r"(g.r[8]), "+r"(g.r[9]), "+r"(g.r[10]), "+r"(g.r[11]), "+r"(g.r[12]), "+r"(g.r[13]),
+                   "+r"(g.r[14]), "+r"(g.r[15])
+                 :
+                 : "memory");
 }
 
 // Shared-memory matrix descriptor, K-major, no swizzle (canonical layout
@@ -231,20 +249,23 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag
     }
 }
 
-// --------------------------------------------------------------- roles ----
+// ---------------------------------------------------------- barriers ----
 struct Bars {
     uint32_t base;
-    int stages;
-    __device__ uint32_t full_w(int s) const { return base + 8u * s; }
-    __device__ uint32_t full_x(int s) const { return base + 8u * (stages + s); }
-    __device__ uint32_t empty(int s) const { return base + 8u * (2 * stages + s); }
-    __device__ uint32_t acc_full(int ab) const { return base + 8u * (3 * stages + ab); }
-    __device__ uint32_t acc_empty(int ab) const { return base + 8u * (3 * stages + 2 + ab); }
-    __device__ uint32_t final_bar() const { return base + 8u * (3 * stages + 4); }
-    __device__ uint32_t wres() const { return base + 8u * (3 * stages + 5); }
-    static constexpr int count(int stages) { return 3 * stages + 6; }
+    __device__ uint32_t a_full(int s) const { return base + 8u * s; }
+    __device__ uint32_t a_empty(int s) const { return base + 8u * (kMaxRing + s); }
+    __device__ uint32_t b_full(int s) const { return base + 8u * (2 * kMaxRing + s); }
+    __device__ uint32_t b_empty(int s) const { return base + 8u * (3 * kMaxRing + s); }
+    __device__ uint32_t r_full(int s) const { return base + 8u * (4 * kMaxRing + s); }
+    __device__ uint32_t r_empty(int s) const { return base + 8u * (5 * kMaxRing + s); }
+    __device__ uint32_t acc_full(int ab) const { return base + 8u * (6 * kMaxRing + ab); }
+    __device__ uint32_t acc_empty(int ab) const { return base + 8u * (6 * kMaxRing + 2 + ab); }
+    __device__ uint32_t final_bar() const { return base + 8u * (6 * kMaxRing + 4); }
+    __device__ uint32_t wres() const { return base + 8u * (6 * kMaxRing + 5); }
+    static constexpr int kCount = 6 * kMaxRing + 6;
 };
 
+// ------------------------------------------------------------- roles ----
 __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint32_t tmem, volatile int *abort_flag) {
     int it = 0, j = 0;
     bool ok = true;
@@ -258,17 +279,15 @@ __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint
         tc_fence_after();
         const uint32_t dcol = tmem + ab * kAccStride;
         for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int s = it % a.stages;
-            const uint32_t ph = (it / a.stages) & 1;
-            if ((!a.resident && !wait_bar(bars.full_w(s), ph, abort_flag, a.err)) ||
-                !wait_bar(bars.full_x(s), ph, abort_flag, a.err)) {
+            const int sa = it % a.na, sb = it % a.nb;
+            if ((!a.resident && !wait_bar(bars.a_full(sa), (it / a.na) & 1, abort_flag, a.err)) ||
+                !wait_bar(bars.b_full(sb), (it / a.nb) & 1, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t S0 = sbase + a.stage0_off + s * a.stage_bytes;
-            const uint32_t A0 = a.resident ? sbase + c * a.a_bytes : S0;
-            const uint32_t B0 = S0 + a.b_off;
+            const uint32_t A0 = sbase + a.a_off + (a.resident ? c : sa) * a.a_bytes;
+            const uint32_t B0 = sbase + a.b_off + sb * a.b_bytes;
             for (int u = 0; u < a.U; ++u) {
                 for (int sk = 0; sk <= a.S + 1; ++sk) {
 #pragma unroll
@@ -280,7 +299,9 @@ __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint
                     }
                 }
             }
-            mma_commit(bars.empty(s));  // stage s may be refilled once these MMAs are done
+            // the stages may be refilled once these MMAs are done
+            mma_commit(bars.b_empty(sb));
+            if (!a.resident) mma_commit(bars.a_empty(sa));
         }
         if (!ok) break;
         mma_commit(bars.acc_full(ab));  // accumulator ab is complete
@@ -297,128 +318,122 @@ __device__ void weight_role(const TcArgs &a, uint32_t sbase, const Bars &bars, v
         const uint32_t total = a.chunks * a.a_bytes;
         mbar_arrive_expect_tx(bars.wres(), total);
         for (uint32_t off = 0; off < total; off += 16384u)
-            bulk_g2s(sbase + off, wsrc + off, min(16384u, total - off), bars.wres());
+            bulk_g2s(sbase + a.a_off + off, wsrc + off, min(16384u, total - off), bars.wres());
         wait_bar(bars.wres(), 0, abort_flag, a.err, false);
         return;
     }
     int it = 0;
-    int last_par[kMaxStages];
-    bool issued[kMaxStages];
-    for (int s = 0; s < kMaxStages; ++s) issued[s] = false, last_par[s] = 0;
+    int last_par[kMaxRing];
+    bool issued[kMaxRing];
+    for (int s = 0; s < kMaxRing; ++s) issued[s] = false, last_par[s] = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
         for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int s = it % a.stages;
-            const uint32_t ph = (it / a.stages) & 1;
-            if (!wait_bar(bars.empty(s), ph ^ 1, abort_flag, a.err)) {
+            const int s = it % a.na;
+            const uint32_t ph = (it / a.na) & 1;
+            if (!wait_bar(bars.a_empty(s), ph ^ 1, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
-            const uint32_t dst = sbase + a.stage0_off + s * a.stage_bytes;
+            const uint32_t dst = sbase + a.a_off + s * a.a_bytes;
             const char *src = wsrc + (size_t)c * a.a_bytes;
-            mbar_arrive_expect_tx(bars.full_w(s), a.a_bytes);
-            for (uint32_t off = 0; off < a.a_bytes; off += 16384u) {
-                const uint32_t n = min(16384u, a.a_bytes - off);
-                bulk_g2s(dst + off, src + off, n, bars.full_w(s));
-            }
+            mbar_arrive_expect_tx(bars.a_full(s), a.a_bytes);
+            for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
+                bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(s));
             issued[s] = true, last_par[s] = ph;
         }
     }
     // copies still in flight land before the CTA exits
-    for (int s = 0; s < a.stages; ++s)
-        if (issued[s]) wait_bar(bars.full_w(s), last_par[s], abort_flag, a.err, false);
+    for (int s = 0; s < a.na; ++s)
+        if (issued[s]) wait_bar(bars.a_full(s), last_par[s], abort_flag, a.err, false);
 }
 
-// Converter warps: x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] -> B plane
-// [ci4][q][4] of a stage.  Work item = one 4x4 block: 4 consecutive positions
-// (one 16-byte global load per channel) x 4 channels; a register transpose
-// turns it into 4 position rows of 16 bytes, rounded to tf32.  The rows are
-// stored in a per-thread rotated order so that the 8 threads of a store phase
-// hit 8 different bank groups.  Positions outside the image are zero.
-// Registers hold two chunks: the loads of chunk it+1 are in flight while the
-// thread waits for its stage and stores chunk it.
-template <int NB>
-struct ConvRegs {
-    float4 v[NB][4];
-    int row[NB];  // first B-plane row of the block (jg*PL + q), -1 when absent
-};
+// TMA producer: raw tile of chunk (unit, c) = x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1]
+// into staging slot it % nr, laid out [8][Rin][W]; rows >= H arrive as zeros.
+__device__ void tile_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
+    prefetch_tensormap(&a.xmap);
+    int it = 0;
+    int last_par[kMaxRing];
+    bool issued[kMaxRing];
+    for (int s = 0; s < kMaxRing; ++s) issued[s] = false, last_par[s] = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
+        const int n = unit / a.units_per_img;
+        const int r0 = (unit % a.units_per_img) * a.RU;
+        for (int c = 0; c < a.chunks; ++c, ++it) {
+            const int s = it % a.nr;
+            const uint32_t ph = (it / a.nr) & 1;
+            if (!wait_bar(bars.r_empty(s), ph ^ 1, abort_flag, a.err)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(bars.r_full(s), a.raw_tx);
+            tma_load_4d(sbase + a.raw_off + s * a.raw_bytes, &a.xmap, 0, r0, 8 * c, n, bars.r_full(s));
+            issued[s] = true, last_par[s] = ph;
+        }
+    }
+    for (int s = 0; s < a.nr; ++s)
+        if (issued[s]) wait_bar(bars.r_full(s), last_par[s], abort_flag, a.err, false);
+}
 
+// Converter warps: staged tile [8][Rin][W] -> B plane [ci4][q][4].  Work item =
+// one 4x4 block: 4 consecutive positions (one 16-byte shared load per
+// channel) x 4 channels, transposed in registers into 4 position rows of
+// 16 bytes, rounded to tf32.  The rows are stored in a per-thread rotated
+// order so that the 8 threads of a store phase hit 8 different bank groups.
+// Positions past the staged rows, or with w >= W, are zero.
 __device__ __forceinline__ float pick(const float4 &v, int p) {
     return p == 0 ? v.x : (p == 1 ? v.y : (p == 2 ? v.z : v.w));
 }
 
-template <int NT, int NB>
-__device__ __forceinline__ void conv_issue(const TcArgs &a, ConvRegs<NB> &r, int t, int flat) {
-    const int unit = blockIdx.x + (flat / a.chunks) * gridDim.x;
-    const int c = flat % a.chunks;
-    const int n = unit / a.units_per_img;
-    const int r0 = (unit % a.units_per_img) * a.RU;
-    const size_t HW = (size_t)a.H * a.W;
+__device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
+    const int t = threadIdx.x - kConvWarp0 * 32;
     const int qpp = a.PL >> 2;  // 4-position groups per ci4 plane
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-        const int b = t + k * NT;
-        r.row[k] = -1;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) r.v[k][e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (b < 2 * qpp) {
-            const int jg = b >= qpp ? 1 : 0;
-            const int q = 4 * (b - jg * qpp);
-            const int rr = __umulhi((uint32_t)q, a.p_magic);
-            const int w = q - rr * a.P;
-            const int h = r0 + rr;
-            r.row[k] = jg * a.PL + q;
-            if (h < a.H && w < a.W) {
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    a.x + (((size_t)n * a.Cin + 8 * c + 4 * jg) * HW + (size_t)h * a.W + w));
-#pragma unroll
-                for (int e = 0; e < 4; ++e) r.v[k][e] = __ldg(src + e * (HW >> 2));
+    const int nblk = 2 * qpp;
+    const int plane_stride = a.Rin * a.W;  // floats between channels of a staged tile
+    int it = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
+        for (int c = 0; c < a.chunks; ++c, ++it) {
+            const int sr = it % a.nr, sb = it % a.nb;
+            if (!wait_bar(bars.r_full(sr), (it / a.nr) & 1, abort_flag, a.err) ||
+                !wait_bar(bars.b_empty(sb), ((it / a.nb) & 1) ^ 1, abort_flag, a.err)) {
+                ok = false;
+                break;
             }
-        }
-    }
-}
-
-template <int NB>
-__device__ __forceinline__ void conv_store(const TcArgs &a, const ConvRegs<NB> &r, uint8_t *plane) {
+            const float *raw = reinterpret_cast<const float *>(smem + a.raw_off + sr * a.raw_bytes);
+            uint4 *plane = reinterpret_cast<uint4 *>(smem + a.b_off + sb * a.b_bytes);
+            for (int blk = t; blk < nblk; blk += kConvThreads) {
+                const int jg = blk >= qpp ? 1 : 0;
+                const int q = 4 * (blk - jg * qpp);
+                const int rr = __umulhi((uint32_t)q, a.p_magic);
+                const int w = q - rr * a.P;
+                float4 v[4];
+                if (rr < a.Rin && w < a.W) {
+                    const float *src = raw + (4 * jg) * plane_stride + rr * a.W + w;
 #pragma unroll
-    for (int k = 0; k < NB; ++k) {
-        if (r.row[k] < 0) continue;
-        const int rot = (r.row[k] >> 3) & 3;  // (position group / 2) mod 4
+                    for (int e = 0; e < 4; ++e) v[e] = *reinterpret_cast<const float4 *>(src + e * plane_stride);
+                } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int p = (i + rot) & 3;
-            uint4 o;
-            o.x = f32_to_tf32(pick(r.v[k][0], p));
-            o.y = f32_to_tf32(pick(r.v[k][1], p));
-            o.z = f32_to_tf32(pick(r.v[k][2], p));
-            o.w = f32_to_tf32(pick(r.v[k][3], p));
-            reinterpret_cast<uint4 *>(plane)[r.row[k] + p] = o;
+                    for (int e = 0; e < 4; ++e) v[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                const int row = jg * a.PL + q;
+                const int rot = (row >> 3) & 3;  // (position group / 2) mod 4
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int p = (i + rot) & 3;
+                    uint4 o;
+                    o.x = f32_to_tf32(pick(v[0], p));
+                    o.y = f32_to_tf32(pick(v[1], p));
+                    o.z = f32_to_tf32(pick(v[2], p));
+                    o.w = f32_to_tf32(pick(v[3], p));
+                    plane[row + p] = o;
+                }
+            }
+            mbar_arrive(bars.r_empty(sr));  // staged tile read
+            fence_proxy_async_smem();       // make the generic-proxy stores visible to the tensor core
+            mbar_arrive(bars.b_full(sb));
         }
-    }
-}
-
-template <int NT, int NB>
-__device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag,
-                               int t) {
-    const int my_units = a.total_units > (int)blockIdx.x ? (a.total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int total = my_units * a.chunks;
-    ConvRegs<NB> ra, rb;
-    auto finish = [&](const ConvRegs<NB> &r, int it) -> bool {
-        const int s = it % a.stages;
-        const uint32_t ph = (it / a.stages) & 1;
-        if (!wait_bar(bars.empty(s), ph ^ 1, abort_flag, a.err)) return false;
-        conv_store<NB>(a, r, smem + a.stage0_off + s * a.stage_bytes + a.b_off);
-        fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
-        mbar_arrive(bars.full_x(s));
-        return true;
-    };
-    if (total > 0) conv_issue<NT, NB>(a, ra, t, 0);
-    for (int it = 0; it < total; it += 2) {
-        if (it + 1 < total) conv_issue<NT, NB>(a, rb, t, it + 1);
-        if (!finish(ra, it)) return;
-        if (it + 1 >= total) break;
-        if (it + 2 < total) conv_issue<NT, NB>(a, ra, t, it + 2);
-        if (!finish(rb, it + 1)) return;
     }
 }
 
@@ -451,24 +466,71 @@ __device__ __forceinline__ void reduce_scatter16(float (&v)[16], int lane, int s
 
 __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erff(t * 0.70710678118654752f)); }
 
+// Per-chunk work of the min / per-channel chains on 16 accumulator columns.
+template <int KIND>
+__device__ __forceinline__ void epi_chunk(const TcArgs &a, const Frag16 &f, float bias, float mult, int sgn,
+                                          int lane, int qd, int ew, int u, int n, int row, int col0,
+                                          float *scratch) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(f.r[i]) + bias;
+    if (KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN) {
+        reduce_scatter16(v, lane, sgn);
+        if ((lane & 1) == 0) scratch[(u * 4 + qd) * a.P + col0 + (lane >> 1)] = v[0];
+    } else {
+        // per-channel chain: transpose 32 channels x 16 columns through shared
+        // memory so each store instruction writes 4 rows of 64 contiguous bytes
+        float *stg = scratch + ew * 32 * kStgPitch;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            float t0 = v[i] * mult, t1 = v[i + 1] * mult;
+            t0 = t0 > 0.0f ? t0 : a.slope * t0;
+            t1 = t1 > 0.0f ? t1 : a.slope * t1;
+            *reinterpret_cast<float2 *>(stg + lane * kStgPitch + i) = make_float2(gelu_erf(t0), gelu_erf(t1));
+        }
+        __syncwarp();
+        if (row < a.Ho) {
+            const int c2 = 2 * (lane & 7);
+            if ((a.Wo & 1) == 0) {
+#pragma unroll
+                for (int rp = 0; rp < 8; ++rp) {
+                    const int rr = 4 * rp + (lane >> 3);
+                    const int cor = (qd * 32 + rr) % a.Cout;
+                    if (col0 + c2 < a.Wo) {
+                        float *dst = a.out + (((size_t)n * a.Cout + cor) * a.Ho + row) * a.Wo + col0 + c2;
+                        *reinterpret_cast<float2 *>(dst) = *reinterpret_cast<const float2 *>(stg + rr * kStgPitch + c2);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int rp = 0; rp < 8; ++rp) {
+                    const int rr = 4 * rp + (lane >> 3);
+                    const int cor = (qd * 32 + rr) % a.Cout;
+                    float *dst = a.out + (((size_t)n * a.Cout + cor) * a.Ho + row) * a.Wo + col0 + c2;
+                    if (col0 + c2 < a.Wo) dst[0] = stg[rr * kStgPitch + c2];
+                    if (col0 + c2 + 1 < a.Wo) dst[1] = stg[rr * kStgPitch + c2 + 1];
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
 template <int KIND>
 __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars, uint32_t tmem,
                               volatile int *abort_flag) {
-    using R = Roles<KIND>;
-    constexpr int NH = R::kColGroups;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ew = warp - R::kEpiWarp0;
-    const int et = threadIdx.x - R::kEpiWarp0 * 32;
+    const int ew = warp - kEpiWarp0;  // 0..7
+    const int et = threadIdx.x - kEpiWarp0 * 32;
     const int qd = warp & 3;          // tensor-memory lane quadrant
-    const int hc = ew >> 2;           // which 16-column chunks: cc = hc, hc + NH, ...
+    const int hc = ew >> 2;           // column group: chunks cc = hc, hc + 2, ...
     const int L = qd * 32 + lane;     // accumulator row
     const int slot = L / a.Cout, co = L % a.Cout;
     const float bias = __ldg(&a.b[co]);
     const int sgn = a.scalar > 0.0f ? 1 : (a.scalar < 0.0f ? -1 : 0);
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
-    float mult = 0.0f;
-    if (KIND == CONV_EPI_MUL_LRELU_GELU) mult = __ldg(&a.chan_scale[co]);
+    const float mult = KIND == CONV_EPI_MUL_LRELU_GELU ? __ldg(&a.chan_scale[co]) : 0.0f;
     const int nchunks = a.P / 16;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     int j = 0;
@@ -478,15 +540,16 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
         const int r0 = ru * a.RU;
         const int ab = j & 1;
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
-        if (epi_bar_any<R::kEpiThreads>(!ok)) break;  // all epilogue warps leave together
+        if (epi_bar_any(!ok)) break;  // all epilogue warps leave together
         tc_fence_after();
+        const uint32_t tbase = tmem + lane_off + ab * kAccStride;
 
-        // GN per-thread state (registers): pooled max/min of this thread's
-        // 4-column windows (4 per 16-column chunk, at most 4 chunks: P <= 128)
+        // GN per-thread state: pooled max/min of this thread's 4-column windows
+        // (4 per 16-column chunk, at most 4 chunks: P <= 128), and sums of y, y^2
         constexpr int kMaxWin = 16;
         float pmx[kMaxWin], pmn[kMaxWin];
         float ls = 0.0f, lss = 0.0f;
-        if (kGN) {
+        if constexpr (kGN) {
 #pragma unroll
             for (int k = 0; k < kMaxWin; ++k) pmx[k] = -INFINITY, pmn[k] = INFINITY;
         }
@@ -494,62 +557,51 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
         for (int u = 0; u < a.U; ++u) {
             const int row = r0 + u * a.S + slot;  // the same for the whole warp
             if constexpr (kGN) {
+                Frag16 f[kMaxWin / 4];
+#pragma unroll
+                for (int kc = 0; kc < kMaxWin / 4; ++kc)
+                    if (hc + 2 * kc < nchunks) tmem_ld16_issue(tbase + u * a.ucol + (hc + 2 * kc) * 16, f[kc]);
+                tmem_ld_wait2(f[0], f[1]);
+                tmem_ld_wait2(f[2], f[3]);
 #pragma unroll
                 for (int kc = 0; kc < kMaxWin / 4; ++kc) {
-                    const int cc = hc + NH * kc;
-                    if (cc >= nchunks) break;
+                    const int cc = hc + 2 * kc;
+                    if (cc >= nchunks || row >= a.Ho) continue;
                     const int col0 = cc * 16;
                     float v[16];
-                    tmem_ld16(tmem + lane_off + ab * kAccStride + u * a.ucol + col0, v);
-                    if (row < a.Ho) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            v[i] += bias;
-                            if (col0 + i < a.Wo) {
-                                ls += v[i];
-                                lss = fmaf(v[i], v[i], lss);
-                            }
+                    for (int i = 0; i < 16; ++i) {
+                        v[i] = __uint_as_float(f[kc].r[i]) + bias;
+                        if (col0 + i < a.Wo) {
+                            ls += v[i];
+                            lss = fmaf(v[i], v[i], lss);
                         }
+                    }
 #pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            const float mx = fmaxf(fmaxf(v[4 * wi], v[4 * wi + 1]), fmaxf(v[4 * wi + 2], v[4 * wi + 3]));
-                            const float mn = fminf(fminf(v[4 * wi], v[4 * wi + 1]), fminf(v[4 * wi + 2], v[4 * wi + 3]));
-                            pmx[4 * kc + wi] = fmaxf(pmx[4 * kc + wi], mx);
-                            pmn[4 * kc + wi] = fminf(pmn[4 * kc + wi], mn);
-                        }
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const float mx = fmaxf(fmaxf(v[4 * wi], v[4 * wi + 1]), fmaxf(v[4 * wi + 2], v[4 * wi + 3]));
+                        const float mn = fminf(fminf(v[4 * wi], v[4 * wi + 1]), fminf(v[4 * wi + 2], v[4 * wi + 3]));
+                        pmx[4 * kc + wi] = fmaxf(pmx[4 * kc + wi], mx);
+                        pmn[4 * kc + wi] = fminf(pmn[4 * kc + wi], mn);
                     }
                 }
             } else {
-            for (int cc = hc; cc < nchunks; cc += NH) {
-                const int col0 = cc * 16;
-                float v[16];
-                tmem_ld16(tmem + lane_off + ab * kAccStride + u * a.ucol + col0, v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] += bias;
-                if (kMin) {
-                    reduce_scatter16(v, lane, sgn);
-                    if ((lane & 1) == 0) scratch[(u * 4 + qd) * a.P + col0 + (lane >> 1)] = v[0];
-                } else if (KIND == CONV_EPI_MUL_LRELU_GELU) {
-                    float *stg = scratch + ew * 32 * kStgPitch;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float t = v[i] * mult;
-                        t = t > 0.0f ? t : a.slope * t;
-                        stg[lane * kStgPitch + i] = gelu_erf(t);
-                    }
-                    __syncwarp();
-                    const int c = lane & 15;
-                    if (row < a.Ho && col0 + c < a.Wo) {
-#pragma unroll 4
-                        for (int rp = 0; rp < 16; ++rp) {
-                            const int rr = 2 * rp + (lane >> 4);
-                            const int cor = (qd * 32 + rr) % a.Cout;
-                            a.out[(((size_t)n * a.Cout + cor) * a.Ho + row) * a.Wo + col0 + c] = stg[rr * kStgPitch + c];
-                        }
-                    }
-                    __syncwarp();
+                // software-pipelined: the load of chunk cc+2 is in flight while chunk cc is processed
+                int cc = hc;
+                Frag16 cur, nxt;
+                if (cc < nchunks) {
+                    tmem_ld16_issue(tbase + u * a.ucol + cc * 16, cur);
+                    tmem_ld_wait(cur);
                 }
-            }
+                for (; cc < nchunks; cc += 2) {
+                    const bool more = cc + 2 < nchunks;
+                    if (more) tmem_ld16_issue(tbase + u * a.ucol + (cc + 2) * 16, nxt);
+                    epi_chunk<KIND>(a, cur, bias, mult, sgn, lane, qd, ew, u, n, row, cc * 16, scratch);
+                    if (more) {
+                        tmem_ld_wait(nxt);
+                        cur = nxt;
+                    }
+                }
             }
         }
         // tensor memory of this unit is no longer needed
@@ -557,10 +609,10 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.acc_empty(ab));
 
-        if (kMin) {
-            epi_bar<R::kEpiThreads>();
+        if constexpr (kMin) {
+            epi_bar();
             const int qps = 4 / a.S;  // quadrants per slot
-            for (int idx = et; idx < a.U * a.S * a.P; idx += R::kEpiThreads) {
+            for (int idx = et; idx < a.U * a.S * a.P; idx += kEpiThreads) {
                 const int u = idx / (a.S * a.P), rem = idx % (a.S * a.P);
                 const int s = rem / a.P, col = rem % a.P;
                 const int row = r0 + u * a.S + s;
@@ -571,79 +623,86 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
                 if (KIND == CONV_EPI_MIN_TANH2) o = tanhf(tanhf(o));
                 a.out[((size_t)n * a.Ho + row) * a.Wo + col] = o;
             }
-            epi_bar<R::kEpiThreads>();
-        } else if (kGN) {
-            // pool: combine the two row slots (S == 2) through shared memory
-            float *xg = scratch;                                  // [8 warps][32 lanes][kMaxWin][2]
-            float *st = scratch + R::kEpiWarps * 32 * kMaxWin * 2;  // [8 warps][32 lanes][2]
-            st[(ew * 32 + lane) * 2] = ls;
-            st[(ew * 32 + lane) * 2 + 1] = lss;
-#pragma unroll
-            for (int k = 0; k < kMaxWin; ++k) {
-                xg[((ew * 32 + lane) * kMaxWin + k) * 2] = pmx[k];
-                xg[((ew * 32 + lane) * kMaxWin + k) * 2 + 1] = pmn[k];
-            }
-            epi_bar<R::kEpiThreads>();
-            if (slot == 0 && ru < a.Hp) {
-                const int ew1 = hc * 4 + qd + 2;  // warp holding the same channel in row slot 1
+            epi_bar();
+        } else if constexpr (kGN) {
+            // pooled tile [2][64 channels][kPoolPitch]: slot 1 writes, slot 0 folds in, all store
+            float *pmaxs = scratch, *pmins = scratch + 64 * kPoolPitch;
+            float *st = scratch + 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
+            st[ew * 32 + lane] = ls;
+            st[kEpiThreads + ew * 32 + lane] = lss;
+            const int cl = (qd & 1) * 32 + lane;  // channel within the tile (Cout = 64)
+            if (slot == 1) {
 #pragma unroll
                 for (int k = 0; k < kMaxWin; ++k) {
-                    const int cc = hc + NH * (k / 4);
-                    const int pw = cc * 4 + (k % 4);
-                    if (cc >= nchunks || pw >= a.Wp) continue;
-                    float mx = pmx[k], mn = pmn[k];
-                    if (a.S == 2) {
-                        mx = fmaxf(mx, xg[((ew1 * 32 + lane) * kMaxWin + k) * 2]);
-                        mn = fminf(mn, xg[((ew1 * 32 + lane) * kMaxWin + k) * 2 + 1]);
-                    }
-                    const size_t o = (((size_t)n * a.Cout + co) * a.Hp + ru) * a.Wp + pw;
-                    a.gn.pmax[o] = mx;
-                    a.gn.pmin[o] = mn;
+                    const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
+                    if (pw < 32) pmaxs[cl * kPoolPitch + pw] = pmx[k], pmins[cl * kPoolPitch + pw] = pmn[k];
                 }
             }
-            // statistics: fixed-order sum per group
+            epi_bar();
+            if (slot == 0) {
+#pragma unroll
+                for (int k = 0; k < kMaxWin; ++k) {
+                    const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
+                    if (pw < 32) {
+                        pmaxs[cl * kPoolPitch + pw] = fmaxf(pmaxs[cl * kPoolPitch + pw], pmx[k]);
+                        pmins[cl * kPoolPitch + pw] = fminf(pmins[cl * kPoolPitch + pw], pmn[k]);
+                    }
+                }
+            }
+            epi_bar();
+            if (ru < a.Hp) {
+                for (int idx = et; idx < 64 * a.Wp; idx += kEpiThreads) {
+                    const int c2 = idx / a.Wp, pw = idx % a.Wp;
+                    const size_t o = (((size_t)n * a.Cout + c2) * a.Hp + ru) * a.Wp + pw;
+                    a.gn.pmax[o] = pmaxs[c2 * kPoolPitch + pw];
+                    a.gn.pmin[o] = pmins[c2 * kPoolPitch + pw];
+                }
+            }
+            // statistics: fixed-order sum per group over its channels, both row
+            // slots and both column groups
             const int cpg = a.Cout / a.groups;
-            for (int g = et; g < a.groups; g += R::kEpiThreads) {
+            for (int g = et; g < a.groups; g += kEpiThreads) {
                 double s0 = 0.0, s1 = 0.0;
                 for (int s = 0; s < a.S; ++s)
                     for (int h2 = 0; h2 < 2; ++h2)
                         for (int c2 = g * cpg; c2 < (g + 1) * cpg; ++c2) {
                             const int LL = s * a.Cout + c2;
                             const int e2 = h2 * 4 + (LL >> 5);
-                            s0 += st[(e2 * 32 + (LL & 31)) * 2];
-                            s1 += st[(e2 * 32 + (LL & 31)) * 2 + 1];
+                            s0 += st[e2 * 32 + (LL & 31)];
+                            s1 += st[kEpiThreads + e2 * 32 + (LL & 31)];
                         }
                 double *dst = a.gn.part + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2;
                 dst[0] = s0;
                 dst[1] = s1;
             }
-            epi_bar<R::kEpiThreads>();
+            epi_bar();
         }
     }
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant__ TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
     Bars bars;
-    bars.base = sbase + a.stage0_off + a.stages * a.stage_bytes;
-    bars.stages = a.stages;
-    uint32_t *tmem_slot =
-        reinterpret_cast<uint32_t *>(smem + a.stage0_off + a.stages * a.stage_bytes + 8 * Bars::count(a.stages));
+    bars.base = sbase + a.bar_off;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + a.bar_off + 8 * Bars::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *scratch = reinterpret_cast<float *>(smem + a.scratch_off);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(bars.full_w(s), 1);
-            mbar_init(bars.full_x(s), Roles<KIND>::kConvThreads);
-            mbar_init(bars.empty(s), 1);
+        for (int s = 0; s < kMaxRing; ++s) {
+            mbar_init(bars.a_full(s), 1);
+            mbar_init(bars.a_empty(s), 1);
+            mbar_init(bars.b_full(s), kConvThreads);
+            mbar_init(bars.b_empty(s), 1);
+            mbar_init(bars.r_full(s), 1);
+            mbar_init(bars.r_empty(s), kConvThreads);
         }
         for (int ab = 0; ab < 2; ++ab) {
             mbar_init(bars.acc_full(ab), 1);
-            mbar_init(bars.acc_empty(ab), Roles<KIND>::kEpiWarps);
+            mbar_init(bars.acc_empty(ab), kEpiWarps);
         }
         mbar_init(bars.final_bar(), 1);
         mbar_init(bars.wres(), 1);
@@ -666,9 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const TcArgs a) {
     } else if (warp == 1) {
         if (lane == 0) weight_role(a, sbase, bars, abort_flag);
         __syncwarp();
-    } else if (warp < Roles<KIND>::kEpiWarp0) {
-        converter_role<Roles<KIND>::kConvThreads, Roles<KIND>::kNBMax>(
-            a, smem, bars, abort_flag, threadIdx.x - Roles<KIND>::kConvWarp0 * 32);
+    } else if (warp == 2) {
+        if (lane == 0) tile_role(a, sbase, bars, abort_flag);
+        __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        converter_role(a, smem, bars, abort_flag);
     } else {
         epilogue_role<KIND>(a, scratch, bars, tmem, abort_flag);
     }
@@ -710,8 +771,9 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
 // ----------------------------------------------------------- planning ----
 struct Plan {
     int S, P, U, RU, Rin, PL, chunks, ucol;
-    uint32_t a_bytes, b_bytes, stage_bytes, scratch_bytes, scratch_off, stage0_off, b_off;
-    int stages, resident;
+    int resident, na, nb, nr;
+    uint32_t a_bytes, b_bytes, raw_bytes, scratch_bytes;
+    uint32_t a_off, b_off, raw_off, bar_off, scratch_off;
     size_t smem;
 };
 
@@ -721,27 +783,17 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_SCALE_MIN:
         return (uint32_t)(U * 4 * P * sizeof(float));
     case CONV_EPI_MUL_LRELU_GELU:
-        return (uint32_t)(Roles<CONV_EPI_MUL_LRELU_GELU>::kEpiWarps * 32 * kStgPitch * sizeof(float));
-    case CONV_EPI_GN_SCALE_POOL_CLAMP: {
-        constexpr int ew = Roles<CONV_EPI_GN_SCALE_POOL_CLAMP>::kEpiWarps;
-        return (uint32_t)((ew * 32 * 16 * 2 + ew * 32 * 2) * sizeof(float));
-    }
+        return (uint32_t)(kEpiWarps * 32 * kStgPitch * sizeof(float));
+    case CONV_EPI_GN_SCALE_POOL_CLAMP:
+        return (uint32_t)((2 * 64 * kPoolPitch + 2 * kEpiThreads) * sizeof(float));
     }
     return 0;
 }
 
-int conv_threads_for(int kind) {
-    switch (kind) {
-    case CONV_EPI_MIN_TANH2: return Roles<CONV_EPI_MIN_TANH2>::kConvThreads * Roles<CONV_EPI_MIN_TANH2>::kNBMax;
-    case CONV_EPI_SCALE_MIN: return Roles<CONV_EPI_SCALE_MIN>::kConvThreads * Roles<CONV_EPI_SCALE_MIN>::kNBMax;
-    case CONV_EPI_MUL_LRELU_GELU:
-        return Roles<CONV_EPI_MUL_LRELU_GELU>::kConvThreads * Roles<CONV_EPI_MUL_LRELU_GELU>::kNBMax;
-    default:
-        return Roles<CONV_EPI_GN_SCALE_POOL_CLAMP>::kConvThreads * Roles<CONV_EPI_GN_SCALE_POOL_CLAMP>::kNBMax;
-    }
-}
+uint32_t up1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 
-// Shared memory: [resident filter][stages x (A? + B)][mbarriers][tmem slot, abort][scratch]
+// Shared memory: [filter: resident or ring][B ring][staged-tile ring][mbarriers,
+// tmem slot, abort flag][epilogue scratch]
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (!(d.Cout == 64 || d.Cout == 128)) return false;
     if (d.Cin % 8 != 0 || d.W % 4 != 0 || d.W > 256 || d.H < 3) return false;
@@ -751,39 +803,39 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.U = kAccStride / pl.ucol;
     pl.RU = pl.U * pl.S;
     pl.Rin = pl.RU + 2;
+    if (pl.Rin > 256) return false;  // TMA box height
     pl.PL = (pl.Rin * pl.P + 4 + 7) / 8 * 8;
     pl.chunks = d.Cin / 8;
     if (pl.PL >= (1 << 16)) return false;
-    // every 4x4 block of a chunk's B plane has a converter slot
-    if (pl.PL / 2 > conv_threads_for(kind)) return false;
-    pl.a_bytes = 3u * 2u * (2 * pl.S + 1) * d.Cout * 16u;
-    pl.b_bytes = 2u * pl.PL * 16u;
+    pl.a_bytes = up1k(3u * 2u * (2 * pl.S + 1) * d.Cout * 16u);
+    pl.b_bytes = up1k(2u * pl.PL * 16u);
+    pl.raw_bytes = up1k(8u * pl.Rin * d.W * 4u);
     pl.scratch_bytes = scratch_bytes_for(kind, pl.U, pl.P);
-    auto fits = [&](int st, uint32_t stage, uint32_t res) {
-        const size_t bars_end = (size_t)res + (size_t)st * stage + 8u * Bars::count(st) + 8u;
-        return ((bars_end + 15) & ~(size_t)15) + pl.scratch_bytes <= (size_t)kSmemLimit;
+    const uint32_t tail = 8u * Bars::kCount + 16u + pl.scratch_bytes;
+    auto total = [&](int na, int nb, int nr) {
+        return (size_t)na * pl.a_bytes + (size_t)nb * pl.b_bytes + (size_t)nr * pl.raw_bytes + tail;
     };
-    // keep the whole filter resident when it leaves room for at least 3 stages of B
-    const uint32_t res_bytes = (pl.chunks * pl.a_bytes + 1023u) & ~1023u;
-    const uint32_t b_stage = (pl.b_bytes + 1023u) & ~1023u;
-    if (fits(3, b_stage, res_bytes)) {
-        pl.resident = 1;
-        pl.stage_bytes = b_stage;
-        pl.stage0_off = res_bytes;
-        pl.b_off = 0;
-    } else {
-        pl.resident = 0;
-        pl.stage_bytes = (pl.a_bytes + pl.b_bytes + 1023u) & ~1023u;
-        pl.stage0_off = 0;
-        pl.b_off = pl.a_bytes;
+    // resident filter when it still leaves 2 B planes and 2 staged tiles
+    pl.resident = total(pl.chunks, 2, 2) <= (size_t)kSmemLimit;
+    const int na_min = pl.resident ? pl.chunks : 2;
+    pl.na = na_min, pl.nb = 2, pl.nr = 2;
+    if (total(pl.na, pl.nb, pl.nr) > (size_t)kSmemLimit) return false;
+    // grow the rings while they fit: staged tiles first (they hide DRAM
+    // latency), then B planes, then filter stages
+    for (bool grew = true; grew;) {
+        grew = false;
+        if (pl.nr < kMaxRing && total(pl.na, pl.nb, pl.nr + 1) <= (size_t)kSmemLimit) ++pl.nr, grew = true;
+        if (pl.nb < 3 && total(pl.na, pl.nb + 1, pl.nr) <= (size_t)kSmemLimit) ++pl.nb, grew = true;
+        if (!pl.resident && pl.na < 3 && total(pl.na + 1, pl.nb, pl.nr) <= (size_t)kSmemLimit) ++pl.na, grew = true;
     }
-    int st = kMaxStages;
-    while (st >= 2 && !fits(st, pl.stage_bytes, pl.stage0_off)) --st;
-    if (st < 2) return false;
-    pl.stages = st;
-    pl.scratch_off = (pl.stage0_off + (uint32_t)st * pl.stage_bytes + 8u * Bars::count(st) + 8u + 15u) & ~15u;
+    pl.a_off = 0;
+    pl.b_off = pl.na * pl.a_bytes;
+    pl.raw_off = pl.b_off + pl.nb * pl.b_bytes;
+    pl.bar_off = pl.raw_off + pl.nr * pl.raw_bytes;
+    pl.scratch_off = (pl.bar_off + 8u * Bars::kCount + 8u + 15u) & ~15u;
     pl.smem = pl.scratch_off + pl.scratch_bytes;
-    return true;
+    if (pl.resident) pl.na = 1;  // no filter ring: the resident block is read per chunk
+    return pl.smem <= (size_t)kSmemLimit;
 }
 
 uint32_t make_idesc(int M, int N) {
@@ -791,6 +843,23 @@ uint32_t make_idesc(int M, int N) {
     // B tf32 (bits 10-12 = 2), both K-major (bits 15, 16 = 0), N>>3 at bits 17-22,
     // M>>4 at bits 24-28; dense, no negation, no saturation.
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
 }
 
 template <int KIND>
@@ -809,16 +878,17 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
     const int kind = e ? e->kind : CONV_EPI_MIN_TANH2;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     if (e && e->kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
-        // the epilogue pools 4x4 windows over one band of 4 rows per unit,
-        // with at most 4 sixteen-column chunks per epilogue warp
-        if (e->pool_k != 4 || pl.RU != 4 || pl.P > 128 || pl.S != 2) return CONV_EPI_ERR_UNSUPPORTED;
+        // the epilogue pools 4x4 windows over one band of 4 rows per unit
+        // (two 64-channel row slots), at most 4 sixteen-column chunks per warp
+        if (e->pool_k != 4 || pl.RU != 4 || pl.P > 128 || pl.S != 2 || d.Cout != 64) return CONV_EPI_ERR_UNSUPPORTED;
     }
     return CONV_EPI_OK;
 }
 
 size_t tc_wpack_bytes(const conv_epi_desc &d) {
     const int S = d.Cout >= 128 ? 1 : 2;
-    return (size_t)d.Cin * 3 * (2 * S + 1) * d.Cout * sizeof(float) + 256;
+    const size_t chunk = ((size_t)3 * 2 * (2 * S + 1) * d.Cout * 16 + 1023) & ~(size_t)1023;
+    return (size_t)(d.Cin / 8 + 1) * chunk + 256;
 }
 
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
@@ -832,35 +902,53 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     const conv_epi_desc &d = h->d;
     Plan pl;
     if (!make_plan(d, e.kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
-    // 1) pack the filter for this call
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return CONV_EPI_ERR_CUDA;
+    TcArgs a;
+    memset(&a, 0, sizeof a);
     {
-        const size_t total = (size_t)d.Cin * 3 * (2 * pl.S + 1) * d.Cout;
+        const cuuint64_t dims[4] = {(cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.Cin, (cuuint64_t)d.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)d.W * 4, (cuuint64_t)d.W * d.H * 4,
+                                       (cuuint64_t)d.W * d.H * d.Cin * 4};
+        const cuuint32_t box[4] = {(cuuint32_t)d.W, (cuuint32_t)pl.Rin, 8u, 1u};
+        const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+        const CUresult r = enc(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims, strides, box,
+                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return CONV_EPI_ERR_UNSUPPORTED;
+    }
+    // 1) pack the filter for this call: chunk c at byte offset c * a_bytes
+    {
+        const size_t per_chunk = (size_t)3 * 2 * (2 * pl.S + 1) * d.Cout * 4;  // floats
+        const size_t total = (size_t)pl.chunks * per_chunk;
         const int threads = 256;
         const int blocks = (int)((total + threads - 1) / threads);
+        if (pl.a_bytes != per_chunk * 4) return CONV_EPI_ERR_UNSUPPORTED;  // chunks must pack back to back
         pack_weights<<<blocks, threads, 0, s>>>(w, h->wpack, d.Cin, d.Cout, pl.S);
         CE_CUDA(cudaGetLastError());
     }
-    TcArgs a{};
     a.x = x, a.b = b, a.wpack = h->wpack, a.out = out, a.err = h->dev_err;
     a.N = d.N, a.Cin = d.Cin, a.H = d.H, a.W = d.W, a.Cout = d.Cout, a.Ho = h->Ho, a.Wo = h->Wo;
-    a.S = pl.S, a.P = pl.P, a.U = pl.U, a.RU = pl.RU, a.PL = pl.PL, a.ucol = pl.ucol;
+    a.S = pl.S, a.P = pl.P, a.U = pl.U, a.RU = pl.RU, a.Rin = pl.Rin, a.PL = pl.PL, a.ucol = pl.ucol;
     a.p_magic = (uint32_t)((((uint64_t)1 << 32) + pl.P - 1) / pl.P);
     a.chunks = pl.chunks;
     a.units_per_img = (h->Ho + pl.RU - 1) / pl.RU;
     a.total_units = d.N * a.units_per_img;
-    a.stages = pl.stages;
-    a.a_bytes = pl.a_bytes, a.b_bytes = pl.b_bytes, a.stage_bytes = pl.stage_bytes, a.scratch_off = pl.scratch_off;
-    a.resident = pl.resident, a.stage0_off = pl.stage0_off, a.b_off = pl.b_off;
+    a.resident = pl.resident, a.na = pl.na, a.nb = pl.nb, a.nr = pl.nr;
+    a.a_bytes = pl.a_bytes, a.b_bytes = pl.b_bytes, a.raw_bytes = pl.raw_bytes;
+    a.raw_tx = 8u * pl.Rin * d.W * 4u;
+    a.a_off = pl.a_off, a.b_off = pl.b_off, a.raw_off = pl.raw_off, a.bar_off = pl.bar_off;
+    a.scratch_off = pl.scratch_off;
     a.a_plane_bytes = (uint32_t)d.Cout * 16u;
     a.a_lbo = (uint32_t)(2 * pl.S + 1) * a.a_plane_bytes;
     a.a_kw_stride = 2u * a.a_lbo;
     a.idesc = make_idesc(128, pl.P);
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.slope = e.lrelu_slope;
-    a.groups = e.groups, a.pool_k = e.pool_k;
+    a.groups = e.groups;
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
-        if (h->gn.units != a.units_per_img) return CONV_EPI_ERR_INVALID_ARG;
+        if (h->gn.units != a.units_per_img || a.Wp > 32) return CONV_EPI_ERR_INVALID_ARG;
     }
     const int grid = a.total_units < h->sm_count ? a.total_units : h->sm_count;
     conv_epi_status st;
