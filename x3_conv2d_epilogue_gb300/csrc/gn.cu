@@ -21,7 +21,7 @@
 namespace conv_epi {
 namespace {
 
-constexpr int kChan = 16;  // channels per CTA
+constexpr int kThreads = 256;
 
 struct GnArgs {
     GnWork gn;
@@ -32,13 +32,22 @@ struct GnArgs {
     int32_t *idx;
 };
 
-__global__ void __launch_bounds__(256) gn_finalize_kernel(const GnArgs a) {
-    __shared__ float sA[kChan], sB[kChan];
-    const int n = blockIdx.x;
-    const int c0 = blockIdx.y * kChan;
-    const int nc = min(kChan, a.C - c0);
-    if (threadIdx.x < nc) {
-        const int c = c0 + threadIdx.x;
+// One thread per pooled output.  A CTA covers kThreads consecutive outputs
+// of the [N][C][Hp][Wp] tensor, i.e. at most a few (n, c) planes; its first
+// threads fold the partial sums of those planes' groups (fixed order, fp64)
+// into the per-channel affine coefficients.
+__global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
+    constexpr int kMaxPlanes = kThreads + 1;  // (n, c) planes one CTA can touch
+    __shared__ float sA[kMaxPlanes], sB[kMaxPlanes];
+    const int per = a.gn.Hp * a.gn.Wp;
+    const size_t total = (size_t)a.N * a.C * per;
+    const size_t first = (size_t)blockIdx.x * kThreads;
+    const size_t plane0 = first / per;
+    const size_t last = min(total, first + kThreads) - 1;
+    const int nplanes = (int)(last / per - plane0 + 1);
+    for (int k = threadIdx.x; k < nplanes; k += kThreads) {
+        const size_t pl = plane0 + k;
+        const int n = (int)(pl / a.C), c = (int)(pl % a.C);
         const int cpg = a.C / a.groups;
         const int g = c / cpg;
         double s = 0.0, ss = 0.0;
@@ -50,20 +59,17 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const GnArgs a) {
         if (var < 0.0) var = 0.0;
         const double rstd = 1.0 / sqrt(var + (double)a.eps);
         const double gm = a.gamma[c], sc = a.scale[c];
-        sA[threadIdx.x] = (float)(gm * sc * rstd);
-        sB[threadIdx.x] = (float)((a.beta[c] - gm * mean * rstd) * sc);
+        sA[k] = (float)(gm * sc * rstd);
+        sB[k] = (float)((a.beta[c] - gm * mean * rstd) * sc);
     }
     __syncthreads();
-    const int per = a.gn.Hp * a.gn.Wp;
-    for (int i = threadIdx.x; i < nc * per; i += blockDim.x) {
-        const int cl = i / per;
-        const size_t o = ((size_t)n * a.C + c0 + cl) * per + (i % per);
-        const float A = sA[cl];
-        const float y = A >= 0.0f ? a.gn.pmax[o] : a.gn.pmin[o];
-        const float z = fmaf(A, y, sB[cl]);
-        a.out[o] = fminf(fmaxf(z, a.lo), a.hi);
-        if (a.idx) a.idx[o] = A > 0.0f ? a.gn.amax[o] : (A < 0.0f ? a.gn.amin[o] : 0);
-    }
+    const size_t o = first + threadIdx.x;
+    if (o >= total) return;
+    const int k = (int)(o / per - plane0);
+    const float A = sA[k];
+    const float y = A >= 0.0f ? a.gn.pmax[o] : a.gn.pmin[o];
+    a.out[o] = fminf(fmaxf(fmaf(A, y, sB[k]), a.lo), a.hi);
+    if (a.idx) a.idx[o] = A > 0.0f ? a.gn.amax[o] : (A < 0.0f ? a.gn.amin[o] : 0);
 }
 
 }  // namespace
@@ -75,8 +81,10 @@ conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, 
     a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
     a.gamma = e.gamma, a.beta = e.beta, a.scale = e.chan_scale;
     a.out = out, a.idx = e.index_out;
-    dim3 grid(h->d.N, (h->d.Cout + kChan - 1) / kChan);
-    gn_finalize_kernel<<<grid, 256, 0, s>>>(a);
+    const size_t per = (size_t)h->gn.Hp * h->gn.Wp;
+    const size_t total = (size_t)a.N * a.C * per;
+    const unsigned blocks = (unsigned)((total + kThreads - 1) / kThreads);
+    gn_finalize_kernel<<<blocks, kThreads, 0, s>>>(a);
     CE_CUDA(cudaGetLastError());
     return CONV_EPI_OK;
 }

@@ -35,9 +35,10 @@
 //
 // One CTA per SM (persistent), 16 warps:
 //   warp 0      tensor-memory allocator + single-thread MMA issuer
-//   warp 1      filter producer (bulk copies, or one resident load)
-//   warp 2      input-tile producer (TMA tensor loads into the staging ring)
-//   warps 3-7   converters (staged tile -> B plane)
+//   warp 1      producer: TMA tensor loads of input tiles into the staging
+//               ring and bulk copies of the filter (streamed per chunk, or
+//               loaded once when it stays resident)
+//   warps 2-7   converters (staged tile -> B plane)
 //   warps 8-15  epilogue (tensor memory -> chain -> global), two warps per
 //               32-lane quadrant, alternating column chunks
 // Rings (mbarrier full/empty pairs): filter stages, B planes, staged tiles;
@@ -56,7 +57,7 @@ namespace conv_epi {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 3, kConvWarps = 5, kConvThreads = kConvWarps * 32;
+constexpr int kConvWarp0 = 2, kConvWarps = 6, kConvThreads = kConvWarps * 32;
 constexpr int kEpiWarp0 = 8, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;     // columns per accumulator buffer
@@ -311,86 +312,74 @@ __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint
     wait_bar(bars.final_bar(), 0, abort_flag, a.err, false);
 }
 
-__device__ void weight_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
+// Producer (one thread): per chunk (unit, c), in order, the raw input tile
+// x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] into staging slot it % nr (laid
+// out [8][Rin][W]; rows >= H arrive as zeros) and, when the filter streams,
+// chunk c of the packed filter into filter slot it % na.
+__device__ void producer_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
+    prefetch_tensormap(&a.xmap);
     if (a.resident) {
-        // the whole packed filter, once
         const uint32_t total = a.chunks * a.a_bytes;
         mbar_arrive_expect_tx(bars.wres(), total);
         for (uint32_t off = 0; off < total; off += 16384u)
             bulk_g2s(sbase + a.a_off + off, wsrc + off, min(16384u, total - off), bars.wres());
-        wait_bar(bars.wres(), 0, abort_flag, a.err, false);
-        return;
     }
     int it = 0;
-    int last_par[kMaxRing];
-    bool issued[kMaxRing];
-    for (int s = 0; s < kMaxRing; ++s) issued[s] = false, last_par[s] = 0;
-    bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
-        for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int s = it % a.na;
-            const uint32_t ph = (it / a.na) & 1;
-            if (!wait_bar(bars.a_empty(s), ph ^ 1, abort_flag, a.err)) {
-                ok = false;
-                break;
-            }
-            const uint32_t dst = sbase + a.a_off + s * a.a_bytes;
-            const char *src = wsrc + (size_t)c * a.a_bytes;
-            mbar_arrive_expect_tx(bars.a_full(s), a.a_bytes);
-            for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
-                bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(s));
-            issued[s] = true, last_par[s] = ph;
-        }
-    }
-    // copies still in flight land before the CTA exits
-    for (int s = 0; s < a.na; ++s)
-        if (issued[s]) wait_bar(bars.a_full(s), last_par[s], abort_flag, a.err, false);
-}
-
-// TMA producer: raw tile of chunk (unit, c) = x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1]
-// into staging slot it % nr, laid out [8][Rin][W]; rows >= H arrive as zeros.
-__device__ void tile_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
-    prefetch_tensormap(&a.xmap);
-    int it = 0;
-    int last_par[kMaxRing];
-    bool issued[kMaxRing];
-    for (int s = 0; s < kMaxRing; ++s) issued[s] = false, last_par[s] = 0;
+    int r_par[kMaxRing], a_par[kMaxRing];
+    bool r_iss[kMaxRing], a_iss[kMaxRing];
+    for (int s = 0; s < kMaxRing; ++s) r_iss[s] = a_iss[s] = false, r_par[s] = a_par[s] = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
         const int n = unit / a.units_per_img;
         const int r0 = (unit % a.units_per_img) * a.RU;
         for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int s = it % a.nr;
-            const uint32_t ph = (it / a.nr) & 1;
-            if (!wait_bar(bars.r_empty(s), ph ^ 1, abort_flag, a.err)) {
+            const int sr = it % a.nr;
+            const uint32_t pr = (it / a.nr) & 1;
+            if (!wait_bar(bars.r_empty(sr), pr ^ 1, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(bars.r_full(s), a.raw_tx);
-            tma_load_4d(sbase + a.raw_off + s * a.raw_bytes, &a.xmap, 0, r0, 8 * c, n, bars.r_full(s));
-            issued[s] = true, last_par[s] = ph;
+            mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
+            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, &a.xmap, 0, r0, 8 * c, n, bars.r_full(sr));
+            r_iss[sr] = true, r_par[sr] = pr;
+            if (!a.resident) {
+                const int sa = it % a.na;
+                const uint32_t pa = (it / a.na) & 1;
+                if (!wait_bar(bars.a_empty(sa), pa ^ 1, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = sbase + a.a_off + sa * a.a_bytes;
+                const char *src = wsrc + (size_t)c * a.a_bytes;
+                mbar_arrive_expect_tx(bars.a_full(sa), a.a_bytes);
+                for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
+                    bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(sa));
+                a_iss[sa] = true, a_par[sa] = pa;
+            }
         }
     }
+    // copies still in flight land before the CTA exits
+    if (a.resident) wait_bar(bars.wres(), 0, abort_flag, a.err, false);
     for (int s = 0; s < a.nr; ++s)
-        if (issued[s]) wait_bar(bars.r_full(s), last_par[s], abort_flag, a.err, false);
+        if (r_iss[s]) wait_bar(bars.r_full(s), r_par[s], abort_flag, a.err, false);
+    for (int s = 0; s < a.na; ++s)
+        if (a_iss[s]) wait_bar(bars.a_full(s), a_par[s], abort_flag, a.err, false);
 }
 
-// Converter warps: staged tile [8][Rin][W] -> B plane [ci4][q][4].  Work item =
-// one 4x4 block: 4 consecutive positions (one 16-byte shared load per
-// channel) x 4 channels, transposed in registers into 4 position rows of
-// 16 bytes, rounded to tf32.  The rows are stored in a per-thread rotated
-// order so that the 8 threads of a store phase hit 8 different bank groups.
-// Positions past the staged rows, or with w >= W, are zero.
-__device__ __forceinline__ float pick(const float4 &v, int p) {
-    return p == 0 ? v.x : (p == 1 ? v.y : (p == 2 ? v.z : v.w));
-}
-
+// Converter warps: staged tile [8][Rin][W] -> B plane [ci4][q][4].  A warp
+// takes 32 consecutive positions of one (ci4 group, input row): each lane
+// reads its position from the 4 channel rows (consecutive lanes, consecutive
+// words: no bank conflict), rounds to tf32 and writes one 16-byte plane row
+// (consecutive lanes, consecutive rows: no bank conflict).  Positions with
+// w >= W are zero; plane rows past the staged rows are never written (they
+// only feed output columns >= Wo, which are discarded).
 __device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
-    const int t = threadIdx.x - kConvWarp0 * 32;
-    const int qpp = a.PL >> 2;  // 4-position groups per ci4 plane
-    const int nblk = 2 * qpp;
-    const int plane_stride = a.Rin * a.W;  // floats between channels of a staged tile
+    const int cw = (threadIdx.x >> 5) - kConvWarp0;
+    const int lane = threadIdx.x & 31;
+    const int ps = a.Rin * a.W;          // floats between channels of a staged tile
+    const int mP = (a.P + 31) >> 5;      // 32-position groups per input row
+    const int nrc = 2 * a.Rin * mP;      // (ci4 group, row, group) work items per chunk
     int it = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
@@ -403,31 +392,26 @@ __device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars,
             }
             const float *raw = reinterpret_cast<const float *>(smem + a.raw_off + sr * a.raw_bytes);
             uint4 *plane = reinterpret_cast<uint4 *>(smem + a.b_off + sb * a.b_bytes);
-            for (int blk = t; blk < nblk; blk += kConvThreads) {
-                const int jg = blk >= qpp ? 1 : 0;
-                const int q = 4 * (blk - jg * qpp);
-                const int rr = __umulhi((uint32_t)q, a.p_magic);
-                const int w = q - rr * a.P;
-                float4 v[4];
-                if (rr < a.Rin && w < a.W) {
-                    const float *src = raw + (4 * jg) * plane_stride + rr * a.W + w;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) v[e] = *reinterpret_cast<const float4 *>(src + e * plane_stride);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) v[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            int m = cw % mP, t2 = cw / mP;
+            int rr = t2 % a.Rin, jg = t2 / a.Rin;
+#pragma unroll 2
+            for (int rc = cw; rc < nrc; rc += kConvWarps) {
+                const int w = m * 32 + lane;
+                if (w < a.P) {
+                    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                    if (w < a.W) {
+                        const float *src = raw + 4 * jg * ps + rr * a.W + w;
+                        o.x = f32_to_tf32(src[0]);
+                        o.y = f32_to_tf32(src[ps]);
+                        o.z = f32_to_tf32(src[2 * ps]);
+                        o.w = f32_to_tf32(src[3 * ps]);
+                    }
+                    plane[jg * a.PL + rr * a.P + w] = o;
                 }
-                const int row = jg * a.PL + q;
-                const int rot = (row >> 3) & 3;  // (position group / 2) mod 4
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int p = (i + rot) & 3;
-                    uint4 o;
-                    o.x = f32_to_tf32(pick(v[0], p));
-                    o.y = f32_to_tf32(pick(v[1], p));
-                    o.z = f32_to_tf32(pick(v[2], p));
-                    o.w = f32_to_tf32(pick(v[3], p));
-                    plane[row + p] = o;
+                m += kConvWarps;
+                while (m >= mP) {
+                    m -= mP;
+                    if (++rr == a.Rin) rr = 0, ++jg;
                 }
             }
             mbar_arrive(bars.r_empty(sr));  // staged tile read
@@ -723,10 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         if (lane == 0) mma_role(a, sbase, bars, tmem, abort_flag);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) weight_role(a, sbase, bars, abort_flag);
-        __syncwarp();
-    } else if (warp == 2) {
-        if (lane == 0) tile_role(a, sbase, bars, abort_flag);
+        if (lane == 0) producer_role(a, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         converter_role(a, smem, bars, abort_flag);
