@@ -33,9 +33,9 @@ struct GnArgs {
 };
 
 // One thread per pooled output.  A CTA covers kThreads consecutive outputs
-// of the [N][C][Hp][Wp] tensor, i.e. at most a few (n, c) planes; its first
-// threads fold the partial sums of those planes' groups (fixed order, fp64)
-// into the per-channel affine coefficients.
+// of the [N][C][Hp][Wp] tensor, i.e. at most a few (n, c) planes; one warp
+// per plane folds the partial sums of that plane's group (fixed order, fp64)
+// into the channel's affine coefficients.
 __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
     constexpr int kMaxPlanes = kThreads + 1;  // (n, c) planes one CTA can touch
     __shared__ float sA[kMaxPlanes], sB[kMaxPlanes];
@@ -45,22 +45,32 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
     const size_t plane0 = first / per;
     const size_t last = min(total, first + kThreads) - 1;
     const int nplanes = (int)(last / per - plane0 + 1);
-    for (int k = threadIdx.x; k < nplanes; k += kThreads) {
+    // one warp per plane: lanes load the per-unit partial sums in parallel and
+    // fold them in a fixed order (strided lane sums, then a fixed shuffle tree)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int k = warp; k < nplanes; k += kThreads / 32) {
         const size_t pl = plane0 + k;
         const int n = (int)(pl / a.C), c = (int)(pl % a.C);
         const int cpg = a.C / a.groups;
         const int g = c / cpg;
         double s = 0.0, ss = 0.0;
         const double *p = a.gn.part + ((size_t)n * a.gn.units * a.groups + g) * 2;
-        for (int u = 0; u < a.gn.units; ++u, p += 2 * a.groups) s += p[0], ss += p[1];
-        const double cnt = (double)cpg * a.Ho * a.Wo;
-        const double mean = s / cnt;
-        double var = ss / cnt - mean * mean;
-        if (var < 0.0) var = 0.0;
-        const double rstd = 1.0 / sqrt(var + (double)a.eps);
-        const double gm = a.gamma[c], sc = a.scale[c];
-        sA[k] = (float)(gm * sc * rstd);
-        sB[k] = (float)((a.beta[c] - gm * mean * rstd) * sc);
+        for (int u = lane; u < a.gn.units; u += 32) s += p[(size_t)u * 2 * a.groups], ss += p[(size_t)u * 2 * a.groups + 1];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            s += __shfl_xor_sync(0xffffffffu, s, off);
+            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        }
+        if (lane == 0) {
+            const double cnt = (double)cpg * a.Ho * a.Wo;
+            const double mean = s / cnt;
+            double var = ss / cnt - mean * mean;
+            if (var < 0.0) var = 0.0;
+            const double rstd = 1.0 / sqrt(var + (double)a.eps);
+            const double gm = a.gamma[c], sc = a.scale[c];
+            sA[k] = (float)(gm * sc * rstd);
+            sB[k] = (float)((a.beta[c] - gm * mean * rstd) * sc);
+        }
     }
     __syncthreads();
     const size_t o = first + threadIdx.x;

@@ -66,8 +66,11 @@ constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kStgPitch = 18;       // per-channel epilogue staging pitch (floats, even: float2 rows)
 constexpr int kPoolPitch = 33;      // GroupNorm pooled tile pitch (floats)
 
-struct TcArgs {  // 64-byte aligned through CUtensorMap
-    CUtensorMap xmap;  // x as a 4-D tensor (W, H, Cin, N); box (W, Rin, 8, 1)
+// Scalar kernel configuration.  The kernel copies it out of the parameter
+// space into a local at entry, so the roles keep the fields in registers
+// (reads through the parameter would be repeated after every asm statement
+// that clobbers memory, on the critical path of every loop).
+struct Cfg {
     const float *x, *b, *wpack;
     float *out;
     unsigned *err;
@@ -86,6 +89,11 @@ struct TcArgs {  // 64-byte aligned through CUtensorMap
     float slope;
     int groups, Hp, Wp;
     GnWork gn;
+};
+
+struct TcArgs {        // 64-byte aligned through CUtensorMap
+    CUtensorMap xmap;  // x as a 4-D tensor (W, H, Cin, N); box (W, Rin, 8, 1)
+    Cfg c;
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -267,7 +275,7 @@ struct Bars {
 };
 
 // ------------------------------------------------------------- roles ----
-__device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint32_t tmem, volatile int *abort_flag) {
+__device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bars &bars, uint32_t tmem, volatile int *abort_flag) {
     int it = 0, j = 0;
     bool ok = true;
     if (a.resident) ok = wait_bar(bars.wres(), 0, abort_flag, a.err);
@@ -316,9 +324,10 @@ __device__ void mma_role(const TcArgs &a, uint32_t sbase, const Bars &bars, uint
 // x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] into staging slot it % nr (laid
 // out [8][Rin][W]; rows >= H arrive as zeros) and, when the filter streams,
 // chunk c of the packed filter into filter slot it % na.
-__device__ void producer_role(const TcArgs &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
+__device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *xmap, uint32_t sbase, const Bars &bars,
+                                              volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
-    prefetch_tensormap(&a.xmap);
+    prefetch_tensormap(xmap);
     if (a.resident) {
         const uint32_t total = a.chunks * a.a_bytes;
         mbar_arrive_expect_tx(bars.wres(), total);
@@ -341,7 +350,7 @@ __device__ void producer_role(const TcArgs &a, uint32_t sbase, const Bars &bars,
                 break;
             }
             mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
-            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, &a.xmap, 0, r0, 8 * c, n, bars.r_full(sr));
+            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, r0, 8 * c, n, bars.r_full(sr));
             r_iss[sr] = true, r_par[sr] = pr;
             if (!a.resident) {
                 const int sa = it % a.na;
@@ -374,7 +383,7 @@ __device__ void producer_role(const TcArgs &a, uint32_t sbase, const Bars &bars,
 // (consecutive lanes, consecutive rows: no bank conflict).  Positions with
 // w >= W are zero; plane rows past the staged rows are never written (they
 // only feed output columns >= Wo, which are discarded).
-__device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
+__device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
     const int cw = (threadIdx.x >> 5) - kConvWarp0;
     const int lane = threadIdx.x & 31;
     const int ps = a.Rin * a.W;          // floats between channels of a staged tile
@@ -414,9 +423,14 @@ __device__ void converter_role(const TcArgs &a, uint8_t *smem, const Bars &bars,
                     if (++rr == a.Rin) rr = 0, ++jg;
                 }
             }
-            mbar_arrive(bars.r_empty(sr));  // staged tile read
-            fence_proxy_async_smem();       // make the generic-proxy stores visible to the tensor core
-            mbar_arrive(bars.b_full(sb));
+            // each thread makes its own generic-proxy stores visible to the
+            // tensor core, then one arrive per warp on each barrier
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bars.r_empty(sr));  // staged tile read
+                mbar_arrive(bars.b_full(sb));
+            }
         }
     }
 }
@@ -452,7 +466,7 @@ __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + e
 
 // Per-chunk work of the min / per-channel chains on 16 accumulator columns.
 template <int KIND>
-__device__ __forceinline__ void epi_chunk(const TcArgs &a, const Frag16 &f, float bias, float mult, int sgn,
+__device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, float bias, float mult, int sgn,
                                           int lane, int qd, int ew, int u, int n, int row, int col0,
                                           float *scratch) {
     float v[16];
@@ -501,7 +515,7 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &a, const Frag16 &f, floa
 }
 
 template <int KIND>
-__device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars, uint32_t tmem,
+__device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, const Bars &bars, uint32_t tmem,
                               volatile int *abort_flag) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ew = warp - kEpiWarp0;  // 0..7
@@ -665,8 +679,9 @@ __device__ void epilogue_role(const TcArgs &a, float *scratch, const Bars &bars,
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant__ TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    const Cfg a = args.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
     Bars bars;
@@ -679,10 +694,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         for (int s = 0; s < kMaxRing; ++s) {
             mbar_init(bars.a_full(s), 1);
             mbar_init(bars.a_empty(s), 1);
-            mbar_init(bars.b_full(s), kConvThreads);
+            mbar_init(bars.b_full(s), kConvWarps);
             mbar_init(bars.b_empty(s), 1);
             mbar_init(bars.r_full(s), 1);
-            mbar_init(bars.r_empty(s), kConvThreads);
+            mbar_init(bars.r_empty(s), kConvWarps);
         }
         for (int ab = 0; ab < 2; ++ab) {
             mbar_init(bars.acc_full(ab), 1);
@@ -707,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         if (lane == 0) mma_role(a, sbase, bars, tmem, abort_flag);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) producer_role(a, sbase, bars, abort_flag);
+        if (lane == 0) producer_role(a, &args.xmap, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         converter_role(a, smem, bars, abort_flag);
@@ -844,10 +859,10 @@ EncodeTiledFn encode_tiled() {
 }
 
 template <int KIND>
-conv_epi_status launch_tc(const TcArgs &a, const Plan &pl, int grid, cudaStream_t s) {
+conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStream_t s) {
     auto k = tc_conv_epi<KIND>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
-    k<<<grid, kThreads, pl.smem, s>>>(a);
+    k<<<grid, kThreads, pl.smem, s>>>(args);
     CE_CUDA(cudaGetLastError());
     return CONV_EPI_OK;
 }
@@ -885,15 +900,16 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (!make_plan(d, e.kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return CONV_EPI_ERR_CUDA;
-    TcArgs a;
-    memset(&a, 0, sizeof a);
+    TcArgs args;
+    memset(&args, 0, sizeof args);
+    Cfg &a = args.c;
     {
         const cuuint64_t dims[4] = {(cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.Cin, (cuuint64_t)d.N};
         const cuuint64_t strides[3] = {(cuuint64_t)d.W * 4, (cuuint64_t)d.W * d.H * 4,
                                        (cuuint64_t)d.W * d.H * d.Cin * 4};
         const cuuint32_t box[4] = {(cuuint32_t)d.W, (cuuint32_t)pl.Rin, 8u, 1u};
         const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-        const CUresult r = enc(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims, strides, box,
+        const CUresult r = enc(&args.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims, strides, box,
                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV_EPI_ERR_UNSUPPORTED;
@@ -934,10 +950,10 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     const int grid = a.total_units < h->sm_count ? a.total_units : h->sm_count;
     conv_epi_status st;
     switch (e.kind) {
-    case CONV_EPI_MIN_TANH2: st = launch_tc<CONV_EPI_MIN_TANH2>(a, pl, grid, s); break;
-    case CONV_EPI_SCALE_MIN: st = launch_tc<CONV_EPI_SCALE_MIN>(a, pl, grid, s); break;
-    case CONV_EPI_MUL_LRELU_GELU: st = launch_tc<CONV_EPI_MUL_LRELU_GELU>(a, pl, grid, s); break;
-    case CONV_EPI_GN_SCALE_POOL_CLAMP: st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(a, pl, grid, s); break;
+    case CONV_EPI_MIN_TANH2: st = launch_tc<CONV_EPI_MIN_TANH2>(args, pl, grid, s); break;
+    case CONV_EPI_SCALE_MIN: st = launch_tc<CONV_EPI_SCALE_MIN>(args, pl, grid, s); break;
+    case CONV_EPI_MUL_LRELU_GELU: st = launch_tc<CONV_EPI_MUL_LRELU_GELU>(args, pl, grid, s); break;
+    case CONV_EPI_GN_SCALE_POOL_CLAMP: st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s); break;
     default: return CONV_EPI_ERR_INVALID_ARG;
     }
     if (st) return st;
