@@ -120,6 +120,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// as above, but a thread whose phase is not complete sleeps until it
+// completes or `ns` nanoseconds pass, instead of returning at once: waiting
+// warps then issue nothing (a polling loop of plain try_waits competes with
+// the converters' shared-memory traffic in the same pipe)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -142,6 +157,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// explicit shared-space accesses on 32-bit shared addresses (volatile: they
+// stay in program order with the barrier waits around them)
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ uint32_t f32_to_tf32(float f) {
@@ -241,14 +267,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // bounded wait: true when the phase completed, false on timeout or (when
-// honor_abort) once another role has given up
+// honor_abort) once another role has given up.  Sleeps in the try_wait
+// between checks of the abort flag and of the time limit.
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err,
                          bool honor_abort = true) {
-    for (int i = 0; i < 64; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
         if (honor_abort && *abort_flag) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             atomicOr(err, ERRBIT_TIMEOUT);
@@ -376,19 +402,42 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
         if (a_iss[s]) wait_bar(bars.a_full(s), a_par[s], abort_flag, a.err, false);
 }
 
-// Converter warps: staged tile [8][Rin][W] -> B plane [ci4][q][4].  A warp
-// takes 32 consecutive positions of one (ci4 group, input row): each lane
+// Converter warps: staged tile [8][Rin][W] -> B plane [ci4][q][4].  Work
+// item = 32 consecutive positions of one (ci4 group, input row): each lane
 // reads its position from the 4 channel rows (consecutive lanes, consecutive
 // words: no bank conflict), rounds to tf32 and writes one 16-byte plane row
 // (consecutive lanes, consecutive rows: no bank conflict).  Positions with
 // w >= W are zero; plane rows past the staged rows are never written (they
 // only feed output columns >= Wo, which are discarded).
-__device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
+// A warp's items are the same in every chunk, so their shared-memory
+// offsets are computed once; per chunk a thread issues all its loads before
+// its first convert/store (kConvItems items in flight, no latency chain).
+constexpr int kConvItems = 12;  // items per converter warp per chunk (2*Rin*ceil(P/32) <= 72, checked on host)
+
+__device__ __forceinline__ void converter_role(const Cfg &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
     const int cw = (threadIdx.x >> 5) - kConvWarp0;
     const int lane = threadIdx.x & 31;
-    const int ps = a.Rin * a.W;          // floats between channels of a staged tile
-    const int mP = (a.P + 31) >> 5;      // 32-position groups per input row
-    const int nrc = 2 * a.Rin * mP;      // (ci4 group, row, group) work items per chunk
+    const int P = a.P, W = a.W, Rin = a.Rin, PL = a.PL;
+    const int ps = Rin * W;             // floats between channels of a staged tile
+    const int mP = (P + 31) >> 5;       // 32-position groups per input row
+    const int nrc = 2 * Rin * mP;       // items per chunk
+    // per item: byte offset into the staged tile (or -1: position past W ->
+    // zero row, -2: no item) and byte offset of the plane row
+    int src_off[kConvItems], dst_off[kConvItems];
+#pragma unroll
+    for (int k = 0; k < kConvItems; ++k) {
+        const int rc = cw + k * kConvWarps;
+        src_off[k] = -2, dst_off[k] = 0;
+        if (rc < nrc) {
+            const int m = rc % mP, t2 = rc / mP;
+            const int rr = t2 % Rin, jg = t2 / Rin;
+            const int w = m * 32 + lane;
+            if (w < P) {
+                src_off[k] = w < W ? 4 * (4 * jg * ps + rr * W + w) : -1;
+                dst_off[k] = 16 * (jg * PL + rr * P + w);
+            }
+        }
+    }
     int it = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
@@ -399,28 +448,27 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, cons
                 ok = false;
                 break;
             }
-            const float *raw = reinterpret_cast<const float *>(smem + a.raw_off + sr * a.raw_bytes);
-            uint4 *plane = reinterpret_cast<uint4 *>(smem + a.b_off + sb * a.b_bytes);
-            int m = cw % mP, t2 = cw / mP;
-            int rr = t2 % a.Rin, jg = t2 / a.Rin;
-#pragma unroll 2
-            for (int rc = cw; rc < nrc; rc += kConvWarps) {
-                const int w = m * 32 + lane;
-                if (w < a.P) {
-                    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-                    if (w < a.W) {
-                        const float *src = raw + 4 * jg * ps + rr * a.W + w;
-                        o.x = f32_to_tf32(src[0]);
-                        o.y = f32_to_tf32(src[ps]);
-                        o.z = f32_to_tf32(src[2 * ps]);
-                        o.w = f32_to_tf32(src[3 * ps]);
-                    }
-                    plane[jg * a.PL + rr * a.P + w] = o;
+            const uint32_t raw = sbase + a.raw_off + sr * a.raw_bytes;
+            const uint32_t plane = sbase + a.b_off + sb * a.b_bytes;
+            float v[kConvItems][4];
+#pragma unroll
+            for (int k = 0; k < kConvItems; ++k) {
+                v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.0f;
+                if (src_off[k] >= 0) {
+                    const uint32_t src = raw + (uint32_t)src_off[k];
+                    v[k][0] = lds_f32(src);
+                    v[k][1] = lds_f32(src + 4u * ps);
+                    v[k][2] = lds_f32(src + 8u * ps);
+                    v[k][3] = lds_f32(src + 12u * ps);
                 }
-                m += kConvWarps;
-                while (m >= mP) {
-                    m -= mP;
-                    if (++rr == a.Rin) rr = 0, ++jg;
+            }
+#pragma unroll
+            for (int k = 0; k < kConvItems; ++k) {
+                if (src_off[k] >= -1) {
+                    uint4 o;
+                    o.x = f32_to_tf32(v[k][0]), o.y = f32_to_tf32(v[k][1]);
+                    o.z = f32_to_tf32(v[k][2]), o.w = f32_to_tf32(v[k][3]);
+                    sts_v4(plane + (uint32_t)dst_off[k], o);
                 }
             }
             // each thread makes its own generic-proxy stores visible to the
@@ -435,31 +483,18 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, cons
     }
 }
 
-// min (or max, sgn < 0) of 16 columns over the warp's 32 lanes, reduce-scatter:
-// on return lanes 2c and 2c+1 hold column c's result in v[0]
 __device__ __forceinline__ float rs_op(float x, float y, int sgn) { return sgn >= 0 ? fminf(x, y) : fmaxf(x, y); }
-__device__ __forceinline__ void reduce_scatter16(float (&v)[16], int lane, int sgn) {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float send = b4 ? v[i] : v[i + 8], keep = b4 ? v[i + 8] : v[i];
-        v[i] = rs_op(keep, __shfl_xor_sync(0xffffffffu, send, 16), sgn);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = b3 ? v[i] : v[i + 4], keep = b3 ? v[i + 4] : v[i];
-        v[i] = rs_op(keep, __shfl_xor_sync(0xffffffffu, send, 8), sgn);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = b2 ? v[i] : v[i + 2], keep = b2 ? v[i + 2] : v[i];
-        v[i] = rs_op(keep, __shfl_xor_sync(0xffffffffu, send, 4), sgn);
-    }
-    {
-        const float send = b1 ? v[0] : v[1], keep = b1 ? v[1] : v[0];
-        v[0] = rs_op(keep, __shfl_xor_sync(0xffffffffu, send, 2), sgn);
-    }
-    v[0] = rs_op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1), sgn);
+
+// warp-wide min / max of one fp32 value per lane, returned to every lane
+__device__ __forceinline__ float warp_min_f32(float v) {
+    float r;
+    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erff(t * 0.70710678118654752f)); }
@@ -473,8 +508,16 @@ __device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, float b
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(f.r[i]) + bias;
     if (KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN) {
-        reduce_scatter16(v, lane, sgn);
-        if ((lane & 1) == 0) scratch[(u * 4 + qd) * a.P + col0 + (lane >> 1)] = v[0];
+        // min (max when the scalar is negative) over this warp's 32 channels,
+        // one warp reduction per column; lane 0 stores the 16 results
+        float r[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = sgn >= 0 ? warp_min_f32(v[i]) : warp_max_f32(v[i]);
+        if (lane == 0) {
+            float4 *dst = reinterpret_cast<float4 *>(scratch + (u * 4 + qd) * a.P + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+        }
     } else {
         // per-channel chain: transpose 32 channels x 16 columns through shared
         // memory so each store instruction writes 4 rows of 64 contiguous bytes
@@ -725,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         if (lane == 0) producer_role(a, &args.xmap, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
-        converter_role(a, smem, bars, abort_flag);
+        converter_role(a, sbase, bars, abort_flag);
     } else {
         epilogue_role<KIND>(a, scratch, bars, tmem, abort_flag);
     }
@@ -803,6 +846,7 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.PL = (pl.Rin * pl.P + 4 + 7) / 8 * 8;
     pl.chunks = d.Cin / 8;
     if (pl.PL >= (1 << 16)) return false;
+    if (2 * pl.Rin * ((pl.P + 31) / 32) > kConvItems * kConvWarps) return false;  // converter items per chunk
     pl.a_bytes = up1k(3u * 2u * (2 * pl.S + 1) * d.Cout * 16u);
     pl.b_bytes = up1k(2u * pl.PL * 16u);
     pl.raw_bytes = up1k(8u * pl.Rin * d.W * 4u);
