@@ -133,6 +133,35 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
                                                    const float *b, const conv_epi_epilogue_desc *epi,
                                                    float *out, void *stream);
 
+/* Forward for callers that cannot allocate device memory (no counterpart on
+ * the pages: it exists for users of this library).  Code that runs inside a
+ * custom allocator or memory-pool callback, code that must not grow the
+ * device's memory footprint after start-up, or a runtime that lends this
+ * library only its input and output buffers cannot call conv_epi_create,
+ * which allocates the scratch the tensor-core kernel needs.  This call takes
+ * the problem description instead of a handle and keeps that scratch (the
+ * packed tf32 filter) in a fixed 1 MiB array inside the library's device
+ * image, which every GPU that loads the library holds until the process
+ * exits.  It allocates and frees nothing.
+ *   desc: as for conv_epi_create; mode must be CONV_EPI_MODE_TF32.
+ *   x, w, b, the chain's parameters, out: device pointers as for
+ *   conv_epi_forward.  Chains MIN_TANH2, SCALE_MIN and MUL_LRELU_GELU only
+ *   (the GroupNorm chain needs a larger workspace); index_out must be NULL.
+ * Returns CONV_EPI_ERR_UNSUPPORTED when the packed filter of the problem does
+ * not fit the array (Cin*3*(2S+1)*Cout floats plus one 8-channel chunk, with
+ * S = 128/Cout) or the shape is outside the tensor-core path.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress) and
+ * clears its error word with a synchronous cudaMemset, so make that first
+ * call before any stream capture.  Every call on a device shares the array
+ * and the array keeps the last call's contents; each call rewrites the part
+ * it reads, so nothing needs to start at zero, but calls whose kernels
+ * overlap on the GPU (unordered streams) race on it.  Asynchronous on
+ * `stream` like conv_epi_forward; a device-side barrier timeout is recorded
+ * in the array's error word and not reported by this call. */
+CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_desc *desc, const float *x, const float *w,
+                                                      const float *b, const conv_epi_epilogue_desc *epi, float *out,
+                                                      void *stream);
+
 /* Wait for `stream` and report any device-side error flag the library's
  * kernels raised on this handle since the last call (then clear it). */
 CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream);

@@ -76,6 +76,7 @@ def _lib():
             L.conv_epi_reserve.argtypes = [P, C.POINTER(EpilogueDesc)]
             L.conv_epi_forward.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_forward_host.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
+            L.conv_epi_forward_noalloc.argtypes = [C.POINTER(Desc), P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_sync.argtypes = [P, P]
             L.conv_epi_destroy.argtypes = [P]
             L.conv_epi_workspace_bytes.argtypes = [P]
@@ -154,6 +155,15 @@ def conv_epi_forward(h, x, w, b, epi, out, stream=None):
 def conv_epi_forward_host(h, x, w, b, epi, out, stream=None):
     _check(_lib().conv_epi_forward_host(h, _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out), _stream(stream)),
            "conv_epi_forward_host")
+    return out
+
+
+def conv_epi_forward_noalloc(N, Cin, H, W, Cout, x, w, b, epi, out, stream=None, mode=MODE_TF32):
+    """Tensor-core forward without a handle: the library allocates nothing and
+    uses its fixed device-side scratch array (see include/conv_epi.h)."""
+    d = Desc(N, Cin, H, W, Cout, mode)
+    _check(_lib().conv_epi_forward_noalloc(C.byref(d), _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out),
+                                           _stream(stream)), "conv_epi_forward_noalloc")
     return out
 
 
