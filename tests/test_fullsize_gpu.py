@@ -1,0 +1,90 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+bench times: the whole batch in one conv_epi_forward, both modes.  The oracle
+checks sampled outputs one by one (min chains: whole channel columns;
+per-channel chain: single elements; GroupNorm chain: every pooled output of
+a few whole (image, group) pairs, statistics included), and properties that
+hold at every output (finite; tanh∘tanh inside (-tanh 1, tanh 1); clamp range).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity_util import (FP32_ATOL, TF32_ATOL, TF32_RTOL, epilogue_for, torch_inputs)
+
+pytestmark = pytest.mark.gpu
+
+NS = 256          # sampled outputs per check
+GN_GROUPS = 3     # (n, g) pairs checked for the GroupNorm chain
+
+
+@pytest.fixture(scope="module", params=["c2_min_tanh2", "c3_mul_lrelu_gelu", "c4_scale_min", "c5_gn_pool_clamp"])
+def full(request):
+    wl = synth.WORKLOADS[request.param]
+    t = synth.make_inputs(wl, seed=0)
+    return wl, t, torch_inputs(t)
+
+
+def run(wl, d, mode):
+    import torch
+    import x3_conv2d_epilogue_gb300 as ce
+    epi = epilogue_for(wl, d)
+    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode)
+    try:
+        out = torch.full(ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, epi, mode), float("nan"),
+                         device="cuda", dtype=torch.float32)
+        ce.conv_epi_forward(h, d["x"], d["w"], d["b"], epi, out)
+        ce.conv_epi_sync(h)
+    finally:
+        ce.conv_epi_destroy(h)
+    return out
+
+
+def close(got, ref, mode):
+    err = np.abs(got.astype(np.float64) - ref)
+    if mode == "fp32":
+        return err <= FP32_ATOL, err
+    return err <= TF32_ATOL + TF32_RTOL * np.abs(ref), err
+
+
+@pytest.mark.parametrize("mode", ["tf32", "fp32"])
+def test_full_size(full, mode):
+    import torch
+    import x3_conv2d_epilogue_gb300 as ce
+    wl, t, d = full
+    m = ce.MODE_TF32 if mode == "tf32" else ce.MODE_FP32
+    out = run(wl, d, m)
+    assert bool(torch.isfinite(out).all()), "non-finite outputs"
+    rng = np.random.default_rng(1234)
+    Ho, Wo = wl.H - 2, wl.W - 2
+    if wl.kind in (synth.KIND_MIN_TANH2, synth.KIND_SCALE_MIN):
+        if wl.kind == synth.KIND_MIN_TANH2:
+            assert float(out.abs().max()) < math.tanh(1.0)
+        n, i, j = rng.integers(0, wl.N, NS), rng.integers(0, Ho, NS), rng.integers(0, Wo, NS)
+        # always include the image corners and the last rows/columns
+        n[:4], i[:4], j[:4] = [0, wl.N - 1, 0, wl.N - 1], [0, Ho - 1, Ho - 1, 0], [0, Wo - 1, 0, Wo - 1]
+        ref, _ = oracle.min_at(t.x, t.w, t.b, n, i, j, scalar=wl.scalar, tanh2=wl.kind == synth.KIND_MIN_TANH2)
+        idx = torch.as_tensor(np.stack([n, np.zeros_like(n), i, j]), device="cuda")
+        got = out[idx[0], idx[1], idx[2], idx[3]].cpu().numpy()
+    elif wl.kind == synth.KIND_MUL_LRELU_GELU:
+        n, co = rng.integers(0, wl.N, NS), rng.integers(0, wl.Cout, NS)
+        i, j = rng.integers(0, Ho, NS), rng.integers(0, Wo, NS)
+        n[:2], co[:2], i[:2], j[:2] = [0, wl.N - 1], [0, wl.Cout - 1], [0, Ho - 1], [0, Wo - 1]
+        ref = oracle.mul_lrelu_gelu_at(t.x, t.w, t.b, t.mult, n, co, i, j, slope=wl.lrelu_slope)
+        got = out[torch.as_tensor(n), torch.as_tensor(co), torch.as_tensor(i), torch.as_tensor(j)].cpu().numpy()
+    else:
+        assert float(out.min()) >= wl.clamp_lo and float(out.max()) <= wl.clamp_hi
+        ch = oracle.chain_for(wl, t)
+        cpg = wl.Cout // wl.groups
+        pairs = [(0, 0), (wl.N - 1, wl.groups - 1)] + [(int(rng.integers(0, wl.N)), int(rng.integers(0, wl.groups)))
+                                                       for _ in range(GN_GROUPS - 2)]
+        refs, gots = [], []
+        for (n, g) in pairs:
+            r, _, _, _ = oracle.gn_group(t.x, t.w, t.b, ch, n, g)
+            refs.append(r.ravel())
+            gots.append(out[n, g * cpg:(g + 1) * cpg].cpu().numpy().ravel())
+        ref, got = np.concatenate(refs), np.concatenate(gots)
+    ok, err = close(got, ref, mode)
+    assert ok.all(), f"{wl.name} {mode}: {int((~ok).sum())} of {ok.size} sampled outputs off; max err {err.max():.3g}"
