@@ -21,7 +21,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // GroupNorm-chain workspace, written by either conv path and read by the
 // finalize kernel.  For each (n, c, ph, pw) of the pooled output:
-//   pmax / pmin : max / min of y = conv + bias over the k x k window;
+//   pmax / pmin : max / min of y = conv + bias over the k x k window (the
+//                 tf32 path leaves only the one the channel's slope selects,
+//                 in pmax);
 //   amax / amin : window offset a*k+b of the first max / min (fp32 mode only);
 // and for each (n, unit, group) the partial sums of y and y^2 (double) over
 // the rows/cols the unit covered.
@@ -87,8 +89,10 @@ int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
 conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
                            const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
 
-// GroupNorm finalize (gn.cu): pooled max/min + statistics -> output
+// GroupNorm finalize (gn.cu): pooled max/min + statistics -> output.
+// presel: the conv path left in pmax, per channel, the window extreme that the
+// sign of gamma * scale selects (max when it is >= 0, else min), and no pmin.
 conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, float *out,
-                            cudaStream_t s);
+                            cudaStream_t s, bool presel);
 
 }  // namespace conv_epi

@@ -373,7 +373,7 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
         else st = launch<CONV_EPI_GN_SCALE_POOL_CLAMP, 1>(a, L, d.N * a.units, s);
         if (st) return st;
         h->last_launches = 1;
-        st = gn_finalize(h, e, out, s);
+        st = gn_finalize(h, e, out, s, false);
         if (st == CONV_EPI_OK) h->last_launches = 2;
         return st;
     }

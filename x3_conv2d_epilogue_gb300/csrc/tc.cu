@@ -85,7 +85,7 @@ struct Cfg {
     uint32_t a_kw_stride, a_lbo, a_plane_bytes;
     uint32_t idesc;
     float scalar;
-    const float *chan_scale;
+    const float *chan_scale, *gamma;
     float slope;
     int groups, Hp, Wp;
     GnWork gn;
@@ -483,42 +483,67 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint32_t sbase, con
     }
 }
 
-__device__ __forceinline__ float rs_op(float x, float y, int sgn) { return sgn >= 0 ? fminf(x, y) : fmaxf(x, y); }
-
-// warp-wide min / max of one fp32 value per lane, returned to every lane
-__device__ __forceinline__ float warp_min_f32(float v) {
-    float r;
-    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
+// Column-wise minimum over the 32 lanes (channels) of a warp for 16 columns
+// held one per register, by a transposing butterfly: at each level a lane
+// keeps half of its live columns and trades the other half with the partner
+// lane that keeps the opposite half, so every exchanged value is consumed by
+// one min.  16 + 8 + 4 + 2 columns are live before the four trading levels
+// (xor 16, 8, 4, 2) and one plain level (xor 1) finishes: 16 shuffles in all
+// for 16 columns, against 5 per column for a per-column reduction.  Lane l
+// ends with column l >> 1 (bits 4..1 of l name the halves it kept).
+__device__ __forceinline__ float warp_colmin16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int lvl = 0; lvl < 4; ++lvl) {
+        const int h = 8 >> lvl;  // columns kept at this level
+        const bool up = (lane & (2 * h)) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[i + h];
+            const float keep = up ? v[i + h] : v[i];
+            v[i] = fminf(keep, __shfl_xor_sync(0xffffffffu, send, 2 * h));
+        }
+    }
+    return fminf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
 }
-__device__ __forceinline__ float warp_max_f32(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
 
-__device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erff(t * 0.70710678118654752f)); }
+// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26: for x >= 0, erf(x) = 1 - (a1 u + a2 u^2 + a3 u^3 + a4 u^4 + a5 u^5)
+// exp(-x^2) with u = 1 / (1 + p x), |error| <= 1.5e-7; erf(-x) = -erf(x).
+// Branch-free (one reciprocal, one exponential, five FMAs), which matters in
+// the per-channel epilogue; the strict fp32 mode keeps the library erff.
+__device__ __forceinline__ float erf_as7126(float x) {
+    const float ax = fabsf(x);
+    const float u = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+    float poly = fmaf(1.061405429f, u, -1.453152027f);
+    poly = fmaf(poly, u, 1.421413741f);
+    poly = fmaf(poly, u, -0.284496736f);
+    poly = fmaf(poly, u, 0.254829592f);
+    poly *= u;
+    const float r = 1.0f - poly * __expf(-ax * ax);
+    return copysignf(r, x);
+}
+// GELU with the exact-erf form 0.5 t (1 + erf(t / sqrt 2))
+__device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erf_as7126(t * 0.70710678118654752f)); }
 
 // Per-chunk work of the min / per-channel chains on 16 accumulator columns.
 template <int KIND>
-__device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, float bias, float mult, int sgn,
+__device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, float bias, float mult,
                                           int lane, int qd, int ew, int u, int n, int row, int col0,
                                           float *scratch) {
     float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(f.r[i]) + bias;
     if (KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN) {
-        // min (max when the scalar is negative) over this warp's 32 channels,
-        // one warp reduction per column; lane 0 stores the 16 results
-        float r[16];
+        // the chain's minimum over channels of scalar * y: the scalar goes in
+        // first, so a negative scalar needs no separate max; the butterfly
+        // leaves column col0 + (lane >> 1) of this warp's 32 channels in lane
+        // pairs, and the even lane stores it
+        const float sb = a.scalar * bias;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = sgn >= 0 ? warp_min_f32(v[i]) : warp_max_f32(v[i]);
-        if (lane == 0) {
-            float4 *dst = reinterpret_cast<float4 *>(scratch + (u * 4 + qd) * a.P + col0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-        }
+        for (int i = 0; i < 16; ++i) v[i] = fmaf(__uint_as_float(f.r[i]), a.scalar, sb);
+        const float m = warp_colmin16(v, lane);
+        if ((lane & 1) == 0) scratch[(u * 4 + qd) * a.P + col0 + (lane >> 1)] = m;
     } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(f.r[i]) + bias;
         // per-channel chain: transpose 32 channels x 16 columns through shared
         // memory so each store instruction writes 4 rows of 64 contiguous bytes
         float *stg = scratch + ew * 32 * kStgPitch;
@@ -568,10 +593,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int L = qd * 32 + lane;     // accumulator row
     const int slot = L / a.Cout, co = L % a.Cout;
     const float bias = __ldg(&a.b[co]);
-    const int sgn = a.scalar > 0.0f ? 1 : (a.scalar < 0.0f ? -1 : 0);
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
     const float mult = KIND == CONV_EPI_MUL_LRELU_GELU ? __ldg(&a.chan_scale[co]) : 0.0f;
+    const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
     const int nchunks = a.P / 16;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     int j = 0;
@@ -585,14 +610,17 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         tc_fence_after();
         const uint32_t tbase = tmem + lane_off + ab * kAccStride;
 
-        // GN per-thread state: pooled max/min of this thread's 4-column windows
-        // (4 per 16-column chunk, at most 4 chunks: P <= 128), and sums of y, y^2
+        // GN per-thread state: the pooled extreme of this thread's 4-column
+        // windows (4 per 16-column chunk, at most 4 chunks: P <= 128), and sums
+        // of y, y^2.  The extreme is the max of gsg * y: gsg = -1 turns it into
+        // the min for channels whose affine slope gamma * scale * rstd is
+        // negative (rstd > 0, so the sign is known before the statistics).
         constexpr int kMaxWin = 16;
-        float pmx[kMaxWin], pmn[kMaxWin];
+        float pext[kMaxWin];
         float ls = 0.0f, lss = 0.0f;
         if constexpr (kGN) {
 #pragma unroll
-            for (int k = 0; k < kMaxWin; ++k) pmx[k] = -INFINITY, pmn[k] = INFINITY;
+            for (int k = 0; k < kMaxWin; ++k) pext[k] = -INFINITY;
         }
 
         for (int u = 0; u < a.U; ++u) {
@@ -620,10 +648,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
-                        const float mx = fmaxf(fmaxf(v[4 * wi], v[4 * wi + 1]), fmaxf(v[4 * wi + 2], v[4 * wi + 3]));
-                        const float mn = fminf(fminf(v[4 * wi], v[4 * wi + 1]), fminf(v[4 * wi + 2], v[4 * wi + 3]));
-                        pmx[4 * kc + wi] = fmaxf(pmx[4 * kc + wi], mx);
-                        pmn[4 * kc + wi] = fminf(pmn[4 * kc + wi], mn);
+                        const float m01 = fmaxf(gsg * v[4 * wi], gsg * v[4 * wi + 1]);
+                        const float m23 = fmaxf(gsg * v[4 * wi + 2], gsg * v[4 * wi + 3]);
+                        pext[4 * kc + wi] = fmaxf(pext[4 * kc + wi], fmaxf(m01, m23));
                     }
                 }
             } else {
@@ -637,7 +664,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 for (; cc < nchunks; cc += 2) {
                     const bool more = cc + 2 < nchunks;
                     if (more) tmem_ld16_issue(tbase + u * a.ucol + (cc + 2) * 16, nxt);
-                    epi_chunk<KIND>(a, cur, bias, mult, sgn, lane, qd, ew, u, n, row, cc * 16, scratch);
+                    epi_chunk<KIND>(a, cur, bias, mult, lane, qd, ew, u, n, row, cc * 16, scratch);
                     if (more) {
                         tmem_ld_wait(nxt);
                         cur = nxt;
@@ -658,25 +685,32 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 const int s = rem / a.P, col = rem % a.P;
                 const int row = r0 + u * a.S + s;
                 if (row >= a.Ho || col >= a.Wo) continue;
-                float m = scratch[(u * 4 + s * qps) * a.P + col];
-                for (int k = 1; k < qps; ++k) m = rs_op(m, scratch[(u * 4 + s * qps + k) * a.P + col], sgn);
-                float o = sgn == 0 ? 0.0f * m : a.scalar * m;
+                float o = scratch[(u * 4 + s * qps) * a.P + col];
+                for (int k = 1; k < qps; ++k) o = fminf(o, scratch[(u * 4 + s * qps + k) * a.P + col]);
                 if (KIND == CONV_EPI_MIN_TANH2) o = tanhf(tanhf(o));
                 a.out[((size_t)n * a.Ho + row) * a.Wo + col] = o;
             }
             epi_bar();
         } else if constexpr (kGN) {
-            // pooled tile [2][64 channels][kPoolPitch]: slot 1 writes, slot 0 folds in, all store
-            float *pmaxs = scratch, *pmins = scratch + 64 * kPoolPitch;
-            float *st = scratch + 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
-            st[ew * 32 + lane] = ls;
-            st[kEpiThreads + ew * 32 + lane] = lss;
+            // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
+            // channels) add by shuffles, the rest folds below in a fixed order
+            const int cpg = a.Cout / a.groups, cw = cpg < 32 ? cpg : 32;
+            float gs = ls, gss = lss;
+            for (int o = 1; o < cw; o <<= 1) {
+                gs += __shfl_xor_sync(0xffffffffu, gs, o);
+                gss += __shfl_xor_sync(0xffffffffu, gss, o);
+            }
+            // pooled tile [64 channels][kPoolPitch]: slot 1 writes, slot 0 folds in, all store
+            float *pt = scratch;
+            float *st = scratch + 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
+            st[ew * 32 + lane] = gs;
+            st[kEpiThreads + ew * 32 + lane] = gss;
             const int cl = (qd & 1) * 32 + lane;  // channel within the tile (Cout = 64)
             if (slot == 1) {
 #pragma unroll
                 for (int k = 0; k < kMaxWin; ++k) {
                     const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
-                    if (pw < 32) pmaxs[cl * kPoolPitch + pw] = pmx[k], pmins[cl * kPoolPitch + pw] = pmn[k];
+                    if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
                 }
             }
             epi_bar();
@@ -684,37 +718,32 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 #pragma unroll
                 for (int k = 0; k < kMaxWin; ++k) {
                     const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
-                    if (pw < 32) {
-                        pmaxs[cl * kPoolPitch + pw] = fmaxf(pmaxs[cl * kPoolPitch + pw], pmx[k]);
-                        pmins[cl * kPoolPitch + pw] = fminf(pmins[cl * kPoolPitch + pw], pmn[k]);
-                    }
+                    if (pw < 32) pt[cl * kPoolPitch + pw] = gsg * fmaxf(pt[cl * kPoolPitch + pw], pext[k]);
+                }
+            } else if (ew == 2) {
+                // one warp of slot 1: per group, its shuffled sums from both row
+                // slots and both column groups (fixed order)
+                for (int g = lane; g < a.groups; g += 32) {
+                    float s0 = 0.0f, s1 = 0.0f;
+                    for (int sl = 0; sl < a.S; ++sl)
+                        for (int h2 = 0; h2 < 2; ++h2)
+                            for (int c2 = g * cpg; c2 < (g + 1) * cpg; c2 += cw) {
+                                const int LL = sl * a.Cout + c2;
+                                const int e2 = h2 * 4 + (LL >> 5);
+                                s0 += st[e2 * 32 + (LL & 31)];
+                                s1 += st[kEpiThreads + e2 * 32 + (LL & 31)];
+                            }
+                    double *dst = a.gn.part + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2;
+                    dst[0] = s0;
+                    dst[1] = s1;
                 }
             }
             epi_bar();
             if (ru < a.Hp) {
                 for (int idx = et; idx < 64 * a.Wp; idx += kEpiThreads) {
                     const int c2 = idx / a.Wp, pw = idx % a.Wp;
-                    const size_t o = (((size_t)n * a.Cout + c2) * a.Hp + ru) * a.Wp + pw;
-                    a.gn.pmax[o] = pmaxs[c2 * kPoolPitch + pw];
-                    a.gn.pmin[o] = pmins[c2 * kPoolPitch + pw];
+                    a.gn.pmax[(((size_t)n * a.Cout + c2) * a.Hp + ru) * a.Wp + pw] = pt[c2 * kPoolPitch + pw];
                 }
-            }
-            // statistics: fixed-order sum per group over its channels, both row
-            // slots and both column groups
-            const int cpg = a.Cout / a.groups;
-            for (int g = et; g < a.groups; g += kEpiThreads) {
-                double s0 = 0.0, s1 = 0.0;
-                for (int s = 0; s < a.S; ++s)
-                    for (int h2 = 0; h2 < 2; ++h2)
-                        for (int c2 = g * cpg; c2 < (g + 1) * cpg; ++c2) {
-                            const int LL = s * a.Cout + c2;
-                            const int e2 = h2 * 4 + (LL >> 5);
-                            s0 += st[e2 * 32 + (LL & 31)];
-                            s1 += st[kEpiThreads + e2 * 32 + (LL & 31)];
-                        }
-                double *dst = a.gn.part + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2;
-                dst[0] = s0;
-                dst[1] = s1;
             }
             epi_bar();
         }
@@ -824,7 +853,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_MUL_LRELU_GELU:
         return (uint32_t)(kEpiWarps * 32 * kStgPitch * sizeof(float));
     case CONV_EPI_GN_SCALE_POOL_CLAMP:
-        return (uint32_t)((2 * 64 * kPoolPitch + 2 * kEpiThreads) * sizeof(float));
+        return (uint32_t)((64 * kPoolPitch + 2 * kEpiThreads) * sizeof(float));
     }
     return 0;
 }
@@ -984,7 +1013,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.a_lbo = (uint32_t)(2 * pl.S + 1) * a.a_plane_bytes;
     a.a_kw_stride = 2u * a.a_lbo;
     a.idesc = make_idesc(128, pl.P);
-    a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.slope = e.lrelu_slope;
+    a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
         a.gn = h->gn;
@@ -1003,7 +1032,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (st) return st;
     h->last_launches = 2;
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
-        if ((st = gn_finalize(h, e, out, s))) return st;
+        if ((st = gn_finalize(h, e, out, s, true))) return st;
         h->last_launches = 3;
     }
     return CONV_EPI_OK;
