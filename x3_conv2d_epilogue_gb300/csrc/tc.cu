@@ -301,8 +301,22 @@ struct Bars {
 };
 
 // ------------------------------------------------------------- roles ----
+// One thread issues every MMA, so the work between two issues is on the
+// critical path of the tensor pipe: a descriptor rebuilt from scratch per MMA
+// (multiplies, shifts, masks) costs more than a 128-cycle M128 x N256 x K8
+// MMA.  The descriptors are therefore built once per chunk and stepped with
+// plain adds: the start-address field sits in the low bits in 16-byte units,
+// so adding (bytes >> 4) moves the start (no carry leaves the field: shared
+// addresses stay below 2^18).  Ring slots and phases advance by counters.
 __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bars &bars, uint32_t tmem, volatile int *abort_flag) {
-    int it = 0, j = 0;
+    const uint64_t a_desc0 = smem_desc(0, a.a_lbo, 128);      // LBO, SBO, version; start 0
+    const uint64_t b_desc0 = smem_desc(0, 16u * a.PL, 128);
+    const uint32_t a_kw16 = a.a_kw_stride >> 4, a_pl16 = a.a_plane_bytes >> 4;
+    const uint32_t P16 = (uint32_t)a.P;                        // one position row = 16 bytes
+    const uint32_t idesc = a.idesc;
+    int sa = 0, sb = 0;
+    uint32_t pa = 0, pb = 0;
+    int j = 0;
     bool ok = true;
     if (a.resident) ok = wait_bar(bars.wres(), 0, abort_flag, a.err);
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x, ++j) {
@@ -313,30 +327,33 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
         }
         tc_fence_after();
         const uint32_t dcol = tmem + ab * kAccStride;
-        for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int sa = it % a.na, sb = it % a.nb;
-            if ((!a.resident && !wait_bar(bars.a_full(sa), (it / a.na) & 1, abort_flag, a.err)) ||
-                !wait_bar(bars.b_full(sb), (it / a.nb) & 1, abort_flag, a.err)) {
+        for (int c = 0; c < a.chunks; ++c) {
+            if ((!a.resident && !wait_bar(bars.a_full(sa), pa, abort_flag, a.err)) ||
+                !wait_bar(bars.b_full(sb), pb, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t A0 = sbase + a.a_off + (a.resident ? c : sa) * a.a_bytes;
-            const uint32_t B0 = sbase + a.b_off + sb * a.b_bytes;
-            for (int u = 0; u < a.U; ++u) {
-                for (int sk = 0; sk <= a.S + 1; ++sk) {
-#pragma unroll
-                    for (int kw = 0; kw < 3; ++kw) {
-                        const uint64_t ad = smem_desc(A0 + kw * a.a_kw_stride + (a.S + 1 - sk) * a.a_plane_bytes,
-                                                      a.a_lbo, 128);
-                        const uint64_t bd = smem_desc(B0 + 16u * ((u * a.S + sk) * a.P + kw), 16u * a.PL, 128);
-                        mma_tf32(dcol + u * a.ucol, ad, bd, a.idesc, (c | sk | kw) != 0);
-                    }
+            // A for shift sk starts at plane S+1-sk; tap kw adds kw planes-blocks
+            const uint64_t ad0 = a_desc0 + ((sbase + a.a_off + (a.resident ? c : sa) * a.a_bytes) >> 4) +
+                                 (uint64_t)((a.S + 1) * a_pl16);
+            uint64_t bdu = b_desc0 + ((sbase + a.b_off + sb * a.b_bytes) >> 4);
+            uint32_t dcu = dcol;
+            for (int u = 0; u < a.U; ++u, dcu += a.ucol, bdu += a.S * P16) {
+                uint64_t ad = ad0, bd = bdu;
+                for (int sk = 0; sk <= a.S + 1; ++sk, ad -= a_pl16, bd += P16) {
+                    mma_tf32(dcu, ad, bd, idesc, (c | sk) != 0);
+                    mma_tf32(dcu, ad + a_kw16, bd + 1, idesc, 1u);
+                    mma_tf32(dcu, ad + 2 * a_kw16, bd + 2, idesc, 1u);
                 }
             }
             // the stages may be refilled once these MMAs are done
             mma_commit(bars.b_empty(sb));
-            if (!a.resident) mma_commit(bars.a_empty(sa));
+            if (++sb == a.nb) sb = 0, pb ^= 1u;
+            if (!a.resident) {
+                mma_commit(bars.a_empty(sa));
+                if (++sa == a.na) sa = 0, pa ^= 1u;
+            }
         }
         if (!ok) break;
         mma_commit(bars.acc_full(ab));  // accumulator ab is complete
@@ -347,9 +364,9 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
 }
 
 // Producer (one thread): per chunk (unit, c), in order, the raw input tile
-// x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] into staging slot it % nr (laid
+// x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] into the next staging slot (laid
 // out [8][Rin][W]; rows >= H arrive as zeros) and, when the filter streams,
-// chunk c of the packed filter into filter slot it % na.
+// chunk c of the packed filter into the next filter slot.
 __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *xmap, uint32_t sbase, const Bars &bars,
                                               volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
@@ -360,27 +377,25 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
         for (uint32_t off = 0; off < total; off += 16384u)
             bulk_g2s(sbase + a.a_off + off, wsrc + off, min(16384u, total - off), bars.wres());
     }
-    int it = 0;
-    int r_par[kMaxRing], a_par[kMaxRing];
-    bool r_iss[kMaxRing], a_iss[kMaxRing];
-    for (int s = 0; s < kMaxRing; ++s) r_iss[s] = a_iss[s] = false, r_par[s] = a_par[s] = 0;
+    // ring slots and phases by counters; per slot, whether a copy was issued
+    // into it and that copy's phase (bit s of the masks)
+    int sr = 0, sa = 0;
+    uint32_t pr = 0, pa = 0;
+    uint32_t r_iss = 0, r_par = 0, a_iss = 0, a_par = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
         const int n = unit / a.units_per_img;
         const int r0 = (unit % a.units_per_img) * a.RU;
-        for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int sr = it % a.nr;
-            const uint32_t pr = (it / a.nr) & 1;
+        for (int c = 0; c < a.chunks; ++c) {
             if (!wait_bar(bars.r_empty(sr), pr ^ 1, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
             mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
             tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, r0, 8 * c, n, bars.r_full(sr));
-            r_iss[sr] = true, r_par[sr] = pr;
+            r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
+            if (++sr == a.nr) sr = 0, pr ^= 1u;
             if (!a.resident) {
-                const int sa = it % a.na;
-                const uint32_t pa = (it / a.na) & 1;
                 if (!wait_bar(bars.a_empty(sa), pa ^ 1, abort_flag, a.err)) {
                     ok = false;
                     break;
@@ -390,16 +405,17 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
                 mbar_arrive_expect_tx(bars.a_full(sa), a.a_bytes);
                 for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
                     bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(sa));
-                a_iss[sa] = true, a_par[sa] = pa;
+                a_iss |= 1u << sa, a_par = (a_par & ~(1u << sa)) | (pa << sa);
+                if (++sa == a.na) sa = 0, pa ^= 1u;
             }
         }
     }
     // copies still in flight land before the CTA exits
     if (a.resident) wait_bar(bars.wres(), 0, abort_flag, a.err, false);
     for (int s = 0; s < a.nr; ++s)
-        if (r_iss[s]) wait_bar(bars.r_full(s), r_par[s], abort_flag, a.err, false);
+        if ((r_iss >> s) & 1u) wait_bar(bars.r_full(s), (r_par >> s) & 1u, abort_flag, a.err, false);
     for (int s = 0; s < a.na; ++s)
-        if (a_iss[s]) wait_bar(bars.a_full(s), a_par[s], abort_flag, a.err, false);
+        if ((a_iss >> s) & 1u) wait_bar(bars.a_full(s), (a_par >> s) & 1u, abort_flag, a.err, false);
 }
 
 // Converter warps: staged tile [8][Rin][W] -> B plane [ci4][q][4].  Work
@@ -438,13 +454,12 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint32_t sbase, con
             }
         }
     }
-    int it = 0;
+    int sr = 0, sb = 0;
+    uint32_t pr = 0, pb = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
-        for (int c = 0; c < a.chunks; ++c, ++it) {
-            const int sr = it % a.nr, sb = it % a.nb;
-            if (!wait_bar(bars.r_full(sr), (it / a.nr) & 1, abort_flag, a.err) ||
-                !wait_bar(bars.b_empty(sb), ((it / a.nb) & 1) ^ 1, abort_flag, a.err)) {
+        for (int c = 0; c < a.chunks; ++c) {
+            if (!wait_bar(bars.r_full(sr), pr, abort_flag, a.err) || !wait_bar(bars.b_empty(sb), pb ^ 1, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
@@ -479,6 +494,8 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint32_t sbase, con
                 mbar_arrive(bars.r_empty(sr));  // staged tile read
                 mbar_arrive(bars.b_full(sb));
             }
+            if (++sr == a.nr) sr = 0, pr ^= 1u;
+            if (++sb == a.nb) sb = 0, pb ^= 1u;
         }
     }
 }
