@@ -236,6 +236,24 @@ __device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, Frag16 &f) {
         : "r"(taddr)
         : "memory");
 }
+// The same 16 columns of a warp's 32 lanes as two 16x256b loads (lanes 0-15
+// into r[0..7], lanes 16-31 into r[8..15]).  In that shape thread t holds, of
+// its 16-lane half, lane t/4 at columns 2(t%4), 2(t%4)+1 (r0, r1) and +8
+// (r4, r5), and lane t/4 + 8 at the same columns (r2, r3, r6, r7): four
+// channels of four columns per thread, so a reduction over channels starts
+// inside the thread.
+__device__ __forceinline__ void tmem_ld16_rows4_issue(uint32_t taddr, Frag16 &f) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(f.r[0]), "=r"(f.r[1]), "=r"(f.r[2]), "=r"(f.r[3]), "=r"(f.r[4]), "=r"(f.r[5]), "=r"(f.r[6]),
+                   "=r"(f.r[7])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(f.r[8]), "=r"(f.r[9]), "=r"(f.r[10]), "=r"(f.r[11]), "=r"(f.r[12]), "=r"(f.r[13]),
+                   "=r"(f.r[14]), "=r"(f.r[15])
+                 : "r"(taddr + (16u << 16))
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait(Frag16 &f) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(f.r[0]), "+r"(f.r[1]), "+r"(f.r[2]), "+r"(f.r[3]), "+r"(f.r[4]), "+r"(f.r[5]),
@@ -500,27 +518,37 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint32_t sbase, con
     }
 }
 
-// Column-wise minimum over the 32 lanes (channels) of a warp for 16 columns
-// held one per register, by a transposing butterfly: at each level a lane
-// keeps half of its live columns and trades the other half with the partner
-// lane that keeps the opposite half, so every exchanged value is consumed by
-// one min.  16 + 8 + 4 + 2 columns are live before the four trading levels
-// (xor 16, 8, 4, 2) and one plain level (xor 1) finishes: 16 shuffles in all
-// for 16 columns, against 5 per column for a per-column reduction.  Lane l
-// ends with column l >> 1 (bits 4..1 of l name the halves it kept).
-__device__ __forceinline__ float warp_colmin16(float (&v)[16], int lane) {
+// Column-wise minimum of scalar * (acc + bias) over the 32 channels (lanes)
+// of a warp for 16 columns, from a tmem_ld16_rows4_issue fragment.  Each
+// thread first takes the min over its four channels for its four columns
+// 2m, 2m+1, 8+2m, 9+2m (m = lane & 3); the eight lanes that share m then
+// finish with a transposing butterfly over lane bits 4 and 3 (each level a
+// lane keeps half of its columns and trades the other half with the partner
+// that keeps the opposite half) and a plain exchange over bit 2: four
+// shuffles for 16 columns.  Lane l ends with column
+// 8*bit4(l) + 2*(l & 3) + bit3(l), which lanes l and l ^ 4 share.
+__device__ __forceinline__ float warp_colmin16_rows4(const Frag16 &f, float s, const float (&sb)[4], int lane) {
+    float c[4];
 #pragma unroll
-    for (int lvl = 0; lvl < 4; ++lvl) {
-        const int h = 8 >> lvl;  // columns kept at this level
-        const bool up = (lane & (2 * h)) != 0;
-#pragma unroll
-        for (int i = 0; i < h; ++i) {
-            const float send = up ? v[i] : v[i + h];
-            const float keep = up ? v[i + h] : v[i];
-            v[i] = fminf(keep, __shfl_xor_sync(0xffffffffu, send, 2 * h));
-        }
+    for (int j = 0; j < 4; ++j) {
+        const int b = (j >> 1) * 4 + (j & 1);  // register of channel 0 at column j
+        const float x0 = fmaf(__uint_as_float(f.r[b]), s, sb[0]);
+        const float x1 = fmaf(__uint_as_float(f.r[b + 2]), s, sb[1]);
+        const float x2 = fmaf(__uint_as_float(f.r[b + 8]), s, sb[2]);
+        const float x3 = fmaf(__uint_as_float(f.r[b + 10]), s, sb[3]);
+        c[j] = fminf(fminf(x0, x1), fminf(x2, x3));
     }
-    return fminf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+    const bool up16 = (lane & 16) != 0;  // keeps columns 8+2m, 9+2m
+    {
+        const float s0 = up16 ? c[0] : c[2], s1 = up16 ? c[1] : c[3];
+        const float k0 = up16 ? c[2] : c[0], k1 = up16 ? c[3] : c[1];
+        c[0] = fminf(k0, __shfl_xor_sync(0xffffffffu, s0, 16));
+        c[1] = fminf(k1, __shfl_xor_sync(0xffffffffu, s1, 16));
+    }
+    const bool up8 = (lane & 8) != 0;    // keeps the odd column of the pair
+    const float sd = up8 ? c[0] : c[1], kp = up8 ? c[1] : c[0];
+    const float m = fminf(kp, __shfl_xor_sync(0xffffffffu, sd, 8));
+    return fminf(m, __shfl_xor_sync(0xffffffffu, m, 4));
 }
 
 // erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
@@ -543,55 +571,50 @@ __device__ __forceinline__ float erf_as7126(float x) {
 __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erf_as7126(t * 0.70710678118654752f)); }
 
 // Per-chunk work of the min / per-channel chains on 16 accumulator columns.
+// Min chains: f is a tmem_ld16_rows4_issue fragment and sb[k] = scalar * bias
+// of the thread's k-th channel.  Per-channel chain: f is a 32x32b fragment
+// (one channel per lane, 16 columns) and orow points at this lane's first
+// output column of the lane group's first channel in the current row.
 template <int KIND>
-__device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, float bias, float mult,
-                                          int lane, int qd, int ew, int u, int n, int row, int col0,
-                                          float *scratch) {
-    float v[16];
+__device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, const float (&sb)[4], float bias, float mult,
+                                          int lane, int qd, int ew, int u, bool row_ok, int col0, float *orow,
+                                          size_t cstride4, float *scratch) {
     if (KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN) {
         // the chain's minimum over channels of scalar * y: the scalar goes in
-        // first, so a negative scalar needs no separate max; the butterfly
-        // leaves column col0 + (lane >> 1) of this warp's 32 channels in lane
-        // pairs, and the even lane stores it
-        const float sb = a.scalar * bias;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = fmaf(__uint_as_float(f.r[i]), a.scalar, sb);
-        const float m = warp_colmin16(v, lane);
-        if ((lane & 1) == 0) scratch[(u * 4 + qd) * a.P + col0 + (lane >> 1)] = m;
+        // first, so a negative scalar needs no separate max
+        const float m = warp_colmin16_rows4(f, a.scalar, sb, lane);
+        if ((lane & 4) == 0)
+            scratch[(u * 4 + qd) * a.P + col0 + 8 * ((lane >> 4) & 1) + 2 * (lane & 3) + ((lane >> 3) & 1)] = m;
     } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(f.r[i]) + bias;
         // per-channel chain: transpose 32 channels x 16 columns through shared
-        // memory so each store instruction writes 4 rows of 64 contiguous bytes
+        // memory so each store instruction writes 4 channel rows of 64
+        // contiguous bytes; lane l stores columns c2, c2+1 (c2 = 2 (l & 7)) of
+        // channels l/8 + 4 rp, rp = 0..7
         float *stg = scratch + ew * 32 * kStgPitch;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-            float t0 = v[i] * mult, t1 = v[i + 1] * mult;
+            float t0 = (__uint_as_float(f.r[i]) + bias) * mult, t1 = (__uint_as_float(f.r[i + 1]) + bias) * mult;
             t0 = t0 > 0.0f ? t0 : a.slope * t0;
             t1 = t1 > 0.0f ? t1 : a.slope * t1;
             *reinterpret_cast<float2 *>(stg + lane * kStgPitch + i) = make_float2(gelu_erf(t0), gelu_erf(t1));
         }
         __syncwarp();
-        if (row < a.Ho) {
+        if (row_ok) {
             const int c2 = 2 * (lane & 7);
+            const float *src = stg + (lane >> 3) * kStgPitch + c2;
+            float *dst = orow + col0;
             if ((a.Wo & 1) == 0) {
+                if (col0 + c2 < a.Wo) {
 #pragma unroll
-                for (int rp = 0; rp < 8; ++rp) {
-                    const int rr = 4 * rp + (lane >> 3);
-                    const int cor = (qd * 32 + rr) % a.Cout;
-                    if (col0 + c2 < a.Wo) {
-                        float *dst = a.out + (((size_t)n * a.Cout + cor) * a.Ho + row) * a.Wo + col0 + c2;
-                        *reinterpret_cast<float2 *>(dst) = *reinterpret_cast<const float2 *>(stg + rr * kStgPitch + c2);
-                    }
+                    for (int rp = 0; rp < 8; ++rp)
+                        *reinterpret_cast<float2 *>(dst + rp * cstride4) =
+                            *reinterpret_cast<const float2 *>(src + 4 * rp * kStgPitch);
                 }
             } else {
 #pragma unroll
                 for (int rp = 0; rp < 8; ++rp) {
-                    const int rr = 4 * rp + (lane >> 3);
-                    const int cor = (qd * 32 + rr) % a.Cout;
-                    float *dst = a.out + (((size_t)n * a.Cout + cor) * a.Ho + row) * a.Wo + col0 + c2;
-                    if (col0 + c2 < a.Wo) dst[0] = stg[rr * kStgPitch + c2];
-                    if (col0 + c2 + 1 < a.Wo) dst[1] = stg[rr * kStgPitch + c2 + 1];
+                    if (col0 + c2 < a.Wo) dst[rp * cstride4] = src[4 * rp * kStgPitch];
+                    if (col0 + c2 + 1 < a.Wo) dst[rp * cstride4 + 1] = src[4 * rp * kStgPitch + 1];
                 }
             }
         }
@@ -614,6 +637,15 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
     const float mult = KIND == CONV_EPI_MUL_LRELU_GELU ? __ldg(&a.chan_scale[co]) : 0.0f;
     const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
+    // min chains: scalar * bias of the four channels this thread holds in a
+    // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4)
+    float sb4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sb4[k] = kMin ? a.scalar * __ldg(&a.b[(qd * 32 + (lane >> 2) + 8 * k) % a.Cout]) : 0.0f;
+    // per-channel chain: this lane's stores go to channels cb + 4 rp
+    const int cb = (qd * 32) % a.Cout + (lane >> 3);
+    const size_t plane = (size_t)a.Ho * a.Wo;
+    const size_t cstride4 = 4 * plane;
     const int nchunks = a.P / 16;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     int j = 0;
@@ -672,16 +704,22 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 }
             } else {
                 // software-pipelined: the load of chunk cc+2 is in flight while chunk cc is processed
+                const bool row_ok = row < a.Ho;
+                float *orow = a.out + (((size_t)n * a.Cout + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + 2 * (lane & 7);
                 int cc = hc;
                 Frag16 cur, nxt;
                 if (cc < nchunks) {
-                    tmem_ld16_issue(tbase + u * a.ucol + cc * 16, cur);
+                    if (kMin) tmem_ld16_rows4_issue(tbase + u * a.ucol + cc * 16, cur);
+                    else tmem_ld16_issue(tbase + u * a.ucol + cc * 16, cur);
                     tmem_ld_wait(cur);
                 }
                 for (; cc < nchunks; cc += 2) {
                     const bool more = cc + 2 < nchunks;
-                    if (more) tmem_ld16_issue(tbase + u * a.ucol + (cc + 2) * 16, nxt);
-                    epi_chunk<KIND>(a, cur, bias, mult, lane, qd, ew, u, n, row, cc * 16, scratch);
+                    if (more) {
+                        if (kMin) tmem_ld16_rows4_issue(tbase + u * a.ucol + (cc + 2) * 16, nxt);
+                        else tmem_ld16_issue(tbase + u * a.ucol + (cc + 2) * 16, nxt);
+                    }
+                    epi_chunk<KIND>(a, cur, sb4, bias, mult, lane, qd, ew, u, row_ok, cc * 16, orow, cstride4, scratch);
                     if (more) {
                         tmem_ld_wait(nxt);
                         cur = nxt;
