@@ -112,3 +112,38 @@ def test_repeated_forward_is_deterministic():
     a, _ = gpu_run(wl, t, ce.MODE_FP32, repeats=1)
     b, _ = gpu_run(wl, t, ce.MODE_FP32, repeats=3)
     np.testing.assert_array_equal(a, b)
+
+
+def tf32_rna(x: np.ndarray) -> np.ndarray:
+    """fp32 -> tf32 by the rounding rule of the tensor-core mode: keep 10
+    mantissa bits, round to nearest with ties away from zero (finite values)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x1000) & 0xFFFFE000).astype(np.uint32)
+    return r.view(np.float32)
+
+
+def test_tf32_operand_rounding_is_exact():
+    """tf32 mode with a centre-tap filter on one channel and every other
+    channel biased far above it: the channel minimum is that channel's
+    y = tf32(x) * 1, an exact product and a single-term sum, so the output must
+    equal the rounded input bit for bit.  Inputs include exact ties (dropped
+    bits 0x1000) of both signs, values one below and one above a tie, and
+    values whose rounding carries into the exponent."""
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = W["c4_scale_min"].resized(N=1, Cin=8, H=6, W=32, Cout=64, scalar=1.0)
+    t = synth.make_inputs(wl, seed=11)
+    rng = np.random.default_rng(3)
+    bits = rng.normal(size=t.x.shape).astype(np.float32).view(np.uint32)
+    flat = bits.reshape(-1)
+    special = np.array([0x1000, 0x0FFF, 0x1001, 0x1FFF, 0x2000], dtype=np.uint32)
+    flat[:] = (flat & 0xFFFFE000) | special[np.arange(flat.size) % special.size]
+    flat[::7] |= 0x80000000                          # both signs on the tie patterns
+    flat[5::11] = (flat[5::11] & 0x80000000) | 0x3F7FF000   # rounds up into the next binade
+    t.x[:] = bits.view(np.float32)
+    t.w[:] = 0
+    t.w[0, 3, 1, 1] = 1.0
+    t.b[:] = 1.0e6
+    t.b[0] = 0.0
+    got, _ = gpu_run(wl, t, ce.MODE_TF32)
+    want = tf32_rna(t.x[:, 3:4, 1:-1, 1:-1])
+    np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))

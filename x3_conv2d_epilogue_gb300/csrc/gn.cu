@@ -38,11 +38,16 @@ struct GnArgs {
 
 // One CTA per (image, group).  Warp 0 folds the group's per-unit partial sums
 // (fixed order, fp64: lanes take units lane, lane+32, ..., then a fixed
-// shuffle tree) into the mean and the reciprocal standard deviation; then the
-// CTA writes the group's pooled outputs, channel by channel (C/groups
-// consecutive [Hp][Wp] planes: contiguous loads and stores).
+// shuffle tree) into the mean and variance; the first C/groups threads turn
+// them into each channel's affine coefficients (fp32; rstd = 1/sqrt(var +
+// eps) from the fp64 variance).  Then the CTA writes the group's pooled
+// outputs, channel by channel (C/groups consecutive [Hp][Wp] planes:
+// contiguous loads and stores).  fp64 is kept to the fold: it is a slow pipe
+// on this part, so no per-output or per-thread fp64 work.
 __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
-    __shared__ double s_stat[2];
+    constexpr int kMaxCpg = 64;
+    __shared__ float s_mean, s_rstd;
+    __shared__ float sA[kMaxCpg], sB[kMaxCpg];
     const int n = blockIdx.x / a.groups, g = blockIdx.x % a.groups;
     const int cpg = a.C / a.groups;
     if (threadIdx.x < 32) {
@@ -59,24 +64,33 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
             const double mean = s * a.inv_cnt;
             double var = ss * a.inv_cnt - mean * mean;
             if (var < 0.0) var = 0.0;
-            s_stat[0] = mean;
-            s_stat[1] = 1.0 / sqrt(var + (double)a.eps);
+            s_mean = (float)mean;
+            s_rstd = rsqrtf((float)var + a.eps);
         }
     }
     __syncthreads();
-    const double mean = s_stat[0], rstd = s_stat[1];
-    const int per = a.gn.Hp * a.gn.Wp;
-    for (int cl = 0; cl < cpg; ++cl) {
-        const int c = g * cpg + cl;
-        const double gm = a.gamma[c], sc = a.scale[c];
-        const float A = (float)(gm * sc * rstd);
-        const float B = (float)((a.beta[c] - gm * mean * rstd) * sc);
-        const size_t base = ((size_t)n * a.C + c) * per;
-        for (int p = threadIdx.x; p < per; p += kThreads) {
-            const size_t o = base + p;
-            const float y = (a.presel || A >= 0.0f) ? a.gn.pmax[o] : a.gn.pmin[o];
-            a.out[o] = fminf(fmaxf(fmaf(A, y, B), a.lo), a.hi);
-            if (a.idx) a.idx[o] = A > 0.0f ? a.gn.amax[o] : (A < 0.0f ? a.gn.amin[o] : 0);
+    const float mean = s_mean, rstd = s_rstd;
+    for (int cl0 = 0; cl0 < cpg; cl0 += kMaxCpg) {
+        const int ncl = min(kMaxCpg, cpg - cl0);
+        if (cl0 > 0) __syncthreads();  // the previous batch's coefficients are no longer read
+        if (threadIdx.x < ncl) {
+            const int c = g * cpg + cl0 + threadIdx.x;
+            const float gm = a.gamma[c], sc = a.scale[c];
+            sA[threadIdx.x] = gm * sc * rstd;
+            sB[threadIdx.x] = (a.beta[c] - gm * mean * rstd) * sc;
+        }
+        __syncthreads();
+        const int per = a.gn.Hp * a.gn.Wp;
+        for (int cl = 0; cl < ncl; ++cl) {
+            const int c = g * cpg + cl0 + cl;
+            const float A = sA[cl], B = sB[cl];
+            const size_t base = ((size_t)n * a.C + c) * per;
+            for (int p = threadIdx.x; p < per; p += kThreads) {
+                const size_t o = base + p;
+                const float y = (a.presel || A >= 0.0f) ? a.gn.pmax[o] : a.gn.pmin[o];
+                a.out[o] = fminf(fmaxf(fmaf(A, y, B), a.lo), a.hi);
+                if (a.idx) a.idx[o] = A > 0.0f ? a.gn.amax[o] : (A < 0.0f ? a.gn.amin[o] : 0);
+            }
         }
     }
 }
