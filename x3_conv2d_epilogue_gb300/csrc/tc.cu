@@ -57,7 +57,7 @@ namespace conv_epi {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 2, kConvWarps = 6, kConvThreads = kConvWarps * 32;
+constexpr int kConvWarp0 = 2, kConvWarps = 6;
 constexpr int kEpiWarp0 = 8, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;     // columns per accumulator buffer
@@ -157,17 +157,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-// explicit shared-space accesses on 32-bit shared addresses (volatile: they
-// stay in program order with the barrier waits around them)
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // fp32 -> tf32 (10 explicit mantissa bits), round to nearest with ties away
@@ -451,30 +440,34 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
 // its first convert/store (kConvItems items in flight, no latency chain).
 constexpr int kConvItems = 12;  // items per converter warp per chunk (2*Rin*ceil(P/32) <= 72, checked on host)
 
-__device__ __forceinline__ void converter_role(const Cfg &a, uint32_t sbase, const Bars &bars, volatile int *abort_flag) {
+__device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
     const int cw = (threadIdx.x >> 5) - kConvWarp0;
     const int lane = threadIdx.x & 31;
     const int P = a.P, W = a.W, Rin = a.Rin, PL = a.PL;
     const int ps = Rin * W;             // floats between channels of a staged tile
     const int mP = (P + 31) >> 5;       // 32-position groups per input row
     const int nrc = 2 * Rin * mP;       // items per chunk
-    // per item: byte offset into the staged tile (or -1: position past W ->
-    // zero row, -2: no item) and byte offset of the plane row
-    int src_off[kConvItems], dst_off[kConvItems];
+    // per item: float offset into the staged tile (-1: position past W, a
+    // zero row; -2: no row for this lane) and float4 offset of the plane row
+    int so[kConvItems], dof[kConvItems];
+    int nk = 0;                         // items of this warp (the same for all its lanes)
 #pragma unroll
     for (int k = 0; k < kConvItems; ++k) {
         const int rc = cw + k * kConvWarps;
-        src_off[k] = -2, dst_off[k] = 0;
+        so[k] = -2, dof[k] = 0;
         if (rc < nrc) {
+            nk = k + 1;
             const int m = rc % mP, t2 = rc / mP;
             const int rr = t2 % Rin, jg = t2 / Rin;
             const int w = m * 32 + lane;
             if (w < P) {
-                src_off[k] = w < W ? 4 * (4 * jg * ps + rr * W + w) : -1;
-                dst_off[k] = 16 * (jg * PL + rr * P + w);
+                so[k] = w < W ? 4 * jg * ps + rr * W + w : -1;
+                dof[k] = jg * PL + rr * P + w;
             }
         }
     }
+    // every lane of every item on a position inside the row: no per-lane tests
+    const bool dense = P == W && (P & 31) == 0;
     int sr = 0, sb = 0;
     uint32_t pr = 0, pb = 0;
     bool ok = true;
@@ -484,28 +477,35 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint32_t sbase, con
                 ok = false;
                 break;
             }
-            const uint32_t raw = sbase + a.raw_off + sr * a.raw_bytes;
-            const uint32_t plane = sbase + a.b_off + sb * a.b_bytes;
-            float v[kConvItems][4];
+            const float *raw = reinterpret_cast<const float *>(smem + a.raw_off + sr * a.raw_bytes);
+            uint4 *plane = reinterpret_cast<uint4 *>(smem + a.b_off + sb * a.b_bytes);
+            float4 v[kConvItems];
+            if (dense) {
 #pragma unroll
-            for (int k = 0; k < kConvItems; ++k) {
-                v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.0f;
-                if (src_off[k] >= 0) {
-                    const uint32_t src = raw + (uint32_t)src_off[k];
-                    v[k][0] = lds_f32(src);
-                    v[k][1] = lds_f32(src + 4u * ps);
-                    v[k][2] = lds_f32(src + 8u * ps);
-                    v[k][3] = lds_f32(src + 12u * ps);
-                }
-            }
+                for (int k = 0; k < kConvItems; ++k)
+                    if (k < nk) {
+                        const float *src = raw + so[k];
+                        v[k] = make_float4(src[0], src[ps], src[2 * ps], src[3 * ps]);
+                    }
 #pragma unroll
-            for (int k = 0; k < kConvItems; ++k) {
-                if (src_off[k] >= -1) {
-                    uint4 o;
-                    o.x = f32_to_tf32(v[k][0]), o.y = f32_to_tf32(v[k][1]);
-                    o.z = f32_to_tf32(v[k][2]), o.w = f32_to_tf32(v[k][3]);
-                    sts_v4(plane + (uint32_t)dst_off[k], o);
+                for (int k = 0; k < kConvItems; ++k)
+                    if (k < nk)
+                        plane[dof[k]] = make_uint4(f32_to_tf32(v[k].x), f32_to_tf32(v[k].y), f32_to_tf32(v[k].z),
+                                                   f32_to_tf32(v[k].w));
+            } else {
+#pragma unroll
+                for (int k = 0; k < kConvItems; ++k) {
+                    v[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (so[k] >= 0) {
+                        const float *src = raw + so[k];
+                        v[k] = make_float4(src[0], src[ps], src[2 * ps], src[3 * ps]);
+                    }
                 }
+#pragma unroll
+                for (int k = 0; k < kConvItems; ++k)
+                    if (so[k] >= -1)
+                        plane[dof[k]] = make_uint4(f32_to_tf32(v[k].x), f32_to_tf32(v[k].y), f32_to_tf32(v[k].z),
+                                                   f32_to_tf32(v[k].w));
             }
             // each thread makes its own generic-proxy stores visible to the
             // tensor core, then one arrive per warp on each barrier
@@ -569,6 +569,13 @@ __device__ __forceinline__ float erf_as7126(float x) {
     poly *= u;
     const float r = 1.0f - poly * __expf(-ax * ax);
     return copysignf(r, x);
+}
+// tanh from its exponential form: tanh|x| = (1 - e) / (1 + e), e = exp(-2|x|),
+// odd in x; about 1e-7 absolute error (no cancellation problem in absolute
+// terms for small |x|, e -> 0 saturates to 1 for large |x|)
+__device__ __forceinline__ float tanh_exp(float x) {
+    const float e = __expf(-2.0f * fabsf(x));
+    return copysignf(__fdividef(1.0f - e, 1.0f + e), x);
 }
 // GELU with the exact-erf form 0.5 t (1 + erf(t / sqrt 2))
 __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erf_as7126(t * 0.70710678118654752f)); }
@@ -705,23 +712,55 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         pext[4 * kc + wi] = fmaxf(pext[4 * kc + wi], fmaxf(m01, m23));
                     }
                 }
+            } else if constexpr (kMin) {
+                // 32-column superchunks (two 16-column fragments per wait, the
+                // next superchunk's loads in flight while this one is reduced);
+                // the warp takes superchunks hc, hc + 2, ...  Two fragment sets
+                // alternate (no register copies between iterations).
+                const uint32_t tb = tbase + u * a.ucol;
+                const int nsc = (nchunks + 1) >> 1;
+                auto issue = [&](int q, Frag16 &f0, Frag16 &f1) {
+                    tmem_ld16_rows4_issue(tb + q * 32, f0);
+                    if (2 * q + 1 < nchunks) tmem_ld16_rows4_issue(tb + q * 32 + 16, f1);
+                };
+                auto reduce = [&](int q, const Frag16 &f0, const Frag16 &f1) {
+                    epi_chunk<KIND>(a, f0, sb4, bias, mult, lane, qd, ew, u, true, q * 32, nullptr, 0, scratch);
+                    if (2 * q + 1 < nchunks)
+                        epi_chunk<KIND>(a, f1, sb4, bias, mult, lane, qd, ew, u, true, q * 32 + 16, nullptr, 0, scratch);
+                };
+                Frag16 a0, a1, b0, b1;
+                int q = hc;
+                if (q < nsc) {
+                    issue(q, a0, a1);
+                    tmem_ld_wait2(a0, a1);
+                }
+                while (q < nsc) {
+                    if (q + 2 < nsc) issue(q + 2, b0, b1);
+                    reduce(q, a0, a1);
+                    q += 2;
+                    if (q >= nsc) break;
+                    tmem_ld_wait2(b0, b1);
+                    if (q + 2 < nsc) issue(q + 2, a0, a1);
+                    reduce(q, b0, b1);
+                    q += 2;
+                    if (q >= nsc) break;
+                    tmem_ld_wait2(a0, a1);
+                }
             } else {
-                // software-pipelined: the load of chunk cc+2 is in flight while chunk cc is processed
+                // 16-column chunks cc = hc, hc + 2, ...: the load of the next
+                // chunk is in flight while this one is processed
                 const bool row_ok = row < a.Ho;
                 float *orow = a.out + (((size_t)n * a.Cout + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + 2 * (lane & 7);
+                const uint32_t tb = tbase + u * a.ucol;
                 int cc = hc;
                 Frag16 cur, nxt;
                 if (cc < nchunks) {
-                    if (kMin) tmem_ld16_rows4_issue(tbase + u * a.ucol + cc * 16, cur);
-                    else tmem_ld16_issue(tbase + u * a.ucol + cc * 16, cur);
+                    tmem_ld16_issue(tb + cc * 16, cur);
                     tmem_ld_wait(cur);
                 }
                 for (; cc < nchunks; cc += 2) {
                     const bool more = cc + 2 < nchunks;
-                    if (more) {
-                        if (kMin) tmem_ld16_rows4_issue(tbase + u * a.ucol + (cc + 2) * 16, nxt);
-                        else tmem_ld16_issue(tbase + u * a.ucol + (cc + 2) * 16, nxt);
-                    }
+                    if (more) tmem_ld16_issue(tb + (cc + 2) * 16, nxt);
                     epi_chunk<KIND>(a, cur, sb4, bias, mult, lane, qd, ew, u, row_ok, cc * 16, orow, cstride4, scratch);
                     if (more) {
                         tmem_ld_wait(nxt);
@@ -736,19 +775,24 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         if (lane == 0) mbar_arrive(bars.acc_empty(ab));
 
         if constexpr (kMin) {
+            // every warp's partial minima of this unit are in scratch; the
+            // barrier at the start of the next unit keeps them there until all
+            // threads are done reading
             epi_bar();
             const int qps = 4 / a.S;  // quadrants per slot
-            for (int idx = et; idx < a.U * a.S * a.P; idx += kEpiThreads) {
-                const int u = idx / (a.S * a.P), rem = idx % (a.S * a.P);
-                const int s = rem / a.P, col = rem % a.P;
-                const int row = r0 + u * a.S + s;
-                if (row >= a.Ho || col >= a.Wo) continue;
-                float o = scratch[(u * 4 + s * qps) * a.P + col];
-                for (int k = 1; k < qps; ++k) o = fminf(o, scratch[(u * 4 + s * qps + k) * a.P + col]);
-                if (KIND == CONV_EPI_MIN_TANH2) o = tanhf(tanhf(o));
-                a.out[((size_t)n * a.Ho + row) * a.Wo + col] = o;
-            }
-            epi_bar();
+            for (int uu = 0; uu < a.U; ++uu)
+                for (int s = 0; s < a.S; ++s) {
+                    const int row = r0 + uu * a.S + s;
+                    if (row >= a.Ho) continue;
+                    const float *src = scratch + (uu * 4 + s * qps) * a.P;
+                    float *dst = a.out + ((size_t)n * a.Ho + row) * a.Wo;
+                    for (int col = et; col < a.Wo; col += kEpiThreads) {
+                        float o = src[col];
+                        for (int k = 1; k < qps; ++k) o = fminf(o, src[k * a.P + col]);
+                        if (KIND == CONV_EPI_MIN_TANH2) o = tanh_exp(tanh_exp(o));
+                        dst[col] = o;
+                    }
+                }
         } else if constexpr (kGN) {
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
@@ -803,7 +847,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     a.gn.pmax[(((size_t)n * a.Cout + c2) * a.Hp + ru) * a.Wp + pw] = pt[c2 * kPoolPitch + pw];
                 }
             }
-            epi_bar();
+            // (the barrier at the start of the next unit keeps the tile until all stores have read it)
         }
     }
 }
@@ -855,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         if (lane == 0) producer_role(a, &args.xmap, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
-        converter_role(a, sbase, bars, abort_flag);
+        converter_role(a, smem, bars, abort_flag);
     } else {
         epilogue_role<KIND>(a, scratch, bars, tmem, abort_flag);
     }
