@@ -318,6 +318,21 @@ struct Bars {
 // plain adds: the start-address field sits in the low bits in 16-byte units,
 // so adding (bytes >> 4) moves the start (no carry leaves the field: shared
 // addresses stay below 2^18).  Ring slots and phases advance by counters.
+// The (S + 2) x 3 MMAs of one accumulator slot set and one chunk, unrolled:
+// shift sk reads input row sk of the B plane with the A planes for kh = sk - s
+// of each row slot s; tap kw moves both operands by kw.
+template <int S>
+__device__ __forceinline__ void mma_taps(uint32_t d, uint64_t ad0, uint64_t bd0, uint32_t a_pl16, uint32_t a_kw16,
+                                         uint32_t P16, uint32_t idesc, bool acc0) {
+#pragma unroll
+    for (int sk = 0; sk <= S + 1; ++sk) {
+        const uint64_t ad = ad0 - (uint64_t)(sk * a_pl16), bd = bd0 + (uint64_t)(sk * P16);
+        mma_tf32(d, ad, bd, idesc, (acc0 || sk != 0) ? 1u : 0u);
+        mma_tf32(d, ad + a_kw16, bd + 1, idesc, 1u);
+        mma_tf32(d, ad + 2 * a_kw16, bd + 2, idesc, 1u);
+    }
+}
+
 __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bars &bars, uint32_t tmem, volatile int *abort_flag) {
     const uint64_t a_desc0 = smem_desc(0, a.a_lbo, 128);      // LBO, SBO, version; start 0
     const uint64_t b_desc0 = smem_desc(0, 16u * a.PL, 128);
@@ -350,12 +365,8 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
             uint64_t bdu = b_desc0 + ((sbase + a.b_off + sb * a.b_bytes) >> 4);
             uint32_t dcu = dcol;
             for (int u = 0; u < a.U; ++u, dcu += a.ucol, bdu += a.S * P16) {
-                uint64_t ad = ad0, bd = bdu;
-                for (int sk = 0; sk <= a.S + 1; ++sk, ad -= a_pl16, bd += P16) {
-                    mma_tf32(dcu, ad, bd, idesc, (c | sk) != 0);
-                    mma_tf32(dcu, ad + a_kw16, bd + 1, idesc, 1u);
-                    mma_tf32(dcu, ad + 2 * a_kw16, bd + 2, idesc, 1u);
-                }
+                if (a.S == 2) mma_taps<2>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0);
+                else mma_taps<1>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0);
             }
             // the stages may be refilled once these MMAs are done
             mma_commit(bars.b_empty(sb));
@@ -889,10 +900,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    if ((tmem & 0xFFFFu) != 0 && threadIdx.x == 0) atomicOr(a.err, ERRBIT_TMEM);
+    // A CTA that allocates all 512 columns owns the whole tensor memory, so the
+    // allocation starts at lane 0, column 0: the roles use that constant base
+    // (uniform, no per-thread copy of the loaded address).  Any other answer
+    // is reported and the CTA does no work.
+    constexpr uint32_t tmem = 0;
+    const bool tmem_ok = *tmem_slot == tmem;
+    if (!tmem_ok && threadIdx.x == 0) atomicOr(a.err, ERRBIT_TMEM);
 
-    if (warp == 0) {
+    if (!tmem_ok) {
+        // nothing issued, nothing to drain
+    } else if (warp == 0) {
         if (lane == 0) mma_role(a, sbase, bars, tmem, abort_flag);
         __syncwarp();
     } else if (warp == 1) {
@@ -908,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(*tmem_slot, kTmemCols);
     }
 }
 
