@@ -85,11 +85,25 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
             const int c = g * cpg + cl0 + cl;
             const float A = sA[cl], B = sB[cl];
             const size_t base = ((size_t)n * a.C + c) * per;
-            for (int p = threadIdx.x; p < per; p += kThreads) {
-                const size_t o = base + p;
-                const float y = (a.presel || A >= 0.0f) ? a.gn.pmax[o] : a.gn.pmin[o];
-                a.out[o] = fminf(fmaxf(fmaf(A, y, B), a.lo), a.hi);
-                if (a.idx) a.idx[o] = A > 0.0f ? a.gn.amax[o] : (A < 0.0f ? a.gn.amin[o] : 0);
+            const float *__restrict__ src = ((a.presel || A >= 0.0f) ? a.gn.pmax : a.gn.pmin) + base;
+            float *__restrict__ dst = a.out + base;
+            if (a.idx) {
+                const int32_t *__restrict__ isrc = (A > 0.0f ? a.gn.amax : a.gn.amin) + base;
+                for (int p = threadIdx.x; p < per; p += kThreads) {
+                    dst[p] = fminf(fmaxf(fmaf(A, src[p], B), a.lo), a.hi);
+                    a.idx[base + p] = A != 0.0f ? isrc[p] : 0;
+                }
+            } else {
+                // four independent loads in flight per thread
+                int p = threadIdx.x;
+                for (; p + 3 * kThreads < per; p += 4 * kThreads) {
+                    const float y0 = src[p], y1 = src[p + kThreads], y2 = src[p + 2 * kThreads], y3 = src[p + 3 * kThreads];
+                    dst[p] = fminf(fmaxf(fmaf(A, y0, B), a.lo), a.hi);
+                    dst[p + kThreads] = fminf(fmaxf(fmaf(A, y1, B), a.lo), a.hi);
+                    dst[p + 2 * kThreads] = fminf(fmaxf(fmaf(A, y2, B), a.lo), a.hi);
+                    dst[p + 3 * kThreads] = fminf(fmaxf(fmaf(A, y3, B), a.lo), a.hi);
+                }
+                for (; p < per; p += kThreads) dst[p] = fminf(fmaxf(fmaf(A, src[p], B), a.lo), a.hi);
             }
         }
     }

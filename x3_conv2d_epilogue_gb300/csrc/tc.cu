@@ -33,14 +33,17 @@
 // both rows; the two missing (kh = -1, kh = 3) blocks are zero, so 12 MMAs do
 // the work of 9 full-height ones -- still 1.5x the rate of the M = 64 shape.
 //
-// One CTA per SM (persistent), 16 warps:
+// One CTA per SM (persistent), 16 warps; warp w issues on sub-partition w % 4:
 //   warp 0      tensor-memory allocator + single-thread MMA issuer
-//   warp 1      producer: TMA tensor loads of input tiles into the staging
+//   warp 4      producer: TMA tensor loads of input tiles into the staging
 //               ring and bulk copies of the filter (streamed per chunk, or
 //               loaded once when it stays resident)
-//   warps 2-7   converters (staged tile -> B plane)
+//   warps 1-3, 5-7  converters (staged tile -> B plane)
 //   warps 8-15  epilogue (tensor memory -> chain -> global), two warps per
 //               32-lane quadrant, alternating column chunks
+// The MMA thread's instruction stream (descriptor steps, MMA issue, commits)
+// is on the tensor pipe's critical path, so its sub-partition carries no
+// converter: only the mostly waiting producer and two epilogue warps.
 // Rings (mbarrier full/empty pairs): filter stages, B planes, staged tiles;
 // two accumulator buffers in tensor memory so the epilogue of one unit
 // overlaps the main loop of the next.  Every wait is bounded (2 s of
@@ -57,7 +60,9 @@ namespace conv_epi {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 2, kConvWarps = 6;
+constexpr int kProducerWarp = 4, kConvWarps = 6;
+// converter index 0..5 of warps 1-3, 5-7
+__device__ __forceinline__ int conv_index(int warp) { return warp < kProducerWarp ? warp - 1 : warp - 2; }
 constexpr int kEpiWarp0 = 8, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;     // columns per accumulator buffer
@@ -320,19 +325,29 @@ struct Bars {
 // addresses stay below 2^18).  Ring slots and phases advance by counters.
 // The (S + 2) x 3 MMAs of one accumulator slot set and one chunk, unrolled:
 // shift sk reads input row sk of the B plane with the A planes for kh = sk - s
-// of each row slot s; tap kw moves both operands by kw.
-template <int S>
+// of each row slot s; tap kw moves both operands by kw.  `poll` runs after the
+// second-to-last shift, while the last MMAs are still queued ahead of the
+// tensor pipe, so the latency of what it does is hidden behind them.
+template <int S, typename Poll>
 __device__ __forceinline__ void mma_taps(uint32_t d, uint64_t ad0, uint64_t bd0, uint32_t a_pl16, uint32_t a_kw16,
-                                         uint32_t P16, uint32_t idesc, bool acc0) {
+                                         uint32_t P16, uint32_t idesc, bool acc0, Poll &&poll) {
 #pragma unroll
     for (int sk = 0; sk <= S + 1; ++sk) {
         const uint64_t ad = ad0 - (uint64_t)(sk * a_pl16), bd = bd0 + (uint64_t)(sk * P16);
         mma_tf32(d, ad, bd, idesc, (acc0 || sk != 0) ? 1u : 0u);
         mma_tf32(d, ad + a_kw16, bd + 1, idesc, 1u);
         mma_tf32(d, ad + 2 * a_kw16, bd + 2, idesc, 1u);
+        if (sk == S) poll();
     }
 }
 
+// The MMA issuer (one thread).  The tensor pipe queues only about one MMA
+// ahead of the one it executes, so every cycle this thread spends between two
+// MMAs beyond that is idle tensor time.  Chunk and unit boundaries therefore
+// carry as little as possible: the next chunk's stage barriers (and, at the
+// last chunk of a unit, the next accumulator's barrier) are tested inside the
+// current chunk's MMA sequence, and a boundary waits only when that early
+// test found the stage not ready yet.
 __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bars &bars, uint32_t tmem, volatile int *abort_flag) {
     const uint64_t a_desc0 = smem_desc(0, a.a_lbo, 128);      // LBO, SBO, version; start 0
     const uint64_t b_desc0 = smem_desc(0, 16u * a.PL, 128);
@@ -341,40 +356,57 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
     const uint32_t idesc = a.idesc;
     int sa = 0, sb = 0;
     uint32_t pa = 0, pb = 0;
+    bool a_ready = false, b_ready = false, acc_ready = false;  // found complete by an early test
     int j = 0;
     bool ok = true;
     if (a.resident) ok = wait_bar(bars.wres(), 0, abort_flag, a.err);
     for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x, ++j) {
         const int ab = j & 1;
-        if (!wait_bar(bars.acc_empty(ab), ((j >> 1) & 1) ^ 1, abort_flag, a.err)) {
+        if (!acc_ready && !wait_bar(bars.acc_empty(ab), ((j >> 1) & 1) ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
         }
+        acc_ready = false;
         tc_fence_after();
         const uint32_t dcol = tmem + ab * kAccStride;
+        const bool more_units = unit + (int)gridDim.x < a.total_units;
         for (int c = 0; c < a.chunks; ++c) {
-            if ((!a.resident && !wait_bar(bars.a_full(sa), pa, abort_flag, a.err)) ||
-                !wait_bar(bars.b_full(sb), pb, abort_flag, a.err)) {
+            if ((!a.resident && !a_ready && !wait_bar(bars.a_full(sa), pa, abort_flag, a.err)) ||
+                (!b_ready && !wait_bar(bars.b_full(sb), pb, abort_flag, a.err))) {
                 ok = false;
                 break;
             }
+            a_ready = b_ready = false;
             tc_fence_after();
             // A for shift sk starts at plane S+1-sk; tap kw adds kw planes-blocks
             const uint64_t ad0 = a_desc0 + ((sbase + a.a_off + (a.resident ? c : sa) * a.a_bytes) >> 4) +
                                  (uint64_t)((a.S + 1) * a_pl16);
             uint64_t bdu = b_desc0 + ((sbase + a.b_off + sb * a.b_bytes) >> 4);
+            // stage slots of the next chunk, and the next unit's accumulator
+            const int sb2 = sb + 1 == a.nb ? 0 : sb + 1, sa2 = sa + 1 == a.na ? 0 : sa + 1;
+            const uint32_t pb2 = sb + 1 == a.nb ? pb ^ 1u : pb, pa2 = sa + 1 == a.na ? pa ^ 1u : pa;
+            const bool test_acc = c + 1 == a.chunks && more_units;
+            auto poll = [&]() {
+                b_ready = mbar_try_wait(bars.b_full(sb2), pb2);
+                if (!a.resident) a_ready = mbar_try_wait(bars.a_full(sa2), pa2);
+                if (test_acc) acc_ready = mbar_try_wait(bars.acc_empty(ab ^ 1), (((j + 1) >> 1) & 1) ^ 1);
+            };
+            auto none = []() {};
             uint32_t dcu = dcol;
             for (int u = 0; u < a.U; ++u, dcu += a.ucol, bdu += a.S * P16) {
-                if (a.S == 2) mma_taps<2>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0);
-                else mma_taps<1>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0);
+                const bool last_u = u + 1 == a.U;
+                if (a.S == 2) {
+                    if (last_u) mma_taps<2>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0, poll);
+                    else mma_taps<2>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0, none);
+                } else {
+                    if (last_u) mma_taps<1>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0, poll);
+                    else mma_taps<1>(dcu, ad0, bdu, a_pl16, a_kw16, P16, idesc, c != 0, none);
+                }
             }
             // the stages may be refilled once these MMAs are done
             mma_commit(bars.b_empty(sb));
-            if (++sb == a.nb) sb = 0, pb ^= 1u;
-            if (!a.resident) {
-                mma_commit(bars.a_empty(sa));
-                if (++sa == a.na) sa = 0, pa ^= 1u;
-            }
+            if (!a.resident) mma_commit(bars.a_empty(sa));
+            sb = sb2, pb = pb2, sa = sa2, pa = pa2;
         }
         if (!ok) break;
         mma_commit(bars.acc_full(ab));  // accumulator ab is complete
@@ -452,7 +484,7 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
 constexpr int kConvItems = 12;  // items per converter warp per chunk (2*Rin*ceil(P/32) <= 72, checked on host)
 
 __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
-    const int cw = (threadIdx.x >> 5) - kConvWarp0;
+    const int cw = conv_index(threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int P = a.P, W = a.W, Rin = a.Rin, PL = a.PL;
     const int ps = Rin * W;             // floats between channels of a staged tile
@@ -687,7 +719,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         // negative (rstd > 0, so the sign is known before the statistics).
         constexpr int kMaxWin = 16;
         float pext[kMaxWin];
-        float ls = 0.0f, lss = 0.0f;
+        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f}, lss[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains each
         if constexpr (kGN) {
 #pragma unroll
             for (int k = 0; k < kMaxWin; ++k) pext[k] = -INFINITY;
@@ -702,60 +734,59 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     if (hc + 2 * kc < nchunks) tmem_ld16_issue(tbase + u * a.ucol + (hc + 2 * kc) * 16, f[kc]);
                 tmem_ld_wait2(f[0], f[1]);
                 tmem_ld_wait2(f[2], f[3]);
+                if (row < a.Ho) {
 #pragma unroll
-                for (int kc = 0; kc < kMaxWin / 4; ++kc) {
-                    const int cc = hc + 2 * kc;
-                    if (cc >= nchunks || row >= a.Ho) continue;
-                    const int col0 = cc * 16;
-                    float v[16];
+                    for (int kc = 0; kc < kMaxWin / 4; ++kc) {
+                        const int cc = hc + 2 * kc;
+                        if (cc >= nchunks) continue;
+                        const int col0 = cc * 16;
+                        float v[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        v[i] = __uint_as_float(f[kc].r[i]) + bias;
-                        if (col0 + i < a.Wo) {
-                            ls += v[i];
-                            lss = fmaf(v[i], v[i], lss);
+                        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(f[kc].r[i]) + bias;
+                        if (col0 + 16 <= a.Wo) {  // whole chunk inside the row
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                ls[i & 3] += v[i];
+                                lss[i & 3] = fmaf(v[i], v[i], lss[i & 3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (col0 + i < a.Wo) {
+                                    ls[i & 3] += v[i];
+                                    lss[i & 3] = fmaf(v[i], v[i], lss[i & 3]);
+                                }
                         }
-                    }
 #pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        const float m01 = fmaxf(gsg * v[4 * wi], gsg * v[4 * wi + 1]);
-                        const float m23 = fmaxf(gsg * v[4 * wi + 2], gsg * v[4 * wi + 3]);
-                        pext[4 * kc + wi] = fmaxf(pext[4 * kc + wi], fmaxf(m01, m23));
+                        for (int wi = 0; wi < 4; ++wi) {
+                            const float m01 = fmaxf(gsg * v[4 * wi], gsg * v[4 * wi + 1]);
+                            const float m23 = fmaxf(gsg * v[4 * wi + 2], gsg * v[4 * wi + 3]);
+                            pext[4 * kc + wi] = fmaxf(pext[4 * kc + wi], fmaxf(m01, m23));
+                        }
                     }
                 }
             } else if constexpr (kMin) {
-                // 32-column superchunks (two 16-column fragments per wait, the
-                // next superchunk's loads in flight while this one is reduced);
-                // the warp takes superchunks hc, hc + 2, ...  Two fragment sets
-                // alternate (no register copies between iterations).
+                // 64-column batches: the warp takes batches hc, hc + 2, ...,
+                // loads a batch's four 16-column fragments with one wait and
+                // reduces them as four independent chains
                 const uint32_t tb = tbase + u * a.ucol;
-                const int nsc = (nchunks + 1) >> 1;
-                auto issue = [&](int q, Frag16 &f0, Frag16 &f1) {
-                    tmem_ld16_rows4_issue(tb + q * 32, f0);
-                    if (2 * q + 1 < nchunks) tmem_ld16_rows4_issue(tb + q * 32 + 16, f1);
-                };
-                auto reduce = [&](int q, const Frag16 &f0, const Frag16 &f1) {
-                    epi_chunk<KIND>(a, f0, sb4, bias, mult, lane, qd, ew, u, true, q * 32, nullptr, 0, scratch);
-                    if (2 * q + 1 < nchunks)
-                        epi_chunk<KIND>(a, f1, sb4, bias, mult, lane, qd, ew, u, true, q * 32 + 16, nullptr, 0, scratch);
-                };
-                Frag16 a0, a1, b0, b1;
-                int q = hc;
-                if (q < nsc) {
-                    issue(q, a0, a1);
-                    tmem_ld_wait2(a0, a1);
-                }
-                while (q < nsc) {
-                    if (q + 2 < nsc) issue(q + 2, b0, b1);
-                    reduce(q, a0, a1);
-                    q += 2;
-                    if (q >= nsc) break;
-                    tmem_ld_wait2(b0, b1);
-                    if (q + 2 < nsc) issue(q + 2, a0, a1);
-                    reduce(q, b0, b1);
-                    q += 2;
-                    if (q >= nsc) break;
-                    tmem_ld_wait2(a0, a1);
+                const int nbt = (nchunks + 3) >> 2;
+                for (int q = hc; q < nbt; q += 2) {
+                    Frag16 f0, f1, f2, f3;
+                    const int c0 = 4 * q;
+                    tmem_ld16_rows4_issue(tb + c0 * 16, f0);
+                    if (c0 + 1 < nchunks) tmem_ld16_rows4_issue(tb + (c0 + 1) * 16, f1);
+                    if (c0 + 2 < nchunks) tmem_ld16_rows4_issue(tb + (c0 + 2) * 16, f2);
+                    if (c0 + 3 < nchunks) tmem_ld16_rows4_issue(tb + (c0 + 3) * 16, f3);
+                    tmem_ld_wait2(f0, f1);
+                    tmem_ld_wait2(f2, f3);
+                    epi_chunk<KIND>(a, f0, sb4, bias, mult, lane, qd, ew, u, true, c0 * 16, nullptr, 0, scratch);
+                    if (c0 + 1 < nchunks)
+                        epi_chunk<KIND>(a, f1, sb4, bias, mult, lane, qd, ew, u, true, (c0 + 1) * 16, nullptr, 0, scratch);
+                    if (c0 + 2 < nchunks)
+                        epi_chunk<KIND>(a, f2, sb4, bias, mult, lane, qd, ew, u, true, (c0 + 2) * 16, nullptr, 0, scratch);
+                    if (c0 + 3 < nchunks)
+                        epi_chunk<KIND>(a, f3, sb4, bias, mult, lane, qd, ew, u, true, (c0 + 3) * 16, nullptr, 0, scratch);
                 }
             } else {
                 // 16-column chunks cc = hc, hc + 2, ...: the load of the next
@@ -808,7 +839,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
             const int cpg = a.Cout / a.groups, cw = cpg < 32 ? cpg : 32;
-            float gs = ls, gss = lss;
+            float gs = (ls[0] + ls[1]) + (ls[2] + ls[3]), gss = (lss[0] + lss[1]) + (lss[2] + lss[3]);
             for (int o = 1; o < cw; o <<= 1) {
                 gs += __shfl_xor_sync(0xffffffffu, gs, o);
                 gss += __shfl_xor_sync(0xffffffffu, gss, o);
@@ -853,10 +884,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             }
             epi_bar();
             if (ru < a.Hp) {
-                for (int idx = et; idx < 64 * a.Wp; idx += kEpiThreads) {
-                    const int c2 = idx / a.Wp, pw = idx % a.Wp;
-                    a.gn.pmax[(((size_t)n * a.Cout + c2) * a.Hp + ru) * a.Wp + pw] = pt[c2 * kPoolPitch + pw];
-                }
+                // warp ew stores channels ew, ew + 8, ...: one pooled row each (Wp <= 32)
+                float *dst = a.gn.pmax + (((size_t)n * a.Cout + ew) * a.Hp + ru) * a.Wp + lane;
+                const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+                for (int c2 = ew; c2 < 64; c2 += kEpiWarps, dst += cstep)
+                    if (lane < a.Wp) *dst = pt[c2 * kPoolPitch + lane];
             }
             // (the barrier at the start of the next unit keeps the tile until all stores have read it)
         }
@@ -913,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
     } else if (warp == 0) {
         if (lane == 0) mma_role(a, sbase, bars, tmem, abort_flag);
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == kProducerWarp) {
         if (lane == 0) producer_role(a, &args.xmap, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
