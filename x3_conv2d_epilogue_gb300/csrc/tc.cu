@@ -573,7 +573,8 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, cons
 // that keeps the opposite half) and a plain exchange over bit 2: four
 // shuffles for 16 columns.  Lane l ends with column
 // 8*bit4(l) + 2*(l & 3) + bit3(l), which lanes l and l ^ 4 share.
-__device__ __forceinline__ float warp_colmin16_rows4(const Frag16 &f, float s, const float (&sb)[4], int lane) {
+// in-register step: this thread's four channels, columns 2m, 2m+1, 8+2m, 9+2m
+__device__ __forceinline__ float4 colmin16_own(const Frag16 &f, float s, const float (&sb)[4]) {
     float c[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -584,6 +585,11 @@ __device__ __forceinline__ float warp_colmin16_rows4(const Frag16 &f, float s, c
         const float x3 = fmaf(__uint_as_float(f.r[b + 10]), s, sb[3]);
         c[j] = fminf(fminf(x0, x1), fminf(x2, x3));
     }
+    return make_float4(c[0], c[1], c[2], c[3]);
+}
+// butterfly step across the eight lanes that share m
+__device__ __forceinline__ float colmin16_lanes(float4 c4, int lane) {
+    float c[4] = {c4.x, c4.y, c4.z, c4.w};
     const bool up16 = (lane & 16) != 0;  // keeps columns 8+2m, 9+2m
     {
         const float s0 = up16 ? c[0] : c[2], s1 = up16 ? c[1] : c[3];
@@ -595,6 +601,10 @@ __device__ __forceinline__ float warp_colmin16_rows4(const Frag16 &f, float s, c
     const float sd = up8 ? c[0] : c[1], kp = up8 ? c[1] : c[0];
     const float m = fminf(kp, __shfl_xor_sync(0xffffffffu, sd, 8));
     return fminf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+}
+// scratch slot of the column a lane ends with, for the 16 columns at col0
+__device__ __forceinline__ int colmin16_col(int col0, int lane) {
+    return col0 + 8 * ((lane >> 4) & 1) + 2 * (lane & 3) + ((lane >> 3) & 1);
 }
 
 // erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
@@ -635,9 +645,8 @@ __device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, const f
     if (KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN) {
         // the chain's minimum over channels of scalar * y: the scalar goes in
         // first, so a negative scalar needs no separate max
-        const float m = warp_colmin16_rows4(f, a.scalar, sb, lane);
-        if ((lane & 4) == 0)
-            scratch[(u * 4 + qd) * a.P + col0 + 8 * ((lane >> 4) & 1) + 2 * (lane & 3) + ((lane >> 3) & 1)] = m;
+        const float m = colmin16_lanes(colmin16_own(f, a.scalar, sb), lane);
+        if ((lane & 4) == 0) scratch[(u * 4 + qd) * a.P + colmin16_col(col0, lane)] = m;
     } else {
         // per-channel chain: transpose 32 channels x 16 columns through shared
         // memory so each store instruction writes 4 channel rows of 64
@@ -768,25 +777,46 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             } else if constexpr (kMin) {
                 // 64-column batches: the warp takes batches hc, hc + 2, ...,
                 // loads a batch's four 16-column fragments with one wait and
-                // reduces them as four independent chains
+                // reduces each fragment's own four channels in registers;
+                // then the next batch's loads go out, and the butterflies and
+                // stores of this batch run while they are in flight
                 const uint32_t tb = tbase + u * a.ucol;
                 const int nbt = (nchunks + 3) >> 2;
-                for (int q = hc; q < nbt; q += 2) {
-                    Frag16 f0, f1, f2, f3;
+                float *srow = scratch + (u * 4 + qd) * a.P;
+                auto load = [&](int q, Frag16 &f0, Frag16 &f1, Frag16 &f2, Frag16 &f3) {
                     const int c0 = 4 * q;
                     tmem_ld16_rows4_issue(tb + c0 * 16, f0);
                     if (c0 + 1 < nchunks) tmem_ld16_rows4_issue(tb + (c0 + 1) * 16, f1);
                     if (c0 + 2 < nchunks) tmem_ld16_rows4_issue(tb + (c0 + 2) * 16, f2);
                     if (c0 + 3 < nchunks) tmem_ld16_rows4_issue(tb + (c0 + 3) * 16, f3);
+                };
+                int q = hc;
+                if (q < nbt) {
+                    Frag16 f0, f1, f2, f3;
+                    load(q, f0, f1, f2, f3);
                     tmem_ld_wait2(f0, f1);
                     tmem_ld_wait2(f2, f3);
-                    epi_chunk<KIND>(a, f0, sb4, bias, mult, lane, qd, ew, u, true, c0 * 16, nullptr, 0, scratch);
-                    if (c0 + 1 < nchunks)
-                        epi_chunk<KIND>(a, f1, sb4, bias, mult, lane, qd, ew, u, true, (c0 + 1) * 16, nullptr, 0, scratch);
-                    if (c0 + 2 < nchunks)
-                        epi_chunk<KIND>(a, f2, sb4, bias, mult, lane, qd, ew, u, true, (c0 + 2) * 16, nullptr, 0, scratch);
-                    if (c0 + 3 < nchunks)
-                        epi_chunk<KIND>(a, f3, sb4, bias, mult, lane, qd, ew, u, true, (c0 + 3) * 16, nullptr, 0, scratch);
+                    float4 c0 = colmin16_own(f0, a.scalar, sb4), c1 = colmin16_own(f1, a.scalar, sb4);
+                    float4 c2 = colmin16_own(f2, a.scalar, sb4), c3 = colmin16_own(f3, a.scalar, sb4);
+                    for (;;) {
+                        const bool more = q + 2 < nbt;
+                        if (more) load(q + 2, f0, f1, f2, f3);
+                        const int col = 64 * q;
+                        const float m0 = colmin16_lanes(c0, lane), m1 = colmin16_lanes(c1, lane);
+                        const float m2 = colmin16_lanes(c2, lane), m3 = colmin16_lanes(c3, lane);
+                        if ((lane & 4) == 0) {
+                            srow[colmin16_col(col, lane)] = m0;
+                            if (4 * q + 1 < nchunks) srow[colmin16_col(col + 16, lane)] = m1;
+                            if (4 * q + 2 < nchunks) srow[colmin16_col(col + 32, lane)] = m2;
+                            if (4 * q + 3 < nchunks) srow[colmin16_col(col + 48, lane)] = m3;
+                        }
+                        if (!more) break;
+                        q += 2;
+                        tmem_ld_wait2(f0, f1);
+                        tmem_ld_wait2(f2, f3);
+                        c0 = colmin16_own(f0, a.scalar, sb4), c1 = colmin16_own(f1, a.scalar, sb4);
+                        c2 = colmin16_own(f2, a.scalar, sb4), c3 = colmin16_own(f3, a.scalar, sb4);
+                    }
                 }
             } else {
                 // 16-column chunks cc = hc, hc + 2, ...: the load of the next
