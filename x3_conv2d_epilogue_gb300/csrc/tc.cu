@@ -490,27 +490,62 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, cons
     const int ps = Rin * W;             // floats between channels of a staged tile
     const int mP = (P + 31) >> 5;       // 32-position groups per input row
     const int nrc = 2 * Rin * mP;       // items per chunk
-    // per item: float offset into the staged tile (-1: position past W, a
-    // zero row; -2: no row for this lane) and float4 offset of the plane row
+    // Every position of every item inside the row ("dense"): items go in pairs
+    // 32 positions apart in the same row and channel group, so the second item
+    // reuses the first one's four channel addresses with fixed offsets (+32
+    // floats to load, +32 plane rows to store).  Otherwise one item at a time,
+    // with per-lane tests.  Per item (pair): float offset into the staged tile
+    // (-1: position past W, a zero row; -2: no row for this lane) and float4
+    // offset of the plane row.
+    const bool dense = P == W && (P & 63) == 0 && (2 * Rin * (P >> 6)) % kConvWarps <= kConvWarps / 2;
     int so[kConvItems], dof[kConvItems];
-    int nk = 0;                         // items of this warp (the same for all its lanes)
-#pragma unroll
-    for (int k = 0; k < kConvItems; ++k) {
-        const int rc = cw + k * kConvWarps;
-        so[k] = -2, dof[k] = 0;
-        if (rc < nrc) {
-            nk = k + 1;
-            const int m = rc % mP, t2 = rc / mP;
+    int nk = 0;                         // items (pairs) of this warp, the same for all its lanes
+    // dense: pairs beyond a whole number per warp are split into single items,
+    // one each for the first warps, so no warp converts more than one item
+    // above the average
+    bool xone = false;                  // this warp also converts one single item
+    int xso = 0, xdof = 0;
+    if (dense) {
+        const int mP2 = P >> 6;         // 64-position pairs per input row
+        const int nrp = 2 * Rin * mP2;  // pairs per chunk (at most kConvItems / 2 per warp, checked on host)
+        const int npw = nrp / kConvWarps;  // whole pairs per warp
+        auto pair_at = [&](int rc, int &o_s, int &o_d, int half) {
+            const int m2 = rc % mP2, t2 = rc / mP2;
             const int rr = t2 % Rin, jg = t2 / Rin;
-            const int w = m * 32 + lane;
-            if (w < P) {
-                so[k] = w < W ? 4 * jg * ps + rr * W + w : -1;
-                dof[k] = jg * PL + rr * P + w;
+            const int w = m2 * 64 + half * 32 + lane;
+            o_s = 4 * jg * ps + rr * W + w;
+            o_d = jg * PL + rr * P + w;
+        };
+#pragma unroll
+        for (int k = 0; k < kConvItems / 2; ++k) {
+            so[k] = 0, dof[k] = 0;
+            if (k < npw) {
+                nk = k + 1;
+                pair_at(cw + k * kConvWarps, so[k], dof[k], 0);
+            }
+        }
+        const int left = 2 * (nrp - npw * kConvWarps);  // single items left over (<= kConvWarps by the test above)
+        if (cw < left) {
+            xone = true;
+            pair_at(npw * kConvWarps + (cw >> 1), xso, xdof, cw & 1);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kConvItems; ++k) {
+            const int rc = cw + k * kConvWarps;
+            so[k] = -2, dof[k] = 0;
+            if (rc < nrc) {
+                nk = k + 1;
+                const int m = rc % mP, t2 = rc / mP;
+                const int rr = t2 % Rin, jg = t2 / Rin;
+                const int w = m * 32 + lane;
+                if (w < P) {
+                    so[k] = w < W ? 4 * jg * ps + rr * W + w : -1;
+                    dof[k] = jg * PL + rr * P + w;
+                }
             }
         }
     }
-    // every lane of every item on a position inside the row: no per-lane tests
-    const bool dense = P == W && (P & 31) == 0;
     int sr = 0, sb = 0;
     uint32_t pr = 0, pb = 0;
     bool ok = true;
@@ -525,16 +560,26 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, cons
             float4 v[kConvItems];
             if (dense) {
 #pragma unroll
-                for (int k = 0; k < kConvItems; ++k)
+                for (int k = 0; k < kConvItems / 2; ++k)
                     if (k < nk) {
-                        const float *src = raw + so[k];
-                        v[k] = make_float4(src[0], src[ps], src[2 * ps], src[3 * ps]);
+                        const float *s0 = raw + so[k], *s1 = s0 + ps, *s2 = s1 + ps, *s3 = s2 + ps;
+                        v[2 * k] = make_float4(s0[0], s1[0], s2[0], s3[0]);
+                        v[2 * k + 1] = make_float4(s0[32], s1[32], s2[32], s3[32]);
                     }
 #pragma unroll
-                for (int k = 0; k < kConvItems; ++k)
-                    if (k < nk)
-                        plane[dof[k]] = make_uint4(f32_to_tf32(v[k].x), f32_to_tf32(v[k].y), f32_to_tf32(v[k].z),
-                                                   f32_to_tf32(v[k].w));
+                for (int k = 0; k < kConvItems / 2; ++k)
+                    if (k < nk) {
+                        uint4 *d = plane + dof[k];
+                        d[0] = make_uint4(f32_to_tf32(v[2 * k].x), f32_to_tf32(v[2 * k].y), f32_to_tf32(v[2 * k].z),
+                                          f32_to_tf32(v[2 * k].w));
+                        d[32] = make_uint4(f32_to_tf32(v[2 * k + 1].x), f32_to_tf32(v[2 * k + 1].y),
+                                           f32_to_tf32(v[2 * k + 1].z), f32_to_tf32(v[2 * k + 1].w));
+                    }
+                if (xone) {
+                    const float *s0 = raw + xso;
+                    const float4 x = make_float4(s0[0], s0[ps], s0[2 * ps], s0[3 * ps]);
+                    plane[xdof] = make_uint4(f32_to_tf32(x.x), f32_to_tf32(x.y), f32_to_tf32(x.z), f32_to_tf32(x.w));
+                }
             } else {
 #pragma unroll
                 for (int k = 0; k < kConvItems; ++k) {
