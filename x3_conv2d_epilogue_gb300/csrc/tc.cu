@@ -419,7 +419,13 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
 // Producer (one thread): per chunk (unit, c), in order, the raw input tile
 // x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] into the next staging slot (laid
 // out [8][Rin][W]; rows >= H arrive as zeros) and, when the filter streams,
-// chunk c of the packed filter into the next filter slot.
+// chunk c of the packed filter into the next filter slot.  The two sequences
+// advance independently: while both run, the thread tests both rings without
+// blocking and issues whichever copy has a free slot, so a full filter ring
+// (freed only as MMAs complete) does not hold back the input tiles, which have
+// the longer latency; it sleeps briefly when neither can move, and gives up
+// like every other wait after kWaitLimitNs without progress.  Once only the
+// tiles are left (always, with a resident filter) it blocks in wait_bar.
 __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *xmap, uint32_t sbase, const Bars &bars,
                                               volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
@@ -430,38 +436,60 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
         for (uint32_t off = 0; off < total; off += 16384u)
             bulk_g2s(sbase + a.a_off + off, wsrc + off, min(16384u, total - off), bars.wres());
     }
+    // this CTA's chunk sequence: units blockIdx.x, + gridDim.x, ..., chunks 0..chunks-1
+    const int my_units = a.total_units > (int)blockIdx.x ? (a.total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_units * a.chunks;
     // ring slots and phases by counters; per slot, whether a copy was issued
     // into it and that copy's phase (bit s of the masks)
     int sr = 0, sa = 0;
     uint32_t pr = 0, pa = 0;
     uint32_t r_iss = 0, r_par = 0, a_iss = 0, a_par = 0;
-    bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < a.total_units; unit += gridDim.x) {
-        const int n = unit / a.units_per_img;
-        const int r0 = (unit % a.units_per_img) * a.RU;
-        for (int c = 0; c < a.chunks; ++c) {
-            if (!wait_bar(bars.r_empty(sr), pr ^ 1, abort_flag, a.err)) {
-                ok = false;
-                break;
-            }
+    int ir = 0, ia = a.resident ? total : 0;  // next raw tile / next filter chunk
+    int ur = 0, cr = 0;                       // (unit index within this CTA, chunk) of tile ir
+    uint64_t t_idle = 0;
+    while (ir < total || ia < total) {
+        bool moved = false;
+        // with the filter sequence done (or resident), the tile sequence
+        // blocks in the ordinary bounded wait
+        const bool tiles_only = ia >= total;
+        if (tiles_only && !wait_bar(bars.r_empty(sr), pr ^ 1, abort_flag, a.err)) break;
+        if (ir < total && (tiles_only || mbar_try_wait(bars.r_empty(sr), pr ^ 1))) {
+            const int unit = (int)blockIdx.x + ur * (int)gridDim.x;
+            const int n = unit / a.units_per_img;
+            const int r0 = (unit % a.units_per_img) * a.RU;
             mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
-            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, r0, 8 * c, n, bars.r_full(sr));
+            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, r0, 8 * cr, n, bars.r_full(sr));
             r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
             if (++sr == a.nr) sr = 0, pr ^= 1u;
-            if (!a.resident) {
-                if (!wait_bar(bars.a_empty(sa), pa ^ 1, abort_flag, a.err)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t dst = sbase + a.a_off + sa * a.a_bytes;
-                const char *src = wsrc + (size_t)c * a.a_bytes;
-                mbar_arrive_expect_tx(bars.a_full(sa), a.a_bytes);
-                for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
-                    bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(sa));
-                a_iss |= 1u << sa, a_par = (a_par & ~(1u << sa)) | (pa << sa);
-                if (++sa == a.na) sa = 0, pa ^= 1u;
-            }
+            if (++cr == a.chunks) cr = 0, ++ur;
+            ++ir;
+            moved = true;
         }
+        if (ia < total && mbar_try_wait(bars.a_empty(sa), pa ^ 1)) {
+            const int c = ia % a.chunks;
+            const uint32_t dst = sbase + a.a_off + sa * a.a_bytes;
+            const char *src = wsrc + (size_t)c * a.a_bytes;
+            mbar_arrive_expect_tx(bars.a_full(sa), a.a_bytes);
+            for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
+                bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(sa));
+            a_iss |= 1u << sa, a_par = (a_par & ~(1u << sa)) | (pa << sa);
+            if (++sa == a.na) sa = 0, pa ^= 1u;
+            ++ia;
+            moved = true;
+        }
+        if (moved) {
+            t_idle = 0;
+            continue;
+        }
+        if (*abort_flag) break;
+        const uint64_t now = globaltimer();
+        if (t_idle == 0) t_idle = now;
+        else if (now - t_idle > kWaitLimitNs) {
+            atomicOr(a.err, ERRBIT_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        __nanosleep(64);
     }
     // copies still in flight land before the CTA exits
     if (a.resident) wait_bar(bars.wres(), 0, abort_flag, a.err, false);
