@@ -25,6 +25,8 @@ SMALL = {
     "c4neg": W["c4_scale_min"].resized(N=1, H=7, W=96, scalar=-1.5),          # max branch
     "c5s": W["c5_gn_pool_clamp"].resized(N=2, H=42),                         # 40 rows: 10 bands, no tail
     "c5t": W["c5_gn_pool_clamp"].resized(N=2, H=40),                         # 38 rows: 9 bands + 2 stat rows
+    "c4w128": W["c4_scale_min"].resized(N=1, H=9, W=128),                    # tf32 converter falls back to single items
+    "c2w64": W["c2_min_tanh2"].resized(N=2, H=23, W=64),                     # four row pairs per accumulator, ragged units
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 
