@@ -299,6 +299,18 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag
     }
 }
 
+// (image, row block) of unit blockIdx.x + k * gridDim.x, stepped without
+// divisions: the row block advances by the grid size and wraps into the image
+// index (units_per_img >= 1)
+struct UnitPos {
+    int n, ru;
+    __device__ void init(int unit, int upi) { n = unit / upi, ru = unit % upi; }
+    __device__ void step(int stride, int upi) {
+        ru += stride;
+        while (ru >= upi) ru -= upi, ++n;
+    }
+};
+
 // ---------------------------------------------------------- barriers ----
 struct Bars {
     uint32_t base;
@@ -445,7 +457,9 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
     uint32_t pr = 0, pa = 0;
     uint32_t r_iss = 0, r_par = 0, a_iss = 0, a_par = 0;
     int ir = 0, ia = a.resident ? total : 0;  // next raw tile / next filter chunk
-    int ur = 0, cr = 0;                       // (unit index within this CTA, chunk) of tile ir
+    int cr = 0, ca = 0;                       // chunk of tile ir / of filter chunk ia
+    UnitPos pos;                              // (image, row block) of tile ir
+    pos.init(blockIdx.x, a.units_per_img);
     uint64_t t_idle = 0;
     while (ir < total || ia < total) {
         bool moved = false;
@@ -454,21 +468,18 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
         const bool tiles_only = ia >= total;
         if (tiles_only && !wait_bar(bars.r_empty(sr), pr ^ 1, abort_flag, a.err)) break;
         if (ir < total && (tiles_only || mbar_try_wait(bars.r_empty(sr), pr ^ 1))) {
-            const int unit = (int)blockIdx.x + ur * (int)gridDim.x;
-            const int n = unit / a.units_per_img;
-            const int r0 = (unit % a.units_per_img) * a.RU;
             mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
-            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, r0, 8 * cr, n, bars.r_full(sr));
+            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, pos.ru * a.RU, 8 * cr, pos.n, bars.r_full(sr));
             r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
             if (++sr == a.nr) sr = 0, pr ^= 1u;
-            if (++cr == a.chunks) cr = 0, ++ur;
+            if (++cr == a.chunks) cr = 0, pos.step(gridDim.x, a.units_per_img);
             ++ir;
             moved = true;
         }
         if (ia < total && mbar_try_wait(bars.a_empty(sa), pa ^ 1)) {
-            const int c = ia % a.chunks;
             const uint32_t dst = sbase + a.a_off + sa * a.a_bytes;
-            const char *src = wsrc + (size_t)c * a.a_bytes;
+            const char *src = wsrc + (size_t)ca * a.a_bytes;
+            if (++ca == a.chunks) ca = 0;
             mbar_arrive_expect_tx(bars.a_full(sa), a.a_bytes);
             for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
                 bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(sa));
@@ -784,9 +795,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int nchunks = a.P / 16;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     int j = 0;
-    for (int unit = blockIdx.x; unit < a.total_units; unit += gridDim.x, ++j) {
-        const int n = unit / a.units_per_img;
-        const int ru = unit % a.units_per_img;
+    UnitPos pos;
+    pos.init(blockIdx.x, a.units_per_img);
+    for (int unit = blockIdx.x; unit < a.total_units; unit += gridDim.x, ++j, pos.step(gridDim.x, a.units_per_img)) {
+        const int n = pos.n;
+        const int ru = pos.ru;
         const int r0 = ru * a.RU;
         const int ab = j & 1;
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
