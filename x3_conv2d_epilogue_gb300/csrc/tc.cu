@@ -794,6 +794,12 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const size_t cstride4 = 4 * plane;
     const int nchunks = a.P / 16;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    // GroupNorm chain: group size, lanes per group inside a warp, and the sign
+    // table of the pooled extremes (a 64-float array after the tiles, written
+    // here and first read after the first combine barrier)
+    const int gn_cpg = kGN ? a.Cout / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
+    float *gn_sgn = scratch + 2 * 64 * kPoolPitch + 2 * kEpiThreads;
+    if (kGN && slot == 0) gn_sgn[co] = gsg;
     int j = 0;
     UnitPos pos;
     pos.init(blockIdx.x, a.units_per_img);
@@ -954,40 +960,33 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         } else if constexpr (kGN) {
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
-            const int cpg = a.Cout / a.groups, cw = cpg < 32 ? cpg : 32;
             float gs = (ls[0] + ls[1]) + (ls[2] + ls[3]), gss = (lss[0] + lss[1]) + (lss[2] + lss[3]);
-            for (int o = 1; o < cw; o <<= 1) {
+            for (int o = 1; o < gn_cw; o <<= 1) {
                 gs += __shfl_xor_sync(0xffffffffu, gs, o);
                 gss += __shfl_xor_sync(0xffffffffu, gss, o);
             }
-            // pooled tile [64 channels][kPoolPitch]: slot 1 writes, slot 0 folds in, all store
-            float *pt = scratch;
-            float *st = scratch + 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
+            // pooled tiles [2 row slots][64 channels][kPoolPitch] (window
+            // extremes in gsg space); both slots write, one barrier, and the
+            // stores fold the two slots
+            float *pt = scratch + slot * 64 * kPoolPitch;
+            float *st = scratch + 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
             st[ew * 32 + lane] = gs;
             st[kEpiThreads + ew * 32 + lane] = gss;
             const int cl = (qd & 1) * 32 + lane;  // channel within the tile (Cout = 64)
-            if (slot == 1) {
 #pragma unroll
-                for (int k = 0; k < kMaxWin; ++k) {
-                    const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
-                    if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
-                }
+            for (int k = 0; k < kMaxWin; ++k) {
+                const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
+                if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
             }
             epi_bar();
-            if (slot == 0) {
-#pragma unroll
-                for (int k = 0; k < kMaxWin; ++k) {
-                    const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
-                    if (pw < 32) pt[cl * kPoolPitch + pw] = gsg * fmaxf(pt[cl * kPoolPitch + pw], pext[k]);
-                }
-            } else if (ew == 2) {
-                // one warp of slot 1: per group, its shuffled sums from both row
-                // slots and both column groups (fixed order)
+            if (ew == 2) {
+                // one warp: per group, the shuffled sums from both row slots and
+                // both column groups (fixed order)
                 for (int g = lane; g < a.groups; g += 32) {
                     float s0 = 0.0f, s1 = 0.0f;
                     for (int sl = 0; sl < a.S; ++sl)
                         for (int h2 = 0; h2 < 2; ++h2)
-                            for (int c2 = g * cpg; c2 < (g + 1) * cpg; c2 += cw) {
+                            for (int c2 = g * gn_cpg; c2 < (g + 1) * gn_cpg; c2 += gn_cw) {
                                 const int LL = sl * a.Cout + c2;
                                 const int e2 = h2 * 4 + (LL >> 5);
                                 s0 += st[e2 * 32 + (LL & 31)];
@@ -998,13 +997,15 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     dst[1] = s1;
                 }
             }
-            epi_bar();
             if (ru < a.Hp) {
-                // warp ew stores channels ew, ew + 8, ...: one pooled row each (Wp <= 32)
+                // warp ew stores channels ew, ew + 8, ...: one pooled row each
+                // (Wp <= 32), the two row slots folded and the sign restored
+                const float *pt0 = scratch, *pt1 = scratch + 64 * kPoolPitch;
                 float *dst = a.gn.pmax + (((size_t)n * a.Cout + ew) * a.Hp + ru) * a.Wp + lane;
                 const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
                 for (int c2 = ew; c2 < 64; c2 += kEpiWarps, dst += cstep)
-                    if (lane < a.Wp) *dst = pt[c2 * kPoolPitch + lane];
+                    if (lane < a.Wp)
+                        *dst = gn_sgn[c2] * fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]);
             }
             // (the barrier at the start of the next unit keeps the tile until all stores have read it)
         }
@@ -1121,7 +1122,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_MUL_LRELU_GELU:
         return (uint32_t)(kEpiWarps * 32 * kStgPitch * sizeof(float));
     case CONV_EPI_GN_SCALE_POOL_CLAMP:
-        return (uint32_t)((64 * kPoolPitch + 2 * kEpiThreads) * sizeof(float));
+        return (uint32_t)((2 * 64 * kPoolPitch + 2 * kEpiThreads + 64) * sizeof(float));
     }
     return 0;
 }
