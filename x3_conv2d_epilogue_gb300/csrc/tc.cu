@@ -70,6 +70,7 @@ constexpr int kMaxRing = 4;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kStgPitch = 18;       // per-channel epilogue staging pitch (floats, even: float2 rows)
 constexpr int kPoolPitch = 33;      // GroupNorm pooled tile pitch (floats)
+constexpr int kMaxQ = 8;            // min chains: quadrant partials of a column loaded together
 
 // Scalar kernel configuration.  The kernel copies it out of the parameter
 // space into a local at entry, so the roles keep the fields in registers
@@ -943,20 +944,40 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // barrier at the start of the next unit keeps them there until all
             // threads are done reading
             epi_bar();
+            // Every partial of a column (each row of the unit, each quadrant)
+            // is loaded before any is used: under the tensor core's operand
+            // traffic a shared-memory load waits long, so the loads go out
+            // together instead of one row after another.  Scratch row k of
+            // the unit (k = u * 4 + quadrant) holds quadrant partials; row
+            // slot s of u uses quadrants s * qps .. s * qps + qps - 1.
             const int qps = 4 / a.S;  // quadrants per slot
-            for (int uu = 0; uu < a.U; ++uu)
-                for (int s = 0; s < a.S; ++s) {
-                    const int row = r0 + uu * a.S + s;
-                    if (row >= a.Ho) continue;
-                    const float *src = scratch + (uu * 4 + s * qps) * a.P;
-                    float *dst = a.out + ((size_t)n * a.Ho + row) * a.Wo;
-                    for (int col = et; col < a.Wo; col += kEpiThreads) {
-                        float o = src[col];
-                        for (int k = 1; k < qps; ++k) o = fminf(o, src[k * a.P + col]);
+            const int nq = a.U * 4;   // scratch rows of the unit (<= 32)
+            float *orow0 = a.out + ((size_t)n * a.Ho + r0) * a.Wo;
+            for (int col = et; col < a.Wo; col += kEpiThreads)
+              for (int kb = 0; kb < nq; kb += kMaxQ) {  // two u at a time (nq is a multiple of 4)
+                float pv[kMaxQ];
+#pragma unroll
+                for (int k = 0; k < kMaxQ; ++k)
+                    if (kb + k < nq) pv[k] = scratch[(kb + k) * a.P + col];
+#pragma unroll
+                for (int k = 0; k < kMaxQ; k += 4) {
+                    if (kb + k >= nq) break;
+                    // the 4 quadrants of u = (kb + k) / 4: one row (qps = 4) or two (qps = 2)
+                    const int u = (kb + k) >> 2;
+                    if (qps == 4) {
+                        const int row = r0 + u;
+                        float o = fminf(fminf(pv[k], pv[k + 1]), fminf(pv[k + 2], pv[k + 3]));
                         if (KIND == CONV_EPI_MIN_TANH2) o = tanh_exp(tanh_exp(o));
-                        dst[col] = o;
+                        if (row < a.Ho) orow0[(size_t)(u) * a.Wo + col] = o;
+                    } else {
+                        const int row = r0 + 2 * u;
+                        float o0 = fminf(pv[k], pv[k + 1]), o1 = fminf(pv[k + 2], pv[k + 3]);
+                        if (KIND == CONV_EPI_MIN_TANH2) o0 = tanh_exp(tanh_exp(o0)), o1 = tanh_exp(tanh_exp(o1));
+                        if (row < a.Ho) orow0[(size_t)(2 * u) * a.Wo + col] = o0;
+                        if (row + 1 < a.Ho) orow0[(size_t)(2 * u + 1) * a.Wo + col] = o1;
                     }
                 }
+            }
         } else if constexpr (kGN) {
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
