@@ -148,8 +148,8 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
  *   conv_epi_forward.  Chains MIN_TANH2, SCALE_MIN and MUL_LRELU_GELU only
  *   (the GroupNorm chain needs a larger workspace); index_out must be NULL.
  * Returns CONV_EPI_ERR_UNSUPPORTED when the packed filter of the problem does
- * not fit the array (Cin*3*(2S+1)*Cout floats plus one 8-channel chunk, with
- * S = 128/Cout) or the shape is outside the tensor-core path.  The first call
+ * not fit the array (Cin rounded up to a multiple of 8, times 3*(2S+1)*Cout
+ * floats, plus one 8-channel chunk, with S = 128/Cout) or the shape is outside the tensor-core path.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress) and
  * clears its error word with a synchronous cudaMemset, so make that first
  * call before any stream capture.  Every call on a device shares the array

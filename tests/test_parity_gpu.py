@@ -27,6 +27,9 @@ SMALL = {
     "c5t": W["c5_gn_pool_clamp"].resized(N=2, H=40),                         # 38 rows: 9 bands + 2 stat rows
     "c4w128": W["c4_scale_min"].resized(N=1, H=9, W=128),                    # tf32 converter falls back to single items
     "c2w64": W["c2_min_tanh2"].resized(N=2, H=23, W=64),                     # four row pairs per accumulator, ragged units
+    "c2cin12": W["c2_min_tanh2"].resized(N=1, H=11, Cin=12),                 # Cin not a multiple of 8 (zero-padded chunk)
+    "c3cin3": W["c3_mul_lrelu_gelu"].resized(N=1, H=9, W=64, Cin=3),        # 3 input channels (one padded chunk)
+    "c4cin20": W["c4_scale_min"].resized(N=1, H=7, Cin=20),                  # Cout 128, Cin 20
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 

@@ -1103,10 +1103,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
 // ------------------------------------------------------ filter packing ----
 // wpack[c][kw][jg][p][co][e] = tf32(w[co][8c + 4jg + e][kh][kw]) with
 // kh = S+1-p when 0 <= kh <= 2, else 0 (the zero planes that pad the
-// stacked row slots).
+// stacked row slots), and 0 for input channels 8c + 4jg + e >= Cin (the last
+// chunk of a Cin that is not a multiple of 8; the input tile's matching
+// channels arrive as zeros too, from the tensor load's out-of-range fill).
 __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp, int Cin, int Cout, int S) {
     const int planes = 2 * S + 1;
-    const size_t total = (size_t)Cin * 3 * planes * Cout;  // = chunks*3*2*planes*Cout*4
+    const int Cpad = (Cin + 7) / 8 * 8;
+    const size_t total = (size_t)Cpad * 3 * planes * Cout;  // = chunks*3*2*planes*Cout*4
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
         size_t r = i;
         const int e = r % 4;
@@ -1121,7 +1124,8 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
         const int c = (int)(r / 3);
         const int kh = S + 1 - p;
         float v = 0.0f;
-        if (kh >= 0 && kh <= 2) v = w[(((size_t)co * Cin + 8 * c + 4 * jg + e) * 3 + kh) * 3 + kw];
+        const int ci = 8 * c + 4 * jg + e;
+        if (kh >= 0 && kh <= 2 && ci < Cin) v = w[(((size_t)co * Cin + ci) * 3 + kh) * 3 + kw];
         wp[i] = __uint_as_float(f32_to_tf32(v));
     }
 }
@@ -1154,7 +1158,7 @@ uint32_t up1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 // tmem slot, abort flag][epilogue scratch]
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (!(d.Cout == 64 || d.Cout == 128)) return false;
-    if (d.Cin % 8 != 0 || d.W % 4 != 0 || d.W > 256 || d.H < 3) return false;
+    if (d.Cin < 1 || d.W % 4 != 0 || d.W > 256 || d.H < 3) return false;
     pl.S = 128 / d.Cout;
     pl.P = (d.W + 15) / 16 * 16;
     pl.ucol = (pl.P + 31) / 32 * 32;
@@ -1163,7 +1167,7 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.Rin = pl.RU + 2;
     if (pl.Rin > 256) return false;  // TMA box height
     pl.PL = (pl.Rin * pl.P + 4 + 7) / 8 * 8;
-    pl.chunks = d.Cin / 8;
+    pl.chunks = (d.Cin + 7) / 8;  // the last chunk of a Cin not a multiple of 8 is zero-padded
     if (pl.PL >= (1 << 16)) return false;
     if (2 * pl.Rin * ((pl.P + 31) / 32) > kConvItems * kConvWarps) return false;  // converter items per chunk
     pl.a_bytes = up1k(3u * 2u * (2 * pl.S + 1) * d.Cout * 16u);
@@ -1247,7 +1251,7 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
 size_t tc_wpack_bytes(const conv_epi_desc &d) {
     const int S = d.Cout >= 128 ? 1 : 2;
     const size_t chunk = ((size_t)3 * 2 * (2 * S + 1) * d.Cout * 16 + 1023) & ~(size_t)1023;
-    return (size_t)(d.Cin / 8 + 1) * chunk + 256;
+    return (size_t)((d.Cin + 7) / 8 + 1) * chunk + 256;
 }
 
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
