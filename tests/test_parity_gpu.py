@@ -30,6 +30,9 @@ SMALL = {
     "c2cin12": W["c2_min_tanh2"].resized(N=1, H=11, Cin=12),                 # Cin not a multiple of 8 (zero-padded chunk)
     "c3cin3": W["c3_mul_lrelu_gelu"].resized(N=1, H=9, W=64, Cin=3),        # 3 input channels (one padded chunk)
     "c4cin20": W["c4_scale_min"].resized(N=1, H=7, Cin=20),                  # Cout 128, Cin 20
+    "c2co48": W["c2_min_tanh2"].resized(N=1, H=9, Cout=48),                  # Cout padded to 64 (zero filters)
+    "c4co100": W["c4_scale_min"].resized(N=1, H=7, W=128, Cout=100, scalar=-0.5),  # padded to 128, max branch
+    "c3co40": W["c3_mul_lrelu_gelu"].resized(N=1, H=9, W=128, Cout=40),      # per-channel stores skip padding
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 

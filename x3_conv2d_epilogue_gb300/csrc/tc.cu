@@ -80,7 +80,8 @@ struct Cfg {
     const float *x, *b, *wpack;
     float *out;
     unsigned *err;
-    int N, Cin, H, W, Cout, Ho, Wo;
+    int N, Cin, H, W, Cout, Ho, Wo;  // Cout: the GEMM's (64 or 128); Co: the problem's (<= Cout)
+    int Co;
     int S, P, U, RU, Rin, PL, ucol;
     uint32_t p_magic;  // ceil(2^32 / P): exact q / P for q < 2^16
     int chunks, units_per_img, total_units;
@@ -750,16 +751,21 @@ __device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, const f
             const int c2 = 2 * (lane & 7);
             const float *src = stg + (lane >> 3) * kStgPitch + c2;
             float *dst = orow + col0;
+            // rp < nrp: this lane's channels cb + 4 rp below Co (all 8 unless the GEMM is padded)
+            const int cb0 = (qd * 32) % a.Cout + (lane >> 3);
+            const int nrp = a.Co >= a.Cout ? 8 : max(0, min(8, (a.Co - cb0 + 3) >> 2));
             if ((a.Wo & 1) == 0) {
                 if (col0 + c2 < a.Wo) {
 #pragma unroll
                     for (int rp = 0; rp < 8; ++rp)
-                        *reinterpret_cast<float2 *>(dst + rp * cstride4) =
-                            *reinterpret_cast<const float2 *>(src + 4 * rp * kStgPitch);
+                        if (rp < nrp)
+                            *reinterpret_cast<float2 *>(dst + rp * cstride4) =
+                                *reinterpret_cast<const float2 *>(src + 4 * rp * kStgPitch);
                 }
             } else {
 #pragma unroll
                 for (int rp = 0; rp < 8; ++rp) {
+                    if (rp >= nrp) break;
                     if (col0 + c2 < a.Wo) dst[rp * cstride4] = src[4 * rp * kStgPitch];
                     if (col0 + c2 + 1 < a.Wo) dst[rp * cstride4 + 1] = src[4 * rp * kStgPitch + 1];
                 }
@@ -779,16 +785,21 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int hc = ew >> 2;           // column group: chunks cc = hc, hc + 2, ...
     const int L = qd * 32 + lane;     // accumulator row
     const int slot = L / a.Cout, co = L % a.Cout;
-    const float bias = __ldg(&a.b[co]);
+    const bool real = co < a.Co;      // channels Co..Cout-1 pad the GEMM (zero filters)
+    const float bias = real ? __ldg(&a.b[co]) : 0.0f;
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
-    const float mult = KIND == CONV_EPI_MUL_LRELU_GELU ? __ldg(&a.chan_scale[co]) : 0.0f;
+    const float mult = KIND == CONV_EPI_MUL_LRELU_GELU && real ? __ldg(&a.chan_scale[co]) : 0.0f;
     const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
     // min chains: scalar * bias of the four channels this thread holds in a
     // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4)
     float sb4[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sb4[k] = kMin ? a.scalar * __ldg(&a.b[(qd * 32 + (lane >> 2) + 8 * k) % a.Cout]) : 0.0f;
+    for (int k = 0; k < 4; ++k) {
+        const int ch = (qd * 32 + (lane >> 2) + 8 * k) % a.Cout;
+        // a padding channel never wins the minimum
+        sb4[k] = !kMin ? 0.0f : ch < a.Co ? a.scalar * __ldg(&a.b[ch]) : INFINITY;
+    }
     // per-channel chain: this lane's stores go to channels cb + 4 rp
     const int cb = (qd * 32) % a.Cout + (lane >> 3);
     const size_t plane = (size_t)a.Ho * a.Wo;
@@ -915,7 +926,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // 16-column chunks cc = hc, hc + 2, ...: the load of the next
                 // chunk is in flight while this one is processed
                 const bool row_ok = row < a.Ho;
-                float *orow = a.out + (((size_t)n * a.Cout + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + 2 * (lane & 7);
+                float *orow = a.out + (((size_t)n * a.Co + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + 2 * (lane & 7);
                 const uint32_t tb = tbase + u * a.ucol;
                 int cc = hc;
                 Frag16 cur, nxt;
@@ -1103,10 +1114,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
 // ------------------------------------------------------ filter packing ----
 // wpack[c][kw][jg][p][co][e] = tf32(w[co][8c + 4jg + e][kh][kw]) with
 // kh = S+1-p when 0 <= kh <= 2, else 0 (the zero planes that pad the
-// stacked row slots), and 0 for input channels 8c + 4jg + e >= Cin (the last
+// stacked row slots), 0 for output channels co >= Co (a problem Cout below the
+// GEMM's 64 or 128 is padded with zero filters), and 0 for input channels
+// 8c + 4jg + e >= Cin (the last
 // chunk of a Cin that is not a multiple of 8; the input tile's matching
 // channels arrive as zeros too, from the tensor load's out-of-range fill).
-__global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp, int Cin, int Cout, int S) {
+__global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp, int Cin, int Cout, int Co, int S) {
     const int planes = 2 * S + 1;
     const int Cpad = (Cin + 7) / 8 * 8;
     const size_t total = (size_t)Cpad * 3 * planes * Cout;  // = chunks*3*2*planes*Cout*4
@@ -1125,7 +1138,7 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
         const int kh = S + 1 - p;
         float v = 0.0f;
         const int ci = 8 * c + 4 * jg + e;
-        if (kh >= 0 && kh <= 2 && ci < Cin) v = w[(((size_t)co * Cin + ci) * 3 + kh) * 3 + kw];
+        if (kh >= 0 && kh <= 2 && ci < Cin && co < Co) v = w[(((size_t)co * Cin + ci) * 3 + kh) * 3 + kw];
         wp[i] = __uint_as_float(f32_to_tf32(v));
     }
 }
@@ -1156,10 +1169,15 @@ uint32_t up1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 
 // Shared memory: [filter: resident or ring][B ring][staged-tile ring][mbarriers,
 // tmem slot, abort flag][epilogue scratch]
+// the GEMM's output-channel count: a problem Cout up to 64 runs as 64 (two
+// stacked row slots), up to 128 as 128, with zero filters for the rest
+int gemm_cout(int Cout) { return Cout <= 64 ? 64 : 128; }
+
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
-    if (!(d.Cout == 64 || d.Cout == 128)) return false;
+    if (d.Cout < 1 || d.Cout > 128) return false;
     if (d.Cin < 1 || d.W % 4 != 0 || d.W > 256 || d.H < 3) return false;
-    pl.S = 128 / d.Cout;
+    const int Cg = gemm_cout(d.Cout);
+    pl.S = 128 / Cg;
     pl.P = (d.W + 15) / 16 * 16;
     pl.ucol = (pl.P + 31) / 32 * 32;
     pl.U = kAccStride / pl.ucol;
@@ -1170,7 +1188,7 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.chunks = (d.Cin + 7) / 8;  // the last chunk of a Cin not a multiple of 8 is zero-padded
     if (pl.PL >= (1 << 16)) return false;
     if (2 * pl.Rin * ((pl.P + 31) / 32) > kConvItems * kConvWarps) return false;  // converter items per chunk
-    pl.a_bytes = up1k(3u * 2u * (2 * pl.S + 1) * d.Cout * 16u);
+    pl.a_bytes = up1k(3u * 2u * (2 * pl.S + 1) * Cg * 16u);
     pl.b_bytes = up1k(2u * pl.PL * 16u);
     pl.raw_bytes = up1k(8u * pl.Rin * d.W * 4u);
     pl.scratch_bytes = scratch_bytes_for(kind, pl.U, pl.P);
@@ -1249,8 +1267,8 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
 }
 
 size_t tc_wpack_bytes(const conv_epi_desc &d) {
-    const int S = d.Cout >= 128 ? 1 : 2;
-    const size_t chunk = ((size_t)3 * 2 * (2 * S + 1) * d.Cout * 16 + 1023) & ~(size_t)1023;
+    const int Cg = gemm_cout(d.Cout), S = 128 / Cg;
+    const size_t chunk = ((size_t)3 * 2 * (2 * S + 1) * Cg * 16 + 1023) & ~(size_t)1023;
     return (size_t)((d.Cin + 7) / 8 + 1) * chunk + 256;
 }
 
@@ -1283,16 +1301,16 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     }
     // 1) pack the filter for this call: chunk c at byte offset c * a_bytes
     {
-        const size_t per_chunk = (size_t)3 * 2 * (2 * pl.S + 1) * d.Cout * 4;  // floats
+        const size_t per_chunk = (size_t)3 * 2 * (2 * pl.S + 1) * gemm_cout(d.Cout) * 4;  // floats
         const size_t total = (size_t)pl.chunks * per_chunk;
         const int threads = 256;
         const int blocks = (int)((total + threads - 1) / threads);
         if (pl.a_bytes != per_chunk * 4) return CONV_EPI_ERR_UNSUPPORTED;  // chunks must pack back to back
-        pack_weights<<<blocks, threads, 0, s>>>(w, h->wpack, d.Cin, d.Cout, pl.S);
+        pack_weights<<<blocks, threads, 0, s>>>(w, h->wpack, d.Cin, gemm_cout(d.Cout), d.Cout, pl.S);
         CE_CUDA(cudaGetLastError());
     }
     a.x = x, a.b = b, a.wpack = h->wpack, a.out = out, a.err = h->dev_err;
-    a.N = d.N, a.Cin = d.Cin, a.H = d.H, a.W = d.W, a.Cout = d.Cout, a.Ho = h->Ho, a.Wo = h->Wo;
+    a.N = d.N, a.Cin = d.Cin, a.H = d.H, a.W = d.W, a.Cout = gemm_cout(d.Cout), a.Co = d.Cout, a.Ho = h->Ho, a.Wo = h->Wo;
     a.S = pl.S, a.P = pl.P, a.U = pl.U, a.RU = pl.RU, a.Rin = pl.Rin, a.PL = pl.PL, a.ucol = pl.ucol;
     a.p_magic = (uint32_t)((((uint64_t)1 << 32) + pl.P - 1) / pl.P);
     a.chunks = pl.chunks;
@@ -1303,7 +1321,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.raw_tx = 8u * pl.Rin * d.W * 4u;
     a.a_off = pl.a_off, a.b_off = pl.b_off, a.raw_off = pl.raw_off, a.bar_off = pl.bar_off;
     a.scratch_off = pl.scratch_off;
-    a.a_plane_bytes = (uint32_t)d.Cout * 16u;
+    a.a_plane_bytes = (uint32_t)a.Cout * 16u;
     a.a_lbo = (uint32_t)(2 * pl.S + 1) * a.a_plane_bytes;
     a.a_kw_stride = 2u * a.a_lbo;
     a.idesc = make_idesc(128, pl.P);
