@@ -14,6 +14,10 @@ Prints ONE JSON line (rank 0).  Metric: TFLOP/s = 2*N*Cout*Ho*Wo*Cin*9 / time.
                the measured bf16 peak (x 1.1/2.25, the nominal tf32:bf16 ratio)
   cpu_baseline - the fp64 oracle on the host cores over a bounded sample
   clocks     - nvidia-smi samples taken during the timed region
+  unfused    - context only, off the measured path: the unfused pipeline the
+               pages start from (PyTorch conv2d on cuDNN, the full conv output
+               written to HBM, then the chain as PyTorch ops), same inputs,
+               same arithmetic mode, timed the same way
 
 ``--impl reference`` times the oracle instead (the only reference this
 method has), on the same workload and metric, one bounded sample per step.
@@ -167,6 +171,45 @@ def oracle_sample(wl, seconds: float, max_images: int):
     return conv_flops(one) * done / el / 1e12, el, done, cores
 
 
+def unfused_chain(wl, dev, mode_tf32: bool):
+    """The unfused pipeline as a PyTorch function of the resident inputs:
+    conv2d (cuDNN; tf32 allowed only in the tf32 mode) writing the full conv
+    output, then the chain in PyTorch ops."""
+    import torch
+    import torch.nn.functional as F
+    torch.backends.cudnn.allow_tf32 = mode_tf32
+    torch.backends.cuda.matmul.allow_tf32 = mode_tf32
+    x, w, b = dev["x"], dev["w"], dev["b"]
+
+    def run():
+        y = F.conv2d(x, w, b)
+        if wl.kind == synth.KIND_MIN_TANH2:
+            return torch.tanh(torch.tanh(torch.min(y * wl.scalar, dim=1, keepdim=True)[0]))
+        if wl.kind == synth.KIND_SCALE_MIN:
+            return torch.min(y * wl.scalar, dim=1, keepdim=True)[0]
+        if wl.kind == synth.KIND_MUL_LRELU_GELU:
+            return F.gelu(F.leaky_relu(y * dev["mult"].view(1, -1, 1, 1), wl.lrelu_slope))
+        z = F.group_norm(y, wl.groups, dev["gamma"], dev["beta"], wl.eps) * dev["scale"].view(1, -1, 1, 1)
+        return torch.clamp(F.max_pool2d(z, wl.pool_k), wl.clamp_lo, wl.clamp_hi)
+    return run
+
+
+def time_unfused(wl, dev, mode_tf32: bool, steps: int, warmup: int, stream):
+    import torch
+    run = unfused_chain(wl, dev, mode_tf32)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def traffic_for(kernel_src_hash: str, workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -226,6 +269,7 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=15.0, help="oracle sample length per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--no-unfused", action="store_true", help="skip the unfused PyTorch/cuDNN comparison (context only)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -312,6 +356,17 @@ def main(argv=None):
 
     ce.conv_epi_destroy(h)
 
+    # ---- context: the unfused pipeline on the same inputs (not the product) ----
+    unfused = None
+    if not args.no_unfused and rank == 0:
+        del out
+        torch.cuda.empty_cache()
+        u_ms = time_unfused(wl, dev, args.mode == "tf32", min(args.steps, 10), 3, stream)
+        unfused = {"value": flops / (u_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": u_ms,
+                   "fused_speedup": u_ms / kern_ms,
+                   "kind": "PyTorch conv2d (cuDNN, full conv output to HBM) + the chain as PyTorch ops; "
+                           "context only, not on the measured path"}
+
     if rank != 0:
         return 0
 
@@ -337,6 +392,7 @@ def main(argv=None):
                      "hbm_gbs": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm,
                      "hbm_frac": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9 / hbm},
         "cpu_baseline": cpu,
+        "unfused": unfused,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
