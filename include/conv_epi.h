@@ -166,6 +166,18 @@ CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_desc *desc,
  * kernels raised on this handle since the last call (then clear it). */
 CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream);
 
+/* Test hook for the bounded barrier waits (tf32 mode only).  The next
+ * conv_epi_forward on this handle has each CTA's producer skip one copy: the
+ * staged input tile with index `tile` in that CTA's own sequence (0 = its
+ * first).  The copy is neither issued nor announced on its barrier, so the
+ * converters waiting on that slot give up after the wait limit (2 s), raise
+ * the timeout bit and every role of the CTA drains and returns;
+ * conv_epi_sync() then reports CONV_EPI_ERR_TIMEOUT and the context stays
+ * usable.  The output of that forward is undefined.  tile = -1 cancels; the
+ * setting applies to one forward only.  Returns CONV_EPI_ERR_UNSUPPORTED on
+ * an fp32-mode handle (whose kernels have no barrier rings). */
+CONV_EPI_API conv_epi_status conv_epi_test_drop_tile(conv_epi_handle h, int tile);
+
 /* Release the handle and its workspace (synchronises the device first). */
 CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h);
 

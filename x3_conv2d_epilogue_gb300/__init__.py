@@ -78,6 +78,7 @@ def _lib():
             L.conv_epi_forward_host.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_forward_noalloc.argtypes = [C.POINTER(Desc), P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_sync.argtypes = [P, P]
+            L.conv_epi_test_drop_tile.argtypes = [P, I]
             L.conv_epi_destroy.argtypes = [P]
             L.conv_epi_workspace_bytes.argtypes = [P]
             L.conv_epi_workspace_bytes.restype = C.c_size_t
@@ -169,6 +170,12 @@ def conv_epi_forward_noalloc(N, Cin, H, W, Cout, x, w, b, epi, out, stream=None,
 
 def conv_epi_sync(h, stream=None):
     _check(_lib().conv_epi_sync(h, _stream(stream)), "conv_epi_sync")
+
+
+def conv_epi_test_drop_tile(h, tile):
+    """Test hook: the next tf32 forward on ``h`` skips staged tile ``tile`` of
+    every CTA's sequence, so its bounded waits time out (-1 cancels)."""
+    _check(_lib().conv_epi_test_drop_tile(h, tile), "conv_epi_test_drop_tile")
 
 
 def conv_epi_destroy(h):

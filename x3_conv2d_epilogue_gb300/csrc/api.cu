@@ -282,6 +282,13 @@ CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream) {
     return CONV_EPI_OK;
 }
 
+CONV_EPI_API conv_epi_status conv_epi_test_drop_tile(conv_epi_handle h, int tile) {
+    if (!h || tile < -1) return CONV_EPI_ERR_INVALID_ARG;
+    if (h->d.mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;
+    h->test_drop_tile = tile;
+    return CONV_EPI_OK;
+}
+
 CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
     if (!h) return CONV_EPI_ERR_INVALID_ARG;
     cudaSetDevice(h->device);

@@ -60,6 +60,9 @@ struct conv_epi_handle_s {
     size_t stage_bytes = 0;
 
     int last_launches = 0;
+
+    // conv_epi_test_drop_tile: the next tf32 forward skips this staged tile
+    int test_drop_tile = -1;
 };
 
 namespace conv_epi {

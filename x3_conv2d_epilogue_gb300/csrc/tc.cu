@@ -96,6 +96,7 @@ struct Cfg {
     float slope;
     int groups, Hp, Wp;
     GnWork gn;
+    int drop_tile;  // test hook: per-CTA staged-tile index the producer never issues (-1: none)
 };
 
 struct TcArgs {        // 64-byte aligned through CUtensorMap
@@ -470,9 +471,15 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
         const bool tiles_only = ia >= total;
         if (tiles_only && !wait_bar(bars.r_empty(sr), pr ^ 1, abort_flag, a.err)) break;
         if (ir < total && (tiles_only || mbar_try_wait(bars.r_empty(sr), pr ^ 1))) {
-            mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
-            tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, pos.ru * a.RU, 8 * cr, pos.n, bars.r_full(sr));
-            r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
+            if (ir != a.drop_tile) {
+                mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
+                tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, pos.ru * a.RU, 8 * cr, pos.n, bars.r_full(sr));
+                r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
+            } else {
+                // test hook: this slot's phase never completes, so its
+                // consumers' bounded waits run out; nothing is in flight here
+                r_iss &= ~(1u << sr);
+            }
             if (++sr == a.nr) sr = 0, pr ^= 1u;
             if (++cr == a.chunks) cr = 0, pos.step(gridDim.x, a.units_per_img);
             ++ir;
@@ -1327,6 +1334,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.idesc = make_idesc(128, pl.P);
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
+    a.drop_tile = h->test_drop_tile;
+    h->test_drop_tile = -1;  // one forward only
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
