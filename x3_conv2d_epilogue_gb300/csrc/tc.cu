@@ -20,10 +20,11 @@
 //
 // Input path.  The TMA engine loads each raw NCHW tile (8 channels x the
 // unit's input rows x W) into a ring of staging buffers, zero-filling rows past
-// the image.  Converter warps transpose a staged tile shared->shared into the
-// B plane (4x4 register transposes, tf32 round-to-nearest), so their
-// proxy fence before handing the plane to the tensor core covers only short
-// shared-memory stores -- never global loads in flight.
+// the image.  Converter warps rewrite a staged tile shared->shared into the
+// B plane (each lane gathers one position's four channels, rounds them to
+// tf32 and stores one 16-byte plane row), so their proxy fence before handing
+// the plane to the tensor core covers only short shared-memory stores --
+// never global loads in flight.
 //
 // Row slots.  The MMA's M is 128.  With Cout = 128 a tile is one output row
 // per accumulator.  With Cout = 64 the 128 accumulator lanes hold TWO output
