@@ -216,6 +216,26 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// two fp32 values as one 64-bit register pair, and the packed fp32x2 FMA
+// d = a * b + c on such pairs (both halves rounded to nearest)
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+// minimum of three (NaN operands are ignored, as by fminf)
+__device__ __forceinline__ float fmin3(float x, float y, float z) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+    return r;
+}
 // arrive on `bar` once every MMA this thread issued before has completed
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -667,17 +687,21 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, cons
 // that keeps the opposite half) and a plain exchange over bit 2: four
 // shuffles for 16 columns.  Lane l ends with column
 // 8*bit4(l) + 2*(l & 3) + bit3(l), which lanes l and l ^ 4 share.
-// in-register step: this thread's four channels, columns 2m, 2m+1, 8+2m, 9+2m
-__device__ __forceinline__ float4 colmin16_own(const Frag16 &f, float s, const float (&sb)[4]) {
+// in-register step: this thread's four channels, columns 2m, 2m+1, 8+2m, 9+2m.
+// A channel's two adjacent columns sit in an even/odd register pair, so the
+// scale and bias go in with one packed fp32x2 FMA per pair (ss = (s, s),
+// sb2[k] = (sb[k], sb[k])).
+__device__ __forceinline__ float4 colmin16_own(const Frag16 &f, uint64_t ss, const uint64_t (&sb2)[4]) {
     float c[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int b = (j >> 1) * 4 + (j & 1);  // register of channel 0 at column j
-        const float x0 = fmaf(__uint_as_float(f.r[b]), s, sb[0]);
-        const float x1 = fmaf(__uint_as_float(f.r[b + 2]), s, sb[1]);
-        const float x2 = fmaf(__uint_as_float(f.r[b + 8]), s, sb[2]);
-        const float x3 = fmaf(__uint_as_float(f.r[b + 10]), s, sb[3]);
-        c[j] = fminf(fminf(x0, x1), fminf(x2, x3));
+    for (int h = 0; h < 2; ++h) {              // columns 2m, 2m+1 (h = 0) and 8+2m, 9+2m (h = 1)
+        const int b = 4 * h;                   // registers of channel 0
+        const float2 x0 = fma2(pack2(f.r[b], f.r[b + 1]), ss, sb2[0]);
+        const float2 x1 = fma2(pack2(f.r[b + 2], f.r[b + 3]), ss, sb2[1]);
+        const float2 x2 = fma2(pack2(f.r[b + 8], f.r[b + 9]), ss, sb2[2]);
+        const float2 x3 = fma2(pack2(f.r[b + 10], f.r[b + 11]), ss, sb2[3]);
+        c[2 * h] = fminf(fmin3(x0.x, x1.x, x2.x), x3.x);
+        c[2 * h + 1] = fminf(fmin3(x0.y, x1.y, x2.y), x3.y);
     }
     return make_float4(c[0], c[1], c[2], c[3]);
 }
@@ -727,25 +751,17 @@ __device__ __forceinline__ float tanh_exp(float x) {
 // GELU with the exact-erf form 0.5 t (1 + erf(t / sqrt 2))
 __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erf_as7126(t * 0.70710678118654752f)); }
 
-// Per-chunk work of the min / per-channel chains on 16 accumulator columns.
-// Min chains: f is a tmem_ld16_rows4_issue fragment and sb[k] = scalar * bias
-// of the thread's k-th channel.  Per-channel chain: f is a 32x32b fragment
-// (one channel per lane, 16 columns) and orow points at this lane's first
-// output column of the lane group's first channel in the current row.
-template <int KIND>
-__device__ __forceinline__ void epi_chunk(const Cfg &a, const Frag16 &f, const float (&sb)[4], float bias, float mult,
-                                          int lane, int qd, int ew, int u, bool row_ok, int col0, float *orow,
-                                          size_t cstride4, float *scratch) {
-    if (KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN) {
-        // the chain's minimum over channels of scalar * y: the scalar goes in
-        // first, so a negative scalar needs no separate max
-        const float m = colmin16_lanes(colmin16_own(f, a.scalar, sb), lane);
-        if ((lane & 4) == 0) scratch[(u * 4 + qd) * a.P + colmin16_col(col0, lane)] = m;
-    } else {
-        // per-channel chain: transpose 32 channels x 16 columns through shared
-        // memory so each store instruction writes 4 channel rows of 64
-        // contiguous bytes; lane l stores columns c2, c2+1 (c2 = 2 (l & 7)) of
-        // channels l/8 + 4 rp, rp = 0..7
+// Per-chunk work of the per-channel chain on 16 accumulator columns: f is a
+// 32x32b fragment (one channel per lane, 16 columns) and orow points at this
+// lane's first output column of the lane group's first channel in the
+// current row.  The 32 channels x 16 columns are transposed through shared
+// memory so each store instruction writes 4 channel rows of 64 contiguous
+// bytes; lane l stores columns c2, c2+1 (c2 = 2 (l & 7)) of channels
+// l/8 + 4 rp, rp = 0..7.
+__device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, float bias, float mult, int lane, int qd,
+                                               int ew, bool row_ok, int col0, float *orow, size_t cstride4,
+                                               float *scratch) {
+    {
         float *stg = scratch + ew * 32 * kStgPitch;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
@@ -800,14 +816,19 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const float mult = KIND == CONV_EPI_MUL_LRELU_GELU && real ? __ldg(&a.chan_scale[co]) : 0.0f;
     const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
     // min chains: scalar * bias of the four channels this thread holds in a
-    // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4)
-    float sb4[4];
+    // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4),
+    // each duplicated into a register pair, and the scalar likewise.  The
+    // chain's minimum over channels is of scalar * y: the scalar goes in
+    // first, so a negative scalar needs no separate max.
+    uint64_t sb2[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int ch = (qd * 32 + (lane >> 2) + 8 * k) % a.Cout;
         // a padding channel never wins the minimum
-        sb4[k] = !kMin ? 0.0f : ch < a.Co ? a.scalar * __ldg(&a.b[ch]) : INFINITY;
+        const float v = !kMin ? 0.0f : ch < a.Co ? a.scalar * __ldg(&a.b[ch]) : INFINITY;
+        sb2[k] = pack2(__float_as_uint(v), __float_as_uint(v));
     }
+    const uint64_t ss = pack2(__float_as_uint(a.scalar), __float_as_uint(a.scalar));
     // per-channel chain: this lane's stores go to channels cb + 4 rp
     const int cb = (qd * 32) % a.Cout + (lane >> 3);
     const size_t plane = (size_t)a.Ho * a.Wo;
@@ -820,6 +841,45 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int gn_cpg = kGN ? a.Cout / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
     float *gn_sgn = scratch + 2 * 64 * kPoolPitch + 2 * kEpiThreads;
     if (kGN && slot == 0) gn_sgn[co] = gsg;
+    // Min chains: the cross-quadrant combine of a unit's partial minima, the
+    // chain's tail and the row stores.  Every partial of a column (each row of
+    // the unit, each quadrant) is loaded before any is used: under the tensor
+    // core's operand traffic a shared-memory load waits long, so the loads go
+    // out together instead of one row after another.  Scratch row k of the
+    // unit (k = u * 4 + quadrant) holds quadrant partials; row slot s of u
+    // uses quadrants s * qps .. s * qps + qps - 1.
+    auto combine_min = [&](int pn, int pr0) {
+        const int qps = 4 / a.S;  // quadrants per slot
+        const int nq = a.U * 4;   // scratch rows of the unit (<= 32)
+        float *orow0 = a.out + ((size_t)pn * a.Ho + pr0) * a.Wo;
+        for (int col = et; col < a.Wo; col += kEpiThreads)
+            for (int kb = 0; kb < nq; kb += kMaxQ) {  // two u at a time (nq is a multiple of 4)
+                float pv[kMaxQ];
+#pragma unroll
+                for (int k = 0; k < kMaxQ; ++k)
+                    if (kb + k < nq) pv[k] = scratch[(kb + k) * a.P + col];
+#pragma unroll
+                for (int k = 0; k < kMaxQ; k += 4) {
+                    if (kb + k >= nq) break;
+                    // the 4 quadrants of u = (kb + k) / 4: one row (qps = 4) or two (qps = 2)
+                    const int u = (kb + k) >> 2;
+                    if (qps == 4) {
+                        const int row = pr0 + u;
+                        float o = fmin3(pv[k], pv[k + 1], pv[k + 2]);
+                        o = fminf(o, pv[k + 3]);
+                        if (KIND == CONV_EPI_MIN_TANH2) o = tanh_exp(tanh_exp(o));
+                        if (row < a.Ho) orow0[(size_t)(u) * a.Wo + col] = o;
+                    } else {
+                        const int row = pr0 + 2 * u;
+                        float o0 = fminf(pv[k], pv[k + 1]), o1 = fminf(pv[k + 2], pv[k + 3]);
+                        if (KIND == CONV_EPI_MIN_TANH2) o0 = tanh_exp(tanh_exp(o0)), o1 = tanh_exp(tanh_exp(o1));
+                        if (row < a.Ho) orow0[(size_t)(2 * u) * a.Wo + col] = o0;
+                        if (row + 1 < a.Ho) orow0[(size_t)(2 * u + 1) * a.Wo + col] = o1;
+                    }
+                }
+            }
+    };
+    int prev_n = -1, prev_r0 = 0;  // min chains: the unit whose combine is still due
     int j = 0;
     UnitPos pos;
     pos.init(blockIdx.x, a.units_per_img);
@@ -829,7 +889,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         const int r0 = ru * a.RU;
         const int ab = j & 1;
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
-        if (epi_bar_any(!ok)) break;  // all epilogue warps leave together
+        if (epi_bar_any(!ok)) {  // all epilogue warps leave together
+            prev_n = -1;
+            break;
+        }
         tc_fence_after();
         const uint32_t tbase = tmem + lane_off + ab * kAccStride;
 
@@ -903,13 +966,21 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     if (c0 + 3 < nchunks) tmem_ld16_rows4_issue(tb + (c0 + 3) * 16, f3);
                 };
                 int q = hc;
+                Frag16 f0, f1, f2, f3;
+                if (q < nbt) load(q, f0, f1, f2, f3);
+                if (u == 0) {
+                    // the previous unit's combine runs while these loads are
+                    // in flight (its partials were made visible by the barrier
+                    // at the top of this unit); the barrier after it keeps this
+                    // unit's partial stores behind every thread's reads
+                    if (prev_n >= 0) combine_min(prev_n, prev_r0);
+                    epi_bar();
+                }
                 if (q < nbt) {
-                    Frag16 f0, f1, f2, f3;
-                    load(q, f0, f1, f2, f3);
                     tmem_ld_wait2(f0, f1);
                     tmem_ld_wait2(f2, f3);
-                    float4 c0 = colmin16_own(f0, a.scalar, sb4), c1 = colmin16_own(f1, a.scalar, sb4);
-                    float4 c2 = colmin16_own(f2, a.scalar, sb4), c3 = colmin16_own(f3, a.scalar, sb4);
+                    float4 c0 = colmin16_own(f0, ss, sb2), c1 = colmin16_own(f1, ss, sb2);
+                    float4 c2 = colmin16_own(f2, ss, sb2), c3 = colmin16_own(f3, ss, sb2);
                     for (;;) {
                         const bool more = q + 2 < nbt;
                         if (more) load(q + 2, f0, f1, f2, f3);
@@ -926,8 +997,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         q += 2;
                         tmem_ld_wait2(f0, f1);
                         tmem_ld_wait2(f2, f3);
-                        c0 = colmin16_own(f0, a.scalar, sb4), c1 = colmin16_own(f1, a.scalar, sb4);
-                        c2 = colmin16_own(f2, a.scalar, sb4), c3 = colmin16_own(f3, a.scalar, sb4);
+                        c0 = colmin16_own(f0, ss, sb2), c1 = colmin16_own(f1, ss, sb2);
+                        c2 = colmin16_own(f2, ss, sb2), c3 = colmin16_own(f3, ss, sb2);
                     }
                 }
             } else {
@@ -945,7 +1016,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 for (; cc < nchunks; cc += 2) {
                     const bool more = cc + 2 < nchunks;
                     if (more) tmem_ld16_issue(tb + (cc + 2) * 16, nxt);
-                    epi_chunk<KIND>(a, cur, sb4, bias, mult, lane, qd, ew, u, row_ok, cc * 16, orow, cstride4, scratch);
+                    epi_chunk_chan(a, cur, bias, mult, lane, qd, ew, row_ok, cc * 16, orow, cstride4, scratch);
                     if (more) {
                         tmem_ld_wait(nxt);
                         cur = nxt;
@@ -959,44 +1030,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         if (lane == 0) mbar_arrive(bars.acc_empty(ab));
 
         if constexpr (kMin) {
-            // every warp's partial minima of this unit are in scratch; the
-            // barrier at the start of the next unit keeps them there until all
-            // threads are done reading
-            epi_bar();
-            // Every partial of a column (each row of the unit, each quadrant)
-            // is loaded before any is used: under the tensor core's operand
-            // traffic a shared-memory load waits long, so the loads go out
-            // together instead of one row after another.  Scratch row k of
-            // the unit (k = u * 4 + quadrant) holds quadrant partials; row
-            // slot s of u uses quadrants s * qps .. s * qps + qps - 1.
-            const int qps = 4 / a.S;  // quadrants per slot
-            const int nq = a.U * 4;   // scratch rows of the unit (<= 32)
-            float *orow0 = a.out + ((size_t)n * a.Ho + r0) * a.Wo;
-            for (int col = et; col < a.Wo; col += kEpiThreads)
-              for (int kb = 0; kb < nq; kb += kMaxQ) {  // two u at a time (nq is a multiple of 4)
-                float pv[kMaxQ];
-#pragma unroll
-                for (int k = 0; k < kMaxQ; ++k)
-                    if (kb + k < nq) pv[k] = scratch[(kb + k) * a.P + col];
-#pragma unroll
-                for (int k = 0; k < kMaxQ; k += 4) {
-                    if (kb + k >= nq) break;
-                    // the 4 quadrants of u = (kb + k) / 4: one row (qps = 4) or two (qps = 2)
-                    const int u = (kb + k) >> 2;
-                    if (qps == 4) {
-                        const int row = r0 + u;
-                        float o = fminf(fminf(pv[k], pv[k + 1]), fminf(pv[k + 2], pv[k + 3]));
-                        if (KIND == CONV_EPI_MIN_TANH2) o = tanh_exp(tanh_exp(o));
-                        if (row < a.Ho) orow0[(size_t)(u) * a.Wo + col] = o;
-                    } else {
-                        const int row = r0 + 2 * u;
-                        float o0 = fminf(pv[k], pv[k + 1]), o1 = fminf(pv[k + 2], pv[k + 3]);
-                        if (KIND == CONV_EPI_MIN_TANH2) o0 = tanh_exp(tanh_exp(o0)), o1 = tanh_exp(tanh_exp(o1));
-                        if (row < a.Ho) orow0[(size_t)(2 * u) * a.Wo + col] = o0;
-                        if (row + 1 < a.Ho) orow0[(size_t)(2 * u + 1) * a.Wo + col] = o1;
-                    }
-                }
-            }
+            // this unit's partial minima are in scratch; they are combined
+            // during the next unit's first tensor-memory loads (or after the
+            // loop, for the last unit)
+            prev_n = n, prev_r0 = r0;
         } else if constexpr (kGN) {
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
@@ -1048,6 +1085,12 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         *dst = gn_sgn[c2] * fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]);
             }
             // (the barrier at the start of the next unit keeps the tile until all stores have read it)
+        }
+    }
+    if constexpr (kMin) {
+        if (prev_n >= 0) {  // the last unit's combine
+            epi_bar();
+            combine_min(prev_n, prev_r0);
         }
     }
 }
