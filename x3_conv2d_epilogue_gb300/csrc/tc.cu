@@ -223,17 +223,31 @@ __device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
     return r;
 }
-__device__ __forceinline__ float2 fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
     float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
     return r;
 }
-// minimum of three (NaN operands are ignored, as by fminf)
+__device__ __forceinline__ uint64_t fma2u(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2u(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float2 fma2(uint64_t a, uint64_t b, uint64_t c) { return unpack2(fma2u(a, b, c)); }
+// minimum / maximum of three (NaN operands are ignored, as by fminf / fmaxf)
 __device__ __forceinline__ float fmin3(float x, float y, float z) {
     float r;
     asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float x, float y, float z) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
     return r;
 }
 // arrive on `bar` once every MMA this thread issued before has completed
@@ -815,6 +829,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
     const float mult = KIND == CONV_EPI_MUL_LRELU_GELU && real ? __ldg(&a.chan_scale[co]) : 0.0f;
     const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
+    const uint64_t gg2 = pack2(__float_as_uint(gsg), __float_as_uint(gsg));
+    const uint64_t gb2 = pack2(__float_as_uint(gsg * bias), __float_as_uint(gsg * bias));
     // min chains: scalar * bias of the four channels this thread holds in a
     // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4),
     // each duplicated into a register pair, and the scalar likewise.  The
@@ -903,7 +919,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         // negative (rstd > 0, so the sign is known before the statistics).
         constexpr int kMaxWin = 16;
         float pext[kMaxWin];
-        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f}, lss[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains each
+        // sums of w and w^2 in four chains each (two packed pairs)
+        uint64_t ls2[2] = {0ull, 0ull}, lss2[2] = {0ull, 0ull};
         if constexpr (kGN) {
 #pragma unroll
             for (int k = 0; k < kMaxWin; ++k) pext[k] = -INFINITY;
@@ -924,28 +941,32 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         const int cc = hc + 2 * kc;
                         if (cc >= nchunks) continue;
                         const int col0 = cc * 16;
-                        float v[16];
+                        // w = gsg * y = gsg * acc + gsg * bias (the sign flip is
+                        // exact, so w is -y or y rounded once), two adjacent
+                        // columns per packed FMA
+                        uint64_t w2[8];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(f[kc].r[i]) + bias;
-                        if (col0 + 16 <= a.Wo) {  // whole chunk inside the row
+                        for (int p = 0; p < 8; ++p) w2[p] = fma2u(pack2(f[kc].r[2 * p], f[kc].r[2 * p + 1]), gg2, gb2);
+                        if (col0 + 16 > a.Wo) {  // the row's ragged end: columns >= Wo add nothing
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                ls[i & 3] += v[i];
-                                lss[i & 3] = fmaf(v[i], v[i], lss[i & 3]);
+                            for (int p = 0; p < 8; ++p) {
+                                const float2 w = unpack2(w2[p]);
+                                w2[p] = pack2(__float_as_uint(col0 + 2 * p < a.Wo ? w.x : 0.0f),
+                                              __float_as_uint(col0 + 2 * p + 1 < a.Wo ? w.y : 0.0f));
                             }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (col0 + i < a.Wo) {
-                                    ls[i & 3] += v[i];
-                                    lss[i & 3] = fmaf(v[i], v[i], lss[i & 3]);
-                                }
                         }
+                        // column i feeds chain i & 3: pair p's halves go to
+                        // chains 2 (p & 1) and 2 (p & 1) + 1
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            ls2[p & 1] = add2u(ls2[p & 1], w2[p]);
+                            lss2[p & 1] = fma2u(w2[p], w2[p], lss2[p & 1]);
+                        }
+                        // window extremes (windows past Wp are never stored)
 #pragma unroll
                         for (int wi = 0; wi < 4; ++wi) {
-                            const float m01 = fmaxf(gsg * v[4 * wi], gsg * v[4 * wi + 1]);
-                            const float m23 = fmaxf(gsg * v[4 * wi + 2], gsg * v[4 * wi + 3]);
-                            pext[4 * kc + wi] = fmaxf(pext[4 * kc + wi], fmaxf(m01, m23));
+                            const float2 a01 = unpack2(w2[2 * wi]), a23 = unpack2(w2[2 * wi + 1]);
+                            pext[4 * kc + wi] = fmax3(fmax3(a01.x, a01.y, a23.x), a23.y, pext[4 * kc + wi]);
                         }
                     }
                 }
@@ -1037,7 +1058,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         } else if constexpr (kGN) {
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
-            float gs = (ls[0] + ls[1]) + (ls[2] + ls[3]), gss = (lss[0] + lss[1]) + (lss[2] + lss[3]);
+            const float2 l0 = unpack2(ls2[0]), l1 = unpack2(ls2[1]), q0 = unpack2(lss2[0]), q1 = unpack2(lss2[1]);
+            float gs = gsg * ((l0.x + l0.y) + (l1.x + l1.y)), gss = (q0.x + q0.y) + (q1.x + q1.y);  // back to y
             for (int o = 1; o < gn_cw; o <<= 1) {
                 gs += __shfl_xor_sync(0xffffffffu, gs, o);
                 gss += __shfl_xor_sync(0xffffffffu, gss, o);
