@@ -33,6 +33,8 @@ SMALL = {
     "c2co48": W["c2_min_tanh2"].resized(N=1, H=9, Cout=48),                  # Cout padded to 64 (zero filters)
     "c4co100": W["c4_scale_min"].resized(N=1, H=7, W=128, Cout=100, scalar=-0.5),  # padded to 128, max branch
     "c3co40": W["c3_mul_lrelu_gelu"].resized(N=1, H=9, W=128, Cout=40),      # per-channel stores skip padding
+    "c5g1": W["c5_gn_pool_clamp"].resized(N=1, H=22, groups=1),               # one group: 64 channels over two quadrants
+    "c5g4": W["c5_gn_pool_clamp"].resized(N=1, H=18, groups=4),               # 16 channels per group
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 

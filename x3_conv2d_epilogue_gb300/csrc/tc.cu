@@ -1079,32 +1079,47 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             }
             epi_bar();
             if (ew == 2) {
-                // one warp: per group, the shuffled sums from both row slots and
-                // both column groups (fixed order)
+                // one warp: per group, the shuffled sums from both row slots,
+                // both column groups and (cpg = 64: two lane groups) both
+                // halves, loaded together and added in a fixed order
+                const int nci = gn_cpg / gn_cw;  // 1, or 2 when a group spans two warps' lanes
                 for (int g = lane; g < a.groups; g += 32) {
+                    float v0[8], v1[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {  // k = (row slot, column group, half)
+                        const int sl = k >> 2, h2 = (k >> 1) & 1, ci = k & 1;
+                        v0[k] = v1[k] = 0.0f;
+                        if (ci < nci) {
+                            const int LL = sl * a.Cout + g * gn_cpg + ci * gn_cw;
+                            const int e2 = h2 * 4 + (LL >> 5);
+                            v0[k] = st[e2 * 32 + (LL & 31)];
+                            v1[k] = st[kEpiThreads + e2 * 32 + (LL & 31)];
+                        }
+                    }
                     float s0 = 0.0f, s1 = 0.0f;
-                    for (int sl = 0; sl < a.S; ++sl)
-                        for (int h2 = 0; h2 < 2; ++h2)
-                            for (int c2 = g * gn_cpg; c2 < (g + 1) * gn_cpg; c2 += gn_cw) {
-                                const int LL = sl * a.Cout + c2;
-                                const int e2 = h2 * 4 + (LL >> 5);
-                                s0 += st[e2 * 32 + (LL & 31)];
-                                s1 += st[kEpiThreads + e2 * 32 + (LL & 31)];
-                            }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if ((k & 1) < nci) s0 += v0[k], s1 += v1[k];
                     double *dst = a.gn.part + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2;
                     dst[0] = s0;
                     dst[1] = s1;
                 }
             }
-            if (ru < a.Hp) {
-                // warp ew stores channels ew, ew + 8, ...: one pooled row each
-                // (Wp <= 32), the two row slots folded and the sign restored
+            if (ru < a.Hp && lane < a.Wp) {
+                // warp ew stores channels ew, ew + 8, ..., ew + 56: one pooled
+                // row each (Wp <= 32), the two row slots folded and the sign
+                // restored; all sixteen tile reads go out before the stores
                 const float *pt0 = scratch, *pt1 = scratch + 64 * kPoolPitch;
                 float *dst = a.gn.pmax + (((size_t)n * a.Cout + ew) * a.Hp + ru) * a.Wp + lane;
                 const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
-                for (int c2 = ew; c2 < 64; c2 += kEpiWarps, dst += cstep)
-                    if (lane < a.Wp)
-                        *dst = gn_sgn[c2] * fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]);
+                float m[64 / kEpiWarps];
+#pragma unroll
+                for (int i = 0; i < 64 / kEpiWarps; ++i) {
+                    const int c2 = ew + kEpiWarps * i;
+                    m[i] = gn_sgn[c2] * fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]);
+                }
+#pragma unroll
+                for (int i = 0; i < 64 / kEpiWarps; ++i) dst[i * cstep] = m[i];
             }
             // (the barrier at the start of the next unit keeps the tile until all stores have read it)
         }
