@@ -34,7 +34,86 @@ struct GnArgs {
     int32_t *idx;
     int presel;      // 1: pmax already holds the extreme the slope's sign selects
     double inv_cnt;  // 1 / (C/groups * Ho * Wo)
+    uint32_t per_magic;  // ceil(2^32 / (Hp * Wp)): exact f / (Hp * Wp) for f < 2^16
 };
+
+// Mean and rstd of group g of image n from the per-unit partial sums (one
+// warp: fixed order in fp64, lanes take units lane, lane+32, ..., then a fixed
+// shuffle tree); every lane returns the same values.
+__device__ __forceinline__ void group_stats(const GnArgs &a, int n, int g, float &mean_f, float &rstd_f) {
+    const int lane = threadIdx.x & 31;
+    double s = 0.0, ss = 0.0;
+    const double *p = a.gn.part + ((size_t)n * a.gn.units * a.groups + g) * 2;
+    for (int u = lane; u < a.gn.units; u += 32) s += p[(size_t)u * 2 * a.groups], ss += p[(size_t)u * 2 * a.groups + 1];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    }
+    const double mean = s * a.inv_cnt;
+    double var = ss * a.inv_cnt - mean * mean;
+    if (var < 0.0) var = 0.0;
+    mean_f = (float)mean;
+    rstd_f = rsqrtf((float)var + a.eps);
+}
+
+// The tensor-core path's case: pmax holds, per channel, the extreme that the
+// slope's sign selects, and no indices are wanted.  The group's C/groups
+// pooled planes are one contiguous block of F = cpg * Hp * Wp floats (F a
+// multiple of 4, 16-byte aligned: checked on the host), so every thread first
+// issues its 16-byte loads of the block's first 4096 floats, then warp 0
+// computes the statistics and each channel's coefficients while those loads
+// are in flight; one barrier, then z = clamp(A * y + B) and 16-byte stores.
+constexpr int kVec = 4;  // float4 loads in flight per thread
+__global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs a) {
+    constexpr int kMaxCpg = 64;
+    __shared__ float sA[kMaxCpg], sB[kMaxCpg];
+    const int n = blockIdx.x / a.groups, g = blockIdx.x % a.groups;
+    const int cpg = a.C / a.groups;
+    const uint32_t per = (uint32_t)(a.gn.Hp * a.gn.Wp);
+    const size_t base = ((size_t)n * a.C + (size_t)g * cpg) * per;
+    const float4 *__restrict__ src = reinterpret_cast<const float4 *>(a.gn.pmax + base);
+    float4 *__restrict__ dst = reinterpret_cast<float4 *>(a.out + base);
+    const int nv = (int)((size_t)cpg * per / 4);
+    float4 v[kVec];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        if (i < nv) v[k] = src[i];
+    }
+    if (threadIdx.x < 32) {
+        float mean, rstd;
+        group_stats(a, n, g, mean, rstd);
+        for (int cl = threadIdx.x; cl < cpg; cl += 32) {
+            const int c = g * cpg + cl;
+            const float gm = a.gamma[c], sc = a.scale[c];
+            sA[cl] = gm * sc * rstd;
+            sB[cl] = (a.beta[c] - gm * mean * rstd) * sc;
+        }
+    }
+    __syncthreads();
+    auto apply = [&](float y, uint32_t f) {
+        const uint32_t cl = __umulhi(f, a.per_magic);  // f / per
+        return fminf(fmaxf(fmaf(sA[cl], y, sB[cl]), a.lo), a.hi);
+    };
+    for (int i0 = 0; i0 < nv; i0 += kVec * kThreads) {
+        if (i0 > 0) {
+#pragma unroll
+            for (int k = 0; k < kVec; ++k) {
+                const int i = i0 + threadIdx.x + k * kThreads;
+                if (i < nv) v[k] = src[i];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+            const int i = i0 + threadIdx.x + k * kThreads;
+            if (i < nv) {
+                const uint32_t f = 4u * (uint32_t)i;
+                dst[i] = make_float4(apply(v[k].x, f), apply(v[k].y, f + 1), apply(v[k].z, f + 2), apply(v[k].w, f + 3));
+            }
+        }
+    }
+}
 
 // One CTA per (image, group).  Warp 0 folds the group's per-unit partial sums
 // (fixed order, fp64: lanes take units lane, lane+32, ..., then a fixed
@@ -51,22 +130,9 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
     const int n = blockIdx.x / a.groups, g = blockIdx.x % a.groups;
     const int cpg = a.C / a.groups;
     if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        double s = 0.0, ss = 0.0;
-        const double *p = a.gn.part + ((size_t)n * a.gn.units * a.groups + g) * 2;
-        for (int u = lane; u < a.gn.units; u += 32) s += p[(size_t)u * 2 * a.groups], ss += p[(size_t)u * 2 * a.groups + 1];
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            s += __shfl_xor_sync(0xffffffffu, s, off);
-            ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        }
-        if (lane == 0) {
-            const double mean = s * a.inv_cnt;
-            double var = ss * a.inv_cnt - mean * mean;
-            if (var < 0.0) var = 0.0;
-            s_mean = (float)mean;
-            s_rstd = rsqrtf((float)var + a.eps);
-        }
+        float mean, rstd;
+        group_stats(a, n, g, mean, rstd);
+        if (threadIdx.x == 0) s_mean = mean, s_rstd = rstd;
     }
     __syncthreads();
     const float mean = s_mean, rstd = s_rstd;
@@ -121,8 +187,17 @@ conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, 
     a.out = out, a.idx = e.index_out;
     a.presel = presel ? 1 : 0;
     a.inv_cnt = 1.0 / ((double)(a.C / a.groups) * a.Ho * a.Wo);
+    const uint32_t per = (uint32_t)(h->gn.Hp * h->gn.Wp);
+    a.per_magic = (uint32_t)((((uint64_t)1 << 32) + per - 1) / per);
     const unsigned blocks = (unsigned)(a.N * a.groups);
-    gn_finalize_kernel<<<blocks, kThreads, 0, s>>>(a);
+    // the vector kernel: whole group blocks of float4 (F = cpg * per a multiple
+    // of 4 keeps every block 16-byte aligned), flat indices below 2^16 for the
+    // channel division, at most 64 channels per group
+    const size_t F = (size_t)(a.C / a.groups) * per;
+    const bool vec = presel && !e.index_out && F % 4 == 0 && F < (1u << 16) && a.C / a.groups <= 64 &&
+                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0;
+    if (vec) gn_finalize_vec_kernel<<<blocks, kThreads, 0, s>>>(a);
+    else gn_finalize_kernel<<<blocks, kThreads, 0, s>>>(a);
     CE_CUDA(cudaGetLastError());
     return CONV_EPI_OK;
 }
