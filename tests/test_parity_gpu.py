@@ -35,8 +35,19 @@ SMALL = {
     "c3co40": W["c3_mul_lrelu_gelu"].resized(N=1, H=9, W=128, Cout=40),      # per-channel stores skip padding
     "c5g1": W["c5_gn_pool_clamp"].resized(N=1, H=22, groups=1),               # one group: 64 channels over two quadrants
     "c5g4": W["c5_gn_pool_clamp"].resized(N=1, H=18, groups=4),               # 16 channels per group
+    # degenerate and boundary shapes
+    "min_cout1": W["pr1_min_tanh2"].resized(N=1, Cin=1, H=3, W=4, Cout=1),   # one input and one output channel, 1 x 2 output
+    "c2_w4": W["c2_min_tanh2"].resized(N=1, H=8, W=4),                       # two output columns
+    "c4_one_row": W["c4_scale_min"].resized(N=2, H=3, W=64),                 # one output row per image
+    "c2_cin256": W["c2_min_tanh2"].resized(N=1, H=6, W=64, Cin=256),          # 32 input chunks, filter streamed
+    "c3_cout1": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=32, Cout=1),      # a single per-channel row
+    "c5_w16": W["c5_gn_pool_clamp"].resized(N=2, H=10, W=16),                # 3 pooled columns, 2 pooled rows
+    "c5_one_band": W["c5_gn_pool_clamp"].resized(N=1, H=6),                  # one pooling band per image
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
+# shapes the tf32 kernel refuses (its GroupNorm epilogue pools one band of four
+# rows per unit, which needs 64 < W <= 128): the call must say so, not fall back
+TF32_REFUSED = {"c5_w16"}
 
 
 def modes():
@@ -50,6 +61,12 @@ def test_small_parity(case, mode):
     wl = SMALL[case]
     t = synth.make_inputs(wl, seed=0)
     m = modes()[mode]
+    if mode == "tf32" and case in TF32_REFUSED:
+        import x3_conv2d_epilogue_gb300 as ce
+        with pytest.raises(ce.ConvEpiError) as info:
+            gpu_run(wl, t, m)
+        assert ce.STATUS[info.value.status] == "UNSUPPORTED"
+        return
     got, idx = gpu_run(wl, t, m, want_index=(mode == "fp32" and wl.kind != synth.KIND_MUL_LRELU_GELU))
     ref, ref_idx = oracle_run(wl, t)
     if mode == "fp32":
