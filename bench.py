@@ -264,6 +264,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c2_min_tanh2", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", choices=["tf32", "fp32"], default="tf32")
+    ap.add_argument("--layout", choices=["nchw", "nhwc"], default="nchw",
+                    help="memory layout of x handed to the library (nhwc: tf32 mode, channels last)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=15.0, help="oracle sample length per reference step")
@@ -289,13 +291,17 @@ def main(argv=None):
 
     # inputs resident in HBM (same seeded recipe on every rank: weak scaling)
     t = synth.make_inputs(wl, seed=0)
+    nhwc = args.layout == "nhwc"
+    layout = ce.LAYOUT_NHWC if nhwc else ce.LAYOUT_NCHW
+    if nhwc:  # the same values, channels last
+        t.x = np.ascontiguousarray(t.x.transpose(0, 2, 3, 1))
     host = {k: getattr(t, k) for k in ("x", "w", "b", "mult", "gamma", "beta", "scale")}
     dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in host.items()}
     chan = dev["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else dev["scale"]
     epi = ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan, lrelu_slope=wl.lrelu_slope, groups=wl.groups,
                       eps=wl.eps, gamma=dev["gamma"], beta=dev["beta"], pool_k=wl.pool_k, clamp_lo=wl.clamp_lo,
                       clamp_hi=wl.clamp_hi)
-    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode)
+    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode, layout)
     ce.conv_epi_reserve(h, epi)
     shape = ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, epi, mode)
     out = torch.empty(shape, device="cuda", dtype=torch.float32)
@@ -358,7 +364,7 @@ def main(argv=None):
 
     # ---- context: the unfused pipeline on the same inputs (not the product) ----
     unfused = None
-    if not args.no_unfused and rank == 0:
+    if not args.no_unfused and not nhwc and rank == 0:
         del out
         torch.cuda.empty_cache()
         u_ms = time_unfused(wl, dev, args.mode == "tf32", min(args.steps, 10), 3, stream)
@@ -383,10 +389,12 @@ def main(argv=None):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.mode, "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": wl.name, "x": [wl.N, wl.Cin, wl.H, wl.W], "Cout": wl.Cout, "chain": wl.desc,
-                   "mode": args.mode, "l2": f"inputs larger than L2 ({x_bytes / 1e6:.0f} MB of x per step)",
+                   "mode": args.mode, "layout": args.layout,
+                   "l2": f"inputs larger than L2 ({x_bytes / 1e6:.0f} MB of x per step)",
                    "per_gpu_batch": wl.N},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tf32_peak, "traffic": traffic_for(kernel_hash(), wl.name),
+                     "frac": achieved / tf32_peak,
+                     "traffic": traffic_for(kernel_hash(), wl.name + ("_nhwc" if nhwc else "")),
                      "peak_source": f"{src} bf16 burst {bf16:.1f} x {TF32_PER_BF16:.4f}",
                      "kernel": "conv_epi forward (prep + fused conv kernel)",
                      "hbm_gbs": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm,

@@ -63,10 +63,24 @@ typedef enum {
     CONV_EPI_MODE_FP32 = 1  /* CUDA cores, fp32 fused multiply-add (strict-tolerance mode) */
 } conv_epi_mode;
 
+/* Memory layout of the input x (the filter is [Cout][Cin][3][3] and every
+ * output NCHW in both). */
+typedef enum {
+    CONV_EPI_LAYOUT_NCHW = 0, /* x[N][Cin][H][W], the layout the problem is stated in */
+    CONV_EPI_LAYOUT_NHWC = 1  /* x[N][H][W][Cin] (channels last).  tf32 mode only, Cin a multiple
+                                 of 4.  Each input tile is copied straight into the tensor core's
+                                 operand layout (four channels of a position are adjacent in both),
+                                 so no conversion pass runs: the tensor core uses the top 19 bits
+                                 of each fp32 input (its low 13 mantissa bits are dropped, i.e.
+                                 truncated toward zero) where the NCHW path rounds to nearest.  The
+                                 filter is rounded to nearest in both layouts. */
+} conv_epi_layout;
+
 /* Problem description.  Kernel 3x3, stride 1, padding 0 are implied. */
 typedef struct {
-    int N, Cin, H, W, Cout; /* input [N][Cin][H][W], filter [Cout][Cin][3][3] */
+    int N, Cin, H, W, Cout; /* input [N][Cin][H][W] (or [N][H][W][Cin]), filter [Cout][Cin][3][3] */
     int mode;               /* conv_epi_mode */
+    int layout;             /* conv_epi_layout of x; 0 = NCHW */
 } conv_epi_desc;
 
 typedef enum {

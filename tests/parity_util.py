@@ -37,17 +37,21 @@ def epilogue_for(wl: synth.Workload, d, index_out=None):
                        clamp_hi=wl.clamp_hi, index_out=index_out)
 
 
-def gpu_run(wl: synth.Workload, t: synth.Tensors, mode: int, want_index=False, repeats=1):
-    """Run conv + chain on cuda:0 through the C ABI; returns numpy (out, index)."""
+def gpu_run(wl: synth.Workload, t: synth.Tensors, mode: int, want_index=False, repeats=1, layout=0):
+    """Run conv + chain on cuda:0 through the C ABI; returns numpy (out, index).
+    layout 1 hands the library x in channels-last order (a transposed copy of
+    the same values)."""
     import torch
     import x3_conv2d_epilogue_gb300 as ce
     d = torch_inputs(t)
+    if layout == ce.LAYOUT_NHWC:
+        d["x"] = d["x"].permute(0, 2, 3, 1).contiguous()
     probe = ce.epilogue(wl.kind, groups=wl.groups, pool_k=wl.pool_k, chan_scale=1, gamma=1, beta=1)
     shape = ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, probe, mode)
     out = torch.full(shape, float("nan"), device="cuda", dtype=torch.float32)
     idx = torch.full(shape, -7, device="cuda", dtype=torch.int32) if want_index else None
     epi = epilogue_for(wl, d, idx)
-    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode)
+    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode, layout)
     try:
         for _ in range(repeats):
             ce.conv_epi_forward(h, d["x"], d["w"], d["b"], epi, out)

@@ -60,14 +60,31 @@ def test_output_shapes(lib):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(N=0), dict(Cin=0), dict(H=2), dict(W=1), dict(Cout=0), dict(mode=7),
+    dict(N=0), dict(Cin=0), dict(H=2), dict(W=1), dict(Cout=0), dict(mode=7), dict(layout=2), dict(layout=-1),
 ])
 def test_bad_descriptions_rejected(lib, bad):
-    d = dict(N=1, Cin=4, H=8, W=8, Cout=8, mode=ce.MODE_FP32)
+    d = dict(N=1, Cin=4, H=8, W=8, Cout=8, mode=ce.MODE_FP32, layout=ce.LAYOUT_NCHW)
     d.update(bad)
     with pytest.raises(ce.ConvEpiError) as ei:
-        ce.conv_epi_output_shape(d["N"], d["Cin"], d["H"], d["W"], d["Cout"], ce.epilogue(ce.MIN_TANH2), d["mode"])
+        ce.conv_epi_output_shape(d["N"], d["Cin"], d["H"], d["W"], d["Cout"], ce.epilogue(ce.MIN_TANH2), d["mode"],
+                                 d["layout"])
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("mode,cin,want", [
+    (ce.MODE_FP32, 8, 2),   # channels-last input is a tensor-core path only
+    (ce.MODE_TF32, 6, 2),   # a position's channels must start on 16-byte boundaries
+    (ce.MODE_TF32, 8, 4),   # accepted: the call reaches the (absent) device
+])
+def test_channels_last_checked_before_the_device(lib, mode, cin, want):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = C.c_void_p()
+    d = ce.Desc(1, cin, 8, 8, 8, mode, ce.LAYOUT_NHWC)
+    assert lib.conv_epi_create(C.byref(d), C.byref(h)) == want and not h.value
+    # the output shape does not depend on the input layout
+    assert ce.conv_epi_output_shape(2, cin, 10, 12, 8, ce.epilogue(ce.MIN_TANH2), mode, ce.LAYOUT_NHWC) == (2, 1, 8, 10)
 
 
 @pytest.mark.parametrize("kw", [

@@ -174,3 +174,53 @@ def test_tf32_operand_rounding_is_exact():
     got, _ = gpu_run(wl, t, ce.MODE_TF32)
     want = tf32_rna(t.x[:, 3:4, 1:-1, 1:-1])
     np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_channels_last_parity(case):
+    """The tf32 path with channels-last input: the same seeded values,
+    transposed, against the same oracle and bound.  Shapes whose Cin is not a
+    multiple of 4, and the GroupNorm shape the tf32 kernel cannot pool, are
+    refused with UNSUPPORTED."""
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = SMALL[case]
+    t = synth.make_inputs(wl, seed=0)
+    if wl.Cin % 4 != 0 or case in TF32_REFUSED:
+        with pytest.raises(ce.ConvEpiError) as info:
+            gpu_run(wl, t, ce.MODE_TF32, layout=ce.LAYOUT_NHWC)
+        assert ce.STATUS[info.value.status] == "UNSUPPORTED"
+        return
+    got, _ = gpu_run(wl, t, ce.MODE_TF32, layout=ce.LAYOUT_NHWC)
+    check_tf32(got, oracle_run(wl, t)[0], case + " nhwc")
+
+
+def tf32_trunc(x: np.ndarray) -> np.ndarray:
+    """fp32 -> the top 19 bits (sign, exponent, 10 mantissa bits): truncation
+    toward zero of the low 13 mantissa bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return (u & np.uint32(0xFFFFE000)).view(np.float32)
+
+
+def test_channels_last_operands_are_truncated():
+    """Channels-last input reaches the tensor core without a rounding pass:
+    with a centre-tap filter on one channel and every other channel biased
+    far above it, the channel minimum is that channel's y = x * 1 with x cut
+    to its top 19 bits, bit for bit (the same inputs as the rounding test,
+    whose tie patterns tell truncation from rounding)."""
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = W["c4_scale_min"].resized(N=1, Cin=8, H=6, W=32, Cout=64, scalar=1.0)
+    t = synth.make_inputs(wl, seed=11)
+    rng = np.random.default_rng(3)
+    bits = rng.normal(size=t.x.shape).astype(np.float32).view(np.uint32)
+    flat = bits.reshape(-1)
+    special = np.array([0x1000, 0x0FFF, 0x1001, 0x1FFF, 0x2000], dtype=np.uint32)
+    flat[:] = (flat & 0xFFFFE000) | special[np.arange(flat.size) % special.size]
+    flat[::7] |= 0x80000000
+    t.x[:] = bits.view(np.float32)
+    t.w[:] = 0
+    t.w[0, 3, 1, 1] = 1.0
+    t.b[:] = 1.0e6
+    t.b[0] = 0.0
+    got, _ = gpu_run(wl, t, ce.MODE_TF32, layout=ce.LAYOUT_NHWC)
+    want = tf32_trunc(t.x[:, 3:4, 1:-1, 1:-1])
+    np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))

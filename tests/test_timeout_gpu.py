@@ -23,11 +23,14 @@ pytestmark = pytest.mark.gpu
 W = synth.WORKLOADS
 CASES = {
     # filter resident in shared memory; the producer blocks on the tile ring
-    "c2_resident": (W["c2_min_tanh2"].resized(N=2, H=21), 1),
+    "c2_resident": (W["c2_min_tanh2"].resized(N=2, H=21), 1, 0),
     # filter streamed (Cin 64): the producer polls both rings without blocking
-    "c3_streamed": (W["c3_mul_lrelu_gelu"].resized(N=2, H=11), 2),
+    "c3_streamed": (W["c3_mul_lrelu_gelu"].resized(N=2, H=11), 2, 0),
     # GroupNorm chain: the finalize kernel still runs after the timed-out conv
-    "c5_gn_first_tile": (W["c5_gn_pool_clamp"].resized(N=2, H=42), 0),
+    "c5_gn_first_tile": (W["c5_gn_pool_clamp"].resized(N=2, H=42), 0, 0),
+    # channels-last input: the dropped copy is a B plane, so the MMA thread's
+    # wait is the one that runs out
+    "c4_channels_last": (W["c4_scale_min"].resized(N=1, H=12), 3, 1),
 }
 
 
@@ -35,14 +38,16 @@ CASES = {
 def test_dropped_tile_times_out_then_recovers(case):
     import torch
     import x3_conv2d_epilogue_gb300 as ce
-    wl, tile = CASES[case]
+    wl, tile, layout = CASES[case]
     t = synth.make_inputs(wl, seed=21)
     d = torch_inputs(t)
+    if layout == ce.LAYOUT_NHWC:
+        d["x"] = d["x"].permute(0, 2, 3, 1).contiguous()
     probe = ce.epilogue(wl.kind, groups=wl.groups, pool_k=wl.pool_k, chan_scale=1, gamma=1, beta=1)
     shape = ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, probe, ce.MODE_TF32)
     out = torch.full(shape, float("nan"), device="cuda", dtype=torch.float32)
     epi = epilogue_for(wl, d)
-    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, ce.MODE_TF32)
+    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, ce.MODE_TF32, layout)
     try:
         ce.conv_epi_test_drop_tile(h, tile)
         t0 = time.perf_counter()

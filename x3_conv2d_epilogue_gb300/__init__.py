@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libconv_epi.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "conv_epi.h")
 
 MODE_TF32, MODE_FP32 = 0, 1
+LAYOUT_NCHW, LAYOUT_NHWC = 0, 1
 MIN_TANH2, SCALE_MIN, MUL_LRELU_GELU, GN_SCALE_POOL_CLAMP = 1, 2, 3, 4
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CUDA", 5: "TIMEOUT",
           6: "NO_MEMORY", 7: "DEVICE"}
@@ -35,7 +36,8 @@ class ConvEpiError(RuntimeError):
 
 class Desc(C.Structure):
     _fields_ = [("N", C.c_int), ("Cin", C.c_int), ("H", C.c_int), ("W", C.c_int), ("Cout", C.c_int),
-                ("mode", C.c_int)]
+                ("mode", C.c_int),
+                ("layout", C.c_int)]
 
 
 class EpilogueDesc(C.Structure):
@@ -128,17 +130,19 @@ def epilogue(kind, scalar=1.0, chan_scale=None, lrelu_slope=0.01, groups=16, eps
     return e
 
 
-def conv_epi_output_shape(N, Cin, H, W, Cout, epi, mode=MODE_TF32):
+def conv_epi_output_shape(N, Cin, H, W, Cout, epi, mode=MODE_TF32, layout=LAYOUT_NCHW):
     import numpy as np
     s = np.zeros(4, dtype=np.int64)
-    d = Desc(N, Cin, H, W, Cout, mode)
+    d = Desc(N, Cin, H, W, Cout, mode, layout)
     _check(_lib().conv_epi_output_shape(C.byref(d), C.byref(epi), s.ctypes.data), "conv_epi_output_shape")
     return tuple(int(v) for v in s)
 
 
-def conv_epi_create(N, Cin, H, W, Cout, mode=MODE_TF32):
+def conv_epi_create(N, Cin, H, W, Cout, mode=MODE_TF32, layout=LAYOUT_NCHW):
+    """layout: LAYOUT_NCHW (x[N][Cin][H][W]) or LAYOUT_NHWC (x[N][H][W][Cin],
+    tf32 mode, Cin a multiple of 4)."""
     h = C.c_void_p()
-    d = Desc(N, Cin, H, W, Cout, mode)
+    d = Desc(N, Cin, H, W, Cout, mode, layout)
     _check(_lib().conv_epi_create(C.byref(d), C.byref(h)), "conv_epi_create")
     return h
 
@@ -159,10 +163,11 @@ def conv_epi_forward_host(h, x, w, b, epi, out, stream=None):
     return out
 
 
-def conv_epi_forward_noalloc(N, Cin, H, W, Cout, x, w, b, epi, out, stream=None, mode=MODE_TF32):
+def conv_epi_forward_noalloc(N, Cin, H, W, Cout, x, w, b, epi, out, stream=None, mode=MODE_TF32,
+                             layout=LAYOUT_NCHW):
     """Tensor-core forward without a handle: the library allocates nothing and
     uses its fixed device-side scratch array (see include/conv_epi.h)."""
-    d = Desc(N, Cin, H, W, Cout, mode)
+    d = Desc(N, Cin, H, W, Cout, mode, layout)
     _check(_lib().conv_epi_forward_noalloc(C.byref(d), _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out),
                                            _stream(stream)), "conv_epi_forward_noalloc")
     return out
@@ -201,13 +206,14 @@ def conv_epi_status_string(status):
 class ConvEpi:
     """Owns one handle; ``forward`` allocates the output with torch."""
 
-    def __init__(self, N, Cin, H, W, Cout, mode=MODE_TF32):
+    def __init__(self, N, Cin, H, W, Cout, mode=MODE_TF32, layout=LAYOUT_NCHW):
         self.dims = (N, Cin, H, W, Cout)
         self.mode = mode
-        self.h = conv_epi_create(N, Cin, H, W, Cout, mode)
+        self.layout = layout
+        self.h = conv_epi_create(N, Cin, H, W, Cout, mode, layout)
 
     def output_shape(self, epi):
-        return conv_epi_output_shape(*self.dims, epi, self.mode)
+        return conv_epi_output_shape(*self.dims, epi, self.mode, self.layout)
 
     def forward(self, x, w, b, epi, out=None, stream=None):
         import torch

@@ -19,6 +19,7 @@ conv_epi_status check_desc(const conv_epi_desc *d) {
     if (!d) return CONV_EPI_ERR_INVALID_ARG;
     if (d->N < 1 || d->Cin < 1 || d->Cout < 1 || d->H < 3 || d->W < 3) return CONV_EPI_ERR_INVALID_ARG;
     if (d->mode != CONV_EPI_MODE_TF32 && d->mode != CONV_EPI_MODE_FP32) return CONV_EPI_ERR_INVALID_ARG;
+    if (d->layout != CONV_EPI_LAYOUT_NCHW && d->layout != CONV_EPI_LAYOUT_NHWC) return CONV_EPI_ERR_INVALID_ARG;
     // element counts and offsets are kept in 64-bit, but every single tensor
     // must stay below 2^31 elements
     const int64_t nx = (int64_t)d->N * d->Cin * d->H * d->W;
@@ -67,6 +68,10 @@ void shape_of(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, int64_t s
 }
 
 conv_epi_status check_mode_support(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
+    // channels-last input feeds the tensor core directly: tf32 mode, and a
+    // position's channels must start on 16-byte boundaries
+    if (d.layout == CONV_EPI_LAYOUT_NHWC && (d.mode != CONV_EPI_MODE_TF32 || d.Cin % 4 != 0))
+        return CONV_EPI_ERR_UNSUPPORTED;
     if (d.mode == CONV_EPI_MODE_FP32)
         return e ? conv_epi::simt_supported(d, *e) : CONV_EPI_OK;
     return conv_epi::tc_supported(d, e);
@@ -144,7 +149,7 @@ CONV_EPI_API const char *conv_epi_status_string(conv_epi_status s) {
 
 CONV_EPI_API const char *conv_epi_last_cuda_error(void) { return g_cuda_err; }
 
-CONV_EPI_API int conv_epi_version(void) { return 10000; }
+CONV_EPI_API int conv_epi_version(void) { return 10100; }
 
 CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc, const conv_epi_epilogue_desc *epi,
                                                    int64_t shape[4]) {

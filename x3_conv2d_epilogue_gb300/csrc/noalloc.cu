@@ -80,7 +80,9 @@ extern "C" CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_
     if (!desc || !x || !w || !b || !epi || !out) return CONV_EPI_ERR_INVALID_ARG;
     const conv_epi_desc &d = *desc;
     if (d.N < 1 || d.Cin < 1 || d.Cout < 1 || d.H < 3 || d.W < 3) return CONV_EPI_ERR_INVALID_ARG;
+    if (d.layout != CONV_EPI_LAYOUT_NCHW && d.layout != CONV_EPI_LAYOUT_NHWC) return CONV_EPI_ERR_INVALID_ARG;
     if (d.mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;
+    if (d.layout == CONV_EPI_LAYOUT_NHWC && d.Cin % 4 != 0) return CONV_EPI_ERR_UNSUPPORTED;
     if ((int64_t)d.N * d.Cin * d.H * d.W >= (1ll << 31) || (int64_t)d.N * d.Cout * (d.H - 2) * (d.W - 2) >= (1ll << 31))
         return CONV_EPI_ERR_UNSUPPORTED;
     switch (epi->kind) {

@@ -98,6 +98,7 @@ struct Cfg {
     int groups, Hp, Wp;
     GnWork gn;
     int drop_tile;  // test hook: per-CTA staged-tile index the producer never issues (-1: none)
+    int nhwc;       // channels-last input: tiles go straight into the B planes (no staging, no converters)
 };
 
 struct TcArgs {        // 64-byte aligned through CUtensorMap
@@ -468,7 +469,9 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
 
 // Producer (one thread): per chunk (unit, c), in order, the raw input tile
 // x[n][8c .. 8c+7][r0 .. r0+Rin-1][0 .. W-1] into the next staging slot (laid
-// out [8][Rin][W]; rows >= H arrive as zeros) and, when the filter streams,
+// out [8][Rin][W]; rows >= H arrive as zeros) -- for channels-last input the
+// tile's two 4-channel halves straight into the next B plane, each laid out
+// [Rin][P][4] -- and, when the filter streams,
 // chunk c of the packed filter into the next filter slot.  The two sequences
 // advance independently: while both run, the thread tests both rings without
 // blocking and issues whichever copy has a free slot, so a full filter ring
@@ -491,6 +494,13 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
     const int total = my_units * a.chunks;
     // ring slots and phases by counters; per slot, whether a copy was issued
     // into it and that copy's phase (bit s of the masks)
+    // the tile ring: staging buffers (NCHW, read by the converters) or, for
+    // channels-last input, the B planes themselves (two 4-channel boxes per
+    // chunk, one per K-group plane, read by the MMAs)
+    const int tn = a.nhwc ? a.nb : a.nr;
+    const uint32_t t_off = a.nhwc ? a.b_off : a.raw_off, t_bytes = a.nhwc ? a.b_bytes : a.raw_bytes;
+    auto t_empty = [&](int s) { return a.nhwc ? bars.b_empty(s) : bars.r_empty(s); };
+    auto t_full = [&](int s) { return a.nhwc ? bars.b_full(s) : bars.r_full(s); };
     int sr = 0, sa = 0;
     uint32_t pr = 0, pa = 0;
     uint32_t r_iss = 0, r_par = 0, a_iss = 0, a_par = 0;
@@ -504,18 +514,26 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
         // with the filter sequence done (or resident), the tile sequence
         // blocks in the ordinary bounded wait
         const bool tiles_only = ia >= total;
-        if (tiles_only && !wait_bar(bars.r_empty(sr), pr ^ 1, abort_flag, a.err)) break;
-        if (ir < total && (tiles_only || mbar_try_wait(bars.r_empty(sr), pr ^ 1))) {
+        if (tiles_only && !wait_bar(t_empty(sr), pr ^ 1, abort_flag, a.err)) break;
+        if (ir < total && (tiles_only || mbar_try_wait(t_empty(sr), pr ^ 1))) {
             if (ir != a.drop_tile) {
-                mbar_arrive_expect_tx(bars.r_full(sr), a.raw_tx);
-                tma_load_4d(sbase + a.raw_off + sr * a.raw_bytes, xmap, 0, pos.ru * a.RU, 8 * cr, pos.n, bars.r_full(sr));
+                const uint32_t dst = sbase + t_off + sr * t_bytes;
+                mbar_arrive_expect_tx(t_full(sr), a.raw_tx);
+                if (a.nhwc) {
+                    // x as (C, W, H, N): channels 8c..8c+3 and 8c+4..8c+7 of
+                    // rows r0.., columns 0..P-1 (past W and H: zeros)
+                    tma_load_4d(dst, xmap, 8 * cr, 0, pos.ru * a.RU, pos.n, t_full(sr));
+                    tma_load_4d(dst + 16u * a.PL, xmap, 8 * cr + 4, 0, pos.ru * a.RU, pos.n, t_full(sr));
+                } else {
+                    tma_load_4d(dst, xmap, 0, pos.ru * a.RU, 8 * cr, pos.n, t_full(sr));
+                }
                 r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
             } else {
                 // test hook: this slot's phase never completes, so its
                 // consumers' bounded waits run out; nothing is in flight here
                 r_iss &= ~(1u << sr);
             }
-            if (++sr == a.nr) sr = 0, pr ^= 1u;
+            if (++sr == tn) sr = 0, pr ^= 1u;
             if (++cr == a.chunks) cr = 0, pos.step(gridDim.x, a.units_per_img);
             ++ir;
             moved = true;
@@ -548,8 +566,8 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
     }
     // copies still in flight land before the CTA exits
     if (a.resident) wait_bar(bars.wres(), 0, abort_flag, a.err, false);
-    for (int s = 0; s < a.nr; ++s)
-        if ((r_iss >> s) & 1u) wait_bar(bars.r_full(s), (r_par >> s) & 1u, abort_flag, a.err, false);
+    for (int s = 0; s < tn; ++s)
+        if ((r_iss >> s) & 1u) wait_bar(t_full(s), (r_par >> s) & 1u, abort_flag, a.err, false);
     for (int s = 0; s < a.na; ++s)
         if ((a_iss >> s) & 1u) wait_bar(bars.a_full(s), (a_par >> s) & 1u, abort_flag, a.err, false);
 }
@@ -567,6 +585,7 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
 constexpr int kConvItems = 12;  // items per converter warp per chunk (2*Rin*ceil(P/32) <= 72, checked on host)
 
 __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, const Bars &bars, volatile int *abort_flag) {
+    if (a.nhwc) return;  // channels-last tiles arrive in the B layout
     const int cw = conv_index(threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int P = a.P, W = a.W, Rin = a.Rin, PL = a.PL;
@@ -1148,7 +1167,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         for (int s = 0; s < kMaxRing; ++s) {
             mbar_init(bars.a_full(s), 1);
             mbar_init(bars.a_empty(s), 1);
-            mbar_init(bars.b_full(s), kConvWarps);
+            mbar_init(bars.b_full(s), a.nhwc ? 1 : kConvWarps);  // NHWC: the producer's transaction arrive
             mbar_init(bars.b_empty(s), 1);
             mbar_init(bars.r_full(s), 1);
             mbar_init(bars.r_empty(s), kConvWarps);
@@ -1264,6 +1283,8 @@ int gemm_cout(int Cout) { return Cout <= 64 ? 64 : 128; }
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (d.Cout < 1 || d.Cout > 128) return false;
     if (d.Cin < 1 || d.W % 4 != 0 || d.W > 256 || d.H < 3) return false;
+    const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
+    if (nhwc && d.Cin % 4 != 0) return false;  // 16-byte position stride
     const int Cg = gemm_cout(d.Cout);
     pl.S = 128 / Cg;
     pl.P = (d.W + 15) / 16 * 16;
@@ -1275,26 +1296,28 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.PL = (pl.Rin * pl.P + 4 + 7) / 8 * 8;
     pl.chunks = (d.Cin + 7) / 8;  // the last chunk of a Cin not a multiple of 8 is zero-padded
     if (pl.PL >= (1 << 16)) return false;
-    if (2 * pl.Rin * ((pl.P + 31) / 32) > kConvItems * kConvWarps) return false;  // converter items per chunk
+    if (!nhwc && 2 * pl.Rin * ((pl.P + 31) / 32) > kConvItems * kConvWarps) return false;  // converter items per chunk
     pl.a_bytes = up1k(3u * 2u * (2 * pl.S + 1) * Cg * 16u);
     pl.b_bytes = up1k(2u * pl.PL * 16u);
-    pl.raw_bytes = up1k(8u * pl.Rin * d.W * 4u);
+    pl.raw_bytes = nhwc ? 0u : up1k(8u * pl.Rin * d.W * 4u);  // channels last: no staging ring
     pl.scratch_bytes = scratch_bytes_for(kind, pl.U, pl.P);
     const uint32_t tail = 8u * Bars::kCount + 16u + pl.scratch_bytes;
     auto total = [&](int na, int nb, int nr) {
         return (size_t)na * pl.a_bytes + (size_t)nb * pl.b_bytes + (size_t)nr * pl.raw_bytes + tail;
     };
     // resident filter when it still leaves 2 B planes and 2 staged tiles
-    pl.resident = total(pl.chunks, 2, 2) <= (size_t)kSmemLimit;
+    const int nr0 = nhwc ? 0 : 2;
+    pl.resident = total(pl.chunks, 2, nr0) <= (size_t)kSmemLimit;
     const int na_min = pl.resident ? pl.chunks : 2;
-    pl.na = na_min, pl.nb = 2, pl.nr = 2;
+    pl.na = na_min, pl.nb = 2, pl.nr = nr0;
     if (total(pl.na, pl.nb, pl.nr) > (size_t)kSmemLimit) return false;
     // grow the rings while they fit: staged tiles first (they hide DRAM
     // latency), then B planes, then filter stages
     for (bool grew = true; grew;) {
         grew = false;
-        if (pl.nr < kMaxRing && total(pl.na, pl.nb, pl.nr + 1) <= (size_t)kSmemLimit) ++pl.nr, grew = true;
-        if (pl.nb < 3 && total(pl.na, pl.nb + 1, pl.nr) <= (size_t)kSmemLimit) ++pl.nb, grew = true;
+        if (!nhwc && pl.nr < kMaxRing && total(pl.na, pl.nb, pl.nr + 1) <= (size_t)kSmemLimit) ++pl.nr, grew = true;
+        // channels last, the B planes are also the input prefetch ring
+        if (pl.nb < (nhwc ? kMaxRing : 3) && total(pl.na, pl.nb + 1, pl.nr) <= (size_t)kSmemLimit) ++pl.nb, grew = true;
         if (!pl.resident && pl.na < 3 && total(pl.na + 1, pl.nb, pl.nr) <= (size_t)kSmemLimit) ++pl.na, grew = true;
     }
     pl.a_off = 0;
@@ -1376,11 +1399,24 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     TcArgs args;
     memset(&args, 0, sizeof args);
     Cfg &a = args.c;
+    const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
     {
-        const cuuint64_t dims[4] = {(cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.Cin, (cuuint64_t)d.N};
-        const cuuint64_t strides[3] = {(cuuint64_t)d.W * 4, (cuuint64_t)d.W * d.H * 4,
-                                       (cuuint64_t)d.W * d.H * d.Cin * 4};
-        const cuuint32_t box[4] = {(cuuint32_t)d.W, (cuuint32_t)pl.Rin, 8u, 1u};
+        // NCHW: x as (W, H, C, N), box (W, Rin, 8, 1) -> staging [8][Rin][W].
+        // NHWC: x as (C, W, H, N), box (4, P, Rin, 1) -> a B plane [Rin][P][4]
+        // (columns W..P-1, rows past H and channels past Cin read as zeros).
+        cuuint64_t dims[4], strides[3];
+        cuuint32_t box[4];
+        if (nhwc) {
+            dims[0] = (cuuint64_t)d.Cin, dims[1] = (cuuint64_t)d.W, dims[2] = (cuuint64_t)d.H, dims[3] = (cuuint64_t)d.N;
+            strides[0] = (cuuint64_t)d.Cin * 4, strides[1] = (cuuint64_t)d.Cin * d.W * 4,
+            strides[2] = (cuuint64_t)d.Cin * d.W * d.H * 4;
+            box[0] = 4u, box[1] = (cuuint32_t)pl.P, box[2] = (cuuint32_t)pl.Rin, box[3] = 1u;
+        } else {
+            dims[0] = (cuuint64_t)d.W, dims[1] = (cuuint64_t)d.H, dims[2] = (cuuint64_t)d.Cin, dims[3] = (cuuint64_t)d.N;
+            strides[0] = (cuuint64_t)d.W * 4, strides[1] = (cuuint64_t)d.W * d.H * 4,
+            strides[2] = (cuuint64_t)d.W * d.H * d.Cin * 4;
+            box[0] = (cuuint32_t)d.W, box[1] = (cuuint32_t)pl.Rin, box[2] = 8u, box[3] = 1u;
+        }
         const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
         const CUresult r = enc(&args.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims, strides, box,
                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1406,7 +1442,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.total_units = d.N * a.units_per_img;
     a.resident = pl.resident, a.na = pl.na, a.nb = pl.nb, a.nr = pl.nr;
     a.a_bytes = pl.a_bytes, a.b_bytes = pl.b_bytes, a.raw_bytes = pl.raw_bytes;
-    a.raw_tx = 8u * pl.Rin * d.W * 4u;
+    a.raw_tx = nhwc ? 2u * 4u * pl.P * pl.Rin * 4u : 8u * pl.Rin * d.W * 4u;  // bytes one tile delivers
+    a.nhwc = nhwc ? 1 : 0;
     a.a_off = pl.a_off, a.b_off = pl.b_off, a.raw_off = pl.raw_off, a.bar_off = pl.bar_off;
     a.scratch_off = pl.scratch_off;
     a.a_plane_bytes = (uint32_t)a.Cout * 16u;
