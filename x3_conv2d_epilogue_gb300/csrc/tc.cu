@@ -24,7 +24,9 @@
 // B plane (each lane gathers one position's four channels, rounds them to
 // tf32 and stores one 16-byte plane row), so their proxy fence before handing
 // the plane to the tensor core covers only short shared-memory stores --
-// never global loads in flight.
+// never global loads in flight.  Channels-last input (x as [N][H][W][Cin])
+// skips both: its 4-channel boxes land straight in the B planes, whose
+// 16-byte position rows they already match.
 //
 // Row slots.  The MMA's M is 128.  With Cout = 128 a tile is one output row
 // per accumulator.  With Cout = 64 the 128 accumulator lanes hold TWO output
