@@ -82,13 +82,26 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
         if (i < nv) v[k] = src[i];
     }
     if (threadIdx.x < 32) {
+        // the channel parameters (at most two channels per lane) are loaded
+        // before the fold, so their latency overlaps it
+        float gm[kMaxCpg / 32], sc[kMaxCpg / 32], bt[kMaxCpg / 32];
+#pragma unroll
+        for (int k = 0; k < kMaxCpg / 32; ++k) {
+            const int cl = threadIdx.x + 32 * k;
+            if (cl < cpg) {
+                const int c = g * cpg + cl;
+                gm[k] = a.gamma[c], sc[k] = a.scale[c], bt[k] = a.beta[c];
+            }
+        }
         float mean, rstd;
         group_stats(a, n, g, mean, rstd);
-        for (int cl = threadIdx.x; cl < cpg; cl += 32) {
-            const int c = g * cpg + cl;
-            const float gm = a.gamma[c], sc = a.scale[c];
-            sA[cl] = gm * sc * rstd;
-            sB[cl] = (a.beta[c] - gm * mean * rstd) * sc;
+#pragma unroll
+        for (int k = 0; k < kMaxCpg / 32; ++k) {
+            const int cl = threadIdx.x + 32 * k;
+            if (cl < cpg) {
+                sA[cl] = gm[k] * sc[k] * rstd;
+                sB[cl] = (bt[k] - gm[k] * mean * rstd) * sc[k];
+            }
         }
     }
     __syncthreads();
