@@ -43,7 +43,8 @@ def _stale(target: str, deps) -> bool:
 
 def build(verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(OBJ_DIR, exist_ok=True)
-    headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    headers = (glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
+               glob.glob(os.path.join(INCLUDE, "*.h")))
     procs, objs = [], []
     for src in sources():
         obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")

@@ -106,7 +106,8 @@ conv_epi_status ensure_gn_workspace(conv_epi_handle h, int pool_k, int groups, i
     const size_t npool = (size_t)d.N * d.Cout * Hp * Wp;
     const size_t npart = (size_t)d.N * units * groups * 2;
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
-    const size_t bytes = 2 * up(npool * sizeof(float)) + 2 * up(npool * sizeof(int32_t)) + up(npart * sizeof(double));
+    const size_t bytes = 2 * up(npool * sizeof(float)) + 2 * up(npool * sizeof(int32_t)) + up(npart * sizeof(double)) +
+                         256;  // + the arrival counter
     if (h->gn_mem && bytes <= h->gn_bytes) {
         // reuse the larger buffer
     } else {
@@ -123,7 +124,8 @@ conv_epi_status ensure_gn_workspace(conv_epi_handle h, int pool_k, int groups, i
     h->gn.pmin = reinterpret_cast<float *>(p), p += up(npool * sizeof(float));
     h->gn.amax = reinterpret_cast<int32_t *>(p), p += up(npool * sizeof(int32_t));
     h->gn.amin = reinterpret_cast<int32_t *>(p), p += up(npool * sizeof(int32_t));
-    h->gn.part = reinterpret_cast<double *>(p);
+    h->gn.part = reinterpret_cast<double *>(p), p += up(npart * sizeof(double));
+    h->gn.arrive = reinterpret_cast<unsigned *>(p);
     h->gn.units = units, h->gn.Hp = Hp, h->gn.Wp = Wp;
     h->gn_pool_k = pool_k, h->gn_groups = groups, h->gn_units = units;
     return CONV_EPI_OK;
@@ -180,6 +182,7 @@ CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi
     h->device = dev;
     h->sm_count = prop.multiProcessorCount;
     h->cc_major = prop.major, h->cc_minor = prop.minor;
+    h->coop = prop.cooperativeLaunch;
     cudaError_t e = cudaMalloc(&h->dev_err, 256);
     if (e == cudaSuccess) e = cudaMemset(h->dev_err, 0, 256);
     if (e == cudaSuccess && desc->mode == CONV_EPI_MODE_TF32) {

@@ -18,6 +18,7 @@
 // inside the square root.
 #include <math.h>
 
+#include "gn_common.cuh"
 #include "internal.h"
 
 namespace conv_epi {
@@ -37,24 +38,8 @@ struct GnArgs {
     uint32_t per_magic;  // ceil(2^32 / (Hp * Wp)): exact f / (Hp * Wp) for f < 2^16
 };
 
-// Mean and rstd of group g of image n from the per-unit partial sums (one
-// warp: fixed order in fp64, lanes take units lane, lane+32, ..., then a fixed
-// shuffle tree); every lane returns the same values.
 __device__ __forceinline__ void group_stats(const GnArgs &a, int n, int g, float &mean_f, float &rstd_f) {
-    const int lane = threadIdx.x & 31;
-    double s = 0.0, ss = 0.0;
-    const double *p = a.gn.part + ((size_t)n * a.gn.units * a.groups + g) * 2;
-    for (int u = lane; u < a.gn.units; u += 32) s += p[(size_t)u * 2 * a.groups], ss += p[(size_t)u * 2 * a.groups + 1];
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, off);
-        ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    }
-    const double mean = s * a.inv_cnt;
-    double var = ss * a.inv_cnt - mean * mean;
-    if (var < 0.0) var = 0.0;
-    mean_f = (float)mean;
-    rstd_f = rsqrtf((float)var + a.eps);
+    gn_group_stats(a.gn.part, a.gn.units, a.groups, n, g, a.inv_cnt, a.eps, mean_f, rstd_f);
 }
 
 // The tensor-core path's case: pmax holds, per channel, the extreme that the
@@ -98,10 +83,7 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
 #pragma unroll
         for (int k = 0; k < kMaxCpg / 32; ++k) {
             const int cl = threadIdx.x + 32 * k;
-            if (cl < cpg) {
-                sA[cl] = gm[k] * sc[k] * rstd;
-                sB[cl] = (bt[k] - gm[k] * mean * rstd) * sc[k];
-            }
+            if (cl < cpg) gn_coeffs(gm[k], bt[k], sc[k], mean, rstd, sA[cl], sB[cl]);
         }
     }
     __syncthreads();
@@ -154,9 +136,7 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
         if (cl0 > 0) __syncthreads();  // the previous batch's coefficients are no longer read
         if (threadIdx.x < ncl) {
             const int c = g * cpg + cl0 + threadIdx.x;
-            const float gm = a.gamma[c], sc = a.scale[c];
-            sA[threadIdx.x] = gm * sc * rstd;
-            sB[threadIdx.x] = (a.beta[c] - gm * mean * rstd) * sc;
+            gn_coeffs(a.gamma[c], a.beta[c], a.scale[c], mean, rstd, sA[threadIdx.x], sB[threadIdx.x]);
         }
         __syncthreads();
         const int per = a.gn.Hp * a.gn.Wp;

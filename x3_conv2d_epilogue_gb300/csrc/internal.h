@@ -31,6 +31,7 @@ struct GnWork {
     float *pmax = nullptr, *pmin = nullptr;
     int32_t *amax = nullptr, *amin = nullptr;
     double *part = nullptr;  // [N][units][groups][2]
+    unsigned *arrive = nullptr;  // grid-wide arrival counter of the tf32 kernel's in-kernel finalize
     int units = 0;           // partial-sum slots per image
     int Hp = 0, Wp = 0;
 };
@@ -43,6 +44,7 @@ struct conv_epi_handle_s {
     int device = 0;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
+    int coop = 0;  // the device takes cooperative launches
     unsigned *dev_err = nullptr;  // device error word
 
     // packed tf32 weights for the tensor-core path

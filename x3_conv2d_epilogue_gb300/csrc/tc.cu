@@ -57,6 +57,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "gn_common.cuh"
 #include "internal.h"
 
 namespace conv_epi {
@@ -101,6 +102,13 @@ struct Cfg {
     GnWork gn;
     int drop_tile;  // test hook: per-CTA staged-tile index the producer never issues (-1: none)
     int nhwc;       // channels-last input: tiles go straight into the B planes (no staging, no converters)
+    // GroupNorm chain finalized inside this kernel (cooperative launch)
+    int gn_fin;
+    const float *beta;
+    float eps, lo, hi;
+    double inv_cnt;       // 1 / (C/groups * Ho * Wo)
+    uint32_t per_magic;   // ceil(2^32 / (Hp * Wp))
+    uint32_t f4_magic;    // ceil(2^32 / F4), F4 = float4 per (image, group) block
 };
 
 struct TcArgs {        // 64-byte aligned through CUtensorMap
@@ -1153,6 +1161,99 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     }
 }
 
+// In-kernel GroupNorm finalize (launched cooperatively, so every CTA is
+// resident and a grid-wide arrival count is safe to wait on).  After every
+// CTA has stored its units' partial sums and pooled extremes and released
+// tensor memory, CTA b takes the (image, group) pairs b, b + gridDim.x, ...
+// in batches of one pair per warp: the warp folds the pair's statistics and
+// its channels' coefficients into shared memory, then all threads apply
+// z = clamp(A y + B) over the batch's pooled blocks (contiguous, F4 float4
+// each) with 16-byte loads and stores, sixteen in flight per thread (the
+// first sixteen issued before the statistics fold).  The
+// pooled extremes are read back from L2 rather than by a second launch.
+constexpr int kFinPairs = kThreads / 32;
+__device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, volatile int *abort_flag) {
+    // (the pipeline's shared memory is free now: coefficient tables and a flag)
+    float *sA = reinterpret_cast<float *>(smem), *sB = sA + kFinPairs * 64;
+    int &s_go = *reinterpret_cast<int *>(sB + kFinPairs * 64);
+    __threadfence();  // this CTA's partials and pooled extremes, device-wide
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicAdd(a.gn.arrive, 1u);
+        int go = 1;
+        const uint64_t t0 = globaltimer();
+        for (;;) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.gn.arrive) : "memory");
+            if (v >= gridDim.x) break;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                atomicOr(a.err, ERRBIT_TIMEOUT);
+                go = 0;
+                break;
+            }
+            __nanosleep(256);
+        }
+        __threadfence();
+        s_go = go && !*abort_flag;
+    }
+    __syncthreads();
+    if (!s_go) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cpg = a.Cout / a.groups;
+    const uint32_t per = (uint32_t)(a.Hp * a.Wp), F4 = (uint32_t)cpg * per / 4u;
+    const int npairs = a.N * a.groups;
+    const float4 *__restrict__ src = reinterpret_cast<const float4 *>(a.gn.pmax);
+    float4 *__restrict__ dst = reinterpret_cast<float4 *>(a.out);
+    constexpr int kV = 16;  // float4 loads in flight per thread
+    for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * kFinPairs) {
+        const int nbp = min(kFinPairs, (npairs - p0 + (int)gridDim.x - 1) / (int)gridDim.x);  // pairs in this batch
+        const uint32_t total = (uint32_t)nbp * F4;
+        float4 v[kV];
+        uint32_t jb[kV], fo[kV];
+        auto load_round = [&](uint32_t t0) {
+#pragma unroll
+            for (int k = 0; k < kV; ++k) {
+                const uint32_t t = t0 + (uint32_t)(k * kThreads) + threadIdx.x;
+                jb[k] = __umulhi(t, a.f4_magic);  // t / F4: the pair within the batch
+                fo[k] = t - jb[k] * F4;           // float4 within the pair's block
+                if (t < total) v[k] = src[(size_t)(p0 + (int)jb[k] * (int)gridDim.x) * F4 + fo[k]];
+            }
+        };
+        // the first loads go out before the statistics: they do not need them
+        load_round(0);
+        const int p = p0 + warp * (int)gridDim.x;
+        if (warp < nbp) {
+            const int n = p / a.groups, g = p % a.groups;
+            float mean, rstd;
+            gn_group_stats(a.gn.part, a.units_per_img, a.groups, n, g, a.inv_cnt, a.eps, mean, rstd);
+            for (int cl = lane; cl < cpg; cl += 32) {
+                const int c = g * cpg + cl;
+                gn_coeffs(__ldg(&a.gamma[c]), __ldg(&a.beta[c]), __ldg(&a.chan_scale[c]), mean, rstd,
+                          sA[warp * 64 + cl], sB[warp * 64 + cl]);
+            }
+        }
+        __syncthreads();
+        for (uint32_t t0 = 0; t0 < total; t0 += kV * kThreads) {
+            if (t0 > 0) load_round(t0);
+#pragma unroll
+            for (int k = 0; k < kV; ++k) {
+                const uint32_t t = t0 + (uint32_t)(k * kThreads) + threadIdx.x;
+                if (t >= total) continue;
+                const float *cA = sA + jb[k] * 64, *cB = sB + jb[k] * 64;
+                const uint32_t e = 4u * fo[k];
+                float r[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
+                    r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
+                }
+                dst[(size_t)(p0 + (int)jb[k] * (int)gridDim.x) * F4 + fo[k]] = make_float4(r[0], r[1], r[2], r[3]);
+            }
+        }
+        __syncthreads();  // the next batch rewrites the coefficients
+    }
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant__ TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1217,6 +1318,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(*tmem_slot, kTmemCols);
+    }
+    if constexpr (KIND == CONV_EPI_GN_SCALE_POOL_CLAMP) {
+        if (a.gn_fin) gn_finalize_tail(a, smem, abort_flag);
     }
 }
 
@@ -1360,7 +1464,22 @@ template <int KIND>
 conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStream_t s) {
     auto k = tc_conv_epi<KIND>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
-    k<<<grid, kThreads, pl.smem, s>>>(args);
+    if (args.c.gn_fin) {
+        // the in-kernel finalize waits for every CTA: a cooperative launch
+        // guarantees they are all resident (one per SM, grid <= SM count).
+        // Where the device refuses it (fewer SMs granted to this context),
+        // the caller runs the separate finalize kernel instead.
+        void *kargs[] = {const_cast<TcArgs *>(&args)};
+        const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3(grid),
+                                                          dim3(kThreads), kargs, pl.smem, s);
+        if (e == cudaErrorCooperativeLaunchTooLarge) {
+            (void)cudaGetLastError();
+            return CONV_EPI_ERR_UNSUPPORTED;
+        }
+        CE_CUDA(e);
+    } else {
+        k<<<grid, kThreads, pl.smem, s>>>(args);
+    }
     CE_CUDA(cudaGetLastError());
     return CONV_EPI_OK;
 }
@@ -1460,6 +1579,20 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
         if (h->gn.units != a.units_per_img || a.Wp > 32) return CONV_EPI_ERR_INVALID_ARG;
+        // finalize inside the kernel when each (image, group) block of pooled
+        // values is whole float4s (16-byte aligned blocks) and small enough
+        // for the multiply-high divisions (t < 2^18 pooled float4 per batch,
+        // channel offsets < 2^16); otherwise the separate finalize kernel
+        const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
+        a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
+                    (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
+                       ? 1 : 0;
+        a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
+        a.inv_cnt = 1.0 / ((double)(d.Cout / e.groups) * h->Ho * h->Wo);
+        a.per_magic = (uint32_t)((((uint64_t)1 << 32) + per - 1) / per);
+        const uint32_t F4 = F / 4 ? F / 4 : 1;
+        a.f4_magic = (uint32_t)((((uint64_t)1 << 32) + F4 - 1) / F4);
+        if (a.gn_fin) CE_CUDA(cudaMemsetAsync(h->gn.arrive, 0, sizeof(unsigned), s));
     }
     const int grid = a.total_units < h->sm_count ? a.total_units : h->sm_count;
     conv_epi_status st;
@@ -1467,12 +1600,18 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     case CONV_EPI_MIN_TANH2: st = launch_tc<CONV_EPI_MIN_TANH2>(args, pl, grid, s); break;
     case CONV_EPI_SCALE_MIN: st = launch_tc<CONV_EPI_SCALE_MIN>(args, pl, grid, s); break;
     case CONV_EPI_MUL_LRELU_GELU: st = launch_tc<CONV_EPI_MUL_LRELU_GELU>(args, pl, grid, s); break;
-    case CONV_EPI_GN_SCALE_POOL_CLAMP: st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s); break;
+    case CONV_EPI_GN_SCALE_POOL_CLAMP:
+        st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
+        if (st == CONV_EPI_ERR_UNSUPPORTED && a.gn_fin) {  // cooperative launch refused: finalize separately
+            a.gn_fin = 0;
+            st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
+        }
+        break;
     default: return CONV_EPI_ERR_INVALID_ARG;
     }
     if (st) return st;
     h->last_launches = 2;
-    if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
+    if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
         if ((st = gn_finalize(h, e, out, s, true))) return st;
         h->last_launches = 3;
     }
