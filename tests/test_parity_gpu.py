@@ -43,11 +43,16 @@ SMALL = {
     "c3_cout1": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=32, Cout=1),      # a single per-channel row
     "c5_w16": W["c5_gn_pool_clamp"].resized(N=2, H=10, W=16),                # 3 pooled columns, 2 pooled rows
     "c5_one_band": W["c5_gn_pool_clamp"].resized(N=1, H=6),                  # one pooling band per image
+    # rows wider than one tile (the tf32 path splits them into column tiles of 252 outputs)
+    "c2_w300": W["c2_min_tanh2"].resized(N=1, H=6, W=300),                   # 2 tiles: 252 + 46 columns
+    "c3_w520": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=520),              # 3 tiles, per-channel stores
+    "c4_w516": W["c4_scale_min"].resized(N=2, H=4, W=516, scalar=-1.0),      # 3 tiles, Cout 128, max branch
+    "c5_w260": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=260),              # GroupNorm: one tile only (refused in tf32)
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 # shapes the tf32 kernel refuses (its GroupNorm epilogue pools one band of four
 # rows per unit, which needs 64 < W <= 128): the call must say so, not fall back
-TF32_REFUSED = {"c5_w16"}
+TF32_REFUSED = {"c5_w16", "c5_w260"}
 
 
 def modes():

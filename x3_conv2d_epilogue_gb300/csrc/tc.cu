@@ -89,6 +89,7 @@ struct Cfg {
     int S, P, U, RU, Rin, PL, ucol;
     uint32_t p_magic;  // ceil(2^32 / P): exact q / P for q < 2^16
     int chunks, units_per_img, total_units;
+    int CT, CW, BW;    // column tiles per row block, output columns per tile, staged tile width (NCHW)
     int resident;      // 1: the whole packed filter stays in shared memory
     int na, nb, nr;    // ring depths: filter stages (streaming), B planes, staged tiles
     uint32_t a_bytes, b_bytes, raw_bytes, raw_tx;  // raw_tx: exact bytes of one staged tile
@@ -112,7 +113,7 @@ struct Cfg {
 };
 
 struct TcArgs {        // 64-byte aligned through CUtensorMap
-    CUtensorMap xmap;  // x as a 4-D tensor (W, H, Cin, N); box (W, Rin, 8, 1)
+    CUtensorMap xmap;  // x as a 4-D tensor: (W, H, Cin, N) with box (BW, Rin, 8, 1), or channels last
     Cfg c;
 };
 
@@ -348,9 +349,10 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag
     }
 }
 
-// (image, row block) of unit blockIdx.x + k * gridDim.x, stepped without
-// divisions: the row block advances by the grid size and wraps into the image
-// index (units_per_img >= 1)
+// (image, unit within the image) of unit blockIdx.x + k * gridDim.x, stepped
+// without divisions: the index advances by the grid size and wraps into the
+// image index (units_per_img >= 1).  A unit within the image is a row block
+// and, for rows wider than one tile, a column tile: ru = rb * CT + ct.
 struct UnitPos {
     int n, ru;
     __device__ void init(int unit, int upi) { n = unit / upi, ru = unit % upi; }
@@ -358,6 +360,9 @@ struct UnitPos {
         ru += stride;
         while (ru >= upi) ru -= upi, ++n;
     }
+    // row block and column tile (no division for a single column tile)
+    __device__ __forceinline__ int rb(int CT) const { return CT == 1 ? ru : ru / CT; }
+    __device__ __forceinline__ int ct(int CT) const { return CT == 1 ? 0 : ru - (ru / CT) * CT; }
 };
 
 // ---------------------------------------------------------- barriers ----
@@ -489,9 +494,11 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
 // the longer latency; it sleeps briefly when neither can move, and gives up
 // like every other wait after kWaitLimitNs without progress.  Once only the
 // tiles are left (always, with a resident filter) it blocks in wait_bar.
+template <bool TILED>
 __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *xmap, uint32_t sbase, const Bars &bars,
                                               volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
+    const int CT = TILED ? a.CT : 1;  // column tiles per row block (a constant 1 for rows of one tile)
     prefetch_tensormap(xmap);
     if (a.resident) {
         const uint32_t total = a.chunks * a.a_bytes;
@@ -532,10 +539,12 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
                 if (a.nhwc) {
                     // x as (C, W, H, N): channels 8c..8c+3 and 8c+4..8c+7 of
                     // rows r0.., columns 0..P-1 (past W and H: zeros)
-                    tma_load_4d(dst, xmap, 8 * cr, 0, pos.ru * a.RU, pos.n, t_full(sr));
-                    tma_load_4d(dst + 16u * a.PL, xmap, 8 * cr + 4, 0, pos.ru * a.RU, pos.n, t_full(sr));
+                    const int c0 = pos.ct(CT) * a.CW, r0 = pos.rb(CT) * a.RU;
+                    tma_load_4d(dst, xmap, 8 * cr, c0, r0, pos.n, t_full(sr));
+                    tma_load_4d(dst + 16u * a.PL, xmap, 8 * cr + 4, c0, r0, pos.n, t_full(sr));
                 } else {
-                    tma_load_4d(dst, xmap, 0, pos.ru * a.RU, 8 * cr, pos.n, t_full(sr));
+                    // the tile's first column (a multiple of 4: 16-byte aligned)
+                    tma_load_4d(dst, xmap, pos.ct(CT) * a.CW, pos.rb(CT) * a.RU, 8 * cr, pos.n, t_full(sr));
                 }
                 r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
             } else {
@@ -598,7 +607,7 @@ __device__ __forceinline__ void converter_role(const Cfg &a, uint8_t *smem, cons
     if (a.nhwc) return;  // channels-last tiles arrive in the B layout
     const int cw = conv_index(threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const int P = a.P, W = a.W, Rin = a.Rin, PL = a.PL;
+    const int P = a.P, W = a.BW, Rin = a.Rin, PL = a.PL;  // W: the staged tile's row length
     const int ps = Rin * W;             // floats between channels of a staged tile
     const int mP = (P + 31) >> 5;       // 32-position groups per input row
     const int nrc = 2 * Rin * mP;       // items per chunk
@@ -802,7 +811,7 @@ __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + e
 // bytes; lane l stores columns c2, c2+1 (c2 = 2 (l & 7)) of channels
 // l/8 + 4 rp, rp = 0..7.
 __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, float bias, float mult, int lane, int qd,
-                                               int ew, bool row_ok, int col0, float *orow, size_t cstride4,
+                                               int ew, bool row_ok, int col0, float *orow, size_t cstride4, int wv,
                                                float *scratch) {
     {
         float *stg = scratch + ew * 32 * kStgPitch;
@@ -821,8 +830,9 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
             // rp < nrp: this lane's channels cb + 4 rp below Co (all 8 unless the GEMM is padded)
             const int cb0 = (qd * 32) % a.Cout + (lane >> 3);
             const int nrp = a.Co >= a.Cout ? 8 : max(0, min(8, (a.Co - cb0 + 3) >> 2));
+            // wv: the output columns of this column tile (Wo for a single tile)
             if ((a.Wo & 1) == 0) {
-                if (col0 + c2 < a.Wo) {
+                if (col0 + c2 < wv) {
 #pragma unroll
                     for (int rp = 0; rp < 8; ++rp)
                         if (rp < nrp)
@@ -833,8 +843,8 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
 #pragma unroll
                 for (int rp = 0; rp < 8; ++rp) {
                     if (rp >= nrp) break;
-                    if (col0 + c2 < a.Wo) dst[rp * cstride4] = src[4 * rp * kStgPitch];
-                    if (col0 + c2 + 1 < a.Wo) dst[rp * cstride4 + 1] = src[4 * rp * kStgPitch + 1];
+                    if (col0 + c2 < wv) dst[rp * cstride4] = src[4 * rp * kStgPitch];
+                    if (col0 + c2 + 1 < wv) dst[rp * cstride4 + 1] = src[4 * rp * kStgPitch + 1];
                 }
             }
         }
@@ -842,7 +852,7 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
     }
 }
 
-template <int KIND>
+template <int KIND, bool TILED>
 __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, const Bars &bars, uint32_t tmem,
                               volatile int *abort_flag) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -893,11 +903,12 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // out together instead of one row after another.  Scratch row k of the
     // unit (k = u * 4 + quadrant) holds quadrant partials; row slot s of u
     // uses quadrants s * qps .. s * qps + qps - 1.
-    auto combine_min = [&](int pn, int pr0) {
+    auto combine_min = [&](int pn, int pr0, int pc0) {
         const int qps = 4 / a.S;  // quadrants per slot
         const int nq = a.U * 4;   // scratch rows of the unit (<= 32)
-        float *orow0 = a.out + ((size_t)pn * a.Ho + pr0) * a.Wo;
-        for (int col = et; col < a.Wo; col += kEpiThreads)
+        const int wv = TILED ? min(a.CW, a.Wo - pc0) : a.Wo;  // the column tile's output columns
+        float *orow0 = a.out + ((size_t)pn * a.Ho + pr0) * a.Wo + (TILED ? pc0 : 0);
+        for (int col = et; col < wv; col += kEpiThreads)
             for (int kb = 0; kb < nq; kb += kMaxQ) {  // two u at a time (nq is a multiple of 4)
                 float pv[kMaxQ];
 #pragma unroll
@@ -924,14 +935,16 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 }
             }
     };
-    int prev_n = -1, prev_r0 = 0;  // min chains: the unit whose combine is still due
+    int prev_n = -1, prev_r0 = 0, prev_c0 = 0;  // min chains: the unit whose combine is still due
     int j = 0;
     UnitPos pos;
     pos.init(blockIdx.x, a.units_per_img);
     for (int unit = blockIdx.x; unit < a.total_units; unit += gridDim.x, ++j, pos.step(gridDim.x, a.units_per_img)) {
         const int n = pos.n;
-        const int ru = pos.ru;
-        const int r0 = ru * a.RU;
+        const int ru = pos.ru;                  // (GroupNorm: one column tile, so also the row block)
+        const int CT = TILED ? a.CT : 1;        // a constant 1 for rows of one tile
+        const int r0 = pos.rb(CT) * a.RU;       // first output row of the unit
+        const int c0 = pos.ct(CT) * a.CW;       // first output column of the unit
         const int ab = j & 1;
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
         if (epi_bar_any(!ok)) {  // all epilogue warps leave together
@@ -1023,7 +1036,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     // in flight (its partials were made visible by the barrier
                     // at the top of this unit); the barrier after it keeps this
                     // unit's partial stores behind every thread's reads
-                    if (prev_n >= 0) combine_min(prev_n, prev_r0);
+                    if (prev_n >= 0) combine_min(prev_n, prev_r0, prev_c0);
                     epi_bar();
                 }
                 if (q < nbt) {
@@ -1055,7 +1068,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // 16-column chunks cc = hc, hc + 2, ...: the load of the next
                 // chunk is in flight while this one is processed
                 const bool row_ok = row < a.Ho;
-                float *orow = a.out + (((size_t)n * a.Co + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + 2 * (lane & 7);
+                float *orow = a.out + (((size_t)n * a.Co + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + c0 + 2 * (lane & 7);
+                const int wv = TILED ? min(a.CW, a.Wo - c0) : a.Wo;  // the column tile's output columns
                 const uint32_t tb = tbase + u * a.ucol;
                 int cc = hc;
                 Frag16 cur, nxt;
@@ -1066,7 +1080,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 for (; cc < nchunks; cc += 2) {
                     const bool more = cc + 2 < nchunks;
                     if (more) tmem_ld16_issue(tb + (cc + 2) * 16, nxt);
-                    epi_chunk_chan(a, cur, bias, mult, lane, qd, ew, row_ok, cc * 16, orow, cstride4, scratch);
+                    epi_chunk_chan(a, cur, bias, mult, lane, qd, ew, row_ok, cc * 16, orow, cstride4, wv, scratch);
                     if (more) {
                         tmem_ld_wait(nxt);
                         cur = nxt;
@@ -1083,7 +1097,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // this unit's partial minima are in scratch; they are combined
             // during the next unit's first tensor-memory loads (or after the
             // loop, for the last unit)
-            prev_n = n, prev_r0 = r0;
+            prev_n = n, prev_r0 = r0, prev_c0 = c0;
         } else if constexpr (kGN) {
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
@@ -1156,7 +1170,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     if constexpr (kMin) {
         if (prev_n >= 0) {  // the last unit's combine
             epi_bar();
-            combine_min(prev_n, prev_r0);
+            combine_min(prev_n, prev_r0, prev_c0);
         }
     }
 }
@@ -1254,7 +1268,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     }
 }
 
-template <int KIND>
+template <int KIND, bool TILED>
 __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant__ TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Cfg a = args.c;
@@ -1305,12 +1319,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         if (lane == 0) mma_role(a, sbase, bars, tmem, abort_flag);
         __syncwarp();
     } else if (warp == kProducerWarp) {
-        if (lane == 0) producer_role(a, &args.xmap, sbase, bars, abort_flag);
+        if (lane == 0) producer_role<TILED>(a, &args.xmap, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         converter_role(a, smem, bars, abort_flag);
     } else {
-        epilogue_role<KIND>(a, scratch, bars, tmem, abort_flag);
+        epilogue_role<KIND, TILED>(a, scratch, bars, tmem, abort_flag);
     }
 
     tc_fence_before();
@@ -1359,6 +1373,7 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
 // ----------------------------------------------------------- planning ----
 struct Plan {
     int S, P, U, RU, Rin, PL, chunks, ucol;
+    int CT, CW, BW;  // column tiles, output columns per tile, staged tile width
     int resident, na, nb, nr;
     uint32_t a_bytes, b_bytes, raw_bytes, scratch_bytes;
     uint32_t a_off, b_off, raw_off, bar_off, scratch_off;
@@ -1388,12 +1403,24 @@ int gemm_cout(int Cout) { return Cout <= 64 ? 64 : 128; }
 
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (d.Cout < 1 || d.Cout > 128) return false;
-    if (d.Cin < 1 || d.W % 4 != 0 || d.W > 256 || d.H < 3) return false;
+    if (d.Cin < 1 || d.W % 4 != 0 || d.H < 3) return false;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
     if (nhwc && d.Cin % 4 != 0) return false;  // 16-byte position stride
     const int Cg = gemm_cout(d.Cout);
     pl.S = 128 / Cg;
-    pl.P = (d.W + 15) / 16 * 16;
+    if (d.W <= 256) {
+        // one tile spans the row
+        pl.P = (d.W + 15) / 16 * 16;
+        pl.CT = 1, pl.CW = d.W - 2, pl.BW = d.W;
+    } else {
+        // column tiles of 252 outputs from 256 staged columns (the last two
+        // unused; tiles start on multiples of 4 columns, 16-byte aligned);
+        // past the image's right edge the tensor load fills zeros
+        if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP) return false;
+        pl.P = 256;
+        pl.CW = 252, pl.BW = 256;
+        pl.CT = (d.W - 2 + pl.CW - 1) / pl.CW;
+    }
     pl.ucol = (pl.P + 31) / 32 * 32;
     pl.U = kAccStride / pl.ucol;
     pl.RU = pl.U * pl.S;
@@ -1405,7 +1432,7 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (!nhwc && 2 * pl.Rin * ((pl.P + 31) / 32) > kConvItems * kConvWarps) return false;  // converter items per chunk
     pl.a_bytes = up1k(3u * 2u * (2 * pl.S + 1) * Cg * 16u);
     pl.b_bytes = up1k(2u * pl.PL * 16u);
-    pl.raw_bytes = nhwc ? 0u : up1k(8u * pl.Rin * d.W * 4u);  // channels last: no staging ring
+    pl.raw_bytes = nhwc ? 0u : up1k(8u * pl.Rin * pl.BW * 4u);  // channels last: no staging ring
     pl.scratch_bytes = scratch_bytes_for(kind, pl.U, pl.P);
     const uint32_t tail = 8u * Bars::kCount + 16u + pl.scratch_bytes;
     auto total = [&](int na, int nb, int nr) {
@@ -1460,9 +1487,13 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
+// rows of one tile and rows split into column tiles run separate
+// instantiations, so the common case carries none of the tiling arithmetic
+// (the GroupNorm chain never tiles)
 template <int KIND>
 conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStream_t s) {
-    auto k = tc_conv_epi<KIND>;
+    auto k = (KIND != CONV_EPI_GN_SCALE_POOL_CLAMP && args.c.CT > 1) ? tc_conv_epi<KIND, true>
+                                                                      : tc_conv_epi<KIND, false>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
     if (args.c.gn_fin) {
         // the in-kernel finalize waits for every CTA: a cooperative launch
@@ -1522,7 +1553,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     Cfg &a = args.c;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
     {
-        // NCHW: x as (W, H, C, N), box (W, Rin, 8, 1) -> staging [8][Rin][W].
+        // NCHW: x as (W, H, C, N), box (BW, Rin, 8, 1) -> staging [8][Rin][BW]
+        // (BW = W, or 256 per column tile of a wider row).
         // NHWC: x as (C, W, H, N), box (4, P, Rin, 1) -> a B plane [Rin][P][4]
         // (columns W..P-1, rows past H and channels past Cin read as zeros).
         cuuint64_t dims[4], strides[3];
@@ -1536,7 +1568,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
             dims[0] = (cuuint64_t)d.W, dims[1] = (cuuint64_t)d.H, dims[2] = (cuuint64_t)d.Cin, dims[3] = (cuuint64_t)d.N;
             strides[0] = (cuuint64_t)d.W * 4, strides[1] = (cuuint64_t)d.W * d.H * 4,
             strides[2] = (cuuint64_t)d.W * d.H * d.Cin * 4;
-            box[0] = (cuuint32_t)d.W, box[1] = (cuuint32_t)pl.Rin, box[2] = 8u, box[3] = 1u;
+            box[0] = (cuuint32_t)pl.BW, box[1] = (cuuint32_t)pl.Rin, box[2] = 8u, box[3] = 1u;
         }
         const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
         const CUresult r = enc(&args.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims, strides, box,
@@ -1559,11 +1591,12 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.S = pl.S, a.P = pl.P, a.U = pl.U, a.RU = pl.RU, a.Rin = pl.Rin, a.PL = pl.PL, a.ucol = pl.ucol;
     a.p_magic = (uint32_t)((((uint64_t)1 << 32) + pl.P - 1) / pl.P);
     a.chunks = pl.chunks;
-    a.units_per_img = (h->Ho + pl.RU - 1) / pl.RU;
+    a.CT = pl.CT, a.CW = pl.CW, a.BW = pl.BW;
+    a.units_per_img = (h->Ho + pl.RU - 1) / pl.RU * pl.CT;
     a.total_units = d.N * a.units_per_img;
     a.resident = pl.resident, a.na = pl.na, a.nb = pl.nb, a.nr = pl.nr;
     a.a_bytes = pl.a_bytes, a.b_bytes = pl.b_bytes, a.raw_bytes = pl.raw_bytes;
-    a.raw_tx = nhwc ? 2u * 4u * pl.P * pl.Rin * 4u : 8u * pl.Rin * d.W * 4u;  // bytes one tile delivers
+    a.raw_tx = nhwc ? 2u * 4u * pl.P * pl.Rin * 4u : 8u * pl.Rin * pl.BW * 4u;  // bytes one tile delivers
     a.nhwc = nhwc ? 1 : 0;
     a.a_off = pl.a_off, a.b_off = pl.b_off, a.raw_off = pl.raw_off, a.bar_off = pl.bar_off;
     a.scratch_off = pl.scratch_off;
