@@ -55,7 +55,6 @@
 #include <cuda.h>
 #include <math.h>
 #include <stdint.h>
-#include <string.h>
 
 #include "gn_common.cuh"
 #include "internal.h"
@@ -1474,16 +1473,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// the driver's tensor-map encoder, looked up once (a function-local static:
+// initialised exactly once even when several host threads call first)
 EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1548,8 +1549,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (!make_plan(d, e.kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return CONV_EPI_ERR_CUDA;
-    TcArgs args;
-    memset(&args, 0, sizeof args);
+    TcArgs args{};  // value-initialised: zeros, and the workspace pointers' defaults
     Cfg &a = args.c;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
     {
