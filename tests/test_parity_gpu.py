@@ -48,6 +48,10 @@ SMALL = {
     "c3_w520": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=520),              # 3 tiles, per-channel stores
     "c4_w516": W["c4_scale_min"].resized(N=2, H=4, W=516, scalar=-1.0),      # 3 tiles, Cout 128, max branch
     "c5_w260": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=260),              # GroupNorm: one tile only (refused in tf32)
+    # more than 128 output channels (the tf32 path runs channel tiles of 128)
+    "c4_co256": W["c4_scale_min"].resized(N=1, H=5, W=64, Cout=256),        # 2 channel tiles, atomic minimum
+    "c3_co200": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=64, Cout=200),   # 2 tiles, the second padded
+    "c2_co300_w300": W["c2_min_tanh2"].resized(N=1, H=4, W=300, Cout=300),  # 3 channel x 2 column tiles
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 # shapes the tf32 kernel refuses (its GroupNorm epilogue pools one band of four

@@ -89,6 +89,7 @@ struct Cfg {
     uint32_t p_magic;  // ceil(2^32 / P): exact q / P for q < 2^16
     int chunks, units_per_img, total_units;
     int CT, CW, BW;    // column tiles per row block, output columns per tile, staged tile width (NCHW)
+    int MT;            // output-channel tiles of 128 (Cout > 128), each its own unit
     int resident;      // 1: the whole packed filter stays in shared memory
     int na, nb, nr;    // ring depths: filter stages (streaming), B planes, staged tiles
     uint32_t a_bytes, b_bytes, raw_bytes, raw_tx;  // raw_tx: exact bytes of one staged tile
@@ -250,6 +251,12 @@ __device__ __forceinline__ uint64_t add2u(uint64_t a, uint64_t b) {
     return d;
 }
 __device__ __forceinline__ float2 fma2(uint64_t a, uint64_t b, uint64_t c) { return unpack2(fma2u(a, b, c)); }
+// atomic minimum of a float in global memory: non-negative floats order like
+// their bit patterns as signed integers, negative ones in reverse as unsigned
+__device__ __forceinline__ void atomic_min_f32(float *p, float v) {
+    if (v >= 0.0f) atomicMin(reinterpret_cast<int *>(p), __float_as_int(v));
+    else atomicMax(reinterpret_cast<unsigned *>(p), __float_as_uint(v));
+}
 // minimum / maximum of three (NaN operands are ignored, as by fminf / fmaxf)
 __device__ __forceinline__ float fmin3(float x, float y, float z) {
     float r;
@@ -351,7 +358,9 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag
 // (image, unit within the image) of unit blockIdx.x + k * gridDim.x, stepped
 // without divisions: the index advances by the grid size and wraps into the
 // image index (units_per_img >= 1).  A unit within the image is a row block
-// and, for rows wider than one tile, a column tile: ru = rb * CT + ct.
+// and, for rows wider than one tile, a column tile, and for more than 128
+// output channels a channel tile (the fastest index, so the units that share
+// an input tile run side by side and find it in L2).
 struct UnitPos {
     int n, ru;
     __device__ void init(int unit, int upi) { n = unit / upi, ru = unit % upi; }
@@ -359,9 +368,11 @@ struct UnitPos {
         ru += stride;
         while (ru >= upi) ru -= upi, ++n;
     }
-    // row block and column tile (no division for a single column tile)
-    __device__ __forceinline__ int rb(int CT) const { return CT == 1 ? ru : ru / CT; }
-    __device__ __forceinline__ int ct(int CT) const { return CT == 1 ? 0 : ru - (ru / CT) * CT; }
+    // ru = (rb * CT + ct) * MT + mt: row block, column tile and channel tile
+    // (no division when CT = MT = 1, the compile-time case of the fast path)
+    __device__ __forceinline__ int mt(int MT) const { return MT == 1 ? 0 : ru % MT; }
+    __device__ __forceinline__ int ct(int CT, int MT) const { return CT == 1 ? 0 : (MT == 1 ? ru : ru / MT) % CT; }
+    __device__ __forceinline__ int rb(int CT, int MT) const { return (MT == 1 ? ru : ru / MT) / CT; }
 };
 
 // ---------------------------------------------------------- barriers ----
@@ -493,11 +504,11 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
 // the longer latency; it sleeps briefly when neither can move, and gives up
 // like every other wait after kWaitLimitNs without progress.  Once only the
 // tiles are left (always, with a resident filter) it blocks in wait_bar.
-template <bool TILED>
+template <bool GENERAL>
 __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *xmap, uint32_t sbase, const Bars &bars,
                                               volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
-    const int CT = TILED ? a.CT : 1;  // column tiles per row block (a constant 1 for rows of one tile)
+    const int CT = GENERAL ? a.CT : 1, MT = GENERAL ? a.MT : 1;  // (constants 1 on the fast path)
     prefetch_tensormap(xmap);
     if (a.resident) {
         const uint32_t total = a.chunks * a.a_bytes;
@@ -522,8 +533,10 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
     uint32_t r_iss = 0, r_par = 0, a_iss = 0, a_par = 0;
     int ir = 0, ia = a.resident ? total : 0;  // next raw tile / next filter chunk
     int cr = 0, ca = 0;                       // chunk of tile ir / of filter chunk ia
-    UnitPos pos;                              // (image, row block) of tile ir
+    UnitPos pos;                              // (image, unit) of tile ir
     pos.init(blockIdx.x, a.units_per_img);
+    UnitPos fpos;                             // (image, unit) of filter chunk ia (channel tile)
+    fpos.init(blockIdx.x, a.units_per_img);
     uint64_t t_idle = 0;
     while (ir < total || ia < total) {
         bool moved = false;
@@ -538,12 +551,12 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
                 if (a.nhwc) {
                     // x as (C, W, H, N): channels 8c..8c+3 and 8c+4..8c+7 of
                     // rows r0.., columns 0..P-1 (past W and H: zeros)
-                    const int c0 = pos.ct(CT) * a.CW, r0 = pos.rb(CT) * a.RU;
+                    const int c0 = pos.ct(CT, MT) * a.CW, r0 = pos.rb(CT, MT) * a.RU;
                     tma_load_4d(dst, xmap, 8 * cr, c0, r0, pos.n, t_full(sr));
                     tma_load_4d(dst + 16u * a.PL, xmap, 8 * cr + 4, c0, r0, pos.n, t_full(sr));
                 } else {
                     // the tile's first column (a multiple of 4: 16-byte aligned)
-                    tma_load_4d(dst, xmap, pos.ct(CT) * a.CW, pos.rb(CT) * a.RU, 8 * cr, pos.n, t_full(sr));
+                    tma_load_4d(dst, xmap, pos.ct(CT, MT) * a.CW, pos.rb(CT, MT) * a.RU, 8 * cr, pos.n, t_full(sr));
                 }
                 r_iss |= 1u << sr, r_par = (r_par & ~(1u << sr)) | (pr << sr);
             } else {
@@ -558,8 +571,11 @@ __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *x
         }
         if (ia < total && mbar_try_wait(bars.a_empty(sa), pa ^ 1)) {
             const uint32_t dst = sbase + a.a_off + sa * a.a_bytes;
-            const char *src = wsrc + (size_t)ca * a.a_bytes;
-            if (++ca == a.chunks) ca = 0;
+            const char *src = wsrc + ((size_t)fpos.mt(MT) * a.chunks + ca) * a.a_bytes;
+            if (++ca == a.chunks) {
+                ca = 0;
+                if (GENERAL) fpos.step(gridDim.x, a.units_per_img);
+            }
             mbar_arrive_expect_tx(bars.a_full(sa), a.a_bytes);
             for (uint32_t off = 0; off < a.a_bytes; off += 16384u)
                 bulk_g2s(dst + off, src + off, min(16384u, a.a_bytes - off), bars.a_full(sa));
@@ -811,7 +827,7 @@ __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + e
 // l/8 + 4 rp, rp = 0..7.
 __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, float bias, float mult, int lane, int qd,
                                                int ew, bool row_ok, int col0, float *orow, size_t cstride4, int wv,
-                                               float *scratch) {
+                                               int co_left, float *scratch) {
     {
         float *stg = scratch + ew * 32 * kStgPitch;
 #pragma unroll
@@ -826,9 +842,10 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
             const int c2 = 2 * (lane & 7);
             const float *src = stg + (lane >> 3) * kStgPitch + c2;
             float *dst = orow + col0;
-            // rp < nrp: this lane's channels cb + 4 rp below Co (all 8 unless the GEMM is padded)
+            // rp < nrp: this lane's channels cb + 4 rp below the tile's real
+            // channels co_left (all 8 unless the GEMM is padded)
             const int cb0 = (qd * 32) % a.Cout + (lane >> 3);
-            const int nrp = a.Co >= a.Cout ? 8 : max(0, min(8, (a.Co - cb0 + 3) >> 2));
+            const int nrp = co_left >= a.Cout ? 8 : max(0, min(8, (co_left - cb0 + 3) >> 2));
             // wv: the output columns of this column tile (Wo for a single tile)
             if ((a.Wo & 1) == 0) {
                 if (col0 + c2 < wv) {
@@ -851,7 +868,7 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
     }
 }
 
-template <int KIND, bool TILED>
+template <int KIND, bool GENERAL>
 __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, const Bars &bars, uint32_t tmem,
                               volatile int *abort_flag) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -861,11 +878,14 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int hc = ew >> 2;           // column group: chunks cc = hc, hc + 2, ...
     const int L = qd * 32 + lane;     // accumulator row
     const int slot = L / a.Cout, co = L % a.Cout;
-    const bool real = co < a.Co;      // channels Co..Cout-1 pad the GEMM (zero filters)
-    const float bias = real ? __ldg(&a.b[co]) : 0.0f;
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
-    const float mult = KIND == CONV_EPI_MUL_LRELU_GELU && real ? __ldg(&a.chan_scale[co]) : 0.0f;
+    // this lane's channel parameters; with more than 128 output channels they
+    // belong to the unit's channel tile and are reloaded when it changes
+    // (channels Co.. pad the GEMM with zero filters)
+    int cbase = 0;                    // first channel of the current channel tile
+    float bias = co < a.Co ? __ldg(&a.b[co]) : 0.0f;
+    float mult = KIND == CONV_EPI_MUL_LRELU_GELU && co < a.Co ? __ldg(&a.chan_scale[co]) : 0.0f;
     const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
     const uint64_t gg2 = pack2(__float_as_uint(gsg), __float_as_uint(gsg));
     const uint64_t gb2 = pack2(__float_as_uint(gsg * bias), __float_as_uint(gsg * bias));
@@ -875,13 +895,16 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // chain's minimum over channels is of scalar * y: the scalar goes in
     // first, so a negative scalar needs no separate max.
     uint64_t sb2[4];
+    auto load_sb2 = [&](int cb0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int ch = (qd * 32 + (lane >> 2) + 8 * k) % a.Cout;
-        // a padding channel never wins the minimum
-        const float v = !kMin ? 0.0f : ch < a.Co ? a.scalar * __ldg(&a.b[ch]) : INFINITY;
-        sb2[k] = pack2(__float_as_uint(v), __float_as_uint(v));
-    }
+        for (int k = 0; k < 4; ++k) {
+            const int ch = cb0 + (qd * 32 + (lane >> 2) + 8 * k) % a.Cout;
+            // a padding channel never wins the minimum
+            const float v = !kMin ? 0.0f : ch < a.Co ? a.scalar * __ldg(&a.b[ch]) : INFINITY;
+            sb2[k] = pack2(__float_as_uint(v), __float_as_uint(v));
+        }
+    };
+    load_sb2(0);
     const uint64_t ss = pack2(__float_as_uint(a.scalar), __float_as_uint(a.scalar));
     // per-channel chain: this lane's stores go to channels cb + 4 rp
     const int cb = (qd * 32) % a.Cout + (lane >> 3);
@@ -902,11 +925,18 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // out together instead of one row after another.  Scratch row k of the
     // unit (k = u * 4 + quadrant) holds quadrant partials; row slot s of u
     // uses quadrants s * qps .. s * qps + qps - 1.
+    // with several channel tiles each one's minimum (tanh∘tanh is increasing,
+    // so it commutes with the minimum) goes in by an atomic minimum on the
+    // output, which starts at +inf
+    auto store_min = [&](float *dst, float v) {
+        if (GENERAL && a.MT > 1) atomic_min_f32(dst, v);
+        else *dst = v;
+    };
     auto combine_min = [&](int pn, int pr0, int pc0) {
         const int qps = 4 / a.S;  // quadrants per slot
         const int nq = a.U * 4;   // scratch rows of the unit (<= 32)
-        const int wv = TILED ? min(a.CW, a.Wo - pc0) : a.Wo;  // the column tile's output columns
-        float *orow0 = a.out + ((size_t)pn * a.Ho + pr0) * a.Wo + (TILED ? pc0 : 0);
+        const int wv = GENERAL ? min(a.CW, a.Wo - pc0) : a.Wo;  // the column tile's output columns
+        float *orow0 = a.out + ((size_t)pn * a.Ho + pr0) * a.Wo + (GENERAL ? pc0 : 0);
         for (int col = et; col < wv; col += kEpiThreads)
             for (int kb = 0; kb < nq; kb += kMaxQ) {  // two u at a time (nq is a multiple of 4)
                 float pv[kMaxQ];
@@ -923,13 +953,13 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         float o = fmin3(pv[k], pv[k + 1], pv[k + 2]);
                         o = fminf(o, pv[k + 3]);
                         if (KIND == CONV_EPI_MIN_TANH2) o = tanh_exp(tanh_exp(o));
-                        if (row < a.Ho) orow0[(size_t)(u) * a.Wo + col] = o;
+                        if (row < a.Ho) store_min(orow0 + (size_t)(u) * a.Wo + col, o);
                     } else {
                         const int row = pr0 + 2 * u;
                         float o0 = fminf(pv[k], pv[k + 1]), o1 = fminf(pv[k + 2], pv[k + 3]);
                         if (KIND == CONV_EPI_MIN_TANH2) o0 = tanh_exp(tanh_exp(o0)), o1 = tanh_exp(tanh_exp(o1));
-                        if (row < a.Ho) orow0[(size_t)(2 * u) * a.Wo + col] = o0;
-                        if (row + 1 < a.Ho) orow0[(size_t)(2 * u + 1) * a.Wo + col] = o1;
+                        if (row < a.Ho) store_min(orow0 + (size_t)(2 * u) * a.Wo + col, o0);
+                        if (row + 1 < a.Ho) store_min(orow0 + (size_t)(2 * u + 1) * a.Wo + col, o1);
                     }
                 }
             }
@@ -941,9 +971,19 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     for (int unit = blockIdx.x; unit < a.total_units; unit += gridDim.x, ++j, pos.step(gridDim.x, a.units_per_img)) {
         const int n = pos.n;
         const int ru = pos.ru;                  // (GroupNorm: one column tile, so also the row block)
-        const int CT = TILED ? a.CT : 1;        // a constant 1 for rows of one tile
-        const int r0 = pos.rb(CT) * a.RU;       // first output row of the unit
-        const int c0 = pos.ct(CT) * a.CW;       // first output column of the unit
+        const int CT = GENERAL ? a.CT : 1, MT = GENERAL ? a.MT : 1;  // constants 1 on the fast path
+        const int r0 = pos.rb(CT, MT) * a.RU;   // first output row of the unit
+        const int c0 = pos.ct(CT, MT) * a.CW;   // first output column of the unit
+        if (GENERAL && MT > 1) {
+            const int cb_unit = pos.mt(MT) * a.Cout;  // the unit's channel tile
+            if (cb_unit != cbase) {
+                cbase = cb_unit;
+                const int ch = cbase + co;
+                bias = ch < a.Co ? __ldg(&a.b[ch]) : 0.0f;
+                mult = KIND == CONV_EPI_MUL_LRELU_GELU && ch < a.Co ? __ldg(&a.chan_scale[ch]) : 0.0f;
+                if (kMin) load_sb2(cbase);
+            }
+        }
         const int ab = j & 1;
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
         if (epi_bar_any(!ok)) {  // all epilogue warps leave together
@@ -1067,8 +1107,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // 16-column chunks cc = hc, hc + 2, ...: the load of the next
                 // chunk is in flight while this one is processed
                 const bool row_ok = row < a.Ho;
-                float *orow = a.out + (((size_t)n * a.Co + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + c0 + 2 * (lane & 7);
-                const int wv = TILED ? min(a.CW, a.Wo - c0) : a.Wo;  // the column tile's output columns
+                float *orow = a.out + (((size_t)n * a.Co + cbase + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + c0 + 2 * (lane & 7);
+                const int wv = GENERAL ? min(a.CW, a.Wo - c0) : a.Wo;  // the column tile's output columns
                 const uint32_t tb = tbase + u * a.ucol;
                 int cc = hc;
                 Frag16 cur, nxt;
@@ -1079,7 +1119,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 for (; cc < nchunks; cc += 2) {
                     const bool more = cc + 2 < nchunks;
                     if (more) tmem_ld16_issue(tb + (cc + 2) * 16, nxt);
-                    epi_chunk_chan(a, cur, bias, mult, lane, qd, ew, row_ok, cc * 16, orow, cstride4, wv, scratch);
+                    epi_chunk_chan(a, cur, bias, mult, lane, qd, ew, row_ok, cc * 16, orow, cstride4, wv, a.Co - cbase,
+                                   scratch);
                     if (more) {
                         tmem_ld_wait(nxt);
                         cur = nxt;
@@ -1267,7 +1308,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     }
 }
 
-template <int KIND, bool TILED>
+template <int KIND, bool GENERAL>
 __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant__ TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Cfg a = args.c;
@@ -1318,12 +1359,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         if (lane == 0) mma_role(a, sbase, bars, tmem, abort_flag);
         __syncwarp();
     } else if (warp == kProducerWarp) {
-        if (lane == 0) producer_role<TILED>(a, &args.xmap, sbase, bars, abort_flag);
+        if (lane == 0) producer_role<GENERAL>(a, &args.xmap, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         converter_role(a, smem, bars, abort_flag);
     } else {
-        epilogue_role<KIND, TILED>(a, scratch, bars, tmem, abort_flag);
+        epilogue_role<KIND, GENERAL>(a, scratch, bars, tmem, abort_flag);
     }
 
     tc_fence_before();
@@ -1369,10 +1410,16 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
     }
 }
 
+// the min chains' output before channel tiles take their atomic minima
+__global__ void fill_f32(float *__restrict__ p, size_t n, float v) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = v;
+}
+
 // ----------------------------------------------------------- planning ----
 struct Plan {
     int S, P, U, RU, Rin, PL, chunks, ucol;
     int CT, CW, BW;  // column tiles, output columns per tile, staged tile width
+    int MT;          // channel tiles
     int resident, na, nb, nr;
     uint32_t a_bytes, b_bytes, raw_bytes, scratch_bytes;
     uint32_t a_off, b_off, raw_off, bar_off, scratch_off;
@@ -1396,13 +1443,17 @@ uint32_t up1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 
 // Shared memory: [filter: resident or ring][B ring][staged-tile ring][mbarriers,
 // tmem slot, abort flag][epilogue scratch]
-// the GEMM's output-channel count: a problem Cout up to 64 runs as 64 (two
-// stacked row slots), up to 128 as 128, with zero filters for the rest
+// the GEMM's output-channel count per channel tile: a problem Cout up to 64
+// runs as 64 (two stacked row slots), larger ones as tiles of 128, with zero
+// filters for the rest
 int gemm_cout(int Cout) { return Cout <= 64 ? 64 : 128; }
+int channel_tiles(int Cout) { return Cout <= 128 ? 1 : (Cout + 127) / 128; }
 
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
-    if (d.Cout < 1 || d.Cout > 128) return false;
+    if (d.Cout < 1) return false;
     if (d.Cin < 1 || d.W % 4 != 0 || d.H < 3) return false;
+    pl.MT = channel_tiles(d.Cout);
+    if (pl.MT > 1 && kind == CONV_EPI_GN_SCALE_POOL_CLAMP) return false;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
     if (nhwc && d.Cin % 4 != 0) return false;  // 16-byte position stride
     const int Cg = gemm_cout(d.Cout);
@@ -1439,7 +1490,9 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     };
     // resident filter when it still leaves 2 B planes and 2 staged tiles
     const int nr0 = nhwc ? 0 : 2;
-    pl.resident = total(pl.chunks, 2, nr0) <= (size_t)kSmemLimit;
+    // (with several channel tiles the units alternate between their filters,
+    // so the filter streams)
+    pl.resident = pl.MT == 1 && total(pl.chunks, 2, nr0) <= (size_t)kSmemLimit;
     const int na_min = pl.resident ? pl.chunks : 2;
     pl.na = na_min, pl.nb = 2, pl.nr = nr0;
     if (total(pl.na, pl.nb, pl.nr) > (size_t)kSmemLimit) return false;
@@ -1488,13 +1541,13 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// rows of one tile and rows split into column tiles run separate
-// instantiations, so the common case carries none of the tiling arithmetic
-// (the GroupNorm chain never tiles)
+// rows of one tile with at most 128 output channels, and everything else
+// (column tiles, channel tiles) run separate instantiations, so the common
+// case carries none of the tiling arithmetic (the GroupNorm chain never tiles)
 template <int KIND>
 conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStream_t s) {
-    auto k = (KIND != CONV_EPI_GN_SCALE_POOL_CLAMP && args.c.CT > 1) ? tc_conv_epi<KIND, true>
-                                                                      : tc_conv_epi<KIND, false>;
+    auto k = (KIND != CONV_EPI_GN_SCALE_POOL_CLAMP && (args.c.CT > 1 || args.c.MT > 1)) ? tc_conv_epi<KIND, true>
+                                                                                         : tc_conv_epi<KIND, false>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
     if (args.c.gn_fin) {
         // the in-kernel finalize waits for every CTA: a cooperative launch
@@ -1533,7 +1586,7 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
 size_t tc_wpack_bytes(const conv_epi_desc &d) {
     const int Cg = gemm_cout(d.Cout), S = 128 / Cg;
     const size_t chunk = ((size_t)3 * 2 * (2 * S + 1) * Cg * 16 + 1023) & ~(size_t)1023;
-    return (size_t)((d.Cin + 7) / 8 + 1) * chunk + 256;
+    return ((size_t)channel_tiles(d.Cout) * ((d.Cin + 7) / 8) + 1) * chunk + 256;
 }
 
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
@@ -1583,16 +1636,21 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         const int threads = 256;
         const int blocks = (int)((total + threads - 1) / threads);
         if (pl.a_bytes != per_chunk * 4) return CONV_EPI_ERR_UNSUPPORTED;  // chunks must pack back to back
-        pack_weights<<<blocks, threads, 0, s>>>(w, h->wpack, d.Cin, gemm_cout(d.Cout), d.Cout, pl.S);
-        CE_CUDA(cudaGetLastError());
+        // channel tile m: filters 128m .. 128m + 127, after the previous tiles' chunks
+        for (int m = 0; m < pl.MT; ++m) {
+            const int Cg = gemm_cout(d.Cout);
+            pack_weights<<<blocks, threads, 0, s>>>(w + (size_t)m * Cg * d.Cin * 9, h->wpack + (size_t)m * total,
+                                                    d.Cin, Cg, min(Cg, d.Cout - m * Cg), pl.S);
+            CE_CUDA(cudaGetLastError());
+        }
     }
     a.x = x, a.b = b, a.wpack = h->wpack, a.out = out, a.err = h->dev_err;
     a.N = d.N, a.Cin = d.Cin, a.H = d.H, a.W = d.W, a.Cout = gemm_cout(d.Cout), a.Co = d.Cout, a.Ho = h->Ho, a.Wo = h->Wo;
     a.S = pl.S, a.P = pl.P, a.U = pl.U, a.RU = pl.RU, a.Rin = pl.Rin, a.PL = pl.PL, a.ucol = pl.ucol;
     a.p_magic = (uint32_t)((((uint64_t)1 << 32) + pl.P - 1) / pl.P);
     a.chunks = pl.chunks;
-    a.CT = pl.CT, a.CW = pl.CW, a.BW = pl.BW;
-    a.units_per_img = (h->Ho + pl.RU - 1) / pl.RU * pl.CT;
+    a.CT = pl.CT, a.CW = pl.CW, a.BW = pl.BW, a.MT = pl.MT;
+    a.units_per_img = (h->Ho + pl.RU - 1) / pl.RU * pl.CT * pl.MT;
     a.total_units = d.N * a.units_per_img;
     a.resident = pl.resident, a.na = pl.na, a.nb = pl.nb, a.nr = pl.nr;
     a.a_bytes = pl.a_bytes, a.b_bytes = pl.b_bytes, a.raw_bytes = pl.raw_bytes;
@@ -1628,6 +1686,14 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         if (a.gn_fin) CE_CUDA(cudaMemsetAsync(h->gn.arrive, 0, sizeof(unsigned), s));
     }
     const int grid = a.total_units < h->sm_count ? a.total_units : h->sm_count;
+    int fills = 0;
+    if (pl.MT > 1 && (e.kind == CONV_EPI_MIN_TANH2 || e.kind == CONV_EPI_SCALE_MIN)) {
+        const size_t n_out = (size_t)d.N * h->Ho * h->Wo;
+        const size_t fb = (n_out + 255) / 256;
+        fill_f32<<<(unsigned)(fb < 4096 ? fb : 4096), 256, 0, s>>>(out, n_out, INFINITY);
+        CE_CUDA(cudaGetLastError());
+        fills = 1;
+    }
     conv_epi_status st;
     switch (e.kind) {
     case CONV_EPI_MIN_TANH2: st = launch_tc<CONV_EPI_MIN_TANH2>(args, pl, grid, s); break;
@@ -1643,10 +1709,10 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     default: return CONV_EPI_ERR_INVALID_ARG;
     }
     if (st) return st;
-    h->last_launches = 2;
+    h->last_launches = pl.MT + 1 + fills;  // packs, fill, conv
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
         if ((st = gn_finalize(h, e, out, s, true))) return st;
-        h->last_launches = 3;
+        h->last_launches += 1;
     }
     return CONV_EPI_OK;
 }
