@@ -1,7 +1,8 @@
 /*
  * conv_epi.h -- fused 3x3 Conv2d + epilogue for NVIDIA GB300 (sm_103a).
  *
- * One call computes, for an NCHW float32 input x[N][Cin][H][W], filter
+ * One call computes, for a float32 input x[N][Cin][H][W] (NCHW; in tf32 mode
+ * also channels last, x[N][H][W][Cin], see conv_epi_layout), filter
  * w[Cout][Cin][3][3] and bias b[Cout],
  *
  *     y[n,co,i,j] = b[co] + sum_{ci,kh,kw} w[co,ci,kh,kw] * x[n,ci,i+kh,j+kw]
@@ -21,8 +22,9 @@
  * output; here the parameters travel in the arguments of conv_epi_forward.
  *
  * Conventions for every entry point:
- *   - Tensors are dense, contiguous, row-major (NCHW), float32, and must start
- *     on a 16-byte boundary.  "device pointer" means memory the current CUDA
+ *   - Tensors are dense, contiguous, row-major (NCHW; x may be NHWC, as the
+ *     description's layout says), float32, and must start on a 16-byte
+ *     boundary.  "device pointer" means memory the current CUDA
  *     device can read (cudaMalloc, torch CUDA tensors); "host pointer" means
  *     ordinary (ideally pinned) host memory.
  *   - The caller owns every tensor it passes; the library owns the handle and
@@ -123,7 +125,16 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
 /* Create a handle for one problem size and mode on the current CUDA device.
  * Validates the description and allocates the workspace every chain needs
  * except the GN chain's pooled buffers, which are allocated on the first GN
- * forward (conv_epi_reserve allocates them up front).  Synchronous. */
+ * forward (conv_epi_reserve allocates them up front).  Synchronous.
+ * Shapes: CONV_EPI_MODE_FP32 takes any N, Cin, Cout and H, W >= 3 (its GN
+ * chain: pool_k 1, 2 or 4 and at most 64 groups).  CONV_EPI_MODE_TF32 takes
+ * any N, Cin, Cout, H >= 3 and W a multiple of 4 (rows wider than 256 run as
+ * column tiles, more than 128 output channels as channel tiles); its GN chain
+ * needs Cout = 64, pool_k = 4 and 64 < W <= 128, and runs as one cooperative
+ * launch (every CTA resident) that finalizes inside the kernel, or, where the
+ * device refuses that launch, with a second finalize kernel.  Shapes outside
+ * these return CONV_EPI_ERR_UNSUPPORTED (at create, or at the first forward
+ * for chain-specific limits). */
 CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi_handle *out);
 
 /* Allocate, ahead of the first forward, whatever workspace `epi` will need
