@@ -251,6 +251,13 @@ __device__ __forceinline__ uint64_t add2u(uint64_t a, uint64_t b) {
     return d;
 }
 __device__ __forceinline__ float2 fma2(uint64_t a, uint64_t b, uint64_t c) { return unpack2(fma2u(a, b, c)); }
+__device__ __forceinline__ uint64_t mul2u(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack2f(float lo, float hi) { return pack2(__float_as_uint(lo), __float_as_uint(hi)); }
+__device__ __forceinline__ uint64_t neg2(uint64_t a) { return a ^ 0x8000000080000000ull; }  // exact
 // atomic minimum of a float in global memory: non-negative floats order like
 // their bit patterns as signed integers, negative ones in reverse as unsigned
 __device__ __forceinline__ void atomic_min_f32(float *p, float v) {
@@ -817,6 +824,28 @@ __device__ __forceinline__ float tanh_exp(float x) {
 }
 // GELU with the exact-erf form 0.5 t (1 + erf(t / sqrt 2))
 __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erf_as7126(t * 0.70710678118654752f)); }
+// The same GELU (erf by 7.1.26 above) on a pair of values: the arithmetic in
+// packed fp32x2 operations, the reciprocal, exponential, absolute value and
+// sign per value.  Each value takes the same operations, in the same order
+// and rounding, as gelu_erf with 1 - poly*e as one fused multiply-add.
+__device__ __forceinline__ float2 gelu_erf2(float t0, float t1) {
+    const uint64_t t = pack2f(t0, t1);
+    const float2 xv = unpack2(mul2u(t, pack2f(0.70710678118654752f, 0.70710678118654752f)));
+    const uint64_t ax = pack2f(fabsf(xv.x), fabsf(xv.y));
+    const float2 dv = unpack2(fma2u(pack2f(0.3275911f, 0.3275911f), ax, pack2f(1.0f, 1.0f)));
+    const uint64_t u = pack2f(__fdividef(1.0f, dv.x), __fdividef(1.0f, dv.y));
+    uint64_t poly = fma2u(pack2f(1.061405429f, 1.061405429f), u, pack2f(-1.453152027f, -1.453152027f));
+    poly = fma2u(poly, u, pack2f(1.421413741f, 1.421413741f));
+    poly = fma2u(poly, u, pack2f(-0.284496736f, -0.284496736f));
+    poly = fma2u(poly, u, pack2f(0.254829592f, 0.254829592f));
+    poly = mul2u(poly, u);
+    const float2 nv = unpack2(mul2u(neg2(ax), ax));  // -x^2
+    const uint64_t e = pack2f(__expf(nv.x), __expf(nv.y));
+    const float2 rv = unpack2(fma2u(neg2(poly), e, pack2f(1.0f, 1.0f)));
+    const uint64_t erfv = pack2f(copysignf(rv.x, xv.x), copysignf(rv.y, xv.y));
+    const uint64_t half_t = mul2u(pack2f(0.5f, 0.5f), t);
+    return unpack2(mul2u(half_t, add2u(pack2f(1.0f, 1.0f), erfv)));
+}
 
 // Per-chunk work of the per-channel chain on 16 accumulator columns: f is a
 // 32x32b fragment (one channel per lane, 16 columns) and orow points at this
@@ -830,12 +859,15 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
                                                int co_left, float *scratch) {
     {
         float *stg = scratch + ew * 32 * kStgPitch;
+        const uint64_t bias2 = pack2f(bias, bias), mult2 = pack2f(mult, mult), slope2 = pack2f(a.slope, a.slope);
+        auto tv2 = [](float2 v) { return pack2f(v.x, v.y); };
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-            float t0 = (__uint_as_float(f.r[i]) + bias) * mult, t1 = (__uint_as_float(f.r[i + 1]) + bias) * mult;
-            t0 = t0 > 0.0f ? t0 : a.slope * t0;
-            t1 = t1 > 0.0f ? t1 : a.slope * t1;
-            *reinterpret_cast<float2 *>(stg + lane * kStgPitch + i) = make_float2(gelu_erf(t0), gelu_erf(t1));
+            // (acc + bias) * mult for two columns, then LeakyReLU per value
+            const float2 tv = unpack2(mul2u(add2u(pack2(f.r[i], f.r[i + 1]), bias2), mult2));
+            const float2 sv = unpack2(mul2u(tv2(tv), slope2));
+            const float t0 = tv.x > 0.0f ? tv.x : sv.x, t1 = tv.y > 0.0f ? tv.y : sv.y;
+            *reinterpret_cast<float2 *>(stg + lane * kStgPitch + i) = gelu_erf2(t0, t1);
         }
         __syncwarp();
         if (row_ok) {
