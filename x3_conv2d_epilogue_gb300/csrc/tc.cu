@@ -799,22 +799,6 @@ __device__ __forceinline__ int colmin16_col(int col0, int lane) {
     return col0 + 8 * ((lane >> 4) & 1) + 2 * (lane & 3) + ((lane >> 3) & 1);
 }
 
-// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
-// 7.1.26: for x >= 0, erf(x) = 1 - (a1 u + a2 u^2 + a3 u^3 + a4 u^4 + a5 u^5)
-// exp(-x^2) with u = 1 / (1 + p x), |error| <= 1.5e-7; erf(-x) = -erf(x).
-// Branch-free (one reciprocal, one exponential, five FMAs), which matters in
-// the per-channel epilogue; the strict fp32 mode keeps the library erff.
-__device__ __forceinline__ float erf_as7126(float x) {
-    const float ax = fabsf(x);
-    const float u = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
-    float poly = fmaf(1.061405429f, u, -1.453152027f);
-    poly = fmaf(poly, u, 1.421413741f);
-    poly = fmaf(poly, u, -0.284496736f);
-    poly = fmaf(poly, u, 0.254829592f);
-    poly *= u;
-    const float r = 1.0f - poly * __expf(-ax * ax);
-    return copysignf(r, x);
-}
 // tanh from its exponential form: tanh|x| = (1 - e) / (1 + e), e = exp(-2|x|),
 // odd in x; about 1e-7 absolute error (no cancellation problem in absolute
 // terms for small |x|, e -> 0 saturates to 1 for large |x|)
@@ -822,12 +806,17 @@ __device__ __forceinline__ float tanh_exp(float x) {
     const float e = __expf(-2.0f * fabsf(x));
     return copysignf(__fdividef(1.0f - e, 1.0f + e), x);
 }
-// GELU with the exact-erf form 0.5 t (1 + erf(t / sqrt 2))
-__device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erf_as7126(t * 0.70710678118654752f)); }
-// The same GELU (erf by 7.1.26 above) on a pair of values: the arithmetic in
-// packed fp32x2 operations, the reciprocal, exponential, absolute value and
-// sign per value.  Each value takes the same operations, in the same order
-// and rounding, as gelu_erf with 1 - poly*e as one fused multiply-add.
+// GELU with the exact-erf form 0.5 t (1 + erf(t / sqrt 2)), on a pair of
+// values.  erf by Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26: for x >= 0, erf(x) = 1 - (a1 u + a2 u^2 + a3 u^3 + a4 u^4 +
+// a5 u^5) exp(-x^2) with u = 1 / (1 + p x), |error| <= 1.5e-7, and
+// erf(-x) = -erf(x): branch-free (one reciprocal, one exponential, five FMAs
+// per value), which matters in the per-channel epilogue; the strict fp32 mode
+// keeps the library erff.  The arithmetic runs in packed fp32x2 operations,
+// the reciprocal, exponential, absolute value and sign per value; each value
+// takes the same operations and roundings as the scalar form
+// 0.5 t (1 + copysign(1 - poly(u) u exp(-x^2), x)), x = t / sqrt 2, with
+// 1 - poly*e as one fused multiply-add.
 __device__ __forceinline__ float2 gelu_erf2(float t0, float t1) {
     const uint64_t t = pack2f(t0, t1);
     const float2 xv = unpack2(mul2u(t, pack2f(0.70710678118654752f, 0.70710678118654752f)));
