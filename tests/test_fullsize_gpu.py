@@ -1,5 +1,6 @@
 """GPU parity at the full workload sizes, in the launch configuration the
-bench times: the whole batch in one conv_epi_forward, both modes.  The oracle
+bench times: the whole batch in one conv_epi_forward, both modes (tf32 also with
+channels-last input).  The oracle
 checks sampled outputs one by one (min chains: whole channel columns;
 per-channel chain: single elements; GroupNorm chain: every pooled output of
 a few whole (image, group) pairs, statistics included), and properties that
@@ -27,15 +28,16 @@ def full(request):
     return wl, t, torch_inputs(t)
 
 
-def run(wl, d, mode):
+def run(wl, d, mode, layout=0):
     import torch
     import x3_conv2d_epilogue_gb300 as ce
     epi = epilogue_for(wl, d)
-    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode)
+    x = d["x"].permute(0, 2, 3, 1).contiguous() if layout == ce.LAYOUT_NHWC else d["x"]
+    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode, layout)
     try:
         out = torch.full(ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, epi, mode), float("nan"),
                          device="cuda", dtype=torch.float32)
-        ce.conv_epi_forward(h, d["x"], d["w"], d["b"], epi, out)
+        ce.conv_epi_forward(h, x, d["w"], d["b"], epi, out)
         ce.conv_epi_sync(h)
     finally:
         ce.conv_epi_destroy(h)
@@ -49,13 +51,14 @@ def close(got, ref, mode):
     return err <= TF32_ATOL + TF32_RTOL * np.abs(ref), err
 
 
-@pytest.mark.parametrize("mode", ["tf32", "fp32"])
+@pytest.mark.parametrize("mode", ["tf32", "fp32", "tf32_nhwc"])
 def test_full_size(full, mode):
     import torch
     import x3_conv2d_epilogue_gb300 as ce
     wl, t, d = full
-    m = ce.MODE_TF32 if mode == "tf32" else ce.MODE_FP32
-    out = run(wl, d, m)
+    m = ce.MODE_FP32 if mode == "fp32" else ce.MODE_TF32
+    out = run(wl, d, m, ce.LAYOUT_NHWC if mode == "tf32_nhwc" else ce.LAYOUT_NCHW)
+    mode = "fp32" if mode == "fp32" else "tf32"  # the tolerance
     assert bool(torch.isfinite(out).all()), "non-finite outputs"
     rng = np.random.default_rng(1234)
     Ho, Wo = wl.H - 2, wl.W - 2
