@@ -83,10 +83,9 @@ struct Cfg {
     const float *x, *b, *wpack;
     float *out;
     unsigned *err;
-    int N, Cin, H, W, Cout, Ho, Wo;  // Cout: the GEMM's (64 or 128); Co: the problem's (<= Cout)
-    int Co;
+    int N, Cin, H, W, Cout, Ho, Wo;  // Cout: the GEMM's per channel tile (64 or 128)
+    int Co;                          // the problem's output channels (<= Cout * MT)
     int S, P, U, RU, Rin, PL, ucol;
-    uint32_t p_magic;  // ceil(2^32 / P): exact q / P for q < 2^16
     int chunks, units_per_img, total_units;
     int CT, CW, BW;    // column tiles per row block, output columns per tile, staged tile width (NCHW)
     int MT;            // output-channel tiles of 128 (Cout > 128), each its own unit
@@ -1403,7 +1402,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
 // wpack[c][kw][jg][p][co][e] = tf32(w[co][8c + 4jg + e][kh][kw]) with
 // kh = S+1-p when 0 <= kh <= 2, else 0 (the zero planes that pad the
 // stacked row slots), 0 for output channels co >= Co (a problem Cout below the
-// GEMM's 64 or 128 is padded with zero filters), and 0 for input channels
+// GEMM's 64 or 128, or the last channel tile's remainder, is padded with zero
+// filters; one launch per channel tile), and 0 for input channels
 // 8c + 4jg + e >= Cin (the last
 // chunk of a Cin that is not a multiple of 8; the input tile's matching
 // channels arrive as zeros too, from the tensor load's out-of-range fill).
@@ -1668,7 +1668,6 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.x = x, a.b = b, a.wpack = h->wpack, a.out = out, a.err = h->dev_err;
     a.N = d.N, a.Cin = d.Cin, a.H = d.H, a.W = d.W, a.Cout = gemm_cout(d.Cout), a.Co = d.Cout, a.Ho = h->Ho, a.Wo = h->Wo;
     a.S = pl.S, a.P = pl.P, a.U = pl.U, a.RU = pl.RU, a.Rin = pl.Rin, a.PL = pl.PL, a.ucol = pl.ucol;
-    a.p_magic = (uint32_t)((((uint64_t)1 << 32) + pl.P - 1) / pl.P);
     a.chunks = pl.chunks;
     a.CT = pl.CT, a.CW = pl.CW, a.BW = pl.BW, a.MT = pl.MT;
     a.units_per_img = (h->Ho + pl.RU - 1) / pl.RU * pl.CT * pl.MT;
