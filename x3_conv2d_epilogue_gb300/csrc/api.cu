@@ -253,7 +253,7 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
     float *dout = dp2 + up(nc);
     int32_t *didx = reinterpret_cast<int32_t *>(dout + up(no));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    CE_CUDA(cudaMemcpyAsync(dx, x, nx * sizeof(float), cudaMemcpyHostToDevice, s));
+    // the filter, bias and chain parameters first, on the caller's stream
     CE_CUDA(cudaMemcpyAsync(dw, w, nw * sizeof(float), cudaMemcpyHostToDevice, s));
     CE_CUDA(cudaMemcpyAsync(db, b, nc * sizeof(float), cudaMemcpyHostToDevice, s));
     conv_epi_epilogue_desc de = *epi;
@@ -269,12 +269,63 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
         CE_CUDA(cudaMemcpyAsync(dp2, epi->beta, nc * sizeof(float), cudaMemcpyHostToDevice, s));
         de.beta = dp2;
     }
-    if (epi->index_out) de.index_out = didx;
-    st = conv_epi_forward(h, dx, dw, db, &de, dout, stream);
-    if (st) return st;
-    CE_CUDA(cudaMemcpyAsync(out, dout, no * sizeof(float), cudaMemcpyDeviceToHost, s));
-    if (epi->index_out)
-        CE_CUDA(cudaMemcpyAsync(epi->index_out, didx, no * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    // The batch in slices of whole images (every step of every chain is
+    // independent per image): slice k's input copy, on a copy stream, runs
+    // while slice k-1 is computed on the caller's stream and slice k-2's
+    // result copies back on a third stream, so the transfer, which takes the
+    // longest, hides the compute.
+    if (!h->host_copy) {
+        CE_CUDA(cudaStreamCreateWithFlags(&h->host_copy, cudaStreamNonBlocking));
+        CE_CUDA(cudaStreamCreateWithFlags(&h->host_back, cudaStreamNonBlocking));
+        CE_CUDA(cudaEventCreateWithFlags(&h->ev_entry, cudaEventDisableTiming));
+        CE_CUDA(cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming));
+        for (int k = 0; k < conv_epi_handle_s::kHostSlices; ++k) {
+            CE_CUDA(cudaEventCreateWithFlags(&h->ev_in[k], cudaEventDisableTiming));
+            CE_CUDA(cudaEventCreateWithFlags(&h->ev_out[k], cudaEventDisableTiming));
+        }
+    }
+    const size_t xi = nx / d.N, oi = no / d.N;  // elements per image
+    // slices start on 16-byte boundaries only when an image is a whole number
+    // of float4s in and out; otherwise the batch goes as one slice
+    int K = d.N < conv_epi_handle_s::kHostSlices ? d.N : conv_epi_handle_s::kHostSlices;
+    if (xi % 4 != 0 || oi % 4 != 0) K = 1;
+    // the GroupNorm workspace belongs to the handle: allocate it here, not in
+    // a slice's copy of the handle
+    if (epi->kind == CONV_EPI_GN_SCALE_POOL_CLAMP && (st = conv_epi_reserve(h, epi))) return st;
+    CE_CUDA(cudaEventRecord(h->ev_entry, s));   // work already on the caller's stream comes first
+    CE_CUDA(cudaStreamWaitEvent(h->host_copy, h->ev_entry, 0));
+    CE_CUDA(cudaStreamWaitEvent(h->host_back, h->ev_entry, 0));
+    for (int k = 0; k < K; ++k) {
+        const size_t n0 = (size_t)d.N * k / K, n1 = (size_t)d.N * (k + 1) / K;
+        CE_CUDA(cudaMemcpyAsync(dx + n0 * xi, x + n0 * xi, (n1 - n0) * xi * sizeof(float), cudaMemcpyHostToDevice,
+                                h->host_copy));
+        CE_CUDA(cudaEventRecord(h->ev_in[k], h->host_copy));
+    }
+    const int drop = h->test_drop_tile;
+    int launches = 0;
+    for (int k = 0; k < K; ++k) {
+        const size_t n0 = (size_t)d.N * k / K, n1 = (size_t)d.N * (k + 1) / K;
+        conv_epi_handle_s sub = *h;  // the same workspace, for images n0 .. n1-1
+        sub.d.N = (int)(n1 - n0);
+        sub.test_drop_tile = k == 0 ? drop : -1;
+        conv_epi_epilogue_desc dk = de;
+        if (epi->index_out) dk.index_out = didx + n0 * oi;
+        CE_CUDA(cudaStreamWaitEvent(s, h->ev_in[k], 0));
+        st = conv_epi_forward(&sub, dx + n0 * xi, dw, db, &dk, dout + n0 * oi, stream);
+        if (st) return st;
+        launches += sub.last_launches;
+        CE_CUDA(cudaEventRecord(h->ev_out[k], s));
+        CE_CUDA(cudaStreamWaitEvent(h->host_back, h->ev_out[k], 0));
+        CE_CUDA(cudaMemcpyAsync(out + n0 * oi, dout + n0 * oi, (n1 - n0) * oi * sizeof(float), cudaMemcpyDeviceToHost,
+                                h->host_back));
+        if (epi->index_out)
+            CE_CUDA(cudaMemcpyAsync(epi->index_out + n0 * oi, didx + n0 * oi, (n1 - n0) * oi * sizeof(int32_t),
+                                    cudaMemcpyDeviceToHost, h->host_back));
+    }
+    h->test_drop_tile = -1;
+    h->last_launches = launches;
+    CE_CUDA(cudaEventRecord(h->ev_done, h->host_back));
+    CE_CUDA(cudaStreamWaitEvent(s, h->ev_done, 0));
     return conv_epi_sync(h, stream);
 }
 
@@ -305,6 +356,16 @@ CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
     cudaFree(h->wpack);
     cudaFree(h->gn_mem);
     cudaFree(h->stage);
+    if (h->host_copy) {
+        cudaStreamDestroy(h->host_copy);
+        cudaStreamDestroy(h->host_back);
+        cudaEventDestroy(h->ev_entry);
+        cudaEventDestroy(h->ev_done);
+        for (int k = 0; k < conv_epi_handle_s::kHostSlices; ++k) {
+            cudaEventDestroy(h->ev_in[k]);
+            cudaEventDestroy(h->ev_out[k]);
+        }
+    }
     delete h;
     return e == cudaSuccess ? CONV_EPI_OK : conv_epi::cuda_fail(e, "conv_epi_destroy");
 }

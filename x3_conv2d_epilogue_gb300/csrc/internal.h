@@ -57,9 +57,14 @@ struct conv_epi_handle_s {
     int gn_pool_k = 0, gn_groups = 0, gn_units = 0;
     conv_epi::GnWork gn;
 
-    // device staging for conv_epi_forward_host
+    // device staging for conv_epi_forward_host, and the two streams and the
+    // events that pipeline its copies with the forward
     void *stage = nullptr;
     size_t stage_bytes = 0;
+    static constexpr int kHostSlices = 8;
+    cudaStream_t host_copy = nullptr, host_back = nullptr;
+    cudaEvent_t ev_entry = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_in[kHostSlices] = {}, ev_out[kHostSlices] = {};
 
     int last_launches = 0;
 
