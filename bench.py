@@ -127,29 +127,40 @@ class ClockSampler:
 
 
 def dist_setup():
+    """Ranks from the torchrun environment; NCCL between GPUs, gloo where no
+    GPU is visible (the CPU tests of this host logic)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl"
-        dist.init_process_group(backend=backend)
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
+
+
+def _on_gpu():
+    import torch.distributed as dist
+    return dist.get_backend() == "nccl"
 
 
 def barrier(world):
     if world > 1:
         import torch
         import torch.distributed as dist
-        dist.barrier(device_ids=[torch.cuda.current_device()])
+        if _on_gpu():
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
 
 
 def max_over_ranks(v, world):
+    """The largest of every rank's v (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if _on_gpu() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
