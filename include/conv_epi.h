@@ -130,7 +130,7 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  * chain: pool_k 1, 2 or 4 and at most 64 groups).  CONV_EPI_MODE_TF32 takes
  * any N, Cin, Cout, H >= 3 and W a multiple of 4 (rows wider than 256 run as
  * column tiles, more than 128 output channels as channel tiles); its GN chain
- * needs Cout = 64, pool_k = 4 and 64 < W <= 128, and runs as one cooperative
+ * needs Cout = 64, pool_k = 4 and W <= 128, and runs as one cooperative
  * launch (every CTA resident) that finalizes inside the kernel, or, where the
  * device refuses that launch, with a second finalize kernel.  Shapes outside
  * these return CONV_EPI_ERR_UNSUPPORTED (at create, or at the first forward

@@ -41,7 +41,9 @@ SMALL = {
     "c4_one_row": W["c4_scale_min"].resized(N=2, H=3, W=64),                 # one output row per image
     "c2_cin256": W["c2_min_tanh2"].resized(N=1, H=6, W=64, Cin=256),          # 32 input chunks, filter streamed
     "c3_cout1": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=32, Cout=1),      # a single per-channel row
-    "c5_w16": W["c5_gn_pool_clamp"].resized(N=2, H=10, W=16),                # 3 pooled columns, 2 pooled rows
+    "c5_w16": W["c5_gn_pool_clamp"].resized(N=2, H=10, W=16),                # 3 pooled columns, 2 pooled rows (two bands per unit)
+    "c5_w64": W["c5_gn_pool_clamp"].resized(N=2, H=22, W=64),                # two bands per unit, the last unit's second band past Hp
+    "c5_w40": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=40, groups=4),      # rows padded to 64 columns
     "c5_one_band": W["c5_gn_pool_clamp"].resized(N=1, H=6),                  # one pooling band per image
     # rows wider than one tile (the tf32 path splits them into column tiles of 252 outputs)
     "c2_w300": W["c2_min_tanh2"].resized(N=1, H=6, W=300),                   # 2 tiles: 252 + 46 columns
@@ -54,9 +56,10 @@ SMALL = {
     "c2_co300_w300": W["c2_min_tanh2"].resized(N=1, H=4, W=300, Cout=300),  # 3 channel x 2 column tiles
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
-# shapes the tf32 kernel refuses (its GroupNorm epilogue pools one band of four
-# rows per unit, which needs 64 < W <= 128): the call must say so, not fall back
-TF32_REFUSED = {"c5_w16", "c5_w260"}
+# shapes the tf32 kernel refuses (its GroupNorm epilogue pools whole bands of
+# four rows inside a unit, which needs W <= 128): the call must say so, not
+# fall back
+TF32_REFUSED = {"c5_w260"}
 
 
 def modes():

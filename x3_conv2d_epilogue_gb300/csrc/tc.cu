@@ -936,7 +936,13 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // table of the pooled extremes (a 64-float array after the tiles, written
     // here and first read after the first combine barrier)
     const int gn_cpg = kGN ? a.Cout / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
-    float *gn_sgn = scratch + 2 * 64 * kPoolPitch + 2 * kEpiThreads;
+    // pooling bands of 4 rows per unit: one (rows of 80..128 columns: two u
+    // of two row slots) or, in the general instantiation, two (rows of up to
+    // 64 columns: four u); 16-column chunks per warp and u: 4 or 2
+    constexpr int kNB = (kGN && GENERAL) ? 2 : 1;
+    constexpr int kKC = (kGN && GENERAL) ? 2 : 4;
+    constexpr int kWin = 4 * kKC;  // pooling windows per band and thread
+    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads;
     if (kGN && slot == 0) gn_sgn[co] = gsg;
     // Min chains: the cross-quadrant combine of a unit's partial minima, the
     // chain's tail and the row stores.  Every partial of a column (each row of
@@ -1014,31 +1020,36 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         const uint32_t tbase = tmem + lane_off + ab * kAccStride;
 
         // GN per-thread state: the pooled extreme of this thread's 4-column
-        // windows (4 per 16-column chunk, at most 4 chunks: P <= 128), and sums
-        // of y, y^2.  The extreme is the max of gsg * y: gsg = -1 turns it into
-        // the min for channels whose affine slope gamma * scale * rstd is
-        // negative (rstd > 0, so the sign is known before the statistics).
-        constexpr int kMaxWin = 16;
-        float pext[kMaxWin];
+        // windows (4 per 16-column chunk) in each band, and sums of y, y^2.
+        // The extreme is the max of gsg * y: gsg = -1 turns it into the min
+        // for channels whose affine slope gamma * scale * rstd is negative
+        // (rstd > 0, so the sign is known before the statistics).  One array
+        // per band, so every index is a compile-time constant.
+        float pext0[kWin], pext1[kNB == 2 ? kWin : 1];
         // sums of w and w^2 in four chains each (two packed pairs)
         uint64_t ls2[2] = {0ull, 0ull}, lss2[2] = {0ull, 0ull};
         if constexpr (kGN) {
 #pragma unroll
-            for (int k = 0; k < kMaxWin; ++k) pext[k] = -INFINITY;
+            for (int k = 0; k < kWin; ++k) pext0[k] = -INFINITY;
+            if constexpr (kNB == 2) {
+#pragma unroll
+                for (int k = 0; k < kWin; ++k) pext1[k] = -INFINITY;
+            }
         }
 
         for (int u = 0; u < a.U; ++u) {
             const int row = r0 + u * a.S + slot;  // the same for the whole warp
             if constexpr (kGN) {
-                Frag16 f[kMaxWin / 4];
+                Frag16 f[kKC];
 #pragma unroll
-                for (int kc = 0; kc < kMaxWin / 4; ++kc)
+                for (int kc = 0; kc < kKC; ++kc)
                     if (hc + 2 * kc < nchunks) tmem_ld16_issue(tbase + u * a.ucol + (hc + 2 * kc) * 16, f[kc]);
                 tmem_ld_wait2(f[0], f[1]);
-                tmem_ld_wait2(f[2], f[3]);
-                if (row < a.Ho) {
+                if constexpr (kKC == 4) tmem_ld_wait2(f[2], f[3]);
+                // this u's rows belong to band u / 2 (two row slots per u)
+                auto gn_update = [&](float (&pext)[kWin]) {
 #pragma unroll
-                    for (int kc = 0; kc < kMaxWin / 4; ++kc) {
+                    for (int kc = 0; kc < kKC; ++kc) {
                         const int cc = hc + 2 * kc;
                         if (cc >= nchunks) continue;
                         const int col0 = cc * 16;
@@ -1069,6 +1080,14 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                             const float2 a01 = unpack2(w2[2 * wi]), a23 = unpack2(w2[2 * wi + 1]);
                             pext[4 * kc + wi] = fmax3(fmax3(a01.x, a01.y, a23.x), a23.y, pext[4 * kc + wi]);
                         }
+                    }
+                };
+                if (row < a.Ho) {
+                    if constexpr (kNB == 2) {
+                        if (u >= 2) gn_update(pext1);
+                        else gn_update(pext0);
+                    } else {
+                        gn_update(pext0);
                     }
                 }
             } else if constexpr (kMin) {
@@ -1167,19 +1186,23 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 gs += __shfl_xor_sync(0xffffffffu, gs, o);
                 gss += __shfl_xor_sync(0xffffffffu, gss, o);
             }
-            // pooled tiles [2 row slots][64 channels][kPoolPitch] (window
+            // pooled tiles [band][2 row slots][64 channels][kPoolPitch] (window
             // extremes in gsg space); both slots write, one barrier, and the
             // stores fold the two slots
-            float *pt = scratch + slot * 64 * kPoolPitch;
-            float *st = scratch + 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
+            float *st = scratch + kNB * 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
             st[ew * 32 + lane] = gs;
             st[kEpiThreads + ew * 32 + lane] = gss;
             const int cl = (qd & 1) * 32 + lane;  // channel within the tile (Cout = 64)
+            auto put_tile = [&](int band, const float (&pext)[kWin]) {
+                float *pt = scratch + (band * 2 + slot) * 64 * kPoolPitch;
 #pragma unroll
-            for (int k = 0; k < kMaxWin; ++k) {
-                const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
-                if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
-            }
+                for (int k = 0; k < kWin; ++k) {
+                    const int pw = (hc + 2 * (k / 4)) * 4 + (k % 4);
+                    if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
+                }
+            };
+            put_tile(0, pext0);
+            if constexpr (kNB == 2) put_tile(1, pext1);
             epi_bar();
             if (ew == 2) {
                 // one warp: per group, the shuffled sums from both row slots,
@@ -1208,21 +1231,26 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     dst[1] = s1;
                 }
             }
-            if (ru < a.Hp && lane < a.Wp) {
-                // warp ew stores channels ew, ew + 8, ..., ew + 56: one pooled
-                // row each (Wp <= 32), the two row slots folded and the sign
-                // restored; all sixteen tile reads go out before the stores
-                const float *pt0 = scratch, *pt1 = scratch + 64 * kPoolPitch;
-                float *dst = a.gn.pmax + (((size_t)n * a.Cout + ew) * a.Hp + ru) * a.Wp + lane;
-                const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
-                float m[64 / kEpiWarps];
 #pragma unroll
-                for (int i = 0; i < 64 / kEpiWarps; ++i) {
-                    const int c2 = ew + kEpiWarps * i;
-                    m[i] = gn_sgn[c2] * fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]);
+            for (int band = 0; band < kNB; ++band) {
+                const int prow = ru * kNB + band;  // pooled row of this band
+                if (prow < a.Hp && lane < a.Wp) {
+                    // warp ew stores channels ew, ew + 8, ..., ew + 56: one
+                    // pooled row each (Wp <= 32), the two row slots folded and
+                    // the sign restored; all sixteen tile reads go out before
+                    // the stores
+                    const float *pt0 = scratch + band * 2 * 64 * kPoolPitch, *pt1 = pt0 + 64 * kPoolPitch;
+                    float *dst = a.gn.pmax + (((size_t)n * a.Cout + ew) * a.Hp + prow) * a.Wp + lane;
+                    const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+                    float m[64 / kEpiWarps];
+#pragma unroll
+                    for (int i = 0; i < 64 / kEpiWarps; ++i) {
+                        const int c2 = ew + kEpiWarps * i;
+                        m[i] = gn_sgn[c2] * fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 64 / kEpiWarps; ++i) dst[i * cstep] = m[i];
                 }
-#pragma unroll
-                for (int i = 0; i < 64 / kEpiWarps; ++i) dst[i * cstep] = m[i];
             }
             // (the barrier at the start of the next unit keeps the tile until all stores have read it)
         }
@@ -1454,8 +1482,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
         return (uint32_t)(U * 4 * P * sizeof(float));
     case CONV_EPI_MUL_LRELU_GELU:
         return (uint32_t)(kEpiWarps * 32 * kStgPitch * sizeof(float));
-    case CONV_EPI_GN_SCALE_POOL_CLAMP:
-        return (uint32_t)((2 * 64 * kPoolPitch + 2 * kEpiThreads + 64) * sizeof(float));
+    case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign table
+        return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 64) * sizeof(float));
     }
     return 0;
 }
@@ -1480,8 +1508,10 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     const int Cg = gemm_cout(d.Cout);
     pl.S = 128 / Cg;
     if (d.W <= 256) {
-        // one tile spans the row
+        // one tile spans the row; the GroupNorm chain runs rows of up to 64
+        // columns at P = 64 (four u per unit: two pooling bands)
         pl.P = (d.W + 15) / 16 * 16;
+        if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP && pl.P < 64) pl.P = 64;
         pl.CT = 1, pl.CW = d.W - 2, pl.BW = d.W;
     } else {
         // column tiles of 252 outputs from 256 staged columns (the last two
@@ -1567,8 +1597,9 @@ EncodeTiledFn encode_tiled() {
 // case carries none of the tiling arithmetic (the GroupNorm chain never tiles)
 template <int KIND>
 conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStream_t s) {
-    auto k = (KIND != CONV_EPI_GN_SCALE_POOL_CLAMP && (args.c.CT > 1 || args.c.MT > 1)) ? tc_conv_epi<KIND, true>
-                                                                                         : tc_conv_epi<KIND, false>;
+    // (the GroupNorm chain's general instantiation pools two bands per unit)
+    const bool general = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? args.c.U == 4 : (args.c.CT > 1 || args.c.MT > 1);
+    auto k = general ? tc_conv_epi<KIND, true> : tc_conv_epi<KIND, false>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
     if (args.c.gn_fin) {
         // the in-kernel finalize waits for every CTA: a cooperative launch
@@ -1597,9 +1628,12 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
     const int kind = e ? e->kind : CONV_EPI_MIN_TANH2;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     if (e && e->kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
-        // the epilogue pools 4x4 windows over one band of 4 rows per unit
-        // (two 64-channel row slots), at most 4 sixteen-column chunks per warp
-        if (e->pool_k != 4 || pl.RU != 4 || pl.P > 128 || pl.S != 2 || d.Cout != 64) return CONV_EPI_ERR_UNSUPPORTED;
+        // the epilogue pools 4x4 windows over bands of 4 rows (two 64-channel
+        // row slots per u): one band per unit with P in 80..128 (at most 4
+        // sixteen-column chunks per warp), two with P = 64 (2 chunks)
+        const bool one_band = pl.RU == 4 && pl.P > 64 && pl.P <= 128;
+        const bool two_bands = pl.RU == 8 && pl.P == 64;
+        if (e->pool_k != 4 || !(one_band || two_bands) || pl.S != 2 || d.Cout != 64) return CONV_EPI_ERR_UNSUPPORTED;
     }
     return CONV_EPI_OK;
 }
