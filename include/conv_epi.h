@@ -31,6 +31,10 @@
  *     its workspace (packed weights, GroupNorm partial sums, pooled max/min).
  *   - Calls are asynchronous on the given stream unless stated otherwise and
  *     return a status; no C++ exception crosses this boundary.
+ *   - A handle serves one caller at a time: its calls share its workspace,
+ *     so forwards on one handle must be ordered (one stream, or streams
+ *     joined by events); concurrent work takes one handle each.  Calls on
+ *     different handles are independent.
  *   - There is no CPU fallback: without a usable sm_103a device, calls that
  *     compute return CONV_EPI_ERR_CUDA or CONV_EPI_ERR_UNSUPPORTED.
  */
