@@ -102,20 +102,55 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                 }
                 for (int ci0 = 0; ci0 < a.Cin; ci0 += kCI) {
                     __syncthreads();
-                    for (int i = tid; i < kCI * 3 * XW; i += blockDim.x) {
-                        const int col = i % XW, rr = (i / XW) % 3, ci = i / (3 * XW);
-                        const int gci = ci0 + ci, gw = wo0 + col;
-                        float v = 0.0f;
-                        if (gci < a.Cin && gw < a.W)
-                            v = __ldg(&a.x[(((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw]);
-                        xs[i] = v;
+                    // staging: element i of each tile, its (channel, row or
+                    // tap, column) stepped by the block size without
+                    // divisions, four loads in flight per thread before
+                    // their stores
+                    {
+                        const int total = kCI * 3 * XW;
+                        int col = tid % XW, rr = (tid / XW) % 3, ci = tid / (3 * XW);
+                        for (int i0 = tid; i0 < total; i0 += 4 * (int)blockDim.x) {
+                            float v[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int i = i0 + k * (int)blockDim.x;
+                                const int gci = ci0 + ci, gw = wo0 + col;
+                                v[k] = 0.0f;
+                                if (i < total && gci < a.Cin && gw < a.W)
+                                    v[k] = __ldg(&a.x[(((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw]);
+                                col += blockDim.x;
+                                while (col >= XW) {
+                                    col -= XW;
+                                    if (++rr == 3) rr = 0, ++ci;
+                                }
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                if (i0 + k * (int)blockDim.x < total) xs[i0 + k * blockDim.x] = v[k];
+                        }
                     }
-                    for (int i = tid; i < kCI * 9 * COP; i += blockDim.x) {
-                        const int col = i % COP, tap = (i / COP) % 9, ci = i / (9 * COP);
-                        const int gci = ci0 + ci, gco = cobase + col;
-                        float v = 0.0f;
-                        if (gci < a.Cin && gco < a.Cout) v = __ldg(&a.w[((size_t)gco * a.Cin + gci) * 9 + tap]);
-                        ws[i] = v;
+                    {
+                        const int total = kCI * 9 * COP;
+                        int col = tid % COP, tap = (tid / COP) % 9, ci = tid / (9 * COP);
+                        for (int i0 = tid; i0 < total; i0 += 4 * (int)blockDim.x) {
+                            float v[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int i = i0 + k * (int)blockDim.x;
+                                const int gci = ci0 + ci, gco = cobase + col;
+                                v[k] = 0.0f;
+                                if (i < total && gci < a.Cin && gco < a.Cout)
+                                    v[k] = __ldg(&a.w[((size_t)gco * a.Cin + gci) * 9 + tap]);
+                                col += blockDim.x;
+                                while (col >= COP) {
+                                    col -= COP;
+                                    if (++tap == 9) tap = 0, ++ci;
+                                }
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                if (i0 + k * (int)blockDim.x < total) ws[i0 + k * blockDim.x] = v[k];
+                        }
                     }
                     __syncthreads();
                     const int nci = min(kCI, a.Cin - ci0);
