@@ -27,6 +27,7 @@ namespace {
 constexpr int kCI = 16;  // input channels staged per step
 constexpr int kCO = 16;  // output channels per thread per pass
 constexpr int kPX = 4;   // consecutive output pixels per thread
+constexpr int kStageLoads = 4;  // staging loads in flight per thread (8 measured no better)
 
 struct SimtArgs {
     const float *x, *w, *b;
@@ -104,15 +105,15 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                     __syncthreads();
                     // staging: element i of each tile, its (channel, row or
                     // tap, column) stepped by the block size without
-                    // divisions, four loads in flight per thread before
+                    // divisions, kStageLoads loads in flight per thread before
                     // their stores
                     {
                         const int total = kCI * 3 * XW;
                         int col = tid % XW, rr = (tid / XW) % 3, ci = tid / (3 * XW);
-                        for (int i0 = tid; i0 < total; i0 += 4 * (int)blockDim.x) {
-                            float v[4];
+                        for (int i0 = tid; i0 < total; i0 += kStageLoads * (int)blockDim.x) {
+                            float v[kStageLoads];
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
+                            for (int k = 0; k < kStageLoads; ++k) {
                                 const int i = i0 + k * (int)blockDim.x;
                                 const int gci = ci0 + ci, gw = wo0 + col;
                                 v[k] = 0.0f;
@@ -125,17 +126,17 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                                 }
                             }
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
+                            for (int k = 0; k < kStageLoads; ++k)
                                 if (i0 + k * (int)blockDim.x < total) xs[i0 + k * blockDim.x] = v[k];
                         }
                     }
                     {
                         const int total = kCI * 9 * COP;
                         int col = tid % COP, tap = (tid / COP) % 9, ci = tid / (9 * COP);
-                        for (int i0 = tid; i0 < total; i0 += 4 * (int)blockDim.x) {
-                            float v[4];
+                        for (int i0 = tid; i0 < total; i0 += kStageLoads * (int)blockDim.x) {
+                            float v[kStageLoads];
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
+                            for (int k = 0; k < kStageLoads; ++k) {
                                 const int i = i0 + k * (int)blockDim.x;
                                 const int gci = ci0 + ci, gco = cobase + col;
                                 v[k] = 0.0f;
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                                 }
                             }
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
+                            for (int k = 0; k < kStageLoads; ++k)
                                 if (i0 + k * (int)blockDim.x < total) ws[i0 + k * blockDim.x] = v[k];
                         }
                     }
