@@ -27,6 +27,7 @@ namespace {
 constexpr int kCI = 16;  // input channels staged per step
 constexpr int kCO = 16;  // output channels per thread per pass
 constexpr int kPX = 4;   // consecutive output pixels per thread
+constexpr int kRowsPerCta = 4;  // output rows per CTA for the min and per-channel chains
 constexpr int kStageLoads = 4;  // staging loads in flight per thread (8 measured no better)
 
 struct SimtArgs {
@@ -34,6 +35,7 @@ struct SimtArgs {
     int N, Cin, H, W, Cout, Ho, Wo;
     int PG, CS;          // thread layout
     int units;           // CTAs per image
+    int rpc;             // output rows per CTA (min and per-channel chains)
     int ntiles;          // pixel tiles of PG*4 columns along a row
     float scalar;        // MIN kinds
     const float *chan_scale;
@@ -61,10 +63,17 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
     const int u = blockIdx.x % a.units;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
-    const int r0 = kGN ? u * PK : u;
-    const int r1 = kGN ? min(r0 + PK, a.Ho) : u + 1;
+    // rows of this CTA: a pooling band (GroupNorm), else rpc output rows, one
+    // after the other (r0 .. r1 - 1 is the current band or row)
+    const int row_lo = kGN ? u * PK : u * a.rpc;
+    const int row_hi = kGN ? row_lo + 1 : min(row_lo + a.rpc, a.Ho);
     // min kinds: +1 tracks the minimum of y (scalar > 0), -1 the maximum (scalar < 0)
     const int sgn = a.scalar > 0.0f ? 1 : (a.scalar < 0.0f ? -1 : 0);
+    // one input-channel step and one output-channel pass: the filter tile is
+    // the same for every row and column tile of the CTA and is staged once,
+    // when the reductions' scratch (at the start of shared memory) stays
+    // below it
+    const bool w_once = a.Cin <= kCI && a.Cout <= COP && 2 * CS * TW <= kCI * 3 * XW && 2 * COP * PG <= kCI * 3 * XW;
 
     // GroupNorm per-CTA group partial sums, in a fixed summation order
     __shared__ double gpart[2 * 64];
@@ -72,6 +81,9 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
         for (int i = tid; i < 2 * 64; i += blockDim.x) gpart[i] = 0.0;
     }
 
+    for (int row = row_lo; row < row_hi; ++row) {
+    const int r0 = kGN ? row_lo : row;
+    const int r1 = kGN ? min(row_lo + PK, a.Ho) : row + 1;
     for (int t = 0; t < a.ntiles; ++t) {
         const int wo0 = t * TW;
         float best[kPX];
@@ -130,7 +142,7 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                                 if (i0 + k * (int)blockDim.x < total) xs[i0 + k * blockDim.x] = v[k];
                         }
                     }
-                    {
+                    if (!w_once || (row == row_lo && t == 0 && r == r0)) {
                         const int total = kCI * 9 * COP;
                         int col = tid % COP, tap = (tid / COP) % 9, ci = tid / (9 * COP);
                         for (int i0 = tid; i0 < total; i0 += kStageLoads * (int)blockDim.x) {
@@ -309,6 +321,7 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
             }
         }
     }  // pixel tiles
+    }  // rows of the CTA
 
     if (kGN) {
         __syncthreads();
@@ -385,18 +398,22 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.slope = e.lrelu_slope;
     a.groups = e.groups;
     a.out = out, a.idx = e.index_out;
+    // several rows per CTA only where they reuse the staged filter (one
+    // input-channel step and one output-channel pass); otherwise one row per
+    // CTA keeps more CTAs in flight (measured: 4 rows cost C3/C4 3-4%)
+    a.rpc = (d.Cin <= kCI && d.Cout <= L.COP) ? kRowsPerCta : 1;
     conv_epi_status st;
     switch (e.kind) {
     case CONV_EPI_MIN_TANH2:
-        a.units = h->Ho;
+        a.units = (h->Ho + a.rpc - 1) / a.rpc;
         st = launch<CONV_EPI_MIN_TANH2, 1>(a, L, d.N * a.units, s);
         break;
     case CONV_EPI_SCALE_MIN:
-        a.units = h->Ho;
+        a.units = (h->Ho + a.rpc - 1) / a.rpc;
         st = launch<CONV_EPI_SCALE_MIN, 1>(a, L, d.N * a.units, s);
         break;
     case CONV_EPI_MUL_LRELU_GELU:
-        a.units = h->Ho;
+        a.units = (h->Ho + a.rpc - 1) / a.rpc;
         st = launch<CONV_EPI_MUL_LRELU_GELU, 1>(a, L, d.N * a.units, s);
         break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP: {
