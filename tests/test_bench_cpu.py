@@ -1,0 +1,53 @@
+"""The bench's bookkeeping on CPU: the work and byte counts its roofline
+divides by (the figures the method's definition fixes: 2 flops per
+multiply-add, x read once), the traffic lookup that must not report counters
+taken on other kernel source, and the reference arm's JSON line."""
+import io
+import json
+import contextlib
+
+import bench
+import synth
+
+W = synth.WORKLOADS
+
+
+def test_flops_are_two_per_multiply_add():
+    # 2 * N * Cout * Ho * Wo * Cin * 9
+    assert bench.conv_flops(W["c2_min_tanh2"]) == 2 * 128 * 64 * 254 * 254 * 16 * 9
+    assert abs(bench.conv_flops(W["c2_min_tanh2"]) / 1e9 - 152.2) < 0.1
+    assert abs(bench.conv_flops(W["c3_mul_lrelu_gelu"]) / 1e9 - 304.4) < 0.1
+    assert abs(bench.conv_flops(W["c4_scale_min"]) / 1e9 - 608.8) < 0.1
+    assert abs(bench.conv_flops(W["c5_gn_pool_clamp"]) / 1e9 - 18.7) < 0.1
+
+
+def test_algorithmic_bytes():
+    c2 = W["c2_min_tanh2"]
+    x = 128 * 16 * 256 * 256 * 4
+    out = 128 * 254 * 254 * 4
+    assert bench.algorithmic_bytes(c2) == x + (64 * 16 * 9 + 64) * 4 + out
+    c5 = W["c5_gn_pool_clamp"]  # pooled output 31 x 31 per channel, three parameter vectors
+    assert bench.algorithmic_bytes(c5) == 4 * (128 * 8 * 128 * 128 + 64 * 8 * 9 + 64 * 4 + 128 * 64 * 31 * 31)
+
+
+def test_traffic_only_for_the_profiled_source():
+    h = bench.kernel_hash()
+    t = json.load(open(bench.os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    for wl in ("c2_min_tanh2", "c3_mul_lrelu_gelu", "c4_scale_min", "c5_gn_pool_clamp"):
+        want = t[wl]["dram_bytes_per_launch"] if t[wl]["src_sha1"] == h else None
+        assert bench.traffic_for(h, wl) == want
+        assert bench.traffic_for("0" * 40, wl) is None       # another kernel source
+    assert bench.traffic_for(h, "no_such_workload") is None
+
+
+def test_reference_arm_line():
+    buf = io.StringIO()
+    args = type("A", (), {"warmup": 0, "steps": 1, "ref_seconds": 0.0, "gpus": 1})()
+    with contextlib.redirect_stdout(buf):
+        assert bench.run_reference(args, W["pr1_min_tanh2"], 1, 0) == 0
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
