@@ -115,6 +115,9 @@ def test_null_pointers_rejected(lib):
     assert L.conv_epi_sync(None, None) == 1
     assert L.conv_epi_workspace_bytes(None) == 0
     assert L.conv_epi_output_shape(None, None, None) == 1
+    assert L.conv_epi_test_drop_tile(None, 0) == 1
+    assert L.conv_epi_reserve(None, None) == 1
+    assert L.conv_epi_forward_noalloc(None, None, None, None, None, None, None) == 1
 
 
 def test_create_without_device_fails_cleanly(lib):
@@ -126,3 +129,13 @@ def test_create_without_device_fails_cleanly(lib):
     st = lib.conv_epi_create(C.byref(d), C.byref(h))
     assert st in (2, 4) and not h.value
     assert isinstance(ce.conv_epi_status_string(st), str)
+
+
+def test_output_shapes_of_wide_and_many_channel_problems(lib):
+    """Shapes the tf32 path runs in column and channel tiles have the plain
+    output shapes (pure host call)."""
+    shape = ce.conv_epi_output_shape
+    assert shape(1, 16, 10, 520, 300, ce.epilogue(ce.MIN_TANH2)) == (1, 1, 8, 518)
+    assert shape(2, 64, 7, 300, 200, ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=16)) == (2, 200, 5, 298)
+    gn = ce.epilogue(ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=16, pool_k=4)
+    assert shape(3, 8, 18, 16, 64, gn) == (3, 64, 4, 3)
