@@ -132,8 +132,11 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  * forward (conv_epi_reserve allocates them up front).  Synchronous.
  * Shapes: CONV_EPI_MODE_FP32 takes any N, Cin, Cout and H, W >= 3 (its GN
  * chain: pool_k 1, 2 or 4 and at most 64 groups).  CONV_EPI_MODE_TF32 takes
- * any N, Cin, Cout, H >= 3 and W a multiple of 4 (rows wider than 256 run as
- * column tiles, more than 128 output channels as channel tiles); its GN chain
+ * any N, Cin, Cout and H, W >= 3 (rows wider than 256 run as column tiles,
+ * more than 128 output channels as channel tiles; NCHW rows whose W is not a
+ * multiple of 4 are first copied, by a small kernel, into a handle-owned
+ * buffer of rows padded to a multiple of 4 floats, because the tensor load
+ * needs 16-byte row strides: one more read and write of x); its GN chain
  * needs Cout = 64, pool_k = 4 and W <= 128, and runs as one cooperative
  * launch (every CTA resident) that finalizes inside the kernel, or, where the
  * device refuses that launch, with a second finalize kernel.  Shapes outside
@@ -178,7 +181,9 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
  *   (the GroupNorm chain needs a larger workspace); index_out must be NULL.
  * Returns CONV_EPI_ERR_UNSUPPORTED when the packed filter of the problem does
  * not fit the array (Cin rounded up to a multiple of 8, times 3*(2S+1)*Cout
- * floats, plus one 8-channel chunk, with S = 128/Cout) or the shape is outside the tensor-core path.  The first call
+ * floats, plus one 8-channel chunk, with S = 128/Cout), when an NCHW input's W
+ * is not a multiple of 4 (that needs the padded copy's buffer), or when the
+ * shape is outside the tensor-core path.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress) and
  * clears its error word with a synchronous cudaMemset, so make that first
  * call before any stream capture.  Every call on a device shares the array

@@ -139,3 +139,33 @@ def test_output_shapes_of_wide_and_many_channel_problems(lib):
     assert shape(2, 64, 7, 300, 200, ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=16)) == (2, 200, 5, 298)
     gn = ce.epilogue(ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=16, pool_k=4)
     assert shape(3, 8, 18, 16, 64, gn) == (3, 64, 4, 3)
+
+
+@pytest.mark.parametrize("layout,width,want", [
+    (ce.LAYOUT_NCHW, 7, 4),    # accepted: rows of 7 floats are padded on the device
+    (ce.LAYOUT_NHWC, 7, 4),    # accepted: channels-last rows need no padding
+    (ce.LAYOUT_NCHW, 8, 4),
+])
+def test_tf32_takes_any_row_width(lib, layout, width, want):
+    """Every W >= 3 reaches the device in tf32 mode (here: the absent one)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = C.c_void_p()
+    d = ce.Desc(1, 8, 8, width, 64, ce.MODE_TF32, layout)
+    assert lib.conv_epi_create(C.byref(d), C.byref(h)) == want and not h.value
+
+
+def test_noalloc_refuses_rows_that_need_padding_before_the_device(lib):
+    """The allocation-free forward has no buffer for the padded copy of NCHW
+    rows whose width is not a multiple of 4: refused before any device call
+    (the pointers are never dereferenced on the host)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    fake = C.c_void_p(1 << 20)  # 16-byte aligned, never touched
+    epi = ce.epilogue(ce.SCALE_MIN)
+    d = ce.Desc(1, 8, 8, 7, 64, ce.MODE_TF32, ce.LAYOUT_NCHW)
+    assert lib.conv_epi_forward_noalloc(C.byref(d), fake, fake, fake, C.byref(epi), fake, None) == 2
+    d = ce.Desc(1, 8, 8, 7, 64, ce.MODE_TF32, ce.LAYOUT_NHWC)  # channels last: reaches the device
+    assert lib.conv_epi_forward_noalloc(C.byref(d), fake, fake, fake, C.byref(epi), fake, None) == 4

@@ -2,7 +2,8 @@
 allocates nothing), a conv_epi_forward captured on a stream and replayed
 gives the same outputs as a direct call, for a min chain, the per-channel
 chain and the GroupNorm chain (whose tf32 form is a cooperative launch plus a
-memset of its arrival counter)."""
+memset of its arrival counter), and for rows that the library first copies
+into 16-byte-padded rows."""
 import numpy as np
 import pytest
 
@@ -16,6 +17,7 @@ CASES = {
     "c2": W["c2_min_tanh2"].resized(N=2, H=21),
     "c3": W["c3_mul_lrelu_gelu"].resized(N=1, H=9),
     "c5": W["c5_gn_pool_clamp"].resized(N=2, H=42),
+    "c2_w63": W["c2_min_tanh2"].resized(N=2, H=9, W=63),    # the row-padding kernel is captured too
 }
 
 

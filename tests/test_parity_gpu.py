@@ -54,6 +54,14 @@ SMALL = {
     "c4_co256": W["c4_scale_min"].resized(N=1, H=5, W=64, Cout=256),        # 2 channel tiles, atomic minimum
     "c3_co200": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=64, Cout=200),   # 2 tiles, the second padded
     "c2_co300_w300": W["c2_min_tanh2"].resized(N=1, H=4, W=300, Cout=300),  # 3 channel x 2 column tiles
+    # rows whose width is not a multiple of 4 (the tf32 path copies NCHW input
+    # into rows padded to whole 16-byte units first; channels last needs no copy)
+    "c2_w255": W["c2_min_tanh2"].resized(N=1, H=7, W=255),                   # 253 outputs per row
+    "c3_w67": W["c3_mul_lrelu_gelu"].resized(N=2, H=6, W=67),               # odd output rows: scalar stores
+    "c4_w262": W["c4_scale_min"].resized(N=1, H=4, W=262),                   # 2 column tiles over padded rows
+    "c5_w126": W["c5_gn_pool_clamp"].resized(N=1, H=18, W=126),              # 124 columns: 31 whole windows
+    "c5_w37": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=37),                # two bands per unit, 3 columns past the pool
+    "min_w3": W["pr1_min_tanh2"].resized(N=2, Cin=2, H=3, W=3, Cout=1),      # a single output per image
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 # shapes the tf32 kernel refuses (its GroupNorm epilogue pools whole bands of

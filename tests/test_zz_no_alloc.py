@@ -61,3 +61,8 @@ def test_noalloc_refuses_what_it_cannot_hold():
     with pytest.raises(ce.ConvEpiError) as ei:
         ce.conv_epi_forward_noalloc(1, 512, 8, 8, 128, xb, big_w, p.repeat(2), ce.epilogue(ce.SCALE_MIN), ob)
     assert ei.value.status == 2
+    xo = torch.zeros(1, 8, 8, 7, device="cuda")            # NCHW rows of 7 floats need the padded copy
+    oo = torch.zeros(1, 1, 6, 5, device="cuda")
+    with pytest.raises(ce.ConvEpiError) as ei:
+        ce.conv_epi_forward_noalloc(1, 8, 8, 7, 64, xo, w, b, ce.epilogue(ce.SCALE_MIN), oo)
+    assert ei.value.status == 2

@@ -189,10 +189,14 @@ CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi
         h->wpack_bytes = conv_epi::tc_wpack_bytes(*desc);
         e = cudaMalloc(&h->wpack, h->wpack_bytes);
     }
+    // tf32 NCHW rows not a multiple of 4 floats: room for the padded copy of x
+    if (e == cudaSuccess && (h->xpad_bytes = conv_epi::tc_xpad_bytes(*desc)) != 0)
+        e = cudaMalloc(&h->xpad, h->xpad_bytes);
     if (e != cudaSuccess) {
         st = conv_epi::cuda_fail(e, "conv_epi_create workspace");
         cudaFree(h->dev_err);
         cudaFree(h->wpack);
+        cudaFree(h->xpad);
         delete h;
         return st;
     }
@@ -354,6 +358,7 @@ CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
     cudaError_t e = cudaDeviceSynchronize();
     cudaFree(h->dev_err);
     cudaFree(h->wpack);
+    cudaFree(h->xpad);
     cudaFree(h->gn_mem);
     cudaFree(h->stage);
     if (h->host_copy) {
@@ -372,7 +377,7 @@ CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
 
 CONV_EPI_API size_t conv_epi_workspace_bytes(conv_epi_handle h) {
     if (!h) return 0;
-    return 256 + h->wpack_bytes + h->gn_bytes + h->stage_bytes;
+    return 256 + h->wpack_bytes + h->xpad_bytes + h->gn_bytes + h->stage_bytes;
 }
 
 CONV_EPI_API int conv_epi_last_launch_count(conv_epi_handle h) { return h ? h->last_launches : 0; }

@@ -51,6 +51,12 @@ struct conv_epi_handle_s {
     float *wpack = nullptr;
     size_t wpack_bytes = 0;
 
+    // tf32 mode, NCHW rows that are not whole 16-byte units (W not a multiple
+    // of 4): x is copied here first, rows padded to a multiple of 4 floats,
+    // because the tensor load needs 16-byte row strides
+    float *xpad = nullptr;
+    size_t xpad_bytes = 0;
+
     // GroupNorm workspace (allocated on demand / by conv_epi_reserve)
     void *gn_mem = nullptr;
     size_t gn_bytes = 0;
@@ -94,6 +100,7 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
 
 // tcgen05 tf32 path (tc.cu)
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e);
+size_t tc_xpad_bytes(const conv_epi_desc &d);  // 0 unless the input rows need the padded copy
 size_t tc_wpack_bytes(const conv_epi_desc &d);
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
 conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, const float *b,

@@ -83,6 +83,8 @@ extern "C" CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_
     if (d.layout != CONV_EPI_LAYOUT_NCHW && d.layout != CONV_EPI_LAYOUT_NHWC) return CONV_EPI_ERR_INVALID_ARG;
     if (d.mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;
     if (d.layout == CONV_EPI_LAYOUT_NHWC && d.Cin % 4 != 0) return CONV_EPI_ERR_UNSUPPORTED;
+    // NCHW rows that are not whole 16-byte units need a padded copy of x
+    if (d.layout == CONV_EPI_LAYOUT_NCHW && d.W % 4 != 0) return CONV_EPI_ERR_UNSUPPORTED;
     if ((int64_t)d.N * d.Cin * d.H * d.W >= (1ll << 31) || (int64_t)d.N * d.Cout * (d.H - 2) * (d.W - 2) >= (1ll << 31))
         return CONV_EPI_ERR_UNSUPPORTED;
     switch (epi->kind) {

@@ -1464,6 +1464,20 @@ __global__ void fill_f32(float *__restrict__ p, size_t n, float v) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = v;
 }
 
+// x viewed as rows [rows][W] -> xp [rows][Wp] (Wp = W rounded up to 4): one
+// warp per row at a time, consecutive lanes on consecutive floats.  The pad
+// columns are left unwritten: the tensor map's row extent stays W, so the
+// tensor load never reads them (it fills zeros past W).
+__global__ void pad_rows(const float *__restrict__ x, float *__restrict__ xp, size_t rows, int W, int Wp) {
+    const int lane = threadIdx.x & 31;
+    const size_t warps = ((size_t)gridDim.x * blockDim.x) >> 5;
+    for (size_t r = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+        const float *src = x + r * W;
+        float *dst = xp + r * Wp;
+        for (int c = lane; c < W; c += 32) dst[c] = __ldg(src + c);
+    }
+}
+
 // ----------------------------------------------------------- planning ----
 struct Plan {
     int S, P, U, RU, Rin, PL, chunks, ucol;
@@ -1496,11 +1510,17 @@ uint32_t up1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 // runs as 64 (two stacked row slots), larger ones as tiles of 128, with zero
 // filters for the rest
 int gemm_cout(int Cout) { return Cout <= 64 ? 64 : 128; }
+// floats per row of the input the tensor load reads: W rounded up to whole
+// 16-byte units (row strides of a tensor map are multiples of 16 bytes)
+int row_pitch(int W) { return (W + 3) / 4 * 4; }
+// NCHW input whose rows are not whole 16-byte units is first copied into
+// rows of row_pitch(W) floats
+bool needs_xpad(const conv_epi_desc &d) { return d.layout == CONV_EPI_LAYOUT_NCHW && d.W % 4 != 0; }
 int channel_tiles(int Cout) { return Cout <= 128 ? 1 : (Cout + 127) / 128; }
 
 bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (d.Cout < 1) return false;
-    if (d.Cin < 1 || d.W % 4 != 0 || d.H < 3) return false;
+    if (d.Cin < 1 || d.W < 3 || d.H < 3) return false;
     pl.MT = channel_tiles(d.Cout);
     if (pl.MT > 1 && kind == CONV_EPI_GN_SCALE_POOL_CLAMP) return false;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
@@ -1512,7 +1532,8 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
         // columns at P = 64 (four u per unit: two pooling bands)
         pl.P = (d.W + 15) / 16 * 16;
         if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP && pl.P < 64) pl.P = 64;
-        pl.CT = 1, pl.CW = d.W - 2, pl.BW = d.W;
+        // (staged rows are whole 16-byte units: columns W..BW-1 arrive as zeros)
+        pl.CT = 1, pl.CW = d.W - 2, pl.BW = row_pitch(d.W);
     } else {
         // column tiles of 252 outputs from 256 staged columns (the last two
         // unused; tiles start on multiples of 4 columns, 16-byte aligned);
@@ -1638,6 +1659,11 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
     return CONV_EPI_OK;
 }
 
+size_t tc_xpad_bytes(const conv_epi_desc &d) {
+    if (d.mode != CONV_EPI_MODE_TF32 || !needs_xpad(d)) return 0;
+    return (size_t)d.N * d.Cin * d.H * row_pitch(d.W) * sizeof(float);
+}
+
 size_t tc_wpack_bytes(const conv_epi_desc &d) {
     const int Cg = gemm_cout(d.Cout), S = 128 / Cg;
     const size_t chunk = ((size_t)3 * 2 * (2 * S + 1) * Cg * 16 + 1023) & ~(size_t)1023;
@@ -1660,9 +1686,15 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     TcArgs args{};  // value-initialised: zeros, and the workspace pointers' defaults
     Cfg &a = args.c;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
+    // NCHW rows that are not whole 16-byte units: the tensor map describes the
+    // padded copy (filled by pad_rows below, before the conv kernel)
+    const bool padded = needs_xpad(d);
+    const size_t nrows = (size_t)d.N * d.Cin * d.H;
+    if (padded && (!h->xpad || h->xpad_bytes < nrows * row_pitch(d.W) * sizeof(float))) return CONV_EPI_ERR_UNSUPPORTED;
     {
         // NCHW: x as (W, H, C, N), box (BW, Rin, 8, 1) -> staging [8][Rin][BW]
-        // (BW = W, or 256 per column tile of a wider row).
+        // (BW = W rounded up to 4, or 256 per column tile of a wider row); the
+        // row stride is the padded copy's when W is not a multiple of 4.
         // NHWC: x as (C, W, H, N), box (4, P, Rin, 1) -> a B plane [Rin][P][4]
         // (columns W..P-1, rows past H and channels past Cin read as zeros).
         cuuint64_t dims[4], strides[3];
@@ -1673,13 +1705,14 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
             strides[2] = (cuuint64_t)d.Cin * d.W * d.H * 4;
             box[0] = 4u, box[1] = (cuuint32_t)pl.P, box[2] = (cuuint32_t)pl.Rin, box[3] = 1u;
         } else {
+            const cuuint64_t pitch = (cuuint64_t)(padded ? row_pitch(d.W) : d.W);
             dims[0] = (cuuint64_t)d.W, dims[1] = (cuuint64_t)d.H, dims[2] = (cuuint64_t)d.Cin, dims[3] = (cuuint64_t)d.N;
-            strides[0] = (cuuint64_t)d.W * 4, strides[1] = (cuuint64_t)d.W * d.H * 4,
-            strides[2] = (cuuint64_t)d.W * d.H * d.Cin * 4;
+            strides[0] = pitch * 4, strides[1] = pitch * d.H * 4, strides[2] = pitch * d.H * d.Cin * 4;
             box[0] = (cuuint32_t)pl.BW, box[1] = (cuuint32_t)pl.Rin, box[2] = 8u, box[3] = 1u;
         }
         const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-        const CUresult r = enc(&args.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims, strides, box,
+        void *base = padded ? static_cast<void *>(h->xpad) : const_cast<float *>(x);
+        const CUresult r = enc(&args.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box,
                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV_EPI_ERR_UNSUPPORTED;
@@ -1698,6 +1731,11 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
                                                     d.Cin, Cg, min(Cg, d.Cout - m * Cg), pl.S);
             CE_CUDA(cudaGetLastError());
         }
+    }
+    if (padded) {
+        const size_t blocks = (nrows + 7) / 8;  // 8 warps (rows) per block
+        pad_rows<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(x, h->xpad, nrows, d.W, row_pitch(d.W));
+        CE_CUDA(cudaGetLastError());
     }
     a.x = x, a.b = b, a.wpack = h->wpack, a.out = out, a.err = h->dev_err;
     a.N = d.N, a.Cin = d.Cin, a.H = d.H, a.W = d.W, a.Cout = gemm_cout(d.Cout), a.Co = d.Cout, a.Ho = h->Ho, a.Wo = h->Wo;
@@ -1763,7 +1801,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     default: return CONV_EPI_ERR_INVALID_ARG;
     }
     if (st) return st;
-    h->last_launches = pl.MT + 1 + fills;  // packs, fill, conv
+    h->last_launches = pl.MT + 1 + fills + (padded ? 1 : 0);  // packs, fill, conv, row padding
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
         if ((st = gn_finalize(h, e, out, s, true))) return st;
         h->last_launches += 1;
