@@ -130,18 +130,21 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  * Validates the description and allocates the workspace every chain needs
  * except the GN chain's pooled buffers, which are allocated on the first GN
  * forward (conv_epi_reserve allocates them up front).  Synchronous.
- * Shapes: CONV_EPI_MODE_FP32 takes any N, Cin, Cout and H, W >= 3 (its GN
- * chain: pool_k 1, 2 or 4 and at most 64 groups).  CONV_EPI_MODE_TF32 takes
- * any N, Cin, Cout and H, W >= 3 (rows wider than 256 run as column tiles,
- * more than 128 output channels as channel tiles; NCHW rows whose W is not a
- * multiple of 4 are first copied, by a small kernel, into a handle-owned
- * buffer of rows padded to a multiple of 4 floats, because the tensor load
- * needs 16-byte row strides: one more read and write of x); its GN chain
- * needs Cout = 64, pool_k = 4 and W <= 128, and runs as one cooperative
- * launch (every CTA resident) that finalizes inside the kernel, or, where the
- * device refuses that launch, with a second finalize kernel.  Shapes outside
- * these return CONV_EPI_ERR_UNSUPPORTED (at create, or at the first forward
- * for chain-specific limits). */
+ *
+ * Shapes:
+ *   CONV_EPI_MODE_FP32: any N, Cin, Cout and H, W >= 3.
+ *     GN chain: pool_k 1, 2 or 4, at most 64 groups.
+ *   CONV_EPI_MODE_TF32: any N, Cin, Cout and H, W >= 3.
+ *     GN chain: Cout = 64, pool_k = 4, W <= 128.
+ *     Rows wider than 256 run as column tiles, more than 128 output channels
+ *     as channel tiles.  NCHW rows whose W is not a multiple of 4 are first
+ *     copied, by a small kernel, into a handle-owned buffer of rows padded to
+ *     a multiple of 4 floats (the tensor load needs 16-byte row strides):
+ *     one more read and write of x.  The GN chain runs as one cooperative
+ *     launch (every CTA resident) that finalizes inside the kernel; where the
+ *     device refuses that launch, a second finalize kernel follows.
+ *   Other shapes return CONV_EPI_ERR_UNSUPPORTED: at create, or at the first
+ *   forward for chain-specific limits. */
 CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi_handle *out);
 
 /* Allocate, ahead of the first forward, whatever workspace `epi` will need
