@@ -151,7 +151,7 @@ CONV_EPI_API const char *conv_epi_status_string(conv_epi_status s) {
 
 CONV_EPI_API const char *conv_epi_last_cuda_error(void) { return g_cuda_err; }
 
-CONV_EPI_API int conv_epi_version(void) { return 10100; }
+CONV_EPI_API int conv_epi_version(void) { return 10200; }
 
 CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc, const conv_epi_epilogue_desc *epi,
                                                    int64_t shape[4]) {
