@@ -165,13 +165,19 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
-def oracle_sample(wl, seconds: float, max_images: int):
-    """Time the fp64 oracle on whole images of the workload until ~seconds."""
+# the single-core oracle figure is taken on one image where that image's
+# conv is at most this many FLOPs (about a second on one host core)
+SINGLE_CORE_MAX_FLOPS = 2.0e9
+
+
+def oracle_sample(wl, seconds: float, max_images: int, cores: int = 0):
+    """Time the fp64 oracle on whole images of the workload until ~seconds,
+    on `cores` threads (0: every host core)."""
     import oracle
     one = wl.with_batch(1)
     t = synth.make_inputs(one, seed=0)
     ch = oracle.chain_for(one, t)
-    cores = os.cpu_count() or 1
+    cores = cores or os.cpu_count() or 1
     done, t0 = 0, time.perf_counter()
     while True:
         oracle.forward(t.x, t.w, t.b, ch, nthreads=cores, want_index=False)
@@ -395,6 +401,9 @@ def main(argv=None):
         v, el, done, cores = oracle_sample(wl, args.cpu_seconds, wl.N)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{done} of {wl.N} images of {wl.name} ({el:.1f} s, fp64 direct loops)"}
+        if conv_flops(wl.with_batch(1)) <= SINGLE_CORE_MAX_FLOPS:  # one image on one core, where that is short
+            v1, el1, _, _ = oracle_sample(wl, 0.0, 1, cores=1)
+            cpu["single_core"] = {"value": v1, "unit": "TFLOP/s", "sample": f"1 image on 1 thread ({el1:.2f} s)"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,

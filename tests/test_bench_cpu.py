@@ -51,3 +51,13 @@ def test_reference_arm_line():
         assert k in line, k
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_single_core_oracle_sample():
+    """The cpu_baseline adds a one-image, one-thread oracle figure where an
+    image's conv is short (the 32x32 case, C2, C5) and leaves it out where
+    one image would take many seconds on one core (C3, C4)."""
+    short = [n for n in W if bench.conv_flops(W[n].with_batch(1)) <= bench.SINGLE_CORE_MAX_FLOPS]
+    assert sorted(short) == ["c2_min_tanh2", "c5_gn_pool_clamp", "pr1_min_tanh2"]
+    v, el, done, cores = bench.oracle_sample(W["pr1_min_tanh2"], 0.0, 1, cores=1)
+    assert cores == 1 and done == 1 and v > 0 and el > 0
