@@ -28,7 +28,9 @@
  *     device can read (cudaMalloc, torch CUDA tensors); "host pointer" means
  *     ordinary (ideally pinned) host memory.
  *   - The caller owns every tensor it passes; the library owns the handle and
- *     its workspace (packed weights, GroupNorm partial sums, pooled max/min).
+ *     its workspace (packed weights, GroupNorm partial sums, pooled max/min,
+ *     the padded copy of x for tf32 NCHW rows whose W is not a multiple of 4,
+ *     and the device staging of conv_epi_forward_host).
  *   - Calls are asynchronous on the given stream unless stated otherwise and
  *     return a status; no C++ exception crosses this boundary.
  *   - A handle serves one caller at a time: its calls share its workspace,
@@ -160,10 +162,16 @@ CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x,
                                               const float *b, const conv_epi_epilogue_desc *epi,
                                               float *out, void *stream);
 
-/* Same computation from HOST buffers: copies x, w, b and the chain's
- * parameters to library-owned device buffers on `stream`, runs the forward,
- * copies the result back into host `out` and waits for the stream.  Every
- * pointer (including those inside `epi`) is a host pointer. */
+/* Same computation from HOST buffers.  Every pointer (including those inside
+ * `epi`) is a host pointer; pinned memory lets the copies run asynchronously.
+ * w, b and the chain's parameters are copied on `stream` into library-owned
+ * device staging (kept by the handle, grown to the largest call, freed by
+ * conv_epi_destroy).  The batch then goes in up to eight slices of whole
+ * images (one slice when an image is not a whole number of 16-byte units in
+ * or out): slice k's input copy runs on a library-owned copy stream while
+ * slice k-1 is computed on `stream` and slice k-2's result copies back on a
+ * second library-owned stream, joined by events.  Synchronous: returns after
+ * the last result copy, with the device-side status as conv_epi_sync(). */
 CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const float *x, const float *w,
                                                    const float *b, const conv_epi_epilogue_desc *epi,
                                                    float *out, void *stream);
