@@ -207,6 +207,50 @@ CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_desc *desc,
                                                       const float *b, const conv_epi_epilogue_desc *epi, float *out,
                                                       void *stream);
 
+/* The tensor-core kernel's plan for one problem and chain, as a forward on
+ * a handle would launch it: tiling, ring stages, the shared-memory layout,
+ * the tensor-load box and the filter operand layout.  For diagnostics and
+ * host-side tests of the kernel's index ranges; a pure host call (no device
+ * is needed).  Every field is an int64_t; sizes are in bytes unless stated. */
+typedef struct {
+    int64_t struct_bytes;    /* sizeof(conv_epi_plan), set by the call */
+    int64_t gemm_cout;       /* output channels per channel tile of the GEMM: 64 or 128 */
+    int64_t S;               /* output rows stacked in the 128 accumulator lanes (128 / gemm_cout) */
+    int64_t P;               /* positions per accumulator row (the MMA's N) */
+    int64_t U;               /* accumulator row sets per unit */
+    int64_t RU;              /* output rows per unit (U * S) */
+    int64_t Rin;             /* input rows staged per unit (RU + 2) */
+    int64_t PL;              /* 16-byte rows per 4-channel group of a B plane */
+    int64_t ucol;            /* tensor-memory columns per accumulator row set */
+    int64_t chunks;          /* 8-channel K chunks */
+    int64_t CT;              /* column tiles per output row */
+    int64_t CW;              /* output columns per column tile */
+    int64_t BW;              /* staged row width, floats (NCHW) */
+    int64_t MT;              /* channel tiles */
+    int64_t units_per_image; /* row blocks x column tiles x channel tiles */
+    int64_t resident;        /* 1: the whole packed filter stays in shared memory */
+    int64_t na, nb, nr;      /* ring stages: filter chunks, B planes, staged input tiles */
+    int64_t a_bytes, b_bytes, raw_bytes, scratch_bytes;  /* one stage of each ring; the epilogue scratch */
+    int64_t a_off, b_off, raw_off, bar_off, scratch_off; /* shared-memory offsets */
+    int64_t bar_bytes;       /* the mbarriers */
+    int64_t smem;            /* dynamic shared memory per CTA */
+    int64_t smem_limit;      /* the most the kernel requests */
+    int64_t a_plane_bytes, a_lbo, a_kw_stride;  /* filter operand: one plane, K-group stride, tap stride */
+    int64_t x_pitch;         /* floats between input rows as the tensor load reads them (NCHW) */
+    int64_t box[4];          /* tensor-load box: NCHW (BW, Rin, 8, 1); NHWC (4, P, Rin, 1) */
+    int64_t acc_cols;        /* tensor-memory columns per accumulator buffer (two buffers) */
+    int64_t tmem_cols;       /* tensor-memory columns the kernel allocates */
+    int64_t conv_items;      /* converter work items the kernel holds per chunk */
+} conv_epi_plan;
+
+/* Fill *plan for desc (mode must be CONV_EPI_MODE_TF32) and epi.  Returns
+ * CONV_EPI_ERR_INVALID_ARG for a null pointer or an invalid description or
+ * chain, CONV_EPI_ERR_UNSUPPORTED where the tensor-core kernel refuses the
+ * shape (as conv_epi_create / conv_epi_forward would; *plan is then filled
+ * as far as a plan exists, else zero), else CONV_EPI_OK. */
+CONV_EPI_API conv_epi_status conv_epi_plan_query(const conv_epi_desc *desc, const conv_epi_epilogue_desc *epi,
+                                                 conv_epi_plan *plan);
+
 /* Wait for `stream` and report any device-side error flag the library's
  * kernels raised on this handle since the last call (then clear it). */
 CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream);

@@ -1,0 +1,208 @@
+"""The tensor-core kernel's index ranges, checked on the CPU.
+
+conv_epi_plan_query returns the plan a forward would launch (a pure host
+call).  For every shape the GPU tests run, the full-size workloads and a
+seeded sweep of random shapes, these tests check that every access the
+kernel's roles make from that plan stays inside its buffer: the tensor-load
+box and strides follow the 16-byte rules, column tiles start on 16-byte
+boundaries, the shared-memory regions are disjoint and fit, the MMAs' filter
+and input operand ranges stay inside their stages, the accumulators fit the
+tensor memory, and the epilogue scratch holds what the chain stores there.
+The access formulas below restate, from the kernel's roles, which rows and
+bytes each MMA reads.
+"""
+import math
+import random
+
+import pytest
+
+import synth
+import x3_conv2d_epilogue_gb300 as ce
+
+MIN_KINDS = (ce.MIN_TANH2, ce.SCALE_MIN)
+
+
+def epi_for(kind, groups=16, pool_k=4):
+    # the chain's parameter tensors are never read by a plan query: any
+    # non-null value passes the argument checks
+    return ce.epilogue(kind, chan_scale=16, gamma=16, beta=16, groups=groups, pool_k=pool_k)
+
+
+def plan(N, Cin, H, W, Cout, kind, layout=ce.LAYOUT_NCHW, groups=16, pool_k=4):
+    return ce.conv_epi_plan_query(N, Cin, H, W, Cout, epi_for(kind, groups, pool_k), layout)
+
+
+def check_plan(q, N, Cin, H, W, Cout, kind, layout):
+    Ho, Wo = H - 2, W - 2
+    nhwc = layout == ce.LAYOUT_NHWC
+    S, P, U, RU, Rin, PL = q["S"], q["P"], q["U"], q["RU"], q["Rin"], q["PL"]
+    # the GEMM: 64 or 128 output channels per tile, rows stacked into 128 lanes
+    assert q["gemm_cout"] in (64, 128) and S * q["gemm_cout"] == 128
+    assert q["gemm_cout"] == (64 if Cout <= 64 else 128)
+    assert q["MT"] == (1 if Cout <= 128 else math.ceil(Cout / 128))
+    assert q["chunks"] == math.ceil(Cin / 8)
+    # MMA shape (kind::tf32, M = 128): N a multiple of 16 in 16 .. 256
+    assert P % 16 == 0 and 16 <= P <= 256
+    # rows of a unit; the tensor-load box height is at most 256
+    assert RU == U * S and Rin == RU + 2 and Rin <= 256
+    row_blocks = math.ceil(Ho / RU)
+    assert q["units_per_image"] == row_blocks * q["CT"] * q["MT"]
+    # tensor memory: U row sets of ucol >= P columns per buffer, two buffers
+    assert q["ucol"] >= P and q["ucol"] % 32 == 0 and U * q["ucol"] <= q["acc_cols"]
+    assert 2 * q["acc_cols"] <= q["tmem_cols"] <= 512
+    # column tiles: every output column is covered once; tile starts are
+    # 16-byte aligned (the tensor load's x coordinate) and a tile's inputs
+    # (CW + 2 columns) fit the staged row
+    CT, CW, BW = q["CT"], q["CW"], q["BW"]
+    if CT == 1:
+        assert CW == Wo and Wo <= P
+        if not nhwc:
+            assert BW >= W and BW % 4 == 0 and BW <= P
+    else:
+        assert BW == 256 and P == 256 and CW + 2 <= BW
+        assert (CT - 1) * CW < Wo <= CT * CW
+        for ct in range(CT):
+            assert (ct * CW * 4) % 16 == 0
+    # the tensor load: 16-byte inner box extent and strides, dims <= 256
+    box = q["box"]
+    assert all(1 <= v <= 256 for v in box)
+    assert (box[0] * 4) % 16 == 0
+    if nhwc:
+        assert box == [4, P, Rin, 1] and (Cin * 4) % 16 == 0
+        assert q["nr"] == 0 and q["raw_bytes"] == 0
+        # two boxes of 4 channels x P positions x Rin rows land in one B plane
+        assert Rin * P <= PL
+    else:
+        assert box == [BW, Rin, 8, 1]
+        assert q["x_pitch"] >= W and (q["x_pitch"] * 4) % 16 == 0
+        assert q["x_pitch"] == (W if W % 4 == 0 else W + (-W) % 4)
+        assert q["raw_bytes"] >= 8 * Rin * BW * 4 and q["nr"] >= 2
+        # converter: 2 * Rin * ceil(P / 32) items per chunk, within capacity;
+        # it writes plane rows rr * P + w (rr < Rin, w < P) of each group
+        assert 2 * Rin * math.ceil(P / 32) <= q["conv_items"]
+        assert Rin * P <= PL
+    # B operand: accumulator row set u, shift sk (0 .. S+1) and tap kw read P
+    # rows starting at (u*S + sk)*P + kw of each 4-channel group
+    top = max((u * S + sk) * P + kw + P for u in range(U) for sk in range(S + 2) for kw in range(3))
+    assert top <= PL and q["b_bytes"] >= 2 * PL * 16
+    # A operand: shift sk and tap kw start at plane S+1-sk, tap block kw, and
+    # read 128 rows of 16 bytes from each of the two K groups (a_lbo apart)
+    ap, lbo, kws = q["a_plane_bytes"], q["a_lbo"], q["a_kw_stride"]
+    assert ap == q["gemm_cout"] * 16 and lbo == (2 * S + 1) * ap and kws == 2 * lbo
+    for sk in range(S + 2):
+        for kw in range(3):
+            for g in range(2):
+                start = (S + 1 - sk) * ap + kw * kws + g * lbo
+                assert start >= 0 and start + 128 * 16 <= q["a_bytes"]
+    assert q["a_bytes"] % 1024 == 0 and q["b_bytes"] % 1024 == 0 and q["raw_bytes"] % 1024 == 0
+    # shared memory: filter (resident: every chunk), B planes, staged tiles,
+    # barriers, scratch, in order and disjoint, within the CTA limit
+    filt = (q["chunks"] * q["MT"] if q["resident"] else q["na"]) * q["a_bytes"]
+    if q["resident"]:
+        assert q["MT"] == 1 and q["na"] == 1
+    else:
+        assert 2 <= q["na"] <= 4
+    assert 2 <= q["nb"] <= 4 and q["nr"] <= 4
+    assert q["a_off"] == 0 and q["b_off"] >= filt
+    assert q["raw_off"] >= q["b_off"] + q["nb"] * q["b_bytes"]
+    assert q["bar_off"] >= q["raw_off"] + q["nr"] * q["raw_bytes"]
+    assert q["scratch_off"] >= q["bar_off"] + q["bar_bytes"] + 8
+    assert q["smem"] >= q["scratch_off"] + q["scratch_bytes"]
+    assert q["smem"] <= q["smem_limit"] <= 232448
+    assert q["b_off"] % 1024 == 0 and q["raw_off"] % 1024 == 0 and q["bar_off"] % 8 == 0
+    assert q["scratch_off"] % 16 == 0
+    # epilogue scratch: the min chains' per-(u, quadrant) partial rows, the
+    # per-channel transpose tiles, the GroupNorm pooled tiles of each band
+    if kind in MIN_KINDS:
+        assert q["scratch_bytes"] >= U * 4 * P * 4
+    elif kind == ce.MUL_LRELU_GELU:
+        assert q["scratch_bytes"] >= 8 * 32 * 18 * 4
+    else:
+        bands = U // 2
+        assert U in (2, 4) and P <= 128 and S == 2
+        assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 64) * 4
+
+
+def parity_shapes():
+    import test_parity_gpu as tp
+    shapes = dict(tp.SMALL)
+    shapes.update(tp.FP32_ONLY)
+    for name, wl in synth.WORKLOADS.items():
+        shapes["full_" + name] = wl
+    return shapes
+
+
+SHAPES = parity_shapes()
+
+
+@pytest.mark.parametrize("case", sorted(SHAPES))
+@pytest.mark.parametrize("layout", [ce.LAYOUT_NCHW, ce.LAYOUT_NHWC])
+def test_plans_of_tested_shapes(case, layout):
+    wl = SHAPES[case]
+    args = (wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.kind, layout)
+    if layout == ce.LAYOUT_NHWC and wl.Cin % 4:
+        with pytest.raises(ce.ConvEpiError) as ei:
+            plan(*args, groups=wl.groups, pool_k=wl.pool_k)
+        assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
+        return
+    gn_refused = wl.kind == ce.GN_SCALE_POOL_CLAMP and not (wl.Cout == 64 and wl.pool_k == 4 and wl.W <= 128)
+    if gn_refused:
+        with pytest.raises(ce.ConvEpiError) as ei:
+            plan(*args, groups=wl.groups, pool_k=wl.pool_k)
+        assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
+        return
+    check_plan(plan(*args, groups=wl.groups, pool_k=wl.pool_k), *args)
+
+
+def test_random_shapes_all_planned_and_in_range():
+    """Every non-GroupNorm shape with H, W >= 3 has a plan (the tf32 mode takes
+    any size), and every plan passes the range checks; GroupNorm shapes are
+    planned exactly when Cout = 64, pool_k = 4 and W <= 128."""
+    rng = random.Random(20261203)
+    for _ in range(3000):
+        kind = rng.choice([ce.MIN_TANH2, ce.SCALE_MIN, ce.MUL_LRELU_GELU, ce.GN_SCALE_POOL_CLAMP])
+        layout = rng.choice([ce.LAYOUT_NCHW, ce.LAYOUT_NHWC])
+        N = rng.randint(1, 4)
+        W = rng.choice([rng.randint(3, 40), rng.randint(41, 300), rng.randint(301, 1100)])
+        H = rng.randint(3, 60)
+        Cin = rng.choice([rng.randint(1, 24), rng.randint(25, 320)])
+        Cout = rng.choice([rng.randint(1, 64), 64, rng.randint(65, 128), rng.randint(129, 400)])
+        if layout == ce.LAYOUT_NHWC:
+            Cin = max(4, Cin // 4 * 4)
+        groups, pool_k = 1, 4
+        if kind == ce.GN_SCALE_POOL_CLAMP:
+            if rng.random() < 0.7:
+                Cout, W = 64, rng.randint(6, 128)
+            groups = rng.choice([g for g in (1, 2, 4, 8, 16, 32, 64) if Cout % g == 0] or [1])
+            pool_k = rng.choice([4, 4, 4, 2])
+            H = max(H, pool_k + 2)
+            W = max(W, pool_k + 2)
+        args = (N, Cin, H, W, Cout, kind, layout)
+        expect_ok = kind != ce.GN_SCALE_POOL_CLAMP or (Cout == 64 and pool_k == 4 and W <= 128)
+        try:
+            q = plan(*args, groups=groups, pool_k=pool_k)
+        except ce.ConvEpiError as e:
+            assert not expect_ok, (args, groups, pool_k, e)
+            assert ce.STATUS[e.status] == "UNSUPPORTED"
+            continue
+        assert expect_ok, (args, groups, pool_k)
+        check_plan(q, *args)
+
+
+def test_plan_query_arguments():
+    with pytest.raises(ce.ConvEpiError) as ei:          # fp32 mode has no tensor-core plan
+        d = ce.Desc(1, 8, 8, 8, 64, ce.MODE_FP32, ce.LAYOUT_NCHW)
+        q = ce.Plan()
+        ce._check(ce._lib().conv_epi_plan_query(ce.C.byref(d), ce.C.byref(epi_for(ce.MIN_TANH2)),
+                                                ce.C.byref(q)), "plan")
+    assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
+    with pytest.raises(ce.ConvEpiError) as ei:          # bad chain
+        plan(1, 8, 8, 8, 64, 9)
+    assert ce.STATUS[ei.value.status] == "INVALID_ARG"
+    with pytest.raises(ce.ConvEpiError) as ei:          # H < 3
+        plan(1, 8, 2, 8, 64, ce.MIN_TANH2)
+    assert ce.STATUS[ei.value.status] == "INVALID_ARG"
+    assert ce._lib().conv_epi_plan_query(None, None, None) == 1
+    q = plan(128, 16, 256, 256, 64, ce.MIN_TANH2)        # the C2 workload: one resident filter, one row tile
+    assert q["struct_bytes"] == ce.C.sizeof(ce.Plan)
+    assert (q["P"], q["U"], q["RU"], q["CT"], q["MT"], q["resident"]) == (256, 1, 2, 1, 1, 1)

@@ -57,6 +57,25 @@ class EpilogueDesc(C.Structure):
     ]
 
 
+def _plan_fields():
+    """conv_epi_plan's fields in declaration order, read from the header (every
+    field is an int64_t; `box[4]` is an array)."""
+    with open(HEADER) as f:
+        text = f.read()
+    body = re.search(r"typedef struct \{((?:(?!typedef).)*?)\} conv_epi_plan;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in re.findall(r"int64_t\s+([^;]+);", body):
+        for name in decl.split(","):
+            m = re.fullmatch(r"\s*(\w+)\s*(?:\[(\d+)\])?\s*", name)
+            fields.append((m.group(1), C.c_int64 * int(m.group(2)) if m.group(2) else C.c_int64))
+    return fields
+
+
+class Plan(C.Structure):
+    _fields_ = _plan_fields()
+
+
 _lock = threading.Lock()
 _L = None
 
@@ -81,6 +100,7 @@ def _lib():
             L.conv_epi_forward_noalloc.argtypes = [C.POINTER(Desc), P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_sync.argtypes = [P, P]
             L.conv_epi_test_drop_tile.argtypes = [P, I]
+            L.conv_epi_plan_query.argtypes = [C.POINTER(Desc), C.POINTER(EpilogueDesc), C.POINTER(Plan)]
             L.conv_epi_destroy.argtypes = [P]
             L.conv_epi_workspace_bytes.argtypes = [P]
             L.conv_epi_workspace_bytes.restype = C.c_size_t
@@ -136,6 +156,18 @@ def conv_epi_output_shape(N, Cin, H, W, Cout, epi, mode=MODE_TF32, layout=LAYOUT
     d = Desc(N, Cin, H, W, Cout, mode, layout)
     _check(_lib().conv_epi_output_shape(C.byref(d), C.byref(epi), s.ctypes.data), "conv_epi_output_shape")
     return tuple(int(v) for v in s)
+
+
+def conv_epi_plan_query(N, Cin, H, W, Cout, epi, layout=LAYOUT_NCHW):
+    """The tensor-core kernel's plan for this problem and chain (pure host
+    call) as a dict; raises ConvEpiError where the kernel refuses the shape."""
+    d = Desc(N, Cin, H, W, Cout, MODE_TF32, layout)
+    q = Plan()
+    _check(_lib().conv_epi_plan_query(C.byref(d), C.byref(epi), C.byref(q)), "conv_epi_plan_query")
+    if q.struct_bytes != C.sizeof(Plan):
+        raise RuntimeError(f"conv_epi_plan is {q.struct_bytes} bytes in the library, {C.sizeof(Plan)} here")
+    return {name: (list(getattr(q, name)) if hasattr(getattr(q, name), "__len__") else int(getattr(q, name)))
+            for name, _ in Plan._fields_}
 
 
 def conv_epi_create(N, Cin, H, W, Cout, mode=MODE_TF32, layout=LAYOUT_NCHW):

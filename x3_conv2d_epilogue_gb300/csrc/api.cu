@@ -345,6 +345,19 @@ CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream) {
     return CONV_EPI_OK;
 }
 
+CONV_EPI_API conv_epi_status conv_epi_plan_query(const conv_epi_desc *desc, const conv_epi_epilogue_desc *epi,
+                                                 conv_epi_plan *plan) {
+    if (!plan) return CONV_EPI_ERR_INVALID_ARG;
+    *plan = conv_epi_plan{};
+    plan->struct_bytes = (int64_t)sizeof(conv_epi_plan);
+    conv_epi_status st = check_desc(desc);
+    if (st) return st;
+    if ((st = check_epi(*desc, epi))) return st;
+    if (desc->mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;
+    if (desc->layout == CONV_EPI_LAYOUT_NHWC && desc->Cin % 4 != 0) return CONV_EPI_ERR_UNSUPPORTED;
+    return conv_epi::tc_plan_query(*desc, *epi, *plan);
+}
+
 CONV_EPI_API conv_epi_status conv_epi_test_drop_tile(conv_epi_handle h, int tile) {
     if (!h || tile < -1) return CONV_EPI_ERR_INVALID_ARG;
     if (h->d.mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;

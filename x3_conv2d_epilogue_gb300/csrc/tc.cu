@@ -1483,10 +1483,16 @@ struct Plan {
     int S, P, U, RU, Rin, PL, chunks, ucol;
     int CT, CW, BW;  // column tiles, output columns per tile, staged tile width
     int MT;          // channel tiles
+    int Cg;          // the GEMM's output channels per channel tile
     int resident, na, nb, nr;
     uint32_t a_bytes, b_bytes, raw_bytes, scratch_bytes;
     uint32_t a_off, b_off, raw_off, bar_off, scratch_off;
     size_t smem;
+    // filter operand layout [chunk][kw][ci4][plane][co][4]: one plane, the
+    // K-group (ci4) stride, the tap (kw) stride
+    uint32_t a_plane_bytes, a_lbo, a_kw_stride;
+    int xpitch;         // floats between input rows as the tensor load reads them
+    uint32_t box[4];    // tensor-load box: NCHW (BW, Rin, 8, 1), NHWC (4, P, Rin, 1)
 };
 
 uint32_t scratch_bytes_for(int kind, int U, int P) {
@@ -1584,6 +1590,13 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.scratch_off = (pl.bar_off + 8u * Bars::kCount + 8u + 15u) & ~15u;
     pl.smem = pl.scratch_off + pl.scratch_bytes;
     if (pl.resident) pl.na = 1;  // no filter ring: the resident block is read per chunk
+    pl.Cg = Cg;
+    pl.a_plane_bytes = (uint32_t)Cg * 16u;
+    pl.a_lbo = (uint32_t)(2 * pl.S + 1) * pl.a_plane_bytes;
+    pl.a_kw_stride = 2u * pl.a_lbo;
+    pl.xpitch = needs_xpad(d) ? row_pitch(d.W) : d.W;
+    if (nhwc) pl.box[0] = 4u, pl.box[1] = (uint32_t)pl.P, pl.box[2] = (uint32_t)pl.Rin, pl.box[3] = 1u;
+    else pl.box[0] = (uint32_t)pl.BW, pl.box[1] = (uint32_t)pl.Rin, pl.box[2] = 8u, pl.box[3] = 1u;
     return pl.smem <= (size_t)kSmemLimit;
 }
 
@@ -1664,6 +1677,28 @@ size_t tc_xpad_bytes(const conv_epi_desc &d) {
     return (size_t)d.N * d.Cin * d.H * row_pitch(d.W) * sizeof(float);
 }
 
+conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, conv_epi_plan &q) {
+    q = conv_epi_plan{};
+    q.struct_bytes = (int64_t)sizeof(conv_epi_plan);
+    Plan pl;
+    if (!make_plan(d, e.kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
+    q.gemm_cout = pl.Cg, q.S = pl.S, q.P = pl.P, q.U = pl.U, q.RU = pl.RU, q.Rin = pl.Rin, q.PL = pl.PL;
+    q.ucol = pl.ucol, q.chunks = pl.chunks, q.CT = pl.CT, q.CW = pl.CW, q.BW = pl.BW, q.MT = pl.MT;
+    q.units_per_image = (int64_t)((d.H - 2 + pl.RU - 1) / pl.RU) * pl.CT * pl.MT;
+    q.resident = pl.resident, q.na = pl.na, q.nb = pl.nb, q.nr = pl.nr;
+    q.a_bytes = pl.a_bytes, q.b_bytes = pl.b_bytes, q.raw_bytes = pl.raw_bytes, q.scratch_bytes = pl.scratch_bytes;
+    q.a_off = pl.a_off, q.b_off = pl.b_off, q.raw_off = pl.raw_off, q.bar_off = pl.bar_off;
+    q.scratch_off = pl.scratch_off;
+    q.bar_bytes = 8 * Bars::kCount;
+    q.smem = (int64_t)pl.smem, q.smem_limit = kSmemLimit;
+    q.a_plane_bytes = pl.a_plane_bytes, q.a_lbo = pl.a_lbo, q.a_kw_stride = pl.a_kw_stride;
+    q.x_pitch = pl.xpitch;
+    for (int i = 0; i < 4; ++i) q.box[i] = pl.box[i];
+    q.acc_cols = kAccStride, q.tmem_cols = kTmemCols;
+    q.conv_items = kConvItems * kConvWarps;
+    return tc_supported(d, &e);
+}
+
 size_t tc_wpack_bytes(const conv_epi_desc &d) {
     const int Cg = gemm_cout(d.Cout), S = 128 / Cg;
     const size_t chunk = ((size_t)3 * 2 * (2 * S + 1) * Cg * 16 + 1023) & ~(size_t)1023;
@@ -1703,13 +1738,12 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
             dims[0] = (cuuint64_t)d.Cin, dims[1] = (cuuint64_t)d.W, dims[2] = (cuuint64_t)d.H, dims[3] = (cuuint64_t)d.N;
             strides[0] = (cuuint64_t)d.Cin * 4, strides[1] = (cuuint64_t)d.Cin * d.W * 4,
             strides[2] = (cuuint64_t)d.Cin * d.W * d.H * 4;
-            box[0] = 4u, box[1] = (cuuint32_t)pl.P, box[2] = (cuuint32_t)pl.Rin, box[3] = 1u;
         } else {
-            const cuuint64_t pitch = (cuuint64_t)(padded ? row_pitch(d.W) : d.W);
+            const cuuint64_t pitch = (cuuint64_t)pl.xpitch;
             dims[0] = (cuuint64_t)d.W, dims[1] = (cuuint64_t)d.H, dims[2] = (cuuint64_t)d.Cin, dims[3] = (cuuint64_t)d.N;
             strides[0] = pitch * 4, strides[1] = pitch * d.H * 4, strides[2] = pitch * d.H * d.Cin * 4;
-            box[0] = (cuuint32_t)pl.BW, box[1] = (cuuint32_t)pl.Rin, box[2] = 8u, box[3] = 1u;
         }
+        for (int i = 0; i < 4; ++i) box[i] = (cuuint32_t)pl.box[i];
         const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
         void *base = padded ? static_cast<void *>(h->xpad) : const_cast<float *>(x);
         const CUresult r = enc(&args.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box,
@@ -1750,9 +1784,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.nhwc = nhwc ? 1 : 0;
     a.a_off = pl.a_off, a.b_off = pl.b_off, a.raw_off = pl.raw_off, a.bar_off = pl.bar_off;
     a.scratch_off = pl.scratch_off;
-    a.a_plane_bytes = (uint32_t)a.Cout * 16u;
-    a.a_lbo = (uint32_t)(2 * pl.S + 1) * a.a_plane_bytes;
-    a.a_kw_stride = 2u * a.a_lbo;
+    a.a_plane_bytes = pl.a_plane_bytes, a.a_lbo = pl.a_lbo, a.a_kw_stride = pl.a_kw_stride;
     a.idesc = make_idesc(128, pl.P);
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
