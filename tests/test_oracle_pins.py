@@ -59,6 +59,38 @@ def test_golden_shapes():
             raise AssertionError(what)
 
 
+def read_golden_gn_counts():
+    rows = []
+    with open(os.path.join(GOLDEN, "gn_counts.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                rows.append(tuple(int(v) for v in line.split()))
+    return rows
+
+
+def test_golden_gn_counts():
+    """The oracle's GroupNorm statistics run over the element count the pages
+    state.  One conv output of the group holds the count itself and every
+    other one is zero (a centre-tap filter on one channel copies a single
+    non-zero input), so the mean is exactly 1 only if the oracle divides by
+    that count, and the biased variance is exactly count - 1."""
+    rows = read_golden_gn_counts()
+    assert len(rows) == 1
+    for N, Cin, H, W, Cout, G, count, pairs in rows:
+        assert N * G == pairs
+        x = np.zeros((1, Cin, H, W), np.float32)
+        x[0, 0, 1 + 37, 1 + 101] = count
+        w = np.zeros((Cout, Cin, 3, 3), np.float32)
+        w[0, 0, 1, 1] = 1.0
+        b = np.zeros(Cout, np.float32)
+        one = np.ones(Cout, np.float32)
+        ch = oracle.chain(oracle.GN_SCALE_POOL_CLAMP, groups=G, eps=0.0, gamma=one, beta=b, scale=one, pool_k=4)
+        _, _, mean, rstd = oracle.gn_group(x, w, b, ch, 0, 0, nthreads=4)
+        assert mean == 1.0
+        assert abs(rstd * np.sqrt(count - 1.0) - 1.0) < 1e-12
+
+
 def test_pool_out_matches_torch_floor_mode():
     for ho in range(4, 40):
         for k in (2, 3, 4, 5):
