@@ -241,6 +241,8 @@ typedef struct {
     int64_t acc_cols;        /* tensor-memory columns per accumulator buffer (two buffers) */
     int64_t tmem_cols;       /* tensor-memory columns the kernel allocates */
     int64_t conv_items;      /* converter work items the kernel holds per chunk */
+    int64_t wpack_bytes;     /* the handle's packed-filter buffer */
+    int64_t xpad_bytes;      /* the handle's padded copy of x (0 unless NCHW rows need it) */
 } conv_epi_plan;
 
 /* Fill *plan for desc (mode must be CONV_EPI_MODE_TF32) and epi.  Returns

@@ -95,6 +95,14 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
                 start = (S + 1 - sk) * ap + kw * kws + g * lbo
                 assert start >= 0 and start + 128 * 16 <= q["a_bytes"]
     assert q["a_bytes"] % 1024 == 0 and q["b_bytes"] % 1024 == 0 and q["raw_bytes"] % 1024 == 0
+    # the packed filter: the pack kernel writes, and the producer copies,
+    # chunk c of channel tile m at (m * chunks + c) * a_bytes
+    assert q["wpack_bytes"] >= q["MT"] * q["chunks"] * q["a_bytes"]
+    # the padded copy of x: rows of x_pitch floats, one per (image, channel, row)
+    if not nhwc and W % 4:
+        assert q["xpad_bytes"] == N * Cin * H * q["x_pitch"] * 4
+    else:
+        assert q["xpad_bytes"] == 0
     # shared memory: filter (resident: every chunk), B planes, staged tiles,
     # barriers, scratch, in order and disjoint, within the CTA limit
     filt = (q["chunks"] * q["MT"] if q["resident"] else q["na"]) * q["a_bytes"]

@@ -1696,6 +1696,10 @@ conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_de
     for (int i = 0; i < 4; ++i) q.box[i] = pl.box[i];
     q.acc_cols = kAccStride, q.tmem_cols = kTmemCols;
     q.conv_items = kConvItems * kConvWarps;
+    conv_epi_desc dt = d;
+    dt.mode = CONV_EPI_MODE_TF32;
+    q.wpack_bytes = (int64_t)tc_wpack_bytes(dt);
+    q.xpad_bytes = (int64_t)tc_xpad_bytes(dt);
     return tc_supported(d, &e);
 }
 
