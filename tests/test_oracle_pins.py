@@ -91,6 +91,24 @@ def test_golden_gn_counts():
         assert abs(rstd * np.sqrt(count - 1.0) - 1.0) < 1e-12
 
 
+def test_golden_output_counts():
+    """Element counts of the full-size outputs: the product of the oracle's
+    output shape (the pages' printed figures disagree with one another and
+    with their own shapes; the fixture cites them)."""
+    rows = []
+    with open(os.path.join(GOLDEN, "output_counts.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                rows.append(line.split())
+    assert len(rows) == 2
+    for N, Cin, H, W, Cout, chain, count in rows:
+        kind = {"min": oracle.MIN_TANH2, "gn_pool4": oracle.GN_SCALE_POOL_CLAMP}[chain]
+        ch = oracle.chain(kind, groups=16, pool_k=4)
+        shape = oracle.output_shape(int(N), int(Cin), int(H), int(W), int(Cout), ch)
+        assert int(np.prod(shape)) == int(count)
+
+
 def test_pool_out_matches_torch_floor_mode():
     for ho in range(4, 40):
         for k in (2, 3, 4, 5):
