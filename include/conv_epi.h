@@ -146,7 +146,12 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *     launch (every CTA resident) that finalizes inside the kernel; where the
  *     device refuses that launch, a second finalize kernel follows.
  *   Other shapes return CONV_EPI_ERR_UNSUPPORTED: at create, or at the first
- *   forward for chain-specific limits. */
+ *   forward for chain-specific limits.
+ * Debug mode: with the environment variable CONV_EPI_DEBUG set to "1" when
+ * the handle is created, every conv_epi_forward on it waits for its stream
+ * and returns the device-side status itself (as conv_epi_sync would), so a
+ * barrier timeout surfaces at the call that caused it.  Such forwards cannot
+ * be captured into a CUDA graph. */
 CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi_handle *out);
 
 /* Allocate, ahead of the first forward, whatever workspace `epi` will need

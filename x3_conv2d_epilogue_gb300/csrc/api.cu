@@ -3,6 +3,7 @@
 // path, host-buffer forward and device error reporting.
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <new>
@@ -183,6 +184,8 @@ CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi
     h->sm_count = prop.multiProcessorCount;
     h->cc_major = prop.major, h->cc_minor = prop.minor;
     h->coop = prop.cooperativeLaunch;
+    const char *dbg = getenv("CONV_EPI_DEBUG");
+    h->debug = dbg && dbg[0] == '1' && dbg[1] == '\0';
     cudaError_t e = cudaMalloc(&h->dev_err, 256);
     if (e == cudaSuccess) e = cudaMemset(h->dev_err, 0, 256);
     if (e == cudaSuccess && desc->mode == CONV_EPI_MODE_TF32) {
@@ -225,8 +228,11 @@ CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x,
     if (epi->kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
         if ((st = conv_epi_reserve(h, epi))) return st;
     }
-    if (h->d.mode == CONV_EPI_MODE_FP32) return conv_epi::simt_forward(h, x, w, b, *epi, out, s);
-    return conv_epi::tc_forward(h, x, w, b, *epi, out, s);
+    st = h->d.mode == CONV_EPI_MODE_FP32 ? conv_epi::simt_forward(h, x, w, b, *epi, out, s)
+                                         : conv_epi::tc_forward(h, x, w, b, *epi, out, s);
+    // debug handles report device-side errors (a barrier timeout) here
+    if (st == CONV_EPI_OK && h->debug) st = conv_epi_sync(h, stream);
+    return st;
 }
 
 CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const float *x, const float *w,

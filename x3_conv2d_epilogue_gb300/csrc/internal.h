@@ -74,6 +74,10 @@ struct conv_epi_handle_s {
 
     int last_launches = 0;
 
+    // CONV_EPI_DEBUG=1 at create: every forward waits for its stream and
+    // returns the device-side status itself
+    int debug = 0;
+
     // conv_epi_test_drop_tile: the next tf32 forward skips this staged tile
     int test_drop_tile = -1;
 };
