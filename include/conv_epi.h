@@ -123,7 +123,9 @@ typedef struct {
                                  Only CONV_EPI_MODE_FP32 produces indices. */
 } conv_epi_epilogue_desc;
 
-/* Output shape of a chain: shape[4] = {N, C, Ho', Wo'}.  Pure host call. */
+/* Output shape of a chain: shape[4] = {N, C, Ho', Wo'}.  Pure host call.
+ * The min chains reduce with keepdim (C = 1); without keepdim the same
+ * N*Ho*Wo floats are the [N][Ho][Wo] tensor, so one output serves both. */
 CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
                                                    const conv_epi_epilogue_desc *epi,
                                                    int64_t shape[4]);
