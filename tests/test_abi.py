@@ -169,3 +169,25 @@ def test_noalloc_refuses_rows_that_need_padding_before_the_device(lib):
     assert lib.conv_epi_forward_noalloc(C.byref(d), fake, fake, fake, C.byref(epi), fake, None) == 2
     d = ce.Desc(1, 8, 8, 7, 64, ce.MODE_TF32, ce.LAYOUT_NHWC)  # channels last: reaches the device
     assert lib.conv_epi_forward_noalloc(C.byref(d), fake, fake, fake, C.byref(epi), fake, None) == 4
+
+
+def test_binding_checks_tensor_arguments():
+    """The binding refuses, before any library call, tensors whose element
+    type, layout or memory a raw pointer cannot carry."""
+    import torch
+    f32 = torch.zeros(8)
+    with pytest.raises(TypeError):
+        ce.conv_epi_forward(None, torch.zeros(8, dtype=torch.float64), f32, f32, ce.epilogue(ce.SCALE_MIN), f32)
+    with pytest.raises(ValueError):                                   # not contiguous
+        ce.conv_epi_forward_host(None, torch.zeros(4, 4).t(), f32, f32, ce.epilogue(ce.SCALE_MIN), f32)
+    with pytest.raises(ValueError):                                   # host tensor to a device call
+        ce.conv_epi_forward(None, f32, f32, f32, ce.epilogue(ce.SCALE_MIN), f32)
+    with pytest.raises(ValueError):                                   # numpy array to a device call
+        ce.conv_epi_forward_noalloc(1, 8, 8, 8, 64, np.zeros(8, np.float32), f32, f32, ce.epilogue(ce.SCALE_MIN), f32)
+    with pytest.raises(TypeError):                                    # the chain's parameters are float32
+        ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=np.zeros(8, np.float64))
+    with pytest.raises(TypeError):                                    # indices are int32
+        ce.epilogue(ce.SCALE_MIN, index_out=np.zeros(8, np.float32))
+    with pytest.raises(ValueError):                                   # host parameters to a device call
+        ce.conv_epi_forward(None, 1 << 20, 1 << 20, 1 << 20,
+                            ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=np.zeros(8, np.float32)), 1 << 20)

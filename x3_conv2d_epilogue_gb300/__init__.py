@@ -5,7 +5,10 @@ it calls (include/conv_epi.h) and takes torch CUDA tensors (or, for
 ``conv_epi_forward_host``, numpy arrays / CPU tensors) in place of pointers.
 Every step of the computation runs in the library's CUDA kernels; there is no
 fallback: if ``libconv_epi.so`` is missing or the device is not sm_103a, the
-calls raise.
+calls raise.  Before a call, tensor arguments are checked for what their raw
+addresses cannot carry: element type (float32, int32 for indices),
+C-contiguity, and device or host memory as the call requires.  Their sizes
+must match the problem description; plain integers pass as raw addresses.
 """
 from __future__ import annotations
 
@@ -120,14 +123,42 @@ def exported_symbols():
     return sorted(set(re.findall(r"CONV_EPI_API\s+[\w\s\*]*?\b(conv_epi_\w+)\s*\(", text)))
 
 
-def _ptr(t):
-    if t is None:
-        return None
-    if hasattr(t, "data_ptr"):
+def _arg(t, what, device=None, index=False):
+    """Address of a tensor argument after the checks a raw pointer cannot
+    carry: element type (float32; int32 for an index output), C-contiguity
+    and, where the call fixes it, device (True) or host (False) memory.
+    None and plain integers (raw addresses) pass unchecked."""
+    if t is None or isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):  # torch tensor
+        import torch
+        want = torch.int32 if index else torch.float32
+        if t.dtype != want:
+            raise TypeError(f"{what}: dtype {t.dtype}, expected {want}")
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: not contiguous")
+        if device is not None and bool(t.is_cuda) != device:
+            raise ValueError(f"{what}: expected {'device' if device else 'host'} memory")
         return t.data_ptr()
-    if hasattr(t, "ctypes"):
+    if hasattr(t, "ctypes"):  # numpy array: host memory
+        import numpy as np
+        want = np.int32 if index else np.float32
+        if t.dtype != want:
+            raise TypeError(f"{what}: dtype {t.dtype}, expected {np.dtype(want)}")
+        if not t.flags.c_contiguous:
+            raise ValueError(f"{what}: not C-contiguous")
+        if device:
+            raise ValueError(f"{what}: a numpy array is host memory; this call takes device memory")
         return t.ctypes.data
     return int(t)
+
+
+def _tensors(x, w, b, epi, out, device):
+    """The forward's pointer arguments, checked; the chain's tensors too."""
+    keep = getattr(epi, "_keep", (None, None, None, None))
+    for v, what, index in zip(keep, ("chan_scale", "gamma", "beta", "index_out"), (False, False, False, True)):
+        _arg(v, what, device, index)
+    return _arg(x, "x", device), _arg(w, "w", device), _arg(b, "b", device), _arg(out, "out", device)
 
 
 def _stream(stream):
@@ -147,8 +178,8 @@ def _check(st, where):
 def epilogue(kind, scalar=1.0, chan_scale=None, lrelu_slope=0.01, groups=16, eps=1e-5, gamma=None, beta=None,
              pool_k=4, clamp_lo=0.0, clamp_hi=1.0, index_out=None):
     """Build a conv_epi_epilogue_desc; tensors are kept alive on the object."""
-    e = EpilogueDesc(kind, scalar, _ptr(chan_scale), lrelu_slope, groups, eps, _ptr(gamma), _ptr(beta), pool_k,
-                     clamp_lo, clamp_hi, _ptr(index_out))
+    e = EpilogueDesc(kind, scalar, _arg(chan_scale, "chan_scale"), lrelu_slope, groups, eps, _arg(gamma, "gamma"),
+                     _arg(beta, "beta"), pool_k, clamp_lo, clamp_hi, _arg(index_out, "index_out", index=True))
     e._keep = (chan_scale, gamma, beta, index_out)
     return e
 
@@ -187,14 +218,14 @@ def conv_epi_reserve(h, epi):
 
 
 def conv_epi_forward(h, x, w, b, epi, out, stream=None):
-    _check(_lib().conv_epi_forward(h, _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out), _stream(stream)),
-           "conv_epi_forward")
+    px, pw, pb, po = _tensors(x, w, b, epi, out, device=True)
+    _check(_lib().conv_epi_forward(h, px, pw, pb, C.byref(epi), po, _stream(stream)), "conv_epi_forward")
     return out
 
 
 def conv_epi_forward_host(h, x, w, b, epi, out, stream=None):
-    _check(_lib().conv_epi_forward_host(h, _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out), _stream(stream)),
-           "conv_epi_forward_host")
+    px, pw, pb, po = _tensors(x, w, b, epi, out, device=False)
+    _check(_lib().conv_epi_forward_host(h, px, pw, pb, C.byref(epi), po, _stream(stream)), "conv_epi_forward_host")
     return out
 
 
@@ -203,8 +234,9 @@ def conv_epi_forward_noalloc(N, Cin, H, W, Cout, x, w, b, epi, out, stream=None,
     """Tensor-core forward without a handle: the library allocates nothing and
     uses its fixed device-side scratch array (see include/conv_epi.h)."""
     d = Desc(N, Cin, H, W, Cout, mode, layout)
-    _check(_lib().conv_epi_forward_noalloc(C.byref(d), _ptr(x), _ptr(w), _ptr(b), C.byref(epi), _ptr(out),
-                                           _stream(stream)), "conv_epi_forward_noalloc")
+    px, pw, pb, po = _tensors(x, w, b, epi, out, device=True)
+    _check(_lib().conv_epi_forward_noalloc(C.byref(d), px, pw, pb, C.byref(epi), po, _stream(stream)),
+           "conv_epi_forward_noalloc")
     return out
 
 
