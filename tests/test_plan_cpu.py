@@ -133,8 +133,10 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
 
 def parity_shapes():
     import test_parity_gpu as tp
+    import test_zz_guard_gpu as tg
     shapes = dict(tp.SMALL)
     shapes.update(tp.FP32_ONLY)
+    shapes.update({"guard_" + k: v for k, v in tg.CASES.items()})
     for name, wl in synth.WORKLOADS.items():
         shapes["full_" + name] = wl
     return shapes

@@ -24,6 +24,10 @@ CASES = {
     "c5t": W["c5_gn_pool_clamp"].resized(N=2, H=40),                     # pooled rows past the last band
     "c5_w37": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=37),            # two bands, columns past the pool
     "min_cout1": W["pr1_min_tanh2"].resized(N=1, Cin=1, H=3, W=4, Cout=1),
+    # narrow rows with many output channels: the fp32 kernel stages fewer
+    # channel slots per pass so the filter taps fit shared memory
+    "c4_co512_w8": W["c4_scale_min"].resized(N=2, H=6, W=8, Cout=512),
+    "c3_co640_w10": W["c3_mul_lrelu_gelu"].resized(N=1, Cin=24, H=5, W=10, Cout=640),
 }
 GUARD = 64          # elements on each side (256 bytes: the output stays 16-byte aligned)
 SENTINEL = -1234.5

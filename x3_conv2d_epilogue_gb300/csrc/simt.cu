@@ -29,6 +29,9 @@ constexpr int kCO = 16;  // output channels per thread per pass
 constexpr int kPX = 4;   // consecutive output pixels per thread
 constexpr int kRowsPerCta = 4;  // output rows per CTA for the min and per-channel chains
 constexpr int kStageLoads = 4;  // staging loads in flight per thread (8 measured no better)
+// dynamic shared memory per CTA: the 227 KB opt-in less the static group sums
+// and a margin
+constexpr size_t kSmemDynLimit = 227 * 1024 - 2 * 1024;
 
 struct SimtArgs {
     const float *x, *w, *b;
@@ -351,14 +354,22 @@ Layout layout_for(const conv_epi_desc &d, int Wo) {
     const int cg = (d.Cout + kCO - 1) / kCO;
     L.CS = 256 / L.PG;
     if (L.CS > cg) L.CS = cg;
-    L.TW = L.PG * kPX, L.XW = L.TW + 4, L.COP = L.CS * kCO;
+    L.TW = L.PG * kPX, L.XW = L.TW + 4;
     L.ntiles = (Wo + L.TW - 1) / L.TW;
-    const size_t stage = (size_t)(kCI * 3 * L.XW + kCI * 9 * L.COP) * sizeof(float);
-    const size_t red_min = (size_t)2 * L.CS * L.TW * sizeof(float);
-    const size_t red_gn = (size_t)2 * L.COP * L.PG * sizeof(float);
-    L.smem = stage;
-    if (red_min > L.smem) L.smem = red_min;
-    if (red_gn > L.smem) L.smem = red_gn;
+    // fewer channel slots where narrow rows would otherwise stage more filter
+    // taps than a CTA's shared memory holds (many output channels, few pixel
+    // groups); the channel passes then take the rest
+    for (;;) {
+        L.COP = L.CS * kCO;
+        const size_t stage = (size_t)(kCI * 3 * L.XW + kCI * 9 * L.COP) * sizeof(float);
+        const size_t red_min = (size_t)2 * L.CS * L.TW * sizeof(float);
+        const size_t red_gn = (size_t)2 * L.COP * L.PG * sizeof(float);
+        L.smem = stage;
+        if (red_min > L.smem) L.smem = red_min;
+        if (red_gn > L.smem) L.smem = red_gn;
+        if (L.smem <= kSmemDynLimit || L.CS == 1) break;
+        --L.CS;
+    }
     return L;
 }
 
