@@ -26,7 +26,9 @@
 // the plane to the tensor core covers only short shared-memory stores --
 // never global loads in flight.  Channels-last input (x as [N][H][W][Cin])
 // skips both: its 4-channel boxes land straight in the B planes, whose
-// 16-byte position rows they already match.
+// 16-byte position rows they already match.  A tensor map's row stride must
+// be a multiple of 16 bytes, so NCHW rows whose W is not a multiple of 4 are
+// read from a padded copy of x (pad_rows, before the conv kernel).
 //
 // Row slots.  The MMA's M is 128.  With Cout = 128 a tile is one output row
 // per accumulator.  With Cout = 64 the 128 accumulator lanes hold TWO output
