@@ -104,9 +104,9 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
 
 // tcgen05 tf32 path (tc.cu)
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e);
-size_t tc_xpad_bytes(const conv_epi_desc &d);
+size_t tc_xpad_bytes(const conv_epi_desc &d);  // 0 unless the input rows need the padded copy
 // the plan a forward would launch (pure host; conv_epi_plan_query)
-conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, conv_epi_plan &q);  // 0 unless the input rows need the padded copy
+conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, conv_epi_plan &q);
 size_t tc_wpack_bytes(const conv_epi_desc &d);
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
 conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
