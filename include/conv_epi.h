@@ -39,6 +39,8 @@
  *     different handles are independent.
  *   - There is no CPU fallback: without a usable sm_103a device, calls that
  *     compute return CONV_EPI_ERR_CUDA or CONV_EPI_ERR_UNSUPPORTED.
+ *   - An empty batch (N = 0) is valid.  Its forwards check the chain as usual
+ *     and return CONV_EPI_OK without device work; x and out may then be null.
  */
 #ifndef CONV_EPI_H
 #define CONV_EPI_H

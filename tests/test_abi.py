@@ -60,7 +60,7 @@ def test_output_shapes(lib):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(N=0), dict(Cin=0), dict(H=2), dict(W=1), dict(Cout=0), dict(mode=7), dict(layout=2), dict(layout=-1),
+    dict(N=-1), dict(Cin=0), dict(H=2), dict(W=1), dict(Cout=0), dict(mode=7), dict(layout=2), dict(layout=-1),
 ])
 def test_bad_descriptions_rejected(lib, bad):
     d = dict(N=1, Cin=4, H=8, W=8, Cout=8, mode=ce.MODE_FP32, layout=ce.LAYOUT_NCHW)
@@ -191,3 +191,23 @@ def test_binding_checks_tensor_arguments():
     with pytest.raises(ValueError):                                   # host parameters to a device call
         ce.conv_epi_forward(None, 1 << 20, 1 << 20, 1 << 20,
                             ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=np.zeros(8, np.float32)), 1 << 20)
+
+
+def test_empty_batch(lib):
+    """N = 0 is a valid, empty problem: its output has no elements, and the
+    allocation-free forward (which needs no handle) returns OK with null
+    tensors and no device work, after the same chain checks and refusals."""
+    assert ce.conv_epi_output_shape(0, 16, 10, 12, 64, ce.epilogue(ce.MIN_TANH2)) == (0, 1, 8, 10)
+    gn = ce.epilogue(ce.GN_SCALE_POOL_CLAMP, chan_scale=16, gamma=16, beta=16, groups=16, pool_k=4)
+    assert ce.conv_epi_output_shape(0, 8, 18, 16, 64, gn) == (0, 64, 4, 3)
+    d = ce.Desc(0, 16, 10, 12, 64, ce.MODE_TF32, ce.LAYOUT_NCHW)
+    assert lib.conv_epi_forward_noalloc(C.byref(d), None, None, None, C.byref(ce.epilogue(ce.MIN_TANH2)), None,
+                                        None) == 0
+    assert lib.conv_epi_forward_noalloc(C.byref(d), None, None, None, C.byref(ce.epilogue(9)), None, None) == 1
+    assert lib.conv_epi_forward_noalloc(C.byref(d), None, None, None, C.byref(gn), None, None) == 2
+    odd = ce.Desc(0, 16, 10, 13, 64, ce.MODE_TF32, ce.LAYOUT_NCHW)   # would need the padded copy
+    assert lib.conv_epi_forward_noalloc(C.byref(odd), None, None, None, C.byref(ce.epilogue(ce.MIN_TANH2)), None,
+                                        None) == 2
+    full = ce.Desc(1, 16, 10, 12, 64, ce.MODE_TF32, ce.LAYOUT_NCHW)  # a non-empty batch still needs tensors
+    assert lib.conv_epi_forward_noalloc(C.byref(full), None, None, None, C.byref(ce.epilogue(ce.MIN_TANH2)), None,
+                                        None) == 1

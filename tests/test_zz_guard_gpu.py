@@ -79,3 +79,31 @@ def test_writes_stay_inside_the_output(case, mode):
         check_fp32(got, ref, case)
     else:
         check_tf32(got, ref, case)
+
+
+@pytest.mark.parametrize("mode", ["tf32", "fp32"])
+def test_empty_batch_is_a_no_op(mode):
+    """N = 0: a handle is created, every forward (device and host buffers,
+    every chain) returns OK with empty tensors and launches nothing."""
+    import torch
+    import x3_conv2d_epilogue_gb300 as ce
+    m = ce.MODE_TF32 if mode == "tf32" else ce.MODE_FP32
+    p = torch.ones(64, device="cuda")
+    chains = [ce.epilogue(ce.MIN_TANH2), ce.epilogue(ce.SCALE_MIN, scalar=-2.0),
+              ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=p),
+              ce.epilogue(ce.GN_SCALE_POOL_CLAMP, chan_scale=p, gamma=p, beta=p, groups=16, pool_k=4)]
+    x = torch.empty(0, 8, 18, 16, device="cuda")
+    w = torch.zeros(64, 8, 3, 3, device="cuda")
+    h = ce.conv_epi_create(0, 8, 18, 16, 64, m)
+    try:
+        for epi in chains:
+            out = torch.empty(ce.conv_epi_output_shape(0, 8, 18, 16, 64, epi, m), device="cuda")
+            assert out.numel() == 0
+            ce.conv_epi_forward(h, x, w, p, epi, out)
+            assert ce.conv_epi_last_launch_count(h) == 0
+        ce.conv_epi_sync(h)
+        host = ce.epilogue(ce.MIN_TANH2)
+        ce.conv_epi_forward_host(h, np.empty((0, 8, 18, 16), np.float32), np.zeros((64, 8, 3, 3), np.float32),
+                                 np.ones(64, np.float32), host, np.empty((0, 1, 16, 14), np.float32))
+    finally:
+        ce.conv_epi_destroy(h)

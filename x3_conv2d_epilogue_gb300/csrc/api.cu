@@ -18,7 +18,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 conv_epi_status check_desc(const conv_epi_desc *d) {
     if (!d) return CONV_EPI_ERR_INVALID_ARG;
-    if (d->N < 1 || d->Cin < 1 || d->Cout < 1 || d->H < 3 || d->W < 3) return CONV_EPI_ERR_INVALID_ARG;
+    if (d->N < 0 || d->Cin < 1 || d->Cout < 1 || d->H < 3 || d->W < 3) return CONV_EPI_ERR_INVALID_ARG;
     if (d->mode != CONV_EPI_MODE_TF32 && d->mode != CONV_EPI_MODE_FP32) return CONV_EPI_ERR_INVALID_ARG;
     if (d->layout != CONV_EPI_LAYOUT_NCHW && d->layout != CONV_EPI_LAYOUT_NHWC) return CONV_EPI_ERR_INVALID_ARG;
     // element counts and offsets are kept in 64-bit, but every single tensor
@@ -76,6 +76,14 @@ conv_epi_status check_mode_support(const conv_epi_desc &d, const conv_epi_epilog
     if (d.mode == CONV_EPI_MODE_FP32)
         return e ? conv_epi::simt_supported(d, *e) : CONV_EPI_OK;
     return conv_epi::tc_supported(d, e);
+}
+
+// An empty batch (N = 0) computes nothing: its forwards validate the chain
+// against the handle's problem and return without touching the device (the
+// tensor pointers may then be null).
+conv_epi_status empty_batch(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
+    const conv_epi_status st = check_epi(d, e);
+    return st ? st : check_mode_support(d, e);
 }
 
 conv_epi_status forward_checks(conv_epi_handle h, const float *x, const float *w, const float *b,
@@ -221,6 +229,10 @@ CONV_EPI_API conv_epi_status conv_epi_reserve(conv_epi_handle h, const conv_epi_
 
 CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
                                               const conv_epi_epilogue_desc *epi, float *out, void *stream) {
+    if (h && h->d.N == 0) {
+        h->last_launches = 0;
+        return empty_batch(h->d, epi);
+    }
     conv_epi_status st = forward_checks(h, x, w, b, epi, out);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -238,6 +250,10 @@ CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x,
 CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const float *x, const float *w,
                                                    const float *b, const conv_epi_epilogue_desc *epi, float *out,
                                                    void *stream) {
+    if (h && h->d.N == 0) {
+        h->last_launches = 0;
+        return empty_batch(h->d, epi);
+    }
     if (!h || !x || !w || !b || !epi || !out) return CONV_EPI_ERR_INVALID_ARG;
     conv_epi_status st = check_epi(h->d, epi);
     if (st) return st;

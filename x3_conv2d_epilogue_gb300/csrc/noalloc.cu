@@ -77,9 +77,10 @@ extern "C" CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_
                                                                  const float *w, const float *b,
                                                                  const conv_epi_epilogue_desc *epi, float *out,
                                                                  void *stream) {
-    if (!desc || !x || !w || !b || !epi || !out) return CONV_EPI_ERR_INVALID_ARG;
+    if (!desc || !epi) return CONV_EPI_ERR_INVALID_ARG;
     const conv_epi_desc &d = *desc;
-    if (d.N < 1 || d.Cin < 1 || d.Cout < 1 || d.H < 3 || d.W < 3) return CONV_EPI_ERR_INVALID_ARG;
+    if (d.N > 0 && (!x || !w || !b || !out)) return CONV_EPI_ERR_INVALID_ARG;  // an empty batch may pass nulls
+    if (d.N < 0 || d.Cin < 1 || d.Cout < 1 || d.H < 3 || d.W < 3) return CONV_EPI_ERR_INVALID_ARG;
     if (d.layout != CONV_EPI_LAYOUT_NCHW && d.layout != CONV_EPI_LAYOUT_NHWC) return CONV_EPI_ERR_INVALID_ARG;
     if (d.mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;
     if (d.layout == CONV_EPI_LAYOUT_NHWC && d.Cin % 4 != 0) return CONV_EPI_ERR_UNSUPPORTED;
@@ -101,6 +102,11 @@ extern "C" CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_
         return CONV_EPI_ERR_INVALID_ARG;
     }
     if (epi->index_out) return CONV_EPI_ERR_UNSUPPORTED;  // indices come from the fp32 mode only
+    if (d.N == 0) {  // an empty batch: the same refusals, then nothing to compute
+        const conv_epi_status st0 = conv_epi::tc_supported(d, epi);
+        if (st0) return st0;
+        return conv_epi::tc_wpack_bytes(d) > kNoAllocScratchBytes ? CONV_EPI_ERR_UNSUPPORTED : CONV_EPI_OK;
+    }
     if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(out)) return CONV_EPI_ERR_ALIGNMENT;
     conv_epi_status st = conv_epi::tc_supported(d, epi);
     if (st) return st;
