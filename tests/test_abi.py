@@ -211,3 +211,10 @@ def test_empty_batch(lib):
     full = ce.Desc(1, 16, 10, 12, 64, ce.MODE_TF32, ce.LAYOUT_NCHW)  # a non-empty batch still needs tensors
     assert lib.conv_epi_forward_noalloc(C.byref(full), None, None, None, C.byref(ce.epilogue(ce.MIN_TANH2)), None,
                                         None) == 1
+
+
+def test_binding_has_every_entry_point():
+    """The binding offers a function of the same name for every call the
+    header declares."""
+    assert [n for n in ce.exported_symbols() if not callable(getattr(ce, n, None))] == []
+    assert isinstance(ce.conv_epi_last_cuda_error(), str)

@@ -270,6 +270,11 @@ def conv_epi_status_string(status):
     return _lib().conv_epi_status_string(status).decode()
 
 
+def conv_epi_last_cuda_error():
+    """Text of the last failing CUDA call the library recorded."""
+    return _lib().conv_epi_last_cuda_error().decode()
+
+
 class ConvEpi:
     """Owns one handle; ``forward`` allocates the output with torch."""
 
