@@ -218,3 +218,43 @@ def test_binding_has_every_entry_point():
     header declares."""
     assert [n for n in ce.exported_symbols() if not callable(getattr(ce, n, None))] == []
     assert isinstance(ce.conv_epi_last_cuda_error(), str)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "conv_epi.h"
+int main(void) {
+    conv_epi_desc d = {128, 16, 256, 256, 64, CONV_EPI_MODE_TF32, CONV_EPI_LAYOUT_NCHW};
+    conv_epi_epilogue_desc e = {0};
+    e.kind = CONV_EPI_MIN_TANH2;
+    e.scalar = 1.0f;
+    int64_t s[4];
+    conv_epi_plan q;
+    int st = (int)conv_epi_output_shape(&d, &e, s);
+    int sq = (int)conv_epi_plan_query(&d, &e, &q);
+    printf("%d %d %lld %lld %lld %lld %d %lld\n", conv_epi_version(), st, (long long)s[0], (long long)s[1],
+           (long long)s[2], (long long)s[3], sq, (long long)q.struct_bytes);
+    return 0;
+}
+"""
+
+
+def test_plain_c_program_uses_the_abi(lib, tmp_path):
+    """The header is plain C (C11, pedantic, no warnings) and a C program
+    links against the library and calls it without any Python or torch."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    pkg = os.path.dirname(ce.LIB_PATH)
+    inc = os.path.dirname(ce.HEADER)
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src), "-L", pkg,
+                        "-lconv_epi", f"-Wl,-rpath,{pkg}", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert int(out[0]) == ce.conv_epi_version()
+    assert out[1:6] == ["0", "128", "1", "254", "254"]
+    assert out[6] == "0" and int(out[7]) == ce.C.sizeof(ce.Plan)
