@@ -1613,7 +1613,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// the driver's tensor-map encoder, looked up once (a function-local static:
+// the CUDA driver API's tensor-map encoder, looked up once (a function-local static:
 // initialised exactly once even when several host threads call first)
 EncodeTiledFn encode_tiled() {
     static const EncodeTiledFn fn = []() -> EncodeTiledFn {
