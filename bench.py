@@ -2,18 +2,28 @@
 """Throughput of the fused 3x3 conv + epilogue on GB300.
 
 One step = one conv_epi_forward over the whole batch of the workload (conv +
-fused chain), inputs resident in HBM.  Default workload: x[128,16,256,256],
-Conv2d 16->64 (k3, s1, p0) with bias, min over channels, tanh, tanh
-(``c2_min_tanh2``), in the tf32 tensor-core mode.
+fused chain), inputs resident in HBM.  Default workload (the largest of the
+five, and the headline): x[64,64,256,256], Conv2d 64->128 (k3, s1, p0) with
+bias, x 2.0, min over channels (``c4_scale_min``), in the tf32 tensor-core
+mode.  L2 is flushed between timed steps (outside the step's events): a write
+of a buffer larger than L2 evicts what the previous step left there, and a
+read of a second one replaces the flush's own dirty lines with clean ones, so
+that their write-back does not land inside the next timed step.
 
 Prints ONE JSON line (rank 0).  Metric: TFLOP/s = 2*N*Cout*Ho*Wo*Cin*9 / time.
-  value      - whole-job TFLOP/s over the K timed steps (max over ranks)
+  value      - whole-job TFLOP/s over the K timed steps (sum of the steps'
+               event times; max over ranks)
   e2e        - the same metric through conv_epi_forward_host, host buffers in
                and out (pinned), copies inside the timed region
-  roofline   - the fused conv kernel against the tf32 tensor peak derived from
-               the measured bf16 peak (x 1.1/2.25, the nominal tf32:bf16 ratio)
+  roofline   - the forward against the tf32 tensor peak derived from the
+               measured bf16 peak (x 1.1/2.25, the nominal dense tf32:bf16
+               ratio of the GB300's published rates), and against the
+               measured HBM copy bandwidth
+  per_config - every other workload timed the same way in the same process:
+               TFLOP/s, ms, both roofline fractions, the oracle on the host
+               cores and the unfused comparator
   cpu_baseline - the fp64 oracle on the host cores over a bounded sample
-  clocks     - nvidia-smi samples taken during the timed region
+  clocks     - nvidia-smi samples taken during the timed regions
   unfused    - context only, off the measured path: the unfused pipeline the
                pages start from (PyTorch conv2d on cuDNN, the full conv output
                written to HBM, then the chain as PyTorch ops), same inputs,
@@ -46,7 +56,9 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "fused conv+epilogue TFLOP/s and % of GB300 TF32 dense peak (1 GPU)"
-TF32_PER_BF16 = 1.1 / 2.25        # nominal dense tf32 : bf16 tensor rates
+# nominal dense tensor rates of a GB300 (no 2:4 sparsity): tf32 1.1 PFLOP/s,
+# bf16 2.25 PFLOP/s; the tf32 peak is the measured bf16 peak times their ratio
+TF32_PER_BF16 = 1.1 / 2.25
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -211,22 +223,6 @@ def unfused_chain(wl, dev, mode_tf32: bool):
     return run
 
 
-def time_unfused(wl, dev, mode_tf32: bool, steps: int, warmup: int, stream):
-    import torch
-    run = unfused_chain(wl, dev, mode_tf32)
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            run()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(steps):
-            run()
-        b.record(stream)
-        torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps
-
-
 def traffic_for(kernel_src_hash: str, workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -273,22 +269,142 @@ def run_reference(args, wl, world, rank):
     return 0
 
 
+class L2Flush:
+    """Evicts L2 between timed steps, outside their events: a write of a
+    buffer larger than L2 (what the previous step left there goes out), then
+    a read of a second such buffer (the write's dirty lines are replaced by
+    clean ones, so their write-back does not land in the next timed step)."""
+
+    def __init__(self, torch, stream):
+        l2 = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0))
+        self.bytes = max(2 * l2, 256 << 20)
+        self.w = torch.empty(self.bytes // 4, dtype=torch.float32, device="cuda")
+        self.r = torch.zeros(self.bytes // 4, dtype=torch.float32, device="cuda")
+        self.sink = torch.empty(1, dtype=torch.float32, device="cuda")
+        self.stream = stream
+        self.torch = torch
+        self.l2 = l2
+
+    def __call__(self):
+        with self.torch.cuda.stream(self.stream):
+            self.w.fill_(1.0)
+            self.torch.amax(self.r, dim=0, keepdim=True, out=self.sink)
+
+    def describe(self):
+        return (f"L2 ({self.l2 / 1e6:.0f} MB) flushed between timed steps, outside the steps' events: "
+                f"write {self.bytes / 1e6:.0f} MB, then read {self.bytes / 1e6:.0f} MB")
+
+
+class Case:
+    """One workload on the device: resident inputs, its chain, a handle and
+    the output, with the forward as a step."""
+
+    def __init__(self, wl, mode_name, layout_name, stream):
+        import torch
+        import x3_conv2d_epilogue_gb300 as ce
+        self.ce = ce
+        self.wl, self.stream = wl, stream
+        self.mode = ce.MODE_TF32 if mode_name == "tf32" else ce.MODE_FP32
+        self.nhwc = layout_name == "nhwc"
+        t = synth.make_inputs(wl, seed=0)
+        if self.nhwc:  # the same values, channels last
+            t.x = np.ascontiguousarray(t.x.transpose(0, 2, 3, 1))
+        self.host = {k: getattr(t, k) for k in ("x", "w", "b", "mult", "gamma", "beta", "scale")}
+        self.dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in self.host.items()}
+        self.epi = self.epilogue(self.dev)
+        self.h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, self.mode,
+                                    ce.LAYOUT_NHWC if self.nhwc else ce.LAYOUT_NCHW)
+        ce.conv_epi_reserve(self.h, self.epi)
+        self.shape = ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, self.epi, self.mode)
+        self.out = torch.empty(self.shape, device="cuda", dtype=torch.float32)
+
+    def epilogue(self, t):
+        wl = self.wl
+        chan = t["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else t["scale"]
+        return self.ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan, lrelu_slope=wl.lrelu_slope,
+                                groups=wl.groups, eps=wl.eps, gamma=t["gamma"], beta=t["beta"],
+                                pool_k=wl.pool_k, clamp_lo=wl.clamp_lo, clamp_hi=wl.clamp_hi)
+
+    def step(self):
+        self.ce.conv_epi_forward(self.h, self.dev["x"], self.dev["w"], self.dev["b"], self.epi, self.out, self.stream)
+
+    def sync(self):
+        self.ce.conv_epi_sync(self.h, self.stream)
+
+    def close(self):
+        if self.h:
+            self.ce.conv_epi_destroy(self.h)
+            self.h = None
+
+
+def time_steps(step, stream, steps, warmup, flush, world=1):
+    """W untimed warm-up steps, then K steps, each bracketed by CUDA events on
+    the launching stream, with the L2 flush between them (outside the events);
+    a barrier and a device synchronize on both sides.  Returns the per-step
+    times (ms)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush()
+            step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            step()
+            b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline_of(wl, ms, tf32_peak, hbm):
+    """Both roofline fractions of one forward; `bound` is the roofline with
+    the longer ideal time at the measured peaks."""
+    flops, nbytes = conv_flops(wl), algorithmic_bytes(wl)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    bound = "tensor" if flops / (tf32_peak * 1e12) >= nbytes / (hbm * 1e9) else "hbm"
+    return {"tflops": tflops, "tensor_frac": tflops / tf32_peak, "hbm_gbs": gbs, "hbm_frac": gbs / hbm,
+            "bound": bound, "flops": flops, "algorithmic_bytes": nbytes}
+
+
+def measure_unfused(wl, case, mode_name, steps, warmup, flush, stream, kern_ms):
+    """The unfused pipeline on the case's inputs (context only)."""
+    import torch
+    run = unfused_chain(wl, case.dev, mode_name == "tf32")
+    per = time_steps(run, stream, min(steps, 10), warmup, flush)
+    u_ms = float(np.mean(per))
+    torch.cuda.empty_cache()
+    return {"value": conv_flops(wl) / (u_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": u_ms,
+            "fused_speedup": u_ms / kern_ms,
+            "kind": "PyTorch conv2d (cuDNN, full conv output to HBM) + the chain as PyTorch ops; "
+                    "context only, not on the measured path"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c2_min_tanh2", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="c4_scale_min", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", choices=["tf32", "fp32"], default="tf32")
     ap.add_argument("--layout", choices=["nchw", "nhwc"], default="nchw",
                     help="memory layout of x handed to the library (nhwc: tf32 mode, channels last)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length for cpu_baseline")
+    ap.add_argument("--cfg-cpu-seconds", type=float, default=4.0, help="oracle sample length per per_config entry")
     ap.add_argument("--ref-seconds", type=float, default=15.0, help="oracle sample length per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--no-unfused", action="store_true", help="skip the unfused PyTorch/cuDNN comparison (context only)")
+    ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--no-flush", action="store_true", help="no L2 flush between steps (profiling runs only)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -304,98 +420,74 @@ def main(argv=None):
     import torch
     import x3_conv2d_epilogue_gb300 as ce
     torch.cuda.set_device(local)
-    mode = ce.MODE_TF32 if args.mode == "tf32" else ce.MODE_FP32
-
-    # inputs resident in HBM (same seeded recipe on every rank: weak scaling)
-    t = synth.make_inputs(wl, seed=0)
-    nhwc = args.layout == "nhwc"
-    layout = ce.LAYOUT_NHWC if nhwc else ce.LAYOUT_NCHW
-    if nhwc:  # the same values, channels last
-        t.x = np.ascontiguousarray(t.x.transpose(0, 2, 3, 1))
-    host = {k: getattr(t, k) for k in ("x", "w", "b", "mult", "gamma", "beta", "scale")}
-    dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in host.items()}
-    chan = dev["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else dev["scale"]
-    epi = ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan, lrelu_slope=wl.lrelu_slope, groups=wl.groups,
-                      eps=wl.eps, gamma=dev["gamma"], beta=dev["beta"], pool_k=wl.pool_k, clamp_lo=wl.clamp_lo,
-                      clamp_hi=wl.clamp_hi)
-    h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode, layout)
-    ce.conv_epi_reserve(h, epi)
-    shape = ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, epi, mode)
-    out = torch.empty(shape, device="cuda", dtype=torch.float32)
+    ce._lib()  # the CUDA library must load: there is no fallback
     stream = torch.cuda.Stream()
-    x_bytes = t.x.nbytes
+    flush = (lambda: None) if args.no_flush else L2Flush(torch, stream)
+    bf16, hbm, src = peaks()
+    tf32_peak = bf16 * TF32_PER_BF16
 
-    def step():
-        ce.conv_epi_forward(h, dev["x"], dev["w"], dev["b"], epi, out, stream)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    ce.conv_epi_sync(h, stream)
-    launches_per_step = ce.conv_epi_last_launch_count(h)
-
-    # ---- timed region: K steps, per-step CUDA events on the launching stream ----
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
+    # ---- the headline workload: K timed steps, per-step CUDA events ----
+    case = Case(wl, args.mode, args.layout, stream)
     with ClockSampler(local) as clk:
         time.sleep(0.3)  # let the sampler start
-        t_begin = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_begin.record(stream)
-        for i in range(args.steps):
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ce.conv_epi_sync(h, stream)
-    total_ms = t_begin.elapsed_time(t_end)
-    per = [a.elapsed_time(b) for a, b in evs]
-    total_ms = max_over_ranks(total_ms, world)
+        per = time_steps(case.step, stream, args.steps, args.warmup, flush, world)
+        launches_per_step = ce.conv_epi_last_launch_count(case.h)
+        case.sync()
+        total_ms = max_over_ranks(float(np.sum(per)), world)
+        kern_ms = float(np.mean(per))
+
+        # ---- every other workload, timed the same way in the same process ----
+        per_config = {}
+        if not args.no_per_config and not args.batch:
+            for name in sorted(synth.WORKLOADS):
+                if name == wl.name:
+                    continue
+                other = synth.WORKLOADS[name]
+                oc = Case(other, args.mode, args.layout, stream)
+                o_per = time_steps(oc.step, stream, args.steps, args.warmup, flush)
+                oc.sync()
+                o_ms = float(np.mean(o_per))
+                entry = {"workload": name, "chain": other.desc, "ms": o_ms, "ms_min": float(np.min(o_per)),
+                         **roofline_of(other, o_ms, tf32_peak, hbm)}
+                entry["launches_per_step"] = ce.conv_epi_last_launch_count(oc.h)
+                if not args.no_unfused and not oc.nhwc and rank == 0:
+                    entry["unfused"] = measure_unfused(other, oc, args.mode, args.steps, 3, flush, stream, o_ms)
+                oc.close()
+                per_config[name] = entry
+                del oc
+                torch.cuda.empty_cache()
     flops = conv_flops(wl)
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
-    kern_ms = float(np.mean(per))
 
     # ---- end to end through the host-buffer entry point ----
     e2e = None
     if not args.no_e2e:
+        host = case.host
         pin = {k: (None if v is None else torch.from_numpy(v).pin_memory()) for k, v in host.items()}
-        chan_h = pin["mult"] if wl.kind == synth.KIND_MUL_LRELU_GELU else pin["scale"]
-        epi_h = ce.epilogue(wl.kind, scalar=wl.scalar, chan_scale=chan_h, lrelu_slope=wl.lrelu_slope,
-                            groups=wl.groups, eps=wl.eps, gamma=pin["gamma"], beta=pin["beta"], pool_k=wl.pool_k,
-                            clamp_lo=wl.clamp_lo, clamp_hi=wl.clamp_hi)
-        out_h = torch.empty(shape, dtype=torch.float32).pin_memory()
-        ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)   # warm (allocates staging)
+        epi_h = case.epilogue(pin)
+        out_h = torch.empty(case.shape, dtype=torch.float32).pin_memory()
+        ce.conv_epi_forward_host(case.h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)   # warm (allocates staging)
         barrier(world)
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            ce.conv_epi_forward_host(h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)
+            ce.conv_epi_forward_host(case.h, pin["x"], pin["w"], pin["b"], epi_h, out_h, stream)
         e2e_s = max_over_ranks(time.perf_counter() - t0, world)
         h2d = sum(v.nbytes for v in host.values() if v is not None)
         e2e = {"value": flops * args.e2e_steps * world / e2e_s / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * 4}
 
-    ce.conv_epi_destroy(h)
-
     # ---- context: the unfused pipeline on the same inputs (not the product) ----
     unfused = None
-    if not args.no_unfused and not nhwc and rank == 0:
-        del out
+    if not args.no_unfused and not case.nhwc and rank == 0:
+        del case.out
         torch.cuda.empty_cache()
-        u_ms = time_unfused(wl, dev, args.mode == "tf32", min(args.steps, 10), 3, stream)
-        unfused = {"value": flops / (u_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": u_ms,
-                   "fused_speedup": u_ms / kern_ms,
-                   "kind": "PyTorch conv2d (cuDNN, full conv output to HBM) + the chain as PyTorch ops; "
-                           "context only, not on the measured path"}
+        unfused = measure_unfused(wl, case, args.mode, args.steps, 3, flush, stream, kern_ms)
+    case.close()
 
     if rank != 0:
         return 0
 
-    bf16, hbm, src = peaks()
-    tf32_peak = bf16 * TF32_PER_BF16
-    achieved = flops / (kern_ms * 1e-3) / 1e12
+    rl = roofline_of(wl, kern_ms, tf32_peak, hbm)
     cpu = None
     if not args.no_cpu_baseline:
         v, el, done, cores = oracle_sample(wl, args.cpu_seconds, wl.N)
@@ -404,21 +496,26 @@ def main(argv=None):
         if conv_flops(wl.with_batch(1)) <= SINGLE_CORE_MAX_FLOPS:  # one image on one core, where that is short
             v1, el1, _, _ = oracle_sample(wl, 0.0, 1, cores=1)
             cpu["single_core"] = {"value": v1, "unit": "TFLOP/s", "sample": f"1 image on 1 thread ({el1:.2f} s)"}
+        for name, entry in per_config.items():
+            other = synth.WORKLOADS[name]
+            ov, oel, odone, ocores = oracle_sample(other, args.cfg_cpu_seconds, other.N)
+            entry["oracle"] = {"value": ov, "unit": "TFLOP/s", "cores": ocores,
+                               "sample": f"{odone} of {other.N} images ({oel:.1f} s)"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.mode, "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": wl.name, "x": [wl.N, wl.Cin, wl.H, wl.W], "Cout": wl.Cout, "chain": wl.desc,
                    "mode": args.mode, "layout": args.layout,
-                   "l2": f"inputs larger than L2 ({x_bytes / 1e6:.0f} MB of x per step)",
+                   "l2": "no flush (profiling run)" if args.no_flush else flush.describe(),
                    "per_gpu_batch": wl.N},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tf32_peak,
-                     "traffic": traffic_for(kernel_hash(), wl.name + ("_nhwc" if nhwc else "")),
-                     "peak_source": f"{src} bf16 burst {bf16:.1f} x {TF32_PER_BF16:.4f}",
-                     "kernel": "conv_epi forward (prep + fused conv kernel)",
-                     "hbm_gbs": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm,
-                     "hbm_frac": algorithmic_bytes(wl) / (kern_ms * 1e-3) / 1e9 / hbm},
+        "roofline": {"bound": rl["bound"], "achieved": rl["tflops"], "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": rl["tensor_frac"],
+                     "traffic": traffic_for(kernel_hash(), wl.name + ("_nhwc" if args.layout == "nhwc" else "")),
+                     "peak_source": f"{src} bf16 burst {bf16:.1f} x {TF32_PER_BF16:.4f} (of {src})",
+                     "kernel": "conv_epi forward (filter pack + fused conv kernel)",
+                     "hbm_gbs": rl["hbm_gbs"], "hbm_peak_gbs": hbm, "hbm_frac": rl["hbm_frac"]},
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "unfused": unfused,
         "e2e": e2e,

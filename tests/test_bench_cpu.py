@@ -61,3 +61,24 @@ def test_single_core_oracle_sample():
     assert sorted(short) == ["c2_min_tanh2", "c5_gn_pool_clamp", "pr1_min_tanh2"]
     v, el, done, cores = bench.oracle_sample(W["pr1_min_tanh2"], 0.0, 1, cores=1)
     assert cores == 1 and done == 1 and v > 0 and el > 0
+
+
+def test_roofline_fractions_and_bound():
+    """Both fractions of one forward, and the bound is the roofline with the
+    longer ideal time at the given peaks."""
+    c3, c4 = W["c3_mul_lrelu_gelu"], W["c4_scale_min"]
+    r = bench.roofline_of(c4, 1.0, 1000.0, 8000.0)          # 1 ms
+    assert abs(r["tflops"] - bench.conv_flops(c4) / 1e9 / 1e3) < 1e-9
+    assert abs(r["tensor_frac"] - r["tflops"] / 1000.0) < 1e-12
+    assert abs(r["hbm_gbs"] - bench.algorithmic_bytes(c4) / 1e6) < 1e-9
+    assert r["bound"] == "tensor"                            # 558 flop/B, far above the ridge
+    # C3 does 143 flop per algorithmic byte: above a ridge of 1000/8 = 125, below 2000/8 = 250
+    assert bench.roofline_of(c3, 1.0, 1000.0, 8000.0)["bound"] == "tensor"
+    assert bench.roofline_of(c3, 1.0, 2000.0, 8000.0)["bound"] == "hbm"
+
+
+def test_headline_is_the_largest_workload():
+    """With no flags the bench times the workload with the most work."""
+    src = open(bench.__file__).read()
+    assert '"--workload", default="c4_scale_min"' in src
+    assert max(W, key=lambda n: bench.conv_flops(W[n])) == "c4_scale_min"
