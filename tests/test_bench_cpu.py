@@ -68,7 +68,7 @@ def test_roofline_fractions_and_bound():
     longer ideal time at the given peaks."""
     c3, c4 = W["c3_mul_lrelu_gelu"], W["c4_scale_min"]
     r = bench.roofline_of(c4, 1.0, 1000.0, 8000.0)          # 1 ms
-    assert abs(r["tflops"] - bench.conv_flops(c4) / 1e9 / 1e3) < 1e-9
+    assert abs(r["tflops"] - bench.conv_flops(c4) / 1e9) < 1e-9
     assert abs(r["tensor_frac"] - r["tflops"] / 1000.0) < 1e-12
     assert abs(r["hbm_gbs"] - bench.algorithmic_bytes(c4) / 1e6) < 1e-9
     assert r["bound"] == "tensor"                            # 558 flop/B, far above the ridge
