@@ -98,10 +98,14 @@ typedef enum {
     CONV_EPI_SCALE_MIN = 2,          /* out[n,0,i,j] = min_c scalar*y[n,c,i,j]               [N,1,Ho,Wo] */
     CONV_EPI_MUL_LRELU_GELU = 3,     /* t = y*chan_scale[c]; t = max(t,0)+slope*min(t,0);
                                         out = 0.5 t (1 + erf(t/sqrt 2))                     [N,Cout,Ho,Wo] */
-    CONV_EPI_GN_SCALE_POOL_CLAMP = 4 /* z = ((y-mean_ng)*rstd_ng*gamma[c] + beta[c]) * chan_scale[c],
+    CONV_EPI_GN_SCALE_POOL_CLAMP = 4, /* z = ((y-mean_ng)*rstd_ng*gamma[c] + beta[c]) * chan_scale[c],
                                         mean/biased var over (C/groups, Ho, Wo) of each (n, group),
                                         rstd = 1/sqrt(var+eps); out = clamp(maxpool_k(z), lo, hi)
                                         with stride k, floor mode                  [N,Cout,Hp,Wp] */
+    CONV_EPI_NONE = 5                /* out = y, the conv output itself (bias added), no chain:
+                                        on every page the reference model's first layer is this
+                                        nn.Conv2d, whose output the chain then consumes (p25, the
+                                        analysis of the reference model)            [N,Cout,Ho,Wo] */
 } conv_epi_kind;
 
 /* Post-conv chain.  Parameter tensors are device pointers of Cout floats
@@ -121,7 +125,7 @@ typedef struct {
                                  MIN kinds -> channel of the minimum (first on ties);
                                  GN kind   -> window offset a*k+b of the pooled value
                                               (first row-major on ties);
-                                 MUL_LRELU_GELU -> not produced (must be NULL).
+                                 MUL_LRELU_GELU, NONE -> not produced (must be NULL).
                                  Only CONV_EPI_MODE_FP32 produces indices. */
 } conv_epi_epilogue_desc;
 
@@ -133,6 +137,16 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
                                                    int64_t shape[4]);
 
 /* Create a handle for one problem size and mode on the current CUDA device.
+ * This is the construction step of the problem as every page states it: a
+ * module built once with the model's arguments (in_channels, out_channels,
+ * kernel_size 3 and the chain's constants; p85 and p54, the ModelNew module
+ * and its __init__), here the sizes of x and the filter and the arithmetic
+ * mode.  desc: read during the call only (the handle keeps a copy).
+ * *out: receives the new handle, or NULL when the call fails.
+ * Errors: INVALID_ARG (null pointer, sizes < 1, H or W < 3, unknown mode or
+ * layout), UNSUPPORTED (shape or device outside the chosen mode, a tensor of
+ * 2^31 or more elements, a device that is not sm_103a), CUDA / NO_MEMORY
+ * (workspace allocation). 
  * Validates the description and allocates the workspace every chain needs
  * except the GN chain's pooled buffers, which are allocated on the first GN
  * forward (conv_epi_reserve allocates them up front).  Synchronous.
@@ -163,10 +177,17 @@ CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi
 CONV_EPI_API conv_epi_status conv_epi_reserve(conv_epi_handle h, const conv_epi_epilogue_desc *epi);
 
 /* Run conv + chain on `stream` (a cudaStream_t; NULL = the legacy default
- * stream).  x, w, b, the chain's parameter tensors and out are device
- * pointers; out must hold conv_epi_output_shape() floats.  Asynchronous:
- * argument errors are returned at once, device-side errors (a barrier wait
- * that timed out) by conv_epi_sync(). */
+ * stream).  This is the module's forward(x) as the pages state it (p85 and
+ * p54, ModelNew.forward: the conv with the module's weight and bias, then
+ * the model's chain, returning the chain's output); the parameters the
+ * module would hold travel as arguments: w [Cout][Cin][3][3], b [Cout] and
+ * the chain's tensors in `epi`.  x, w, b, the chain's parameter tensors and
+ * out are device pointers owned by the caller, read (x, w, b, parameters) or
+ * written (out, index_out) by kernels on `stream` after the call returns;
+ * out must hold conv_epi_output_shape() floats.  Asynchronous: argument
+ * errors are returned at once (INVALID_ARG, ALIGNMENT, UNSUPPORTED), launch
+ * failures as CUDA, device-side errors (a barrier wait that timed out) by
+ * conv_epi_sync(). */
 CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x, const float *w,
                                               const float *b, const conv_epi_epilogue_desc *epi,
                                               float *out, void *stream);
@@ -197,8 +218,10 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
  * exits.  It allocates and frees nothing.
  *   desc: as for conv_epi_create; mode must be CONV_EPI_MODE_TF32.
  *   x, w, b, the chain's parameters, out: device pointers as for
- *   conv_epi_forward.  Chains MIN_TANH2, SCALE_MIN and MUL_LRELU_GELU only
+ *   conv_epi_forward.  Chains MIN_TANH2, SCALE_MIN, MUL_LRELU_GELU and NONE
  *   (the GroupNorm chain needs a larger workspace); index_out must be NULL.
+ * The description and the chain are checked exactly as conv_epi_create and
+ * conv_epi_forward check them, with the same statuses.
  * Returns CONV_EPI_ERR_UNSUPPORTED when the packed filter of the problem does
  * not fit the array (Cin rounded up to a multiple of 8, times 3*(2S+1)*Cout
  * floats, plus one 8-channel chunk, with S = 128/Cout), when an NCHW input's W
@@ -211,10 +234,20 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
  * it reads, so nothing needs to start at zero, but calls whose kernels
  * overlap on the GPU (unordered streams) race on it.  Asynchronous on
  * `stream` like conv_epi_forward; a device-side barrier timeout is recorded
- * in the array's error word and not reported by this call. */
+ * in an error word beside the array (one per device), which
+ * conv_epi_noalloc_sync reports and clears. */
 CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_desc *desc, const float *x, const float *w,
                                                       const float *b, const conv_epi_epilogue_desc *epi, float *out,
                                                       void *stream);
+
+/* Wait for `stream`, then report and clear the error word of the
+ * allocation-free forwards on the current device: CONV_EPI_ERR_TIMEOUT when
+ * one of their kernels gave up waiting on a pipeline barrier since the last
+ * call (its output is then undefined), else CONV_EPI_OK.  The word is shared
+ * by every allocation-free forward on the device.  Allocates nothing
+ * (the first call on a device looks up the word's address, as the first
+ * forward does).  Synchronous. */
+CONV_EPI_API conv_epi_status conv_epi_noalloc_sync(void *stream);
 
 /* The tensor-core kernel's plan for one problem and chain, as a forward on
  * a handle would launch it: tiling, ring stages, the shared-memory layout,
@@ -275,10 +308,16 @@ CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream);
  * conv_epi_sync() then reports CONV_EPI_ERR_TIMEOUT and the context stays
  * usable.  The output of that forward is undefined.  tile = -1 cancels; the
  * setting applies to one forward only.  Returns CONV_EPI_ERR_UNSUPPORTED on
- * an fp32-mode handle (whose kernels have no barrier rings). */
+ * an fp32-mode handle (whose kernels have no barrier rings).  With h = NULL
+ * the setting applies to the next conv_epi_forward_noalloc made by the
+ * calling thread instead (conv_epi_noalloc_sync then reports the timeout). */
 CONV_EPI_API conv_epi_status conv_epi_test_drop_tile(conv_epi_handle h, int tile);
 
-/* Release the handle and its workspace (synchronises the device first). */
+/* Release the handle and its workspace (synchronises the device first):
+ * the end of the module's life (p85 and p54, the ModelNew module, whose
+ * parameters and buffers go with it).  The handle must not be used after
+ * the call.  Returns INVALID_ARG for a null handle, CUDA when the
+ * synchronisation reports an error (the handle is released all the same). */
 CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h);
 
 /* Bytes of device workspace the handle holds now. */

@@ -118,6 +118,7 @@ KIND_MIN_TANH2 = 1
 KIND_SCALE_MIN = 2
 KIND_MUL_LRELU_GELU = 3
 KIND_GN_SCALE_POOL_CLAMP = 4
+KIND_NONE = 5  # the conv output itself, no chain
 
 
 @dataclass(frozen=True)

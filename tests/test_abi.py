@@ -3,12 +3,45 @@ entry point the header declares, and its host-side validation answers
 without touching a device."""
 import ctypes as C
 import os
+import re
 
 import numpy as np
 import pytest
 
 import x3_conv2d_epilogue_gb300 as ce
 from x3_conv2d_epilogue_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "conv_epi.h")
+
+
+def exported_symbols():
+    """Names the header declares as CONV_EPI_API entry points."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"CONV_EPI_API\s+[\w\s\*]*?\b(conv_epi_\w+)\s*\(", text)))
+
+
+def header_plan_fields():
+    """conv_epi_plan's int64_t fields in declaration order, read from the header."""
+    with open(HEADER) as f:
+        text = f.read()
+    body = re.search(r"typedef struct \{((?:(?!typedef).)*?)\} conv_epi_plan;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    assert re.findall(r"(\w+)\s+[^;]+;", body) == ["int64_t"] * len(re.findall(r"[^;]+;", body))
+    fields = []
+    for decl in re.findall(r"int64_t\s+([^;]+);", body):
+        for name in decl.split(","):
+            m = re.fullmatch(r"\s*(\w+)\s*(?:\[(\d+)\])?\s*", name)
+            fields.append((m.group(1), int(m.group(2)) if m.group(2) else 1))
+    return fields
+
+
+def test_binding_plan_matches_the_header():
+    """The binding declares conv_epi_plan statically; its fields are the
+    header's, in the same order and with the same array lengths."""
+    got = [(n, getattr(t, "_length_", 1)) for n, t in ce.Plan._fields_]
+    assert got == header_plan_fields()
+    assert C.sizeof(ce.Plan) == 8 * sum(k for _, k in got)
 
 
 @pytest.fixture(scope="module")
@@ -19,14 +52,14 @@ def lib():
 
 
 def test_header_declares_the_api():
-    names = ce.exported_symbols()
+    names = exported_symbols()
     for must in ("conv_epi_create", "conv_epi_forward", "conv_epi_destroy", "conv_epi_forward_host",
                  "conv_epi_output_shape", "conv_epi_status_string", "conv_epi_sync"):
         assert must in names
 
 
 def test_library_exports_every_declared_symbol(lib):
-    for name in ce.exported_symbols():
+    for name in exported_symbols():
         assert hasattr(lib, name), name
 
 
@@ -36,7 +69,7 @@ def test_library_exports_nothing_else(lib):
     if out.returncode:
         pytest.skip("nm not available")
     names = {ln.split()[-1] for ln in out.stdout.splitlines() if ln.strip()}
-    assert names == set(ce.exported_symbols())
+    assert names == set(exported_symbols())
 
 
 def test_status_strings(lib):
@@ -115,7 +148,10 @@ def test_null_pointers_rejected(lib):
     assert L.conv_epi_sync(None, None) == 1
     assert L.conv_epi_workspace_bytes(None) == 0
     assert L.conv_epi_output_shape(None, None, None) == 1
-    assert L.conv_epi_test_drop_tile(None, 0) == 1
+    assert L.conv_epi_test_drop_tile(None, -2) == 1
+    # a null handle arms the hook for the calling thread's next allocation-free forward
+    assert L.conv_epi_test_drop_tile(None, 0) == 0
+    assert L.conv_epi_test_drop_tile(None, -1) == 0
     assert L.conv_epi_reserve(None, None) == 1
     assert L.conv_epi_forward_noalloc(None, None, None, None, None, None, None) == 1
 
@@ -129,6 +165,21 @@ def test_create_without_device_fails_cleanly(lib):
     st = lib.conv_epi_create(C.byref(d), C.byref(h))
     assert st in (2, 4) and not h.value
     assert isinstance(ce.conv_epi_status_string(st), str)
+    assert lib.conv_epi_noalloc_sync(None) == 4          # no device: a CUDA error, not a crash
+
+
+def test_plain_conv_output_chain(lib):
+    """CONV_EPI_NONE: the conv output itself, [N, Cout, Ho, Wo], no index
+    output, in both modes."""
+    e = ce.epilogue(ce.NONE)
+    assert shape(2, 16, 32, 32, 64, e) == (2, 64, 30, 30)
+    assert shape(3, 5, 9, 11, 200, e, ce.MODE_FP32) == (3, 200, 7, 9)
+    with pytest.raises(ce.ConvEpiError) as ei:
+        shape(1, 4, 8, 8, 8, ce.epilogue(ce.NONE, index_out=64))
+    assert ei.value.status == 1
+    q = ce.conv_epi_plan_query(64, 64, 256, 256, 64, e)     # planned like the per-channel chain
+    r = ce.conv_epi_plan_query(64, 64, 256, 256, 64, ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=16))
+    assert q == r
 
 
 def test_output_shapes_of_wide_and_many_channel_problems(lib):
@@ -216,7 +267,7 @@ def test_empty_batch(lib):
 def test_binding_has_every_entry_point():
     """The binding offers a function of the same name for every call the
     header declares."""
-    assert [n for n in ce.exported_symbols() if not callable(getattr(ce, n, None))] == []
+    assert [n for n in exported_symbols() if not callable(getattr(ce, n, None))] == []
     assert isinstance(ce.conv_epi_last_cuda_error(), str)
 
 
@@ -250,7 +301,7 @@ def test_plain_c_program_uses_the_abi(lib, tmp_path):
     src.write_text(C_PROGRAM)
     exe = tmp_path / "abi"
     pkg = os.path.dirname(ce.LIB_PATH)
-    inc = os.path.dirname(ce.HEADER)
+    inc = os.path.dirname(HEADER)
     r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src), "-L", pkg,
                         "-lconv_epi", f"-Wl,-rpath,{pkg}", "-o", str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr

@@ -5,6 +5,10 @@ checks sampled outputs one by one (min chains: whole channel columns;
 per-channel chain: single elements; GroupNorm chain: every pooled output of
 a few whole (image, group) pairs, statistics included), and properties that
 hold at every output (finite; tanh∘tanh inside (-tanh 1, tanh 1); clamp range).
+In fp32 mode the reductions' indices are checked too (channel of the
+minimum, window offset of the pooled value): at the sampled points, and over
+the whole first and last images element by element, exact wherever the
+oracle's best and second-best candidates differ by more than 1e-5.
 """
 import math
 
@@ -13,7 +17,8 @@ import pytest
 
 import oracle
 import synth
-from parity_util import (FP32_ATOL, TF32_ATOL, TF32_RTOL, epilogue_for, torch_inputs)
+from parity_util import (FP32_ATOL, TF32_ATOL, TF32_RTOL, check_fp32, check_index, epilogue_for, min_index_gap,
+                         pool_index_gap, torch_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -28,20 +33,23 @@ def full(request):
     return wl, t, torch_inputs(t)
 
 
-def run(wl, d, mode, layout=0):
+def run(wl, d, mode, layout=0, want_index=False):
+    """One forward over the whole batch; (out, index or None) as torch tensors."""
     import torch
     import x3_conv2d_epilogue_gb300 as ce
-    epi = epilogue_for(wl, d)
+    probe = epilogue_for(wl, d)
+    shape = ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, probe, mode)
+    idx = torch.full(shape, -7, device="cuda", dtype=torch.int32) if want_index else None
+    epi = epilogue_for(wl, d, idx)
     x = d["x"].permute(0, 2, 3, 1).contiguous() if layout == ce.LAYOUT_NHWC else d["x"]
     h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, mode, layout)
     try:
-        out = torch.full(ce.conv_epi_output_shape(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, epi, mode), float("nan"),
-                         device="cuda", dtype=torch.float32)
+        out = torch.full(shape, float("nan"), device="cuda", dtype=torch.float32)
         ce.conv_epi_forward(h, x, d["w"], d["b"], epi, out)
         ce.conv_epi_sync(h)
     finally:
         ce.conv_epi_destroy(h)
-    return out
+    return out, idx
 
 
 def close(got, ref, mode):
@@ -57,7 +65,7 @@ def test_full_size(full, mode):
     import x3_conv2d_epilogue_gb300 as ce
     wl, t, d = full
     m = ce.MODE_FP32 if mode == "fp32" else ce.MODE_TF32
-    out = run(wl, d, m, ce.LAYOUT_NHWC if mode == "tf32_nhwc" else ce.LAYOUT_NCHW)
+    out, _ = run(wl, d, m, ce.LAYOUT_NHWC if mode == "tf32_nhwc" else ce.LAYOUT_NCHW)
     mode = "fp32" if mode == "fp32" else "tf32"  # the tolerance
     assert bool(torch.isfinite(out).all()), "non-finite outputs"
     rng = np.random.default_rng(1234)
@@ -91,3 +99,45 @@ def test_full_size(full, mode):
         ref, got = np.concatenate(refs), np.concatenate(gots)
     ok, err = close(got, ref, mode)
     assert ok.all(), f"{wl.name} {mode}: {int((~ok).sum())} of {ok.size} sampled outputs off; max err {err.max():.3g}"
+
+
+def gap_at_points(t, wl, n, i, j):
+    """Best-vs-second gap of scalar * y over the channels at sampled points."""
+    y = np.array([[oracle.conv_at(t.x, t.w, t.b, int(a), co, int(p), int(q)) for co in range(wl.Cout)]
+                  for a, p, q in zip(n, i, j)])
+    v = np.sort(wl.scalar * y, axis=1)
+    return v[:, 1] - v[:, 0]
+
+
+@pytest.mark.parametrize("wl_name", ["c2_min_tanh2", "c4_scale_min", "c5_gn_pool_clamp"])
+def test_full_size_fp32_indices(wl_name):
+    """fp32 mode at full size with the index output: values and indices of
+    the first and last whole images against the oracle's forward on those
+    images, plus (min chains) 256 sampled points across the batch."""
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = synth.WORKLOADS[wl_name]
+    t = synth.make_inputs(wl, seed=0)
+    d = torch_inputs(t)
+    out, idx = run(wl, d, ce.MODE_FP32, want_index=True)
+    ties = 0
+    for img in (0, wl.N - 1):
+        one = wl.with_batch(1)
+        ti = synth.Tensors(t.x[img:img + 1], t.w, t.b, t.mult, t.gamma, t.beta, t.scale)
+        ref, ref_idx = oracle.forward(ti.x, ti.w, ti.b, oracle.chain_for(one, ti))
+        got, got_idx = out[img:img + 1].cpu().numpy(), idx[img:img + 1].cpu().numpy()
+        check_fp32(got, ref, f"{wl_name} image {img}")
+        y = oracle.conv3x3(ti.x, ti.w, ti.b)
+        if wl.kind == synth.KIND_GN_SCALE_POOL_CLAMP:
+            slope = t.gamma.astype(np.float64) * t.scale
+            gap = pool_index_gap(y, wl.pool_k, np.where(slope >= 0, 1.0, -1.0)[None, :]) * np.abs(slope)[None, :, None, None]
+        else:
+            gap = min_index_gap(y, wl.scalar)
+        ties += check_index(got_idx, ref_idx, gap, f"{wl_name} image {img}")
+    if wl.kind != synth.KIND_GN_SCALE_POOL_CLAMP:
+        rng = np.random.default_rng(99)
+        Ho, Wo = wl.H - 2, wl.W - 2
+        n, i, j = rng.integers(0, wl.N, NS), rng.integers(0, Ho, NS), rng.integers(0, Wo, NS)
+        _, ref_idx = oracle.min_at(t.x, t.w, t.b, n, i, j, scalar=wl.scalar, tanh2=wl.kind == synth.KIND_MIN_TANH2)
+        got_idx = idx.cpu().numpy()[n, 0, i, j]
+        ties += check_index(got_idx, ref_idx, gap_at_points(t, wl, n, i, j), f"{wl_name} sampled")
+    assert ties <= 16, f"{ties} near-tie index differences"

@@ -123,8 +123,11 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
     # per-channel transpose tiles, the GroupNorm pooled tiles of each band
     if kind in MIN_KINDS:
         assert q["scratch_bytes"] >= U * 4 * P * 4
-    elif kind == ce.MUL_LRELU_GELU:
-        assert q["scratch_bytes"] >= 8 * 32 * 18 * 4
+    elif kind in (ce.MUL_LRELU_GELU, ce.NONE):
+        # a 32 x 16 staging tile per epilogue warp, read and written at
+        # r * 16 + 4 * ((c / 4) ^ ((r / 2) & 3)) + c % 4 (r < 32, c < 16)
+        top = max(r * 16 + 4 * ((c // 4) ^ ((r // 2) & 3)) + c % 4 for r in range(32) for c in range(16))
+        assert top == 32 * 16 - 1 and q["scratch_bytes"] >= 8 * 32 * 16 * 4
     else:
         bands = U // 2
         assert U in (2, 4) and P <= 128 and S == 2
@@ -132,10 +135,12 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
 
 
 def parity_shapes():
+    import test_conv_only_gpu as tn
     import test_parity_gpu as tp
     import test_zz_guard_gpu as tg
     shapes = dict(tp.SMALL)
     shapes.update(tp.FP32_ONLY)
+    shapes.update({"none_" + k: v for k, v in tn.CASES.items()})
     shapes.update({"guard_" + k: v for k, v in tg.CASES.items()})
     for name, wl in synth.WORKLOADS.items():
         shapes["full_" + name] = wl
@@ -170,7 +175,7 @@ def test_random_shapes_all_planned_and_in_range():
     planned exactly when Cout = 64, pool_k = 4 and W <= 128."""
     rng = random.Random(20261203)
     for _ in range(3000):
-        kind = rng.choice([ce.MIN_TANH2, ce.SCALE_MIN, ce.MUL_LRELU_GELU, ce.GN_SCALE_POOL_CLAMP])
+        kind = rng.choice([ce.MIN_TANH2, ce.SCALE_MIN, ce.MUL_LRELU_GELU, ce.GN_SCALE_POOL_CLAMP, ce.NONE])
         layout = rng.choice([ce.LAYOUT_NCHW, ce.LAYOUT_NHWC])
         N = rng.randint(1, 4)
         W = rng.choice([rng.randint(3, 40), rng.randint(41, 300), rng.randint(301, 1100)])

@@ -9,6 +9,7 @@ end of the suite, after the parity tests."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from parity_util import check_fp32, check_tf32, epilogue_for, oracle_run, torch_inputs
 
@@ -28,6 +29,13 @@ CASES = {
     # channel slots per pass so the filter taps fit shared memory
     "c4_co512_w8": W["c4_scale_min"].resized(N=2, H=6, W=8, Cout=512),
     "c3_co640_w10": W["c3_mul_lrelu_gelu"].resized(N=1, Cin=24, H=5, W=10, Cout=640),
+    # the plain conv output: 16-byte row stores where rows start aligned
+    # (ragged last float4 of 254- and 62-wide rows), 8-byte or single-float
+    # stores elsewhere
+    "none_w256": W["c3_mul_lrelu_gelu"].resized(N=1, H=6, kind=synth.KIND_NONE),
+    "none_w64": W["c3_mul_lrelu_gelu"].resized(N=2, H=7, W=64, Cout=40, kind=synth.KIND_NONE),
+    "none_w67": W["c3_mul_lrelu_gelu"].resized(N=1, H=6, W=67, kind=synth.KIND_NONE),
+    "none_w520_co200": W["c3_mul_lrelu_gelu"].resized(N=1, H=4, W=520, Cout=200, kind=synth.KIND_NONE),
 }
 GUARD = 64          # elements on each side (256 bytes: the output stays 16-byte aligned)
 SENTINEL = -1234.5
@@ -60,7 +68,7 @@ def test_writes_stay_inside_the_output(case, mode):
     n = int(np.prod(shape))
     obuf, out = guarded(shape, torch.float32, SENTINEL)
     ibuf, idx = (None, None)
-    if m == ce.MODE_FP32 and wl.kind != synth.KIND_MUL_LRELU_GELU:
+    if m == ce.MODE_FP32 and wl.kind not in (synth.KIND_MUL_LRELU_GELU, synth.KIND_NONE):
         ibuf, idx = guarded(shape, torch.int32, ISENTINEL)
     epi = epilogue_for(wl, d, idx)
     h = ce.conv_epi_create(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, m)
@@ -73,7 +81,7 @@ def test_writes_stay_inside_the_output(case, mode):
     assert guards_intact(obuf, n, SENTINEL), f"{case} {mode}: a write landed outside the output"
     if ibuf is not None:
         assert guards_intact(ibuf, n, ISENTINEL), f"{case} {mode}: a write landed outside the index output"
-    ref = oracle_run(wl, t)[0]
+    ref = oracle.conv3x3(t.x, t.w, t.b) if wl.kind == synth.KIND_NONE else oracle_run(wl, t)[0]
     got = out.cpu().numpy()
     if m == ce.MODE_FP32:
         check_fp32(got, ref, case)
@@ -91,7 +99,8 @@ def test_empty_batch_is_a_no_op(mode):
     p = torch.ones(64, device="cuda")
     chains = [ce.epilogue(ce.MIN_TANH2), ce.epilogue(ce.SCALE_MIN, scalar=-2.0),
               ce.epilogue(ce.MUL_LRELU_GELU, chan_scale=p),
-              ce.epilogue(ce.GN_SCALE_POOL_CLAMP, chan_scale=p, gamma=p, beta=p, groups=16, pool_k=4)]
+              ce.epilogue(ce.GN_SCALE_POOL_CLAMP, chan_scale=p, gamma=p, beta=p, groups=16, pool_k=4),
+              ce.epilogue(ce.NONE)]
     x = torch.empty(0, 8, 18, 16, device="cuda")
     w = torch.zeros(64, 8, 3, 3, device="cuda")
     h = ce.conv_epi_create(0, 8, 18, 16, 64, m)

@@ -14,16 +14,14 @@ from __future__ import annotations
 
 import ctypes as C
 import os
-import re
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libconv_epi.so")
-HEADER = os.path.join(os.path.dirname(HERE), "include", "conv_epi.h")
 
 MODE_TF32, MODE_FP32 = 0, 1
 LAYOUT_NCHW, LAYOUT_NHWC = 0, 1
-MIN_TANH2, SCALE_MIN, MUL_LRELU_GELU, GN_SCALE_POOL_CLAMP = 1, 2, 3, 4
+MIN_TANH2, SCALE_MIN, MUL_LRELU_GELU, GN_SCALE_POOL_CLAMP, NONE = 1, 2, 3, 4, 5
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CUDA", 5: "TIMEOUT",
           6: "NO_MEMORY", 7: "DEVICE"}
 
@@ -60,26 +58,20 @@ class EpilogueDesc(C.Structure):
     ]
 
 
-def _plan_fields():
-    """conv_epi_plan's fields in declaration order, read from the header (every
-    field is an int64_t; `box[4]` is an array).  Without the header the
-    structure stays empty and conv_epi_plan_query refuses to run."""
-    if not os.path.exists(HEADER):
-        return []
-    with open(HEADER) as f:
-        text = f.read()
-    body = re.search(r"typedef struct \{((?:(?!typedef).)*?)\} conv_epi_plan;", text, re.S).group(1)
-    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
-    fields = []
-    for decl in re.findall(r"int64_t\s+([^;]+);", body):
-        for name in decl.split(","):
-            m = re.fullmatch(r"\s*(\w+)\s*(?:\[(\d+)\])?\s*", name)
-            fields.append((m.group(1), C.c_int64 * int(m.group(2)) if m.group(2) else C.c_int64))
-    return fields
+# conv_epi_plan (include/conv_epi.h), every field an int64_t, in declaration
+# order; the library reports its own sizeof in struct_bytes, which
+# conv_epi_plan_query checks against this layout
+_PLAN_FIELDS = (
+    "struct_bytes", "gemm_cout", "S", "P", "U", "RU", "Rin", "PL", "ucol", "chunks", "CT", "CW", "BW", "MT",
+    "units_per_image", "resident", "na", "nb", "nr", "a_bytes", "b_bytes", "raw_bytes", "scratch_bytes",
+    "a_off", "b_off", "raw_off", "bar_off", "scratch_off", "bar_bytes", "smem", "smem_limit",
+    "a_plane_bytes", "a_lbo", "a_kw_stride", "x_pitch", "box[4]", "acc_cols", "tmem_cols", "conv_items",
+    "wpack_bytes", "xpad_bytes",
+)
 
 
 class Plan(C.Structure):
-    _fields_ = _plan_fields()
+    _fields_ = [(f[:-3], C.c_int64 * 4) if f.endswith("[4]") else (f, C.c_int64) for f in _PLAN_FIELDS]
 
 
 _lock = threading.Lock()
@@ -105,6 +97,7 @@ def _lib():
             L.conv_epi_forward_host.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_forward_noalloc.argtypes = [C.POINTER(Desc), P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_sync.argtypes = [P, P]
+            L.conv_epi_noalloc_sync.argtypes = [P]
             L.conv_epi_test_drop_tile.argtypes = [P, I]
             L.conv_epi_plan_query.argtypes = [C.POINTER(Desc), C.POINTER(EpilogueDesc), C.POINTER(Plan)]
             L.conv_epi_destroy.argtypes = [P]
@@ -114,13 +107,6 @@ def _lib():
             L.conv_epi_version.restype = I
             _L = L
     return _L
-
-
-def exported_symbols():
-    """Names the header declares as CONV_EPI_API entry points."""
-    with open(HEADER) as f:
-        text = f.read()
-    return sorted(set(re.findall(r"CONV_EPI_API\s+[\w\s\*]*?\b(conv_epi_\w+)\s*\(", text)))
 
 
 def _arg(t, what, device=None, index=False):
@@ -244,9 +230,18 @@ def conv_epi_sync(h, stream=None):
     _check(_lib().conv_epi_sync(h, _stream(stream)), "conv_epi_sync")
 
 
+def conv_epi_noalloc_sync(stream=None):
+    """Wait for ``stream`` and raise if an allocation-free forward on the
+    current device timed out since the last call (the error word is then
+    cleared)."""
+    _check(_lib().conv_epi_noalloc_sync(_stream(stream)), "conv_epi_noalloc_sync")
+
+
 def conv_epi_test_drop_tile(h, tile):
     """Test hook: the next tf32 forward on ``h`` skips staged tile ``tile`` of
-    every CTA's sequence, so its bounded waits time out (-1 cancels)."""
+    every CTA's sequence, so its bounded waits time out (-1 cancels).  With
+    ``h`` None it applies to the calling thread's next allocation-free
+    forward."""
     _check(_lib().conv_epi_test_drop_tile(h, tile), "conv_epi_test_drop_tile")
 
 

@@ -14,7 +14,21 @@ namespace {
 
 thread_local char g_cuda_err[512] = "no CUDA error recorded";
 
+// conv_epi_test_drop_tile(NULL, k): the tile the next allocation-free
+// forward on this thread skips (-1: none)
+thread_local int g_noalloc_drop_tile = -1;
+
+}  // namespace
+
+namespace conv_epi {
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int take_noalloc_drop_tile() {
+    const int t = g_noalloc_drop_tile;
+    g_noalloc_drop_tile = -1;
+    return t;
+}
 
 conv_epi_status check_desc(const conv_epi_desc *d) {
     if (!d) return CONV_EPI_ERR_INVALID_ARG;
@@ -42,6 +56,9 @@ conv_epi_status check_epi(const conv_epi_desc &d, const conv_epi_epilogue_desc *
         if (!e->chan_scale || !isfinite(e->lrelu_slope)) return CONV_EPI_ERR_INVALID_ARG;
         if (e->index_out) return CONV_EPI_ERR_INVALID_ARG;  // this chain has no index output
         return CONV_EPI_OK;
+    case CONV_EPI_NONE:
+        if (e->index_out) return CONV_EPI_ERR_INVALID_ARG;  // no reduction, no index output
+        return CONV_EPI_OK;
     case CONV_EPI_GN_SCALE_POOL_CLAMP:
         if (!e->chan_scale || !e->gamma || !e->beta) return CONV_EPI_ERR_INVALID_ARG;
         if (e->groups < 1 || d.Cout % e->groups != 0) return CONV_EPI_ERR_INVALID_ARG;
@@ -54,6 +71,14 @@ conv_epi_status check_epi(const conv_epi_desc &d, const conv_epi_epilogue_desc *
     }
 }
 
+}  // namespace conv_epi
+
+namespace {
+
+using conv_epi::aligned16;
+using conv_epi::check_desc;
+using conv_epi::check_epi;
+
 int pool_out(int n, int k) { return (n - k) / k + 1; }
 
 void shape_of(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, int64_t s[4]) {
@@ -61,7 +86,7 @@ void shape_of(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, int64_t s
     s[0] = d.N;
     if (e.kind == CONV_EPI_MIN_TANH2 || e.kind == CONV_EPI_SCALE_MIN) {
         s[1] = 1, s[2] = Ho, s[3] = Wo;
-    } else if (e.kind == CONV_EPI_MUL_LRELU_GELU) {
+    } else if (e.kind == CONV_EPI_MUL_LRELU_GELU || e.kind == CONV_EPI_NONE) {
         s[1] = d.Cout, s[2] = Ho, s[3] = Wo;
     } else {
         s[1] = d.Cout, s[2] = pool_out(Ho, e.pool_k), s[3] = pool_out(Wo, e.pool_k);
@@ -381,7 +406,11 @@ CONV_EPI_API conv_epi_status conv_epi_plan_query(const conv_epi_desc *desc, cons
 }
 
 CONV_EPI_API conv_epi_status conv_epi_test_drop_tile(conv_epi_handle h, int tile) {
-    if (!h || tile < -1) return CONV_EPI_ERR_INVALID_ARG;
+    if (tile < -1) return CONV_EPI_ERR_INVALID_ARG;
+    if (!h) {  // the next allocation-free forward on this thread
+        g_noalloc_drop_tile = tile;
+        return CONV_EPI_OK;
+    }
     if (h->d.mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;
     h->test_drop_tile = tile;
     return CONV_EPI_OK;

@@ -84,6 +84,16 @@ struct conv_epi_handle_s {
 
 namespace conv_epi {
 
+// Argument checks shared by every entry point (api.cu), so that they refuse
+// the same inputs with the same status: the problem description, and the
+// chain description against it (not its pointers' alignment).
+bool aligned16(const void *p);
+conv_epi_status check_desc(const conv_epi_desc *d);
+conv_epi_status check_epi(const conv_epi_desc &d, const conv_epi_epilogue_desc *e);
+// the tile conv_epi_test_drop_tile(NULL, tile) armed for the next
+// allocation-free forward on the calling thread (-1: none); reading disarms it
+int take_noalloc_drop_tile();
+
 // records a failing CUDA call for conv_epi_last_cuda_error()
 conv_epi_status cuda_fail(cudaError_t e, const char *what);
 #define CE_CUDA(call)                                             \

@@ -32,7 +32,8 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB
 constexpr int kMaxDevices = 64;
 
-// the scratch itself, and the error word its kernels report into
+// the scratch itself, and the error word its kernels report into (read and
+// cleared by conv_epi_noalloc_sync)
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 static __device__ __align__(256) unsigned g_noalloc_err[64];
 
@@ -69,48 +70,32 @@ conv_epi_status setup_device(int dev, DeviceSlot *&out) {
     return CONV_EPI_OK;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_desc *desc, const float *x,
                                                                  const float *w, const float *b,
                                                                  const conv_epi_epilogue_desc *epi, float *out,
                                                                  void *stream) {
-    if (!desc || !epi) return CONV_EPI_ERR_INVALID_ARG;
+    // the same description and chain checks, with the same statuses, as
+    // conv_epi_create and conv_epi_forward
+    conv_epi_status st = conv_epi::check_desc(desc);
+    if (st) return st;
     const conv_epi_desc &d = *desc;
+    if ((st = conv_epi::check_epi(d, epi))) return st;
     if (d.N > 0 && (!x || !w || !b || !out)) return CONV_EPI_ERR_INVALID_ARG;  // an empty batch may pass nulls
-    if (d.N < 0 || d.Cin < 1 || d.Cout < 1 || d.H < 3 || d.W < 3) return CONV_EPI_ERR_INVALID_ARG;
-    if (d.layout != CONV_EPI_LAYOUT_NCHW && d.layout != CONV_EPI_LAYOUT_NHWC) return CONV_EPI_ERR_INVALID_ARG;
+    // what this entry point adds: tensor-core mode only, and nothing that
+    // would need a workspace beyond the static array
     if (d.mode != CONV_EPI_MODE_TF32) return CONV_EPI_ERR_UNSUPPORTED;
     if (d.layout == CONV_EPI_LAYOUT_NHWC && d.Cin % 4 != 0) return CONV_EPI_ERR_UNSUPPORTED;
     // NCHW rows that are not whole 16-byte units need a padded copy of x
     if (d.layout == CONV_EPI_LAYOUT_NCHW && d.W % 4 != 0) return CONV_EPI_ERR_UNSUPPORTED;
-    if ((int64_t)d.N * d.Cin * d.H * d.W >= (1ll << 31) || (int64_t)d.N * d.Cout * (d.H - 2) * (d.W - 2) >= (1ll << 31))
-        return CONV_EPI_ERR_UNSUPPORTED;
-    switch (epi->kind) {
-    case CONV_EPI_MIN_TANH2:
-    case CONV_EPI_SCALE_MIN:
-        if (!isfinite(epi->scalar)) return CONV_EPI_ERR_INVALID_ARG;
-        break;
-    case CONV_EPI_MUL_LRELU_GELU:
-        if (!epi->chan_scale || !isfinite(epi->lrelu_slope)) return CONV_EPI_ERR_INVALID_ARG;
-        break;
-    case CONV_EPI_GN_SCALE_POOL_CLAMP:
-        return CONV_EPI_ERR_UNSUPPORTED;  // needs the pooled workspace as well
-    default:
-        return CONV_EPI_ERR_INVALID_ARG;
-    }
+    if (epi->kind == CONV_EPI_GN_SCALE_POOL_CLAMP) return CONV_EPI_ERR_UNSUPPORTED;  // needs the pooled workspace
     if (epi->index_out) return CONV_EPI_ERR_UNSUPPORTED;  // indices come from the fp32 mode only
-    if (d.N == 0) {  // an empty batch: the same refusals, then nothing to compute
-        const conv_epi_status st0 = conv_epi::tc_supported(d, epi);
-        if (st0) return st0;
-        return conv_epi::tc_wpack_bytes(d) > kNoAllocScratchBytes ? CONV_EPI_ERR_UNSUPPORTED : CONV_EPI_OK;
-    }
-    if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(out)) return CONV_EPI_ERR_ALIGNMENT;
-    conv_epi_status st = conv_epi::tc_supported(d, epi);
-    if (st) return st;
+    if ((st = conv_epi::tc_supported(d, epi))) return st;
     if (conv_epi::tc_wpack_bytes(d) > kNoAllocScratchBytes) return CONV_EPI_ERR_UNSUPPORTED;  // scratch too small
+    if (d.N == 0) return CONV_EPI_OK;  // an empty batch: the same refusals, then nothing to compute
+    if (!conv_epi::aligned16(x) || !conv_epi::aligned16(w) || !conv_epi::aligned16(b) || !conv_epi::aligned16(out))
+        return CONV_EPI_ERR_ALIGNMENT;
 
     int dev = 0;
     CE_CUDA(cudaGetDevice(&dev));
@@ -128,5 +113,22 @@ extern "C" CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_
     h.dev_err = sl->err;
     h.wpack = static_cast<float *>(sl->scratch);
     h.wpack_bytes = kNoAllocScratchBytes;
+    h.test_drop_tile = conv_epi::take_noalloc_drop_tile();
     return conv_epi::tc_forward(&h, x, w, b, *epi, out, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" CONV_EPI_API conv_epi_status conv_epi_noalloc_sync(void *stream) {
+    int dev = 0;
+    CE_CUDA(cudaGetDevice(&dev));
+    CE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    DeviceSlot *sl = nullptr;
+    conv_epi_status st = setup_device(dev, sl);
+    if (st) return st;
+    unsigned word = 0;
+    CE_CUDA(cudaMemcpy(&word, sl->err, sizeof word, cudaMemcpyDeviceToHost));
+    if (word) {
+        CE_CUDA(cudaMemset(sl->err, 0, sizeof word));
+        return (word & conv_epi::ERRBIT_TIMEOUT) ? CONV_EPI_ERR_TIMEOUT : CONV_EPI_ERR_DEVICE;
+    }
+    return CONV_EPI_OK;
 }

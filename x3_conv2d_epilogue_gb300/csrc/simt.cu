@@ -1,7 +1,8 @@
 // simt.cu -- fp32 CUDA-core path (CONV_EPI_MODE_FP32, the strict-tolerance
 // mode): a direct 3x3 convolution with the post-conv chain fused into the
 // same kernel, so the full conv output is written only by the per-channel
-// chain (MUL_LRELU_GELU), whose output is the full tensor anyway.
+// chain (MUL_LRELU_GELU) and by CONV_EPI_NONE, whose outputs are the full
+// tensor anyway.
 //
 // Prior art: the p54 page (POPCORNBENCH Kimi-K2.6, level-2 problem 54), in
 // its fused direct-conv design, stages a haloed input tile and a few output
@@ -208,19 +209,24 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                             if (bidx[p] < 0 || better) best[p] = v, bidx[p] = co0 + c;
                         }
                     }
-                } else if (KIND == CONV_EPI_MUL_LRELU_GELU) {
+                } else if (KIND == CONV_EPI_MUL_LRELU_GELU || KIND == CONV_EPI_NONE) {
                     if (wbase < a.Wo) {
 #pragma unroll
                         for (int c = 0; c < kCO; ++c) {
                             const int co = co0 + c;
                             if (co >= a.Cout) break;
-                            const float m = __ldg(&a.chan_scale[co]);
                             float o[kPX];
+                            if (KIND == CONV_EPI_NONE) {  // the conv output itself
 #pragma unroll
-                            for (int p = 0; p < kPX; ++p) {
-                                float v = acc[c][p] * m;
-                                v = v > 0.0f ? v : a.slope * v;
-                                o[p] = gelu_erf(v);
+                                for (int p = 0; p < kPX; ++p) o[p] = acc[c][p];
+                            } else {
+                                const float m = __ldg(&a.chan_scale[co]);
+#pragma unroll
+                                for (int p = 0; p < kPX; ++p) {
+                                    float v = acc[c][p] * m;
+                                    v = v > 0.0f ? v : a.slope * v;
+                                    o[p] = gelu_erf(v);
+                                }
                             }
                             float *dst = a.out + (((size_t)n * a.Cout + co) * a.Ho + r) * a.Wo + wbase;
                             if (wbase + kPX <= a.Wo && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
@@ -426,6 +432,10 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
     case CONV_EPI_MUL_LRELU_GELU:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
         st = launch<CONV_EPI_MUL_LRELU_GELU, 1>(a, L, d.N * a.units, s);
+        break;
+    case CONV_EPI_NONE:
+        a.units = (h->Ho + a.rpc - 1) / a.rpc;
+        st = launch<CONV_EPI_NONE, 1>(a, L, d.N * a.units, s);
         break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP: {
         a.units = simt_gn_units(d, h->Ho, e.pool_k);

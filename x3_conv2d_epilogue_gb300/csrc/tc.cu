@@ -73,7 +73,6 @@ constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;     // columns per accumulator buffer
 constexpr int kMaxRing = 4;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
-constexpr int kStgPitch = 18;       // per-channel epilogue staging pitch (floats, even: float2 rows)
 constexpr int kPoolPitch = 33;      // GroupNorm pooled tile pitch (floats)
 constexpr int kMaxQ = 8;            // min chains: quadrant partials of a column loaded together
 
@@ -837,57 +836,98 @@ __device__ __forceinline__ float2 gelu_erf2(float t0, float t1) {
     return unpack2(mul2u(half_t, add2u(pack2f(1.0f, 1.0f), erfv)));
 }
 
-// Per-chunk work of the per-channel chain on 16 accumulator columns: f is a
-// 32x32b fragment (one channel per lane, 16 columns) and orow points at this
-// lane's first output column of the lane group's first channel in the
-// current row.  The 32 channels x 16 columns are transposed through shared
-// memory so each store instruction writes 4 channel rows of 64 contiguous
-// bytes; lane l stores columns c2, c2+1 (c2 = 2 (l & 7)) of channels
-// l/8 + 4 rp, rp = 0..7.
+// Per-chunk work of the per-channel chains (MUL_LRELU_GELU, NONE) on 16
+// accumulator columns: f is a 32x32b fragment (one channel per lane, 16
+// columns).  The 32 channels x 16 columns go through a per-warp staging tile
+// in shared memory, [32 rows][16 floats] with the 4-float groups of row r
+// XOR-swizzled by (r / 2) & 3, which keeps both sides free of bank
+// conflicts: lane r writes its row as four 16-byte groups, and the stores
+// read it transposed.  Where every lane's row start is 16-byte aligned (v4:
+// even rows of the 254-wide maps, whose 64516-float planes keep channel
+// starts aligned) lane l stores 16 bytes, columns 4 (l & 3) .. +3 of
+// channels l/4 + 8 rp (rp = 0..3): each store instruction writes 8 channel
+// rows of 64 contiguous bytes.  Otherwise (rows starting 8 bytes past a
+// 16-byte boundary) lane l stores 8 bytes, columns 2 (l & 7), +1 of
+// channels l/8 + 4 rp (rp = 0..7), or single floats for odd row widths.
+// o4 / o2: this lane's first output column of its first channel in the
+// current row, in the two store layouts; cstride: floats between channels.
+__device__ __forceinline__ int stg_at(int r, int c) { return r * 16 + 4 * ((c >> 2) ^ ((r >> 1) & 3)) + (c & 3); }
+
+template <int KIND>
 __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, float bias, float mult, int lane, int qd,
-                                               int ew, bool row_ok, int col0, float *orow, size_t cstride4, int wv,
-                                               int co_left, float *scratch) {
+                                               int ew, bool row_ok, bool v4, int col0, float *o4, float *o2,
+                                               size_t cstride, int wv, int co_left, float *scratch) {
+    float *stg = scratch + ew * 32 * 16;
     {
-        float *stg = scratch + ew * 32 * kStgPitch;
         const uint64_t bias2 = pack2f(bias, bias), mult2 = pack2f(mult, mult), slope2 = pack2f(a.slope, a.slope);
         auto tv2 = [](float2 v) { return pack2f(v.x, v.y); };
+        float2 v[8];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-            // (acc + bias) * mult for two columns, then LeakyReLU per value
-            const float2 tv = unpack2(mul2u(add2u(pack2(f.r[i], f.r[i + 1]), bias2), mult2));
-            const float2 sv = unpack2(mul2u(tv2(tv), slope2));
-            const float t0 = tv.x > 0.0f ? tv.x : sv.x, t1 = tv.y > 0.0f ? tv.y : sv.y;
-            *reinterpret_cast<float2 *>(stg + lane * kStgPitch + i) = gelu_erf2(t0, t1);
+            if constexpr (KIND == CONV_EPI_NONE) {
+                // the conv output itself: acc + bias
+                v[i / 2] = unpack2(add2u(pack2(f.r[i], f.r[i + 1]), bias2));
+            } else {
+                // (acc + bias) * mult for two columns, then LeakyReLU per value
+                const float2 tv = unpack2(mul2u(add2u(pack2(f.r[i], f.r[i + 1]), bias2), mult2));
+                const float2 sv = unpack2(mul2u(tv2(tv), slope2));
+                const float t0 = tv.x > 0.0f ? tv.x : sv.x, t1 = tv.y > 0.0f ? tv.y : sv.y;
+                v[i / 2] = gelu_erf2(t0, t1);
+            }
         }
-        __syncwarp();
-        if (row_ok) {
-            const int c2 = 2 * (lane & 7);
-            const float *src = stg + (lane >> 3) * kStgPitch + c2;
-            float *dst = orow + col0;
-            // rp < nrp: this lane's channels cb + 4 rp below the tile's real
-            // channels co_left (all 8 unless the GEMM is padded)
-            const int cb0 = (qd * 32) % a.Cout + (lane >> 3);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            *reinterpret_cast<float4 *>(stg + stg_at(lane, 4 * g)) =
+                make_float4(v[2 * g].x, v[2 * g].y, v[2 * g + 1].x, v[2 * g + 1].y);
+    }
+    __syncwarp();
+    if (row_ok) {
+        const int cq = (qd * 32) % a.Cout;  // the quadrant's first channel in the tile
+        if (v4) {
+            const int k = lane & 3, col = col0 + 4 * k;
+            const int cb0 = cq + (lane >> 2);
+            // rp < nrp: this lane's channels cb0 + 8 rp below the tile's real
+            // channels co_left (all 4 unless the GEMM is padded)
+            const int nrp = co_left >= a.Cout ? 4 : max(0, min(4, (co_left - cb0 + 7) >> 3));
+            const float *src = stg + stg_at(lane >> 2, 4 * k);
+            float *dst = o4 + col0;
+            if (col + 4 <= wv) {
+#pragma unroll
+                for (int rp = 0; rp < 4; ++rp)
+                    if (rp < nrp)
+                        *reinterpret_cast<float4 *>(dst + rp * 8 * cstride) =
+                            *reinterpret_cast<const float4 *>(src + rp * 8 * 16);
+            } else if (col < wv) {  // the row's ragged end
+#pragma unroll
+                for (int rp = 0; rp < 4; ++rp)
+                    if (rp < nrp)
+                        for (int e = 0; e < 4 && col + e < wv; ++e) dst[rp * 8 * cstride + e] = src[rp * 8 * 16 + e];
+            }
+        } else {
+            const int c2 = 2 * (lane & 7), r0 = lane >> 3;
+            const int cb0 = cq + r0;
             const int nrp = co_left >= a.Cout ? 8 : max(0, min(8, (co_left - cb0 + 3) >> 2));
-            // wv: the output columns of this column tile (Wo for a single tile)
+            float *dst = o2 + col0;
             if ((a.Wo & 1) == 0) {
                 if (col0 + c2 < wv) {
 #pragma unroll
                     for (int rp = 0; rp < 8; ++rp)
                         if (rp < nrp)
-                            *reinterpret_cast<float2 *>(dst + rp * cstride4) =
-                                *reinterpret_cast<const float2 *>(src + 4 * rp * kStgPitch);
+                            *reinterpret_cast<float2 *>(dst + rp * 4 * cstride) =
+                                *reinterpret_cast<const float2 *>(stg + stg_at(r0 + 4 * rp, c2));
                 }
             } else {
 #pragma unroll
                 for (int rp = 0; rp < 8; ++rp) {
                     if (rp >= nrp) break;
-                    if (col0 + c2 < wv) dst[rp * cstride4] = src[4 * rp * kStgPitch];
-                    if (col0 + c2 + 1 < wv) dst[rp * cstride4 + 1] = src[4 * rp * kStgPitch + 1];
+                    const float *src = stg + stg_at(r0 + 4 * rp, c2);
+                    if (col0 + c2 < wv) dst[rp * 4 * cstride] = src[0];
+                    if (col0 + c2 + 1 < wv) dst[rp * 4 * cstride + 1] = src[1];
                 }
             }
         }
-        __syncwarp();
     }
+    __syncwarp();
 }
 
 template <int KIND, bool GENERAL>
@@ -928,10 +968,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     };
     load_sb2(0);
     const uint64_t ss = pack2(__float_as_uint(a.scalar), __float_as_uint(a.scalar));
-    // per-channel chain: this lane's stores go to channels cb + 4 rp
-    const int cb = (qd * 32) % a.Cout + (lane >> 3);
+    // per-channel chains: this lane's stores go to channels cb4 + 8 rp
+    // (16-byte stores) or cb2 + 4 rp (8-byte stores)
+    const int cb4 = (qd * 32) % a.Cout + (lane >> 2), cb2 = (qd * 32) % a.Cout + (lane >> 3);
     const size_t plane = (size_t)a.Ho * a.Wo;
-    const size_t cstride4 = 4 * plane;
     const int nchunks = a.P / 16;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     // GroupNorm chain: group size, lanes per group inside a warp, and the sign
@@ -1148,7 +1188,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // 16-column chunks cc = hc, hc + 2, ...: the load of the next
                 // chunk is in flight while this one is processed
                 const bool row_ok = row < a.Ho;
-                float *orow = a.out + (((size_t)n * a.Co + cbase + cb) * a.Ho + (row_ok ? row : 0)) * a.Wo + c0 + 2 * (lane & 7);
+                const size_t rowoff = (size_t)(row_ok ? row : 0) * a.Wo + c0;
+                float *o4 = a.out + ((size_t)n * a.Co + cbase + cb4) * plane + rowoff + 4 * (lane & 3);
+                float *o2 = a.out + ((size_t)n * a.Co + cbase + cb2) * plane + rowoff + 2 * (lane & 7);
+                // 16-byte stores when every lane's row start is 16-byte aligned
+                const bool v4 = __all_sync(0xffffffffu, (reinterpret_cast<uintptr_t>(o4) & 15u) == 0);
                 const int wv = GENERAL ? min(a.CW, a.Wo - c0) : a.Wo;  // the column tile's output columns
                 const uint32_t tb = tbase + u * a.ucol;
                 int cc = hc;
@@ -1160,8 +1204,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 for (; cc < nchunks; cc += 2) {
                     const bool more = cc + 2 < nchunks;
                     if (more) tmem_ld16_issue(tb + (cc + 2) * 16, nxt);
-                    epi_chunk_chan(a, cur, bias, mult, lane, qd, ew, row_ok, cc * 16, orow, cstride4, wv, a.Co - cbase,
-                                   scratch);
+                    epi_chunk_chan<KIND>(a, cur, bias, mult, lane, qd, ew, row_ok, v4, cc * 16, o4, o2, plane, wv,
+                                         a.Co - cbase, scratch);
                     if (more) {
                         tmem_ld_wait(nxt);
                         cur = nxt;
@@ -1503,7 +1547,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_SCALE_MIN:
         return (uint32_t)(U * 4 * P * sizeof(float));
     case CONV_EPI_MUL_LRELU_GELU:
-        return (uint32_t)(kEpiWarps * 32 * kStgPitch * sizeof(float));
+    case CONV_EPI_NONE:
+        return (uint32_t)(kEpiWarps * 32 * 16 * sizeof(float));  // a 32 x 16 staging tile per warp
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign table
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 64) * sizeof(float));
     }
@@ -1829,6 +1874,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     case CONV_EPI_MIN_TANH2: st = launch_tc<CONV_EPI_MIN_TANH2>(args, pl, grid, s); break;
     case CONV_EPI_SCALE_MIN: st = launch_tc<CONV_EPI_SCALE_MIN>(args, pl, grid, s); break;
     case CONV_EPI_MUL_LRELU_GELU: st = launch_tc<CONV_EPI_MUL_LRELU_GELU>(args, pl, grid, s); break;
+    case CONV_EPI_NONE: st = launch_tc<CONV_EPI_NONE>(args, pl, grid, s); break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP:
         st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
         if (st == CONV_EPI_ERR_UNSUPPORTED && a.gn_fin) {  // cooperative launch refused: finalize separately
