@@ -249,6 +249,26 @@ CONV_EPI_API conv_epi_status conv_epi_forward_noalloc(const conv_epi_desc *desc,
  * forward does).  Synchronous. */
 CONV_EPI_API conv_epi_status conv_epi_noalloc_sync(void *stream);
 
+/* The chain alone, as a separate pass over a conv output that is already in
+ * memory: the structure each page designs its kernels for, with the
+ * convolution left to a library call that writes y in full (p25 and p32: a
+ * post-pass that takes the channel minimum per pixel; p54: one elementwise
+ * pass; p85: a GroupNorm statistics kernel, then one kernel that
+ * normalises, scales, max-pools and clamps).  For comparing the fused
+ * forward with that design on one machine, and for callers that hold y.
+ *   h: a handle for the problem (its description gives N, Cout, Ho, Wo; the
+ *      mode and layout do not matter here: the pass computes in fp32).
+ *   y: device pointer, the conv output [N][Cout][Ho][Wo] float32 with the
+ *      bias added, 16-byte aligned; read only.
+ *   epi: the chain, as for conv_epi_forward; index_out must be NULL.
+ *   out: device pointer, conv_epi_output_shape() floats, 16-byte aligned.
+ * Asynchronous on `stream`.  The GroupNorm chain keeps its statistics in a
+ * handle-owned buffer allocated on the first such call.  Returns
+ * INVALID_ARG / ALIGNMENT for bad arguments, UNSUPPORTED when index_out is
+ * set, CUDA or NO_MEMORY on a failing CUDA call. */
+CONV_EPI_API conv_epi_status conv_epi_postpass(conv_epi_handle h, const float *y, const conv_epi_epilogue_desc *epi,
+                                               float *out, void *stream);
+
 /* The tensor-core kernel's plan for one problem and chain, as a forward on
  * a handle would launch it: tiling, ring stages, the shared-memory layout,
  * the tensor-load box and the filter operand layout.  For diagnostics and

@@ -96,6 +96,7 @@ def _lib():
             L.conv_epi_forward.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_forward_host.argtypes = [P, P, P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_forward_noalloc.argtypes = [C.POINTER(Desc), P, P, P, C.POINTER(EpilogueDesc), P, P]
+            L.conv_epi_postpass.argtypes = [P, P, C.POINTER(EpilogueDesc), P, P]
             L.conv_epi_sync.argtypes = [P, P]
             L.conv_epi_noalloc_sync.argtypes = [P]
             L.conv_epi_test_drop_tile.argtypes = [P, I]
@@ -223,6 +224,17 @@ def conv_epi_forward_noalloc(N, Cin, H, W, Cout, x, w, b, epi, out, stream=None,
     px, pw, pb, po = _tensors(x, w, b, epi, out, device=True)
     _check(_lib().conv_epi_forward_noalloc(C.byref(d), px, pw, pb, C.byref(epi), po, _stream(stream)),
            "conv_epi_forward_noalloc")
+    return out
+
+
+def conv_epi_postpass(h, y, epi, out, stream=None):
+    """The chain alone over a stored conv output ``y`` [N, Cout, Ho, Wo]
+    (device, float32, bias included), in fp32 arithmetic."""
+    keep = getattr(epi, "_keep", (None, None, None, None))
+    for v, what, index in zip(keep, ("chan_scale", "gamma", "beta", "index_out"), (False, False, False, True)):
+        _arg(v, what, True, index)
+    _check(_lib().conv_epi_postpass(h, _arg(y, "y", True), C.byref(epi), _arg(out, "out", True), _stream(stream)),
+           "conv_epi_postpass")
     return out
 
 

@@ -380,6 +380,22 @@ CONV_EPI_API conv_epi_status conv_epi_forward_host(conv_epi_handle h, const floa
     return conv_epi_sync(h, stream);
 }
 
+CONV_EPI_API conv_epi_status conv_epi_postpass(conv_epi_handle h, const float *y, const conv_epi_epilogue_desc *epi,
+                                               float *out, void *stream) {
+    if (!h) return CONV_EPI_ERR_INVALID_ARG;
+    conv_epi_status st = check_epi(h->d, epi);
+    if (st) return st;
+    if (epi->index_out) return CONV_EPI_ERR_UNSUPPORTED;  // no index output on this pass
+    if (h->d.N == 0) {
+        h->last_launches = 0;
+        return CONV_EPI_OK;
+    }
+    if (!y || !out) return CONV_EPI_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out)) return CONV_EPI_ERR_ALIGNMENT;
+    CE_CUDA(cudaSetDevice(h->device));
+    return conv_epi::postpass_forward(h, y, *epi, out, static_cast<cudaStream_t>(stream));
+}
+
 CONV_EPI_API conv_epi_status conv_epi_sync(conv_epi_handle h, void *stream) {
     if (!h) return CONV_EPI_ERR_INVALID_ARG;
     CE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
@@ -425,6 +441,7 @@ CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
     cudaFree(h->xpad);
     cudaFree(h->gn_mem);
     cudaFree(h->stage);
+    cudaFree(h->post);
     if (h->host_copy) {
         cudaStreamDestroy(h->host_copy);
         cudaStreamDestroy(h->host_back);
@@ -441,7 +458,7 @@ CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
 
 CONV_EPI_API size_t conv_epi_workspace_bytes(conv_epi_handle h) {
     if (!h) return 0;
-    return 256 + h->wpack_bytes + h->xpad_bytes + h->gn_bytes + h->stage_bytes;
+    return 256 + h->wpack_bytes + h->xpad_bytes + h->gn_bytes + h->stage_bytes + h->post_bytes;
 }
 
 CONV_EPI_API int conv_epi_last_launch_count(conv_epi_handle h) { return h ? h->last_launches : 0; }

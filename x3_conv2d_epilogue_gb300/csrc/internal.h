@@ -72,6 +72,10 @@ struct conv_epi_handle_s {
     cudaEvent_t ev_entry = nullptr, ev_done = nullptr;
     cudaEvent_t ev_in[kHostSlices] = {}, ev_out[kHostSlices] = {};
 
+    // conv_epi_postpass: the GroupNorm statistics [N][groups][2] (on demand)
+    float *post = nullptr;
+    size_t post_bytes = 0;
+
     int last_launches = 0;
 
     // CONV_EPI_DEBUG=1 at create: every forward waits for its stream and
@@ -121,6 +125,10 @@ size_t tc_wpack_bytes(const conv_epi_desc &d);
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
 conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
                            const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
+
+// The chain as a separate pass over a stored conv output (postpass.cu).
+conv_epi_status postpass_forward(conv_epi_handle h, const float *y, const conv_epi_epilogue_desc &e, float *out,
+                                 cudaStream_t s);
 
 // GroupNorm finalize (gn.cu): pooled max/min + statistics -> output.
 // presel: the conv path left in pmax, per channel, the window extreme that the
