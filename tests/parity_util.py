@@ -100,6 +100,8 @@ def pool_index_gap(y: np.ndarray, pool_k: int, mean_sign: np.ndarray) -> np.ndar
     win = y[:, :, :Hp * pool_k, :Wp * pool_k].reshape(N, Cc, Hp, pool_k, Wp, pool_k).transpose(0, 1, 2, 4, 3, 5)
     win = win.reshape(N, Cc, Hp, Wp, pool_k * pool_k)
     win = win * mean_sign.reshape(N, Cc, 1, 1, 1)
+    if pool_k == 1:     # a one-entry window: its index is the only one
+        return np.full(win.shape[:-1], np.inf)
     v = np.sort(win, axis=-1)
     return v[..., -1] - v[..., -2]
 

@@ -1,8 +1,9 @@
 """The forward inside a CUDA graph: after conv_epi_reserve (so the forward
 allocates nothing), a conv_epi_forward captured on a stream and replayed
 gives the same outputs as a direct call, for a min chain, the per-channel
-chain and the GroupNorm chain (whose tf32 form is a cooperative launch plus a
-memset of its arrival counter), and for rows that the library first copies
+chain and the GroupNorm chain (whose fused tf32 form is a cooperative launch
+plus a memset of its arrival counter, and whose two-pass form is the conv
+and the post-pass's kernels), and for rows that the library first copies
 into 16-byte-padded rows."""
 import numpy as np
 import pytest
@@ -18,6 +19,9 @@ CASES = {
     "c3": W["c3_mul_lrelu_gelu"].resized(N=1, H=9),
     "c5": W["c5_gn_pool_clamp"].resized(N=2, H=42),
     "c2_w63": W["c2_min_tanh2"].resized(N=2, H=9, W=63),    # the row-padding kernel is captured too
+    # GroupNorm in two passes (conv into the handle's buffer, then the
+    # post-pass): both buffers come from conv_epi_reserve
+    "c5_two_pass": W["c5_gn_pool_clamp"].resized(N=2, H=14, W=150, Cout=128, groups=16, pool_k=2),
 }
 
 

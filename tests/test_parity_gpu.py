@@ -49,7 +49,7 @@ SMALL = {
     "c2_w300": W["c2_min_tanh2"].resized(N=1, H=6, W=300),                   # 2 tiles: 252 + 46 columns
     "c3_w520": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=520),              # 3 tiles, per-channel stores
     "c4_w516": W["c4_scale_min"].resized(N=2, H=4, W=516, scalar=-1.0),      # 3 tiles, Cout 128, max branch
-    "c5_w260": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=260),              # GroupNorm: one tile only (refused in tf32)
+    "c5_w260": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=260),              # GroupNorm over 2 column tiles (tf32: two passes)
     # more than 128 output channels (the tf32 path runs channel tiles of 128)
     "c4_co256": W["c4_scale_min"].resized(N=1, H=5, W=64, Cout=256),        # 2 channel tiles, atomic minimum
     "c3_co200": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=64, Cout=200),   # 2 tiles, the second padded
@@ -62,12 +62,18 @@ SMALL = {
     "c5_w126": W["c5_gn_pool_clamp"].resized(N=1, H=18, W=126),              # 124 columns: 31 whole windows
     "c5_w37": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=37),                # two bands per unit, 3 columns past the pool
     "min_w3": W["pr1_min_tanh2"].resized(N=2, Cin=2, H=3, W=3, Cout=1),      # a single output per image
+    # GroupNorm shapes the fused tf32 epilogue does not take (tf32: the conv,
+    # then the chain's post-pass, through a handle-owned buffer of y)
+    "c5_co32": W["c5_gn_pool_clamp"].resized(N=2, H=18, W=64, Cout=32, groups=8),     # Cout 32, 4 channels per group
+    "c5_co128": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=96, Cout=128, groups=16),  # Cout 128
+    "c5_co256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=256, groups=32),  # 2 channel tiles
+    "c5_k2": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=50, pool_k=2),               # 2 x 2 windows, odd tail row
+    "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling
+    "c5_k2_w300": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=300, pool_k=2, groups=64),  # 2 column tiles, a group per channel
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
-# shapes the tf32 kernel refuses (its GroupNorm epilogue pools whole bands of
-# four rows inside a unit, which needs W <= 128): the call must say so, not
-# fall back
-TF32_REFUSED = {"c5_w260"}
+# shapes the tf32 kernel refuses: the call must say so, not fall back
+TF32_REFUSED = set()
 
 
 def modes():
@@ -200,8 +206,7 @@ def test_tf32_operand_rounding_is_exact():
 def test_channels_last_parity(case):
     """The tf32 path with channels-last input: the same seeded values,
     transposed, against the same oracle and bound.  Shapes whose Cin is not a
-    multiple of 4, and the GroupNorm shape the tf32 kernel cannot pool, are
-    refused with UNSUPPORTED."""
+    multiple of 4 are refused with UNSUPPORTED."""
     import x3_conv2d_epilogue_gb300 as ce
     wl = SMALL[case]
     t = synth.make_inputs(wl, seed=0)

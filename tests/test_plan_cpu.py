@@ -160,19 +160,28 @@ def test_plans_of_tested_shapes(case, layout):
             plan(*args, groups=wl.groups, pool_k=wl.pool_k)
         assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
         return
-    gn_refused = wl.kind == ce.GN_SCALE_POOL_CLAMP and not (wl.Cout == 64 and wl.pool_k == 4 and wl.W <= 128)
-    if gn_refused:
-        with pytest.raises(ce.ConvEpiError) as ei:
-            plan(*args, groups=wl.groups, pool_k=wl.pool_k)
-        assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
-        return
-    check_plan(plan(*args, groups=wl.groups, pool_k=wl.pool_k), *args)
+    check_gn_form(plan(*args, groups=wl.groups, pool_k=wl.pool_k), *args, pool_k=wl.pool_k)
+
+
+def gn_fused(kind, Cout, W, pool_k):
+    return kind == ce.GN_SCALE_POOL_CLAMP and Cout == 64 and pool_k == 4 and W <= 128
+
+
+def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k):
+    """A GroupNorm shape the fused epilogue does not take runs as two passes:
+    its plan is the plain conv's, and the handle holds the conv output
+    between them."""
+    two_pass = kind == ce.GN_SCALE_POOL_CLAMP and not gn_fused(kind, Cout, W, pool_k)
+    assert q["gn_two_pass"] == int(two_pass)
+    assert q["ybuf_bytes"] == (N * Cout * (H - 2) * (W - 2) * 4 if two_pass else 0)
+    check_plan(q, N, Cin, H, W, Cout, ce.NONE if two_pass else kind, layout)
 
 
 def test_random_shapes_all_planned_and_in_range():
-    """Every non-GroupNorm shape with H, W >= 3 has a plan (the tf32 mode takes
-    any size), and every plan passes the range checks; GroupNorm shapes are
-    planned exactly when Cout = 64, pool_k = 4 and W <= 128."""
+    """Every shape with H, W >= 3 has a plan (the tf32 mode takes any size),
+    and every plan passes the range checks; GroupNorm shapes are fused
+    exactly when Cout = 64, pool_k = 4 and W <= 128, and otherwise planned as
+    the plain conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):
         kind = rng.choice([ce.MIN_TANH2, ce.SCALE_MIN, ce.MUL_LRELU_GELU, ce.GN_SCALE_POOL_CLAMP, ce.NONE])
@@ -193,15 +202,7 @@ def test_random_shapes_all_planned_and_in_range():
             H = max(H, pool_k + 2)
             W = max(W, pool_k + 2)
         args = (N, Cin, H, W, Cout, kind, layout)
-        expect_ok = kind != ce.GN_SCALE_POOL_CLAMP or (Cout == 64 and pool_k == 4 and W <= 128)
-        try:
-            q = plan(*args, groups=groups, pool_k=pool_k)
-        except ce.ConvEpiError as e:
-            assert not expect_ok, (args, groups, pool_k, e)
-            assert ce.STATUS[e.status] == "UNSUPPORTED"
-            continue
-        assert expect_ok, (args, groups, pool_k)
-        check_plan(q, *args)
+        check_gn_form(plan(*args, groups=groups, pool_k=pool_k), *args, pool_k=pool_k)
 
 
 def test_plan_query_arguments():

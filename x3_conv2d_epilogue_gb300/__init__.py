@@ -66,7 +66,7 @@ _PLAN_FIELDS = (
     "units_per_image", "resident", "na", "nb", "nr", "a_bytes", "b_bytes", "raw_bytes", "scratch_bytes",
     "a_off", "b_off", "raw_off", "bar_off", "scratch_off", "bar_bytes", "smem", "smem_limit",
     "a_plane_bytes", "a_lbo", "a_kw_stride", "x_pitch", "box[4]", "acc_cols", "tmem_cols", "conv_items",
-    "wpack_bytes", "xpad_bytes",
+    "wpack_bytes", "xpad_bytes", "gn_two_pass", "ybuf_bytes",
 )
 
 

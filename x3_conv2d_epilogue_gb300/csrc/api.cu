@@ -246,10 +246,9 @@ CONV_EPI_API conv_epi_status conv_epi_reserve(conv_epi_handle h, const conv_epi_
     if (st) return st;
     if ((st = check_mode_support(h->d, epi))) return st;
     if (epi->kind != CONV_EPI_GN_SCALE_POOL_CLAMP) return CONV_EPI_OK;
-    const int units = h->d.mode == CONV_EPI_MODE_FP32 ? conv_epi::simt_gn_units(h->d, h->Ho, epi->pool_k)
-                                                      : conv_epi::tc_gn_units(h->d, h->Ho, epi->pool_k);
     CE_CUDA(cudaSetDevice(h->device));
-    return conv_epi::ensure_gn_workspace(h, epi->pool_k, epi->groups, units);
+    if (h->d.mode == CONV_EPI_MODE_TF32) return conv_epi::tc_reserve(h, *epi);
+    return conv_epi::ensure_gn_workspace(h, epi->pool_k, epi->groups, conv_epi::simt_gn_units(h->d, h->Ho, epi->pool_k));
 }
 
 CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
@@ -442,6 +441,7 @@ CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
     cudaFree(h->gn_mem);
     cudaFree(h->stage);
     cudaFree(h->post);
+    cudaFree(h->ybuf);
     if (h->host_copy) {
         cudaStreamDestroy(h->host_copy);
         cudaStreamDestroy(h->host_back);
@@ -458,7 +458,7 @@ CONV_EPI_API conv_epi_status conv_epi_destroy(conv_epi_handle h) {
 
 CONV_EPI_API size_t conv_epi_workspace_bytes(conv_epi_handle h) {
     if (!h) return 0;
-    return 256 + h->wpack_bytes + h->xpad_bytes + h->gn_bytes + h->stage_bytes + h->post_bytes;
+    return 256 + h->wpack_bytes + h->xpad_bytes + h->gn_bytes + h->stage_bytes + h->post_bytes + h->ybuf_bytes;
 }
 
 CONV_EPI_API int conv_epi_last_launch_count(conv_epi_handle h) { return h ? h->last_launches : 0; }

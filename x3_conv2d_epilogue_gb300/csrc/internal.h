@@ -72,6 +72,11 @@ struct conv_epi_handle_s {
     cudaEvent_t ev_entry = nullptr, ev_done = nullptr;
     cudaEvent_t ev_in[kHostSlices] = {}, ev_out[kHostSlices] = {};
 
+    // tf32 GroupNorm shapes the fused epilogue does not take: the conv output
+    // y [N][Cout][Ho][Wo] between the two passes (by conv_epi_reserve)
+    float *ybuf = nullptr;
+    size_t ybuf_bytes = 0;
+
     // conv_epi_postpass: the GroupNorm statistics [N][groups][2] (on demand)
     float *post = nullptr;
     size_t post_bytes = 0;
@@ -123,10 +128,16 @@ size_t tc_xpad_bytes(const conv_epi_desc &d);  // 0 unless the input rows need t
 conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, conv_epi_plan &q);
 size_t tc_wpack_bytes(const conv_epi_desc &d);
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
+// the GroupNorm chain fused into the conv kernel (else two passes through a
+// buffer of the conv output); workspace for a chain ahead of a forward
+bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e);
+conv_epi_status tc_reserve(conv_epi_handle h, const conv_epi_epilogue_desc &e);
 conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
                            const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
 
-// The chain as a separate pass over a stored conv output (postpass.cu).
+// The chain as a separate pass over a stored conv output (postpass.cu), and
+// the buffer of its GroupNorm statistics, N * groups (mean, rstd) pairs.
+conv_epi_status ensure_post_stats(conv_epi_handle h, int groups);
 conv_epi_status postpass_forward(conv_epi_handle h, const float *y, const conv_epi_epilogue_desc &e, float *out,
                                  cudaStream_t s);
 

@@ -155,6 +155,20 @@ unsigned blocks_for(size_t work, int sm_count) {
 
 }  // namespace
 
+conv_epi_status ensure_post_stats(conv_epi_handle h, int groups) {
+    const size_t need = (size_t)h->d.N * groups * 2 * sizeof(float);
+    if (need > h->post_bytes) {
+        if (h->post) {
+            CE_CUDA(cudaDeviceSynchronize());
+            CE_CUDA(cudaFree(h->post));
+            h->post = nullptr, h->post_bytes = 0;
+        }
+        CE_CUDA(cudaMalloc(&h->post, need));
+        h->post_bytes = need;
+    }
+    return CONV_EPI_OK;
+}
+
 conv_epi_status postpass_forward(conv_epi_handle h, const float *y, const conv_epi_epilogue_desc &e, float *out,
                                  cudaStream_t s) {
     const conv_epi_desc &d = h->d;
@@ -175,16 +189,8 @@ conv_epi_status postpass_forward(conv_epi_handle h, const float *y, const conv_e
             y, out, d.N, d.Cout, plane, nullptr, 0.0f);
         break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP: {
-        const size_t need = (size_t)d.N * e.groups * 2 * sizeof(float);
-        if (need > h->post_bytes) {
-            if (h->post) {
-                CE_CUDA(cudaStreamSynchronize(s));
-                CE_CUDA(cudaFree(h->post));
-                h->post = nullptr, h->post_bytes = 0;
-            }
-            CE_CUDA(cudaMalloc(&h->post, need));
-            h->post_bytes = need;
-        }
+        conv_epi_status st = ensure_post_stats(h, e.groups);
+        if (st) return st;
         const int cpg = d.Cout / e.groups;
         post_gn_stats<<<(unsigned)(d.N * e.groups), kThreads, 0, s>>>(y, h->post, e.groups, cpg, plane,
                                                                       1.0 / ((double)cpg * plane), e.eps);

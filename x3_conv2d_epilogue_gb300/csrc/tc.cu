@@ -1704,20 +1704,28 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
 
 }  // namespace
 
+// The GroupNorm chain fused into the conv kernel: its epilogue pools 4x4
+// windows over bands of 4 rows (two 64-channel row slots per u): one band per
+// unit with P in 80..128 (at most 4 sixteen-column chunks per warp), two with
+// P = 64 (2 chunks).  Other GroupNorm shapes run as two passes (tc_forward).
+bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
+    Plan pl;
+    if (!make_plan(d, CONV_EPI_GN_SCALE_POOL_CLAMP, pl)) return false;
+    const bool one_band = pl.RU == 4 && pl.P > 64 && pl.P <= 128;
+    const bool two_bands = pl.RU == 8 && pl.P == 64;
+    return e.pool_k == 4 && (one_band || two_bands) && pl.S == 2 && d.Cout == 64;
+}
+
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
     Plan pl;
-    const int kind = e ? e->kind : CONV_EPI_MIN_TANH2;
+    int kind = e ? e->kind : CONV_EPI_MIN_TANH2;
+    // a GroupNorm shape the fused epilogue does not take needs the plain conv
+    if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !tc_gn_fused(d, *e)) kind = CONV_EPI_NONE;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
-    if (e && e->kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
-        // the epilogue pools 4x4 windows over bands of 4 rows (two 64-channel
-        // row slots per u): one band per unit with P in 80..128 (at most 4
-        // sixteen-column chunks per warp), two with P = 64 (2 chunks)
-        const bool one_band = pl.RU == 4 && pl.P > 64 && pl.P <= 128;
-        const bool two_bands = pl.RU == 8 && pl.P == 64;
-        if (e->pool_k != 4 || !(one_band || two_bands) || pl.S != 2 || d.Cout != 64) return CONV_EPI_ERR_UNSUPPORTED;
-    }
     return CONV_EPI_OK;
 }
+
+size_t tc_ybuf_bytes(const conv_epi_desc &d) { return (size_t)d.N * d.Cout * (d.H - 2) * (d.W - 2) * sizeof(float); }
 
 size_t tc_xpad_bytes(const conv_epi_desc &d) {
     if (d.mode != CONV_EPI_MODE_TF32 || !needs_xpad(d)) return 0;
@@ -1728,7 +1736,12 @@ conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_de
     q = conv_epi_plan{};
     q.struct_bytes = (int64_t)sizeof(conv_epi_plan);
     Plan pl;
-    if (!make_plan(d, e.kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
+    // a GroupNorm shape the fused epilogue does not take: the plain conv's
+    // plan (its first pass)
+    const bool two_pass = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !tc_gn_fused(d, e);
+    const int kind = two_pass ? CONV_EPI_NONE : e.kind;
+    q.gn_two_pass = two_pass ? 1 : 0;
+    if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     q.gemm_cout = pl.Cg, q.S = pl.S, q.P = pl.P, q.U = pl.U, q.RU = pl.RU, q.Rin = pl.Rin, q.PL = pl.PL;
     q.ucol = pl.ucol, q.chunks = pl.chunks, q.CT = pl.CT, q.CW = pl.CW, q.BW = pl.BW, q.MT = pl.MT;
     q.units_per_image = (int64_t)((d.H - 2 + pl.RU - 1) / pl.RU) * pl.CT * pl.MT;
@@ -1747,6 +1760,7 @@ conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_de
     dt.mode = CONV_EPI_MODE_TF32;
     q.wpack_bytes = (int64_t)tc_wpack_bytes(dt);
     q.xpad_bytes = (int64_t)tc_xpad_bytes(dt);
+    q.ybuf_bytes = two_pass ? (int64_t)tc_ybuf_bytes(dt) : 0;
     return tc_supported(d, &e);
 }
 
@@ -1762,9 +1776,41 @@ int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
     return (Ho + pl.RU - 1) / pl.RU;
 }
 
+conv_epi_status tc_reserve(conv_epi_handle h, const conv_epi_epilogue_desc &e) {
+    if (e.kind != CONV_EPI_GN_SCALE_POOL_CLAMP) return CONV_EPI_OK;
+    if (tc_gn_fused(h->d, e)) return ensure_gn_workspace(h, e.pool_k, e.groups, tc_gn_units(h->d, h->Ho, e.pool_k));
+    const size_t need = tc_ybuf_bytes(h->d);  // the two-pass form: the conv output
+    if (need > h->ybuf_bytes) {
+        if (h->ybuf) {
+            CE_CUDA(cudaDeviceSynchronize());
+            CE_CUDA(cudaFree(h->ybuf));
+            h->ybuf = nullptr, h->ybuf_bytes = 0;
+        }
+        CE_CUDA(cudaMalloc(&h->ybuf, need));
+        h->ybuf_bytes = need;
+    }
+    return ensure_post_stats(h, e.groups);
+}
+
 conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
                            const conv_epi_epilogue_desc &e, float *out, cudaStream_t s) {
     const conv_epi_desc &d = h->d;
+    if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !tc_gn_fused(d, e)) {
+        // GroupNorm shapes the fused epilogue does not take, in two passes:
+        // the tensor-core conv writes y + b to the handle's buffer, then the
+        // chain's post-pass (statistics, then normalise-scale-pool-clamp)
+        if (!h->ybuf || h->ybuf_bytes < tc_ybuf_bytes(d) || h->post_bytes < (size_t)d.N * e.groups * 2 * sizeof(float))
+            return CONV_EPI_ERR_INVALID_ARG;  // conv_epi_reserve sizes both
+        conv_epi_epilogue_desc plain = e;
+        plain.kind = CONV_EPI_NONE;
+        plain.index_out = nullptr;
+        conv_epi_status st = tc_forward(h, x, w, b, plain, h->ybuf, s);
+        if (st) return st;
+        const int conv_launches = h->last_launches;
+        if ((st = postpass_forward(h, h->ybuf, e, out, s))) return st;
+        h->last_launches += conv_launches;
+        return CONV_EPI_OK;
+    }
     Plan pl;
     if (!make_plan(d, e.kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     EncodeTiledFn enc = encode_tiled();
