@@ -61,6 +61,9 @@ SMALL = {
     "c4_w262": W["c4_scale_min"].resized(N=1, H=4, W=262),                   # 2 column tiles over padded rows
     "c5_w126": W["c5_gn_pool_clamp"].resized(N=1, H=18, W=126),              # 124 columns: 31 whole windows
     "c5_w37": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=37),                # two bands per unit, 3 columns past the pool
+    "c5_w98": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=98),                # fused, 112 columns: chunk 6 whole, chunk 7 absent
+    "c5_w107": W["c5_gn_pool_clamp"].resized(N=1, H=13, W=107),              # fused, chunk 6 ragged at column 105
+    "c5_w90": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=90),                # one band of 96 columns: two passes in tf32
     "min_w3": W["pr1_min_tanh2"].resized(N=2, Cin=2, H=3, W=3, Cout=1),      # a single output per image
     # GroupNorm shapes the fused tf32 epilogue does not take (tf32: the conv,
     # then the chain's post-pass, through a handle-owned buffer of y)

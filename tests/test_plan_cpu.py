@@ -130,8 +130,8 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
         assert top == 32 * 16 - 1 and q["scratch_bytes"] >= 8 * 32 * 16 * 4
     else:
         bands = U // 2
-        assert U in (2, 4) and P <= 128 and S == 2
-        assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 64) * 4
+        assert U in (2, 4) and P <= 128 and S == 2 and (P == 64 or W - 2 >= 96)
+        assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 2 * 64) * 4
 
 
 def parity_shapes():
@@ -164,7 +164,9 @@ def test_plans_of_tested_shapes(case, layout):
 
 
 def gn_fused(kind, Cout, W, pool_k):
-    return kind == ce.GN_SCALE_POOL_CLAMP and Cout == 64 and pool_k == 4 and W <= 128
+    # rows of up to 64 columns run as two pooling bands per unit; wider rows as
+    # one band, fused when the first 96 output columns are whole (Wo >= 96)
+    return kind == ce.GN_SCALE_POOL_CLAMP and Cout == 64 and pool_k == 4 and (W <= 64 or 98 <= W <= 128)
 
 
 def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k):
@@ -180,7 +182,7 @@ def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k):
 def test_random_shapes_all_planned_and_in_range():
     """Every shape with H, W >= 3 has a plan (the tf32 mode takes any size),
     and every plan passes the range checks; GroupNorm shapes are fused
-    exactly when Cout = 64, pool_k = 4 and W <= 128, and otherwise planned as
+    exactly when Cout = 64, pool_k = 4 and W <= 64 or 98 <= W <= 128, and otherwise planned as
     the plain conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):

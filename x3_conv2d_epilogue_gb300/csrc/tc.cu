@@ -948,9 +948,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     int cbase = 0;                    // first channel of the current channel tile
     float bias = co < a.Co ? __ldg(&a.b[co]) : 0.0f;
     float mult = KIND == CONV_EPI_MUL_LRELU_GELU && co < a.Co ? __ldg(&a.chan_scale[co]) : 0.0f;
+    // GroupNorm chain: the sign of the channel's affine slope gamma * scale
+    // (rstd > 0), folded into the packed filter: the accumulator is gsg * (y - b)
     const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
-    const uint64_t gg2 = pack2(__float_as_uint(gsg), __float_as_uint(gsg));
-    const uint64_t gb2 = pack2(__float_as_uint(gsg * bias), __float_as_uint(gsg * bias));
     // min chains: scalar * bias of the four channels this thread holds in a
     // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4),
     // each duplicated into a register pair, and the scalar likewise.  The
@@ -984,8 +984,26 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr int kNB = (kGN && GENERAL) ? 2 : 1;
     constexpr int kKC = (kGN && GENERAL) ? 2 : 4;
     constexpr int kWin = 4 * kKC;  // pooling windows per band and thread
-    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads;
-    if (kGN && slot == 0) gn_sgn[co] = gsg;
+    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + 64;
+    if (kGN && slot == 0) gn_sgn[co] = gsg, gn_bias[co] = bias;
+    // GroupNorm: this thread's chunks are cc = hc + 2 kc.  In the one-band
+    // form (kKC = 4) chunks kc < 3 lie below column 96 and are whole (that
+    // form has Wo >= 96); the others may hold columns >= Wo (or lie past P),
+    // which the sums skip: bit 16 (kc - kMask0) + i of gn_rag is set when
+    // column 16 cc + i < Wo.  (A select per value costs as much as the sums
+    // themselves, so only the chunks that can be ragged take it.)  gn_ncol
+    // counts this thread's valid columns.
+    constexpr int kMask0 = kKC == 4 ? 3 : 0;
+    uint32_t gn_rag = 0;
+    int gn_ncol = 0;
+    if constexpr (kGN) {
+        for (int kc = 0; kc < kKC; ++kc) {
+            const int lim = a.Wo - 16 * (hc + 2 * kc);  // valid columns in the chunk
+            const int nv = lim < 0 ? 0 : lim > 16 ? 16 : lim;
+            gn_ncol += nv;
+            if (kc >= kMask0) gn_rag |= ((1u << nv) - 1u) << (16 * (kc - kMask0));
+        }
+    }
     // Min chains: the cross-quadrant combine of a unit's partial minima, the
     // chain's tail and the row stores.  Every partial of a column (each row of
     // the unit, each quadrant) is loaded before any is used: under the tensor
@@ -1079,60 +1097,67 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             }
         }
 
-        for (int u = 0; u < a.U; ++u) {
-            const int row = r0 + u * a.S + slot;  // the same for the whole warp
-            if constexpr (kGN) {
+        int gn_rows = 0;  // this thread's rows below Ho in the unit
+        if constexpr (kGN) {
+            // Per u: the warp's kKC chunks loaded together, then per chunk the
+            // window maxima of the accumulator (sgn * (y - b)) and, over the
+            // valid columns, sums of it and of its square.  The code is
+            // straight-line: only chunks kc >= kMask0 select their valid
+            // columns, and a row at or past Ho is skipped whole (its band is
+            // never stored).
+            auto gn_step = [&](const Frag16 (&f)[kKC], float (&pext)[kWin]) {
+#pragma unroll
+                for (int kc = 0; kc < kKC; ++kc) {
+                    uint64_t v2[8];
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) v2[p] = pack2(f[kc].r[2 * p], f[kc].r[2 * p + 1]);
+                    // window extremes (windows past Wp are never stored)
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const float2 a01 = unpack2(v2[2 * wi]), a23 = unpack2(v2[2 * wi + 1]);
+                        pext[4 * kc + wi] = fmax3(fmax3(a01.x, a01.y, a23.x), a23.y, pext[4 * kc + wi]);
+                    }
+                    if (kc >= kMask0) {  // columns >= Wo add nothing to the sums
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            const uint32_t b0 = 1u << (16 * (kc - kMask0) + 2 * p);
+                            const float2 w = unpack2(v2[p]);
+                            v2[p] = pack2(__float_as_uint((gn_rag & b0) ? w.x : 0.0f),
+                                          __float_as_uint((gn_rag & (b0 << 1)) ? w.y : 0.0f));
+                        }
+                    }
+                    // column i feeds chain i & 3: pair p's halves go to
+                    // chains 2 (p & 1) and 2 (p & 1) + 1
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) {
+                        ls2[p & 1] = add2u(ls2[p & 1], v2[p]);
+                        lss2[p & 1] = fma2u(v2[p], v2[p], lss2[p & 1]);
+                    }
+                }
+            };
+            for (int u = 0; u < a.U; ++u) {
+                const bool row_ok = r0 + u * a.S + slot < a.Ho;  // the same for the whole warp
+                gn_rows += row_ok ? 1 : 0;
                 Frag16 f[kKC];
 #pragma unroll
                 for (int kc = 0; kc < kKC; ++kc)
                     if (hc + 2 * kc < nchunks) tmem_ld16_issue(tbase + u * a.ucol + (hc + 2 * kc) * 16, f[kc]);
                 tmem_ld_wait2(f[0], f[1]);
                 if constexpr (kKC == 4) tmem_ld_wait2(f[2], f[3]);
-                // this u's rows belong to band u / 2 (two row slots per u)
-                auto gn_update = [&](float (&pext)[kWin]) {
-#pragma unroll
-                    for (int kc = 0; kc < kKC; ++kc) {
-                        const int cc = hc + 2 * kc;
-                        if (cc >= nchunks) continue;
-                        const int col0 = cc * 16;
-                        // w = gsg * y = gsg * acc + gsg * bias (the sign flip is
-                        // exact, so w is -y or y rounded once), two adjacent
-                        // columns per packed FMA
-                        uint64_t w2[8];
-#pragma unroll
-                        for (int p = 0; p < 8; ++p) w2[p] = fma2u(pack2(f[kc].r[2 * p], f[kc].r[2 * p + 1]), gg2, gb2);
-                        if (col0 + 16 > a.Wo) {  // the row's ragged end: columns >= Wo add nothing
-#pragma unroll
-                            for (int p = 0; p < 8; ++p) {
-                                const float2 w = unpack2(w2[p]);
-                                w2[p] = pack2(__float_as_uint(col0 + 2 * p < a.Wo ? w.x : 0.0f),
-                                              __float_as_uint(col0 + 2 * p + 1 < a.Wo ? w.y : 0.0f));
-                            }
-                        }
-                        // column i feeds chain i & 3: pair p's halves go to
-                        // chains 2 (p & 1) and 2 (p & 1) + 1
-#pragma unroll
-                        for (int p = 0; p < 8; ++p) {
-                            ls2[p & 1] = add2u(ls2[p & 1], w2[p]);
-                            lss2[p & 1] = fma2u(w2[p], w2[p], lss2[p & 1]);
-                        }
-                        // window extremes (windows past Wp are never stored)
-#pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            const float2 a01 = unpack2(w2[2 * wi]), a23 = unpack2(w2[2 * wi + 1]);
-                            pext[4 * kc + wi] = fmax3(fmax3(a01.x, a01.y, a23.x), a23.y, pext[4 * kc + wi]);
-                        }
-                    }
-                };
-                if (row < a.Ho) {
+                if (row_ok) {
+                    // this u's rows belong to band u / 2 (two row slots per u)
                     if constexpr (kNB == 2) {
-                        if (u >= 2) gn_update(pext1);
-                        else gn_update(pext0);
+                        if (u >= 2) gn_step(f, pext1);
+                        else gn_step(f, pext0);
                     } else {
-                        gn_update(pext0);
+                        gn_step(f, pext0);
                     }
                 }
-            } else if constexpr (kMin) {
+            }
+        } else {
+        for (int u = 0; u < a.U; ++u) {
+            const int row = r0 + u * a.S + slot;  // the same for the whole warp
+            if constexpr (kMin) {
                 // 64-column batches: the warp takes batches hc, hc + 2, ...,
                 // loads a batch's four 16-column fragments with one wait and
                 // reduces each fragment's own four channels in registers;
@@ -1213,6 +1238,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 }
             }
         }
+        }
         // tensor memory of this unit is no longer needed
         tc_fence_before();
         __syncwarp();
@@ -1226,8 +1252,12 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         } else if constexpr (kGN) {
             // group partial sums: lanes of one group (cw = min(cpg, 32) adjacent
             // channels) add by shuffles, the rest folds below in a fixed order
+            // the sums are of v = gsg * (y - b) over cnt values: back to y,
+            // sum y = gsg sum v + cnt b, sum y^2 = sum v^2 + 2 b gsg sum v + cnt b^2
             const float2 l0 = unpack2(ls2[0]), l1 = unpack2(ls2[1]), q0 = unpack2(lss2[0]), q1 = unpack2(lss2[1]);
-            float gs = gsg * ((l0.x + l0.y) + (l1.x + l1.y)), gss = (q0.x + q0.y) + (q1.x + q1.y);  // back to y
+            const float sv = gsg * ((l0.x + l0.y) + (l1.x + l1.y)), svv = (q0.x + q0.y) + (q1.x + q1.y);
+            const float cnt = (float)(gn_ncol * gn_rows);
+            float gs = fmaf(cnt, bias, sv), gss = fmaf(2.0f * bias, sv, fmaf(cnt * bias, bias, svv));
             for (int o = 1; o < gn_cw; o <<= 1) {
                 gs += __shfl_xor_sync(0xffffffffu, gs, o);
                 gss += __shfl_xor_sync(0xffffffffu, gss, o);
@@ -1292,7 +1322,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 #pragma unroll
                     for (int i = 0; i < 64 / kEpiWarps; ++i) {
                         const int c2 = ew + kEpiWarps * i;
-                        m[i] = gn_sgn[c2] * fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]);
+                        m[i] = fmaf(gn_sgn[c2], fmaxf(pt0[c2 * kPoolPitch + lane], pt1[c2 * kPoolPitch + lane]),
+                                    gn_bias[c2]);
                     }
 #pragma unroll
                     for (int i = 0; i < 64 / kEpiWarps; ++i) dst[i * cstep] = m[i];
@@ -1481,7 +1512,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
 // 8c + 4jg + e >= Cin (the last
 // chunk of a Cin that is not a multiple of 8; the input tile's matching
 // channels arrive as zeros too, from the tensor load's out-of-range fill).
-__global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp, int Cin, int Cout, int Co, int S) {
+// For the fused GroupNorm chain (gamma, scale given) filter co is negated
+// where gamma[co] and scale[co] differ in sign, so the accumulator holds
+// sgn * (y - b) with sgn the sign of the channel's affine slope (negation is
+// exact, and tf32 rounding to nearest is symmetric).
+__global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp, int Cin, int Cout, int Co, int S,
+                             const float *__restrict__ gamma, const float *__restrict__ scale) {
     const int planes = 2 * S + 1;
     const int Cpad = (Cin + 7) / 8 * 8;
     const size_t total = (size_t)Cpad * 3 * planes * Cout;  // = chunks*3*2*planes*Cout*4
@@ -1500,7 +1536,10 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
         const int kh = S + 1 - p;
         float v = 0.0f;
         const int ci = 8 * c + 4 * jg + e;
-        if (kh >= 0 && kh <= 2 && ci < Cin && co < Co) v = w[(((size_t)co * Cin + ci) * 3 + kh) * 3 + kw];
+        if (kh >= 0 && kh <= 2 && ci < Cin && co < Co) {
+            v = w[(((size_t)co * Cin + ci) * 3 + kh) * 3 + kw];
+            if (gamma && signbit(__ldg(&gamma[co])) != signbit(__ldg(&scale[co]))) v = -v;
+        }
         wp[i] = __uint_as_float(f32_to_tf32(v));
     }
 }
@@ -1549,8 +1588,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_MUL_LRELU_GELU:
     case CONV_EPI_NONE:
         return (uint32_t)(kEpiWarps * 32 * 16 * sizeof(float));  // a 32 x 16 staging tile per warp
-    case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign table
-        return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 64) * sizeof(float));
+    case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
+        return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
     }
     return 0;
 }
@@ -1706,12 +1745,13 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
 
 // The GroupNorm chain fused into the conv kernel: its epilogue pools 4x4
 // windows over bands of 4 rows (two 64-channel row slots per u): one band per
-// unit with P in 80..128 (at most 4 sixteen-column chunks per warp), two with
-// P = 64 (2 chunks).  Other GroupNorm shapes run as two passes (tc_forward).
+// unit with P in 112..128 (4 sixteen-column chunks per warp; the first 96
+// columns whole, so Wo >= 96), two with P = 64 (2 chunks).  Other GroupNorm
+// shapes run as two passes (tc_forward).
 bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     Plan pl;
     if (!make_plan(d, CONV_EPI_GN_SCALE_POOL_CLAMP, pl)) return false;
-    const bool one_band = pl.RU == 4 && pl.P > 64 && pl.P <= 128;
+    const bool one_band = pl.RU == 4 && pl.P > 64 && pl.P <= 128 && d.W - 2 >= 96;
     const bool two_bands = pl.RU == 8 && pl.P == 64;
     return e.pool_k == 4 && (one_band || two_bands) && pl.S == 2 && d.Cout == 64;
 }
@@ -1858,8 +1898,10 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         // channel tile m: filters 128m .. 128m + 127, after the previous tiles' chunks
         for (int m = 0; m < pl.MT; ++m) {
             const int Cg = gemm_cout(d.Cout);
+            const bool gn_sign = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP;  // (fused: one channel tile)
             pack_weights<<<blocks, threads, 0, s>>>(w + (size_t)m * Cg * d.Cin * 9, h->wpack + (size_t)m * total,
-                                                    d.Cin, Cg, min(Cg, d.Cout - m * Cg), pl.S);
+                                                    d.Cin, Cg, min(Cg, d.Cout - m * Cg), pl.S,
+                                                    gn_sign ? e.gamma : nullptr, gn_sign ? e.chan_scale : nullptr);
             CE_CUDA(cudaGetLastError());
         }
     }
