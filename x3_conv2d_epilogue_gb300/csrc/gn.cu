@@ -35,11 +35,18 @@ struct GnArgs {
     int32_t *idx;
     int presel;      // 1: pmax already holds the extreme the slope's sign selects
     double inv_cnt;  // 1 / (C/groups * Ho * Wo)
+    float cnt;       // C/groups * Ho * Wo
     uint32_t per_magic;  // ceil(2^32 / (Hp * Wp)): exact f / (Hp * Wp) for f < 2^16
 };
 
+// the tensor-core path (presel) stores its partial sums as float pairs, the
+// fp32 CUDA-core path as doubles
 __device__ __forceinline__ void group_stats(const GnArgs &a, int n, int g, float &mean_f, float &rstd_f) {
-    gn_group_stats(a.gn.part, a.gn.units, a.groups, n, g, a.inv_cnt, a.eps, mean_f, rstd_f);
+    if (a.presel)
+        gn_group_stats_f(reinterpret_cast<const float *>(a.gn.part), a.gn.units, a.groups, n, g, a.cnt, a.eps, mean_f,
+                         rstd_f);
+    else
+        gn_group_stats(a.gn.part, a.gn.units, a.groups, n, g, a.inv_cnt, a.eps, mean_f, rstd_f);
 }
 
 // The tensor-core path's case: pmax holds, per channel, the extreme that the
@@ -111,13 +118,14 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
 }
 
 // One CTA per (image, group).  Warp 0 folds the group's per-unit partial sums
-// (fixed order, fp64: lanes take units lane, lane+32, ..., then a fixed
-// shuffle tree) into the mean and variance; the first C/groups threads turn
+// (fixed order: lanes take units lane, lane+32, ..., then a fixed shuffle
+// tree; fp64 for the fp32 path's double partials, double-float for the
+// tensor-core path's float pairs) into the mean and variance; the first C/groups threads turn
 // them into each channel's affine coefficients (fp32; rstd = 1/sqrt(var +
-// eps) from the fp64 variance).  Then the CTA writes the group's pooled
+// eps) from the variance).  Then the CTA writes the group's pooled
 // outputs, channel by channel (C/groups consecutive [Hp][Wp] planes:
-// contiguous loads and stores).  fp64 is kept to the fold: it is a slow pipe
-// on this part, so no per-output or per-thread fp64 work.
+// contiguous loads and stores).  fp64 is kept to the fp32 path's fold: it is
+// a slow pipe on this part, so no per-output or per-thread fp64 work.
 __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
     constexpr int kMaxCpg = 64;
     __shared__ float s_mean, s_rstd;
@@ -180,6 +188,7 @@ conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, 
     a.out = out, a.idx = e.index_out;
     a.presel = presel ? 1 : 0;
     a.inv_cnt = 1.0 / ((double)(a.C / a.groups) * a.Ho * a.Wo);
+    a.cnt = (float)((double)(a.C / a.groups) * a.Ho * a.Wo);
     const uint32_t per = (uint32_t)(h->gn.Hp * h->gn.Wp);
     a.per_magic = (uint32_t)((((uint64_t)1 << 32) + per - 1) / per);
     const unsigned blocks = (unsigned)(a.N * a.groups);

@@ -107,7 +107,7 @@ struct Cfg {
     int gn_fin;
     const float *beta;
     float eps, lo, hi;
-    double inv_cnt;       // 1 / (C/groups * Ho * Wo)
+    float cnt;            // C/groups * Ho * Wo
     uint32_t per_magic;   // ceil(2^32 / (Hp * Wp))
     uint32_t f4_magic;    // ceil(2^32 / F4), F4 = float4 per (image, group) block
 };
@@ -1281,10 +1281,14 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             if constexpr (kNB == 2) put_tile(1, pext1);
             epi_bar();
             if (ew == 2) {
-                // one warp: per group, the shuffled sums from both row slots,
-                // both column groups and (cpg = 64: two lane groups) both
-                // halves, loaded together and added in a fixed order
+                // one warp (the others go on to the band stores): per group,
+                // the shuffled sums from both row slots, both column groups
+                // and (cpg = 64: two lane groups) both halves, loaded together
+                // and added in a fixed order, stored as a float pair.  (Spread
+                // over all eight warps this fold measured slower: every
+                // warp's tail then waits on it.)
                 const int nci = gn_cpg / gn_cw;  // 1, or 2 when a group spans two warps' lanes
+                float *fpart = reinterpret_cast<float *>(a.gn.part);
                 for (int g = lane; g < a.groups; g += 32) {
                     float v0[8], v1[8];
 #pragma unroll
@@ -1302,9 +1306,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         if ((k & 1) < nci) s0 += v0[k], s1 += v1[k];
-                    double *dst = a.gn.part + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2;
-                    dst[0] = s0;
-                    dst[1] = s1;
+                    *reinterpret_cast<float2 *>(fpart + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2) =
+                        make_float2(s0, s1);
                 }
             }
 #pragma unroll
@@ -1404,7 +1407,8 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
         if (warp < nbp) {
             const int n = p / a.groups, g = p % a.groups;
             float mean, rstd;
-            gn_group_stats(a.gn.part, a.units_per_img, a.groups, n, g, a.inv_cnt, a.eps, mean, rstd);
+            gn_group_stats_f(reinterpret_cast<const float *>(a.gn.part), a.units_per_img, a.groups, n, g, a.cnt,
+                             a.eps, mean, rstd);
             for (int cl = lane; cl < cpg; cl += 32) {
                 const int c = g * cpg + cl;
                 gn_coeffs(__ldg(&a.gamma[c]), __ldg(&a.beta[c]), __ldg(&a.chan_scale[c]), mean, rstd,
@@ -1942,7 +1946,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
-        a.inv_cnt = 1.0 / ((double)(d.Cout / e.groups) * h->Ho * h->Wo);
+        a.cnt = (float)((double)(d.Cout / e.groups) * h->Ho * h->Wo);
         a.per_magic = (uint32_t)((((uint64_t)1 << 32) + per - 1) / per);
         const uint32_t F4 = F / 4 ? F / 4 : 1;
         a.f4_magic = (uint32_t)((((uint64_t)1 << 32) + F4 - 1) / F4);
