@@ -105,6 +105,7 @@ struct Cfg {
     int nhwc;       // channels-last input: tiles go straight into the B planes (no staging, no converters)
     // GroupNorm chain finalized inside this kernel (cooperative launch)
     int gn_fin;
+    uint32_t smem_bytes;  // the launch's dynamic shared memory (free for the finalize after the main loop)
     const float *beta;
     float eps, lo, hi;
     float cnt;            // C/groups * Ho * Wo
@@ -167,6 +168,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// shared -> global bulk copy (both addresses 16-byte aligned, size a multiple
+// of 16), tracked by bulk groups of the issuing thread
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the issuing thread's bulk stores have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // 4-D tiled TMA load; coordinates innermost first
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
                                             uint32_t bar) {
@@ -1347,20 +1357,28 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 // resident and a grid-wide arrival count is safe to wait on).  After every
 // CTA has stored its units' partial sums and pooled extremes and released
 // tensor memory, CTA b takes the (image, group) pairs b, b + gridDim.x, ...
-// in batches of one pair per warp: the warp folds the pair's statistics and
-// its channels' coefficients into shared memory, then all threads apply
-// z = clamp(A y + B) over the batch's pooled blocks (contiguous, F4 float4
-// each) with 16-byte loads and stores, sixteen in flight per thread (the
-// first sixteen issued before the statistics fold).  The
-// pooled extremes are read back from L2 rather than by a second launch.
+// in batches of up to one pair per warp, as many as the (now free) shared
+// memory holds.  Thread 0 bulk-copies the batch's pooled blocks (contiguous,
+// F4 float4 each) into shared memory, while one warp per pair folds its
+// statistics and its channels' coefficients; every thread then applies
+// z = clamp(A y + B) in place, and thread 0 bulk-copies the blocks out to
+// the output.  The copies keep the whole batch in flight at once, where
+// per-thread loads left the pass latency-bound.
 constexpr int kFinPairs = kThreads / 32;
+constexpr uint32_t kFinFlagOff = kFinPairs * 64 * 2 * 4;  // after the coefficient tables
+constexpr uint32_t kFinBarOff = kFinFlagOff + 8;
+constexpr uint32_t kFinBufOff = 8448;                     // the pooled blocks (128-byte aligned)
 __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, volatile int *abort_flag) {
-    // (the pipeline's shared memory is free now: coefficient tables and a flag)
     float *sA = reinterpret_cast<float *>(smem), *sB = sA + kFinPairs * 64;
-    int &s_go = *reinterpret_cast<int *>(sB + kFinPairs * 64);
+    int &s_go = *reinterpret_cast<int *>(smem + kFinFlagOff);
+    const uint32_t fbar = smem_u32(smem + kFinBarOff);
+    float4 *buf = reinterpret_cast<float4 *>(smem + kFinBufOff);
     __threadfence();  // this CTA's partials and pooled extremes, device-wide
+    fence_proxy_async_smem();  // this thread's earlier shared-memory accesses before the copies' writes
     __syncthreads();
     if (threadIdx.x == 0) {
+        mbar_init(fbar, 1);
+        fence_mbar_init();
         atomicAdd(a.gn.arrive, 1u);
         int go = 1;
         const uint64_t t0 = globaltimer();
@@ -1376,33 +1394,29 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
             __nanosleep(256);
         }
         __threadfence();
+        // the other CTAs' pooled extremes (generic stores, acquired above)
+        // are read below by bulk copies: order them for the async proxy too
+        asm volatile("fence.proxy.async.global;" ::: "memory");
         s_go = go && !*abort_flag;
     }
     __syncthreads();
     if (!s_go) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cpg = a.Cout / a.groups;
-    const uint32_t per = (uint32_t)(a.Hp * a.Wp), F4 = (uint32_t)cpg * per / 4u;
+    const uint32_t F4 = (uint32_t)cpg * (uint32_t)(a.Hp * a.Wp) / 4u, pbytes = F4 * 16u;
     const int npairs = a.N * a.groups;
-    const float4 *__restrict__ src = reinterpret_cast<const float4 *>(a.gn.pmax);
-    float4 *__restrict__ dst = reinterpret_cast<float4 *>(a.out);
-    constexpr int kV = 16;  // float4 loads in flight per thread
-    for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * kFinPairs) {
-        const int nbp = min(kFinPairs, (npairs - p0 + (int)gridDim.x - 1) / (int)gridDim.x);  // pairs in this batch
-        const uint32_t total = (uint32_t)nbp * F4;
-        float4 v[kV];
-        uint32_t jb[kV], fo[kV];
-        auto load_round = [&](uint32_t t0) {
-#pragma unroll
-            for (int k = 0; k < kV; ++k) {
-                const uint32_t t = t0 + (uint32_t)(k * kThreads) + threadIdx.x;
-                jb[k] = __umulhi(t, a.f4_magic);  // t / F4: the pair within the batch
-                fo[k] = t - jb[k] * F4;           // float4 within the pair's block
-                if (t < total) v[k] = src[(size_t)(p0 + (int)jb[k] * (int)gridDim.x) * F4 + fo[k]];
+    const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / pbytes));  // >= 1: checked on the host
+    uint32_t phase = 0;
+    for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * cap) {
+        const int nbp = min(cap, (npairs - p0 + (int)gridDim.x - 1) / (int)gridDim.x);  // pairs in this batch
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(fbar, (uint32_t)nbp * pbytes);
+            for (int j = 0; j < nbp; ++j) {
+                const char *src = reinterpret_cast<const char *>(a.gn.pmax) + (size_t)(p0 + j * (int)gridDim.x) * pbytes;
+                for (uint32_t off = 0; off < pbytes; off += 16384u)
+                    bulk_g2s(smem_u32(buf) + (uint32_t)j * pbytes + off, src + off, min(16384u, pbytes - off), fbar);
             }
-        };
-        // the first loads go out before the statistics: they do not need them
-        load_round(0);
+        }
         const int p = p0 + warp * (int)gridDim.x;
         if (warp < nbp) {
             const int n = p / a.groups, g = p % a.groups;
@@ -1415,25 +1429,35 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
                           sA[warp * 64 + cl], sB[warp * 64 + cl]);
             }
         }
-        __syncthreads();
-        for (uint32_t t0 = 0; t0 < total; t0 += kV * kThreads) {
-            if (t0 > 0) load_round(t0);
+        const bool landed = wait_bar(fbar, phase, abort_flag, a.err, false);
+        phase ^= 1u;
+        if (__syncthreads_or(!landed)) return;  // (also publishes the coefficients)
+        const uint32_t total = (uint32_t)nbp * F4;
+        for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
+            const uint32_t jb = __umulhi(t, a.f4_magic);  // t / F4: the pair within the batch
+            const float *cA = sA + jb * 64, *cB = sB + jb * 64;
+            const uint32_t e = 4u * (t - jb * F4);
+            const float4 v = buf[t];
+            float r[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int k = 0; k < kV; ++k) {
-                const uint32_t t = t0 + (uint32_t)(k * kThreads) + threadIdx.x;
-                if (t >= total) continue;
-                const float *cA = sA + jb[k] * 64, *cB = sB + jb[k] * 64;
-                const uint32_t e = 4u * fo[k];
-                float r[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
-                    r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
-                }
-                dst[(size_t)(p0 + (int)jb[k] * (int)gridDim.x) * F4 + fo[k]] = make_float4(r[0], r[1], r[2], r[3]);
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
+                r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
             }
+            buf[t] = make_float4(r[0], r[1], r[2], r[3]);
         }
-        __syncthreads();  // the next batch rewrites the coefficients
+        fence_proxy_async_smem();  // these writes before the copies' reads
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int j = 0; j < nbp; ++j) {
+                char *dst = reinterpret_cast<char *>(a.out) + (size_t)(p0 + j * (int)gridDim.x) * pbytes;
+                for (uint32_t off = 0; off < pbytes; off += 16384u)
+                    bulk_s2g(dst + off, smem_u32(buf) + (uint32_t)j * pbytes + off, min(16384u, pbytes - off));
+            }
+            bulk_commit();
+            bulk_wait_read();  // the buffer is read: the next batch (or the exit) may reuse it
+        }
+        __syncthreads();  // (and the next batch rewrites the coefficients)
     }
 }
 
@@ -1931,6 +1955,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.idesc = make_idesc(128, pl.P);
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
+    a.smem_bytes = pl.smem;
     a.drop_tile = h->test_drop_tile;
     h->test_drop_tile = -1;  // one forward only
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
@@ -1943,6 +1968,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         // channel offsets < 2^16); otherwise the separate finalize kernel
         const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
         a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
+                    F * 4u <= pl.smem - kFinBufOff &&  // one pooled block fits the finalize's buffer
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
