@@ -1082,7 +1082,16 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         }
         const int ab = j & 1;
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
-        if (epi_bar_any(!ok)) {  // all epilogue warps leave together
+        if constexpr (kGN) {
+            // the GroupNorm chain votes at the end of the unit's sums (below),
+            // so a warp that finished the previous unit's stores early starts
+            // this unit's loads without waiting for the others; a warp whose
+            // wait failed joins that vote here and leaves with the rest
+            if (!ok) {
+                epi_bar_any(true);
+                break;
+            }
+        } else if (epi_bar_any(!ok)) {  // all epilogue warps leave together
             prev_n = -1;
             break;
         }
@@ -1275,6 +1284,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // pooled tiles [band][2 row slots][64 channels][kPoolPitch] (window
             // extremes in gsg space); both slots write, one barrier, and the
             // stores fold the two slots
+            // every warp is past the previous unit's tile and statistics reads
+            // (and none has given up) before they are rewritten
+            if (epi_bar_any(false)) break;
             float *st = scratch + kNB * 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
             st[ew * 32 + lane] = gs;
             st[kEpiThreads + ew * 32 + lane] = gss;
@@ -1342,7 +1354,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     for (int i = 0; i < 64 / kEpiWarps; ++i) dst[i * cstep] = m[i];
                 }
             }
-            // (the barrier at the start of the next unit keeps the tile until all stores have read it)
+            // (the vote of the next unit keeps the tile until all stores have read it)
         }
     }
     if constexpr (kMin) {
