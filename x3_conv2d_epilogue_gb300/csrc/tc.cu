@@ -189,6 +189,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Programmatic dependent launch: the conv kernel is launched while the
+// small kernel before it (filter pack, row padding, output fill) still runs,
+// so its launch and prologue overlap that kernel; every thread of it waits
+// here for the preceding grid's completion and memory before its roles touch
+// global memory.  (A no-op when launched without the attribute.)
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // fp32 -> tf32 (10 explicit mantissa bits), round to nearest with ties away
 // from zero (the conversion instruction; measured cheaper here than the same
@@ -1517,6 +1524,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
     constexpr uint32_t tmem = 0;
     const bool tmem_ok = *tmem_slot == tmem;
     if (!tmem_ok && threadIdx.x == 0) atomicOr(a.err, ERRBIT_TMEM);
+    grid_dep_wait();
 
     if (!tmem_ok) {
         // nothing issued, nothing to drain
@@ -1557,7 +1565,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
 // sgn * (y - b) with sgn the sign of the channel's affine slope (negation is
 // exact, and tf32 rounding to nearest is symmetric).
 __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp, int Cin, int Cout, int Co, int S,
-                             const float *__restrict__ gamma, const float *__restrict__ scale) {
+                             const float *__restrict__ gamma, const float *__restrict__ scale,
+                             unsigned *__restrict__ reset) {
+    grid_dep_launch();
+    if (reset && blockIdx.x == 0 && threadIdx.x == 0) *reset = 0u;  // the conv kernel's grid-wide arrival count
     const int planes = 2 * S + 1;
     const int Cpad = (Cin + 7) / 8 * 8;
     const size_t total = (size_t)Cpad * 3 * planes * Cout;  // = chunks*3*2*planes*Cout*4
@@ -1586,6 +1597,7 @@ __global__ void pack_weights(const float *__restrict__ w, float *__restrict__ wp
 
 // the min chains' output before channel tiles take their atomic minima
 __global__ void fill_f32(float *__restrict__ p, size_t n, float v) {
+    grid_dep_launch();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = v;
 }
 
@@ -1594,6 +1606,7 @@ __global__ void fill_f32(float *__restrict__ p, size_t n, float v) {
 // columns are left unwritten: the tensor map's row extent stays W, so the
 // tensor load never reads them (it fills zeros past W).
 __global__ void pad_rows(const float *__restrict__ x, float *__restrict__ xp, size_t rows, int W, int Wp) {
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const size_t warps = ((size_t)gridDim.x * blockDim.x) >> 5;
     for (size_t r = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
@@ -1761,22 +1774,38 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
     const bool general = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? args.c.U == 4 : (args.c.CT > 1 || args.c.MT > 1);
     auto k = general ? tc_conv_epi<KIND, true> : tc_conv_epi<KIND, false>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
+    // The in-kernel finalize waits for every CTA: a cooperative launch
+    // guarantees they are all resident (one per SM, grid <= SM count).  Where
+    // the device refuses it (fewer SMs granted to this context), the caller
+    // runs the separate finalize kernel instead.  Every launch also allows
+    // programmatic dependent launch on the kernel before it (see
+    // grid_dep_wait); a launch refused with both attributes is retried
+    // without that one.  (Measured per chain: C4 -3 us, C5 -2 us, the 32x32
+    // case -4 us; the per-channel chains ran slower with it, C3 581 -> 587 us,
+    // so they launch without it.)
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    constexpr bool kPdl = KIND != CONV_EPI_MUL_LRELU_GELU && KIND != CONV_EPI_NONE;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na++].val.programmaticStreamSerializationAllowed = kPdl ? 1 : 0;
     if (args.c.gn_fin) {
-        // the in-kernel finalize waits for every CTA: a cooperative launch
-        // guarantees they are all resident (one per SM, grid <= SM count).
-        // Where the device refuses it (fewer SMs granted to this context),
-        // the caller runs the separate finalize kernel instead.
-        void *kargs[] = {const_cast<TcArgs *>(&args)};
-        const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3(grid),
-                                                          dim3(kThreads), kargs, pl.smem, s);
-        if (e == cudaErrorCooperativeLaunchTooLarge) {
-            (void)cudaGetLastError();
-            return CONV_EPI_ERR_UNSUPPORTED;
-        }
-        CE_CUDA(e);
-    } else {
-        k<<<grid, kThreads, pl.smem, s>>>(args);
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na++].val.cooperative = 1;
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid), cfg.blockDim = dim3(kThreads), cfg.dynamicSmemBytes = pl.smem, cfg.stream = s;
+    cfg.attrs = attr, cfg.numAttrs = (unsigned)na;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, args);
+    if (e != cudaSuccess && e != cudaErrorCooperativeLaunchTooLarge) {
+        (void)cudaGetLastError();
+        cfg.attrs = attr + 1, cfg.numAttrs = (unsigned)(na - 1);
+        e = cudaLaunchKernelEx(&cfg, k, args);
+    }
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        (void)cudaGetLastError();
+        return CONV_EPI_ERR_UNSUPPORTED;
+    }
+    CE_CUDA(e);
     CE_CUDA(cudaGetLastError());
     return CONV_EPI_OK;
 }
@@ -1941,7 +1970,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
             const bool gn_sign = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP;  // (fused: one channel tile)
             pack_weights<<<blocks, threads, 0, s>>>(w + (size_t)m * Cg * d.Cin * 9, h->wpack + (size_t)m * total,
                                                     d.Cin, Cg, min(Cg, d.Cout - m * Cg), pl.S,
-                                                    gn_sign ? e.gamma : nullptr, gn_sign ? e.chan_scale : nullptr);
+                                                    gn_sign ? e.gamma : nullptr, gn_sign ? e.chan_scale : nullptr,
+                                                    m == 0 && gn_sign ? h->gn.arrive : nullptr);
             CE_CUDA(cudaGetLastError());
         }
     }
@@ -1988,7 +2018,6 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         a.per_magic = (uint32_t)((((uint64_t)1 << 32) + per - 1) / per);
         const uint32_t F4 = F / 4 ? F / 4 : 1;
         a.f4_magic = (uint32_t)((((uint64_t)1 << 32) + F4 - 1) / F4);
-        if (a.gn_fin) CE_CUDA(cudaMemsetAsync(h->gn.arrive, 0, sizeof(unsigned), s));
     }
     const int grid = a.total_units < h->sm_count ? a.total_units : h->sm_count;
     int fills = 0;
