@@ -157,9 +157,10 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *   CONV_EPI_MODE_TF32: any N, Cin, Cout and H, W >= 3.
  *     GN chain: fused into the conv kernel for Cout = 64, pool_k = 4 and
  *     W <= 64 or 98 <= W <= 128; any other GN shape runs as two passes, the tensor-core conv
- *     writing y (bias added) into a handle-owned buffer of N*Cout*Ho*Wo
- *     floats (allocated by conv_epi_reserve or the first GN forward), then
- *     the chain's post-pass in fp32 (as conv_epi_postpass).
+ *     writing y (bias added) and its per-unit sums of y and y^2 into a
+ *     handle-owned buffer (conv_epi_plan.ybuf_bytes; allocated by
+ *     conv_epi_reserve or the first GN forward), then the statistics folded
+ *     from those sums and the normalise-scale-pool-clamp pass over y (fp32).
  *     Rows wider than 256 run as column tiles, more than 128 output channels
  *     as channel tiles.  NCHW rows whose W is not a multiple of 4 are first
  *     copied, by a small kernel, into a handle-owned buffer of rows padded to
@@ -311,7 +312,8 @@ typedef struct {
     int64_t xpad_bytes;      /* the handle's padded copy of x (0 unless NCHW rows need it) */
     int64_t gn_two_pass;     /* 1: a GroupNorm shape the fused epilogue does not take; the plan is
                                 that of the plain conv (CONV_EPI_NONE), its first pass */
-    int64_t ybuf_bytes;      /* the handle's buffer of the conv output for that two-pass form (else 0) */
+    int64_t ybuf_bytes;      /* the handle's buffer for that two-pass form (else 0): the conv output, then
+                                the conv kernel's per-unit sums of y and y^2 that the statistics fold */
 } conv_epi_plan;
 
 /* Fill *plan for desc (mode must be CONV_EPI_MODE_TF32) and epi.  Returns

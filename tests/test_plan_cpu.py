@@ -175,7 +175,14 @@ def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k):
     between them."""
     two_pass = kind == ce.GN_SCALE_POOL_CLAMP and not gn_fused(kind, Cout, W, pool_k)
     assert q["gn_two_pass"] == int(two_pass)
-    assert q["ybuf_bytes"] == (N * Cout * (H - 2) * (W - 2) * 4 if two_pass else 0)
+    # the conv output, then (256-byte aligned) the conv kernel's per-unit sums:
+    # (image, unit, 2 column groups, 128 accumulator rows) float pairs
+    if two_pass:
+        ybytes = -(-(N * Cout * (H - 2) * (W - 2) * 4) // 256) * 256
+        units = q["units_per_image"]
+        assert q["ybuf_bytes"] == ybytes + N * units * 2 * 128 * 8
+    else:
+        assert q["ybuf_bytes"] == 0
     check_plan(q, N, Cin, H, W, Cout, ce.NONE if two_pass else kind, layout)
 
 

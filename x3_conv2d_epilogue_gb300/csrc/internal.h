@@ -138,6 +138,12 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
 // The chain as a separate pass over a stored conv output (postpass.cu), and
 // the buffer of its GroupNorm statistics, N * groups (mean, rstd) pairs.
 conv_epi_status ensure_post_stats(conv_epi_handle h, int groups);
+// The GroupNorm chain's second pass for the two-pass tensor-core form: the
+// statistics folded from the conv kernel's per-unit sums (ystat, units per
+// image upi, S accumulator row slots, MT channel tiles of Cg), then the
+// normalise-scale-pool-clamp pass over y.
+conv_epi_status postpass_gn_units(conv_epi_handle h, const float *y, const float2 *ystat, int upi, int S, int MT, int Cg,
+                                  const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
 conv_epi_status postpass_forward(conv_epi_handle h, const float *y, const conv_epi_epilogue_desc &e, float *out,
                                  cudaStream_t s);
 

@@ -147,6 +147,48 @@ __global__ void __launch_bounds__(kThreads) post_gn_pool(const float *__restrict
     }
 }
 
+// The same statistics from the two-pass tensor-core form's per-unit sums:
+// ystat[n][u][hc][L] = (sum y, sum y^2) of accumulator row L's valid outputs
+// in unit u (column group hc); row L of a unit holds channel
+// mt * Cg + L % Cg (mt: the unit's channel tile), so group g's entries are
+// its cpg channels' rows of every row slot s < S, in the units of their
+// tile.  Per-thread fp32 sums over a strided slice, then the CTA's threads in
+// fp64 in a fixed order, as above.
+__global__ void __launch_bounds__(kThreads) post_gn_stats_units(const float2 *__restrict__ ystat, float *__restrict__ stats,
+                                                               int groups, int cpg, int upi, int S, int MT, int Cg,
+                                                               double inv_cnt, float eps) {
+    __shared__ double ws[2][kThreads / 32];
+    const int n = blockIdx.x / groups, g = blockIdx.x % groups;
+    const int per_unit = cpg * S * 2;  // entries of group g in one unit
+    const int total = per_unit * upi;
+    float s = 0.0f, ss = 0.0f;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int u = i / per_unit, r = i - u * per_unit;
+        const int cl = r % cpg, sl = (r / cpg) % S, hc = r / (cpg * S);
+        const int c = g * cpg + cl;
+        if (MT > 1 && u % MT != c / Cg) continue;  // another channel tile's unit
+        const float2 v = __ldg(&ystat[(((size_t)n * upi + u) * 2 + hc) * 128 + sl * Cg + c % Cg]);
+        s += v.x, ss += v.y;
+    }
+    double ds = s, dss = ss;
+    for (int o = 16; o >= 1; o >>= 1) {
+        ds += __shfl_xor_sync(0xffffffffu, ds, o);
+        dss += __shfl_xor_sync(0xffffffffu, dss, o);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) ws[0][warp] = ds, ws[1][warp] = dss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0, tt = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) t += ws[0][w], tt += ws[1][w];
+        const double mean = t * inv_cnt;
+        double var = tt * inv_cnt - mean * mean;
+        if (var < 0.0) var = 0.0;
+        stats[2 * blockIdx.x] = (float)mean;
+        stats[2 * blockIdx.x + 1] = rsqrtf((float)var + eps);
+    }
+}
+
 unsigned blocks_for(size_t work, int sm_count) {
     const size_t b = (work + kThreads - 1) / kThreads;
     const size_t cap = (size_t)sm_count * 8;
@@ -166,6 +208,25 @@ conv_epi_status ensure_post_stats(conv_epi_handle h, int groups) {
         CE_CUDA(cudaMalloc(&h->post, need));
         h->post_bytes = need;
     }
+    return CONV_EPI_OK;
+}
+
+conv_epi_status postpass_gn_units(conv_epi_handle h, const float *y, const float2 *ystat, int upi, int S, int MT, int Cg,
+                                  const conv_epi_epilogue_desc &e, float *out, cudaStream_t s) {
+    const conv_epi_desc &d = h->d;
+    const size_t plane = (size_t)h->Ho * h->Wo;
+    conv_epi_status st = ensure_post_stats(h, e.groups);
+    if (st) return st;
+    const int cpg = d.Cout / e.groups;
+    post_gn_stats_units<<<(unsigned)(d.N * e.groups), kThreads, 0, s>>>(ystat, h->post, e.groups, cpg, upi, S, MT, Cg,
+                                                                       1.0 / ((double)cpg * plane), e.eps);
+    CE_CUDA(cudaGetLastError());
+    const int Hp = (h->Ho - e.pool_k) / e.pool_k + 1, Wp = (h->Wo - e.pool_k) / e.pool_k + 1;
+    post_gn_pool<<<blocks_for((size_t)d.N * d.Cout * Hp * Wp, h->sm_count), kThreads, 0, s>>>(
+        y, out, h->post, e.gamma, e.beta, e.chan_scale, d.N, d.Cout, e.groups, h->Ho, h->Wo, e.pool_k, Hp, Wp,
+        e.clamp_lo, e.clamp_hi);
+    CE_CUDA(cudaGetLastError());
+    h->last_launches = 2;
     return CONV_EPI_OK;
 }
 

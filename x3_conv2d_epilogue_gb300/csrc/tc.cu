@@ -74,6 +74,9 @@ constexpr int kAccStride = 256;     // columns per accumulator buffer
 constexpr int kMaxRing = 4;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kPoolPitch = 33;      // GroupNorm pooled tile pitch (floats)
+// Internal kind: the conv output y (as CONV_EPI_NONE) plus each thread's sums
+// of y and y^2 per unit, the first pass of the two-pass GroupNorm form.
+constexpr int kKindConvStats = 6;
 constexpr int kMaxQ = 8;            // min chains: quadrant partials of a column loaded together
 
 // Scalar kernel configuration.  The kernel copies it out of the parameter
@@ -105,7 +108,10 @@ struct Cfg {
     int nhwc;       // channels-last input: tiles go straight into the B planes (no staging, no converters)
     // GroupNorm chain finalized inside this kernel (cooperative launch)
     int gn_fin;
-    uint32_t smem_bytes;  // the launch's dynamic shared memory (free for the finalize after the main loop)
+    uint32_t smem_bytes;
+    // kKindConvStats: per (image, unit, column group, accumulator row) the sums
+    // of y and y^2 over the thread's valid outputs, as float pairs
+    float2 *ystat;  // the launch's dynamic shared memory (free for the finalize after the main loop)
     const float *beta;
     float eps, lo, hi;
     float cnt;            // C/groups * Ho * Wo
@@ -873,7 +879,8 @@ __device__ __forceinline__ int stg_at(int r, int c) { return r * 16 + 4 * ((c >>
 template <int KIND>
 __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, float bias, float mult, int lane, int qd,
                                                int ew, bool row_ok, bool v4, int col0, float *o4, float *o2,
-                                               size_t cstride, int wv, int co_left, float *scratch) {
+                                               size_t cstride, int wv, int co_left, float *scratch, float &ys,
+                                               float &yss) {
     float *stg = scratch + ew * 32 * 16;
     {
         const uint64_t bias2 = pack2f(bias, bias), mult2 = pack2f(mult, mult), slope2 = pack2f(a.slope, a.slope);
@@ -881,7 +888,7 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
         float2 v[8];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-            if constexpr (KIND == CONV_EPI_NONE) {
+            if constexpr (KIND == CONV_EPI_NONE || KIND == kKindConvStats) {
                 // the conv output itself: acc + bias
                 v[i / 2] = unpack2(add2u(pack2(f.r[i], f.r[i + 1]), bias2));
             } else {
@@ -896,6 +903,21 @@ __device__ __forceinline__ void epi_chunk_chan(const Cfg &a, const Frag16 &f, fl
         for (int g = 0; g < 4; ++g)
             *reinterpret_cast<float4 *>(stg + stg_at(lane, 4 * g)) =
                 make_float4(v[2 * g].x, v[2 * g].y, v[2 * g + 1].x, v[2 * g + 1].y);
+        if constexpr (KIND == kKindConvStats) {
+            // this channel's sums over the chunk's valid outputs
+            if (row_ok) {
+                if (col0 + 16 <= wv) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ys += v[i].x + v[i].y, yss = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, yss));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (col0 + 2 * i < wv) ys += v[i].x, yss = fmaf(v[i].x, v[i].x, yss);
+                        if (col0 + 2 * i + 1 < wv) ys += v[i].y, yss = fmaf(v[i].y, v[i].y, yss);
+                    }
+                }
+            }
+        }
     }
     __syncwarp();
     if (row_ok) {
@@ -1088,6 +1110,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             }
         }
         const int ab = j & 1;
+        float ys = 0.0f, yss = 0.0f;  // kKindConvStats: this thread's sums over the unit
         const bool ok = wait_bar(bars.acc_full(ab), (j >> 1) & 1, abort_flag, a.err);
         if constexpr (kGN) {
             // the GroupNorm chain votes at the end of the unit's sums (below),
@@ -1256,7 +1279,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     const bool more = cc + 2 < nchunks;
                     if (more) tmem_ld16_issue(tb + (cc + 2) * 16, nxt);
                     epi_chunk_chan<KIND>(a, cur, bias, mult, lane, qd, ew, row_ok, v4, cc * 16, o4, o2, plane, wv,
-                                         a.Co - cbase, scratch);
+                                         a.Co - cbase, scratch, ys, yss);
                     if (more) {
                         tmem_ld_wait(nxt);
                         cur = nxt;
@@ -1269,6 +1292,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.acc_empty(ab));
+        if constexpr (KIND == kKindConvStats) {
+            // (image, unit, column group hc, accumulator row L): coalesced float pairs
+            a.ystat[(((size_t)n * a.units_per_img + ru) * 2 + hc) * 128 + L] = make_float2(ys, yss);
+        }
 
         if constexpr (kMin) {
             // this unit's partial minima are in scratch; they are combined
@@ -1640,6 +1667,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
         return (uint32_t)(U * 4 * P * sizeof(float));
     case CONV_EPI_MUL_LRELU_GELU:
     case CONV_EPI_NONE:
+    case kKindConvStats:
         return (uint32_t)(kEpiWarps * 32 * 16 * sizeof(float));  // a 32 x 16 staging tile per warp
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
@@ -1785,7 +1813,7 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
     // so they launch without it.)
     cudaLaunchAttribute attr[2];
     int na = 0;
-    constexpr bool kPdl = KIND != CONV_EPI_MUL_LRELU_GELU && KIND != CONV_EPI_NONE;
+    constexpr bool kPdl = KIND != CONV_EPI_MUL_LRELU_GELU && KIND != CONV_EPI_NONE && KIND != kKindConvStats;
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na++].val.programmaticStreamSerializationAllowed = kPdl ? 1 : 0;
     if (args.c.gn_fin) {
@@ -1834,7 +1862,20 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
     return CONV_EPI_OK;
 }
 
-size_t tc_ybuf_bytes(const conv_epi_desc &d) { return (size_t)d.N * d.Cout * (d.H - 2) * (d.W - 2) * sizeof(float); }
+// The two-pass form's buffer: the conv output y [N][Cout][Ho][Wo], then (from
+// a 256-byte boundary) the conv kernel's per-unit sums
+// [N][units per image][2 column groups][128 accumulator rows] float pairs.
+size_t tc_y_bytes(const conv_epi_desc &d) {
+    return ((size_t)d.N * d.Cout * (d.H - 2) * (d.W - 2) * sizeof(float) + 255) & ~(size_t)255;
+}
+int tc_stat_units(const conv_epi_desc &d) {
+    Plan pl;
+    if (!make_plan(d, kKindConvStats, pl)) return 0;
+    return (d.H - 2 + pl.RU - 1) / pl.RU * pl.CT * pl.MT;
+}
+size_t tc_ybuf_bytes(const conv_epi_desc &d) {
+    return tc_y_bytes(d) + (size_t)d.N * tc_stat_units(d) * 2 * 128 * sizeof(float2);
+}
 
 size_t tc_xpad_bytes(const conv_epi_desc &d) {
     if (d.mode != CONV_EPI_MODE_TF32 || !needs_xpad(d)) return 0;
@@ -1911,12 +1952,16 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         if (!h->ybuf || h->ybuf_bytes < tc_ybuf_bytes(d) || h->post_bytes < (size_t)d.N * e.groups * 2 * sizeof(float))
             return CONV_EPI_ERR_INVALID_ARG;  // conv_epi_reserve sizes both
         conv_epi_epilogue_desc plain = e;
-        plain.kind = CONV_EPI_NONE;
+        plain.kind = kKindConvStats;  // y, and each unit's sums of y and y^2 per channel
         plain.index_out = nullptr;
         conv_epi_status st = tc_forward(h, x, w, b, plain, h->ybuf, s);
         if (st) return st;
         const int conv_launches = h->last_launches;
-        if ((st = postpass_forward(h, h->ybuf, e, out, s))) return st;
+        Plan pl;
+        if (!make_plan(d, kKindConvStats, pl)) return CONV_EPI_ERR_UNSUPPORTED;
+        const float2 *ystat = reinterpret_cast<const float2 *>(reinterpret_cast<const char *>(h->ybuf) + tc_y_bytes(d));
+        if ((st = postpass_gn_units(h, h->ybuf, ystat, tc_stat_units(d), pl.S, pl.MT, gemm_cout(d.Cout), e, out, s)))
+            return st;
         h->last_launches += conv_launches;
         return CONV_EPI_OK;
     }
@@ -1998,6 +2043,9 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
     a.smem_bytes = pl.smem;
+    a.ystat = e.kind == kKindConvStats
+                  ? reinterpret_cast<float2 *>(reinterpret_cast<char *>(h->ybuf) + tc_y_bytes(d))
+                  : nullptr;
     a.drop_tile = h->test_drop_tile;
     h->test_drop_tile = -1;  // one forward only
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
@@ -2034,6 +2082,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     case CONV_EPI_SCALE_MIN: st = launch_tc<CONV_EPI_SCALE_MIN>(args, pl, grid, s); break;
     case CONV_EPI_MUL_LRELU_GELU: st = launch_tc<CONV_EPI_MUL_LRELU_GELU>(args, pl, grid, s); break;
     case CONV_EPI_NONE: st = launch_tc<CONV_EPI_NONE>(args, pl, grid, s); break;
+    case kKindConvStats: st = launch_tc<kKindConvStats>(args, pl, grid, s); break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP:
         st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
         if (st == CONV_EPI_ERR_UNSUPPORTED && a.gn_fin) {  // cooperative launch refused: finalize separately
