@@ -65,9 +65,11 @@ SMALL = {
     "c5_w107": W["c5_gn_pool_clamp"].resized(N=1, H=13, W=107),              # fused, chunk 6 ragged at column 105
     "c5_w90": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=90),                # one band of 96 columns: two passes in tf32
     "min_w3": W["pr1_min_tanh2"].resized(N=2, Cin=2, H=3, W=3, Cout=1),      # a single output per image
-    # GroupNorm shapes the fused tf32 epilogue does not take (tf32: the conv,
-    # then the chain's post-pass, through a handle-owned buffer of y)
-    "c5_co32": W["c5_gn_pool_clamp"].resized(N=2, H=18, W=64, Cout=32, groups=8),     # Cout 32, 4 channels per group
+    # GroupNorm shapes beyond the page's (tf32: fused where the epilogue takes
+    # them, else the conv then the chain's post-pass through a buffer of y)
+    "c5_co32": W["c5_gn_pool_clamp"].resized(N=2, H=18, W=64, Cout=32, groups=8),     # Cout 32 (fused: 32 zero filters)
+    "c5_co16_w128": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=128, Cout=16, groups=2),  # Cout 16, one band, 8 per group
+    "c5_co48": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=48, groups=16),    # 3 channels per group: two passes
     "c5_co128": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=96, Cout=128, groups=16),  # Cout 128
     "c5_co256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=256, groups=32),  # 2 channel tiles
     "c5_k2": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=50, pool_k=2),               # 2 x 2 windows, odd tail row

@@ -160,20 +160,23 @@ def test_plans_of_tested_shapes(case, layout):
             plan(*args, groups=wl.groups, pool_k=wl.pool_k)
         assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
         return
-    check_gn_form(plan(*args, groups=wl.groups, pool_k=wl.pool_k), *args, pool_k=wl.pool_k)
+    check_gn_form(plan(*args, groups=wl.groups, pool_k=wl.pool_k), *args, pool_k=wl.pool_k, groups=wl.groups)
 
 
-def gn_fused(kind, Cout, W, pool_k):
+def gn_fused(kind, Cout, W, pool_k, groups):
     # rows of up to 64 columns run as two pooling bands per unit; wider rows as
-    # one band, fused when the first 96 output columns are whole (Wo >= 96)
-    return kind == ce.GN_SCALE_POOL_CLAMP and Cout == 64 and pool_k == 4 and (W <= 64 or 98 <= W <= 128)
+    # one band, fused when the first 96 output columns are whole (Wo >= 96);
+    # up to 64 channels (a 64-channel GEMM), a group's channels a power of two
+    cpg = Cout // groups
+    return (kind == ce.GN_SCALE_POOL_CLAMP and Cout <= 64 and cpg & (cpg - 1) == 0 and pool_k == 4
+            and (W <= 64 or 98 <= W <= 128))
 
 
-def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k):
+def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
     """A GroupNorm shape the fused epilogue does not take runs as two passes:
     its plan is the plain conv's, and the handle holds the conv output
     between them."""
-    two_pass = kind == ce.GN_SCALE_POOL_CLAMP and not gn_fused(kind, Cout, W, pool_k)
+    two_pass = kind == ce.GN_SCALE_POOL_CLAMP and not gn_fused(kind, Cout, W, pool_k, groups)
     assert q["gn_two_pass"] == int(two_pass)
     # the conv output, then (256-byte aligned) the conv kernel's per-unit sums:
     # (image, unit, 2 column groups, 128 accumulator rows) float pairs
@@ -189,7 +192,8 @@ def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k):
 def test_random_shapes_all_planned_and_in_range():
     """Every shape with H, W >= 3 has a plan (the tf32 mode takes any size),
     and every plan passes the range checks; GroupNorm shapes are fused
-    exactly when Cout = 64, pool_k = 4 and W <= 64 or 98 <= W <= 128, and otherwise planned as
+    exactly when Cout <= 64 (groups of a power-of-two size), pool_k = 4 and W <= 64 or
+    98 <= W <= 128, and otherwise planned as
     the plain conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):
@@ -211,7 +215,7 @@ def test_random_shapes_all_planned_and_in_range():
             H = max(H, pool_k + 2)
             W = max(W, pool_k + 2)
         args = (N, Cin, H, W, Cout, kind, layout)
-        check_gn_form(plan(*args, groups=groups, pool_k=pool_k), *args, pool_k=pool_k)
+        check_gn_form(plan(*args, groups=groups, pool_k=pool_k), *args, pool_k=pool_k, groups=groups)
 
 
 def test_plan_query_arguments():

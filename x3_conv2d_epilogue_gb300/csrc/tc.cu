@@ -989,7 +989,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     float mult = KIND == CONV_EPI_MUL_LRELU_GELU && co < a.Co ? __ldg(&a.chan_scale[co]) : 0.0f;
     // GroupNorm chain: the sign of the channel's affine slope gamma * scale
     // (rstd > 0), folded into the packed filter: the accumulator is gsg * (y - b)
-    const float gsg = kGN && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
+    const float gsg =
+        kGN && co < a.Co && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
     // min chains: scalar * bias of the four channels this thread holds in a
     // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4),
     // each duplicated into a register pair, and the scalar likewise.  The
@@ -1016,7 +1017,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // GroupNorm chain: group size, lanes per group inside a warp, and the sign
     // table of the pooled extremes (a 64-float array after the tiles, written
     // here and first read after the first combine barrier)
-    const int gn_cpg = kGN ? a.Cout / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
+    // (groups of the problem's Co <= 64 channels; the GEMM's channels Co..63
+    // are zero filters whose sums and extremes are never read)
+    const int gn_cpg = kGN ? a.Co / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
     // pooling bands of 4 rows per unit: one (rows of 80..128 columns: two u
     // of two row slots) or, in the general instantiation, two (rows of up to
     // 64 columns: four u); 16-column chunks per warp and u: 4 or 2
@@ -1375,7 +1378,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     // the sign restored; all sixteen tile reads go out before
                     // the stores
                     const float *pt0 = scratch + band * 2 * 64 * kPoolPitch, *pt1 = pt0 + 64 * kPoolPitch;
-                    float *dst = a.gn.pmax + (((size_t)n * a.Cout + ew) * a.Hp + prow) * a.Wp + lane;
+                    float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp + lane;
                     const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
                     float m[64 / kEpiWarps];
 #pragma unroll
@@ -1385,7 +1388,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                                     gn_bias[c2]);
                     }
 #pragma unroll
-                    for (int i = 0; i < 64 / kEpiWarps; ++i) dst[i * cstep] = m[i];
+                    for (int i = 0; i < 64 / kEpiWarps; ++i)
+                        if (ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
                 }
             }
             // (the vote of the next unit keeps the tile until all stores have read it)
@@ -1448,7 +1452,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     __syncthreads();
     if (!s_go) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cpg = a.Cout / a.groups;
+    const int cpg = a.Co / a.groups;
     const uint32_t F4 = (uint32_t)cpg * (uint32_t)(a.Hp * a.Wp) / 4u, pbytes = F4 * 16u;
     const int npairs = a.N * a.groups;
     const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / pbytes));  // >= 1: checked on the host
@@ -1850,7 +1854,10 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     if (!make_plan(d, CONV_EPI_GN_SCALE_POOL_CLAMP, pl)) return false;
     const bool one_band = pl.RU == 4 && pl.P > 64 && pl.P <= 128 && d.W - 2 >= 96;
     const bool two_bands = pl.RU == 8 && pl.P == 64;
-    return e.pool_k == 4 && (one_band || two_bands) && pl.S == 2 && d.Cout == 64;
+    // (Cout below 64 runs as a 64-channel GEMM with zero filters; a group's
+    // channels must be a power-of-two run of lanes for the shuffle sums)
+    const int cpg = d.Cout / e.groups;
+    return e.pool_k == 4 && (one_band || two_bands) && pl.S == 2 && d.Cout <= 64 && (cpg & (cpg - 1)) == 0;
 }
 
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
