@@ -70,7 +70,10 @@ SMALL = {
     "c5_co32": W["c5_gn_pool_clamp"].resized(N=2, H=18, W=64, Cout=32, groups=8),     # Cout 32 (fused: 32 zero filters)
     "c5_co16_w128": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=128, Cout=16, groups=2),  # Cout 16, one band, 8 per group
     "c5_co48": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=48, groups=16),    # 3 channels per group: two passes
-    "c5_co128": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=96, Cout=128, groups=16),  # Cout 128
+    "c5_co128": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=96, Cout=128, groups=16),  # Cout 128, W 96: two passes
+    "c5_co128_w128": W["c5_gn_pool_clamp"].resized(N=2, H=15, W=128, Cout=128, groups=16),  # fused, half bands, a stats-only row
+    "c5_co96_w100": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=100, Cout=96, groups=12),  # fused, 32 zero filters, P 112
+    "c5_co128_g2": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=110, Cout=128, groups=2),   # fused, 64 channels per group
     "c5_co256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=256, groups=32),  # 2 channel tiles
     "c5_k2": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=50, pool_k=2),               # 2 x 2 windows, odd tail row
     "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling

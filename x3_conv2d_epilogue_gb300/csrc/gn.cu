@@ -34,6 +34,7 @@ struct GnArgs {
     float *out;
     int32_t *idx;
     int presel;      // 1: pmax already holds the extreme the slope's sign selects
+    int half;        // with presel: pmax and pmin hold it for the two halves of each band
     double inv_cnt;  // 1 / (C/groups * Ho * Wo)
     float cnt;       // C/groups * Ho * Wo
     uint32_t per_magic;  // ceil(2^32 / (Hp * Wp)): exact f / (Hp * Wp) for f < 2^16
@@ -65,13 +66,17 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
     const uint32_t per = (uint32_t)(a.gn.Hp * a.gn.Wp);
     const size_t base = ((size_t)n * a.C + (size_t)g * cpg) * per;
     const float4 *__restrict__ src = reinterpret_cast<const float4 *>(a.gn.pmax + base);
+    const float4 *__restrict__ src2 = reinterpret_cast<const float4 *>(a.gn.pmin + base);  // (half bands)
     float4 *__restrict__ dst = reinterpret_cast<float4 *>(a.out + base);
     const int nv = (int)((size_t)cpg * per / 4);
-    float4 v[kVec];
+    float4 v[kVec], w[kVec];
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
         const int i = threadIdx.x + k * kThreads;
-        if (i < nv) v[k] = src[i];
+        if (i < nv) {
+            v[k] = src[i];
+            if (a.half) w[k] = src2[i];
+        }
     }
     if (threadIdx.x < 32) {
         // the channel parameters (at most two channels per lane) are loaded
@@ -94,8 +99,10 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
         }
     }
     __syncthreads();
-    auto apply = [&](float y, uint32_t f) {
+    // (half bands: the band's extreme from its halves, by the slope's sign)
+    auto apply = [&](float y, float y2, uint32_t f) {
         const uint32_t cl = __umulhi(f, a.per_magic);  // f / per
+        if (a.half) y = sA[cl] >= 0.0f ? fmaxf(y, y2) : fminf(y, y2);
         return fminf(fmaxf(fmaf(sA[cl], y, sB[cl]), a.lo), a.hi);
     };
     for (int i0 = 0; i0 < nv; i0 += kVec * kThreads) {
@@ -103,7 +110,10 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
 #pragma unroll
             for (int k = 0; k < kVec; ++k) {
                 const int i = i0 + threadIdx.x + k * kThreads;
-                if (i < nv) v[k] = src[i];
+                if (i < nv) {
+                    v[k] = src[i];
+                    if (a.half) w[k] = src2[i];
+                }
             }
         }
 #pragma unroll
@@ -111,7 +121,8 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
             const int i = i0 + threadIdx.x + k * kThreads;
             if (i < nv) {
                 const uint32_t f = 4u * (uint32_t)i;
-                dst[i] = make_float4(apply(v[k].x, f), apply(v[k].y, f + 1), apply(v[k].z, f + 2), apply(v[k].w, f + 3));
+                dst[i] = make_float4(apply(v[k].x, w[k].x, f), apply(v[k].y, w[k].y, f + 1), apply(v[k].z, w[k].z, f + 2),
+                                     apply(v[k].w, w[k].w, f + 3));
             }
         }
     }
@@ -153,6 +164,7 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
             const float A = sA[cl], B = sB[cl];
             const size_t base = ((size_t)n * a.C + c) * per;
             const float *__restrict__ src = ((a.presel || A >= 0.0f) ? a.gn.pmax : a.gn.pmin) + base;
+            const float *__restrict__ src2 = a.gn.pmin + base;  // (half bands: the second half)
             float *__restrict__ dst = a.out + base;
             if (a.idx) {
                 const int32_t *__restrict__ isrc = (A > 0.0f ? a.gn.amax : a.gn.amin) + base;
@@ -161,16 +173,21 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
                     a.idx[base + p] = A != 0.0f ? isrc[p] : 0;
                 }
             } else {
-                // four independent loads in flight per thread
+                // four independent loads in flight per thread (half bands:
+                // each the extreme of the band's two halves by the slope's sign)
+                auto y_at = [&](int q) {
+                    const float y = src[q];
+                    return a.half ? (A >= 0.0f ? fmaxf(y, src2[q]) : fminf(y, src2[q])) : y;
+                };
                 int p = threadIdx.x;
                 for (; p + 3 * kThreads < per; p += 4 * kThreads) {
-                    const float y0 = src[p], y1 = src[p + kThreads], y2 = src[p + 2 * kThreads], y3 = src[p + 3 * kThreads];
+                    const float y0 = y_at(p), y1 = y_at(p + kThreads), y2 = y_at(p + 2 * kThreads), y3 = y_at(p + 3 * kThreads);
                     dst[p] = fminf(fmaxf(fmaf(A, y0, B), a.lo), a.hi);
                     dst[p + kThreads] = fminf(fmaxf(fmaf(A, y1, B), a.lo), a.hi);
                     dst[p + 2 * kThreads] = fminf(fmaxf(fmaf(A, y2, B), a.lo), a.hi);
                     dst[p + 3 * kThreads] = fminf(fmaxf(fmaf(A, y3, B), a.lo), a.hi);
                 }
-                for (; p < per; p += kThreads) dst[p] = fminf(fmaxf(fmaf(A, src[p], B), a.lo), a.hi);
+                for (; p < per; p += kThreads) dst[p] = fminf(fmaxf(fmaf(A, y_at(p), B), a.lo), a.hi);
             }
         }
     }
@@ -179,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
 }  // namespace
 
 conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, float *out, cudaStream_t s,
-                            bool presel) {
+                            bool presel, bool half) {
     GnArgs a;
     a.gn = h->gn;
     a.N = h->d.N, a.C = h->d.Cout, a.Ho = h->Ho, a.Wo = h->Wo, a.groups = e.groups;
@@ -187,6 +204,7 @@ conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, 
     a.gamma = e.gamma, a.beta = e.beta, a.scale = e.chan_scale;
     a.out = out, a.idx = e.index_out;
     a.presel = presel ? 1 : 0;
+    a.half = presel && half ? 1 : 0;
     a.inv_cnt = 1.0 / ((double)(a.C / a.groups) * a.Ho * a.Wo);
     a.cnt = (float)((double)(a.C / a.groups) * a.Ho * a.Wo);
     const uint32_t per = (uint32_t)(h->gn.Hp * h->gn.Wp);

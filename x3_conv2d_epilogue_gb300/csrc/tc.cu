@@ -108,6 +108,8 @@ struct Cfg {
     int nhwc;       // channels-last input: tiles go straight into the B planes (no staging, no converters)
     // GroupNorm chain finalized inside this kernel (cooperative launch)
     int gn_fin;
+    int gn_half;    // GroupNorm over 65..128 channels (no row stacking): a unit pools half a band
+                    // (its 2 rows) into slot ru & 1 of the workspace (pmax, pmin); the finalize folds both
     uint32_t smem_bytes;
     // kKindConvStats: per (image, unit, column group, accumulator row) the sums
     // of y and y^2 over the thread's valid outputs, as float pairs
@@ -1026,7 +1028,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr int kNB = (kGN && GENERAL) ? 2 : 1;
     constexpr int kKC = (kGN && GENERAL) ? 2 : 4;
     constexpr int kWin = 4 * kKC;  // pooling windows per band and thread
-    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + 64;
+    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + 128;
     if (kGN && slot == 0) gn_sgn[co] = gsg, gn_bias[co] = bias;
     // GroupNorm: this thread's chunks are cc = hc + 2 kc.  In the one-band
     // form (kKC = 4) chunks kc < 3 lie below column 96 and are whole (that
@@ -1327,7 +1329,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             float *st = scratch + kNB * 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
             st[ew * 32 + lane] = gs;
             st[kEpiThreads + ew * 32 + lane] = gss;
-            const int cl = (qd & 1) * 32 + lane;  // channel within the tile (Cout = 64)
+            // channel within the tile: two row slots of 64 channels, or (no
+            // stacking) one slot of 128 spanning both slots' space
+            const int cl = a.S == 2 ? (qd & 1) * 32 + lane : L;
             auto put_tile = [&](int band, const float (&pext)[kWin]) {
                 float *pt = scratch + (band * 2 + slot) * 64 * kPoolPitch;
 #pragma unroll
@@ -1354,7 +1358,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     for (int k = 0; k < 8; ++k) {  // k = (row slot, column group, half)
                         const int sl = k >> 2, h2 = (k >> 1) & 1, ci = k & 1;
                         v0[k] = v1[k] = 0.0f;
-                        if (ci < nci) {
+                        if (ci < nci && sl < a.S) {
                             const int LL = sl * a.Cout + g * gn_cpg + ci * gn_cw;
                             const int e2 = h2 * 4 + (LL >> 5);
                             v0[k] = st[e2 * 32 + (LL & 31)];
@@ -1364,11 +1368,30 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        if ((k & 1) < nci) s0 += v0[k], s1 += v1[k];
+                        if ((k & 1) < nci && (k >> 2) < a.S) s0 += v0[k], s1 += v1[k];
                     *reinterpret_cast<float2 *>(fpart + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2) =
                         make_float2(s0, s1);
                 }
             }
+            if (!GENERAL && a.gn_half) {
+                // no stacking: this unit's 2 rows are half of band ru / 2; its
+                // extremes (sign and bias restored: the half's selected y) go
+                // to slot ru & 1, and the finalize folds the two halves
+                const int prow = ru >> 1;
+                if (prow < a.Hp && lane < a.Wp) {
+                    float *dst = ((ru & 1) ? a.gn.pmin : a.gn.pmax) + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp + lane;
+                    const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+                    float m[128 / kEpiWarps];
+#pragma unroll
+                    for (int i = 0; i < 128 / kEpiWarps; ++i) {
+                        const int c2 = ew + kEpiWarps * i;
+                        m[i] = fmaf(gn_sgn[c2], scratch[c2 * kPoolPitch + lane], gn_bias[c2]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 128 / kEpiWarps; ++i)
+                        if (ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
+                }
+            } else
 #pragma unroll
             for (int band = 0; band < kNB; ++band) {
                 const int prow = ru * kNB + band;  // pooled row of this band
@@ -1455,17 +1478,22 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     const int cpg = a.Co / a.groups;
     const uint32_t F4 = (uint32_t)cpg * (uint32_t)(a.Hp * a.Wp) / 4u, pbytes = F4 * 16u;
     const int npairs = a.N * a.groups;
-    const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / pbytes));  // >= 1: checked on the host
+    // (with half bands, a pair's two slots side by side: [pair][slot][F4])
+    const uint32_t nsl = a.gn_half ? 2u : 1u, sbytes = nsl * pbytes;
+    const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / sbytes));  // >= 1: checked on the host
     uint32_t phase = 0;
     for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * cap) {
         const int nbp = min(cap, (npairs - p0 + (int)gridDim.x - 1) / (int)gridDim.x);  // pairs in this batch
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(fbar, (uint32_t)nbp * pbytes);
-            for (int j = 0; j < nbp; ++j) {
-                const char *src = reinterpret_cast<const char *>(a.gn.pmax) + (size_t)(p0 + j * (int)gridDim.x) * pbytes;
-                for (uint32_t off = 0; off < pbytes; off += 16384u)
-                    bulk_g2s(smem_u32(buf) + (uint32_t)j * pbytes + off, src + off, min(16384u, pbytes - off), fbar);
-            }
+            mbar_arrive_expect_tx(fbar, (uint32_t)nbp * sbytes);
+            for (int j = 0; j < nbp; ++j)
+                for (uint32_t sl = 0; sl < nsl; ++sl) {
+                    const char *src = reinterpret_cast<const char *>(sl ? a.gn.pmin : a.gn.pmax) +
+                                      (size_t)(p0 + j * (int)gridDim.x) * pbytes;
+                    const uint32_t dsm = smem_u32(buf) + (uint32_t)j * sbytes + sl * pbytes;
+                    for (uint32_t off = 0; off < pbytes; off += 16384u)
+                        bulk_g2s(dsm + off, src + off, min(16384u, pbytes - off), fbar);
+                }
         }
         const int p = p0 + warp * (int)gridDim.x;
         if (warp < nbp) {
@@ -1486,15 +1514,27 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
         for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
             const uint32_t jb = __umulhi(t, a.f4_magic);  // t / F4: the pair within the batch
             const float *cA = sA + jb * 64, *cB = sB + jb * 64;
-            const uint32_t e = 4u * (t - jb * F4);
-            const float4 v = buf[t];
+            const uint32_t fo = t - jb * F4, e = 4u * fo;
+            float4 *bp = buf + jb * nsl * F4 + fo;
+            const float4 v = bp[0];
             float r[4] = {v.x, v.y, v.z, v.w};
+            if (a.gn_half) {
+                // the band's extreme from its two halves: the larger y where
+                // the slope A is >= 0, else the smaller
+                const float4 w = bp[F4];
+                const float h2[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t cl = __umulhi(e + q, a.per_magic);
+                    r[q] = cA[cl] >= 0.0f ? fmaxf(r[q], h2[q]) : fminf(r[q], h2[q]);
+                }
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
                 r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
             }
-            buf[t] = make_float4(r[0], r[1], r[2], r[3]);
+            bp[0] = make_float4(r[0], r[1], r[2], r[3]);
         }
         fence_proxy_async_smem();  // these writes before the copies' reads
         __syncthreads();
@@ -1502,7 +1542,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
             for (int j = 0; j < nbp; ++j) {
                 char *dst = reinterpret_cast<char *>(a.out) + (size_t)(p0 + j * (int)gridDim.x) * pbytes;
                 for (uint32_t off = 0; off < pbytes; off += 16384u)
-                    bulk_s2g(dst + off, smem_u32(buf) + (uint32_t)j * pbytes + off, min(16384u, pbytes - off));
+                    bulk_s2g(dst + off, smem_u32(buf) + (uint32_t)j * sbytes + off, min(16384u, pbytes - off));
             }
             bulk_commit();
             bulk_wait_read();  // the buffer is read: the next batch (or the exit) may reuse it
@@ -1674,7 +1714,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case kKindConvStats:
         return (uint32_t)(kEpiWarps * 32 * 16 * sizeof(float));  // a 32 x 16 staging tile per warp
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
-        return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
+        return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     }
     return 0;
 }
@@ -1845,19 +1885,26 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
 }  // namespace
 
 // The GroupNorm chain fused into the conv kernel: its epilogue pools 4x4
-// windows over bands of 4 rows (two 64-channel row slots per u): one band per
-// unit with P in 112..128 (4 sixteen-column chunks per warp; the first 96
-// columns whole, so Wo >= 96), two with P = 64 (2 chunks).  Other GroupNorm
-// shapes run as two passes (tc_forward).
+// windows over bands of 4 rows.  Up to 64 channels (two 64-channel row slots
+// per u): one band per unit with P in 112..128 (4 sixteen-column chunks per
+// warp; the first 96 columns whole, so Wo >= 96), two with P = 64 (2
+// chunks).  65..128 channels (one slot of 128, P in 112..128): half a band
+// per unit, folded by the finalize.  Other GroupNorm shapes run as two passes
+// (tc_forward).
 bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     Plan pl;
     if (!make_plan(d, CONV_EPI_GN_SCALE_POOL_CLAMP, pl)) return false;
-    const bool one_band = pl.RU == 4 && pl.P > 64 && pl.P <= 128 && d.W - 2 >= 96;
-    const bool two_bands = pl.RU == 8 && pl.P == 64;
-    // (Cout below 64 runs as a 64-channel GEMM with zero filters; a group's
-    // channels must be a power-of-two run of lanes for the shuffle sums)
+    const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= 96;
+    const bool one_band = pl.S == 2 && pl.RU == 4 && wide;
+    const bool two_bands = pl.S == 2 && pl.RU == 8 && pl.P == 64;
+    // 65..128 channels fill M without stacking: a unit holds 2 rows, half a
+    // band, and the finalize folds the halves
+    const bool half_band = pl.S == 1 && pl.MT == 1 && pl.RU == 2 && wide;
+    // (Cout below 64 or 128 runs as a 64- or 128-channel GEMM with zero
+    // filters; a group's channels must be a power-of-two run of lanes, at
+    // most 64, for the shuffle sums and the fold)
     const int cpg = d.Cout / e.groups;
-    return e.pool_k == 4 && (one_band || two_bands) && pl.S == 2 && d.Cout <= 64 && (cpg & (cpg - 1)) == 0;
+    return e.pool_k == 4 && (one_band || two_bands || half_band) && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
 
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
@@ -2050,6 +2097,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
     a.smem_bytes = pl.smem;
+    a.gn_half = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && pl.S == 1 ? 1 : 0;
     a.ystat = e.kind == kKindConvStats
                   ? reinterpret_cast<float2 *>(reinterpret_cast<char *>(h->ybuf) + tc_y_bytes(d))
                   : nullptr;
@@ -2065,7 +2113,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         // channel offsets < 2^16); otherwise the separate finalize kernel
         const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
         a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
-                    F * 4u <= pl.smem - kFinBufOff &&  // one pooled block fits the finalize's buffer
+                    F * 4u * (pl.S == 1 ? 2u : 1u) <= pl.smem - kFinBufOff &&  // one pair's blocks fit the buffer
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
@@ -2102,7 +2150,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (st) return st;
     h->last_launches = pl.MT + 1 + fills + (padded ? 1 : 0);  // packs, fill, conv, row padding
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
-        if ((st = gn_finalize(h, e, out, s, true))) return st;
+        if ((st = gn_finalize(h, e, out, s, true, a.gn_half != 0))) return st;
         h->last_launches += 1;
     }
     return CONV_EPI_OK;
