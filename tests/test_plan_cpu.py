@@ -132,7 +132,9 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
         bands = U // 2
         assert (S == 2 and U in (2, 4) and P <= 128 and (P == 64 or W - 2 >= 96)) or \
             (S == 1 and U == 2 and 64 < P <= 128 and W - 2 >= 96)
-        assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 2 * 128) * 4
+        # sign and bias tables: 64 channels (the page's 64 stacked channels), else 128
+        tables = 64 if Cout == 64 else 128
+        assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 2 * tables) * 4
 
 
 def parity_shapes():

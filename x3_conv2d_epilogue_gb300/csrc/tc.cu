@@ -77,12 +77,25 @@ constexpr int kPoolPitch = 33;      // GroupNorm pooled tile pitch (floats)
 // Internal kind: the conv output y (as CONV_EPI_NONE) plus each thread's sums
 // of y and y^2 per unit, the first pass of the two-pass GroupNorm form.
 constexpr int kKindConvStats = 6;
+// Internal kind: the GroupNorm chain beyond the page's 64 stacked channels --
+// fewer than 64 (zero filters past Co) or 65..128 (no stacking, half a band
+// per unit).  A separate instantiation, so that the page's shape keeps the
+// lean kernel: with these cases compiled into it, it measured 8-10 us slower
+// (86.5 -> 96 us for C5), its registers at the cap.
+constexpr int kKindGnX = 7;
+__host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || kind == kKindGnX; }
+// the fused GroupNorm kernel for a problem: the page's 64 stacked channels, or the generalised one
+inline int tc_gn_kind(const conv_epi_desc &d) { return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX; }
 constexpr int kMaxQ = 8;            // min chains: quadrant partials of a column loaded together
 
 // Scalar kernel configuration.  The kernel copies it out of the parameter
 // space into a local at entry, so the roles keep the fields in registers
 // (reads through the parameter would be repeated after every asm statement
 // that clobbers memory, on the critical path of every loop).
+// (Measured: on the GroupNorm kernel, one more 8-byte field in this struct cost
+// about 5 us of 88, with the same registers and no spills; so mode flags are
+// derived from fields already here, and the conv-with-sums kind passes its
+// buffer in gn.pmax, which only the GroupNorm kind otherwise uses.)
 struct Cfg {
     const float *x, *b, *wpack;
     float *out;
@@ -108,12 +121,7 @@ struct Cfg {
     int nhwc;       // channels-last input: tiles go straight into the B planes (no staging, no converters)
     // GroupNorm chain finalized inside this kernel (cooperative launch)
     int gn_fin;
-    int gn_half;    // GroupNorm over 65..128 channels (no row stacking): a unit pools half a band
-                    // (its 2 rows) into slot ru & 1 of the workspace (pmax, pmin); the finalize folds both
-    uint32_t smem_bytes;
-    // kKindConvStats: per (image, unit, column group, accumulator row) the sums
-    // of y and y^2 over the thread's valid outputs, as float pairs
-    float2 *ystat;  // the launch's dynamic shared memory (free for the finalize after the main loop)
+    uint32_t smem_bytes;  // the launch's dynamic shared memory (free for the finalize after the main loop)
     const float *beta;
     float eps, lo, hi;
     float cnt;            // C/groups * Ho * Wo
@@ -982,7 +990,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int L = qd * 32 + lane;     // accumulator row
     const int slot = L / a.Cout, co = L % a.Cout;
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
-    constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
+    constexpr bool kGnX = KIND == kKindGnX;  // the generalised GroupNorm chain
+    constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
     // this lane's channel parameters; with more than 128 output channels they
     // belong to the unit's channel tile and are reloaded when it changes
     // (channels Co.. pad the GEMM with zero filters)
@@ -992,7 +1001,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // GroupNorm chain: the sign of the channel's affine slope gamma * scale
     // (rstd > 0), folded into the packed filter: the accumulator is gsg * (y - b)
     const float gsg =
-        kGN && co < a.Co && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f : 1.0f;
+        kGN && (!kGnX || co < a.Co) && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f
+                                                                                                      : 1.0f;
     // min chains: scalar * bias of the four channels this thread holds in a
     // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4),
     // each duplicated into a register pair, and the scalar likewise.  The
@@ -1021,14 +1031,14 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // here and first read after the first combine barrier)
     // (groups of the problem's Co <= 64 channels; the GEMM's channels Co..63
     // are zero filters whose sums and extremes are never read)
-    const int gn_cpg = kGN ? a.Co / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
+    const int gn_cpg = kGN ? (kGnX ? a.Co : a.Cout) / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
     // pooling bands of 4 rows per unit: one (rows of 80..128 columns: two u
     // of two row slots) or, in the general instantiation, two (rows of up to
     // 64 columns: four u); 16-column chunks per warp and u: 4 or 2
     constexpr int kNB = (kGN && GENERAL) ? 2 : 1;
     constexpr int kKC = (kGN && GENERAL) ? 2 : 4;
     constexpr int kWin = 4 * kKC;  // pooling windows per band and thread
-    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + 128;
+    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + (kGnX ? 128 : 64);
     if (kGN && slot == 0) gn_sgn[co] = gsg, gn_bias[co] = bias;
     // GroupNorm: this thread's chunks are cc = hc + 2 kc.  In the one-band
     // form (kKC = 4) chunks kc < 3 lie below column 96 and are whole (that
@@ -1299,7 +1309,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         if (lane == 0) mbar_arrive(bars.acc_empty(ab));
         if constexpr (KIND == kKindConvStats) {
             // (image, unit, column group hc, accumulator row L): coalesced float pairs
-            a.ystat[(((size_t)n * a.units_per_img + ru) * 2 + hc) * 128 + L] = make_float2(ys, yss);
+            // (the buffer comes in gn.pmax: [n][unit][hc][L] float pairs)
+            reinterpret_cast<float2 *>(a.gn.pmax)[(((size_t)n * a.units_per_img + ru) * 2 + hc) * 128 + L] =
+                make_float2(ys, yss);
         }
 
         if constexpr (kMin) {
@@ -1331,7 +1343,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             st[kEpiThreads + ew * 32 + lane] = gss;
             // channel within the tile: two row slots of 64 channels, or (no
             // stacking) one slot of 128 spanning both slots' space
-            const int cl = a.S == 2 ? (qd & 1) * 32 + lane : L;
+            const int cl = kGnX && a.S == 1 ? L : (qd & 1) * 32 + lane;
             auto put_tile = [&](int band, const float (&pext)[kWin]) {
                 float *pt = scratch + (band * 2 + slot) * 64 * kPoolPitch;
 #pragma unroll
@@ -1358,7 +1370,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     for (int k = 0; k < 8; ++k) {  // k = (row slot, column group, half)
                         const int sl = k >> 2, h2 = (k >> 1) & 1, ci = k & 1;
                         v0[k] = v1[k] = 0.0f;
-                        if (ci < nci && sl < a.S) {
+                        if (ci < nci && (!kGnX || sl < a.S)) {
                             const int LL = sl * a.Cout + g * gn_cpg + ci * gn_cw;
                             const int e2 = h2 * 4 + (LL >> 5);
                             v0[k] = st[e2 * 32 + (LL & 31)];
@@ -1368,12 +1380,12 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        if ((k & 1) < nci && (k >> 2) < a.S) s0 += v0[k], s1 += v1[k];
+                        if ((k & 1) < nci && (!kGnX || (k >> 2) < a.S)) s0 += v0[k], s1 += v1[k];
                     *reinterpret_cast<float2 *>(fpart + (((size_t)n * a.units_per_img + ru) * a.groups + g) * 2) =
                         make_float2(s0, s1);
                 }
             }
-            if (!GENERAL && a.gn_half) {
+            if (kGnX && !GENERAL && a.S == 1) {
                 // no stacking: this unit's 2 rows are half of band ru / 2; its
                 // extremes (sign and bias restored: the half's selected y) go
                 // to slot ru & 1, and the finalize folds the two halves
@@ -1401,7 +1413,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     // the sign restored; all sixteen tile reads go out before
                     // the stores
                     const float *pt0 = scratch + band * 2 * 64 * kPoolPitch, *pt1 = pt0 + 64 * kPoolPitch;
-                    float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp + lane;
+                    float *dst = a.gn.pmax + (((size_t)n * (kGnX ? a.Co : a.Cout) + ew) * a.Hp + prow) * a.Wp + lane;
                     const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
                     float m[64 / kEpiWarps];
 #pragma unroll
@@ -1412,7 +1424,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
 #pragma unroll
                     for (int i = 0; i < 64 / kEpiWarps; ++i)
-                        if (ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
+                        if (!kGnX || ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
                 }
             }
             // (the vote of the next unit keeps the tile until all stores have read it)
@@ -1441,6 +1453,7 @@ constexpr int kFinPairs = kThreads / 32;
 constexpr uint32_t kFinFlagOff = kFinPairs * 64 * 2 * 4;  // after the coefficient tables
 constexpr uint32_t kFinBarOff = kFinFlagOff + 8;
 constexpr uint32_t kFinBufOff = 8448;                     // the pooled blocks (128-byte aligned)
+template <bool kGnX>
 __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, volatile int *abort_flag) {
     float *sA = reinterpret_cast<float *>(smem), *sB = sA + kFinPairs * 64;
     int &s_go = *reinterpret_cast<int *>(smem + kFinFlagOff);
@@ -1475,11 +1488,11 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     __syncthreads();
     if (!s_go) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cpg = a.Co / a.groups;
+    const int cpg = (kGnX ? a.Co : a.Cout) / a.groups;
     const uint32_t F4 = (uint32_t)cpg * (uint32_t)(a.Hp * a.Wp) / 4u, pbytes = F4 * 16u;
     const int npairs = a.N * a.groups;
     // (with half bands, a pair's two slots side by side: [pair][slot][F4])
-    const uint32_t nsl = a.gn_half ? 2u : 1u, sbytes = nsl * pbytes;
+    const uint32_t nsl = kGnX && a.S == 1 ? 2u : 1u, sbytes = nsl * pbytes;
     const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / sbytes));  // >= 1: checked on the host
     uint32_t phase = 0;
     for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * cap) {
@@ -1518,7 +1531,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
             float4 *bp = buf + jb * nsl * F4 + fo;
             const float4 v = bp[0];
             float r[4] = {v.x, v.y, v.z, v.w};
-            if (a.gn_half) {
+            if (kGnX && a.S == 1) {
                 // the band's extreme from its two halves: the larger y where
                 // the slope A is >= 0, else the smaller
                 const float4 w = bp[F4];
@@ -1617,8 +1630,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         tc_fence_after();
         tmem_dealloc(*tmem_slot, kTmemCols);
     }
-    if constexpr (KIND == CONV_EPI_GN_SCALE_POOL_CLAMP) {
-        if (a.gn_fin) gn_finalize_tail(a, smem, abort_flag);
+    if constexpr (is_gn(KIND)) {
+        if (a.gn_fin) gn_finalize_tail<KIND == kKindGnX>(a, smem, abort_flag);
     }
 }
 
@@ -1714,6 +1727,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case kKindConvStats:
         return (uint32_t)(kEpiWarps * 32 * 16 * sizeof(float));  // a 32 x 16 staging tile per warp
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
+        return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
+    case kKindGnX:  // (the tables for up to 128 channels)
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     }
     return 0;
@@ -1739,7 +1754,7 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (d.Cout < 1) return false;
     if (d.Cin < 1 || d.W < 3 || d.H < 3) return false;
     pl.MT = channel_tiles(d.Cout);
-    if (pl.MT > 1 && kind == CONV_EPI_GN_SCALE_POOL_CLAMP) return false;
+    if (pl.MT > 1 && is_gn(kind)) return false;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
     if (nhwc && d.Cin % 4 != 0) return false;  // 16-byte position stride
     const int Cg = gemm_cout(d.Cout);
@@ -1748,14 +1763,14 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
         // one tile spans the row; the GroupNorm chain runs rows of up to 64
         // columns at P = 64 (four u per unit: two pooling bands)
         pl.P = (d.W + 15) / 16 * 16;
-        if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP && pl.P < 64) pl.P = 64;
+        if (is_gn(kind) && pl.P < 64) pl.P = 64;
         // (staged rows are whole 16-byte units: columns W..BW-1 arrive as zeros)
         pl.CT = 1, pl.CW = d.W - 2, pl.BW = row_pitch(d.W);
     } else {
         // column tiles of 252 outputs from 256 staged columns (the last two
         // unused; tiles start on multiples of 4 columns, 16-byte aligned);
         // past the image's right edge the tensor load fills zeros
-        if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP) return false;
+        if (is_gn(kind)) return false;
         pl.P = 256;
         pl.CW = 252, pl.BW = 256;
         pl.CT = (d.W - 2 + pl.CW - 1) / pl.CW;
@@ -1843,7 +1858,7 @@ EncodeTiledFn encode_tiled() {
 template <int KIND>
 conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStream_t s) {
     // (the GroupNorm chain's general instantiation pools two bands per unit)
-    const bool general = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? args.c.U == 4 : (args.c.CT > 1 || args.c.MT > 1);
+    const bool general = is_gn(KIND) ? args.c.U == 4 : (args.c.CT > 1 || args.c.MT > 1);
     auto k = general ? tc_conv_epi<KIND, true> : tc_conv_epi<KIND, false>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem));
     // The in-kernel finalize waits for every CTA: a cooperative launch
@@ -1893,7 +1908,7 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
 // (tc_forward).
 bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     Plan pl;
-    if (!make_plan(d, CONV_EPI_GN_SCALE_POOL_CLAMP, pl)) return false;
+    if (!make_plan(d, tc_gn_kind(d), pl)) return false;
     const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= 96;
     const bool one_band = pl.S == 2 && pl.RU == 4 && wide;
     const bool two_bands = pl.S == 2 && pl.RU == 8 && pl.P == 64;
@@ -1911,7 +1926,7 @@ conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_des
     Plan pl;
     int kind = e ? e->kind : CONV_EPI_MIN_TANH2;
     // a GroupNorm shape the fused epilogue does not take needs the plain conv
-    if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !tc_gn_fused(d, *e)) kind = CONV_EPI_NONE;
+    if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP) kind = tc_gn_fused(d, *e) ? tc_gn_kind(d) : CONV_EPI_NONE;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     return CONV_EPI_OK;
 }
@@ -1943,7 +1958,7 @@ conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_de
     // a GroupNorm shape the fused epilogue does not take: the plain conv's
     // plan (its first pass)
     const bool two_pass = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !tc_gn_fused(d, e);
-    const int kind = two_pass ? CONV_EPI_NONE : e.kind;
+    const int kind = two_pass ? CONV_EPI_NONE : e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP ? tc_gn_kind(d) : e.kind;
     q.gn_two_pass = two_pass ? 1 : 0;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     q.gemm_cout = pl.Cg, q.S = pl.S, q.P = pl.P, q.U = pl.U, q.RU = pl.RU, q.Rin = pl.Rin, q.PL = pl.PL;
@@ -2019,8 +2034,10 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         h->last_launches += conv_launches;
         return CONV_EPI_OK;
     }
+    // the kernel: the GroupNorm chain's page-shape or generalised instantiation
+    const int kkind = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP ? tc_gn_kind(d) : e.kind;
     Plan pl;
-    if (!make_plan(d, e.kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
+    if (!make_plan(d, kkind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return CONV_EPI_ERR_CUDA;
     TcArgs args{};  // value-initialised: zeros, and the workspace pointers' defaults
@@ -2097,10 +2114,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
     a.smem_bytes = pl.smem;
-    a.gn_half = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && pl.S == 1 ? 1 : 0;
-    a.ystat = e.kind == kKindConvStats
-                  ? reinterpret_cast<float2 *>(reinterpret_cast<char *>(h->ybuf) + tc_y_bytes(d))
-                  : nullptr;
+    if (e.kind == kKindConvStats)  // the per-unit sums, after y in the two-pass buffer
+        a.gn.pmax = reinterpret_cast<float *>(reinterpret_cast<char *>(h->ybuf) + tc_y_bytes(d));
     a.drop_tile = h->test_drop_tile;
     h->test_drop_tile = -1;  // one forward only
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
@@ -2138,19 +2153,24 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     case CONV_EPI_MUL_LRELU_GELU: st = launch_tc<CONV_EPI_MUL_LRELU_GELU>(args, pl, grid, s); break;
     case CONV_EPI_NONE: st = launch_tc<CONV_EPI_NONE>(args, pl, grid, s); break;
     case kKindConvStats: st = launch_tc<kKindConvStats>(args, pl, grid, s); break;
-    case CONV_EPI_GN_SCALE_POOL_CLAMP:
-        st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
+    case CONV_EPI_GN_SCALE_POOL_CLAMP: {
+        auto launch_gn = [&]() {
+            return kkind == kKindGnX ? launch_tc<kKindGnX>(args, pl, grid, s)
+                                     : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
+        };
+        st = launch_gn();
         if (st == CONV_EPI_ERR_UNSUPPORTED && a.gn_fin) {  // cooperative launch refused: finalize separately
             a.gn_fin = 0;
-            st = launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
+            st = launch_gn();
         }
         break;
+    }
     default: return CONV_EPI_ERR_INVALID_ARG;
     }
     if (st) return st;
     h->last_launches = pl.MT + 1 + fills + (padded ? 1 : 0);  // packs, fill, conv, row padding
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
-        if ((st = gn_finalize(h, e, out, s, true, a.gn_half != 0))) return st;
+        if ((st = gn_finalize(h, e, out, s, true, pl.S == 1))) return st;
         h->last_launches += 1;
     }
     return CONV_EPI_OK;
