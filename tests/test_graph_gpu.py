@@ -22,6 +22,8 @@ CASES = {
     # GroupNorm in two passes (conv into the handle's buffer, then the
     # post-pass): both buffers come from conv_epi_reserve
     "c5_two_pass": W["c5_gn_pool_clamp"].resized(N=2, H=14, W=150, Cout=128, groups=16, pool_k=2),
+    # GroupNorm over 128 channels fused in half bands (the generalised instantiation)
+    "c5_half_bands": W["c5_gn_pool_clamp"].resized(N=2, H=14, W=110, Cout=128, groups=16),
 }
 
 

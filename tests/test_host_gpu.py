@@ -17,6 +17,7 @@ CASES = {
     "c3_tf32": (W["c3_mul_lrelu_gelu"].resized(N=11, H=7), 0),            # eight slices of 1-2 images
     "c5_tf32": (W["c5_gn_pool_clamp"].resized(N=3, H=42), 0),             # GroupNorm, in-kernel finalize
     "c5_tf32_two_pass": (W["c5_gn_pool_clamp"].resized(N=5, H=12, W=140, Cout=128, groups=16), 0),  # conv, then post-pass
+    "c5_tf32_half_bands": (W["c5_gn_pool_clamp"].resized(N=4, H=10, W=100, Cout=96, groups=12), 0),  # fused, 96 channels
     "c4_fp32": (W["c4_scale_min"].resized(N=4, H=7, W=96), 1),            # fp32 mode with channel indices
     "c2_fp32_odd": (W["c2_min_tanh2"].resized(N=3, H=9, W=31), 1),        # odd image sizes: one slice
     "c3_tf32_odd": (W["c3_mul_lrelu_gelu"].resized(N=3, H=6, W=37), 0),   # tf32 rows padded on the device

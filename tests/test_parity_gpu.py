@@ -63,7 +63,10 @@ SMALL = {
     "c5_w37": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=37),                # two bands per unit, 3 columns past the pool
     "c5_w98": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=98),                # fused, 112 columns: chunk 6 whole, chunk 7 absent
     "c5_w107": W["c5_gn_pool_clamp"].resized(N=1, H=13, W=107),              # fused, chunk 6 ragged at column 105
-    "c5_w90": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=90),                # one band of 96 columns: two passes in tf32
+    "c5_w90": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=90),                # one band of 96 columns (generalised kernel)
+    "c5_w66": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=66),                # Wo 64 in P 80: chunk 4 all masked
+    "c5_w65": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=65),                # Wo 63: two passes in tf32
+    "c5_co128_w80": W["c5_gn_pool_clamp"].resized(N=1, H=11, W=80, Cout=128, groups=32),  # half bands in P 80
     "min_w3": W["pr1_min_tanh2"].resized(N=2, Cin=2, H=3, W=3, Cout=1),      # a single output per image
     # GroupNorm shapes beyond the page's (tf32: fused where the epilogue takes
     # them, else the conv then the chain's post-pass through a buffer of y)

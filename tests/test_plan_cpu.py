@@ -130,10 +130,10 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
         assert top == 32 * 16 - 1 and q["scratch_bytes"] >= 8 * 32 * 16 * 4
     else:
         bands = U // 2
-        assert (S == 2 and U in (2, 4) and P <= 128 and (P == 64 or W - 2 >= 96)) or \
-            (S == 1 and U == 2 and 64 < P <= 128 and W - 2 >= 96)
-        # sign and bias tables: 64 channels (the page's 64 stacked channels), else 128
-        tables = 64 if Cout == 64 else 128
+        assert (S == 2 and U in (2, 4) and P <= 128 and (P == 64 or W - 2 >= 64)) or \
+            (S == 1 and U == 2 and 64 < P <= 128 and W - 2 >= 64)
+        # sign and bias tables: 64 channels (the page-shape kernel), else 128
+        tables = 64 if Cout == 64 and (W <= 64 or W - 2 >= 96) else 128
         assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 2 * tables) * 4
 
 
@@ -171,11 +171,12 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     # one band, fused when the first 96 output columns are whole (Wo >= 96);
     # up to 64 channels (a 64-channel GEMM), a group's channels a power of two
     # 65..128 channels (no row stacking) fuse with one-band rows, each unit
-    # pooling half a band
+    # pooling half a band; one-band rows need Wo >= 64 (the generalised
+    # kernel masks the chunks past column 64)
     cpg = Cout // groups
     if kind != ce.GN_SCALE_POOL_CLAMP or pool_k != 4 or cpg & (cpg - 1) or cpg > 64:
         return False
-    return (Cout <= 64 and (W <= 64 or 98 <= W <= 128)) or (64 < Cout <= 128 and 98 <= W <= 128)
+    return (Cout <= 64 and (W <= 64 or 66 <= W <= 128)) or (64 < Cout <= 128 and 66 <= W <= 128)
 
 
 def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
@@ -199,8 +200,8 @@ def test_random_shapes_all_planned_and_in_range():
     """Every shape with H, W >= 3 has a plan (the tf32 mode takes any size),
     and every plan passes the range checks; GroupNorm shapes are fused
     exactly when pool_k = 4, groups have a power-of-two size up to 64, and
-    Cout <= 64 with W <= 64 or 98 <= W <= 128, or 64 < Cout <= 128 with
-    98 <= W <= 128; otherwise they are planned as
+    Cout <= 64 with W <= 64 or 66 <= W <= 128, or 64 < Cout <= 128 with
+    66 <= W <= 128; otherwise they are planned as
     the plain conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):

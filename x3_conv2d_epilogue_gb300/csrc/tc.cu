@@ -83,9 +83,18 @@ constexpr int kKindConvStats = 6;
 // lean kernel: with these cases compiled into it, it measured 8-10 us slower
 // (86.5 -> 96 us for C5), its registers at the cap.
 constexpr int kKindGnX = 7;
-__host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || kind == kKindGnX; }
-// the fused GroupNorm kernel for a problem: the page's 64 stacked channels, or the generalised one
-inline int tc_gn_kind(const conv_epi_desc &d) { return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX; }
+// ... and its one-band rows of 64..95 outputs (P = 80 or 96), which mask one
+// chunk more: an instantiation of their own, so the wider rows keep one mask
+// (measured: the second mask cost Cout 128 at W 128 9 %).
+constexpr int kKindGnXNarrow = 8;
+__host__ __device__ constexpr bool is_gnx(int kind) { return kind == kKindGnX || kind == kKindGnXNarrow; }
+__host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
+// the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
+// 96..126 outputs), or the generalised one
+inline int tc_gn_kind(const conv_epi_desc &d) {
+    if (d.W > 64 && d.W - 2 < 96) return kKindGnXNarrow;
+    return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX;
+}
 constexpr int kMaxQ = 8;            // min chains: quadrant partials of a column loaded together
 
 // Scalar kernel configuration.  The kernel copies it out of the parameter
@@ -990,7 +999,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int L = qd * 32 + lane;     // accumulator row
     const int slot = L / a.Cout, co = L % a.Cout;
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
-    constexpr bool kGnX = KIND == kKindGnX;  // the generalised GroupNorm chain
+    constexpr bool kGnX = is_gnx(KIND);  // the generalised GroupNorm chain
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
     // this lane's channel parameters; with more than 128 output channels they
     // belong to the unit's channel tile and are reloaded when it changes
@@ -1041,13 +1050,14 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + (kGnX ? 128 : 64);
     if (kGN && slot == 0) gn_sgn[co] = gsg, gn_bias[co] = bias;
     // GroupNorm: this thread's chunks are cc = hc + 2 kc.  In the one-band
-    // form (kKC = 4) chunks kc < 3 lie below column 96 and are whole (that
-    // form has Wo >= 96); the others may hold columns >= Wo (or lie past P),
-    // which the sums skip: bit 16 (kc - kMask0) + i of gn_rag is set when
-    // column 16 cc + i < Wo.  (A select per value costs as much as the sums
-    // themselves, so only the chunks that can be ragged take it.)  gn_ncol
-    // counts this thread's valid columns.
-    constexpr int kMask0 = kKC == 4 ? 3 : 0;
+    // form (kKC = 4) chunks kc < kMask0 are whole: below column 96 in the
+    // page-shape kernel (its rows have Wo >= 96), below column 64 in the
+    // generalised one (Wo >= 64); the others may hold columns >= Wo (or lie
+    // past P), which the sums skip: bit 16 (kc - kMask0) + i of gn_rag is set
+    // when column 16 cc + i < Wo.  (A select per value costs as much as the
+    // sums, so only the chunks that can be ragged take it.)  gn_ncol counts
+    // this thread's valid columns.
+    constexpr int kMask0 = kKC == 4 ? (KIND == kKindGnXNarrow ? 2 : 3) : 0;
     uint32_t gn_rag = 0;
     int gn_ncol = 0;
     if constexpr (kGN) {
@@ -1631,7 +1641,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         tmem_dealloc(*tmem_slot, kTmemCols);
     }
     if constexpr (is_gn(KIND)) {
-        if (a.gn_fin) gn_finalize_tail<KIND == kKindGnX>(a, smem, abort_flag);
+        if (a.gn_fin) gn_finalize_tail<is_gnx(KIND)>(a, smem, abort_flag);
     }
 }
 
@@ -1729,6 +1739,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
     case kKindGnX:  // (the tables for up to 128 channels)
+    case kKindGnXNarrow:
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     }
     return 0;
@@ -1901,15 +1912,17 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
 
 // The GroupNorm chain fused into the conv kernel: its epilogue pools 4x4
 // windows over bands of 4 rows.  Up to 64 channels (two 64-channel row slots
-// per u): one band per unit with P in 112..128 (4 sixteen-column chunks per
-// warp; the first 96 columns whole, so Wo >= 96), two with P = 64 (2
-// chunks).  65..128 channels (one slot of 128, P in 112..128): half a band
-// per unit, folded by the finalize.  Other GroupNorm shapes run as two passes
-// (tc_forward).
+// per u): one band per unit with P in 80..128 (4 sixteen-column chunks per
+// warp; Wo >= 96 in the page-shape kernel, Wo >= 64 in the generalised one,
+// which masks one chunk more), two with P = 64 (2 chunks).  65..128 channels
+// (one slot of 128, P in 80..128, Wo >= 64): half a band per unit, folded by
+// the finalize.  Other GroupNorm shapes run as two passes (tc_forward).
 bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     Plan pl;
-    if (!make_plan(d, tc_gn_kind(d), pl)) return false;
-    const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= 96;
+    const int kind = tc_gn_kind(d);
+    if (!make_plan(d, kind, pl)) return false;
+    // one-band rows: the unmasked chunks must be whole (see the epilogue)
+    const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= (kind == kKindGnXNarrow ? 64 : 96);
     const bool one_band = pl.S == 2 && pl.RU == 4 && wide;
     const bool two_bands = pl.S == 2 && pl.RU == 8 && pl.P == 64;
     // 65..128 channels fill M without stacking: a unit holds 2 rows, half a
@@ -2155,8 +2168,9 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     case kKindConvStats: st = launch_tc<kKindConvStats>(args, pl, grid, s); break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP: {
         auto launch_gn = [&]() {
-            return kkind == kKindGnX ? launch_tc<kKindGnX>(args, pl, grid, s)
-                                     : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
+            return kkind == kKindGnX         ? launch_tc<kKindGnX>(args, pl, grid, s)
+                   : kkind == kKindGnXNarrow ? launch_tc<kKindGnXNarrow>(args, pl, grid, s)
+                                             : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
         };
         st = launch_gn();
         if (st == CONV_EPI_ERR_UNSUPPORTED && a.gn_fin) {  // cooperative launch refused: finalize separately
