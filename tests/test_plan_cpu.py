@@ -233,9 +233,10 @@ def test_plan_query_arguments():
         ce._check(ce._lib().conv_epi_plan_query(ce.C.byref(d), ce.C.byref(epi_for(ce.MIN_TANH2)),
                                                 ce.C.byref(q)), "plan")
     assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
-    with pytest.raises(ce.ConvEpiError) as ei:          # bad chain
-        plan(1, 8, 8, 8, 64, 9)
-    assert ce.STATUS[ei.value.status] == "INVALID_ARG"
+    for bad_kind in (6, 7, 8, 9, -1):                    # bad chain (the kernel's internal kinds included)
+        with pytest.raises(ce.ConvEpiError) as ei:
+            plan(1, 8, 8, 8, 64, bad_kind)
+        assert ce.STATUS[ei.value.status] == "INVALID_ARG"
     with pytest.raises(ce.ConvEpiError) as ei:          # H < 3
         plan(1, 8, 2, 8, 64, ce.MIN_TANH2)
     assert ce.STATUS[ei.value.status] == "INVALID_ARG"
