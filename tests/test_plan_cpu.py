@@ -131,10 +131,18 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
     else:
         bands = U // 2
         assert (S == 2 and U in (2, 4) and P <= 128 and (P == 64 or W - 2 >= 64)) or \
-            (S == 1 and U == 2 and 64 < P <= 128 and W - 2 >= 64)
-        # sign and bias tables: 64 channels (the page-shape kernel), else 128
-        tables = 64 if Cout == 64 and (W <= 64 or W - 2 >= 96) else 128
-        assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 2 * tables) * 4
+            (S == 1 and U == 2 and 64 < P <= 128 and W - 2 >= 64) or \
+            (S == 2 and U == 1 and 128 < P <= 256 and W - 2 >= 128)
+        if U == 1:
+            # wide rows: one band region of pitch 65 (up to 63 windows), the
+            # statistics, 128-channel tables; the tile writes reach
+            # slot * 64 * 65 + channel * 65 + window (window < 64)
+            top = max(sl * 64 * 65 + ch * 65 + w for sl in (0, 1) for ch in range(64) for w in range(64))
+            assert top < 2 * 64 * 65 and q["scratch_bytes"] >= (2 * 64 * 65 + 2 * 256 + 2 * 128) * 4
+        else:
+            # sign and bias tables: 64 channels (the page-shape kernel), else 128
+            tables = 64 if Cout == 64 and (W <= 64 or W - 2 >= 96) else 128
+            assert q["scratch_bytes"] >= (bands * 2 * 64 * 33 + 2 * 256 + 2 * tables) * 4
 
 
 def parity_shapes():
@@ -176,7 +184,8 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     cpg = Cout // groups
     if kind != ce.GN_SCALE_POOL_CLAMP or pool_k != 4 or cpg & (cpg - 1) or cpg > 64:
         return False
-    return (Cout <= 64 and (W <= 64 or 66 <= W <= 128)) or (64 < Cout <= 128 and 66 <= W <= 128)
+    # rows of 130..256 columns (Cout <= 64): one row pair per unit
+    return (Cout <= 64 and (W <= 64 or 66 <= W <= 128 or 130 <= W <= 256)) or (64 < Cout <= 128 and 66 <= W <= 128)
 
 
 def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
@@ -200,8 +209,8 @@ def test_random_shapes_all_planned_and_in_range():
     """Every shape with H, W >= 3 has a plan (the tf32 mode takes any size),
     and every plan passes the range checks; GroupNorm shapes are fused
     exactly when pool_k = 4, groups have a power-of-two size up to 64, and
-    Cout <= 64 with W <= 64 or 66 <= W <= 128, or 64 < Cout <= 128 with
-    66 <= W <= 128; otherwise they are planned as
+    Cout <= 64 with W <= 64, 66 <= W <= 128 or 130 <= W <= 256, or
+    64 < Cout <= 128 with 66 <= W <= 128; otherwise they are planned as
     the plain conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):

@@ -87,11 +87,18 @@ constexpr int kKindGnX = 7;
 // chunk more: an instantiation of their own, so the wider rows keep one mask
 // (measured: the second mask cost Cout 128 at W 128 9 %).
 constexpr int kKindGnXNarrow = 8;
-__host__ __device__ constexpr bool is_gnx(int kind) { return kind == kKindGnX || kind == kKindGnXNarrow; }
+// ... and rows of 130..256 columns with Cout <= 64 (P 144..256): one row pair,
+// half a band, per unit, its up to 63 windows in two passes of 4 chunks per
+// warp (the second masked).
+constexpr int kKindGnWide = 9;
+__host__ __device__ constexpr bool is_gnx(int kind) {
+    return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide;
+}
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
 // 96..126 outputs), or the generalised one
 inline int tc_gn_kind(const conv_epi_desc &d) {
+    if (d.W > 128) return kKindGnWide;
     if (d.W > 64 && d.W - 2 < 96) return kKindGnXNarrow;
     return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX;
 }
@@ -1000,6 +1007,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int slot = L / a.Cout, co = L % a.Cout;
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGnX = is_gnx(KIND);  // the generalised GroupNorm chain
+    constexpr bool kWide = KIND == kKindGnWide;  // rows of 130..256 columns: two passes per unit
+    constexpr int kPitch = kWide ? 65 : kPoolPitch;  // pooled tile pitch (up to 63 windows)
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
     // this lane's channel parameters; with more than 128 output channels they
     // belong to the unit's channel tile and are reloaded when it changes
@@ -1047,7 +1056,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr int kNB = (kGN && GENERAL) ? 2 : 1;
     constexpr int kKC = (kGN && GENERAL) ? 2 : 4;
     constexpr int kWin = 4 * kKC;  // pooling windows per band and thread
-    float *gn_sgn = scratch + kNB * 2 * 64 * kPoolPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + (kGnX ? 128 : 64);
+    float *gn_sgn = scratch + kNB * 2 * 64 * kPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + (kGnX ? 128 : 64);
     if (kGN && slot == 0) gn_sgn[co] = gsg, gn_bias[co] = bias;
     // GroupNorm: this thread's chunks are cc = hc + 2 kc.  In the one-band
     // form (kKC = 4) chunks kc < kMask0 are whole: below column 96 in the
@@ -1057,7 +1066,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // when column 16 cc + i < Wo.  (A select per value costs as much as the
     // sums, so only the chunks that can be ragged take it.)  gn_ncol counts
     // this thread's valid columns.
-    constexpr int kMask0 = kKC == 4 ? (KIND == kKindGnXNarrow ? 2 : 3) : 0;
+    constexpr int kMask0 = kWide ? 4 : kKC == 4 ? (KIND == kKindGnXNarrow ? 2 : 3) : 0;
     uint32_t gn_rag = 0;
     int gn_ncol = 0;
     if constexpr (kGN) {
@@ -1066,6 +1075,16 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             const int nv = lim < 0 ? 0 : lim > 16 ? 16 : lim;
             gn_ncol += nv;
             if (kc >= kMask0) gn_rag |= ((1u << nv) - 1u) << (16 * (kc - kMask0));
+        }
+    }
+    // wide rows: the second pass's chunks cc = hc + 8 + 2 kc, bit 16 kc + i
+    // set when column 16 cc + i < Wo (the first pass's lie below 128 <= Wo)
+    uint64_t gn_ragw = 0;
+    if constexpr (kWide) {
+        for (int kc = 0; kc < 4; ++kc) {
+            const int lim = a.Wo - 16 * (hc + 8 + 2 * kc), nv = lim < 0 ? 0 : lim > 16 ? 16 : lim;
+            gn_ncol += nv;
+            gn_ragw |= (uint64_t)((1u << nv) - 1u) << (16 * kc);
         }
     }
     // Min chains: the cross-quadrant combine of a unit's partial minima, the
@@ -1172,6 +1191,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         }
 
         int gn_rows = 0;  // this thread's rows below Ho in the unit
+        bool gn_quit = false;  // wide rows: the mid-unit vote said to leave
         if constexpr (kGN) {
             // Per u: the warp's kKC chunks loaded together, then per chunk the
             // window maxima of the accumulator (sgn * (y - b)) and, over the
@@ -1209,6 +1229,69 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
                 }
             };
+            if constexpr (kWide) {
+                // one u (rows r0, r0 + 1 in the two slots), 8 or fewer chunks
+                // per warp in two passes of 4: the first (columns below 128)
+                // whole, the second masked; each pass's window extremes go to
+                // the tile at once (windows 0..31, then 32..63)
+                auto gn_step_w = [&](const Frag16 (&f)[kKC], float (&pext)[kWin]) {
+#pragma unroll
+                    for (int kc = 0; kc < kKC; ++kc) {
+                        uint64_t v2[8];
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) v2[p] = pack2(f[kc].r[2 * p], f[kc].r[2 * p + 1]);
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            const float2 a01 = unpack2(v2[2 * wi]), a23 = unpack2(v2[2 * wi + 1]);
+                            pext[4 * kc + wi] = fmax3(fmax3(a01.x, a01.y, a23.x), a23.y, pext[4 * kc + wi]);
+                        }
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            const uint64_t b0 = 1ull << (16 * kc + 2 * p);
+                            const float2 w = unpack2(v2[p]);
+                            v2[p] = pack2(__float_as_uint((gn_ragw & b0) ? w.x : 0.0f),
+                                          __float_as_uint((gn_ragw & (b0 << 1)) ? w.y : 0.0f));
+                        }
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            ls2[p & 1] = add2u(ls2[p & 1], v2[p]);
+                            lss2[p & 1] = fma2u(v2[p], v2[p], lss2[p & 1]);
+                        }
+                    }
+                };
+                auto put_w = [&](int pass) {
+                    float *pt = scratch + slot * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch;
+#pragma unroll
+                    for (int k = 0; k < kWin; ++k) {
+                        const int pw = (hc + 8 * pass + 2 * (k / 4)) * 4 + (k % 4);
+                        if (pw < 64) pt[pw] = pext0[k];
+                    }
+                };
+                const bool row_ok = r0 + slot < a.Ho;  // the same for the whole warp
+                gn_rows += row_ok ? 1 : 0;
+                Frag16 f[kKC];
+#pragma unroll
+                for (int kc = 0; kc < kKC; ++kc) tmem_ld16_issue(tbase + (hc + 2 * kc) * 16, f[kc]);
+                tmem_ld_wait2(f[0], f[1]);
+                tmem_ld_wait2(f[2], f[3]);
+                if (row_ok) gn_step(f, pext0);
+                // every warp is past the previous unit's tile and statistics
+                // reads (and none has given up) before the tile is rewritten
+                if (epi_bar_any(false)) {
+                    gn_quit = true;
+                } else {
+                    put_w(0);
+#pragma unroll
+                    for (int k = 0; k < kWin; ++k) pext0[k] = -INFINITY;
+#pragma unroll
+                    for (int kc = 0; kc < kKC; ++kc)
+                        if (hc + 8 + 2 * kc < nchunks) tmem_ld16_issue(tbase + (hc + 8 + 2 * kc) * 16, f[kc]);
+                    tmem_ld_wait2(f[0], f[1]);
+                    tmem_ld_wait2(f[2], f[3]);
+                    if (row_ok) gn_step_w(f, pext0);
+                    put_w(1);
+                }
+            } else
             for (int u = 0; u < a.U; ++u) {
                 const bool row_ok = r0 + u * a.S + slot < a.Ho;  // the same for the whole warp
                 gn_rows += row_ok ? 1 : 0;
@@ -1313,6 +1396,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             }
         }
         }
+        if (gn_quit) break;
         // tensor memory of this unit is no longer needed
         tc_fence_before();
         __syncwarp();
@@ -1347,8 +1431,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // stores fold the two slots
             // every warp is past the previous unit's tile and statistics reads
             // (and none has given up) before they are rewritten
-            if (epi_bar_any(false)) break;
-            float *st = scratch + kNB * 2 * 64 * kPoolPitch;  // [2 stats][8 warps][32 lanes]
+            if (!kWide && epi_bar_any(false)) break;  // (wide rows voted before their first pass's tile)
+            float *st = scratch + kNB * 2 * 64 * kPitch;  // [2 stats][8 warps][32 lanes]
             st[ew * 32 + lane] = gs;
             st[kEpiThreads + ew * 32 + lane] = gss;
             // channel within the tile: two row slots of 64 channels, or (no
@@ -1362,8 +1446,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
                 }
             };
-            put_tile(0, pext0);
-            if constexpr (kNB == 2) put_tile(1, pext1);
+            if constexpr (!kWide) {
+                put_tile(0, pext0);
+                if constexpr (kNB == 2) put_tile(1, pext1);
+            }
             epi_bar();
             if (ew == 2) {
                 // one warp (the others go on to the band stores): per group,
@@ -1395,6 +1481,30 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         make_float2(s0, s1);
                 }
             }
+            if constexpr (kWide) {
+                // half band ru / 2, two row slots folded, sign and bias
+                // restored, into slot ru & 1; windows lane and lane + 32
+                const int prow = ru >> 1;
+                if (prow < a.Hp) {
+                    const float *pt0 = scratch, *pt1 = scratch + 64 * kPitch;
+                    float *dst = ((ru & 1) ? a.gn.pmin : a.gn.pmax) + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
+                    const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+#pragma unroll
+                    for (int hw = 0; hw < 2; ++hw) {
+                        const int w = lane + 32 * hw;
+                        if (w >= a.Wp) continue;
+                        float m[64 / kEpiWarps];
+#pragma unroll
+                        for (int i = 0; i < 64 / kEpiWarps; ++i) {
+                            const int c2 = ew + kEpiWarps * i;
+                            m[i] = fmaf(gn_sgn[c2], fmaxf(pt0[c2 * kPitch + w], pt1[c2 * kPitch + w]), gn_bias[c2]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 64 / kEpiWarps; ++i)
+                            if (ew + kEpiWarps * i < a.Co) dst[i * cstep + w] = m[i];
+                    }
+                }
+            } else
             if (kGnX && !GENERAL && a.S == 1) {
                 // no stacking: this unit's 2 rows are half of band ru / 2; its
                 // extremes (sign and bias restored: the half's selected y) go
@@ -1502,7 +1612,8 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     const uint32_t F4 = (uint32_t)cpg * (uint32_t)(a.Hp * a.Wp) / 4u, pbytes = F4 * 16u;
     const int npairs = a.N * a.groups;
     // (with half bands, a pair's two slots side by side: [pair][slot][F4])
-    const uint32_t nsl = kGnX && a.S == 1 ? 2u : 1u, sbytes = nsl * pbytes;
+    // (a unit of 2 rows holds half a band: 65..128 channels, or rows of 130..256 columns)
+    const uint32_t nsl = kGnX && a.RU == 2 ? 2u : 1u, sbytes = nsl * pbytes;
     const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / sbytes));  // >= 1: checked on the host
     uint32_t phase = 0;
     for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * cap) {
@@ -1541,7 +1652,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
             float4 *bp = buf + jb * nsl * F4 + fo;
             const float4 v = bp[0];
             float r[4] = {v.x, v.y, v.z, v.w};
-            if (kGnX && a.S == 1) {
+            if (kGnX && a.RU == 2) {
                 // the band's extreme from its two halves: the larger y where
                 // the slope A is >= 0, else the smaller
                 const float4 w = bp[F4];
@@ -1738,6 +1849,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
         return (uint32_t)(kEpiWarps * 32 * 16 * sizeof(float));  // a 32 x 16 staging tile per warp
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
+    case kKindGnWide:  // one band region of pitch 65, the statistics, the tables
+        return (uint32_t)((2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnX:  // (the tables for up to 128 channels)
     case kKindGnXNarrow:
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 128) * sizeof(float));
@@ -1928,11 +2041,15 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // 65..128 channels fill M without stacking: a unit holds 2 rows, half a
     // band, and the finalize folds the halves
     const bool half_band = pl.S == 1 && pl.MT == 1 && pl.RU == 2 && wide;
+    // rows of 130..256 columns (Cout <= 64): one row pair per unit (U = 1),
+    // the first 128 output columns whole
+    const bool wide_rows = kind == kKindGnWide && pl.S == 2 && pl.U == 1 && pl.CT == 1 && pl.P > 128 &&
+                           d.W - 2 >= 128;
     // (Cout below 64 or 128 runs as a 64- or 128-channel GEMM with zero
     // filters; a group's channels must be a power-of-two run of lanes, at
     // most 64, for the shuffle sums and the fold)
     const int cpg = d.Cout / e.groups;
-    return e.pool_k == 4 && (one_band || two_bands || half_band) && (cpg & (cpg - 1)) == 0 && cpg <= 64;
+    return e.pool_k == 4 && (one_band || two_bands || half_band || wide_rows) && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
 
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
@@ -2134,14 +2251,14 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
-        if (h->gn.units != a.units_per_img || a.Wp > 32) return CONV_EPI_ERR_INVALID_ARG;
+        if (h->gn.units != a.units_per_img || a.Wp > (kkind == kKindGnWide ? 64 : 32)) return CONV_EPI_ERR_INVALID_ARG;
         // finalize inside the kernel when each (image, group) block of pooled
         // values is whole float4s (16-byte aligned blocks) and small enough
         // for the multiply-high divisions (t < 2^18 pooled float4 per batch,
         // channel offsets < 2^16); otherwise the separate finalize kernel
         const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
         a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
-                    F * 4u * (pl.S == 1 ? 2u : 1u) <= pl.smem - kFinBufOff &&  // one pair's blocks fit the buffer
+                    F * 4u * (pl.RU == 2 ? 2u : 1u) <= pl.smem - kFinBufOff &&  // one pair's blocks fit the buffer
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
@@ -2170,6 +2287,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         auto launch_gn = [&]() {
             return kkind == kKindGnX         ? launch_tc<kKindGnX>(args, pl, grid, s)
                    : kkind == kKindGnXNarrow ? launch_tc<kKindGnXNarrow>(args, pl, grid, s)
+                   : kkind == kKindGnWide    ? launch_tc<kKindGnWide>(args, pl, grid, s)
                                              : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
         };
         st = launch_gn();
@@ -2184,7 +2302,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (st) return st;
     h->last_launches = pl.MT + 1 + fills + (padded ? 1 : 0);  // packs, fill, conv, row padding
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
-        if ((st = gn_finalize(h, e, out, s, true, pl.S == 1))) return st;
+        if ((st = gn_finalize(h, e, out, s, true, pl.RU == 2))) return st;
         h->last_launches += 1;
     }
     return CONV_EPI_OK;
