@@ -18,11 +18,14 @@
 //   per-channel     16-byte loads and stores over each (image, channel) plane
 //                   when a plane is whole float4s, else one float per thread;
 //   GroupNorm       stats: one CTA per (image, group), fp32 per thread, fp64
-//                   across the CTA in a fixed order; apply: one thread per
-//                   pooled output, the window's max (or min, when the
-//                   channel's slope gamma * scale is negative) of y, then
+//                   across the CTA in a fixed order; apply: one warp per
+//                   pooled row, a lane per window, the window's max (or min,
+//                   when the channel's slope gamma * scale is negative) of y
+//                   by vector loads where the rows allow, then
 //                   clamp(A y + B).
 #include <math.h>
+
+#include <type_traits>
 
 #include "gn_common.cuh"
 #include "internal.h"
@@ -117,33 +120,78 @@ __global__ void __launch_bounds__(kThreads) post_gn_stats(const float *__restric
     }
 }
 
-// one thread per pooled output (n, c, ph, pw): z = A y + B over the k x k
-// window, pooled by its max (A's sign picks the max or the min of y), then
-// clamped
+// one warp per pooled row (n, c, ph), its lanes over the row's windows pw:
+// z = A y + B over the k x k window, pooled by its max (A's sign picks the
+// max or the min of y), then clamped.  The row's index arithmetic and the
+// channel's coefficients are taken once per row, and a lane's loads for its
+// next windows (pw = lane + 32 j: 1, 2 or 4 of them for k = 4, 2..3 or 1) go
+// out before any is reduced, so enough bytes are in flight to keep HBM busy.  VEC floats per load: 4 when k = 4
+// and Wo is a multiple of 4, 2 when k is even and Wo is even (every window
+// row then starts on a VEC-float boundary), else 1; K = 0 takes k at run
+// time (one window at a time).
+template <int K, int VEC>
 __global__ void __launch_bounds__(kThreads) post_gn_pool(const float *__restrict__ y, float *__restrict__ out,
                                                         const float *__restrict__ stats, const float *__restrict__ gamma,
                                                         const float *__restrict__ beta, const float *__restrict__ scale,
-                                                        int N, int C, int groups, int Ho, int Wo, int k, int Hp, int Wp,
-                                                        float lo, float hi) {
-    const size_t total = (size_t)N * C * Hp * Wp;
-    const int cpg = C / groups;
-    for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total; o += (size_t)gridDim.x * blockDim.x) {
-        const int pw = (int)(o % Wp);
-        const int ph = (int)((o / Wp) % Hp);
-        const size_t nc = o / ((size_t)Hp * Wp);
-        const int c = (int)(nc % C), n = (int)(nc / C);
-        const int g = c / cpg;
+                                                        int N, int C, int groups, int Ho, int Wo, int k_rt, int Hp,
+                                                        int Wp, float lo, float hi) {
+    const int k = K ? K : k_rt;
+    const size_t rows = (size_t)N * C * Hp;
+    const int cpg = C / groups, lane = threadIdx.x & 31;
+    const size_t warps = (size_t)gridDim.x * (kThreads / 32);
+    for (size_t r = blockIdx.x * (size_t)(kThreads / 32) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const size_t nc = r / Hp;
+        const int ph = (int)(r - nc * Hp);
+        const int c = (int)(nc % C), n = (int)(nc / C), g = c / cpg;
         const float mean = __ldg(&stats[2 * ((size_t)n * groups + g)]), rstd = __ldg(&stats[2 * ((size_t)n * groups + g) + 1]);
         float A, B;
         gn_coeffs(__ldg(&gamma[c]), __ldg(&beta[c]), __ldg(&scale[c]), mean, rstd, A, B);
-        const float *w = y + (nc * Ho + (size_t)ph * k) * Wo + (size_t)pw * k;
-        float mx = -INFINITY, mn = INFINITY;
-        for (int a = 0; a < k; ++a)
-            for (int b = 0; b < k; ++b) {
-                const float v = __ldg(w + (size_t)a * Wo + b);
-                mx = fmaxf(mx, v), mn = fminf(mn, v);
+        const float *w0 = y + (nc * Ho + (size_t)ph * k) * Wo;
+        float *orow = out + r * Wp;
+        if constexpr (K > 0) {
+            constexpr int kJ = K >= 4 ? 1 : K >= 2 ? 2 : 4, kL = K / VEC;  // windows per lane per batch, loads per window row
+            using V = typename std::conditional<VEC == 4, float4, typename std::conditional<VEC == 2, float2, float>::type>::type;
+            for (int pb = 0; pb < Wp; pb += 32 * kJ) {
+                V v[kJ][K][kL];
+#pragma unroll
+                for (int j = 0; j < kJ; ++j) {
+                    const int pw = pb + lane + 32 * j;
+                    if (pw < Wp) {
+#pragma unroll
+                        for (int a = 0; a < K; ++a)
+#pragma unroll
+                            for (int l = 0; l < kL; ++l)
+                                v[j][a][l] = __ldg(reinterpret_cast<const V *>(w0 + (size_t)a * Wo + (size_t)pw * K) + l);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kJ; ++j) {
+                    const int pw = pb + lane + 32 * j;
+                    if (pw >= Wp) break;
+                    float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+                    for (int a = 0; a < K; ++a)
+#pragma unroll
+                        for (int l = 0; l < kL; ++l) {
+                            const float *e = reinterpret_cast<const float *>(&v[j][a][l]);
+#pragma unroll
+                            for (int i = 0; i < VEC; ++i) mx = fmaxf(mx, e[i]), mn = fminf(mn, e[i]);
+                        }
+                    orow[pw] = fminf(fmaxf(fmaf(A, A >= 0.0f ? mx : mn, B), lo), hi);
+                }
             }
-        out[o] = fminf(fmaxf(fmaf(A, A >= 0.0f ? mx : mn, B), lo), hi);
+        } else {
+            for (int pw = lane; pw < Wp; pw += 32) {
+                const float *w = w0 + (size_t)pw * k;
+                float mx = -INFINITY, mn = INFINITY;
+                for (int a = 0; a < k; ++a)
+                    for (int b = 0; b < k; ++b) {
+                        const float v = __ldg(w + (size_t)a * Wo + b);
+                        mx = fmaxf(mx, v), mn = fminf(mn, v);
+                    }
+                orow[pw] = fminf(fmaxf(fmaf(A, A >= 0.0f ? mx : mn, B), lo), hi);
+            }
+        }
     }
 }
 
@@ -195,6 +243,27 @@ unsigned blocks_for(size_t work, int sm_count) {
     return (unsigned)(b < cap ? (b ? b : 1) : cap);
 }
 
+// the pooling pass with the widest loads the window rows allow
+void launch_gn_pool(conv_epi_handle h, const float *y, const conv_epi_epilogue_desc &e, float *out, int Hp, int Wp,
+                    cudaStream_t s) {
+    const conv_epi_desc &d = h->d;
+    const int Ho = h->Ho, Wo = h->Wo, k = e.pool_k;
+    const size_t rows = (size_t)d.N * d.Cout * Hp;
+    const unsigned grid = blocks_for(rows * 32, h->sm_count);
+    auto go = [&](auto kern) {
+        kern<<<grid, kThreads, 0, s>>>(y, out, h->post, e.gamma, e.beta, e.chan_scale, d.N, d.Cout, e.groups, Ho, Wo,
+                                       k, Hp, Wp, e.clamp_lo, e.clamp_hi);
+    };
+    if (k == 4 && Wo % 4 == 0) go(post_gn_pool<4, 4>);
+    else if (k == 4 && Wo % 2 == 0) go(post_gn_pool<4, 2>);
+    else if (k == 4) go(post_gn_pool<4, 1>);
+    else if (k == 2 && Wo % 2 == 0) go(post_gn_pool<2, 2>);
+    else if (k == 2) go(post_gn_pool<2, 1>);
+    else if (k == 1) go(post_gn_pool<1, 1>);
+    else if (k == 3) go(post_gn_pool<3, 1>);
+    else go(post_gn_pool<0, 1>);
+}
+
 }  // namespace
 
 conv_epi_status ensure_post_stats(conv_epi_handle h, int groups) {
@@ -222,9 +291,7 @@ conv_epi_status postpass_gn_units(conv_epi_handle h, const float *y, const float
                                                                        1.0 / ((double)cpg * plane), e.eps);
     CE_CUDA(cudaGetLastError());
     const int Hp = (h->Ho - e.pool_k) / e.pool_k + 1, Wp = (h->Wo - e.pool_k) / e.pool_k + 1;
-    post_gn_pool<<<blocks_for((size_t)d.N * d.Cout * Hp * Wp, h->sm_count), kThreads, 0, s>>>(
-        y, out, h->post, e.gamma, e.beta, e.chan_scale, d.N, d.Cout, e.groups, h->Ho, h->Wo, e.pool_k, Hp, Wp,
-        e.clamp_lo, e.clamp_hi);
+    launch_gn_pool(h, y, e, out, Hp, Wp, s);
     CE_CUDA(cudaGetLastError());
     h->last_launches = 2;
     return CONV_EPI_OK;
@@ -257,9 +324,7 @@ conv_epi_status postpass_forward(conv_epi_handle h, const float *y, const conv_e
                                                                       1.0 / ((double)cpg * plane), e.eps);
         CE_CUDA(cudaGetLastError());
         const int Hp = (h->Ho - e.pool_k) / e.pool_k + 1, Wp = (h->Wo - e.pool_k) / e.pool_k + 1;
-        post_gn_pool<<<blocks_for((size_t)d.N * d.Cout * Hp * Wp, h->sm_count), kThreads, 0, s>>>(
-            y, out, h->post, e.gamma, e.beta, e.chan_scale, d.N, d.Cout, e.groups, h->Ho, h->Wo, e.pool_k, Hp, Wp,
-            e.clamp_lo, e.clamp_hi);
+        launch_gn_pool(h, y, e, out, Hp, Wp, s);
         h->last_launches = 1;
         break;
     }
