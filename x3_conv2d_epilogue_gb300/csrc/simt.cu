@@ -13,7 +13,10 @@
 //
 // Work decomposition (one CTA):
 //   threads  = PG pixel groups x CS channel slots (<= 256)
-//   a thread = 4 consecutive output pixels x 16 output channels per pass
+//   a thread = 4 consecutive output pixels x 16 output channels per pass,
+//              accumulated as 8 channel pairs by the paired fp32 FMA
+//              (fma.rn.f32x2: two FMAs per issued instruction, each rounded
+//              as fmaf, so the bits are those of scalar FMAs)
 //   a pass   = CS*16 channels; passes loop until Cout is covered
 //   staging  = 16 input channels x 3 input rows x (PG*4 + 4) columns of x,
 //              and the matching 16 x 9 x (CS*16) filter taps, in shared memory
@@ -51,6 +54,25 @@ struct SimtArgs {
 };
 
 __device__ __forceinline__ float gelu_erf(float t) { return 0.5f * t * (1.0f + erff(t * 0.70710678118654752f)); }
+
+// two fp32 values as one 64-bit register pair, and the paired FMA on such
+// pairs: each half is fmaf(a, b, c) of its own operands, rounded once, so a
+// paired accumulation gives the same bits as two scalar ones
+__device__ __forceinline__ uint64_t pair(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+    return r;
+}
+__device__ __forceinline__ float2 unpair(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma_pair(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 
 // KIND: conv_epi_kind; PK: pool kernel (GN only; 1, 2 or 4, dividing kPX)
 template <int KIND, int PK>
@@ -110,12 +132,15 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                 }
             }
             for (int r = r0; r < r1; ++r) {
-                float acc[kCO][kPX];
+                // accumulators of channels 2h and 2h + 1 at pixel p, as one
+                // packed pair (acc2[h][p]) for the paired FMA
+                uint64_t acc2[kCO / 2][kPX];
 #pragma unroll
-                for (int c = 0; c < kCO; ++c) {
-                    const float bv = (co0 + c < a.Cout) ? __ldg(&a.b[co0 + c]) : 0.0f;
+                for (int h = 0; h < kCO / 2; ++h) {
+                    const int c = co0 + 2 * h;
+                    const float b0 = c < a.Cout ? __ldg(&a.b[c]) : 0.0f, b1 = c + 1 < a.Cout ? __ldg(&a.b[c + 1]) : 0.0f;
 #pragma unroll
-                    for (int p = 0; p < kPX; ++p) acc[c][p] = bv;
+                    for (int p = 0; p < kPX; ++p) acc2[h][p] = pair(b0, b1);
                 }
                 for (int ci0 = 0; ci0 < a.Cin; ci0 += kCI) {
                     __syncthreads();
@@ -177,24 +202,36 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                             const float *xr = xs + (ci * 3 + kh) * XW + tx * kPX;
                             const float4 xa = *reinterpret_cast<const float4 *>(xr);
                             const float2 xb = *reinterpret_cast<const float2 *>(xr + 4);
-                            const float xv[6] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y};
+                            // each input value twice, as the pair that meets two channels' taps
+                            const uint64_t xd[6] = {pair(xa.x, xa.x), pair(xa.y, xa.y), pair(xa.z, xa.z),
+                                                    pair(xa.w, xa.w), pair(xb.x, xb.x), pair(xb.y, xb.y)};
 #pragma unroll
                             for (int kw = 0; kw < 3; ++kw) {
-                                const float4 *wr = reinterpret_cast<const float4 *>(ws + (ci * 9 + kh * 3 + kw) * COP + ty * kCO);
-                                float wv[kCO];
+                                // the taps of channels 2h, 2h + 1: adjacent in the staged filter
+                                const ulonglong2 *wr =
+                                    reinterpret_cast<const ulonglong2 *>(ws + (ci * 9 + kh * 3 + kw) * COP + ty * kCO);
+                                uint64_t w2[kCO / 2];
 #pragma unroll
                                 for (int q = 0; q < kCO / 4; ++q) {
-                                    const float4 f = wr[q];
-                                    wv[4 * q] = f.x, wv[4 * q + 1] = f.y, wv[4 * q + 2] = f.z, wv[4 * q + 3] = f.w;
+                                    const ulonglong2 f = wr[q];
+                                    w2[2 * q] = f.x, w2[2 * q + 1] = f.y;
                                 }
 #pragma unroll
-                                for (int c = 0; c < kCO; ++c)
+                                for (int h = 0; h < kCO / 2; ++h)
 #pragma unroll
-                                    for (int p = 0; p < kPX; ++p) acc[c][p] = fmaf(wv[c], xv[p + kw], acc[c][p]);
+                                    for (int p = 0; p < kPX; ++p) acc2[h][p] = fma_pair(w2[h], xd[p + kw], acc2[h][p]);
                             }
                         }
                     }
                 }
+                float acc[kCO][kPX];
+#pragma unroll
+                for (int h = 0; h < kCO / 2; ++h)
+#pragma unroll
+                    for (int p = 0; p < kPX; ++p) {
+                        const float2 v = unpair(acc2[h][p]);
+                        acc[2 * h][p] = v.x, acc[2 * h + 1][p] = v.y;
+                    }
 
                 // ---- fold this row into the chain ----
                 const int wbase = wo0 + tx * kPX;
