@@ -18,7 +18,8 @@ Prints ONE JSON line (rank 0).  Metric: TFLOP/s = 2*N*Cout*Ho*Wo*Cin*9 / time.
   roofline   - the forward against the tf32 tensor peak derived from the
                measured bf16 peak (x 1.1/2.25, the nominal dense tf32:bf16
                ratio of the GB300's published rates), and against the
-               measured HBM copy bandwidth
+               measured HBM copy bandwidth; with --mode fp32 against the
+               fp32 FMA rate instead (bound "alu")
   per_config - every other workload timed the same way in the same process:
                TFLOP/s, ms, both roofline fractions, the oracle on the host
                cores and the unfused comparator
@@ -62,6 +63,7 @@ METRIC = "fused conv+epilogue TFLOP/s and % of GB300 TF32 dense peak (1 GPU)"
 TF32_PER_BF16 = 1.1 / 2.25
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_SM_MAX_MHZ = 2070.0  # the GB300 maximum SM clock, where nvidia-smi gave no sample
 
 
 def conv_flops(wl) -> int:
@@ -449,6 +451,7 @@ def main(argv=None):
     flush = (lambda: None) if args.no_flush else L2Flush(torch, stream)
     bf16, hbm, src = peaks()
     tf32_peak = bf16 * TF32_PER_BF16
+    sm_count = torch.cuda.get_device_properties(local).multi_processor_count
 
     # ---- the headline workload: K timed steps, per-step CUDA events ----
     case = Case(wl, args.mode, args.layout, stream)
@@ -547,6 +550,15 @@ def main(argv=None):
         "clocks": clk.summary(),
         "kernel_ms": {"mean": kern_ms, "min": float(np.min(per)), "max": float(np.max(per))},
     }
+    if args.mode == "fp32":
+        # the strict mode runs on the CUDA cores: its roofline is the fp32 FMA
+        # rate (SMs x 128 FMA lanes x 2 flops x the maximum SM clock), and the
+        # tensor kernel's DRAM capture does not describe it
+        sm_max = line["clocks"].get("sm_max_mhz") or FALLBACK_SM_MAX_MHZ
+        fma_peak = sm_count * 128 * 2 * sm_max * 1e-6
+        line["roofline"].update({"bound": "alu", "peak": fma_peak, "frac": rl["tflops"] / fma_peak, "traffic": None,
+                                 "peak_source": f"{sm_count} SMs x 128 fp32 FMA/clk x 2 x {sm_max:.0f} MHz (derived)",
+                                 "kernel": "conv_epi forward (fused fp32 CUDA-core kernel)"})
     print(json.dumps(line), flush=True)
     return 0
 

@@ -19,7 +19,9 @@
 //              as fmaf, so the bits are those of scalar FMAs)
 //   a pass   = CS*16 channels; passes loop until Cout is covered
 //   staging  = 16 input channels x 3 input rows x (PG*4 + 4) columns of x,
-//              and the matching 16 x 9 x (CS*16) filter taps, in shared memory
+//              and the matching 16 x 9 x (CS*16) filter taps, in shared memory,
+//              by asynchronous copies (cp.async; 16-byte ones for x where its
+//              rows are whole 16-byte groups)
 #include <float.h>
 #include <math.h>
 
@@ -32,7 +34,6 @@ constexpr int kCI = 16;  // input channels staged per step
 constexpr int kCO = 16;  // output channels per thread per pass
 constexpr int kPX = 4;   // consecutive output pixels per thread
 constexpr int kRowsPerCta = 4;  // output rows per CTA for the min and per-channel chains
-constexpr int kStageLoads = 4;  // staging loads in flight per thread (8 measured no better)
 // dynamic shared memory per CTA: the 227 KB opt-in less the static group sums
 // and a margin
 constexpr size_t kSmemDynLimit = 227 * 1024 - 2 * 1024;
@@ -74,9 +75,24 @@ __device__ __forceinline__ uint64_t fma_pair(uint64_t a, uint64_t b, uint64_t c)
     return d;
 }
 
+// asynchronous global -> shared copies (cp.async): src_bytes below the copy
+// size zero-fills the rest (0: nothing is read, src need only be a valid
+// address); completed by cp_async_wait_all
+__device__ __forceinline__ void cp_async16(float *dst, const float *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(float *dst, const float *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // KIND: conv_epi_kind; PK: pool kernel (GN only; 1, 2 or 4, dividing kPX)
 template <int KIND, int PK>
-__global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
+__global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 : 2) simt_conv_epi(const SimtArgs a) {
     extern __shared__ float4 smem_f4[];
     float *sm = reinterpret_cast<float *>(smem_f4);
     const int tid = threadIdx.x;
@@ -100,6 +116,10 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
     // when the reductions' scratch (at the start of shared memory) stays
     // below it
     const bool w_once = a.Cin <= kCI && a.Cout <= COP && 2 * CS * TW <= kCI * 3 * XW && 2 * COP * PG <= kCI * 3 * XW;
+    // input rows of whole 16-byte groups (x itself is 16-byte aligned): the
+    // staged rows then start on 16-byte boundaries too (XW and wo0 are
+    // multiples of 4)
+    const bool xv4 = (a.W & 3) == 0;
 
     // GroupNorm per-CTA group partial sums, in a fixed summation order
     __shared__ double gpart[2 * 64];
@@ -144,56 +164,55 @@ __global__ void __launch_bounds__(256) simt_conv_epi(const SimtArgs a) {
                 }
                 for (int ci0 = 0; ci0 < a.Cin; ci0 += kCI) {
                     __syncthreads();
-                    // staging: element i of each tile, its (channel, row or
-                    // tap, column) stepped by the block size without
-                    // divisions, kStageLoads loads in flight per thread before
-                    // their stores
-                    {
+                    // staging by asynchronous copies (every copy of a thread
+                    // in flight at once, no register round trip), zero-filled
+                    // past W, Cin and Cout; element (or 4-float group) i of
+                    // each tile has its (channel, row or tap, column) stepped
+                    // by the block size without divisions
+                    if (xv4) {  // rows of whole 16-byte groups: one copy per 4 columns
+                        const int XW4 = XW >> 2, total = kCI * 3 * XW4;
+                        int col = tid % XW4, rr = (tid / XW4) % 3, ci = tid / (3 * XW4);
+                        for (int i = tid; i < total; i += blockDim.x) {
+                            const int gci = ci0 + ci, gw = wo0 + 4 * col;
+                            const int nv = gci < a.Cin ? max(0, min(4, a.W - gw)) : 0;
+                            const float *src = nv ? a.x + (((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw : a.x;
+                            cp_async16(xs + 4 * i, src, 4 * nv);
+                            col += blockDim.x;
+                            while (col >= XW4) {
+                                col -= XW4;
+                                if (++rr == 3) rr = 0, ++ci;
+                            }
+                        }
+                    } else {
                         const int total = kCI * 3 * XW;
                         int col = tid % XW, rr = (tid / XW) % 3, ci = tid / (3 * XW);
-                        for (int i0 = tid; i0 < total; i0 += kStageLoads * (int)blockDim.x) {
-                            float v[kStageLoads];
-#pragma unroll
-                            for (int k = 0; k < kStageLoads; ++k) {
-                                const int i = i0 + k * (int)blockDim.x;
-                                const int gci = ci0 + ci, gw = wo0 + col;
-                                v[k] = 0.0f;
-                                if (i < total && gci < a.Cin && gw < a.W)
-                                    v[k] = __ldg(&a.x[(((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw]);
-                                col += blockDim.x;
-                                while (col >= XW) {
-                                    col -= XW;
-                                    if (++rr == 3) rr = 0, ++ci;
-                                }
+                        for (int i = tid; i < total; i += blockDim.x) {
+                            const int gci = ci0 + ci, gw = wo0 + col;
+                            const bool ok = gci < a.Cin && gw < a.W;
+                            cp_async4(xs + i, ok ? a.x + (((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw : a.x,
+                                      ok ? 4 : 0);
+                            col += blockDim.x;
+                            while (col >= XW) {
+                                col -= XW;
+                                if (++rr == 3) rr = 0, ++ci;
                             }
-#pragma unroll
-                            for (int k = 0; k < kStageLoads; ++k)
-                                if (i0 + k * (int)blockDim.x < total) xs[i0 + k * blockDim.x] = v[k];
                         }
                     }
                     if (!w_once || (row == row_lo && t == 0 && r == r0)) {
                         const int total = kCI * 9 * COP;
                         int col = tid % COP, tap = (tid / COP) % 9, ci = tid / (9 * COP);
-                        for (int i0 = tid; i0 < total; i0 += kStageLoads * (int)blockDim.x) {
-                            float v[kStageLoads];
-#pragma unroll
-                            for (int k = 0; k < kStageLoads; ++k) {
-                                const int i = i0 + k * (int)blockDim.x;
-                                const int gci = ci0 + ci, gco = cobase + col;
-                                v[k] = 0.0f;
-                                if (i < total && gci < a.Cin && gco < a.Cout)
-                                    v[k] = __ldg(&a.w[((size_t)gco * a.Cin + gci) * 9 + tap]);
-                                col += blockDim.x;
-                                while (col >= COP) {
-                                    col -= COP;
-                                    if (++tap == 9) tap = 0, ++ci;
-                                }
+                        for (int i = tid; i < total; i += blockDim.x) {
+                            const int gci = ci0 + ci, gco = cobase + col;
+                            const bool ok = gci < a.Cin && gco < a.Cout;
+                            cp_async4(ws + i, ok ? a.w + ((size_t)gco * a.Cin + gci) * 9 + tap : a.w, ok ? 4 : 0);
+                            col += blockDim.x;
+                            while (col >= COP) {
+                                col -= COP;
+                                if (++tap == 9) tap = 0, ++ci;
                             }
-#pragma unroll
-                            for (int k = 0; k < kStageLoads; ++k)
-                                if (i0 + k * (int)blockDim.x < total) ws[i0 + k * blockDim.x] = v[k];
                         }
                     }
+                    cp_async_wait_all();
                     __syncthreads();
                     const int nci = min(kCI, a.Cin - ci0);
                     for (int ci = 0; ci < nci; ++ci) {
