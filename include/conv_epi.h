@@ -155,9 +155,10 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *   CONV_EPI_MODE_FP32: any N, Cin, Cout and H, W >= 3.
  *     GN chain: pool_k 1, 2 or 4, at most 64 groups.
  *   CONV_EPI_MODE_TF32: any N, Cin, Cout and H, W >= 3.
- *     GN chain: fused into the conv kernel for pool_k = 4, groups of a
- *     power-of-two number of channels up to 64, and Cout <= 64 with W <= 64
- *     or 66 <= W <= 128 or 130 <= W <= 256, or Cout <= 128 with 66 <= W <= 128;
+ *     GN chain: fused into the conv kernel for groups of a power-of-two
+ *     number of channels up to 64 and either pool_k = 4 with Cout <= 64 and
+ *     W <= 64 or 66 <= W <= 128 or 130 <= W <= 256, or with Cout <= 128 and
+ *     66 <= W <= 128, or pool_k = 2 with Cout <= 64 and 66 <= W <= 128;
  *     any other GN
  *     shape runs as two passes, the tensor-core conv
  *     writing y (bias added) and its per-unit sums of y and y^2 into a

@@ -85,6 +85,11 @@ SMALL = {
     "c5_k2": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=50, pool_k=2),               # 2 x 2 windows, odd tail row
     "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling
     "c5_k2_w300": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=300, pool_k=2, groups=64),  # 2 column tiles, a group per channel
+    # 2 x 2 windows fused (Cout <= 64, W 66..128: two bands of 2 rows per unit)
+    "c5_k2_w128": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=128, pool_k=2),        # 63 windows, a stats-only tail row
+    "c5_k2_w90": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=90, Cout=32, groups=8, pool_k=2),  # P 96, masked chunks
+    "c5_k2_w67": W["c5_gn_pool_clamp"].resized(N=1, H=15, W=67, pool_k=2, groups=1),  # odd Wo: a stats-only column; one group
+    "c5_k2_w66": W["c5_gn_pool_clamp"].resized(N=2, H=9, W=66, Cout=48, groups=12, pool_k=2),  # Wo 64, 48 channels
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 # shapes the tf32 kernel refuses: the call must say so, not fall back

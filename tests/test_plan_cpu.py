@@ -32,7 +32,7 @@ def plan(N, Cin, H, W, Cout, kind, layout=ce.LAYOUT_NCHW, groups=16, pool_k=4):
     return ce.conv_epi_plan_query(N, Cin, H, W, Cout, epi_for(kind, groups, pool_k), layout)
 
 
-def check_plan(q, N, Cin, H, W, Cout, kind, layout):
+def check_plan(q, N, Cin, H, W, Cout, kind, layout, pool_k=4):
     Ho, Wo = H - 2, W - 2
     nhwc = layout == ce.LAYOUT_NHWC
     S, P, U, RU, Rin, PL = q["S"], q["P"], q["U"], q["RU"], q["Rin"], q["PL"]
@@ -133,7 +133,15 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout):
         assert (S == 2 and U in (2, 4) and P <= 128 and (P == 64 or W - 2 >= 64)) or \
             (S == 1 and U == 2 and 64 < P <= 128 and W - 2 >= 64) or \
             (S == 2 and U == 1 and 128 < P <= 256 and W - 2 >= 128)
-        if U == 1:
+        if pool_k == 2:
+            # 2 x 2 windows: two band regions of pitch 65 (up to 63 windows),
+            # the statistics, 128-channel tables; the tile writes reach
+            # (band * 2 + slot) * 64 * 65 + channel * 65 + window (window < 64)
+            assert S == 2 and U == 2
+            top = max((b * 2 + sl) * 64 * 65 + ch * 65 + w for b in (0, 1) for sl in (0, 1) for ch in range(64)
+                      for w in range(64))
+            assert top < 2 * 2 * 64 * 65 and q["scratch_bytes"] >= (2 * 2 * 64 * 65 + 2 * 256 + 2 * 128) * 4
+        elif U == 1:
             # wide rows: one band region of pitch 65 (up to 63 windows), the
             # statistics, 128-channel tables; the tile writes reach
             # slot * 64 * 65 + channel * 65 + window (window < 64)
@@ -182,8 +190,10 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     # pooling half a band; one-band rows need Wo >= 64 (the generalised
     # kernel masks the chunks past column 64)
     cpg = Cout // groups
-    if kind != ce.GN_SCALE_POOL_CLAMP or pool_k != 4 or cpg & (cpg - 1) or cpg > 64:
+    if kind != ce.GN_SCALE_POOL_CLAMP or pool_k not in (2, 4) or cpg & (cpg - 1) or cpg > 64:
         return False
+    if pool_k == 2:  # 2 x 2 windows: two bands per unit, one-band rows, up to 64 channels
+        return Cout <= 64 and 66 <= W <= 128
     # rows of 130..256 columns (Cout <= 64): one row pair per unit
     return (Cout <= 64 and (W <= 64 or 66 <= W <= 128 or 130 <= W <= 256)) or (64 < Cout <= 128 and 66 <= W <= 128)
 
@@ -202,16 +212,17 @@ def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
         assert q["ybuf_bytes"] == ybytes + N * units * 2 * 128 * 8
     else:
         assert q["ybuf_bytes"] == 0
-    check_plan(q, N, Cin, H, W, Cout, ce.NONE if two_pass else kind, layout)
+    check_plan(q, N, Cin, H, W, Cout, ce.NONE if two_pass else kind, layout, pool_k)
 
 
 def test_random_shapes_all_planned_and_in_range():
     """Every shape with H, W >= 3 has a plan (the tf32 mode takes any size),
     and every plan passes the range checks; GroupNorm shapes are fused
-    exactly when pool_k = 4, groups have a power-of-two size up to 64, and
-    Cout <= 64 with W <= 64, 66 <= W <= 128 or 130 <= W <= 256, or
-    64 < Cout <= 128 with 66 <= W <= 128; otherwise they are planned as
-    the plain conv of the two-pass form."""
+    exactly when groups have a power-of-two size up to 64 and either
+    pool_k = 4 with Cout <= 64 and W <= 64, 66 <= W <= 128 or
+    130 <= W <= 256, or 64 < Cout <= 128 with 66 <= W <= 128, or pool_k = 2
+    with Cout <= 64 and 66 <= W <= 128; otherwise they are planned as the
+    plain conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):
         kind = rng.choice([ce.MIN_TANH2, ce.SCALE_MIN, ce.MUL_LRELU_GELU, ce.GN_SCALE_POOL_CLAMP, ce.NONE])
@@ -242,7 +253,7 @@ def test_plan_query_arguments():
         ce._check(ce._lib().conv_epi_plan_query(ce.C.byref(d), ce.C.byref(epi_for(ce.MIN_TANH2)),
                                                 ce.C.byref(q)), "plan")
     assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
-    for bad_kind in (6, 7, 8, 9, -1):                    # bad chain (the kernel's internal kinds included)
+    for bad_kind in (6, 7, 8, 9, 10, -1):                # bad chain (the kernel's internal kinds included)
         with pytest.raises(ce.ConvEpiError) as ei:
             plan(1, 8, 8, 8, 64, bad_kind)
         assert ce.STATUS[ei.value.status] == "INVALID_ARG"

@@ -91,13 +91,17 @@ constexpr int kKindGnXNarrow = 8;
 // half a band, per unit, its up to 63 windows in two passes of 4 chunks per
 // warp (the second masked).
 constexpr int kKindGnWide = 9;
+// ... and 2 x 2 pooling windows (Cout <= 64, rows of 64..126 outputs): each
+// of a unit's two row pairs is a pooling band, 8 windows per 16-column chunk.
+constexpr int kKindGnPool2 = 10;
 __host__ __device__ constexpr bool is_gnx(int kind) {
-    return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide;
+    return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2;
 }
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
 // 96..126 outputs), or the generalised one
-inline int tc_gn_kind(const conv_epi_desc &d) {
+inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
+    if (pool_k == 2 && d.Cout <= 64 && d.W >= 66 && d.W <= 128) return kKindGnPool2;
     if (d.W > 128) return kKindGnWide;
     if (d.W > 64 && d.W - 2 < 96) return kKindGnXNarrow;
     return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX;
@@ -1008,7 +1012,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGnX = is_gnx(KIND);  // the generalised GroupNorm chain
     constexpr bool kWide = KIND == kKindGnWide;  // rows of 130..256 columns: two passes per unit
-    constexpr int kPitch = kWide ? 65 : kPoolPitch;  // pooled tile pitch (up to 63 windows)
+    constexpr bool kPool2 = KIND == kKindGnPool2;  // 2 x 2 windows: a band per u
+    constexpr int kPitch = kWide || kPool2 ? 65 : kPoolPitch;  // pooled tile pitch (up to 63 windows)
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
     // this lane's channel parameters; with more than 128 output channels they
     // belong to the unit's channel tile and are reloaded when it changes
@@ -1053,9 +1058,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // pooling bands of 4 rows per unit: one (rows of 80..128 columns: two u
     // of two row slots) or, in the general instantiation, two (rows of up to
     // 64 columns: four u); 16-column chunks per warp and u: 4 or 2
-    constexpr int kNB = (kGN && GENERAL) ? 2 : 1;
+    // (2 x 2 windows: one band per u, two per unit, 8 windows per chunk
+    // written to the tiles as they are found)
+    constexpr int kNB = (kGN && (GENERAL || kPool2)) ? 2 : 1;
     constexpr int kKC = (kGN && GENERAL) ? 2 : 4;
-    constexpr int kWin = 4 * kKC;  // pooling windows per band and thread
+    constexpr int kWin = 4 * kKC;  // pooling windows per band and thread (4 x 4 windows)
     float *gn_sgn = scratch + kNB * 2 * 64 * kPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + (kGnX ? 128 : 64);
     if (kGN && slot == 0) gn_sgn[co] = gsg, gn_bias[co] = bias;
     // GroupNorm: this thread's chunks are cc = hc + 2 kc.  In the one-band
@@ -1066,7 +1073,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // when column 16 cc + i < Wo.  (A select per value costs as much as the
     // sums, so only the chunks that can be ragged take it.)  gn_ncol counts
     // this thread's valid columns.
-    constexpr int kMask0 = kWide ? 4 : kKC == 4 ? (KIND == kKindGnXNarrow ? 2 : 3) : 0;
+    constexpr int kMask0 = kWide ? 4 : kKC == 4 ? (KIND == kKindGnXNarrow || kPool2 ? 2 : 3) : 0;
     uint32_t gn_rag = 0;
     int gn_ncol = 0;
     if constexpr (kGN) {
@@ -1178,13 +1185,13 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
         // for channels whose affine slope gamma * scale * rstd is negative
         // (rstd > 0, so the sign is known before the statistics).  One array
         // per band, so every index is a compile-time constant.
-        float pext0[kWin], pext1[kNB == 2 ? kWin : 1];
+        float pext0[kWin], pext1[kNB == 2 && !kPool2 ? kWin : 1];
         // sums of w and w^2 in four chains each (two packed pairs)
         uint64_t ls2[2] = {0ull, 0ull}, lss2[2] = {0ull, 0ull};
         if constexpr (kGN) {
 #pragma unroll
             for (int k = 0; k < kWin; ++k) pext0[k] = -INFINITY;
-            if constexpr (kNB == 2) {
+            if constexpr (kNB == 2 && !kPool2) {
 #pragma unroll
                 for (int k = 0; k < kWin; ++k) pext1[k] = -INFINITY;
             }
@@ -1290,6 +1297,57 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     tmem_ld_wait2(f[2], f[3]);
                     if (row_ok) gn_step_w(f, pext0);
                     put_w(1);
+                }
+            } else if constexpr (kPool2) {
+                // two u (rows r0 + 2u, r0 + 2u + 1 in the two row slots), each
+                // one pooling band, so a chunk's 8 window maxima are final
+                // once it is processed: they go to the band's tile at once
+                // (a band with a row at or past Ho is never stored, so such
+                // a row writes nothing).  Every warp is past the previous
+                // unit's tile and statistics reads (and none has given up)
+                // before the first tile write.
+                if (epi_bar_any(false)) {
+                    gn_quit = true;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const bool row_ok = r0 + 2 * u + slot < a.Ho;  // the same for the whole warp
+                        gn_rows += row_ok ? 1 : 0;
+                        Frag16 f[kKC];
+#pragma unroll
+                        for (int kc = 0; kc < kKC; ++kc)
+                            if (hc + 2 * kc < nchunks) tmem_ld16_issue(tbase + u * a.ucol + (hc + 2 * kc) * 16, f[kc]);
+                        tmem_ld_wait2(f[0], f[1]);
+                        tmem_ld_wait2(f[2], f[3]);
+                        if (!row_ok) continue;
+                        float *pt = scratch + (u * 2 + slot) * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch;
+#pragma unroll
+                        for (int kc = 0; kc < kKC; ++kc) {
+                            uint64_t v2[8];
+#pragma unroll
+                            for (int p = 0; p < 8; ++p) v2[p] = pack2(f[kc].r[2 * p], f[kc].r[2 * p + 1]);
+                            const int pw0 = (hc + 2 * kc) * 8;  // this chunk's first window
+#pragma unroll
+                            for (int wi = 0; wi < 8; ++wi) {
+                                const float2 a01 = unpack2(v2[wi]);
+                                if (pw0 + wi < 64) pt[pw0 + wi] = fmaxf(a01.x, a01.y);
+                            }
+                            if (kc >= kMask0) {  // columns >= Wo add nothing to the sums
+#pragma unroll
+                                for (int p = 0; p < 8; ++p) {
+                                    const uint32_t b0 = 1u << (16 * (kc - kMask0) + 2 * p);
+                                    const float2 w = unpack2(v2[p]);
+                                    v2[p] = pack2(__float_as_uint((gn_rag & b0) ? w.x : 0.0f),
+                                                  __float_as_uint((gn_rag & (b0 << 1)) ? w.y : 0.0f));
+                                }
+                            }
+#pragma unroll
+                            for (int p = 0; p < 8; ++p) {
+                                ls2[p & 1] = add2u(ls2[p & 1], v2[p]);
+                                lss2[p & 1] = fma2u(v2[p], v2[p], lss2[p & 1]);
+                            }
+                        }
+                    }
                 }
             } else
             for (int u = 0; u < a.U; ++u) {
@@ -1431,7 +1489,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // stores fold the two slots
             // every warp is past the previous unit's tile and statistics reads
             // (and none has given up) before they are rewritten
-            if (!kWide && epi_bar_any(false)) break;  // (wide rows voted before their first pass's tile)
+            if (!kWide && !kPool2 && epi_bar_any(false)) break;  // (wide rows, 2 x 2 windows: voted before their first tile)
             float *st = scratch + kNB * 2 * 64 * kPitch;  // [2 stats][8 warps][32 lanes]
             st[ew * 32 + lane] = gs;
             st[kEpiThreads + ew * 32 + lane] = gss;
@@ -1446,7 +1504,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
                 }
             };
-            if constexpr (!kWide) {
+            if constexpr (!kWide && !kPool2) {
                 put_tile(0, pext0);
                 if constexpr (kNB == 2) put_tile(1, pext1);
             }
@@ -1481,7 +1539,33 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         make_float2(s0, s1);
                 }
             }
-            if constexpr (kWide) {
+            if constexpr (kPool2) {
+                // bands 2 ru and 2 ru + 1, each the two row slots folded, sign
+                // and bias restored; windows lane and lane + 32
+#pragma unroll
+                for (int band = 0; band < 2; ++band) {
+                    const int prow = ru * 2 + band;
+                    if (prow < a.Hp) {
+                        const float *pt0 = scratch + band * 2 * 64 * kPitch, *pt1 = pt0 + 64 * kPitch;
+                        float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
+                        const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+#pragma unroll
+                        for (int hw = 0; hw < 2; ++hw) {
+                            const int w = lane + 32 * hw;
+                            if (w >= a.Wp) continue;
+                            float m[64 / kEpiWarps];
+#pragma unroll
+                            for (int i = 0; i < 64 / kEpiWarps; ++i) {
+                                const int c2 = ew + kEpiWarps * i;
+                                m[i] = fmaf(gn_sgn[c2], fmaxf(pt0[c2 * kPitch + w], pt1[c2 * kPitch + w]), gn_bias[c2]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 64 / kEpiWarps; ++i)
+                                if (ew + kEpiWarps * i < a.Co) dst[i * cstep + w] = m[i];
+                        }
+                    }
+                }
+            } else if constexpr (kWide) {
                 // half band ru / 2, two row slots folded, sign and bias
                 // restored, into slot ru & 1; windows lane and lane + 32
                 const int prow = ru >> 1;
@@ -1851,6 +1935,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
     case kKindGnWide:  // one band region of pitch 65, the statistics, the tables
         return (uint32_t)((2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
+    case kKindGnPool2:  // two band regions of pitch 65, the statistics, the tables
+        return (uint32_t)((2 * 2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnX:  // (the tables for up to 128 channels)
     case kKindGnXNarrow:
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 128) * sizeof(float));
@@ -2029,10 +2115,13 @@ conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStre
 // warp; Wo >= 96 in the page-shape kernel, Wo >= 64 in the generalised one,
 // which masks one chunk more), two with P = 64 (2 chunks).  65..128 channels
 // (one slot of 128, P in 80..128, Wo >= 64): half a band per unit, folded by
-// the finalize.  Other GroupNorm shapes run as two passes (tc_forward).
+// the finalize.  Rows of 128..254 outputs (up to 64 channels): one row pair
+// per unit, half a band.  2x2 windows (up to 64 channels, Wo 64..126): two
+// bands of 2 rows per unit.  Other GroupNorm shapes run as two passes
+// (tc_forward).
 bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     Plan pl;
-    const int kind = tc_gn_kind(d);
+    const int kind = tc_gn_kind(d, e.pool_k);
     if (!make_plan(d, kind, pl)) return false;
     // one-band rows: the unmasked chunks must be whole (see the epilogue)
     const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= (kind == kKindGnXNarrow ? 64 : 96);
@@ -2048,15 +2137,19 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // (Cout below 64 or 128 runs as a 64- or 128-channel GEMM with zero
     // filters; a group's channels must be a power-of-two run of lanes, at
     // most 64, for the shuffle sums and the fold)
+    // 2 x 2 windows (Cout <= 64): the one-band layout, two bands per unit,
+    // the first 64 output columns whole
+    const bool pool2 = kind == kKindGnPool2 && pl.S == 2 && pl.RU == 4 && pl.P > 64 && pl.P <= 128 && d.W - 2 >= 64;
     const int cpg = d.Cout / e.groups;
-    return e.pool_k == 4 && (one_band || two_bands || half_band || wide_rows) && (cpg & (cpg - 1)) == 0 && cpg <= 64;
+    const bool shape = e.pool_k == 4 ? (one_band || two_bands || half_band || wide_rows) : e.pool_k == 2 && pool2;
+    return shape && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
 
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
     Plan pl;
     int kind = e ? e->kind : CONV_EPI_MIN_TANH2;
     // a GroupNorm shape the fused epilogue does not take needs the plain conv
-    if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP) kind = tc_gn_fused(d, *e) ? tc_gn_kind(d) : CONV_EPI_NONE;
+    if (kind == CONV_EPI_GN_SCALE_POOL_CLAMP) kind = tc_gn_fused(d, *e) ? tc_gn_kind(d, e->pool_k) : CONV_EPI_NONE;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     return CONV_EPI_OK;
 }
@@ -2088,7 +2181,7 @@ conv_epi_status tc_plan_query(const conv_epi_desc &d, const conv_epi_epilogue_de
     // a GroupNorm shape the fused epilogue does not take: the plain conv's
     // plan (its first pass)
     const bool two_pass = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !tc_gn_fused(d, e);
-    const int kind = two_pass ? CONV_EPI_NONE : e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP ? tc_gn_kind(d) : e.kind;
+    const int kind = two_pass ? CONV_EPI_NONE : e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP ? tc_gn_kind(d, e.pool_k) : e.kind;
     q.gn_two_pass = two_pass ? 1 : 0;
     if (!make_plan(d, kind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     q.gemm_cout = pl.Cg, q.S = pl.S, q.P = pl.P, q.U = pl.U, q.RU = pl.RU, q.Rin = pl.Rin, q.PL = pl.PL;
@@ -2165,7 +2258,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         return CONV_EPI_OK;
     }
     // the kernel: the GroupNorm chain's page-shape or generalised instantiation
-    const int kkind = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP ? tc_gn_kind(d) : e.kind;
+    const int kkind = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP ? tc_gn_kind(d, e.pool_k) : e.kind;
     Plan pl;
     if (!make_plan(d, kkind, pl)) return CONV_EPI_ERR_UNSUPPORTED;
     EncodeTiledFn enc = encode_tiled();
@@ -2251,7 +2344,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
-        if (h->gn.units != a.units_per_img || a.Wp > (kkind == kKindGnWide ? 64 : 32)) return CONV_EPI_ERR_INVALID_ARG;
+        if (h->gn.units != a.units_per_img || a.Wp > (kkind == kKindGnWide || kkind == kKindGnPool2 ? 64 : 32))
+            return CONV_EPI_ERR_INVALID_ARG;
         // finalize inside the kernel when each (image, group) block of pooled
         // values is whole float4s (16-byte aligned blocks) and small enough
         // for the multiply-high divisions (t < 2^18 pooled float4 per batch,
@@ -2288,6 +2382,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
             return kkind == kKindGnX         ? launch_tc<kKindGnX>(args, pl, grid, s)
                    : kkind == kKindGnXNarrow ? launch_tc<kKindGnXNarrow>(args, pl, grid, s)
                    : kkind == kKindGnWide    ? launch_tc<kKindGnWide>(args, pl, grid, s)
+                   : kkind == kKindGnPool2   ? launch_tc<kKindGnPool2>(args, pl, grid, s)
                                              : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
         };
         st = launch_gn();
