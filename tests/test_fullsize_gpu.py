@@ -141,3 +141,40 @@ def test_full_size_fp32_indices(wl_name):
         got_idx = idx.cpu().numpy()[n, 0, i, j]
         ties += check_index(got_idx, ref_idx, gap_at_points(t, wl, n, i, j), f"{wl_name} sampled")
     assert ties <= 16, f"{ties} near-tie index differences"
+
+
+# GroupNorm shapes beyond the page's, at the page's batch and image size (the
+# generalised kernel instantiations, whose finalize runs a ring of pair
+# slots that turns over several times per CTA): every pooled output of a few
+# whole (image, group) pairs against the oracle, among them the pairs that
+# land in the ring's last slots
+GN_WIDE = {
+    "c5_pool2": synth.WORKLOADS["c5_gn_pool_clamp"].resized(pool_k=2),                 # 2x2 windows
+    "c5_co128": synth.WORKLOADS["c5_gn_pool_clamp"].resized(Cout=128, groups=16),      # half bands
+    "c5_w256": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=32, H=256, W=256),        # wide rows
+}
+
+
+@pytest.mark.parametrize("case", sorted(GN_WIDE))
+def test_full_batch_generalised_groupnorm(case):
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = GN_WIDE[case]
+    t = synth.make_inputs(wl, seed=0)
+    out, _ = run(wl, torch_inputs(t), ce.MODE_TF32)
+    import torch
+    assert bool(torch.isfinite(out).all()), "non-finite outputs"
+    assert float(out.min()) >= wl.clamp_lo and float(out.max()) <= wl.clamp_hi
+    ch = oracle.chain_for(wl, t)
+    cpg = wl.Cout // wl.groups
+    npairs = wl.N * wl.groups
+    # pair p is finalized by CTA p % 152 as its (p // 152)-th pair
+    picks = [0, npairs - 1, min(npairs - 1, 12 * 152 + 5), min(npairs - 1, 7 * 152 + 100)]
+    refs, gots = [], []
+    for p in picks:
+        n, g = divmod(p, wl.groups)
+        r, _, _, _ = oracle.gn_group(t.x, t.w, t.b, ch, n, g)
+        refs.append(r.ravel())
+        gots.append(out[n, g * cpg:(g + 1) * cpg].cpu().numpy().ravel())
+    ref, got = np.concatenate(refs), np.concatenate(gots)
+    ok, err = close(got, ref, "tf32")
+    assert ok.all(), f"{case}: {int((~ok).sum())} of {ok.size} outputs off; max err {err.max():.3g}"

@@ -1646,17 +1646,25 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 // resident and a grid-wide arrival count is safe to wait on).  After every
 // CTA has stored its units' partial sums and pooled extremes and released
 // tensor memory, CTA b takes the (image, group) pairs b, b + gridDim.x, ...
-// in batches of up to one pair per warp, as many as the (now free) shared
-// memory holds.  Thread 0 bulk-copies the batch's pooled blocks (contiguous,
-// F4 float4 each) into shared memory, while one warp per pair folds its
+// Thread 0 bulk-copies their pooled blocks (contiguous, F4 float4 each) into
+// the (now free) shared memory, while one warp per pair folds its
 // statistics and its channels' coefficients; every thread then applies
 // z = clamp(A y + B) in place, and thread 0 bulk-copies the blocks out to
-// the output.  The copies keep the whole batch in flight at once, where
-// per-thread loads left the pass latency-bound.
+// the output.  The copies keep whole blocks in flight, where per-thread
+// loads left the pass latency-bound.  The page-shape kernel takes the pairs
+// in batches of up to one per warp, as many as shared memory holds (for its
+// 15 KB blocks, nearly all of a CTA's pairs at once).  The generalised
+// kinds, whose blocks are up to four times larger, run a ring of pair slots
+// instead: the copy of pair k + cap goes out as soon as pair k's block has
+// been copied out, so later pairs' loads overlap earlier pairs' apply and
+// stores (x[128,8,128,128] with 2x2 windows 235 -> 203 us, Cout 128
+// 236 -> 222; the ring measured 5 us slower for the page shape's small
+// blocks, and rounds of several pairs slower for both).
 constexpr int kFinPairs = kThreads / 32;
 constexpr uint32_t kFinFlagOff = kFinPairs * 64 * 2 * 4;  // after the coefficient tables
-constexpr uint32_t kFinBarOff = kFinFlagOff + 8;
+constexpr uint32_t kFinBarOff = kFinFlagOff + 8;         // an mbarrier per batch (or per ring slot)
 constexpr uint32_t kFinBufOff = 8448;                     // the pooled blocks (128-byte aligned)
+static_assert(kFinBarOff + 8u * kFinPairs <= kFinBufOff, "finalize barriers overlap the pooled blocks");
 template <bool kGnX>
 __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, volatile int *abort_flag) {
     float *sA = reinterpret_cast<float *>(smem), *sB = sA + kFinPairs * 64;
@@ -1698,74 +1706,161 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     // (with half bands, a pair's two slots side by side: [pair][slot][F4])
     // (a unit of 2 rows holds half a band: 65..128 channels, or rows of 130..256 columns)
     const uint32_t nsl = kGnX && a.RU == 2 ? 2u : 1u, sbytes = nsl * pbytes;
-    const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / sbytes));  // >= 1: checked on the host
-    uint32_t phase = 0;
-    for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * cap) {
-        const int nbp = min(cap, (npairs - p0 + (int)gridDim.x - 1) / (int)gridDim.x);  // pairs in this batch
-        if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(fbar, (uint32_t)nbp * sbytes);
-            for (int j = 0; j < nbp; ++j)
-                for (uint32_t sl = 0; sl < nsl; ++sl) {
-                    const char *src = reinterpret_cast<const char *>(sl ? a.gn.pmin : a.gn.pmax) +
-                                      (size_t)(p0 + j * (int)gridDim.x) * pbytes;
-                    const uint32_t dsm = smem_u32(buf) + (uint32_t)j * sbytes + sl * pbytes;
-                    for (uint32_t off = 0; off < pbytes; off += 16384u)
-                        bulk_g2s(dsm + off, src + off, min(16384u, pbytes - off), fbar);
-                }
-        }
-        const int p = p0 + warp * (int)gridDim.x;
-        if (warp < nbp) {
-            const int n = p / a.groups, g = p % a.groups;
-            float mean, rstd;
-            gn_group_stats_f(reinterpret_cast<const float *>(a.gn.part), a.units_per_img, a.groups, n, g, a.cnt,
-                             a.eps, mean, rstd);
-            for (int cl = lane; cl < cpg; cl += 32) {
-                const int c = g * cpg + cl;
-                gn_coeffs(__ldg(&a.gamma[c]), __ldg(&a.beta[c]), __ldg(&a.chan_scale[c]), mean, rstd,
-                          sA[warp * 64 + cl], sB[warp * 64 + cl]);
-            }
-        }
-        const bool landed = wait_bar(fbar, phase, abort_flag, a.err, false);
-        phase ^= 1u;
-        if (__syncthreads_or(!landed)) return;  // (also publishes the coefficients)
-        const uint32_t total = (uint32_t)nbp * F4;
-        for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
-            const uint32_t jb = __umulhi(t, a.f4_magic);  // t / F4: the pair within the batch
-            const float *cA = sA + jb * 64, *cB = sB + jb * 64;
-            const uint32_t fo = t - jb * F4, e = 4u * fo;
-            float4 *bp = buf + jb * nsl * F4 + fo;
-            const float4 v = bp[0];
-            float r[4] = {v.x, v.y, v.z, v.w};
-            if (kGnX && a.RU == 2) {
-                // the band's extreme from its two halves: the larger y where
-                // the slope A is >= 0, else the smaller
-                const float4 w = bp[F4];
-                const float h2[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t cl = __umulhi(e + q, a.per_magic);
-                    r[q] = cA[cl] >= 0.0f ? fmaxf(r[q], h2[q]) : fminf(r[q], h2[q]);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
-                r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
-            }
-            bp[0] = make_float4(r[0], r[1], r[2], r[3]);
-        }
-        fence_proxy_async_smem();  // these writes before the copies' reads
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int j = 0; j < nbp; ++j) {
-                char *dst = reinterpret_cast<char *>(a.out) + (size_t)(p0 + j * (int)gridDim.x) * pbytes;
+    if constexpr (kGnX) {
+        // this CTA's pairs p = blockIdx.x + k * gridDim.x (k < K) through a ring
+        // of cap slots: pair k lands in slot k % cap, and the copy of pair
+        // k + cap goes out as soon as pair k's block has been copied out of it.
+        // (The slots end below the main loop's barriers and flags, which the
+        // ring must not overlay: a variant whose slots lay over them lost 8
+        // bytes of a block between the apply and the copy out.)
+        const int cap = min(kFinPairs, (int)((a.bar_off - kFinBufOff) / sbytes));  // >= 1: checked on the host
+        const int K = npairs > (int)blockIdx.x ? (npairs - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+        auto issue = [&](int k) {
+            const int sl = k % cap;
+            const size_t p = (size_t)blockIdx.x + (size_t)k * gridDim.x;
+            mbar_arrive_expect_tx(fbar + 8u * (uint32_t)sl, sbytes);
+            for (uint32_t h = 0; h < nsl; ++h) {
+                const char *src = reinterpret_cast<const char *>(h ? a.gn.pmin : a.gn.pmax) + p * pbytes;
+                const uint32_t dsm = smem_u32(buf) + (uint32_t)sl * sbytes + h * pbytes;
                 for (uint32_t off = 0; off < pbytes; off += 16384u)
-                    bulk_s2g(dst + off, smem_u32(buf) + (uint32_t)j * sbytes + off, min(16384u, pbytes - off));
+                    bulk_g2s(dsm + off, src + off, min(16384u, pbytes - off), fbar + 8u * (uint32_t)sl);
             }
-            bulk_commit();
-            bulk_wait_read();  // the buffer is read: the next batch (or the exit) may reuse it
+        };
+        if (threadIdx.x == 0) {
+            for (int sl = 1; sl < cap; ++sl) mbar_init(fbar + 8u * (uint32_t)sl, 1);  // (slot 0's is set up above)
+            fence_mbar_init();
+            for (int k = 0; k < min(cap, K); ++k) issue(k);
         }
-        __syncthreads();  // (and the next batch rewrites the coefficients)
+        uint32_t phases = 0;  // bit sl: the parity of slot sl's next completion
+        for (int k = 0; k < K; ++k) {
+            if (k % kFinPairs == 0) {
+                // the coefficients of pairs k .. k + kFinPairs - 1, one warp per
+                // pair, while their copies are in flight
+                __syncthreads();  // (the barriers are set up; the tables' previous readers are done)
+                const int kk = k + warp;
+                if (kk < K) {
+                    const int p = (int)blockIdx.x + kk * (int)gridDim.x;
+                    const int n = p / a.groups, g = p % a.groups;
+                    float mean, rstd;
+                    gn_group_stats_f(reinterpret_cast<const float *>(a.gn.part), a.units_per_img, a.groups, n, g, a.cnt,
+                                     a.eps, mean, rstd);
+                    for (int cl = lane; cl < cpg; cl += 32) {
+                        const int c = g * cpg + cl;
+                        gn_coeffs(__ldg(&a.gamma[c]), __ldg(&a.beta[c]), __ldg(&a.chan_scale[c]), mean, rstd,
+                                  sA[warp * 64 + cl], sB[warp * 64 + cl]);
+                    }
+                }
+            }
+            const int sl = k % cap;
+            const bool landed = wait_bar(fbar + 8u * (uint32_t)sl, (phases >> sl) & 1u, abort_flag, a.err, false);
+            phases ^= 1u << sl;
+            if (__syncthreads_or(!landed)) return;  // (also publishes the coefficients)
+            const float *cA = sA + (k % kFinPairs) * 64, *cB = sB + (k % kFinPairs) * 64;
+            float4 *bp0 = buf + (uint32_t)sl * nsl * F4;
+            for (uint32_t t = threadIdx.x; t < F4; t += kThreads) {
+                const uint32_t e = 4u * t;
+                float4 *bp = bp0 + t;
+                const float4 v = bp[0];
+                float r[4] = {v.x, v.y, v.z, v.w};
+                if (a.RU == 2) {
+                    // the band's extreme from its two halves: the larger y where
+                    // the slope A is >= 0, else the smaller
+                    const float4 w = bp[F4];
+                    const float h2[4] = {w.x, w.y, w.z, w.w};
+    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t cl = __umulhi(e + q, a.per_magic);
+                        r[q] = cA[cl] >= 0.0f ? fmaxf(r[q], h2[q]) : fminf(r[q], h2[q]);
+                    }
+                }
+    #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
+                    r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
+                }
+                bp[0] = make_float4(r[0], r[1], r[2], r[3]);
+            }
+            fence_proxy_async_smem();  // these writes before the copy's reads
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                char *dst = reinterpret_cast<char *>(a.out) + ((size_t)blockIdx.x + (size_t)k * gridDim.x) * pbytes;
+                for (uint32_t off = 0; off < pbytes; off += 16384u)
+                    bulk_s2g(dst + off, smem_u32(buf) + (uint32_t)sl * sbytes + off, min(16384u, pbytes - off));
+                bulk_commit();
+                bulk_wait_read();  // slot sl is copied out: pair k + cap (or the exit) may reuse it
+                if (k + cap < K) issue(k + cap);
+            }
+        }
+    } else {
+        const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / sbytes));  // >= 1: checked on the host
+        uint32_t phase = 0;
+        for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * cap) {
+            const int nbp = min(cap, (npairs - p0 + (int)gridDim.x - 1) / (int)gridDim.x);  // pairs in this batch
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(fbar, (uint32_t)nbp * sbytes);
+                for (int j = 0; j < nbp; ++j)
+                    for (uint32_t sl = 0; sl < nsl; ++sl) {
+                        const char *src = reinterpret_cast<const char *>(sl ? a.gn.pmin : a.gn.pmax) +
+                                          (size_t)(p0 + j * (int)gridDim.x) * pbytes;
+                        const uint32_t dsm = smem_u32(buf) + (uint32_t)j * sbytes + sl * pbytes;
+                        for (uint32_t off = 0; off < pbytes; off += 16384u)
+                            bulk_g2s(dsm + off, src + off, min(16384u, pbytes - off), fbar);
+                    }
+            }
+            const int p = p0 + warp * (int)gridDim.x;
+            if (warp < nbp) {
+                const int n = p / a.groups, g = p % a.groups;
+                float mean, rstd;
+                gn_group_stats_f(reinterpret_cast<const float *>(a.gn.part), a.units_per_img, a.groups, n, g, a.cnt,
+                                 a.eps, mean, rstd);
+                for (int cl = lane; cl < cpg; cl += 32) {
+                    const int c = g * cpg + cl;
+                    gn_coeffs(__ldg(&a.gamma[c]), __ldg(&a.beta[c]), __ldg(&a.chan_scale[c]), mean, rstd,
+                              sA[warp * 64 + cl], sB[warp * 64 + cl]);
+                }
+            }
+            const bool landed = wait_bar(fbar, phase, abort_flag, a.err, false);
+            phase ^= 1u;
+            if (__syncthreads_or(!landed)) return;  // (also publishes the coefficients)
+            const uint32_t total = (uint32_t)nbp * F4;
+            for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
+                const uint32_t jb = __umulhi(t, a.f4_magic);  // t / F4: the pair within the batch
+                const float *cA = sA + jb * 64, *cB = sB + jb * 64;
+                const uint32_t fo = t - jb * F4, e = 4u * fo;
+                float4 *bp = buf + jb * nsl * F4 + fo;
+                const float4 v = bp[0];
+                float r[4] = {v.x, v.y, v.z, v.w};
+                if (kGnX && a.RU == 2) {
+                    // the band's extreme from its two halves: the larger y where
+                    // the slope A is >= 0, else the smaller
+                    const float4 w = bp[F4];
+                    const float h2[4] = {w.x, w.y, w.z, w.w};
+    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t cl = __umulhi(e + q, a.per_magic);
+                        r[q] = cA[cl] >= 0.0f ? fmaxf(r[q], h2[q]) : fminf(r[q], h2[q]);
+                    }
+                }
+    #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
+                    r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
+                }
+                bp[0] = make_float4(r[0], r[1], r[2], r[3]);
+            }
+            fence_proxy_async_smem();  // these writes before the copies' reads
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                for (int j = 0; j < nbp; ++j) {
+                    char *dst = reinterpret_cast<char *>(a.out) + (size_t)(p0 + j * (int)gridDim.x) * pbytes;
+                    for (uint32_t off = 0; off < pbytes; off += 16384u)
+                        bulk_s2g(dst + off, smem_u32(buf) + (uint32_t)j * sbytes + off, min(16384u, pbytes - off));
+                }
+                bulk_commit();
+                bulk_wait_read();  // the buffer is read: the next batch (or the exit) may reuse it
+            }
+            __syncthreads();  // (and the next batch rewrites the coefficients)
+        }
     }
 }
 
@@ -2352,7 +2447,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         // channel offsets < 2^16); otherwise the separate finalize kernel
         const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
         a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
-                    F * 4u * (pl.RU == 2 ? 2u : 1u) <= pl.smem - kFinBufOff &&  // one pair's blocks fit the buffer
+                    // one pair's blocks fit the buffer (the generalised kinds' ring ends below the barriers)
+                    F * 4u * (pl.RU == 2 ? 2u : 1u) <= (is_gnx(kkind) ? pl.bar_off : (uint32_t)pl.smem) - kFinBufOff &&
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
