@@ -90,6 +90,7 @@ SMALL = {
     "c5_k2_w90": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=90, Cout=32, groups=8, pool_k=2),  # P 96, masked chunks
     "c5_k2_w67": W["c5_gn_pool_clamp"].resized(N=1, H=15, W=67, pool_k=2, groups=1),  # odd Wo: a stats-only column; one group
     "c5_k2_w66": W["c5_gn_pool_clamp"].resized(N=2, H=9, W=66, Cout=48, groups=12, pool_k=2),  # Wo 64, 48 channels
+    "c5_k2_g64": W["c5_gn_pool_clamp"].resized(N=2, H=12, W=100, groups=64, pool_k=2),  # a group per channel: 245-float blocks, separate finalize
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 # shapes the tf32 kernel refuses: the call must say so, not fall back
