@@ -104,7 +104,8 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout, pool_k=4):
     else:
         assert q["xpad_bytes"] == 0
     # shared memory: filter (resident: every chunk), B planes, staged tiles,
-    # barriers, scratch, in order and disjoint, within the CTA limit
+    # scratch, barriers (last: the GroupNorm finalize reuses what lies below
+    # them), in order and disjoint, within the CTA limit
     filt = (q["chunks"] * q["MT"] if q["resident"] else q["na"]) * q["a_bytes"]
     if q["resident"]:
         assert q["MT"] == 1 and q["na"] == 1
@@ -113,9 +114,9 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout, pool_k=4):
     assert 2 <= q["nb"] <= 4 and q["nr"] <= 4
     assert q["a_off"] == 0 and q["b_off"] >= filt
     assert q["raw_off"] >= q["b_off"] + q["nb"] * q["b_bytes"]
-    assert q["bar_off"] >= q["raw_off"] + q["nr"] * q["raw_bytes"]
-    assert q["scratch_off"] >= q["bar_off"] + q["bar_bytes"] + 8
-    assert q["smem"] >= q["scratch_off"] + q["scratch_bytes"]
+    assert q["scratch_off"] >= q["raw_off"] + q["nr"] * q["raw_bytes"]
+    assert q["bar_off"] >= q["scratch_off"] + q["scratch_bytes"]
+    assert q["smem"] >= q["bar_off"] + q["bar_bytes"] + 8
     assert q["smem"] <= q["smem_limit"] <= 232448
     assert q["b_off"] % 1024 == 0 and q["raw_off"] % 1024 == 0 and q["bar_off"] % 8 == 0
     assert q["scratch_off"] % 16 == 0

@@ -141,7 +141,6 @@ struct Cfg {
     int nhwc;       // channels-last input: tiles go straight into the B planes (no staging, no converters)
     // GroupNorm chain finalized inside this kernel (cooperative launch)
     int gn_fin;
-    uint32_t smem_bytes;  // the launch's dynamic shared memory (free for the finalize after the main loop)
     const float *beta;
     float eps, lo, hi;
     float cnt;            // C/groups * Ho * Wo
@@ -1650,8 +1649,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 // the (now free) shared memory, while one warp per pair folds its
 // statistics and its channels' coefficients; every thread then applies
 // z = clamp(A y + B) in place, and thread 0 bulk-copies the blocks out to
-// the output.  The copies keep whole blocks in flight, where per-thread
-// loads left the pass latency-bound.  The page-shape kernel takes the pairs
+// the output.  The blocks take the shared memory from kFinBufOff up to the
+// main loop's barriers and flags, which sit at the end of the layout (a
+// variant whose blocks lay over them lost 8 bytes of a block between the
+// apply and the copy out).  The copies keep whole blocks in flight, where
+// per-thread loads left the pass latency-bound.  The page-shape kernel takes the pairs
 // in batches of up to one per warp, as many as shared memory holds (for its
 // 15 KB blocks, nearly all of a CTA's pairs at once).  The generalised
 // kinds, whose blocks are up to four times larger, run a ring of pair slots
@@ -1710,9 +1712,6 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
         // this CTA's pairs p = blockIdx.x + k * gridDim.x (k < K) through a ring
         // of cap slots: pair k lands in slot k % cap, and the copy of pair
         // k + cap goes out as soon as pair k's block has been copied out of it.
-        // (The slots end below the main loop's barriers and flags, which the
-        // ring must not overlay: a variant whose slots lay over them lost 8
-        // bytes of a block between the apply and the copy out.)
         const int cap = min(kFinPairs, (int)((a.bar_off - kFinBufOff) / sbytes));  // >= 1: checked on the host
         const int K = npairs > (int)blockIdx.x ? (npairs - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
         auto issue = [&](int k) {
@@ -1792,7 +1791,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
             }
         }
     } else {
-        const int cap = min(kFinPairs, (int)((a.smem_bytes - kFinBufOff) / sbytes));  // >= 1: checked on the host
+        const int cap = min(kFinPairs, (int)((a.bar_off - kFinBufOff) / sbytes));  // >= 1: checked on the host
         uint32_t phase = 0;
         for (int p0 = blockIdx.x; p0 < npairs; p0 += (int)gridDim.x * cap) {
             const int nbp = min(cap, (npairs - p0 + (int)gridDim.x - 1) / (int)gridDim.x);  // pairs in this batch
@@ -2041,8 +2040,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
 
 uint32_t up1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 
-// Shared memory: [filter: resident or ring][B ring][staged-tile ring][mbarriers,
-// tmem slot, abort flag][epilogue scratch]
+// Shared memory: [filter: resident or ring][B ring][staged-tile ring][epilogue
+// scratch][mbarriers, tmem slot, abort flag]
 // the GEMM's output-channel count per channel tile: a problem Cout up to 64
 // runs as 64 (two stacked row slots), larger ones as tiles of 128, with zero
 // filters for the rest
@@ -2093,7 +2092,7 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.b_bytes = up1k(2u * pl.PL * 16u);
     pl.raw_bytes = nhwc ? 0u : up1k(8u * pl.Rin * pl.BW * 4u);  // channels last: no staging ring
     pl.scratch_bytes = scratch_bytes_for(kind, pl.U, pl.P);
-    const uint32_t tail = 8u * Bars::kCount + 16u + pl.scratch_bytes;
+    const uint32_t tail = 8u * Bars::kCount + 32u + pl.scratch_bytes;  // (scratch, barriers, slot, flag, alignment)
     auto total = [&](int na, int nb, int nr) {
         return (size_t)na * pl.a_bytes + (size_t)nb * pl.b_bytes + (size_t)nr * pl.raw_bytes + tail;
     };
@@ -2117,9 +2116,11 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     pl.a_off = 0;
     pl.b_off = pl.na * pl.a_bytes;
     pl.raw_off = pl.b_off + pl.nb * pl.b_bytes;
-    pl.bar_off = pl.raw_off + pl.nr * pl.raw_bytes;
-    pl.scratch_off = (pl.bar_off + 8u * Bars::kCount + 8u + 15u) & ~15u;
-    pl.smem = pl.scratch_off + pl.scratch_bytes;
+    // (the barriers, the tensor-memory slot and the abort flag last: the
+    // GroupNorm finalize reuses everything below them once the roles end)
+    pl.scratch_off = (pl.raw_off + pl.nr * pl.raw_bytes + 15u) & ~15u;
+    pl.bar_off = (pl.scratch_off + pl.scratch_bytes + 7u) & ~7u;
+    pl.smem = pl.bar_off + 8u * Bars::kCount + 8u;
     if (pl.resident) pl.na = 1;  // no filter ring: the resident block is read per chunk
     pl.Cg = Cg;
     pl.a_plane_bytes = (uint32_t)Cg * 16u;
@@ -2431,7 +2432,6 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     a.idesc = make_idesc(128, pl.P);
     a.scalar = e.scalar, a.chan_scale = e.chan_scale, a.gamma = e.gamma, a.slope = e.lrelu_slope;
     a.groups = e.groups;
-    a.smem_bytes = pl.smem;
     if (e.kind == kKindConvStats)  // the per-unit sums, after y in the two-pass buffer
         a.gn.pmax = reinterpret_cast<float *>(reinterpret_cast<char *>(h->ybuf) + tc_y_bytes(d));
     a.drop_tile = h->test_drop_tile;
@@ -2448,7 +2448,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
         a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
                     // one pair's blocks fit the buffer (the generalised kinds' ring ends below the barriers)
-                    F * 4u * (pl.RU == 2 ? 2u : 1u) <= (is_gnx(kkind) ? pl.bar_off : (uint32_t)pl.smem) - kFinBufOff &&
+                    F * 4u * (pl.RU == 2 ? 2u : 1u) <= pl.bar_off - kFinBufOff &&
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
