@@ -152,6 +152,7 @@ GN_WIDE = {
     "c5_pool2": synth.WORKLOADS["c5_gn_pool_clamp"].resized(pool_k=2),                 # 2x2 windows
     "c5_co128": synth.WORKLOADS["c5_gn_pool_clamp"].resized(Cout=128, groups=16),      # half bands
     "c5_w256": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=32, H=256, W=256),        # wide rows
+    "c5_co256": synth.WORKLOADS["c5_gn_pool_clamp"].resized(Cout=256, groups=32),     # channel tiles
 }
 
 

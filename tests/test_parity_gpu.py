@@ -91,6 +91,10 @@ SMALL = {
     "c5_k2_w67": W["c5_gn_pool_clamp"].resized(N=1, H=15, W=67, pool_k=2, groups=1),  # odd Wo: a stats-only column; one group
     "c5_k2_w66": W["c5_gn_pool_clamp"].resized(N=2, H=9, W=66, Cout=48, groups=12, pool_k=2),  # Wo 64, 48 channels
     "c5_k2_g64": W["c5_gn_pool_clamp"].resized(N=2, H=12, W=100, groups=64, pool_k=2),  # a group per channel: 245-float blocks, separate finalize
+    # more than 128 channels fused: channel tiles of 128, each unit one tile's half band
+    "c5_co256_w128": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=128, Cout=256, groups=32),  # 2 tiles, a stats-only row
+    "c5_co200_w100": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=100, Cout=200, groups=25),  # last tile 72 channels
+    "c5_co384_w80": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=80, Cout=384, groups=6),     # 3 tiles, 64 per group, P 80
 }
 FP32_ONLY = {"c2wide": W["c2_min_tanh2"].resized(N=1, H=6, W=300)}       # row wider than one tile
 # shapes the tf32 kernel refuses: the call must say so, not fall back

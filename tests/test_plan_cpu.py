@@ -196,7 +196,9 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     if pool_k == 2:  # 2 x 2 windows: two bands per unit, one-band rows, up to 64 channels
         return Cout <= 64 and 66 <= W <= 128
     # rows of 130..256 columns (Cout <= 64): one row pair per unit
-    return (Cout <= 64 and (W <= 64 or 66 <= W <= 128 or 130 <= W <= 256)) or (64 < Cout <= 128 and 66 <= W <= 128)
+    # more than 64 channels: no row stacking, half a band per unit (more than
+    # 128: channel tiles of 128, a unit per tile)
+    return (Cout <= 64 and (W <= 64 or 66 <= W <= 128 or 130 <= W <= 256)) or (Cout > 64 and 66 <= W <= 128)
 
 
 def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
@@ -221,9 +223,9 @@ def test_random_shapes_all_planned_and_in_range():
     and every plan passes the range checks; GroupNorm shapes are fused
     exactly when groups have a power-of-two size up to 64 and either
     pool_k = 4 with Cout <= 64 and W <= 64, 66 <= W <= 128 or
-    130 <= W <= 256, or 64 < Cout <= 128 with 66 <= W <= 128, or pool_k = 2
-    with Cout <= 64 and 66 <= W <= 128; otherwise they are planned as the
-    plain conv of the two-pass form."""
+    130 <= W <= 256, or Cout > 64 with 66 <= W <= 128, or pool_k = 2 with
+    Cout <= 64 and 66 <= W <= 128; otherwise they are planned as the plain
+    conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):
         kind = rng.choice([ce.MIN_TANH2, ce.SCALE_MIN, ce.MUL_LRELU_GELU, ce.GN_SCALE_POOL_CLAMP, ce.NONE])
@@ -254,7 +256,7 @@ def test_plan_query_arguments():
         ce._check(ce._lib().conv_epi_plan_query(ce.C.byref(d), ce.C.byref(epi_for(ce.MIN_TANH2)),
                                                 ce.C.byref(q)), "plan")
     assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
-    for bad_kind in (6, 7, 8, 9, 10, -1):                # bad chain (the kernel's internal kinds included)
+    for bad_kind in (6, 7, 8, 9, 10, 11, -1):            # bad chain (the kernel's internal kinds included)
         with pytest.raises(ce.ConvEpiError) as ei:
             plan(1, 8, 8, 8, 64, bad_kind)
         assert ce.STATUS[ei.value.status] == "INVALID_ARG"

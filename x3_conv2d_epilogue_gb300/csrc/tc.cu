@@ -94,14 +94,20 @@ constexpr int kKindGnWide = 9;
 // ... and 2 x 2 pooling windows (Cout <= 64, rows of 64..126 outputs): each
 // of a unit's two row pairs is a pooling band, 8 windows per 16-column chunk.
 constexpr int kKindGnPool2 = 10;
+// ... and more than 128 channels (rows of 64..126 outputs): channel tiles of
+// 128, each unit one tile's half band (with the tile handling compiled into
+// the kind above, its Cout 128 shapes measured 5 % slower).
+constexpr int kKindGnTiles = 11;
 __host__ __device__ constexpr bool is_gnx(int kind) {
-    return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2;
+    return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2 ||
+           kind == kKindGnTiles;
 }
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
 // 96..126 outputs), or the generalised one
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W >= 66 && d.W <= 128) return kKindGnPool2;
+    if (d.Cout > 128 && d.W > 64) return kKindGnTiles;
     if (d.W > 128) return kKindGnWide;
     if (d.W > 64 && d.W - 2 < 96) return kKindGnXNarrow;
     return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX;
@@ -563,11 +569,13 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
 // the longer latency; it sleeps briefly when neither can move, and gives up
 // like every other wait after kWaitLimitNs without progress.  Once only the
 // tiles are left (always, with a resident filter) it blocks in wait_bar.
-template <bool GENERAL>
+// TILES: channel tiles outside the general instantiation (the generalised
+// GroupNorm kinds).
+template <bool GENERAL, bool TILES>
 __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *xmap, uint32_t sbase, const Bars &bars,
                                               volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
-    const int CT = GENERAL ? a.CT : 1, MT = GENERAL ? a.MT : 1;  // (constants 1 on the fast path)
+    const int CT = GENERAL ? a.CT : 1, MT = GENERAL || TILES ? a.MT : 1;  // (constants 1 on the fast path)
     prefetch_tensormap(xmap);
     if (a.resident) {
         const uint32_t total = a.chunks * a.a_bytes;
@@ -1014,6 +1022,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr bool kPool2 = KIND == kKindGnPool2;  // 2 x 2 windows: a band per u
     constexpr int kPitch = kWide || kPool2 ? 65 : kPoolPitch;  // pooled tile pitch (up to 63 windows)
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
+    // more than 128 channels: channel tiles of 128, each unit one tile
+    constexpr bool kTiles = KIND == kKindGnTiles;
     // this lane's channel parameters; with more than 128 output channels they
     // belong to the unit's channel tile and are reloaded when it changes
     // (channels Co.. pad the GEMM with zero filters)
@@ -1022,9 +1032,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     float mult = KIND == CONV_EPI_MUL_LRELU_GELU && co < a.Co ? __ldg(&a.chan_scale[co]) : 0.0f;
     // GroupNorm chain: the sign of the channel's affine slope gamma * scale
     // (rstd > 0), folded into the packed filter: the accumulator is gsg * (y - b)
-    const float gsg =
-        kGN && (!kGnX || co < a.Co) && (signbit(__ldg(&a.gamma[co])) != signbit(__ldg(&a.chan_scale[co]))) ? -1.0f
-                                                                                                      : 1.0f;
+    auto sign_of = [&](int ch) {
+        return kGN && (!kGnX || ch < a.Co) && (signbit(__ldg(&a.gamma[ch])) != signbit(__ldg(&a.chan_scale[ch]))) ? -1.0f
+                                                                                                          : 1.0f;
+    };
+    float gsg = sign_of(co);
     // min chains: scalar * bias of the four channels this thread holds in a
     // rows4 fragment (lanes g, g+8, g+16, g+24 of the quadrant, g = lane/4),
     // each duplicated into a register pair, and the scalar likewise.  The
@@ -1066,13 +1078,13 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     if (kGN && slot == 0) gn_sgn[co] = gsg, gn_bias[co] = bias;
     // GroupNorm: this thread's chunks are cc = hc + 2 kc.  In the one-band
     // form (kKC = 4) chunks kc < kMask0 are whole: below column 96 in the
-    // page-shape kernel (its rows have Wo >= 96), below column 64 in the
-    // generalised one (Wo >= 64); the others may hold columns >= Wo (or lie
+    // page-shape kernel and the generalised one (their rows have Wo >= 96),
+    // below column 64 in the others (Wo >= 64); the others may hold columns >= Wo (or lie
     // past P), which the sums skip: bit 16 (kc - kMask0) + i of gn_rag is set
     // when column 16 cc + i < Wo.  (A select per value costs as much as the
     // sums, so only the chunks that can be ragged take it.)  gn_ncol counts
     // this thread's valid columns.
-    constexpr int kMask0 = kWide ? 4 : kKC == 4 ? (KIND == kKindGnXNarrow || kPool2 ? 2 : 3) : 0;
+    constexpr int kMask0 = kWide ? 4 : kKC == 4 ? (KIND == kKindGnXNarrow || kPool2 || kTiles ? 2 : 3) : 0;
     uint32_t gn_rag = 0;
     int gn_ncol = 0;
     if constexpr (kGN) {
@@ -1146,10 +1158,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     for (int unit = blockIdx.x; unit < a.total_units; unit += gridDim.x, ++j, pos.step(gridDim.x, a.units_per_img)) {
         const int n = pos.n;
         const int ru = pos.ru;                  // (GroupNorm: one column tile, so also the row block)
-        const int CT = GENERAL ? a.CT : 1, MT = GENERAL ? a.MT : 1;  // constants 1 on the fast path
-        const int r0 = pos.rb(CT, MT) * a.RU;   // first output row of the unit
+        const int CT = GENERAL ? a.CT : 1, MT = GENERAL || kTiles ? a.MT : 1;  // constants 1 on the fast path
+        const int rb = pos.rb(CT, MT);          // row block of the unit
+        const int r0 = rb * a.RU;               // first output row of the unit
         const int c0 = pos.ct(CT, MT) * a.CW;   // first output column of the unit
-        if (GENERAL && MT > 1) {
+        if ((GENERAL || kTiles) && MT > 1) {
             const int cb_unit = pos.mt(MT) * a.Cout;  // the unit's channel tile
             if (cb_unit != cbase) {
                 cbase = cb_unit;
@@ -1157,6 +1170,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 bias = ch < a.Co ? __ldg(&a.b[ch]) : 0.0f;
                 mult = KIND == CONV_EPI_MUL_LRELU_GELU && ch < a.Co ? __ldg(&a.chan_scale[ch]) : 0.0f;
                 if (kMin) load_sb2(cbase);
+                if (kTiles) gsg = sign_of(ch);
             }
         }
         const int ab = j & 1;
@@ -1489,6 +1503,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // every warp is past the previous unit's tile and statistics reads
             // (and none has given up) before they are rewritten
             if (!kWide && !kPool2 && epi_bar_any(false)) break;  // (wide rows, 2 x 2 windows: voted before their first tile)
+            // channel tiles: the sign and bias tables of this unit's tile (the
+            // vote above ends the previous unit's reads of them)
+            if (kTiles && MT > 1) gn_sgn[co] = gsg, gn_bias[co] = bias;
             float *st = scratch + kNB * 2 * 64 * kPitch;  // [2 stats][8 warps][32 lanes]
             st[ew * 32 + lane] = gs;
             st[kEpiThreads + ew * 32 + lane] = gss;
@@ -1518,13 +1535,16 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 const int nci = gn_cpg / gn_cw;  // 1, or 2 when a group spans two warps' lanes
                 float *fpart = reinterpret_cast<float *>(a.gn.part);
                 for (int g = lane; g < a.groups; g += 32) {
+                    // (channel tiles: the groups of other tiles get zero sums from this unit)
+                    const int lc = g * gn_cpg - cbase;
+                    const bool in_tile = !kTiles || (lc >= 0 && lc < a.Cout);
                     float v0[8], v1[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {  // k = (row slot, column group, half)
                         const int sl = k >> 2, h2 = (k >> 1) & 1, ci = k & 1;
                         v0[k] = v1[k] = 0.0f;
-                        if (ci < nci && (!kGnX || sl < a.S)) {
-                            const int LL = sl * a.Cout + g * gn_cpg + ci * gn_cw;
+                        if (in_tile && ci < nci && (!kGnX || sl < a.S)) {
+                            const int LL = sl * a.Cout + lc + ci * gn_cw;
                             const int e2 = h2 * 4 + (LL >> 5);
                             v0[k] = st[e2 * 32 + (LL & 31)];
                             v1[k] = st[kEpiThreads + e2 * 32 + (LL & 31)];
@@ -1589,12 +1609,14 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 }
             } else
             if (kGnX && !GENERAL && a.S == 1) {
-                // no stacking: this unit's 2 rows are half of band ru / 2; its
+                // no stacking: this unit's 2 rows are half of band rb / 2; its
                 // extremes (sign and bias restored: the half's selected y) go
-                // to slot ru & 1, and the finalize folds the two halves
-                const int prow = ru >> 1;
+                // to slot rb & 1, and the finalize folds the two halves
+                // (channels cbase + ...: the unit's channel tile)
+                const int prow = rb >> 1;
                 if (prow < a.Hp && lane < a.Wp) {
-                    float *dst = ((ru & 1) ? a.gn.pmin : a.gn.pmax) + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp + lane;
+                    float *dst = ((rb & 1) ? a.gn.pmin : a.gn.pmax) +
+                                 (((size_t)n * a.Co + cbase + ew) * a.Hp + prow) * a.Wp + lane;
                     const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
                     float m[128 / kEpiWarps];
 #pragma unroll
@@ -1604,7 +1626,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
 #pragma unroll
                     for (int i = 0; i < 128 / kEpiWarps; ++i)
-                        if (ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
+                        if (cbase + ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
                 }
             } else
 #pragma unroll
@@ -1915,7 +1937,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         if (lane == 0) mma_role(a, sbase, bars, tmem, abort_flag);
         __syncwarp();
     } else if (warp == kProducerWarp) {
-        if (lane == 0) producer_role<GENERAL>(a, &args.xmap, sbase, bars, abort_flag);
+        if (lane == 0)
+            producer_role<GENERAL, KIND == kKindGnTiles>(a, &args.xmap, sbase, bars, abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         converter_role(a, smem, bars, abort_flag);
@@ -2033,6 +2056,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
         return (uint32_t)((2 * 2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnX:  // (the tables for up to 128 channels)
     case kKindGnXNarrow:
+    case kKindGnTiles:
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     }
     return 0;
@@ -2058,7 +2082,8 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
     if (d.Cout < 1) return false;
     if (d.Cin < 1 || d.W < 3 || d.H < 3) return false;
     pl.MT = channel_tiles(d.Cout);
-    if (pl.MT > 1 && is_gn(kind)) return false;
+    // (channel tiles of the GroupNorm chain: the generalised kinds' half bands)
+    if (pl.MT > 1 && is_gn(kind) && kind != kKindGnTiles) return false;
     const bool nhwc = d.layout == CONV_EPI_LAYOUT_NHWC;
     if (nhwc && d.Cin % 4 != 0) return false;  // 16-byte position stride
     const int Cg = gemm_cout(d.Cout);
@@ -2220,12 +2245,14 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     const int kind = tc_gn_kind(d, e.pool_k);
     if (!make_plan(d, kind, pl)) return false;
     // one-band rows: the unmasked chunks must be whole (see the epilogue)
-    const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= (kind == kKindGnXNarrow ? 64 : 96);
+    const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= (kind == kKindGnXNarrow || kind == kKindGnTiles ? 64 : 96);
     const bool one_band = pl.S == 2 && pl.RU == 4 && wide;
     const bool two_bands = pl.S == 2 && pl.RU == 8 && pl.P == 64;
     // 65..128 channels fill M without stacking: a unit holds 2 rows, half a
     // band, and the finalize folds the halves
-    const bool half_band = pl.S == 1 && pl.MT == 1 && pl.RU == 2 && wide;
+    // (more than 128 channels: channel tiles of 128, each unit one tile; a
+    // group's channels, a power of two up to 64, never straddle two tiles)
+    const bool half_band = pl.S == 1 && pl.RU == 2 && wide;
     // rows of 130..256 columns (Cout <= 64): one row pair per unit (U = 1),
     // the first 128 output columns whole
     const bool wide_rows = kind == kKindGnWide && pl.S == 2 && pl.U == 1 && pl.CT == 1 && pl.P > 128 &&
@@ -2310,8 +2337,8 @@ size_t tc_wpack_bytes(const conv_epi_desc &d) {
 
 int tc_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
     Plan pl;
-    if (!make_plan(d, CONV_EPI_GN_SCALE_POOL_CLAMP, pl)) return (Ho + pool_k - 1) / pool_k;
-    return (Ho + pl.RU - 1) / pl.RU;
+    if (!make_plan(d, tc_gn_kind(d, pool_k), pl)) return (Ho + pool_k - 1) / pool_k;
+    return (Ho + pl.RU - 1) / pl.RU * pl.CT * pl.MT;  // (channel tiles: a unit per tile)
 }
 
 conv_epi_status tc_reserve(conv_epi_handle h, const conv_epi_epilogue_desc &e) {
@@ -2402,10 +2429,11 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         // channel tile m: filters 128m .. 128m + 127, after the previous tiles' chunks
         for (int m = 0; m < pl.MT; ++m) {
             const int Cg = gemm_cout(d.Cout);
-            const bool gn_sign = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP;  // (fused: one channel tile)
+            const bool gn_sign = e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP;  // (the fused form: the slope's sign)
             pack_weights<<<blocks, threads, 0, s>>>(w + (size_t)m * Cg * d.Cin * 9, h->wpack + (size_t)m * total,
                                                     d.Cin, Cg, min(Cg, d.Cout - m * Cg), pl.S,
-                                                    gn_sign ? e.gamma : nullptr, gn_sign ? e.chan_scale : nullptr,
+                                                    gn_sign ? e.gamma + (size_t)m * Cg : nullptr,
+                                                    gn_sign ? e.chan_scale + (size_t)m * Cg : nullptr,
                                                     m == 0 && gn_sign ? h->gn.arrive : nullptr);
             CE_CUDA(cudaGetLastError());
         }
@@ -2479,6 +2507,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
                    : kkind == kKindGnXNarrow ? launch_tc<kKindGnXNarrow>(args, pl, grid, s)
                    : kkind == kKindGnWide    ? launch_tc<kKindGnWide>(args, pl, grid, s)
                    : kkind == kKindGnPool2   ? launch_tc<kKindGnPool2>(args, pl, grid, s)
+                   : kkind == kKindGnTiles   ? launch_tc<kKindGnTiles>(args, pl, grid, s)
                                              : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
         };
         st = launch_gn();
