@@ -1061,10 +1061,12 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int nchunks = a.P / 16;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     // GroupNorm chain: group size, lanes per group inside a warp, and the sign
-    // table of the pooled extremes (a 64-float array after the tiles, written
-    // here and first read after the first combine barrier)
-    // (groups of the problem's Co <= 64 channels; the GEMM's channels Co..63
-    // are zero filters whose sums and extremes are never read)
+    // and bias tables of the pooled extremes (after the tiles, written here
+    // and first read after the first combine barrier; with channel tiles,
+    // rewritten per unit)
+    // (groups of the problem's Co channels; the GEMM's channels from Co up
+    // to its 64 or 128 are zero filters whose sums and extremes are never
+    // read)
     const int gn_cpg = kGN ? (kGnX ? a.Co : a.Cout) / a.groups : 1, gn_cw = gn_cpg < 32 ? gn_cpg : 32;
     // pooling bands of 4 rows per unit: one (rows of 80..128 columns: two u
     // of two row slots) or, in the general instantiation, two (rows of up to
@@ -1157,7 +1159,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     pos.init(blockIdx.x, a.units_per_img);
     for (int unit = blockIdx.x; unit < a.total_units; unit += gridDim.x, ++j, pos.step(gridDim.x, a.units_per_img)) {
         const int n = pos.n;
-        const int ru = pos.ru;                  // (GroupNorm: one column tile, so also the row block)
+        const int ru = pos.ru;                  // (GroupNorm: one column tile; one channel tile but in the tiles kind)
         const int CT = GENERAL ? a.CT : 1, MT = GENERAL || kTiles ? a.MT : 1;  // constants 1 on the fast path
         const int rb = pos.rb(CT, MT);          // row block of the unit
         const int r0 = rb * a.RU;               // first output row of the unit
@@ -2185,7 +2187,8 @@ EncodeTiledFn encode_tiled() {
 
 // rows of one tile with at most 128 output channels, and everything else
 // (column tiles, channel tiles) run separate instantiations, so the common
-// case carries none of the tiling arithmetic (the GroupNorm chain never tiles)
+// case carries none of the tiling arithmetic (the GroupNorm chain's column
+// tiles never occur, its channel tiles only in their own instantiation)
 template <int KIND>
 conv_epi_status launch_tc(const TcArgs &args, const Plan &pl, int grid, cudaStream_t s) {
     // (the GroupNorm chain's general instantiation pools two bands per unit)
