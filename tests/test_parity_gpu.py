@@ -49,7 +49,7 @@ SMALL = {
     "c2_w300": W["c2_min_tanh2"].resized(N=1, H=6, W=300),                   # 2 tiles: 252 + 46 columns
     "c3_w520": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=520),              # 3 tiles, per-channel stores
     "c4_w516": W["c4_scale_min"].resized(N=2, H=4, W=516, scalar=-1.0),      # 3 tiles, Cout 128, max branch
-    "c5_w260": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=260),              # GroupNorm over 2 column tiles (tf32: two passes)
+    "c5_w260": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=260),              # GroupNorm over 2 column tiles, the last 6 columns
     "c5_w200": W["c5_gn_pool_clamp"].resized(N=2, H=15, W=200),              # wide rows: 49 windows, half bands, a stats-only row
     "c5_w256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=256, groups=4),    # wide rows, P 256: 63 windows
     "c5_w130": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=130, Cout=32, groups=8),  # Wo 128, 32 channels
@@ -91,6 +91,9 @@ SMALL = {
     "c5_k2_w67": W["c5_gn_pool_clamp"].resized(N=1, H=15, W=67, pool_k=2, groups=1),  # odd Wo: a stats-only column; one group
     "c5_k2_w66": W["c5_gn_pool_clamp"].resized(N=2, H=9, W=66, Cout=48, groups=12, pool_k=2),  # Wo 64, 48 channels
     "c5_k2_g64": W["c5_gn_pool_clamp"].resized(N=2, H=12, W=100, groups=64, pool_k=2),  # a group per channel: 245-float blocks, separate finalize
+    # rows wider than 256 fused (Cout <= 64): column tiles of 252 outputs
+    "c5_w300": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=300),                   # last tile 46 columns: both passes masked
+    "c5_w510": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=510, Cout=32, groups=8),  # 3 tiles, the last one window, a stats-only row
     # more than 128 channels fused: channel tiles of 128, each unit one tile's half band
     "c5_co256_w128": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=128, Cout=256, groups=32),  # 2 tiles, a stats-only row
     "c5_co200_w100": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=100, Cout=200, groups=25),  # last tile 72 channels

@@ -98,9 +98,13 @@ constexpr int kKindGnPool2 = 10;
 // 128, each unit one tile's half band (with the tile handling compiled into
 // the kind above, its Cout 128 shapes measured 5 % slower).
 constexpr int kKindGnTiles = 11;
+// ... and rows wider than 256 columns (Cout <= 64): column tiles of 252
+// outputs (63 whole windows), each unit one tile of one row pair, as in the
+// 130..256-column kind but with each unit's column masks and window offset.
+constexpr int kKindGnColTiles = 12;
 __host__ __device__ constexpr bool is_gnx(int kind) {
     return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2 ||
-           kind == kKindGnTiles;
+           kind == kKindGnTiles || kind == kKindGnColTiles;
 }
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
@@ -108,6 +112,7 @@ __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W >= 66 && d.W <= 128) return kKindGnPool2;
     if (d.Cout > 128 && d.W > 64) return kKindGnTiles;
+    if (d.W > 256 && d.Cout <= 64) return kKindGnColTiles;
     if (d.W > 128) return kKindGnWide;
     if (d.W > 64 && d.W - 2 < 96) return kKindGnXNarrow;
     return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX;
@@ -569,13 +574,13 @@ __device__ __forceinline__ void mma_role(const Cfg &a, uint32_t sbase, const Bar
 // the longer latency; it sleeps briefly when neither can move, and gives up
 // like every other wait after kWaitLimitNs without progress.  Once only the
 // tiles are left (always, with a resident filter) it blocks in wait_bar.
-// TILES: channel tiles outside the general instantiation (the generalised
-// GroupNorm kinds).
+// TILES: channel or column tiles outside the general instantiation (the
+// generalised GroupNorm kinds).
 template <bool GENERAL, bool TILES>
 __device__ __forceinline__ void producer_role(const Cfg &a, const CUtensorMap *xmap, uint32_t sbase, const Bars &bars,
                                               volatile int *abort_flag) {
     const char *wsrc = reinterpret_cast<const char *>(a.wpack);
-    const int CT = GENERAL ? a.CT : 1, MT = GENERAL || TILES ? a.MT : 1;  // (constants 1 on the fast path)
+    const int CT = GENERAL || TILES ? a.CT : 1, MT = GENERAL || TILES ? a.MT : 1;  // (constants 1 on the fast path)
     prefetch_tensormap(xmap);
     if (a.resident) {
         const uint32_t total = a.chunks * a.a_bytes;
@@ -1018,7 +1023,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     const int slot = L / a.Cout, co = L % a.Cout;
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGnX = is_gnx(KIND);  // the generalised GroupNorm chain
-    constexpr bool kWide = KIND == kKindGnWide;  // rows of 130..256 columns: two passes per unit
+    // rows of 130..256 columns, or column tiles of wider rows: two passes per unit
+    constexpr bool kWide = KIND == kKindGnWide || KIND == kKindGnColTiles;
+    constexpr bool kColT = KIND == kKindGnColTiles;
     constexpr bool kPool2 = KIND == kKindGnPool2;  // 2 x 2 windows: a band per u
     constexpr int kPitch = kWide || kPool2 ? 65 : kPoolPitch;  // pooled tile pitch (up to 63 windows)
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
@@ -1160,7 +1167,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     for (int unit = blockIdx.x; unit < a.total_units; unit += gridDim.x, ++j, pos.step(gridDim.x, a.units_per_img)) {
         const int n = pos.n;
         const int ru = pos.ru;                  // (GroupNorm: one column tile; one channel tile but in the tiles kind)
-        const int CT = GENERAL ? a.CT : 1, MT = GENERAL || kTiles ? a.MT : 1;  // constants 1 on the fast path
+        const int CT = GENERAL || kColT ? a.CT : 1, MT = GENERAL || kTiles ? a.MT : 1;  // constants 1 on the fast path
         const int rb = pos.rb(CT, MT);          // row block of the unit
         const int r0 = rb * a.RU;               // first output row of the unit
         const int c0 = pos.ct(CT, MT) * a.CW;   // first output column of the unit
@@ -1256,7 +1263,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // per warp in two passes of 4: the first (columns below 128)
                 // whole, the second masked; each pass's window extremes go to
                 // the tile at once (windows 0..31, then 32..63)
-                auto gn_step_w = [&](const Frag16 (&f)[kKC], float (&pext)[kWin]) {
+                auto gn_step_w = [&](const Frag16 (&f)[kKC], float (&pext)[kWin], uint64_t rag) {
 #pragma unroll
                     for (int kc = 0; kc < kKC; ++kc) {
                         uint64_t v2[8];
@@ -1271,8 +1278,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         for (int p = 0; p < 8; ++p) {
                             const uint64_t b0 = 1ull << (16 * kc + 2 * p);
                             const float2 w = unpack2(v2[p]);
-                            v2[p] = pack2(__float_as_uint((gn_ragw & b0) ? w.x : 0.0f),
-                                          __float_as_uint((gn_ragw & (b0 << 1)) ? w.y : 0.0f));
+                            v2[p] = pack2(__float_as_uint((rag & b0) ? w.x : 0.0f),
+                                          __float_as_uint((rag & (b0 << 1)) ? w.y : 0.0f));
                         }
 #pragma unroll
                         for (int p = 0; p < 8; ++p) {
@@ -1291,12 +1298,31 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 };
                 const bool row_ok = r0 + slot < a.Ho;  // the same for the whole warp
                 gn_rows += row_ok ? 1 : 0;
+                // column tiles: this unit's valid columns (the last tile may
+                // end below column 128), bit 16 kc + i of pass p's mask set
+                // when column 16 (hc + 8 p + 2 kc) + i of the tile is an output
+                uint64_t rag0 = 0, rag1 = gn_ragw;
+                if constexpr (kColT) {
+                    const int wv = min(a.CW, a.Wo - c0);
+                    rag1 = 0;
+#pragma unroll
+                    for (int kc = 0; kc < kKC; ++kc) {
+                        const int l0 = wv - 16 * (hc + 2 * kc), l1 = l0 - 128;
+                        const int n0 = l0 < 0 ? 0 : l0 > 16 ? 16 : l0, n1 = l1 < 0 ? 0 : l1 > 16 ? 16 : l1;
+                        rag0 |= (uint64_t)((1u << n0) - 1u) << (16 * kc);
+                        rag1 |= (uint64_t)((1u << n1) - 1u) << (16 * kc);
+                    }
+                    gn_ncol = __popcll(rag0) + __popcll(rag1);
+                }
                 Frag16 f[kKC];
 #pragma unroll
                 for (int kc = 0; kc < kKC; ++kc) tmem_ld16_issue(tbase + (hc + 2 * kc) * 16, f[kc]);
                 tmem_ld_wait2(f[0], f[1]);
                 tmem_ld_wait2(f[2], f[3]);
-                if (row_ok) gn_step(f, pext0);
+                if (row_ok) {
+                    if constexpr (kColT) gn_step_w(f, pext0, rag0);
+                    else gn_step(f, pext0);
+                }
                 // every warp is past the previous unit's tile and statistics
                 // reads (and none has given up) before the tile is rewritten
                 if (epi_bar_any(false)) {
@@ -1310,7 +1336,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         if (hc + 8 + 2 * kc < nchunks) tmem_ld16_issue(tbase + (hc + 8 + 2 * kc) * 16, f[kc]);
                     tmem_ld_wait2(f[0], f[1]);
                     tmem_ld_wait2(f[2], f[3]);
-                    if (row_ok) gn_step_w(f, pext0);
+                    if (row_ok) gn_step_w(f, pext0, rag1);
                     put_w(1);
                 }
             } else if constexpr (kPool2) {
@@ -1587,17 +1613,19 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
                 }
             } else if constexpr (kWide) {
-                // half band ru / 2, two row slots folded, sign and bias
-                // restored, into slot ru & 1; windows lane and lane + 32
-                const int prow = ru >> 1;
+                // half band rb / 2, two row slots folded, sign and bias
+                // restored, into slot rb & 1; windows lane and lane + 32 (of
+                // the column tile's, which start at window c0 / 4)
+                const int prow = rb >> 1;
+                const int w0 = kColT ? c0 / 4 : 0, nw = kColT ? min(a.CW / 4, a.Wp - w0) : a.Wp;
                 if (prow < a.Hp) {
                     const float *pt0 = scratch, *pt1 = scratch + 64 * kPitch;
-                    float *dst = ((ru & 1) ? a.gn.pmin : a.gn.pmax) + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
+                    float *dst = ((rb & 1) ? a.gn.pmin : a.gn.pmax) + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp + w0;
                     const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
 #pragma unroll
                     for (int hw = 0; hw < 2; ++hw) {
                         const int w = lane + 32 * hw;
-                        if (w >= a.Wp) continue;
+                        if (w >= nw) continue;
                         float m[64 / kEpiWarps];
 #pragma unroll
                         for (int i = 0; i < 64 / kEpiWarps; ++i) {
@@ -1940,7 +1968,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         __syncwarp();
     } else if (warp == kProducerWarp) {
         if (lane == 0)
-            producer_role<GENERAL, KIND == kKindGnTiles>(a, &args.xmap, sbase, bars, abort_flag);
+            producer_role<GENERAL, KIND == kKindGnTiles || KIND == kKindGnColTiles>(a, &args.xmap, sbase, bars,
+                                                                                   abort_flag);
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         converter_role(a, smem, bars, abort_flag);
@@ -2053,6 +2082,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
     case kKindGnWide:  // one band region of pitch 65, the statistics, the tables
+    case kKindGnColTiles:
         return (uint32_t)((2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnPool2:  // two band regions of pitch 65, the statistics, the tables
         return (uint32_t)((2 * 2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
@@ -2101,7 +2131,7 @@ bool make_plan(const conv_epi_desc &d, int kind, Plan &pl) {
         // column tiles of 252 outputs from 256 staged columns (the last two
         // unused; tiles start on multiples of 4 columns, 16-byte aligned);
         // past the image's right edge the tensor load fills zeros
-        if (is_gn(kind)) return false;
+        if (is_gn(kind) && kind != kKindGnColTiles) return false;
         pl.P = 256;
         pl.CW = 252, pl.BW = 256;
         pl.CT = (d.W - 2 + pl.CW - 1) / pl.CW;
@@ -2266,8 +2296,12 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // 2 x 2 windows (Cout <= 64): the one-band layout, two bands per unit,
     // the first 64 output columns whole
     const bool pool2 = kind == kKindGnPool2 && pl.S == 2 && pl.RU == 4 && pl.P > 64 && pl.P <= 128 && d.W - 2 >= 64;
+    // rows wider than 256 columns (Cout <= 64): column tiles of 252 outputs,
+    // each unit one row pair of one tile
+    const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.CT > 1 && pl.P == 256;
     const int cpg = d.Cout / e.groups;
-    const bool shape = e.pool_k == 4 ? (one_band || two_bands || half_band || wide_rows) : e.pool_k == 2 && pool2;
+    const bool shape =
+        e.pool_k == 4 ? (one_band || two_bands || half_band || wide_rows || col_tiles) : e.pool_k == 2 && pool2;
     return shape && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
 
@@ -2470,8 +2504,9 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
-        if (h->gn.units != a.units_per_img || a.Wp > (kkind == kKindGnWide || kkind == kKindGnPool2 ? 64 : 32))
-            return CONV_EPI_ERR_INVALID_ARG;
+        // (a unit's windows: up to 32 or, for the two-pass rows, 64; column tiles any number)
+        const int max_wp = kkind == kKindGnColTiles ? a.Wp : kkind == kKindGnWide || kkind == kKindGnPool2 ? 64 : 32;
+        if (h->gn.units != a.units_per_img || a.Wp > max_wp) return CONV_EPI_ERR_INVALID_ARG;
         // finalize inside the kernel when each (image, group) block of pooled
         // values is whole float4s (16-byte aligned blocks) and small enough
         // for the multiply-high divisions (t < 2^18 pooled float4 per batch,
@@ -2511,6 +2546,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
                    : kkind == kKindGnWide    ? launch_tc<kKindGnWide>(args, pl, grid, s)
                    : kkind == kKindGnPool2   ? launch_tc<kKindGnPool2>(args, pl, grid, s)
                    : kkind == kKindGnTiles   ? launch_tc<kKindGnTiles>(args, pl, grid, s)
+                   : kkind == kKindGnColTiles ? launch_tc<kKindGnColTiles>(args, pl, grid, s)
                                              : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
         };
         st = launch_gn();
