@@ -157,8 +157,8 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *   CONV_EPI_MODE_TF32: any N, Cin, Cout and H, W >= 3.
  *     GN chain: fused into the conv kernel for groups of a power-of-two
  *     number of channels up to 64 and either pool_k = 4 with Cout <= 64 and
- *     W <= 64 or W >= 66 except 129 (wider than 256 as column tiles of 252
- *     outputs), or with Cout > 64 and
+ *     W <= 64 or W >= 66 (wider than 256 as column tiles of 252 outputs), or
+ *     with Cout > 64 and
  *     66 <= W <= 128 (more than 128 channels as channel tiles of 128), or
  *     pool_k = 2 with Cout <= 64 and 66 <= W <= 128;
  *     any other GN

@@ -53,7 +53,7 @@ SMALL = {
     "c5_w200": W["c5_gn_pool_clamp"].resized(N=2, H=15, W=200),              # wide rows: 49 windows, half bands, a stats-only row
     "c5_w256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=256, groups=4),    # wide rows, P 256: 63 windows
     "c5_w130": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=130, Cout=32, groups=8),  # Wo 128, 32 channels
-    "c5_w129": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=129),              # Wo 127: two passes in tf32
+    "c5_w129": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=129),              # Wo 127: one column tile, its first pass masked
     # more than 128 output channels (the tf32 path runs channel tiles of 128)
     "c4_co256": W["c4_scale_min"].resized(N=1, H=5, W=64, Cout=256),        # 2 channel tiles, atomic minimum
     "c3_co200": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=64, Cout=200),   # 2 tiles, the second padded

@@ -100,7 +100,8 @@ constexpr int kKindGnPool2 = 10;
 constexpr int kKindGnTiles = 11;
 // ... and rows wider than 256 columns (Cout <= 64): column tiles of 252
 // outputs (63 whole windows), each unit one tile of one row pair, as in the
-// 130..256-column kind but with each unit's column masks and window offset.
+// 130..256-column kind but with each unit's column masks and window offset
+// (also rows of 127 outputs, whose first pass needs the mask).
 constexpr int kKindGnColTiles = 12;
 __host__ __device__ constexpr bool is_gnx(int kind) {
     return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2 ||
@@ -112,7 +113,8 @@ __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W >= 66 && d.W <= 128) return kKindGnPool2;
     if (d.Cout > 128 && d.W > 64) return kKindGnTiles;
-    if (d.W > 256 && d.Cout <= 64) return kKindGnColTiles;
+    // (rows of 127 outputs too: one tile, its first pass masked)
+    if ((d.W > 256 || d.W == 129) && d.Cout <= 64) return kKindGnColTiles;
     if (d.W > 128) return kKindGnWide;
     if (d.W > 64 && d.W - 2 < 96) return kKindGnXNarrow;
     return d.Cout == 64 ? CONV_EPI_GN_SCALE_POOL_CLAMP : kKindGnX;
@@ -2297,8 +2299,8 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // the first 64 output columns whole
     const bool pool2 = kind == kKindGnPool2 && pl.S == 2 && pl.RU == 4 && pl.P > 64 && pl.P <= 128 && d.W - 2 >= 64;
     // rows wider than 256 columns (Cout <= 64): column tiles of 252 outputs,
-    // each unit one row pair of one tile
-    const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.CT > 1 && pl.P == 256;
+    // each unit one row pair of one tile (rows of 127 outputs: one tile)
+    const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.P > 128;
     const int cpg = d.Cout / e.groups;
     const bool shape =
         e.pool_k == 4 ? (one_band || two_bands || half_band || wide_rows || col_tiles) : e.pool_k == 2 && pool2;
