@@ -1403,9 +1403,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 tmem_ld_wait2(f[0], f[1]);
                 if constexpr (kKC == 4) tmem_ld_wait2(f[2], f[3]);
                 if (row_ok) {
-                    // this u's rows belong to band u / 2 (two row slots per u)
+                    // this u's rows belong to band u / 2 (two row slots per
+                    // u; without stacking, the four u are the one band)
                     if constexpr (kNB == 2) {
-                        if (u >= 2) gn_step(f, pext1);
+                        if (u >= 2 && (!kGnX || a.S == 2)) gn_step(f, pext1);
                         else gn_step(f, pext0);
                     } else {
                         gn_step(f, pext0);
@@ -1552,7 +1553,9 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             };
             if constexpr (!kWide && !kPool2) {
                 put_tile(0, pext0);
-                if constexpr (kNB == 2) put_tile(1, pext1);
+                if constexpr (kNB == 2) {
+                    if (!kGnX || a.S == 2) put_tile(1, pext1);
+                }
             }
             epi_bar();
             if (ew == 2) {
@@ -1659,6 +1662,25 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 #pragma unroll
                     for (int i = 0; i < 128 / kEpiWarps; ++i)
                         if (cbase + ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
+                }
+            } else if (kGnX && GENERAL && a.S == 1) {
+                // no stacking, rows of up to 64 columns: the unit's four u
+                // are one whole band, each thread's extremes over all four
+                // rows in the one tile of 128 channels; warp ew stores
+                // channels ew, ew + 8, ..., sign and bias restored
+                const int prow = ru;
+                if (prow < a.Hp && lane < a.Wp) {
+                    float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp + lane;
+                    const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+                    float m[128 / kEpiWarps];
+#pragma unroll
+                    for (int i = 0; i < 128 / kEpiWarps; ++i) {
+                        const int c2 = ew + kEpiWarps * i;
+                        m[i] = fmaf(gn_sgn[c2], scratch[c2 * kPoolPitch + lane], gn_bias[c2]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 128 / kEpiWarps; ++i)
+                        if (ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
                 }
             } else
 #pragma unroll
@@ -2283,6 +2305,9 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= (kind == kKindGnXNarrow || kind == kKindGnTiles ? 64 : 96);
     const bool one_band = pl.S == 2 && pl.RU == 4 && wide;
     const bool two_bands = pl.S == 2 && pl.RU == 8 && pl.P == 64;
+    // 65..128 channels in rows of up to 64 columns: no stacking, the unit's
+    // four rows one whole band
+    const bool one_band_s1 = pl.S == 1 && pl.MT == 1 && pl.RU == 4 && pl.P == 64;
     // 65..128 channels fill M without stacking: a unit holds 2 rows, half a
     // band, and the finalize folds the halves
     // (more than 128 channels: channel tiles of 128, each unit one tile; a
@@ -2303,7 +2328,8 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.P > 128;
     const int cpg = d.Cout / e.groups;
     const bool shape =
-        e.pool_k == 4 ? (one_band || two_bands || half_band || wide_rows || col_tiles) : e.pool_k == 2 && pool2;
+        e.pool_k == 4 ? (one_band || two_bands || one_band_s1 || half_band || wide_rows || col_tiles)
+                      : e.pool_k == 2 && pool2;
     return shape && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
 
