@@ -159,8 +159,8 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *     number of channels up to 64 and either pool_k = 4 with Cout <= 64 and
  *     W <= 64 or W >= 66 (wider than 256 as column tiles of 252 outputs), or
  *     with Cout > 64 and
- *     66 <= W <= 128 (more than 128 channels as channel tiles of 128), or
- *     with 64 < Cout <= 128 and W <= 64, or
+ *     W <= 64 or 66 <= W <= 128 (more than 128 channels as channel tiles of
+ *     128), or
  *     pool_k = 2 with Cout <= 64 and 66 <= W <= 128;
  *     any other GN
  *     shape runs as two passes, the tensor-core conv

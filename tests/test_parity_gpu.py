@@ -81,7 +81,7 @@ SMALL = {
     "c5_co128_w128": W["c5_gn_pool_clamp"].resized(N=2, H=15, W=128, Cout=128, groups=16),  # fused, half bands, a stats-only row
     "c5_co96_w100": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=100, Cout=96, groups=12),  # fused, 32 zero filters, P 112
     "c5_co128_g2": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=110, Cout=128, groups=2),   # fused, 64 channels per group
-    "c5_co256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=256, groups=32),  # 2 channel tiles, W 64: two passes
+    "c5_co256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=256, groups=32),  # 2 channel tiles, W 64: whole bands per tile
     "c5_k2": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=50, pool_k=2),               # 2 x 2 windows, odd tail row
     "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling
     "c5_k2_w300": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=300, pool_k=2, groups=64),  # 2 column tiles, a group per channel
@@ -94,6 +94,7 @@ SMALL = {
     # 65..128 channels in rows of up to 64 columns: no stacking, one whole band per unit
     "c5_co128_w64": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=64, Cout=128, groups=16),  # a stats-only unit
     "c5_co96_w40": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=40, Cout=96, groups=12),   # 32 zero filters, 9 windows
+    "c5_co320_w50": W["c5_gn_pool_clamp"].resized(N=2, H=11, W=50, Cout=320, groups=10),  # 3 tiles, the last 64 channels, 32 per group
     # rows wider than 256 fused (Cout <= 64): column tiles of 252 outputs
     "c5_w300": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=300),                   # last tile 46 columns: both passes masked
     "c5_w510": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=510, Cout=32, groups=8),  # 3 tiles, the last one window, a stats-only row

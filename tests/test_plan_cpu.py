@@ -199,7 +199,7 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     # rows: the same per column tile of 252 outputs
     # more than 64 channels: no row stacking, half a band per unit (more than
     # 128: channel tiles of 128, a unit per tile)
-    return (Cout <= 64 and (W <= 64 or W >= 66)) or (Cout > 64 and 66 <= W <= 128) or (64 < Cout <= 128 and W <= 64)
+    return (Cout <= 64 and (W <= 64 or W >= 66)) or (Cout > 64 and (W <= 64 or 66 <= W <= 128))
 
 
 def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
@@ -223,8 +223,8 @@ def test_random_shapes_all_planned_and_in_range():
     """Every shape with H, W >= 3 has a plan (the tf32 mode takes any size),
     and every plan passes the range checks; GroupNorm shapes are fused
     exactly when groups have a power-of-two size up to 64 and either
-    pool_k = 4 with Cout <= 64 and W != 65, or Cout > 64 with
-    66 <= W <= 128, or 64 < Cout <= 128 with W <= 64, or pool_k = 2 with
+    pool_k = 4 with Cout <= 64 and W != 65, or Cout > 64 with W <= 64 or
+    66 <= W <= 128, or pool_k = 2 with
     Cout <= 64 and 66 <= W <= 128; otherwise they are planned as the plain
     conv of the two-pass form."""
     rng = random.Random(20261203)

@@ -94,9 +94,10 @@ constexpr int kKindGnWide = 9;
 // ... and 2 x 2 pooling windows (Cout <= 64, rows of 64..126 outputs): each
 // of a unit's two row pairs is a pooling band, 8 windows per 16-column chunk.
 constexpr int kKindGnPool2 = 10;
-// ... and more than 128 channels (rows of 64..126 outputs): channel tiles of
-// 128, each unit one tile's half band (with the tile handling compiled into
-// the kind above, its Cout 128 shapes measured 5 % slower).
+// ... and more than 128 channels (rows of up to 64 or of 64..126 outputs):
+// channel tiles of 128, each unit one tile's band or half band (with the
+// tile handling compiled into the kind above, its Cout 128 shapes measured
+// 5 % slower).
 constexpr int kKindGnTiles = 11;
 // ... and rows wider than 256 columns (Cout <= 64): column tiles of 252
 // outputs (63 whole windows), each unit one tile of one row pair, as in the
@@ -112,7 +113,7 @@ __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_
 // 96..126 outputs), or the generalised one
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W >= 66 && d.W <= 128) return kKindGnPool2;
-    if (d.Cout > 128 && d.W > 64) return kKindGnTiles;
+    if (d.Cout > 128) return kKindGnTiles;
     // (rows of 127 outputs too: one tile, its first pass masked)
     if ((d.W > 256 || d.W == 129) && d.Cout <= 64) return kKindGnColTiles;
     if (d.W > 128) return kKindGnWide;
@@ -1667,10 +1668,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // no stacking, rows of up to 64 columns: the unit's four u
                 // are one whole band, each thread's extremes over all four
                 // rows in the one tile of 128 channels; warp ew stores
-                // channels ew, ew + 8, ..., sign and bias restored
-                const int prow = ru;
+                // channels cbase + ew, cbase + ew + 8, ..., sign and bias
+                // restored
+                const int prow = rb;
                 if (prow < a.Hp && lane < a.Wp) {
-                    float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp + lane;
+                    float *dst = a.gn.pmax + (((size_t)n * a.Co + cbase + ew) * a.Hp + prow) * a.Wp + lane;
                     const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
                     float m[128 / kEpiWarps];
 #pragma unroll
@@ -1680,7 +1682,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
 #pragma unroll
                     for (int i = 0; i < 128 / kEpiWarps; ++i)
-                        if (ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
+                        if (cbase + ew + kEpiWarps * i < a.Co) dst[i * cstep] = m[i];
                 }
             } else
 #pragma unroll
@@ -2305,9 +2307,9 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     const bool wide = pl.P > 64 && pl.P <= 128 && d.W - 2 >= (kind == kKindGnXNarrow || kind == kKindGnTiles ? 64 : 96);
     const bool one_band = pl.S == 2 && pl.RU == 4 && wide;
     const bool two_bands = pl.S == 2 && pl.RU == 8 && pl.P == 64;
-    // 65..128 channels in rows of up to 64 columns: no stacking, the unit's
-    // four rows one whole band
-    const bool one_band_s1 = pl.S == 1 && pl.MT == 1 && pl.RU == 4 && pl.P == 64;
+    // more than 64 channels in rows of up to 64 columns: no stacking, the
+    // unit's four rows one whole band (more than 128: per channel tile)
+    const bool one_band_s1 = pl.S == 1 && pl.RU == 4 && pl.P == 64;
     // 65..128 channels fill M without stacking: a unit holds 2 rows, half a
     // band, and the finalize folds the halves
     // (more than 128 channels: channel tiles of 128, each unit one tile; a
