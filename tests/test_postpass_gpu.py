@@ -30,6 +30,14 @@ CASES = {
     "c5_w37": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=37),
     "c5_k2": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=30, pool_k=2),
     "c5_co32": W["c5_gn_pool_clamp"].resized(N=2, H=14, W=40, Cout=32, groups=8),
+    # each instantiation of the pooling pass: 4 x 4 windows by 16-byte loads
+    # (Wo a multiple of 4), 2 x 2 by single floats (odd Wo), no pooling, 3 x 3,
+    # and a window size taken at run time
+    "c5_k4_v4": W["c5_gn_pool_clamp"].resized(N=1, H=13, W=34),
+    "c5_k2_odd": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=31, pool_k=2),
+    "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=20, pool_k=1, groups=4),
+    "c5_k3": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=29, pool_k=3),
+    "c5_k5": W["c5_gn_pool_clamp"].resized(N=1, H=17, W=27, pool_k=5),
 }
 
 
