@@ -365,6 +365,18 @@ def time_steps(step, stream, steps, warmup, flush, world=1):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def fp32_roofline(tflops, sm_count, sm_max_mhz):
+    """The strict mode runs on the CUDA cores: its roofline is the fp32 FMA
+    rate (SMs x 128 FMA lanes x 2 flops x the maximum SM clock, the sampled
+    one or the GB300's 2070 MHz), and the tensor kernel's DRAM capture does
+    not describe it."""
+    sm_max = sm_max_mhz or FALLBACK_SM_MAX_MHZ
+    peak = sm_count * 128 * 2 * sm_max * 1e-6
+    return {"bound": "alu", "peak": peak, "frac": tflops / peak, "traffic": None,
+            "peak_source": f"{sm_count} SMs x 128 fp32 FMA/clk x 2 x {sm_max:.0f} MHz (derived)",
+            "kernel": "conv_epi forward (fused fp32 CUDA-core kernel)"}
+
+
 def roofline_of(wl, ms, tf32_peak, hbm):
     """Both roofline fractions of one forward; `bound` is the roofline with
     the longer ideal time at the measured peaks."""
@@ -551,14 +563,7 @@ def main(argv=None):
         "kernel_ms": {"mean": kern_ms, "min": float(np.min(per)), "max": float(np.max(per))},
     }
     if args.mode == "fp32":
-        # the strict mode runs on the CUDA cores: its roofline is the fp32 FMA
-        # rate (SMs x 128 FMA lanes x 2 flops x the maximum SM clock), and the
-        # tensor kernel's DRAM capture does not describe it
-        sm_max = line["clocks"].get("sm_max_mhz") or FALLBACK_SM_MAX_MHZ
-        fma_peak = sm_count * 128 * 2 * sm_max * 1e-6
-        line["roofline"].update({"bound": "alu", "peak": fma_peak, "frac": rl["tflops"] / fma_peak, "traffic": None,
-                                 "peak_source": f"{sm_count} SMs x 128 fp32 FMA/clk x 2 x {sm_max:.0f} MHz (derived)",
-                                 "kernel": "conv_epi forward (fused fp32 CUDA-core kernel)"})
+        line["roofline"].update(fp32_roofline(rl["tflops"], sm_count, line["clocks"].get("sm_max_mhz")))
     print(json.dumps(line), flush=True)
     return 0
 

@@ -82,3 +82,14 @@ def test_headline_is_the_largest_workload():
     src = open(bench.__file__).read()
     assert '"--workload", default="c4_scale_min"' in src
     assert max(W, key=lambda n: bench.conv_flops(W[n])) == "c4_scale_min"
+
+
+def test_fp32_mode_roofline_is_the_fma_rate():
+    """--mode fp32 is measured against the CUDA cores' FMA rate (bound "alu"),
+    from the sampled maximum clock or the GB300's 2070 MHz, with no DRAM
+    traffic figure (the capture is of the tensor-core kernel)."""
+    r = bench.fp32_roofline(40.25, 152, 2070.0)
+    assert r["bound"] == "alu" and r["traffic"] is None
+    assert abs(r["peak"] - 152 * 128 * 2 * 2.07e-3) < 1e-9
+    assert abs(r["frac"] - 40.25 / r["peak"]) < 1e-12
+    assert bench.fp32_roofline(40.25, 152, None)["peak"] == r["peak"]
