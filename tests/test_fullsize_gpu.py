@@ -154,6 +154,7 @@ GN_WIDE = {
     "c5_w256": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=32, H=256, W=256),        # wide rows
     "c5_co256": synth.WORKLOADS["c5_gn_pool_clamp"].resized(Cout=256, groups=32),     # channel tiles
     "c5_w512": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=8, H=512, W=512),         # column tiles, separate finalize
+    "c5_pool2_co128": synth.WORKLOADS["c5_gn_pool_clamp"].resized(Cout=128, groups=16, pool_k=2),  # 2x2, no stacking
 }
 
 

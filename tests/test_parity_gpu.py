@@ -91,6 +91,8 @@ SMALL = {
     "c5_k2_w67": W["c5_gn_pool_clamp"].resized(N=1, H=15, W=67, pool_k=2, groups=1),  # odd Wo: a stats-only column; one group
     "c5_k2_w66": W["c5_gn_pool_clamp"].resized(N=2, H=9, W=66, Cout=48, groups=12, pool_k=2),  # Wo 64, 48 channels
     "c5_k2_g64": W["c5_gn_pool_clamp"].resized(N=2, H=12, W=100, groups=64, pool_k=2),  # a group per channel: 245-float blocks, separate finalize
+    "c5_k2_co128": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=100, Cout=128, groups=16, pool_k=2),  # no stacking, a stats-only row
+    "c5_k2_co96_w128": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=128, Cout=96, groups=12, pool_k=2),  # 32 zero filters, 63 windows
     # 65..128 channels in rows of up to 64 columns: no stacking, one whole band per unit
     "c5_co128_w64": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=64, Cout=128, groups=16),  # a stats-only unit
     "c5_co96_w40": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=40, Cout=96, groups=12),   # 32 zero filters, 9 windows

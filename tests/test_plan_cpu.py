@@ -138,9 +138,11 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout, pool_k=4):
             # 2 x 2 windows: two band regions of pitch 65 (up to 63 windows),
             # the statistics, 128-channel tables; the tile writes reach
             # (band * 2 + slot) * 64 * 65 + channel * 65 + window (window < 64)
-            assert S == 2 and U == 2
+            # (no stacking: one band, channel rows 0..127 of pitch 65)
+            assert U == 2
             top = max((b * 2 + sl) * 64 * 65 + ch * 65 + w for b in (0, 1) for sl in (0, 1) for ch in range(64)
                       for w in range(64))
+            assert max(ch * 65 + w for ch in range(128) for w in range(64)) < top
             assert top < 2 * 2 * 64 * 65 and q["scratch_bytes"] >= (2 * 2 * 64 * 65 + 2 * 256 + 2 * 128) * 4
         elif U == 1:
             # wide rows: one band region of pitch 65 (up to 63 windows), the
@@ -193,8 +195,8 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     cpg = Cout // groups
     if kind != ce.GN_SCALE_POOL_CLAMP or pool_k not in (2, 4) or cpg & (cpg - 1) or cpg > 64:
         return False
-    if pool_k == 2:  # 2 x 2 windows: two bands per unit, one-band rows, up to 64 channels
-        return Cout <= 64 and 66 <= W <= 128
+    if pool_k == 2:  # 2 x 2 windows: rows of 66..128 columns, up to 128 channels
+        return Cout <= 128 and 66 <= W <= 128
     # rows of 130..256 columns (Cout <= 64): one row pair per unit; wider
     # rows: the same per column tile of 252 outputs
     # more than 64 channels: no row stacking, half a band per unit (more than
@@ -225,7 +227,7 @@ def test_random_shapes_all_planned_and_in_range():
     exactly when groups have a power-of-two size up to 64 and either
     pool_k = 4 with Cout <= 64 and W != 65, or Cout > 64 with W <= 64 or
     66 <= W <= 128, or pool_k = 2 with
-    Cout <= 64 and 66 <= W <= 128; otherwise they are planned as the plain
+    Cout <= 128 and 66 <= W <= 128; otherwise they are planned as the plain
     conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):
@@ -257,7 +259,7 @@ def test_plan_query_arguments():
         ce._check(ce._lib().conv_epi_plan_query(ce.C.byref(d), ce.C.byref(epi_for(ce.MIN_TANH2)),
                                                 ce.C.byref(q)), "plan")
     assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
-    for bad_kind in (6, 7, 8, 9, 10, 11, -1):            # bad chain (the kernel's internal kinds included)
+    for bad_kind in (6, 7, 8, 9, 10, 11, 12, 13, -1):    # bad chain (the kernel's internal kinds included)
         with pytest.raises(ce.ConvEpiError) as ei:
             plan(1, 8, 8, 8, 64, bad_kind)
         assert ce.STATUS[ei.value.status] == "INVALID_ARG"

@@ -104,15 +104,20 @@ constexpr int kKindGnTiles = 11;
 // 130..256-column kind but with each unit's column masks and window offset
 // (also rows of 127 outputs, whose first pass needs the mask).
 constexpr int kKindGnColTiles = 12;
+// ... and 2 x 2 windows over 65..128 channels (rows of 64..126 outputs): no
+// row stacking, a unit's two rows the one band (compiled into the kind of
+// 2 x 2 windows above, the stacking checks cost its shapes 8 %).
+constexpr int kKindGnPool2S1 = 13;
 __host__ __device__ constexpr bool is_gnx(int kind) {
     return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2 ||
-           kind == kKindGnTiles || kind == kKindGnColTiles;
+           kind == kKindGnTiles || kind == kKindGnColTiles || kind == kKindGnPool2S1;
 }
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
 // 96..126 outputs), or the generalised one
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W >= 66 && d.W <= 128) return kKindGnPool2;
+    if (pool_k == 2 && d.Cout <= 128 && d.W >= 66 && d.W <= 128) return kKindGnPool2S1;
     if (d.Cout > 128) return kKindGnTiles;
     // (rows of 127 outputs too: one tile, its first pass masked)
     if ((d.W > 256 || d.W == 129) && d.Cout <= 64) return kKindGnColTiles;
@@ -1029,7 +1034,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // rows of 130..256 columns, or column tiles of wider rows: two passes per unit
     constexpr bool kWide = KIND == kKindGnWide || KIND == kKindGnColTiles;
     constexpr bool kColT = KIND == kKindGnColTiles;
-    constexpr bool kPool2 = KIND == kKindGnPool2;  // 2 x 2 windows: a band per u
+    constexpr bool kPool2 = KIND == kKindGnPool2 || KIND == kKindGnPool2S1;  // 2 x 2 windows: a band per u
+    constexpr bool kP2S1 = KIND == kKindGnPool2S1;  // ... without row stacking: a band per unit
     constexpr int kPitch = kWide || kPool2 ? 65 : kPoolPitch;  // pooled tile pitch (up to 63 windows)
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
     // more than 128 channels: channel tiles of 128, each unit one tile
@@ -1350,12 +1356,16 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // a row writes nothing).  Every warp is past the previous
                 // unit's tile and statistics reads (and none has given up)
                 // before the first tile write.
+                // Without row stacking (65..128 channels) the two u are the
+                // rows r0, r0 + 1 of the one band, both in this thread's
+                // channel row of a 128-channel tile: the first u writes its
+                // maxima, the second folds its own into them in place.
                 if (epi_bar_any(false)) {
                     gn_quit = true;
                 } else {
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const bool row_ok = r0 + 2 * u + slot < a.Ho;  // the same for the whole warp
+                        const bool row_ok = r0 + (kP2S1 ? 1 : 2) * u + slot < a.Ho;  // the same for the whole warp
                         gn_rows += row_ok ? 1 : 0;
                         Frag16 f[kKC];
 #pragma unroll
@@ -1364,7 +1374,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         tmem_ld_wait2(f[0], f[1]);
                         tmem_ld_wait2(f[2], f[3]);
                         if (!row_ok) continue;
-                        float *pt = scratch + (u * 2 + slot) * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch;
+                        constexpr bool s1 = kP2S1;
+                        float *pt = scratch + (s1 ? L * kPitch : (u * 2 + slot) * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch);
 #pragma unroll
                         for (int kc = 0; kc < kKC; ++kc) {
                             uint64_t v2[8];
@@ -1374,7 +1385,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
 #pragma unroll
                             for (int wi = 0; wi < 8; ++wi) {
                                 const float2 a01 = unpack2(v2[wi]);
-                                if (pw0 + wi < 64) pt[pw0 + wi] = fmaxf(a01.x, a01.y);
+                                const float m = fmaxf(a01.x, a01.y);
+                                if (pw0 + wi < 64) pt[pw0 + wi] = s1 && u == 1 ? fmaxf(pt[pw0 + wi], m) : m;
                             }
                             if (kc >= kMask0) {  // columns >= Wo add nothing to the sums
 #pragma unroll
@@ -1593,11 +1605,15 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 }
             }
             if constexpr (kPool2) {
-                // bands 2 ru and 2 ru + 1, each the two row slots folded, sign
-                // and bias restored; windows lane and lane + 32
+                // the unit's bands: one (no stacking: rb, its channels' rows
+                // of the tile already both rows' maxima) or two (2 ru and
+                // 2 ru + 1, each the two row slots folded); sign and bias
+                // restored; windows lane and lane + 32, channels ew + 8 i
+                constexpr bool s1 = kP2S1;
+                constexpr int nbnd = s1 ? 1 : 2, nch = s1 ? 128 / kEpiWarps : 64 / kEpiWarps;
 #pragma unroll
-                for (int band = 0; band < 2; ++band) {
-                    const int prow = ru * 2 + band;
+                for (int band = 0; band < nbnd; ++band) {
+                    const int prow = s1 ? rb : ru * 2 + band;
                     if (prow < a.Hp) {
                         const float *pt0 = scratch + band * 2 * 64 * kPitch, *pt1 = pt0 + 64 * kPitch;
                         float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
@@ -1606,15 +1622,21 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         for (int hw = 0; hw < 2; ++hw) {
                             const int w = lane + 32 * hw;
                             if (w >= a.Wp) continue;
-                            float m[64 / kEpiWarps];
+                            // (8 channels at a time: all their tile reads before the stores)
 #pragma unroll
-                            for (int i = 0; i < 64 / kEpiWarps; ++i) {
-                                const int c2 = ew + kEpiWarps * i;
-                                m[i] = fmaf(gn_sgn[c2], fmaxf(pt0[c2 * kPitch + w], pt1[c2 * kPitch + w]), gn_bias[c2]);
+                            for (int i0 = 0; i0 < nch; i0 += 8) {
+                                float m[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const int c2 = ew + kEpiWarps * (i0 + i);
+                                    const float v =
+                                        s1 ? pt0[c2 * kPitch + w] : fmaxf(pt0[c2 * kPitch + w], pt1[c2 * kPitch + w]);
+                                    m[i] = fmaf(gn_sgn[c2], v, gn_bias[c2]);
+                                }
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    if (ew + kEpiWarps * (i0 + i) < a.Co) dst[(i0 + i) * cstep + w] = m[i];
                             }
-#pragma unroll
-                            for (int i = 0; i < 64 / kEpiWarps; ++i)
-                                if (ew + kEpiWarps * i < a.Co) dst[i * cstep + w] = m[i];
                         }
                     }
                 }
@@ -1745,7 +1767,9 @@ constexpr uint32_t kFinFlagOff = kFinPairs * 64 * 2 * 4;  // after the coefficie
 constexpr uint32_t kFinBarOff = kFinFlagOff + 8;         // an mbarrier per batch (or per ring slot)
 constexpr uint32_t kFinBufOff = 8448;                     // the pooled blocks (128-byte aligned)
 static_assert(kFinBarOff + 8u * kFinPairs <= kFinBufOff, "finalize barriers overlap the pooled blocks");
-template <bool kGnX>
+// kHalf: a unit of 2 rows holds half a 4-row band (65..128 channels, or
+// rows of 127 or more columns), so each pooled block comes in two slots
+template <bool kGnX, bool kHalf>
 __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, volatile int *abort_flag) {
     float *sA = reinterpret_cast<float *>(smem), *sB = sA + kFinPairs * 64;
     int &s_go = *reinterpret_cast<int *>(smem + kFinFlagOff);
@@ -1785,7 +1809,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     const int npairs = a.N * a.groups;
     // (with half bands, a pair's two slots side by side: [pair][slot][F4])
     // (a unit of 2 rows holds half a band: 65..128 channels, or rows of 130..256 columns)
-    const uint32_t nsl = kGnX && a.RU == 2 ? 2u : 1u, sbytes = nsl * pbytes;
+    const uint32_t nsl = kGnX && kHalf && a.RU == 2 ? 2u : 1u, sbytes = nsl * pbytes;
     if constexpr (kGnX) {
         // this CTA's pairs p = blockIdx.x + k * gridDim.x (k < K) through a ring
         // of cap slots: pair k lands in slot k % cap, and the copy of pair
@@ -1839,7 +1863,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
                 float4 *bp = bp0 + t;
                 const float4 v = bp[0];
                 float r[4] = {v.x, v.y, v.z, v.w};
-                if (a.RU == 2) {
+                if (nsl == 2) {
                     // the band's extreme from its two halves: the larger y where
                     // the slope A is >= 0, else the smaller
                     const float4 w = bp[F4];
@@ -1907,7 +1931,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
                 float4 *bp = buf + jb * nsl * F4 + fo;
                 const float4 v = bp[0];
                 float r[4] = {v.x, v.y, v.z, v.w};
-                if (kGnX && a.RU == 2) {
+                if (kGnX && nsl == 2) {
                     // the band's extreme from its two halves: the larger y where
                     // the slope A is >= 0, else the smaller
                     const float4 w = bp[F4];
@@ -2010,7 +2034,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         tmem_dealloc(*tmem_slot, kTmemCols);
     }
     if constexpr (is_gn(KIND)) {
-        if (a.gn_fin) gn_finalize_tail<is_gnx(KIND)>(a, smem, abort_flag);
+        if (a.gn_fin) gn_finalize_tail<is_gnx(KIND), KIND != kKindGnPool2S1>(a, smem, abort_flag);
     }
 }
 
@@ -2111,6 +2135,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case kKindGnColTiles:
         return (uint32_t)((2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnPool2:  // two band regions of pitch 65, the statistics, the tables
+    case kKindGnPool2S1:
         return (uint32_t)((2 * 2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnX:  // (the tables for up to 128 channels)
     case kKindGnXNarrow:
@@ -2324,7 +2349,9 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // most 64, for the shuffle sums and the fold)
     // 2 x 2 windows (Cout <= 64): the one-band layout, two bands per unit,
     // the first 64 output columns whole
-    const bool pool2 = kind == kKindGnPool2 && pl.S == 2 && pl.RU == 4 && pl.P > 64 && pl.P <= 128 && d.W - 2 >= 64;
+    // (65..128 channels: no stacking, a unit's two rows the one band)
+    const bool pool2 = (kind == kKindGnPool2 || kind == kKindGnPool2S1) && pl.U == 2 && pl.P > 64 && pl.P <= 128 &&
+                       d.W - 2 >= 64;
     // rows wider than 256 columns (Cout <= 64): column tiles of 252 outputs,
     // each unit one row pair of one tile (rows of 127 outputs: one tile)
     const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.P > 128;
@@ -2334,6 +2361,11 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
                       : e.pool_k == 2 && pool2;
     return shape && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
+
+// a fused GroupNorm unit of 2 rows holds half a 4-row band (its pooled
+// extremes in two workspace slots, folded by the finalize); 2 x 2 windows
+// make such a unit a whole band
+bool tc_gn_half(const Plan &pl, int kind) { return pl.RU == 2 && kind != kKindGnPool2S1; }
 
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
     Plan pl;
@@ -2535,7 +2567,9 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
         // (a unit's windows: up to 32 or, for the two-pass rows, 64; column tiles any number)
-        const int max_wp = kkind == kKindGnColTiles ? a.Wp : kkind == kKindGnWide || kkind == kKindGnPool2 ? 64 : 32;
+        const int max_wp = kkind == kKindGnColTiles                                                  ? a.Wp
+                           : kkind == kKindGnWide || kkind == kKindGnPool2 || kkind == kKindGnPool2S1 ? 64
+                                                                                                      : 32;
         if (h->gn.units != a.units_per_img || a.Wp > max_wp) return CONV_EPI_ERR_INVALID_ARG;
         // finalize inside the kernel when each (image, group) block of pooled
         // values is whole float4s (16-byte aligned blocks) and small enough
@@ -2543,8 +2577,8 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         // channel offsets < 2^16); otherwise the separate finalize kernel
         const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
         a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
-                    // one pair's blocks fit the buffer (the generalised kinds' ring ends below the barriers)
-                    F * 4u * (pl.RU == 2 ? 2u : 1u) <= pl.bar_off - kFinBufOff &&
+                    // one pair's blocks (two slots each for half bands) fit the buffer
+                    F * 4u * (tc_gn_half(pl, kkind) ? 2u : 1u) <= pl.bar_off - kFinBufOff &&
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
@@ -2575,6 +2609,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
                    : kkind == kKindGnXNarrow ? launch_tc<kKindGnXNarrow>(args, pl, grid, s)
                    : kkind == kKindGnWide    ? launch_tc<kKindGnWide>(args, pl, grid, s)
                    : kkind == kKindGnPool2   ? launch_tc<kKindGnPool2>(args, pl, grid, s)
+                   : kkind == kKindGnPool2S1 ? launch_tc<kKindGnPool2S1>(args, pl, grid, s)
                    : kkind == kKindGnTiles   ? launch_tc<kKindGnTiles>(args, pl, grid, s)
                    : kkind == kKindGnColTiles ? launch_tc<kKindGnColTiles>(args, pl, grid, s)
                                              : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
@@ -2591,7 +2626,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (st) return st;
     h->last_launches = pl.MT + 1 + fills + (padded ? 1 : 0);  // packs, fill, conv, row padding
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
-        if ((st = gn_finalize(h, e, out, s, true, pl.RU == 2))) return st;
+        if ((st = gn_finalize(h, e, out, s, true, tc_gn_half(pl, kkind)))) return st;
         h->last_launches += 1;
     }
     return CONV_EPI_OK;
