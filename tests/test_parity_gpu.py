@@ -82,7 +82,9 @@ SMALL = {
     "c5_co96_w100": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=100, Cout=96, groups=12),  # fused, 32 zero filters, P 112
     "c5_co128_g2": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=110, Cout=128, groups=2),   # fused, 64 channels per group
     "c5_co256": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=64, Cout=256, groups=32),  # 2 channel tiles, W 64: whole bands per tile
-    "c5_k2": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=50, pool_k=2),               # 2 x 2 windows, odd tail row
+    "c5_k2": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=50, pool_k=2),               # 2 x 2 windows, odd tail row (four bands per unit)
+    "c5_k2_w64": W["c5_gn_pool_clamp"].resized(N=1, H=19, W=64, Cout=32, groups=8, pool_k=2),  # a unit of one valid row
+    "c5_k2_w20": W["c5_gn_pool_clamp"].resized(N=2, H=12, W=20, pool_k=2, groups=4),          # 9 windows
     "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling
     "c5_k2_w300": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=300, pool_k=2, groups=64),  # 2 column tiles, a group per channel
     # 2 x 2 windows fused (Cout <= 64, W 66..128: two bands of 2 rows per unit)

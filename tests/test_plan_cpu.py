@@ -138,12 +138,18 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout, pool_k=4):
             # 2 x 2 windows: two band regions of pitch 65 (up to 63 windows),
             # the statistics, 128-channel tables; the tile writes reach
             # (band * 2 + slot) * 64 * 65 + channel * 65 + window (window < 64)
-            # (no stacking: one band, channel rows 0..127 of pitch 65)
-            assert U == 2
-            top = max((b * 2 + sl) * 64 * 65 + ch * 65 + w for b in (0, 1) for sl in (0, 1) for ch in range(64)
-                      for w in range(64))
-            assert max(ch * 65 + w for ch in range(128) for w in range(64)) < top
-            assert top < 2 * 2 * 64 * 65 and q["scratch_bytes"] >= (2 * 2 * 64 * 65 + 2 * 256 + 2 * 128) * 4
+            # (no stacking: one band, channel rows 0..127 of pitch 65; rows of
+            # up to 64 columns: four bands of pitch 33, windows < 32)
+            assert U in (2, 4)
+            if U == 4:
+                top = max((b * 2 + sl) * 64 * 33 + ch * 33 + w for b in range(4) for sl in (0, 1) for ch in range(64)
+                          for w in range(32))
+                assert top < 4 * 2 * 64 * 33 and q["scratch_bytes"] >= (4 * 2 * 64 * 33 + 2 * 256 + 2 * 128) * 4
+            else:
+                top = max((b * 2 + sl) * 64 * 65 + ch * 65 + w for b in (0, 1) for sl in (0, 1) for ch in range(64)
+                          for w in range(64))
+                assert max(ch * 65 + w for ch in range(128) for w in range(64)) < top
+                assert top < 2 * 2 * 64 * 65 and q["scratch_bytes"] >= (2 * 2 * 64 * 65 + 2 * 256 + 2 * 128) * 4
         elif U == 1:
             # wide rows: one band region of pitch 65 (up to 63 windows), the
             # statistics, 128-channel tables; the tile writes reach
@@ -195,8 +201,8 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     cpg = Cout // groups
     if kind != ce.GN_SCALE_POOL_CLAMP or pool_k not in (2, 4) or cpg & (cpg - 1) or cpg > 64:
         return False
-    if pool_k == 2:  # 2 x 2 windows: rows of 66..128 columns, up to 128 channels
-        return Cout <= 128 and 66 <= W <= 128
+    if pool_k == 2:  # 2 x 2 windows: rows of 66..128 columns up to 128 channels, of up to 64 up to 64
+        return (Cout <= 128 and 66 <= W <= 128) or (Cout <= 64 and W <= 64)
     # rows of 130..256 columns (Cout <= 64): one row pair per unit; wider
     # rows: the same per column tile of 252 outputs
     # more than 64 channels: no row stacking, half a band per unit (more than
@@ -227,7 +233,8 @@ def test_random_shapes_all_planned_and_in_range():
     exactly when groups have a power-of-two size up to 64 and either
     pool_k = 4 with Cout <= 64 and W != 65, or Cout > 64 with W <= 64 or
     66 <= W <= 128, or pool_k = 2 with
-    Cout <= 128 and 66 <= W <= 128; otherwise they are planned as the plain
+    Cout <= 128 and 66 <= W <= 128 or Cout <= 64 and W <= 64; otherwise they
+    are planned as the plain
     conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):

@@ -116,7 +116,7 @@ __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
 // 96..126 outputs), or the generalised one
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
-    if (pool_k == 2 && d.Cout <= 64 && d.W >= 66 && d.W <= 128) return kKindGnPool2;
+    if (pool_k == 2 && d.Cout <= 64 && d.W <= 128 && d.W != 65) return kKindGnPool2;
     if (pool_k == 2 && d.Cout <= 128 && d.W >= 66 && d.W <= 128) return kKindGnPool2S1;
     if (d.Cout > 128) return kKindGnTiles;
     // (rows of 127 outputs too: one tile, its first pass masked)
@@ -1036,7 +1036,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr bool kColT = KIND == kKindGnColTiles;
     constexpr bool kPool2 = KIND == kKindGnPool2 || KIND == kKindGnPool2S1;  // 2 x 2 windows: a band per u
     constexpr bool kP2S1 = KIND == kKindGnPool2S1;  // ... without row stacking: a band per unit
-    constexpr int kPitch = kWide || kPool2 ? 65 : kPoolPitch;  // pooled tile pitch (up to 63 windows)
+    // pooled tile pitch: up to 63 windows, or (rows of up to 64 columns) 31
+    constexpr int kPitch = kWide || (kPool2 && !GENERAL) ? 65 : kPoolPitch;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
     // more than 128 channels: channel tiles of 128, each unit one tile
     constexpr bool kTiles = KIND == kKindGnTiles;
@@ -1089,7 +1090,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // 64 columns: four u); 16-column chunks per warp and u: 4 or 2
     // (2 x 2 windows: one band per u, two per unit, 8 windows per chunk
     // written to the tiles as they are found)
-    constexpr int kNB = (kGN && (GENERAL || kPool2)) ? 2 : 1;
+    constexpr int kNB = kPool2 && GENERAL ? 4 : (kGN && (GENERAL || kPool2)) ? 2 : 1;
     constexpr int kKC = (kGN && GENERAL) ? 2 : 4;
     constexpr int kWin = 4 * kKC;  // pooling windows per band and thread (4 x 4 windows)
     float *gn_sgn = scratch + kNB * 2 * 64 * kPitch + 2 * kEpiThreads, *gn_bias = gn_sgn + (kGnX ? 128 : 64);
@@ -1364,7 +1365,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     gn_quit = true;
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
+                    for (int u = 0; u < (GENERAL ? 4 : 2); ++u) {  // (rows of up to 64 columns: four u, four bands)
                         const bool row_ok = r0 + (kP2S1 ? 1 : 2) * u + slot < a.Ho;  // the same for the whole warp
                         gn_rows += row_ok ? 1 : 0;
                         Frag16 f[kKC];
@@ -1375,7 +1376,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         tmem_ld_wait2(f[2], f[3]);
                         if (!row_ok) continue;
                         constexpr bool s1 = kP2S1;
-                        float *pt = scratch + (s1 ? L * kPitch : (u * 2 + slot) * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch);
+                        float *pt =
+                            scratch + (s1 ? L * kPitch : (u * 2 + slot) * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch);
 #pragma unroll
                         for (int kc = 0; kc < kKC; ++kc) {
                             uint64_t v2[8];
@@ -1386,7 +1388,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                             for (int wi = 0; wi < 8; ++wi) {
                                 const float2 a01 = unpack2(v2[wi]);
                                 const float m = fmaxf(a01.x, a01.y);
-                                if (pw0 + wi < 64) pt[pw0 + wi] = s1 && u == 1 ? fmaxf(pt[pw0 + wi], m) : m;
+                                if (pw0 + wi < kPitch - 1) pt[pw0 + wi] = s1 && u == 1 ? fmaxf(pt[pw0 + wi], m) : m;
                             }
                             if (kc >= kMask0) {  // columns >= Wo add nothing to the sums
 #pragma unroll
@@ -1610,10 +1612,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // 2 ru + 1, each the two row slots folded); sign and bias
                 // restored; windows lane and lane + 32, channels ew + 8 i
                 constexpr bool s1 = kP2S1;
-                constexpr int nbnd = s1 ? 1 : 2, nch = s1 ? 128 / kEpiWarps : 64 / kEpiWarps;
+                constexpr int nbnd = s1 ? 1 : kNB, nch = s1 ? 128 / kEpiWarps : 64 / kEpiWarps;
 #pragma unroll
                 for (int band = 0; band < nbnd; ++band) {
-                    const int prow = s1 ? rb : ru * 2 + band;
+                    const int prow = s1 ? rb : ru * nbnd + band;
                     if (prow < a.Hp) {
                         const float *pt0 = scratch + band * 2 * 64 * kPitch, *pt1 = pt0 + 64 * kPitch;
                         float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
@@ -2134,9 +2136,10 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
     case kKindGnWide:  // one band region of pitch 65, the statistics, the tables
     case kKindGnColTiles:
         return (uint32_t)((2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
-    case kKindGnPool2:  // two band regions of pitch 65, the statistics, the tables
-    case kKindGnPool2S1:
-        return (uint32_t)((2 * 2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
+    case kKindGnPool2:  // two band regions of pitch 65 (rows of up to 64 columns: four of pitch 33), the
+    case kKindGnPool2S1:  // statistics, the tables
+        return (uint32_t)(((U == 4 ? 4 * 2 * 64 * kPoolPitch : 2 * 2 * 64 * 65) + 2 * kEpiThreads + 2 * 128) *
+                          sizeof(float));
     case kKindGnX:  // (the tables for up to 128 channels)
     case kKindGnXNarrow:
     case kKindGnTiles:
@@ -2350,8 +2353,9 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // 2 x 2 windows (Cout <= 64): the one-band layout, two bands per unit,
     // the first 64 output columns whole
     // (65..128 channels: no stacking, a unit's two rows the one band)
-    const bool pool2 = (kind == kKindGnPool2 || kind == kKindGnPool2S1) && pl.U == 2 && pl.P > 64 && pl.P <= 128 &&
-                       d.W - 2 >= 64;
+    const bool pool2 = ((kind == kKindGnPool2 || kind == kKindGnPool2S1) && pl.U == 2 && pl.P > 64 && pl.P <= 128 &&
+                        d.W - 2 >= 64) ||
+                       (kind == kKindGnPool2 && pl.S == 2 && pl.U == 4 && pl.P == 64);  // (four bands per unit)
     // rows wider than 256 columns (Cout <= 64): column tiles of 252 outputs,
     // each unit one row pair of one tile (rows of 127 outputs: one tile)
     const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.P > 128;
