@@ -161,8 +161,7 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *     with Cout > 64 and
  *     W <= 64 or 66 <= W <= 128 (more than 128 channels as channel tiles of
  *     128), or
- *     pool_k = 2 with Cout <= 128 and 66 <= W <= 128 or Cout <= 64 and
- *     W <= 64;
+ *     pool_k = 2 with Cout <= 128 and W <= 128 (not 65);
  *     any other GN
  *     shape runs as two passes, the tensor-core conv
  *     writing y (bias added) and its per-unit sums of y and y^2 into a

@@ -201,8 +201,8 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     cpg = Cout // groups
     if kind != ce.GN_SCALE_POOL_CLAMP or pool_k not in (2, 4) or cpg & (cpg - 1) or cpg > 64:
         return False
-    if pool_k == 2:  # 2 x 2 windows: rows of 66..128 columns up to 128 channels, of up to 64 up to 64
-        return (Cout <= 128 and 66 <= W <= 128) or (Cout <= 64 and W <= 64)
+    if pool_k == 2:  # 2 x 2 windows: rows of up to 128 columns, up to 128 channels
+        return Cout <= 128 and W <= 128 and W != 65
     # rows of 130..256 columns (Cout <= 64): one row pair per unit; wider
     # rows: the same per column tile of 252 outputs
     # more than 64 channels: no row stacking, half a band per unit (more than
@@ -233,8 +233,8 @@ def test_random_shapes_all_planned_and_in_range():
     exactly when groups have a power-of-two size up to 64 and either
     pool_k = 4 with Cout <= 64 and W != 65, or Cout > 64 with W <= 64 or
     66 <= W <= 128, or pool_k = 2 with
-    Cout <= 128 and 66 <= W <= 128 or Cout <= 64 and W <= 64; otherwise they
-    are planned as the plain
+    Cout <= 128 and W <= 128 (not 65); otherwise they are planned as the
+    plain
     conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):

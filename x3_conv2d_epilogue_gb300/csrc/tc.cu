@@ -117,7 +117,7 @@ __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_
 // 96..126 outputs), or the generalised one
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W <= 128 && d.W != 65) return kKindGnPool2;
-    if (pool_k == 2 && d.Cout <= 128 && d.W >= 66 && d.W <= 128) return kKindGnPool2S1;
+    if (pool_k == 2 && d.Cout <= 128 && d.W <= 128 && d.W != 65) return kKindGnPool2S1;
     if (d.Cout > 128) return kKindGnTiles;
     // (rows of 127 outputs too: one tile, its first pass masked)
     if ((d.W > 256 || d.W == 129) && d.Cout <= 64) return kKindGnColTiles;
@@ -1375,9 +1375,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                         tmem_ld_wait2(f[0], f[1]);
                         tmem_ld_wait2(f[2], f[3]);
                         if (!row_ok) continue;
+                        // (no stacking: band u / 2's region of 128 channel rows)
                         constexpr bool s1 = kP2S1;
-                        float *pt =
-                            scratch + (s1 ? L * kPitch : (u * 2 + slot) * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch);
+                        float *pt = scratch + (s1 ? ((u >> 1) * 128 + L) * kPitch
+                                                  : (u * 2 + slot) * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch);
 #pragma unroll
                         for (int kc = 0; kc < kKC; ++kc) {
                             uint64_t v2[8];
@@ -1388,7 +1389,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                             for (int wi = 0; wi < 8; ++wi) {
                                 const float2 a01 = unpack2(v2[wi]);
                                 const float m = fmaxf(a01.x, a01.y);
-                                if (pw0 + wi < kPitch - 1) pt[pw0 + wi] = s1 && u == 1 ? fmaxf(pt[pw0 + wi], m) : m;
+                                if (pw0 + wi < kPitch - 1) pt[pw0 + wi] = s1 && (u & 1) ? fmaxf(pt[pw0 + wi], m) : m;
                             }
                             if (kc >= kMask0) {  // columns >= Wo add nothing to the sums
 #pragma unroll
@@ -1612,10 +1613,11 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                 // 2 ru + 1, each the two row slots folded); sign and bias
                 // restored; windows lane and lane + 32, channels ew + 8 i
                 constexpr bool s1 = kP2S1;
-                constexpr int nbnd = s1 ? 1 : kNB, nch = s1 ? 128 / kEpiWarps : 64 / kEpiWarps;
+                // (no stacking: one band per unit, or two in the four-u form)
+                constexpr int nbnd = s1 ? (GENERAL ? 2 : 1) : kNB, nch = s1 ? 128 / kEpiWarps : 64 / kEpiWarps;
 #pragma unroll
                 for (int band = 0; band < nbnd; ++band) {
-                    const int prow = s1 ? rb : ru * nbnd + band;
+                    const int prow = (s1 ? rb : ru) * nbnd + band;
                     if (prow < a.Hp) {
                         const float *pt0 = scratch + band * 2 * 64 * kPitch, *pt1 = pt0 + 64 * kPitch;
                         float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
@@ -2355,7 +2357,7 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // (65..128 channels: no stacking, a unit's two rows the one band)
     const bool pool2 = ((kind == kKindGnPool2 || kind == kKindGnPool2S1) && pl.U == 2 && pl.P > 64 && pl.P <= 128 &&
                         d.W - 2 >= 64) ||
-                       (kind == kKindGnPool2 && pl.S == 2 && pl.U == 4 && pl.P == 64);  // (four bands per unit)
+                       ((kind == kKindGnPool2 || kind == kKindGnPool2S1) && pl.U == 4 && pl.P == 64);  // (four u per unit)
     // rows wider than 256 columns (Cout <= 64): column tiles of 252 outputs,
     // each unit one row pair of one tile (rows of 127 outputs: one tile)
     const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.P > 128;
