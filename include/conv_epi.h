@@ -161,7 +161,10 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *     with Cout > 64 and
  *     W <= 64 or 66 <= W <= 128 (more than 128 channels as channel tiles of
  *     128), or
- *     pool_k = 2 with Cout <= 128 and W <= 128 (not 65);
+ *     pool_k = 2 with Cout <= 128 and W <= 128 (not 65), or Cout <= 64 and
+ *     130 <= W <= 256 where its pooled tile fits the shared memory beside
+ *     the smallest rings (NCHW with Cin <= 8: W <= 240; channels last: up
+ *     to 256);
  *     any other GN
  *     shape runs as two passes, the tensor-core conv
  *     writing y (bias added) and its per-unit sums of y and y^2 into a

@@ -156,6 +156,7 @@ GN_WIDE = {
     "c5_w512": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=8, H=512, W=512),         # column tiles, separate finalize
     "c5_pool2_co128": synth.WORKLOADS["c5_gn_pool_clamp"].resized(Cout=128, groups=16, pool_k=2),  # 2x2, no stacking
     "c5_pool2_w64": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=256, H=64, W=64, pool_k=2),      # 2x2, four bands per unit
+    "c5_pool2_w240": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=32, H=240, W=240, pool_k=2),    # 2x2, rows of 238
 }
 
 

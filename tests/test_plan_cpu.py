@@ -140,8 +140,12 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout, pool_k=4):
             # (band * 2 + slot) * 64 * 65 + channel * 65 + window (window < 64)
             # (no stacking: one band, channel rows 0..127 of pitch 65; rows of
             # up to 64 columns: four bands of pitch 33, windows < 32)
-            assert U in (2, 4)
-            if U == 4:
+            assert U in (1, 2, 4)
+            if U == 1:
+                # rows of 130..240 columns: one row pair, two slots of pitch 129 (windows < 128)
+                top = max(sl * 64 * 129 + ch * 129 + w for sl in (0, 1) for ch in range(64) for w in range(128))
+                assert top < 2 * 64 * 129 and q["scratch_bytes"] >= (2 * 64 * 129 + 2 * 256 + 2 * 128) * 4
+            elif U == 4:
                 top = max((b * 2 + sl) * 64 * 33 + ch * 33 + w for b in range(4) for sl in (0, 1) for ch in range(64)
                           for w in range(32))
                 assert top < 4 * 2 * 64 * 33 and q["scratch_bytes"] >= (4 * 2 * 64 * 33 + 2 * 256 + 2 * 128) * 4
@@ -191,7 +195,25 @@ def test_plans_of_tested_shapes(case, layout):
     check_gn_form(plan(*args, groups=wl.groups, pool_k=wl.pool_k), *args, pool_k=wl.pool_k, groups=wl.groups)
 
 
-def gn_fused(kind, Cout, W, pool_k, groups):
+def wide_p2_fits(Cin, W, nhwc):
+    """2 x 2 windows on rows of 130..256 columns: the smallest plan (the
+    filter resident when it fits beside 2 B planes and 2 staged tiles, else
+    2 filter stages) with its two-slot tile of pitch 129 within the CTA's
+    shared memory -- the kernel's own rule restated."""
+    up1k = lambda v: (v + 1023) // 1024 * 1024
+    P = (W + 15) // 16 * 16
+    a = up1k(3 * 2 * 5 * 64 * 16)
+    pl_ = (4 * P + 4 + 7) // 8 * 8
+    b = up1k(2 * pl_ * 16)
+    raw = 0 if nhwc else up1k(8 * 4 * ((W + 3) // 4 * 4) * 4)
+    nr0 = 0 if nhwc else 2
+    tail = 8 * 30 + 32 + (2 * 64 * 129 + 2 * 256 + 2 * 128) * 4
+    chunks = (Cin + 7) // 8
+    resident = chunks * a + 2 * b + nr0 * raw + tail <= 232448
+    return (chunks * a if resident else 2 * a) + 2 * b + nr0 * raw + tail <= 232448
+
+
+def gn_fused(kind, Cout, W, pool_k, groups, nhwc=False, Cin=8):
     # rows of up to 64 columns run as two pooling bands per unit; wider rows as
     # one band, fused when the first 96 output columns are whole (Wo >= 96);
     # up to 64 channels (a 64-channel GEMM), a group's channels a power of two
@@ -201,8 +223,9 @@ def gn_fused(kind, Cout, W, pool_k, groups):
     cpg = Cout // groups
     if kind != ce.GN_SCALE_POOL_CLAMP or pool_k not in (2, 4) or cpg & (cpg - 1) or cpg > 64:
         return False
-    if pool_k == 2:  # 2 x 2 windows: rows of up to 128 columns, up to 128 channels
-        return Cout <= 128 and W <= 128 and W != 65
+    if pool_k == 2:  # 2 x 2 windows: rows of up to 128 columns up to 128 channels, of 130..240 up to 64
+        # (rows of 130..256: where the plan fits shared memory, e.g. W <= 240 for NCHW with Cin <= 8)
+        return (Cout <= 128 and W <= 128 and W != 65) or (Cout <= 64 and 130 <= W <= 256 and wide_p2_fits(Cin, W, nhwc))
     # rows of 130..256 columns (Cout <= 64): one row pair per unit; wider
     # rows: the same per column tile of 252 outputs
     # more than 64 channels: no row stacking, half a band per unit (more than
@@ -214,7 +237,8 @@ def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
     """A GroupNorm shape the fused epilogue does not take runs as two passes:
     its plan is the plain conv's, and the handle holds the conv output
     between them."""
-    two_pass = kind == ce.GN_SCALE_POOL_CLAMP and not gn_fused(kind, Cout, W, pool_k, groups)
+    two_pass = kind == ce.GN_SCALE_POOL_CLAMP and not gn_fused(kind, Cout, W, pool_k, groups, layout == ce.LAYOUT_NHWC,
+                                                               Cin)
     assert q["gn_two_pass"] == int(two_pass)
     # the conv output, then (256-byte aligned) the conv kernel's per-unit sums:
     # (image, unit, 2 column groups, 128 accumulator rows) float pairs
@@ -233,8 +257,9 @@ def test_random_shapes_all_planned_and_in_range():
     exactly when groups have a power-of-two size up to 64 and either
     pool_k = 4 with Cout <= 64 and W != 65, or Cout > 64 with W <= 64 or
     66 <= W <= 128, or pool_k = 2 with
-    Cout <= 128 and W <= 128 (not 65); otherwise they are planned as the
-    plain
+    Cout <= 128 and W <= 128 (not 65) or Cout <= 64 and 130 <= W <= 256
+    where the plan fits shared memory;
+    otherwise they are planned as the plain
     conv of the two-pass form."""
     rng = random.Random(20261203)
     for _ in range(3000):
@@ -266,7 +291,7 @@ def test_plan_query_arguments():
         ce._check(ce._lib().conv_epi_plan_query(ce.C.byref(d), ce.C.byref(epi_for(ce.MIN_TANH2)),
                                                 ce.C.byref(q)), "plan")
     assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
-    for bad_kind in (6, 7, 8, 9, 10, 11, 12, 13, -1):    # bad chain (the kernel's internal kinds included)
+    for bad_kind in (6, 7, 8, 9, 10, 11, 12, 13, 14, -1):  # bad chain (the kernel's internal kinds included)
         with pytest.raises(ce.ConvEpiError) as ei:
             plan(1, 8, 8, 8, 64, bad_kind)
         assert ce.STATUS[ei.value.status] == "INVALID_ARG"

@@ -108,15 +108,22 @@ constexpr int kKindGnColTiles = 12;
 // row stacking, a unit's two rows the one band (compiled into the kind of
 // 2 x 2 windows above, the stacking checks cost its shapes 8 %).
 constexpr int kKindGnPool2S1 = 13;
+// ... and 2 x 2 windows on rows of 130..240 columns (Cout <= 64): one row
+// pair, one band, per unit, its up to 119 windows gathered in two passes of
+// four chunks per warp (the second masked) straight into the tile (with
+// rows of 256 staged columns the two-slot tile and the minimal rings exceed
+// shared memory).
+constexpr int kKindGnWideP2 = 14;
 __host__ __device__ constexpr bool is_gnx(int kind) {
     return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2 ||
-           kind == kKindGnTiles || kind == kKindGnColTiles || kind == kKindGnPool2S1;
+           kind == kKindGnTiles || kind == kKindGnColTiles || kind == kKindGnPool2S1 || kind == kKindGnWideP2;
 }
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
 // 96..126 outputs), or the generalised one
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W <= 128 && d.W != 65) return kKindGnPool2;
+    if (pool_k == 2 && d.Cout <= 64 && d.W >= 130 && d.W <= 256) return kKindGnWideP2;  // (fused up to 240: below)
     if (pool_k == 2 && d.Cout <= 128 && d.W <= 128 && d.W != 65) return kKindGnPool2S1;
     if (d.Cout > 128) return kKindGnTiles;
     // (rows of 127 outputs too: one tile, its first pass masked)
@@ -1036,8 +1043,10 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr bool kColT = KIND == kKindGnColTiles;
     constexpr bool kPool2 = KIND == kKindGnPool2 || KIND == kKindGnPool2S1;  // 2 x 2 windows: a band per u
     constexpr bool kP2S1 = KIND == kKindGnPool2S1;  // ... without row stacking: a band per unit
-    // pooled tile pitch: up to 63 windows, or (rows of up to 64 columns) 31
-    constexpr int kPitch = kWide || (kPool2 && !GENERAL) ? 65 : kPoolPitch;
+    constexpr bool kWideP2 = KIND == kKindGnWideP2;  // 2 x 2 windows on rows of 130..256 columns
+    // pooled tile pitch: up to 63 windows, (rows of up to 64 columns) 31, or
+    // (2 x 2 windows on wide rows) 127
+    constexpr int kPitch = kWideP2 ? 129 : kWide || (kPool2 && !GENERAL) ? 65 : kPoolPitch;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP || kGnX;
     // more than 128 channels: channel tiles of 128, each unit one tile
     constexpr bool kTiles = KIND == kKindGnTiles;
@@ -1103,7 +1112,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // when column 16 cc + i < Wo.  (A select per value costs as much as the
     // sums, so only the chunks that can be ragged take it.)  gn_ncol counts
     // this thread's valid columns.
-    constexpr int kMask0 = kWide ? 4 : kKC == 4 ? (KIND == kKindGnXNarrow || kPool2 || kTiles ? 2 : 3) : 0;
+    constexpr int kMask0 = kWide || kWideP2 ? 4 : kKC == 4 ? (KIND == kKindGnXNarrow || kPool2 || kTiles ? 2 : 3) : 0;
     uint32_t gn_rag = 0;
     int gn_ncol = 0;
     if constexpr (kGN) {
@@ -1117,7 +1126,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     // wide rows: the second pass's chunks cc = hc + 8 + 2 kc, bit 16 kc + i
     // set when column 16 cc + i < Wo (the first pass's lie below 128 <= Wo)
     uint64_t gn_ragw = 0;
-    if constexpr (kWide) {
+    if constexpr (kWide || kWideP2) {
         for (int kc = 0; kc < 4; ++kc) {
             const int lim = a.Wo - 16 * (hc + 8 + 2 * kc), nv = lim < 0 ? 0 : lim > 16 ? 16 : lim;
             gn_ncol += nv;
@@ -1268,7 +1277,57 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
                 }
             };
-            if constexpr (kWide) {
+            if constexpr (kWideP2) {
+                // one u (rows r0, r0 + 1 in the two slots: one 2 x 2 band),
+                // 8 or fewer chunks per warp in two passes of 4 (the first,
+                // columns below 128, whole; the second masked); a chunk's 8
+                // window maxima go to the tile at once, after the vote that
+                // every warp is past the previous unit's tile reads
+                if (epi_bar_any(false)) {
+                    gn_quit = true;
+                } else {
+                    const bool row_ok = r0 + slot < a.Ho;  // the same for the whole warp
+                    gn_rows += row_ok ? 1 : 0;
+                    float *pt = scratch + slot * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch;
+#pragma unroll
+                    for (int pass = 0; pass < 2; ++pass) {
+                        Frag16 f[kKC];
+#pragma unroll
+                        for (int kc = 0; kc < kKC; ++kc)
+                            if (hc + 8 * pass + 2 * kc < nchunks)
+                                tmem_ld16_issue(tbase + (hc + 8 * pass + 2 * kc) * 16, f[kc]);
+                        tmem_ld_wait2(f[0], f[1]);
+                        tmem_ld_wait2(f[2], f[3]);
+                        if (!row_ok) continue;
+#pragma unroll
+                        for (int kc = 0; kc < kKC; ++kc) {
+                            uint64_t v2[8];
+#pragma unroll
+                            for (int p = 0; p < 8; ++p) v2[p] = pack2(f[kc].r[2 * p], f[kc].r[2 * p + 1]);
+                            const int pw0 = (hc + 8 * pass + 2 * kc) * 8;  // this chunk's first window
+#pragma unroll
+                            for (int wi = 0; wi < 8; ++wi) {
+                                const float2 a01 = unpack2(v2[wi]);
+                                if (pw0 + wi < kPitch - 1) pt[pw0 + wi] = fmaxf(a01.x, a01.y);
+                            }
+                            if (pass == 1) {  // columns >= Wo add nothing to the sums
+#pragma unroll
+                                for (int p = 0; p < 8; ++p) {
+                                    const uint64_t b0 = 1ull << (16 * kc + 2 * p);
+                                    const float2 w = unpack2(v2[p]);
+                                    v2[p] = pack2(__float_as_uint((gn_ragw & b0) ? w.x : 0.0f),
+                                                  __float_as_uint((gn_ragw & (b0 << 1)) ? w.y : 0.0f));
+                                }
+                            }
+#pragma unroll
+                            for (int p = 0; p < 8; ++p) {
+                                ls2[p & 1] = add2u(ls2[p & 1], v2[p]);
+                                lss2[p & 1] = fma2u(v2[p], v2[p], lss2[p & 1]);
+                            }
+                        }
+                    }
+                }
+            } else if constexpr (kWide) {
                 // one u (rows r0, r0 + 1 in the two slots), 8 or fewer chunks
                 // per warp in two passes of 4: the first (columns below 128)
                 // whole, the second masked; each pass's window extremes go to
@@ -1549,7 +1608,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
             // stores fold the two slots
             // every warp is past the previous unit's tile and statistics reads
             // (and none has given up) before they are rewritten
-            if (!kWide && !kPool2 && epi_bar_any(false)) break;  // (wide rows, 2 x 2 windows: voted before their first tile)
+            if (!kWide && !kPool2 && !kWideP2 && epi_bar_any(false)) break;  // (wide rows, 2 x 2 windows: voted before their first tile)
             // channel tiles: the sign and bias tables of this unit's tile (the
             // vote above ends the previous unit's reads of them)
             if (kTiles && MT > 1) gn_sgn[co] = gsg, gn_bias[co] = bias;
@@ -1567,7 +1626,7 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     if (pw < 32) pt[cl * kPoolPitch + pw] = pext[k];
                 }
             };
-            if constexpr (!kWide && !kPool2) {
+            if constexpr (!kWide && !kPool2 && !kWideP2) {
                 put_tile(0, pext0);
                 if constexpr (kNB == 2) {
                     if (!kGnX || a.S == 2) put_tile(1, pext1);
@@ -1642,6 +1701,29 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                                     if (ew + kEpiWarps * (i0 + i) < a.Co) dst[(i0 + i) * cstep + w] = m[i];
                             }
                         }
+                    }
+                }
+            } else if constexpr (kWideP2) {
+                // the unit's one band rb, the two row slots folded, sign and
+                // bias restored; windows lane + 32 hw (up to 127)
+                const int prow = rb;
+                if (prow < a.Hp) {
+                    const float *pt0 = scratch, *pt1 = scratch + 64 * kPitch;
+                    float *dst = a.gn.pmax + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
+                    const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+#pragma unroll
+                    for (int hw = 0; hw < 4; ++hw) {
+                        const int w = lane + 32 * hw;
+                        if (w >= a.Wp) continue;
+                        float m[64 / kEpiWarps];
+#pragma unroll
+                        for (int i = 0; i < 64 / kEpiWarps; ++i) {
+                            const int c2 = ew + kEpiWarps * i;
+                            m[i] = fmaf(gn_sgn[c2], fmaxf(pt0[c2 * kPitch + w], pt1[c2 * kPitch + w]), gn_bias[c2]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 64 / kEpiWarps; ++i)
+                            if (ew + kEpiWarps * i < a.Co) dst[i * cstep + w] = m[i];
                     }
                 }
             } else if constexpr (kWide) {
@@ -2038,7 +2120,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         tmem_dealloc(*tmem_slot, kTmemCols);
     }
     if constexpr (is_gn(KIND)) {
-        if (a.gn_fin) gn_finalize_tail<is_gnx(KIND), KIND != kKindGnPool2S1>(a, smem, abort_flag);
+        if (a.gn_fin) gn_finalize_tail<is_gnx(KIND), KIND != kKindGnPool2S1 && KIND != kKindGnWideP2>(a, smem, abort_flag);
     }
 }
 
@@ -2135,6 +2217,8 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
         return (uint32_t)(kEpiWarps * 32 * 16 * sizeof(float));  // a 32 x 16 staging tile per warp
     case CONV_EPI_GN_SCALE_POOL_CLAMP:  // U / 2 bands of pooled tiles, the statistics, the sign and bias tables
         return (uint32_t)(((U / 2) * 2 * 64 * kPoolPitch + 2 * kEpiThreads + 2 * 64) * sizeof(float));
+    case kKindGnWideP2:  // one band region of pitch 129, the statistics, the tables
+        return (uint32_t)((2 * 64 * 129 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnWide:  // one band region of pitch 65, the statistics, the tables
     case kKindGnColTiles:
         return (uint32_t)((2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
@@ -2362,16 +2446,19 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // each unit one row pair of one tile (rows of 127 outputs: one tile)
     const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.P > 128;
     const int cpg = d.Cout / e.groups;
+    // 2 x 2 windows on rows of 130..240 columns (Cout <= 64): a row pair, one band, per unit (the plan
+    // above fails for wider rows: shared memory)
+    const bool wide_p2 = kind == kKindGnWideP2 && pl.S == 2 && pl.U == 1 && pl.CT == 1 && pl.P > 128 && d.W - 2 >= 128;
     const bool shape =
         e.pool_k == 4 ? (one_band || two_bands || one_band_s1 || half_band || wide_rows || col_tiles)
-                      : e.pool_k == 2 && pool2;
+                      : e.pool_k == 2 && (pool2 || wide_p2);
     return shape && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
 
 // a fused GroupNorm unit of 2 rows holds half a 4-row band (its pooled
 // extremes in two workspace slots, folded by the finalize); 2 x 2 windows
 // make such a unit a whole band
-bool tc_gn_half(const Plan &pl, int kind) { return pl.RU == 2 && kind != kKindGnPool2S1; }
+bool tc_gn_half(const Plan &pl, int kind) { return pl.RU == 2 && kind != kKindGnPool2S1 && kind != kKindGnWideP2; }
 
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
     Plan pl;
@@ -2574,6 +2661,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
         // (a unit's windows: up to 32 or, for the two-pass rows, 64; column tiles any number)
         const int max_wp = kkind == kKindGnColTiles                                                  ? a.Wp
+                           : kkind == kKindGnWideP2                                                   ? 128
                            : kkind == kKindGnWide || kkind == kKindGnPool2 || kkind == kKindGnPool2S1 ? 64
                                                                                                       : 32;
         if (h->gn.units != a.units_per_img || a.Wp > max_wp) return CONV_EPI_ERR_INVALID_ARG;
@@ -2616,6 +2704,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
                    : kkind == kKindGnWide    ? launch_tc<kKindGnWide>(args, pl, grid, s)
                    : kkind == kKindGnPool2   ? launch_tc<kKindGnPool2>(args, pl, grid, s)
                    : kkind == kKindGnPool2S1 ? launch_tc<kKindGnPool2S1>(args, pl, grid, s)
+                   : kkind == kKindGnWideP2  ? launch_tc<kKindGnWideP2>(args, pl, grid, s)
                    : kkind == kKindGnTiles   ? launch_tc<kKindGnTiles>(args, pl, grid, s)
                    : kkind == kKindGnColTiles ? launch_tc<kKindGnColTiles>(args, pl, grid, s)
                                              : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
