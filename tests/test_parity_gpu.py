@@ -89,7 +89,7 @@ SMALL = {
     "c5_k2_co80_w30": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=30, Cout=80, groups=5, pool_k=2),     # 48 zero filters, 16 per group
     "c5_k2_w200": W["c5_gn_pool_clamp"].resized(N=1, H=11, W=200, pool_k=2),                  # rows of 198 outputs, 99 windows
     "c5_k2_w240": W["c5_gn_pool_clamp"].resized(N=2, H=8, W=240, Cout=32, groups=8, pool_k=2),  # 119 windows
-    "c5_k2_w256": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=256, Cout=32, groups=8, pool_k=2),  # 127 windows: two passes
+    "c5_k2_w256": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=256, Cout=32, groups=8, pool_k=2),  # NCHW two passes; channels last fused, 127 windows
     "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling
     "c5_k2_w300": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=300, pool_k=2, groups=64),  # 2 column tiles, a group per channel
     # 2 x 2 windows fused (Cout <= 64, W 66..128: two bands of 2 rows per unit)
