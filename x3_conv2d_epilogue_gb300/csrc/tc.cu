@@ -91,8 +91,9 @@ constexpr int kKindGnXNarrow = 8;
 // half a band, per unit, its up to 63 windows in two passes of 4 chunks per
 // warp (the second masked).
 constexpr int kKindGnWide = 9;
-// ... and 2 x 2 pooling windows (Cout <= 64, rows of 64..126 outputs): each
-// of a unit's two row pairs is a pooling band, 8 windows per 16-column chunk.
+// ... and 2 x 2 pooling windows (Cout <= 64, rows of 64..126 outputs, or of
+// up to 62 in the four-u instantiation): each of a unit's row pairs is a
+// pooling band, 8 windows per 16-column chunk.
 constexpr int kKindGnPool2 = 10;
 // ... and more than 128 channels (rows of up to 64 or of 64..126 outputs):
 // channel tiles of 128, each unit one tile's band or half band (with the
@@ -104,9 +105,10 @@ constexpr int kKindGnTiles = 11;
 // 130..256-column kind but with each unit's column masks and window offset
 // (also rows of 127 outputs, whose first pass needs the mask).
 constexpr int kKindGnColTiles = 12;
-// ... and 2 x 2 windows over 65..128 channels (rows of 64..126 outputs): no
-// row stacking, a unit's two rows the one band (compiled into the kind of
-// 2 x 2 windows above, the stacking checks cost its shapes 8 %).
+// ... and 2 x 2 windows over 65..128 channels (rows of 64..126 outputs, or
+// of up to 62 with four u): no row stacking, each pair of a unit's 1-row u
+// one band (compiled into the kind of 2 x 2 windows above, the stacking
+// checks cost its shapes 8 %).
 constexpr int kKindGnPool2S1 = 13;
 // ... and 2 x 2 windows on rows of 130..240 columns (Cout <= 64): one row
 // pair, one band, per unit, its up to 119 windows gathered in two passes of
@@ -120,10 +122,10 @@ __host__ __device__ constexpr bool is_gnx(int kind) {
 }
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
-// 96..126 outputs), or the generalised one
+// 96..126 outputs), or one of the generalised instantiations (tc_gn_fused decides whether it runs)
 inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W <= 128 && d.W != 65) return kKindGnPool2;
-    if (pool_k == 2 && d.Cout <= 64 && d.W >= 130 && d.W <= 256) return kKindGnWideP2;  // (fused up to 240: below)
+    if (pool_k == 2 && d.Cout <= 64 && d.W >= 130 && d.W <= 256) return kKindGnWideP2;  // (where its plan fits)
     if (pool_k == 2 && d.Cout <= 128 && d.W <= 128 && d.W != 65) return kKindGnPool2S1;
     if (d.Cout > 128) return kKindGnTiles;
     // (rows of 127 outputs too: one tile, its first pass masked)
