@@ -160,7 +160,7 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *     W <= 64 or W >= 66 (wider than 256 as column tiles of 252 outputs), or
  *     with Cout > 64 and
  *     W <= 64 or 66 <= W <= 128 (more than 128 channels as channel tiles of
- *     128), or
+ *     128), or with 64 < Cout <= 128 and 130 <= W <= 256, or
  *     pool_k = 2 with Cout <= 128 and W <= 128 (not 65), or Cout <= 64 and
  *     130 <= W <= 256 where its pooled tile fits the shared memory beside
  *     the smallest rings (NCHW with Cin <= 8: W <= 240; channels last: up

@@ -157,6 +157,7 @@ GN_WIDE = {
     "c5_pool2_co128": synth.WORKLOADS["c5_gn_pool_clamp"].resized(Cout=128, groups=16, pool_k=2),  # 2x2, no stacking
     "c5_pool2_w64": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=256, H=64, W=64, pool_k=2),      # 2x2, four bands per unit
     "c5_pool2_w240": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=32, H=240, W=240, pool_k=2),    # 2x2, rows of 238
+    "c5_co128_w256": synth.WORKLOADS["c5_gn_pool_clamp"].resized(N=32, H=256, W=256, Cout=128, groups=16),  # quarter bands
 }
 
 

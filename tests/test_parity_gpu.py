@@ -104,6 +104,9 @@ SMALL = {
     "c5_co128_w64": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=64, Cout=128, groups=16),  # a stats-only unit
     "c5_co96_w40": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=40, Cout=96, groups=12),   # 32 zero filters, 9 windows
     "c5_co320_w50": W["c5_gn_pool_clamp"].resized(N=2, H=11, W=50, Cout=320, groups=10),  # 3 tiles, the last 64 channels, 32 per group
+    # 65..128 channels on rows of 130..256 columns: a unit of one row, a quarter band
+    "c5_co128_w200": W["c5_gn_pool_clamp"].resized(N=1, H=13, W=200, Cout=128, groups=16),  # stats-only rows
+    "c5_co96_w256": W["c5_gn_pool_clamp"].resized(N=2, H=9, W=256, Cout=96, groups=12),     # 32 zero filters, 63 windows
     # rows wider than 256 fused (Cout <= 64): column tiles of 252 outputs
     "c5_w300": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=300),                   # last tile 46 columns: both passes masked
     "c5_w510": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=510, Cout=32, groups=8),  # 3 tiles, the last one window, a stats-only row

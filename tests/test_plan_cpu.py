@@ -133,7 +133,8 @@ def check_plan(q, N, Cin, H, W, Cout, kind, layout, pool_k=4):
         bands = U // 2
         assert (S == 2 and U in (2, 4) and P <= 128 and (P == 64 or W - 2 >= 64)) or \
             (S == 1 and U == 2 and 64 < P <= 128 and W - 2 >= 64) or (S == 1 and U == 4 and P == 64) or \
-            (S == 2 and U == 1 and 128 < P <= 256 and W - 2 >= 127)  # (127: one column tile, both passes masked)
+            (S == 2 and U == 1 and 128 < P <= 256 and W - 2 >= 127) or \
+            (S == 1 and U == 1 and 128 < P <= 256 and W - 2 >= 128)  # (127: one column tile, both passes masked)
         if pool_k == 2:
             # 2 x 2 windows: two band regions of pitch 65 (up to 63 windows),
             # the statistics, 128-channel tables; the tile writes reach
@@ -230,7 +231,9 @@ def gn_fused(kind, Cout, W, pool_k, groups, nhwc=False, Cin=8):
     # rows: the same per column tile of 252 outputs
     # more than 64 channels: no row stacking, half a band per unit (more than
     # 128: channel tiles of 128, a unit per tile)
-    return (Cout <= 64 and (W <= 64 or W >= 66)) or (Cout > 64 and (W <= 64 or 66 <= W <= 128))
+    # (65..128 channels on rows of 130..256 columns: a quarter band per unit)
+    return ((Cout <= 64 and (W <= 64 or W >= 66)) or (Cout > 64 and (W <= 64 or 66 <= W <= 128)) or
+            (64 < Cout <= 128 and 130 <= W <= 256))
 
 
 def check_gn_form(q, N, Cin, H, W, Cout, kind, layout, pool_k, groups):
@@ -256,7 +259,7 @@ def test_random_shapes_all_planned_and_in_range():
     and every plan passes the range checks; GroupNorm shapes are fused
     exactly when groups have a power-of-two size up to 64 and either
     pool_k = 4 with Cout <= 64 and W != 65, or Cout > 64 with W <= 64 or
-    66 <= W <= 128, or pool_k = 2 with
+    66 <= W <= 128, or 64 < Cout <= 128 with 130 <= W <= 256, or pool_k = 2 with
     Cout <= 128 and W <= 128 (not 65) or Cout <= 64 and 130 <= W <= 256
     where the plan fits shared memory;
     otherwise they are planned as the plain
@@ -291,7 +294,7 @@ def test_plan_query_arguments():
         ce._check(ce._lib().conv_epi_plan_query(ce.C.byref(d), ce.C.byref(epi_for(ce.MIN_TANH2)),
                                                 ce.C.byref(q)), "plan")
     assert ce.STATUS[ei.value.status] == "UNSUPPORTED"
-    for bad_kind in (6, 7, 8, 9, 10, 11, 12, 13, 14, -1):  # bad chain (the kernel's internal kinds included)
+    for bad_kind in (6, 7, 8, 9, 10, 11, 12, 13, 14, 15, -1):  # bad chain (the kernel's internal kinds included)
         with pytest.raises(ce.ConvEpiError) as ei:
             plan(1, 8, 8, 8, 64, bad_kind)
         assert ce.STATUS[ei.value.status] == "INVALID_ARG"

@@ -34,7 +34,8 @@ struct GnArgs {
     float *out;
     int32_t *idx;
     int presel;      // 1: pmax already holds the extreme the slope's sign selects
-    int half;        // with presel: pmax and pmin hold it for the two halves of each band
+    int nsl;         // with presel: the slots holding it for the parts of each band (1; 2: halves in pmax, pmin;
+                     // 4: quarters in pmax, pmin and the index buffers, which the tensor-core path leaves free)
     double inv_cnt;  // 1 / (C/groups * Ho * Wo)
     float cnt;       // C/groups * Ho * Wo
     uint32_t per_magic;  // ceil(2^32 / (Hp * Wp)): exact f / (Hp * Wp) for f < 2^16
@@ -66,17 +67,22 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
     const uint32_t per = (uint32_t)(a.gn.Hp * a.gn.Wp);
     const size_t base = ((size_t)n * a.C + (size_t)g * cpg) * per;
     const float4 *__restrict__ src = reinterpret_cast<const float4 *>(a.gn.pmax + base);
-    const float4 *__restrict__ src2 = reinterpret_cast<const float4 *>(a.gn.pmin + base);  // (half bands)
+    // (bands in parts: the other slots)
+    const float4 *__restrict__ src2 = reinterpret_cast<const float4 *>(a.gn.pmin + base);
+    const float4 *__restrict__ src3 = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(a.gn.amax) + base);
+    const float4 *__restrict__ src4 = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(a.gn.amin) + base);
     float4 *__restrict__ dst = reinterpret_cast<float4 *>(a.out + base);
     const int nv = (int)((size_t)cpg * per / 4);
-    float4 v[kVec], w[kVec];
+    float4 v[kVec], w[kVec], w3[kVec], w4[kVec];
+    auto load = [&](int k, int i) {
+        v[k] = src[i];
+        if (a.nsl > 1) w[k] = src2[i];
+        if (a.nsl > 2) w3[k] = src3[i], w4[k] = src4[i];
+    };
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
         const int i = threadIdx.x + k * kThreads;
-        if (i < nv) {
-            v[k] = src[i];
-            if (a.half) w[k] = src2[i];
-        }
+        if (i < nv) load(k, i);
     }
     if (threadIdx.x < 32) {
         // the channel parameters (at most two channels per lane) are loaded
@@ -99,10 +105,14 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
         }
     }
     __syncthreads();
-    // (half bands: the band's extreme from its halves, by the slope's sign)
-    auto apply = [&](float y, float y2, uint32_t f) {
+    // (bands in parts: the band's extreme from its parts, by the slope's sign)
+    auto apply = [&](float y, float y2, float y3, float y4, uint32_t f) {
         const uint32_t cl = __umulhi(f, a.per_magic);  // f / per
-        if (a.half) y = sA[cl] >= 0.0f ? fmaxf(y, y2) : fminf(y, y2);
+        if (a.nsl > 1) {
+            const bool up = sA[cl] >= 0.0f;
+            y = up ? fmaxf(y, y2) : fminf(y, y2);
+            if (a.nsl > 2) y = up ? fmaxf(y, fmaxf(y3, y4)) : fminf(y, fminf(y3, y4));
+        }
         return fminf(fmaxf(fmaf(sA[cl], y, sB[cl]), a.lo), a.hi);
     };
     for (int i0 = 0; i0 < nv; i0 += kVec * kThreads) {
@@ -110,10 +120,7 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
 #pragma unroll
             for (int k = 0; k < kVec; ++k) {
                 const int i = i0 + threadIdx.x + k * kThreads;
-                if (i < nv) {
-                    v[k] = src[i];
-                    if (a.half) w[k] = src2[i];
-                }
+                if (i < nv) load(k, i);
             }
         }
 #pragma unroll
@@ -121,8 +128,9 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_vec_kernel(const GnArgs 
             const int i = i0 + threadIdx.x + k * kThreads;
             if (i < nv) {
                 const uint32_t f = 4u * (uint32_t)i;
-                dst[i] = make_float4(apply(v[k].x, w[k].x, f), apply(v[k].y, w[k].y, f + 1), apply(v[k].z, w[k].z, f + 2),
-                                     apply(v[k].w, w[k].w, f + 3));
+                dst[i] = make_float4(apply(v[k].x, w[k].x, w3[k].x, w4[k].x, f), apply(v[k].y, w[k].y, w3[k].y, w4[k].y, f + 1),
+                                     apply(v[k].z, w[k].z, w3[k].z, w4[k].z, f + 2),
+                                     apply(v[k].w, w[k].w, w3[k].w, w4[k].w, f + 3));
             }
         }
     }
@@ -164,7 +172,10 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
             const float A = sA[cl], B = sB[cl];
             const size_t base = ((size_t)n * a.C + c) * per;
             const float *__restrict__ src = ((a.presel || A >= 0.0f) ? a.gn.pmax : a.gn.pmin) + base;
-            const float *__restrict__ src2 = a.gn.pmin + base;  // (half bands: the second half)
+            // (bands in parts: the other slots)
+            const float *__restrict__ src2 = a.gn.pmin + base;
+            const float *__restrict__ src3 = reinterpret_cast<const float *>(a.gn.amax) + base;
+            const float *__restrict__ src4 = reinterpret_cast<const float *>(a.gn.amin) + base;
             float *__restrict__ dst = a.out + base;
             if (a.idx) {
                 const int32_t *__restrict__ isrc = (A > 0.0f ? a.gn.amax : a.gn.amin) + base;
@@ -173,11 +184,14 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
                     a.idx[base + p] = A != 0.0f ? isrc[p] : 0;
                 }
             } else {
-                // four independent loads in flight per thread (half bands:
-                // each the extreme of the band's two halves by the slope's sign)
+                // four independent loads in flight per thread (bands in
+                // parts: each the extreme of the band's parts by the slope's sign)
                 auto y_at = [&](int q) {
-                    const float y = src[q];
-                    return a.half ? (A >= 0.0f ? fmaxf(y, src2[q]) : fminf(y, src2[q])) : y;
+                    float y = src[q];
+                    if (a.nsl > 1) y = A >= 0.0f ? fmaxf(y, src2[q]) : fminf(y, src2[q]);
+                    if (a.nsl > 2)
+                        y = A >= 0.0f ? fmaxf(y, fmaxf(src3[q], src4[q])) : fminf(y, fminf(src3[q], src4[q]));
+                    return y;
                 };
                 int p = threadIdx.x;
                 for (; p + 3 * kThreads < per; p += 4 * kThreads) {
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) gn_finalize_kernel(const GnArgs a) {
 }  // namespace
 
 conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, float *out, cudaStream_t s,
-                            bool presel, bool half) {
+                            bool presel, int nslots) {
     GnArgs a;
     a.gn = h->gn;
     a.N = h->d.N, a.C = h->d.Cout, a.Ho = h->Ho, a.Wo = h->Wo, a.groups = e.groups;
@@ -204,7 +218,7 @@ conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, 
     a.gamma = e.gamma, a.beta = e.beta, a.scale = e.chan_scale;
     a.out = out, a.idx = e.index_out;
     a.presel = presel ? 1 : 0;
-    a.half = presel && half ? 1 : 0;
+    a.nsl = presel ? nslots : 1;
     a.inv_cnt = 1.0 / ((double)(a.C / a.groups) * a.Ho * a.Wo);
     a.cnt = (float)((double)(a.C / a.groups) * a.Ho * a.Wo);
     const uint32_t per = (uint32_t)(h->gn.Hp * h->gn.Wp);

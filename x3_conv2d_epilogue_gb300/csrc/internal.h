@@ -150,9 +150,10 @@ conv_epi_status postpass_forward(conv_epi_handle h, const float *y, const conv_e
 // GroupNorm finalize (gn.cu): pooled max/min + statistics -> output.
 // presel: the conv path left in pmax, per channel, the window extreme that the
 // sign of gamma * scale selects (max when it is >= 0, else min), and no pmin;
-// half: with presel, pmax and pmin hold that extreme of each half of a band
-// (its two row pairs), to be folded the same way.
+// nslots: with presel, 1, or 2 (pmax and pmin hold that extreme of each half
+// of a band, its two row pairs) or 4 (pmax, pmin and the index buffers hold
+// it for each quarter, one row each), to be folded the same way.
 conv_epi_status gn_finalize(conv_epi_handle h, const conv_epi_epilogue_desc &e, float *out,
-                            cudaStream_t s, bool presel, bool half = false);
+                            cudaStream_t s, bool presel, int nslots = 1);
 
 }  // namespace conv_epi

@@ -116,9 +116,15 @@ constexpr int kKindGnPool2S1 = 13;
 // rows of 256 staged columns the two-slot tile and the minimal rings exceed
 // shared memory).
 constexpr int kKindGnWideP2 = 14;
+// ... and 65..128 channels on rows of 130..256 columns: no row stacking, so
+// a unit is one row, a quarter of a 4-row band; its extremes go to one of
+// four workspace slots (pmax, pmin and the index buffers, which this path
+// leaves free), folded by the finalize.
+constexpr int kKindGnWideS1 = 15;
 __host__ __device__ constexpr bool is_gnx(int kind) {
     return kind == kKindGnX || kind == kKindGnXNarrow || kind == kKindGnWide || kind == kKindGnPool2 ||
-           kind == kKindGnTiles || kind == kKindGnColTiles || kind == kKindGnPool2S1 || kind == kKindGnWideP2;
+           kind == kKindGnTiles || kind == kKindGnColTiles || kind == kKindGnPool2S1 || kind == kKindGnWideP2 ||
+           kind == kKindGnWideS1;
 }
 __host__ __device__ constexpr bool is_gn(int kind) { return kind == CONV_EPI_GN_SCALE_POOL_CLAMP || is_gnx(kind); }
 // the fused GroupNorm kernel for a problem: the page's 64 stacked channels (rows of up to 64 or of
@@ -127,6 +133,7 @@ inline int tc_gn_kind(const conv_epi_desc &d, int pool_k) {
     if (pool_k == 2 && d.Cout <= 64 && d.W <= 128 && d.W != 65) return kKindGnPool2;
     if (pool_k == 2 && d.Cout <= 64 && d.W >= 130 && d.W <= 256) return kKindGnWideP2;  // (where its plan fits)
     if (pool_k == 2 && d.Cout <= 128 && d.W <= 128 && d.W != 65) return kKindGnPool2S1;
+    if (d.Cout > 64 && d.Cout <= 128 && d.W >= 130 && d.W <= 256) return kKindGnWideS1;
     if (d.Cout > 128) return kKindGnTiles;
     // (rows of 127 outputs too: one tile, its first pass masked)
     if ((d.W > 256 || d.W == 129) && d.Cout <= 64) return kKindGnColTiles;
@@ -1041,7 +1048,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
     constexpr bool kMin = KIND == CONV_EPI_MIN_TANH2 || KIND == CONV_EPI_SCALE_MIN;
     constexpr bool kGnX = is_gnx(KIND);  // the generalised GroupNorm chain
     // rows of 130..256 columns, or column tiles of wider rows: two passes per unit
-    constexpr bool kWide = KIND == kKindGnWide || KIND == kKindGnColTiles;
+    constexpr bool kWide = KIND == kKindGnWide || KIND == kKindGnColTiles || KIND == kKindGnWideS1;
+    constexpr bool kWideS1 = KIND == kKindGnWideS1;  // ... one row (a quarter band) per unit
     constexpr bool kColT = KIND == kKindGnColTiles;
     constexpr bool kPool2 = KIND == kKindGnPool2 || KIND == kKindGnPool2S1;  // 2 x 2 windows: a band per u
     constexpr bool kP2S1 = KIND == kKindGnPool2S1;  // ... without row stacking: a band per unit
@@ -1360,7 +1368,8 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                     }
                 };
                 auto put_w = [&](int pass) {
-                    float *pt = scratch + slot * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch;
+                    // (no stacking: channel row L of a 128-channel tile)
+                    float *pt = scratch + (kWideS1 ? L * kPitch : slot * 64 * kPitch + ((qd & 1) * 32 + lane) * kPitch);
 #pragma unroll
                     for (int k = 0; k < kWin; ++k) {
                         const int pw = (hc + 8 * pass + 2 * (k / 4)) * 4 + (k % 4);
@@ -1728,6 +1737,35 @@ __device__ __forceinline__ void epilogue_role(const Cfg &a, float *scratch, cons
                             if (ew + kEpiWarps * i < a.Co) dst[i * cstep + w] = m[i];
                     }
                 }
+            } else if constexpr (kWideS1) {
+                // quarter rb & 3 of band rb / 4 (sign and bias restored) into
+                // slot rb & 3; windows lane and lane + 32, channels ew + 8 i
+                const int prow = rb >> 2, q = rb & 3;
+                if (prow < a.Hp) {
+                    float *slot_base = q == 0   ? a.gn.pmax
+                                       : q == 1 ? a.gn.pmin
+                                       : q == 2 ? reinterpret_cast<float *>(a.gn.amax)
+                                                : reinterpret_cast<float *>(a.gn.amin);
+                    float *dst = slot_base + (((size_t)n * a.Co + ew) * a.Hp + prow) * a.Wp;
+                    const size_t cstep = (size_t)kEpiWarps * a.Hp * a.Wp;
+#pragma unroll
+                    for (int hw = 0; hw < 2; ++hw) {
+                        const int w = lane + 32 * hw;
+                        if (w >= a.Wp) continue;
+#pragma unroll
+                        for (int i0 = 0; i0 < 128 / kEpiWarps; i0 += 8) {
+                            float m[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int c2 = ew + kEpiWarps * (i0 + i);
+                                m[i] = fmaf(gn_sgn[c2], scratch[c2 * kPitch + w], gn_bias[c2]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                if (ew + kEpiWarps * (i0 + i) < a.Co) dst[(i0 + i) * cstep + w] = m[i];
+                        }
+                    }
+                }
             } else if constexpr (kWide) {
                 // half band rb / 2, two row slots folded, sign and bias
                 // restored, into slot rb & 1; windows lane and lane + 32 (of
@@ -1855,9 +1893,11 @@ constexpr uint32_t kFinFlagOff = kFinPairs * 64 * 2 * 4;  // after the coefficie
 constexpr uint32_t kFinBarOff = kFinFlagOff + 8;         // an mbarrier per batch (or per ring slot)
 constexpr uint32_t kFinBufOff = 8448;                     // the pooled blocks (128-byte aligned)
 static_assert(kFinBarOff + 8u * kFinPairs <= kFinBufOff, "finalize barriers overlap the pooled blocks");
-// kHalf: a unit of 2 rows holds half a 4-row band (65..128 channels, or
-// rows of 127 or more columns), so each pooled block comes in two slots
-template <bool kGnX, bool kHalf>
+// kSl: the parts a band's pooled blocks may come in: 2 where a unit of 2
+// rows holds half a 4-row band (65..128 channels, or rows of 127 or more
+// columns), 4 where a unit of 1 row holds a quarter (65..128 channels on
+// rows of 130..256 columns), else 1
+template <bool kGnX, int kSl>
 __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, volatile int *abort_flag) {
     float *sA = reinterpret_cast<float *>(smem), *sB = sA + kFinPairs * 64;
     int &s_go = *reinterpret_cast<int *>(smem + kFinFlagOff);
@@ -1897,7 +1937,14 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
     const int npairs = a.N * a.groups;
     // (with half bands, a pair's two slots side by side: [pair][slot][F4])
     // (a unit of 2 rows holds half a band: 65..128 channels, or rows of 130..256 columns)
-    const uint32_t nsl = kGnX && kHalf && a.RU == 2 ? 2u : 1u, sbytes = nsl * pbytes;
+    const uint32_t nsl = kSl == 4 ? 4u : kGnX && kSl == 2 && a.RU == 2 ? 2u : 1u, sbytes = nsl * pbytes;
+    // slot h of a pair's pooled block: pmax, pmin and the index buffers
+    auto slot_src = [&](uint32_t h) -> const char * {
+        return reinterpret_cast<const char *>(h == 0   ? a.gn.pmax
+                                              : h == 1 ? a.gn.pmin
+                                              : h == 2 ? reinterpret_cast<const float *>(a.gn.amax)
+                                                       : reinterpret_cast<const float *>(a.gn.amin));
+    };
     if constexpr (kGnX) {
         // this CTA's pairs p = blockIdx.x + k * gridDim.x (k < K) through a ring
         // of cap slots: pair k lands in slot k % cap, and the copy of pair
@@ -1909,7 +1956,7 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
             const size_t p = (size_t)blockIdx.x + (size_t)k * gridDim.x;
             mbar_arrive_expect_tx(fbar + 8u * (uint32_t)sl, sbytes);
             for (uint32_t h = 0; h < nsl; ++h) {
-                const char *src = reinterpret_cast<const char *>(h ? a.gn.pmin : a.gn.pmax) + p * pbytes;
+                const char *src = slot_src(h) + p * pbytes;
                 const uint32_t dsm = smem_u32(buf) + (uint32_t)sl * sbytes + h * pbytes;
                 for (uint32_t off = 0; off < pbytes; off += 16384u)
                     bulk_g2s(dsm + off, src + off, min(16384u, pbytes - off), fbar + 8u * (uint32_t)sl);
@@ -1951,18 +1998,18 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
                 float4 *bp = bp0 + t;
                 const float4 v = bp[0];
                 float r[4] = {v.x, v.y, v.z, v.w};
-                if (nsl == 2) {
-                    // the band's extreme from its two halves: the larger y where
+                for (uint32_t h = 1; h < nsl; ++h) {
+                    // the band's extreme from its parts: the larger y where
                     // the slope A is >= 0, else the smaller
-                    const float4 w = bp[F4];
+                    const float4 w = bp[h * F4];
                     const float h2[4] = {w.x, w.y, w.z, w.w};
-    #pragma unroll
+#pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint32_t cl = __umulhi(e + q, a.per_magic);
                         r[q] = cA[cl] >= 0.0f ? fmaxf(r[q], h2[q]) : fminf(r[q], h2[q]);
                     }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
                     r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
@@ -2024,13 +2071,13 @@ __device__ __forceinline__ void gn_finalize_tail(const Cfg &a, uint8_t *smem, vo
                     // the slope A is >= 0, else the smaller
                     const float4 w = bp[F4];
                     const float h2[4] = {w.x, w.y, w.z, w.w};
-    #pragma unroll
+#pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint32_t cl = __umulhi(e + q, a.per_magic);
                         r[q] = cA[cl] >= 0.0f ? fmaxf(r[q], h2[q]) : fminf(r[q], h2[q]);
                     }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t cl = __umulhi(e + q, a.per_magic);  // channel within the group
                     r[q] = fminf(fmaxf(fmaf(cA[cl], r[q], cB[cl]), a.lo), a.hi);
@@ -2122,7 +2169,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_conv_epi(const __grid_constant
         tmem_dealloc(*tmem_slot, kTmemCols);
     }
     if constexpr (is_gn(KIND)) {
-        if (a.gn_fin) gn_finalize_tail<is_gnx(KIND), KIND != kKindGnPool2S1 && KIND != kKindGnWideP2>(a, smem, abort_flag);
+        if (a.gn_fin)
+            gn_finalize_tail<is_gnx(KIND), KIND == kKindGnWideS1 ? 4 : KIND != kKindGnPool2S1 && KIND != kKindGnWideP2 ? 2 : 1>(
+                a, smem, abort_flag);
     }
 }
 
@@ -2223,6 +2272,7 @@ uint32_t scratch_bytes_for(int kind, int U, int P) {
         return (uint32_t)((2 * 64 * 129 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnWide:  // one band region of pitch 65, the statistics, the tables
     case kKindGnColTiles:
+    case kKindGnWideS1:
         return (uint32_t)((2 * 64 * 65 + 2 * kEpiThreads + 2 * 128) * sizeof(float));
     case kKindGnPool2:  // two band regions of pitch 65 (rows of up to 64 columns: four of pitch 33), the
     case kKindGnPool2S1:  // statistics, the tables
@@ -2448,19 +2498,24 @@ bool tc_gn_fused(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     // each unit one row pair of one tile (rows of 127 outputs: one tile)
     const bool col_tiles = kind == kKindGnColTiles && pl.S == 2 && pl.U == 1 && pl.P > 128;
     const int cpg = d.Cout / e.groups;
+    // 65..128 channels on rows of 130..256 columns: one row, a quarter band, per unit
+    const bool wide_s1 = kind == kKindGnWideS1 && pl.S == 1 && pl.U == 1 && pl.CT == 1 && pl.P > 128 && d.W - 2 >= 128;
     // 2 x 2 windows on rows of 130..240 columns (Cout <= 64): a row pair, one band, per unit (the plan
     // above fails for wider rows: shared memory)
     const bool wide_p2 = kind == kKindGnWideP2 && pl.S == 2 && pl.U == 1 && pl.CT == 1 && pl.P > 128 && d.W - 2 >= 128;
     const bool shape =
-        e.pool_k == 4 ? (one_band || two_bands || one_band_s1 || half_band || wide_rows || col_tiles)
+        e.pool_k == 4 ? (one_band || two_bands || one_band_s1 || half_band || wide_rows || wide_s1 || col_tiles)
                       : e.pool_k == 2 && (pool2 || wide_p2);
     return shape && (cpg & (cpg - 1)) == 0 && cpg <= 64;
 }
 
-// a fused GroupNorm unit of 2 rows holds half a 4-row band (its pooled
-// extremes in two workspace slots, folded by the finalize); 2 x 2 windows
-// make such a unit a whole band
-bool tc_gn_half(const Plan &pl, int kind) { return pl.RU == 2 && kind != kKindGnPool2S1 && kind != kKindGnWideP2; }
+// the workspace slots of a fused GroupNorm band's pooled extremes, folded by
+// the finalize: a unit of 2 rows holds half a 4-row band (2; 2 x 2 windows
+// make such a unit a whole band), a unit of 1 row a quarter (4)
+int tc_gn_slots(const Plan &pl, int kind) {
+    if (kind == kKindGnWideS1) return 4;  // a unit of 1 row: a quarter band
+    return pl.RU == 2 && kind != kKindGnPool2S1 && kind != kKindGnWideP2 ? 2 : 1;
+}
 
 conv_epi_status tc_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
     Plan pl;
@@ -2664,7 +2719,9 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         // (a unit's windows: up to 32 or, for the two-pass rows, 64; column tiles any number)
         const int max_wp = kkind == kKindGnColTiles                                                  ? a.Wp
                            : kkind == kKindGnWideP2                                                   ? 128
-                           : kkind == kKindGnWide || kkind == kKindGnPool2 || kkind == kKindGnPool2S1 ? 64
+                           : kkind == kKindGnWide || kkind == kKindGnWideS1 || kkind == kKindGnPool2 ||
+                                     kkind == kKindGnPool2S1
+                               ? 64
                                                                                                       : 32;
         if (h->gn.units != a.units_per_img || a.Wp > max_wp) return CONV_EPI_ERR_INVALID_ARG;
         // finalize inside the kernel when each (image, group) block of pooled
@@ -2674,7 +2731,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
         const uint32_t per = (uint32_t)(a.Hp * a.Wp), F = (uint32_t)(d.Cout / e.groups) * per;
         a.gn_fin = (F % 4 == 0 && F <= 65536u && d.Cout / e.groups <= 64 && h->coop &&
                     // one pair's blocks (two slots each for half bands) fit the buffer
-                    F * 4u * (tc_gn_half(pl, kkind) ? 2u : 1u) <= pl.bar_off - kFinBufOff &&
+                    F * 4u * (uint32_t)tc_gn_slots(pl, kkind) <= pl.bar_off - kFinBufOff &&
                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(h->gn.pmax) & 15u) == 0)
                        ? 1 : 0;
         a.beta = e.beta, a.eps = e.eps, a.lo = e.clamp_lo, a.hi = e.clamp_hi;
@@ -2707,6 +2764,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
                    : kkind == kKindGnPool2   ? launch_tc<kKindGnPool2>(args, pl, grid, s)
                    : kkind == kKindGnPool2S1 ? launch_tc<kKindGnPool2S1>(args, pl, grid, s)
                    : kkind == kKindGnWideP2  ? launch_tc<kKindGnWideP2>(args, pl, grid, s)
+                   : kkind == kKindGnWideS1  ? launch_tc<kKindGnWideS1>(args, pl, grid, s)
                    : kkind == kKindGnTiles   ? launch_tc<kKindGnTiles>(args, pl, grid, s)
                    : kkind == kKindGnColTiles ? launch_tc<kKindGnColTiles>(args, pl, grid, s)
                                              : launch_tc<CONV_EPI_GN_SCALE_POOL_CLAMP>(args, pl, grid, s);
@@ -2723,7 +2781,7 @@ conv_epi_status tc_forward(conv_epi_handle h, const float *x, const float *w, co
     if (st) return st;
     h->last_launches = pl.MT + 1 + fills + (padded ? 1 : 0);  // packs, fill, conv, row padding
     if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && !a.gn_fin) {
-        if ((st = gn_finalize(h, e, out, s, true, tc_gn_half(pl, kkind)))) return st;
+        if ((st = gn_finalize(h, e, out, s, true, tc_gn_slots(pl, kkind)))) return st;
         h->last_launches += 1;
     }
     return CONV_EPI_OK;
