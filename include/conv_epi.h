@@ -153,7 +153,11 @@ CONV_EPI_API conv_epi_status conv_epi_output_shape(const conv_epi_desc *desc,
  *
  * Shapes:
  *   CONV_EPI_MODE_FP32: any N, Cin, Cout and H, W >= 3.
- *     GN chain: pool_k 1, 2 or 4, at most 64 groups.
+ *     GN chain: fused into the fp32 kernel for pool_k 1, 2 or 4 and at
+ *     most 64 groups (window indices available); any other pool_k or group
+ *     count runs as two passes, the fp32 conv writing y into a handle-owned
+ *     buffer (conv_epi_reserve or the first GN forward allocates it) and the
+ *     chain's post-pass, without indices (index_out: UNSUPPORTED).
  *   CONV_EPI_MODE_TF32: any N, Cin, Cout and H, W >= 3.
  *     GN chain: fused into the conv kernel for groups of a power-of-two
  *     number of channels up to 64 and either pool_k = 4 with Cout <= 64 and

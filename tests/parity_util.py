@@ -37,6 +37,15 @@ def epilogue_for(wl: synth.Workload, d, index_out=None):
                        clamp_hi=wl.clamp_hi, index_out=index_out)
 
 
+def fp32_indices(wl: synth.Workload) -> bool:
+    """The fp32 mode returns indices for the min chains and for the GroupNorm
+    chain it runs fused (pool_k 1, 2 or 4, at most 64 groups); its two-pass
+    GroupNorm form (any other pool_k or group count) gives none."""
+    if wl.kind == synth.KIND_MUL_LRELU_GELU or wl.kind == synth.KIND_NONE:
+        return False
+    return wl.kind != synth.KIND_GN_SCALE_POOL_CLAMP or (wl.pool_k in (1, 2, 4) and wl.groups <= 64)
+
+
 def gpu_run(wl: synth.Workload, t: synth.Tensors, mode: int, want_index=False, repeats=1, layout=0):
     """Run conv + chain on cuda:0 through the C ABI; returns numpy (out, index).
     layout 1 hands the library x in channels-last order (a transposed copy of

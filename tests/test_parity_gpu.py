@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from parity_util import (check_fp32, check_index, check_tf32, gpu_run, min_index_gap, oracle_run,
+from parity_util import (check_fp32, check_index, check_tf32, fp32_indices, gpu_run, min_index_gap, oracle_run,
                          pool_index_gap)
 
 pytestmark = pytest.mark.gpu
@@ -92,6 +92,9 @@ SMALL = {
     "c5_k2_w256": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=256, Cout=32, groups=8, pool_k=2),  # NCHW two passes; channels last fused, 127 windows
     "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling
     "c5_k2_w300": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=300, pool_k=2, groups=64),  # 2 column tiles, a group per channel
+    # GroupNorm shapes the fp32 kernel does not take (two passes there, no indices; tf32 too for pool_k 3)
+    "c5_k3": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=29, pool_k=3),
+    "c5_co128_g128": W["c5_gn_pool_clamp"].resized(N=1, H=10, W=100, Cout=128, groups=128),  # 128 groups
     # 2 x 2 windows fused (Cout <= 64, W 66..128: two bands of 2 rows per unit)
     "c5_k2_w128": W["c5_gn_pool_clamp"].resized(N=2, H=13, W=128, pool_k=2),        # 63 windows, a stats-only tail row
     "c5_k2_w90": W["c5_gn_pool_clamp"].resized(N=1, H=12, W=90, Cout=32, groups=8, pool_k=2),  # P 96, masked chunks
@@ -137,7 +140,7 @@ def test_small_parity(case, mode):
             gpu_run(wl, t, m)
         assert ce.STATUS[info.value.status] == "UNSUPPORTED"
         return
-    got, idx = gpu_run(wl, t, m, want_index=(mode == "fp32" and wl.kind != synth.KIND_MUL_LRELU_GELU))
+    got, idx = gpu_run(wl, t, m, want_index=(mode == "fp32" and fp32_indices(wl)))
     ref, ref_idx = oracle_run(wl, t)
     if mode == "fp32":
         check_fp32(got, ref, case)

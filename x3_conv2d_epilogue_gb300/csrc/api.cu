@@ -248,7 +248,7 @@ CONV_EPI_API conv_epi_status conv_epi_reserve(conv_epi_handle h, const conv_epi_
     if (epi->kind != CONV_EPI_GN_SCALE_POOL_CLAMP) return CONV_EPI_OK;
     CE_CUDA(cudaSetDevice(h->device));
     if (h->d.mode == CONV_EPI_MODE_TF32) return conv_epi::tc_reserve(h, *epi);
-    return conv_epi::ensure_gn_workspace(h, epi->pool_k, epi->groups, conv_epi::simt_gn_units(h->d, h->Ho, epi->pool_k));
+    return conv_epi::simt_reserve(h, *epi);
 }
 
 CONV_EPI_API conv_epi_status conv_epi_forward(conv_epi_handle h, const float *x, const float *w, const float *b,

@@ -117,6 +117,9 @@ conv_epi_status ensure_gn_workspace(conv_epi_handle h, int pool_k, int groups, i
 
 // fp32 CUDA-core path (simt.cu)
 conv_epi_status simt_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc &e);
+// the fp32 mode's GroupNorm workspace, or (shapes its kernel does not take)
+// the buffer of y and the statistics of the two-pass form
+conv_epi_status simt_reserve(conv_epi_handle h, const conv_epi_epilogue_desc &e);
 int simt_gn_units(const conv_epi_desc &d, int Ho, int pool_k);
 conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
                              const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);

@@ -446,13 +446,34 @@ conv_epi_status launch(const SimtArgs &a, const Layout &L, int grid, cudaStream_
 
 }  // namespace
 
+// The GroupNorm chain runs fused in the fp32 kernel for pool_k 1, 2 or 4 and
+// at most 64 groups (the kernel's pooling windows divide its 4-pixel thread
+// strip; its per-CTA group sums are a 64-entry table); other GroupNorm shapes
+// run as two passes, the fp32 conv into a handle-owned buffer of y and the
+// chain's post-pass, which gives no window indices.
+bool simt_gn_two_pass(const conv_epi_epilogue_desc &e) {
+    return e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP && (!(e.pool_k == 1 || e.pool_k == 2 || e.pool_k == 4) || e.groups > 64);
+}
+
 conv_epi_status simt_supported(const conv_epi_desc &d, const conv_epi_epilogue_desc &e) {
     (void)d;
-    if (e.kind == CONV_EPI_GN_SCALE_POOL_CLAMP) {
-        if (!(e.pool_k == 1 || e.pool_k == 2 || e.pool_k == 4)) return CONV_EPI_ERR_UNSUPPORTED;
-        if (e.groups > 64) return CONV_EPI_ERR_UNSUPPORTED;
-    }
+    if (simt_gn_two_pass(e) && e.index_out) return CONV_EPI_ERR_UNSUPPORTED;  // the post-pass gives no indices
     return CONV_EPI_OK;
+}
+
+conv_epi_status simt_reserve(conv_epi_handle h, const conv_epi_epilogue_desc &e) {
+    if (!simt_gn_two_pass(e)) return ensure_gn_workspace(h, e.pool_k, e.groups, simt_gn_units(h->d, h->Ho, e.pool_k));
+    const size_t need = (size_t)h->d.N * h->d.Cout * h->Ho * h->Wo * sizeof(float);  // y
+    if (need > h->ybuf_bytes) {
+        if (h->ybuf) {
+            CE_CUDA(cudaDeviceSynchronize());
+            CE_CUDA(cudaFree(h->ybuf));
+            h->ybuf = nullptr, h->ybuf_bytes = 0;
+        }
+        CE_CUDA(cudaMalloc(&h->ybuf, need));
+        h->ybuf_bytes = need;
+    }
+    return ensure_post_stats(h, e.groups);
 }
 
 int simt_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
@@ -494,6 +515,18 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
         st = launch<CONV_EPI_NONE, 1>(a, L, d.N * a.units, s);
         break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP: {
+        if (simt_gn_two_pass(e)) {
+            // the conv output into the handle's buffer, then the chain's post-pass
+            if (!h->ybuf || h->ybuf_bytes < (size_t)d.N * d.Cout * h->Ho * h->Wo * sizeof(float))
+                return CONV_EPI_ERR_INVALID_ARG;  // conv_epi_reserve sizes it
+            conv_epi_epilogue_desc plain{};
+            plain.kind = CONV_EPI_NONE;
+            if ((st = simt_forward(h, x, w, b, plain, h->ybuf, s))) return st;
+            const int conv_launches = h->last_launches;
+            if ((st = postpass_forward(h, h->ybuf, e, out, s))) return st;
+            h->last_launches += conv_launches;
+            return CONV_EPI_OK;
+        }
         a.units = simt_gn_units(d, h->Ho, e.pool_k);
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
