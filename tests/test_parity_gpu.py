@@ -296,3 +296,16 @@ def test_channels_last_operands_are_truncated():
     got, _ = gpu_run(wl, t, ce.MODE_TF32, layout=ce.LAYOUT_NHWC)
     want = tf32_trunc(t.x[:, 3:4, 1:-1, 1:-1])
     np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_fp32_two_pass_groupnorm_refuses_indices():
+    """The fp32 mode runs GroupNorm shapes its kernel does not take (here
+    3 x 3 windows, and 128 groups) as the conv then the chain's post-pass,
+    which computes no window indices: asking for them is UNSUPPORTED, while
+    the same shapes without indices match the oracle (test_small_parity)."""
+    import x3_conv2d_epilogue_gb300 as ce
+    for wl in (SMALL["c5_k3"], SMALL["c5_co128_g128"]):
+        t = synth.make_inputs(wl, seed=0)
+        with pytest.raises(ce.ConvEpiError) as info:
+            gpu_run(wl, t, ce.MODE_FP32, want_index=True)
+        assert ce.STATUS[info.value.status] == "UNSUPPORTED"
