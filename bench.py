@@ -433,7 +433,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="c4_scale_min", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", choices=["tf32", "fp32"], default="tf32")
     ap.add_argument("--layout", choices=["nchw", "nhwc"], default="nchw",
-                    help="memory layout of x handed to the library (nhwc: tf32 mode, channels last)")
+                    help="memory layout of x handed to the library (nhwc: channels last)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length for cpu_baseline")
     ap.add_argument("--cfg-cpu-seconds", type=float, default=4.0, help="oracle sample length per per_config entry")

@@ -77,8 +77,11 @@ typedef enum {
  * output NCHW in both). */
 typedef enum {
     CONV_EPI_LAYOUT_NCHW = 0, /* x[N][Cin][H][W], the layout the problem is stated in */
-    CONV_EPI_LAYOUT_NHWC = 1  /* x[N][H][W][Cin] (channels last).  tf32 mode only, Cin a multiple
-                                 of 4.  Each input tile is copied straight into the tensor core's
+    CONV_EPI_LAYOUT_NHWC = 1  /* x[N][H][W][Cin] (channels last).  fp32 mode: any Cin; a first
+                                 kernel transposes x into a handle-owned NCHW copy (one more read
+                                 and write of x), so results equal the NCHW run's bit for bit.
+                                 tf32 mode: Cin a multiple of 4 (else CONV_EPI_ERR_UNSUPPORTED).
+                                 Each input tile is copied straight into the tensor core's
                                  operand layout (four channels of a position are adjacent in both),
                                  so no conversion pass runs: the tensor core uses the top 19 bits
                                  of each fp32 input (its low 13 mantissa bits are dropped, i.e.

@@ -105,7 +105,7 @@ def test_bad_descriptions_rejected(lib, bad):
 
 
 @pytest.mark.parametrize("mode,cin,want", [
-    (ce.MODE_FP32, 8, 2),   # channels-last input is a tensor-core path only
+    (ce.MODE_FP32, 6, 4),   # accepted, any Cin (the fp32 mode works on an NCHW copy): reaches the device
     (ce.MODE_TF32, 6, 2),   # a position's channels must start on 16-byte boundaries
     (ce.MODE_TF32, 8, 4),   # accepted: the call reaches the (absent) device
 ])

@@ -309,3 +309,20 @@ def test_fp32_two_pass_groupnorm_refuses_indices():
         with pytest.raises(ce.ConvEpiError) as info:
             gpu_run(wl, t, ce.MODE_FP32, want_index=True)
         assert ce.STATUS[info.value.status] == "UNSUPPORTED"
+
+
+@pytest.mark.parametrize("case", ["c2_w255", "c3_w67", "c5_w37", "c5_k3", "min_w3", "c4_w262"])
+def test_channels_last_fp32_matches_nchw(case):
+    """The fp32 mode with channels-last input: an on-device transpose to
+    NCHW, then the same kernel, so values and indices equal the NCHW run's
+    bit for bit (any Cin; the tensor-core path needs Cin a multiple of 4)."""
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = SMALL[case]
+    t = synth.make_inputs(wl, seed=3)
+    want_index = fp32_indices(wl)
+    ref, ref_idx = gpu_run(wl, t, ce.MODE_FP32, want_index=want_index)
+    got, idx = gpu_run(wl, t, ce.MODE_FP32, want_index=want_index, layout=ce.LAYOUT_NHWC)
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
+    check_fp32(got, oracle_run(wl, t)[0], case)
+    if want_index:
+        np.testing.assert_array_equal(idx, ref_idx)

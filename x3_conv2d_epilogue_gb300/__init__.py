@@ -192,8 +192,8 @@ def conv_epi_plan_query(N, Cin, H, W, Cout, epi, layout=LAYOUT_NCHW):
 
 
 def conv_epi_create(N, Cin, H, W, Cout, mode=MODE_TF32, layout=LAYOUT_NCHW):
-    """layout: LAYOUT_NCHW (x[N][Cin][H][W]) or LAYOUT_NHWC (x[N][H][W][Cin],
-    tf32 mode, Cin a multiple of 4)."""
+    """layout: LAYOUT_NCHW (x[N][Cin][H][W]) or LAYOUT_NHWC (x[N][H][W][Cin];
+    tf32 mode needs Cin a multiple of 4, fp32 mode takes any Cin)."""
     h = C.c_void_p()
     d = Desc(N, Cin, H, W, Cout, mode, layout)
     _check(_lib().conv_epi_create(C.byref(d), C.byref(h)), "conv_epi_create")

@@ -94,9 +94,10 @@ void shape_of(const conv_epi_desc &d, const conv_epi_epilogue_desc &e, int64_t s
 }
 
 conv_epi_status check_mode_support(const conv_epi_desc &d, const conv_epi_epilogue_desc *e) {
-    // channels-last input feeds the tensor core directly: tf32 mode, and a
-    // position's channels must start on 16-byte boundaries
-    if (d.layout == CONV_EPI_LAYOUT_NHWC && (d.mode != CONV_EPI_MODE_TF32 || d.Cin % 4 != 0))
+    // channels-last input feeds the tensor core directly, so a position's
+    // channels must start on 16-byte boundaries there (the fp32 mode takes
+    // any Cin: it works on an NCHW copy)
+    if (d.layout == CONV_EPI_LAYOUT_NHWC && d.mode == CONV_EPI_MODE_TF32 && d.Cin % 4 != 0)
         return CONV_EPI_ERR_UNSUPPORTED;
     if (d.mode == CONV_EPI_MODE_FP32)
         return e ? conv_epi::simt_supported(d, *e) : CONV_EPI_OK;
@@ -225,9 +226,13 @@ CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi
         h->wpack_bytes = conv_epi::tc_wpack_bytes(*desc);
         e = cudaMalloc(&h->wpack, h->wpack_bytes);
     }
-    // tf32 NCHW rows not a multiple of 4 floats: room for the padded copy of x
-    if (e == cudaSuccess && (h->xpad_bytes = conv_epi::tc_xpad_bytes(*desc)) != 0)
-        e = cudaMalloc(&h->xpad, h->xpad_bytes);
+    // tf32 NCHW rows not a multiple of 4 floats: room for the padded copy of
+    // x; fp32 channels-last input: room for its NCHW copy
+    h->xpad_bytes = desc->mode == CONV_EPI_MODE_TF32 ? conv_epi::tc_xpad_bytes(*desc)
+                    : desc->layout == CONV_EPI_LAYOUT_NHWC
+                        ? (size_t)desc->N * desc->Cin * desc->H * desc->W * sizeof(float)
+                        : 0;
+    if (e == cudaSuccess && h->xpad_bytes != 0) e = cudaMalloc(&h->xpad, h->xpad_bytes);
     if (e != cudaSuccess) {
         st = conv_epi::cuda_fail(e, "conv_epi_create workspace");
         cudaFree(h->dev_err);

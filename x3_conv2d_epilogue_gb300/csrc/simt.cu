@@ -481,8 +481,58 @@ int simt_gn_units(const conv_epi_desc &d, int Ho, int pool_k) {
     return (Ho + pool_k - 1) / pool_k;
 }
 
+namespace {
+
+// Channels-last input for the fp32 kernel, which reads NCHW: per image, the
+// [H*W][Cin] plane transposed to [Cin][H*W] through a 32 x 33 shared tile
+// (coalesced reads along the channels, coalesced writes along the
+// positions).
+// Blocks along x run over (image, 32-position tile), along y over 32-channel
+// tiles.
+__global__ void __launch_bounds__(256) nhwc_to_nchw(const float *__restrict__ x, float *__restrict__ y, int C, int HW) {
+    __shared__ float tile[32][33];
+    const unsigned tiles = (unsigned)(HW + 31) / 32;
+    const int n = (int)(blockIdx.x / tiles);
+    const int p0 = (int)(blockIdx.x % tiles) * 32, c0 = blockIdx.y * 32;
+    const float *src = x + (size_t)n * HW * C;
+    float *dst = y + (size_t)n * C * HW;
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int p = p0 + r, c = c0 + threadIdx.x;
+        if (p < HW && c < C) tile[r][threadIdx.x] = src[(size_t)p * C + c];
+    }
+    __syncthreads();
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int c = c0 + r, p = p0 + threadIdx.x;
+        if (c < C && p < HW) dst[(size_t)c * HW + p] = tile[threadIdx.x][r];
+    }
+}
+
+}  // namespace
+
+conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float *w, const float *b,
+                                  const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
+
+// channels-last input: first its NCHW copy in the handle's buffer
 conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, const float *b,
                              const conv_epi_epilogue_desc &e, float *out, cudaStream_t s) {
+    const conv_epi_desc &d = h->d;
+    if (d.layout != CONV_EPI_LAYOUT_NHWC) return simt_forward_nchw(h, x, w, b, e, out, s);
+    const size_t need = (size_t)d.N * d.Cin * d.H * d.W * sizeof(float);
+    if (!h->xpad || h->xpad_bytes < need) return CONV_EPI_ERR_INVALID_ARG;  // conv_epi_create sizes it
+    if ((size_t)d.H * d.W > 0x7fffffe0u) return CONV_EPI_ERR_UNSUPPORTED;
+    const int HW = d.H * d.W;
+    const size_t gx = (size_t)((HW + 31) / 32) * d.N, gy = (size_t)(d.Cin + 31) / 32;
+    if (gx > 0x7fffffffu || gy > 65535) return CONV_EPI_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)gx, (unsigned)gy);
+    nhwc_to_nchw<<<grid, dim3(32, 8), 0, s>>>(x, h->xpad, d.Cin, HW);
+    CE_CUDA(cudaGetLastError());
+    const conv_epi_status st = simt_forward_nchw(h, h->xpad, w, b, e, out, s);
+    if (st == CONV_EPI_OK) h->last_launches += 1;
+    return st;
+}
+
+conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float *w, const float *b,
+                                  const conv_epi_epilogue_desc &e, float *out, cudaStream_t s) {
     const conv_epi_desc &d = h->d;
     const Layout L = layout_for(d, h->Wo);
     SimtArgs a{};
@@ -521,7 +571,7 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
                 return CONV_EPI_ERR_INVALID_ARG;  // conv_epi_reserve sizes it
             conv_epi_epilogue_desc plain{};
             plain.kind = CONV_EPI_NONE;
-            if ((st = simt_forward(h, x, w, b, plain, h->ybuf, s))) return st;
+            if ((st = simt_forward_nchw(h, x, w, b, plain, h->ybuf, s))) return st;
             const int conv_launches = h->last_launches;
             if ((st = postpass_forward(h, h->ybuf, e, out, s))) return st;
             h->last_launches += conv_launches;
