@@ -311,13 +311,22 @@ def test_fp32_two_pass_groupnorm_refuses_indices():
         assert ce.STATUS[info.value.status] == "UNSUPPORTED"
 
 
-@pytest.mark.parametrize("case", ["c2_w255", "c3_w67", "c5_w37", "c5_k3", "min_w3", "c4_w262"])
+CL_EXTRA = {
+    "c4_cin100": W["c4_scale_min"].resized(N=2, H=6, W=40, Cin=100),   # span transpose, 32 positions a block, ragged last
+    "c3_cin129": W["c3_mul_lrelu_gelu"].resized(N=1, H=5, W=37, Cin=129),   # tiled transpose, ragged tiles
+}
+
+
+@pytest.mark.parametrize("case", ["c2_w255", "c3_w67", "c5_w37", "c5_k3", "min_w3", "c4_w262", "c3cin3", "c4cin20",
+                                  "c2cin12", "c2_cin256", "c4_cin100", "c3_cin129"])
 def test_channels_last_fp32_matches_nchw(case):
     """The fp32 mode with channels-last input: an on-device transpose to
     NCHW, then the same kernel, so values and indices equal the NCHW run's
-    bit for bit (any Cin; the tensor-core path needs Cin a multiple of 4)."""
+    bit for bit (any Cin; the tensor-core path needs Cin a multiple of 4).
+    At most 128 channels go through the span transpose, more through 32 x 32
+    tiles."""
     import x3_conv2d_epilogue_gb300 as ce
-    wl = SMALL[case]
+    wl = SMALL.get(case) or CL_EXTRA[case]
     t = synth.make_inputs(wl, seed=3)
     want_index = fp32_indices(wl)
     ref, ref_idx = gpu_run(wl, t, ce.MODE_FP32, want_index=want_index)

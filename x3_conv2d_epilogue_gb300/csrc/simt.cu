@@ -507,6 +507,49 @@ __global__ void __launch_bounds__(256) nhwc_to_nchw(const float *__restrict__ x,
     }
 }
 
+// The same for at most 128 channels, with more bytes per block: a block
+// takes TP = (4096 / C) positions rounded down to a multiple of 32 (at least
+// 32), whose TP * C values are one contiguous span of x, reads the span
+// straight through (16 loads a thread in flight), and writes each channel's
+// run of TP positions.  The shared copy is [TP][C + 1]: for even C both
+// sides are free of bank conflicts.  (Below 32 channels a 32 x 32 tile would
+// also be mostly empty.)
+constexpr int kNarrowC = 128, kNarrowSpan = 4096, kNarrowThreads = 256;
+
+__host__ __device__ inline int narrow_tp(int C) { return kNarrowSpan / C / 32 * 32; }
+
+__global__ void __launch_bounds__(kNarrowThreads)
+    nhwc_to_nchw_narrow(const float *__restrict__ x, float *__restrict__ y, int C, int HW) {
+    __shared__ float tile[2 * kNarrowSpan];  // TP * (C + 1) = TP * C + TP <= 4096 + 4096
+    const int TP = narrow_tp(C);
+    const unsigned tiles = (unsigned)(HW + TP - 1) / TP;
+    const int n = (int)(blockIdx.x / tiles);
+    const int p0 = (int)(blockIdx.x % tiles) * TP;
+    const int np = HW - p0 < TP ? HW - p0 : TP;
+    const int span = np * C;
+    const float *src = x + ((size_t)n * HW + p0) * C;
+    float *dst = y + (size_t)n * C * HW + p0;
+    float v[kNarrowSpan / kNarrowThreads];
+#pragma unroll
+    for (int k = 0; k < kNarrowSpan / kNarrowThreads; ++k) {
+        const int e = threadIdx.x + k * kNarrowThreads;
+        if (e < span) v[k] = src[e];
+    }
+#pragma unroll
+    for (int k = 0; k < kNarrowSpan / kNarrowThreads; ++k) {
+        const int e = threadIdx.x + k * kNarrowThreads;
+        if (e < span) {
+            const int p = e / C, c = e - p * C;
+            tile[p * (C + 1) + c] = v[k];
+        }
+    }
+    __syncthreads();
+    for (int f = threadIdx.x; f < span; f += kNarrowThreads) {
+        const int c = f / np, p = f - c * np;
+        dst[(size_t)c * HW + p] = tile[p * (C + 1) + c];
+    }
+}
+
 }  // namespace
 
 conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float *w, const float *b,
@@ -521,10 +564,16 @@ conv_epi_status simt_forward(conv_epi_handle h, const float *x, const float *w, 
     if (!h->xpad || h->xpad_bytes < need) return CONV_EPI_ERR_INVALID_ARG;  // conv_epi_create sizes it
     if ((size_t)d.H * d.W > 0x7fffffe0u) return CONV_EPI_ERR_UNSUPPORTED;
     const int HW = d.H * d.W;
-    const size_t gx = (size_t)((HW + 31) / 32) * d.N, gy = (size_t)(d.Cin + 31) / 32;
-    if (gx > 0x7fffffffu || gy > 65535) return CONV_EPI_ERR_UNSUPPORTED;
-    const dim3 grid((unsigned)gx, (unsigned)gy);
-    nhwc_to_nchw<<<grid, dim3(32, 8), 0, s>>>(x, h->xpad, d.Cin, HW);
+    if (d.Cin <= kNarrowC) {
+        const int TP = narrow_tp(d.Cin);
+        const size_t gx = (size_t)((HW + TP - 1) / TP) * d.N;
+        if (gx > 0x7fffffffu) return CONV_EPI_ERR_UNSUPPORTED;
+        nhwc_to_nchw_narrow<<<(unsigned)gx, kNarrowThreads, 0, s>>>(x, h->xpad, d.Cin, HW);
+    } else {
+        const size_t gx = (size_t)((HW + 31) / 32) * d.N, gy = (size_t)(d.Cin + 31) / 32;
+        if (gx > 0x7fffffffu || gy > 65535) return CONV_EPI_ERR_UNSUPPORTED;
+        nhwc_to_nchw<<<dim3((unsigned)gx, (unsigned)gy), dim3(32, 8), 0, s>>>(x, h->xpad, d.Cin, HW);
+    }
     CE_CUDA(cudaGetLastError());
     const conv_epi_status st = simt_forward_nchw(h, h->xpad, w, b, e, out, s);
     if (st == CONV_EPI_OK) h->last_launches += 1;
