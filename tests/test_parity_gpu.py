@@ -91,6 +91,11 @@ SMALL = {
     "c5_k2_w240": W["c5_gn_pool_clamp"].resized(N=2, H=8, W=240, Cout=32, groups=8, pool_k=2),  # 119 windows
     "c5_k2_w256": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=256, Cout=32, groups=8, pool_k=2),  # NCHW two passes; channels last fused, 127 windows
     "c5_k1": W["c5_gn_pool_clamp"].resized(N=1, H=9, W=33, pool_k=1, groups=4),      # no pooling
+    # fp32 GroupNorm staging: two input-channel steps (rows staged per output
+    # row), and bands staged at once with rows of odd width and a short last band
+    "c5_cin20": W["c5_gn_pool_clamp"].resized(N=1, H=15, W=40, Cin=20),
+    "c5_cin13_w37": W["c5_gn_pool_clamp"].resized(N=2, H=12, W=37, Cin=13, Cout=32, groups=8),
+    "c5_cin16_k2": W["c5_gn_pool_clamp"].resized(N=1, H=11, W=52, Cin=16, pool_k=2),
     "c5_k2_w300": W["c5_gn_pool_clamp"].resized(N=1, H=8, W=300, pool_k=2, groups=64),  # 2 column tiles, a group per channel
     # GroupNorm shapes the fp32 kernel does not take (two passes there, no indices; tf32 too for pool_k 3)
     "c5_k3": W["c5_gn_pool_clamp"].resized(N=1, H=14, W=29, pool_k=3),

@@ -37,6 +37,8 @@ constexpr int kRowsPerCta = 4;  // output rows per CTA for the min and per-chann
 // dynamic shared memory per CTA: the 227 KB opt-in less the static group sums
 // and a margin
 constexpr size_t kSmemDynLimit = 227 * 1024 - 2 * 1024;
+// a GroupNorm band staged at once, where its tiles keep two CTAs per SM
+constexpr size_t kBandSmemLimit = 110 * 1024;
 
 struct SimtArgs {
     const float *x, *w, *b;
@@ -44,6 +46,8 @@ struct SimtArgs {
     int PG, CS;          // thread layout
     int units;           // CTAs per image
     int rpc;             // output rows per CTA (min and per-channel chains)
+    int xrows;           // input rows staged at a time: 3 (one output row), or
+                         // PK + 2 (a GroupNorm band's rows, staged once)
     int ntiles;          // pixel tiles of PG*4 columns along a row
     float scalar;        // MIN kinds
     const float *chan_scale;
@@ -90,17 +94,24 @@ __device__ __forceinline__ void cp_async4(float *dst, const float *src, int src_
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// KIND: conv_epi_kind; PK: pool kernel (GN only; 1, 2 or 4, dividing kPX)
-template <int KIND, int PK>
-__global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 : 2) simt_conv_epi(const SimtArgs a) {
+// KIND: conv_epi_kind; PK: pool kernel (GN only; 1, 2 or 4, dividing kPX);
+// CO: output channels per thread per pass (16, or 8 for the GroupNorm chain
+// where 16 would leave channel slots of the CTA empty: twice the threads, and
+// its per-channel band state in half the registers, so two CTAs fit an SM;
+// with 1 x 1 windows the state of four windows a channel does not fit 128
+// registers, and that instantiation keeps one CTA per SM)
+template <int KIND, int PK, int CO>
+__global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (CO == 16 || PK == 1) ? 1 : 2)
+    simt_conv_epi(const SimtArgs a) {
     extern __shared__ float4 smem_f4[];
     float *sm = reinterpret_cast<float *>(smem_f4);
     const int tid = threadIdx.x;
     const int PG = a.PG, CS = a.CS;
     const int tx = tid % PG, ty = tid / PG;
-    const int TW = PG * kPX, XW = TW + 4, COP = CS * kCO;
-    float *xs = sm;                  // [kCI][3][XW]
-    float *ws = sm + kCI * 3 * XW;   // [kCI][9][COP]
+    const int TW = PG * kPX, XW = TW + 4, COP = CS * CO;
+    const int NR = a.xrows;          // staged input rows
+    float *xs = sm;                  // [kCI][NR][XW]
+    float *ws = sm + kCI * NR * XW;  // [kCI][9][COP]
     const int n = blockIdx.x / a.units;
     const int u = blockIdx.x % a.units;
     constexpr bool kGN = KIND == CONV_EPI_GN_SCALE_POOL_CLAMP;
@@ -115,7 +126,12 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
     // the same for every row and column tile of the CTA and is staged once,
     // when the reductions' scratch (at the start of shared memory) stays
     // below it
-    const bool w_once = a.Cin <= kCI && a.Cout <= COP && 2 * CS * TW <= kCI * 3 * XW && 2 * COP * PG <= kCI * 3 * XW;
+    const bool w_once = a.Cin <= kCI && a.Cout <= COP && 2 * CS * TW <= kCI * NR * XW && 2 * COP * PG <= kCI * NR * XW;
+    // a GroupNorm band staged at once (one input-channel step, one channel
+    // pass, one pixel tile: the host sets xrows = PK + 2 only then): rows
+    // r0 .. r0 + PK + 1 are staged before the band's first row and serve all
+    // of its rows (rows at or past H, below a short last band, are zeros)
+    const bool band_once = kGN && NR > 3;
     // input rows of whole 16-byte groups (x itself is 16-byte aligned): the
     // staged rows then start on 16-byte boundaries too (XW and wo0 are
     // multiples of 4)
@@ -138,14 +154,14 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
         for (int p = 0; p < kPX; ++p) best[p] = 0.0f, bidx[p] = -1;
 
         for (int cobase = 0; cobase < a.Cout; cobase += COP) {
-            const int co0 = cobase + ty * kCO;
+            const int co0 = cobase + ty * CO;
             constexpr int WPT = kGN ? kPX / PK : 1;  // pooling windows per thread
-            float gs[kCO], gss[kCO];
-            float pmx[kCO][WPT], pmn[kCO][WPT];
-            int amx[kCO][WPT], amn[kCO][WPT];
+            float gs[CO], gss[CO];
+            float pmx[CO][WPT], pmn[CO][WPT];
+            int amx[CO][WPT], amn[CO][WPT];
             if (kGN) {
 #pragma unroll
-                for (int c = 0; c < kCO; ++c) {
+                for (int c = 0; c < CO; ++c) {
                     gs[c] = 0.0f, gss[c] = 0.0f;
 #pragma unroll
                     for (int j = 0; j < WPT; ++j) pmx[c][j] = -FLT_MAX, pmn[c][j] = FLT_MAX, amx[c][j] = -1, amn[c][j] = -1;
@@ -154,15 +170,21 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
             for (int r = r0; r < r1; ++r) {
                 // accumulators of channels 2h and 2h + 1 at pixel p, as one
                 // packed pair (acc2[h][p]) for the paired FMA
-                uint64_t acc2[kCO / 2][kPX];
+                uint64_t acc2[CO / 2][kPX];
 #pragma unroll
-                for (int h = 0; h < kCO / 2; ++h) {
+                for (int h = 0; h < CO / 2; ++h) {
                     const int c = co0 + 2 * h;
                     const float b0 = c < a.Cout ? __ldg(&a.b[c]) : 0.0f, b1 = c + 1 < a.Cout ? __ldg(&a.b[c + 1]) : 0.0f;
 #pragma unroll
                     for (int p = 0; p < kPX; ++p) acc2[h][p] = pair(b0, b1);
                 }
+                // first input row of the staged tile
+                const int rs = band_once ? r0 : r;
                 for (int ci0 = 0; ci0 < a.Cin; ci0 += kCI) {
+                    // channels staged and used in this step (the tiles past
+                    // them are never read)
+                    const int nci = min(kCI, a.Cin - ci0);
+                    if (!band_once || r == r0) {
                     __syncthreads();
                     // staging by asynchronous copies (every copy of a thread
                     // in flight at once, no register round trip), zero-filled
@@ -170,40 +192,40 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                     // each tile has its (channel, row or tap, column) stepped
                     // by the block size without divisions
                     if (xv4) {  // rows of whole 16-byte groups: one copy per 4 columns
-                        const int XW4 = XW >> 2, total = kCI * 3 * XW4;
-                        int col = tid % XW4, rr = (tid / XW4) % 3, ci = tid / (3 * XW4);
+                        const int XW4 = XW >> 2, total = nci * NR * XW4;
+                        int col = tid % XW4, rr = (tid / XW4) % NR, ci = tid / (NR * XW4);
                         for (int i = tid; i < total; i += blockDim.x) {
-                            const int gci = ci0 + ci, gw = wo0 + 4 * col;
-                            const int nv = gci < a.Cin ? max(0, min(4, a.W - gw)) : 0;
-                            const float *src = nv ? a.x + (((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw : a.x;
+                            const int gci = ci0 + ci, gw = wo0 + 4 * col, gr = rs + rr;
+                            const int nv = gr < a.H ? max(0, min(4, a.W - gw)) : 0;
+                            const float *src = nv ? a.x + (((size_t)n * a.Cin + gci) * a.H + gr) * a.W + gw : a.x;
                             cp_async16(xs + 4 * i, src, 4 * nv);
                             col += blockDim.x;
                             while (col >= XW4) {
                                 col -= XW4;
-                                if (++rr == 3) rr = 0, ++ci;
+                                if (++rr == NR) rr = 0, ++ci;
                             }
                         }
                     } else {
-                        const int total = kCI * 3 * XW;
-                        int col = tid % XW, rr = (tid / XW) % 3, ci = tid / (3 * XW);
+                        const int total = nci * NR * XW;
+                        int col = tid % XW, rr = (tid / XW) % NR, ci = tid / (NR * XW);
                         for (int i = tid; i < total; i += blockDim.x) {
-                            const int gci = ci0 + ci, gw = wo0 + col;
-                            const bool ok = gci < a.Cin && gw < a.W;
-                            cp_async4(xs + i, ok ? a.x + (((size_t)n * a.Cin + gci) * a.H + (r + rr)) * a.W + gw : a.x,
+                            const int gci = ci0 + ci, gw = wo0 + col, gr = rs + rr;
+                            const bool ok = gr < a.H && gw < a.W;
+                            cp_async4(xs + i, ok ? a.x + (((size_t)n * a.Cin + gci) * a.H + gr) * a.W + gw : a.x,
                                       ok ? 4 : 0);
                             col += blockDim.x;
                             while (col >= XW) {
                                 col -= XW;
-                                if (++rr == 3) rr = 0, ++ci;
+                                if (++rr == NR) rr = 0, ++ci;
                             }
                         }
                     }
                     if (!w_once || (row == row_lo && t == 0 && r == r0)) {
-                        const int total = kCI * 9 * COP;
+                        const int total = nci * 9 * COP;
                         int col = tid % COP, tap = (tid / COP) % 9, ci = tid / (9 * COP);
                         for (int i = tid; i < total; i += blockDim.x) {
                             const int gci = ci0 + ci, gco = cobase + col;
-                            const bool ok = gci < a.Cin && gco < a.Cout;
+                            const bool ok = gco < a.Cout;
                             cp_async4(ws + i, ok ? a.w + ((size_t)gco * a.Cin + gci) * 9 + tap : a.w, ok ? 4 : 0);
                             col += blockDim.x;
                             while (col >= COP) {
@@ -214,11 +236,11 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                     }
                     cp_async_wait_all();
                     __syncthreads();
-                    const int nci = min(kCI, a.Cin - ci0);
+                    }
                     for (int ci = 0; ci < nci; ++ci) {
 #pragma unroll
                         for (int kh = 0; kh < 3; ++kh) {
-                            const float *xr = xs + (ci * 3 + kh) * XW + tx * kPX;
+                            const float *xr = xs + (ci * NR + (r - rs) + kh) * XW + tx * kPX;
                             const float4 xa = *reinterpret_cast<const float4 *>(xr);
                             const float2 xb = *reinterpret_cast<const float2 *>(xr + 4);
                             // each input value twice, as the pair that meets two channels' taps
@@ -228,24 +250,24 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                             for (int kw = 0; kw < 3; ++kw) {
                                 // the taps of channels 2h, 2h + 1: adjacent in the staged filter
                                 const ulonglong2 *wr =
-                                    reinterpret_cast<const ulonglong2 *>(ws + (ci * 9 + kh * 3 + kw) * COP + ty * kCO);
-                                uint64_t w2[kCO / 2];
+                                    reinterpret_cast<const ulonglong2 *>(ws + (ci * 9 + kh * 3 + kw) * COP + ty * CO);
+                                uint64_t w2[CO / 2];
 #pragma unroll
-                                for (int q = 0; q < kCO / 4; ++q) {
+                                for (int q = 0; q < CO / 4; ++q) {
                                     const ulonglong2 f = wr[q];
                                     w2[2 * q] = f.x, w2[2 * q + 1] = f.y;
                                 }
 #pragma unroll
-                                for (int h = 0; h < kCO / 2; ++h)
+                                for (int h = 0; h < CO / 2; ++h)
 #pragma unroll
                                     for (int p = 0; p < kPX; ++p) acc2[h][p] = fma_pair(w2[h], xd[p + kw], acc2[h][p]);
                             }
                         }
                     }
                 }
-                float acc[kCO][kPX];
+                float acc[CO][kPX];
 #pragma unroll
-                for (int h = 0; h < kCO / 2; ++h)
+                for (int h = 0; h < CO / 2; ++h)
 #pragma unroll
                     for (int p = 0; p < kPX; ++p) {
                         const float2 v = unpair(acc2[h][p]);
@@ -256,7 +278,7 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                 const int wbase = wo0 + tx * kPX;
                 if (kMin) {
 #pragma unroll
-                    for (int c = 0; c < kCO; ++c) {
+                    for (int c = 0; c < CO; ++c) {
                         if (co0 + c >= a.Cout) break;
 #pragma unroll
                         for (int p = 0; p < kPX; ++p) {
@@ -268,7 +290,7 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                 } else if (KIND == CONV_EPI_MUL_LRELU_GELU || KIND == CONV_EPI_NONE) {
                     if (wbase < a.Wo) {
 #pragma unroll
-                        for (int c = 0; c < kCO; ++c) {
+                        for (int c = 0; c < CO; ++c) {
                             const int co = co0 + c;
                             if (co >= a.Cout) break;
                             float o[kPX];
@@ -298,7 +320,7 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                 } else if (kGN) {
                     const bool prow = r < a.Hp * PK;
 #pragma unroll
-                    for (int c = 0; c < kCO; ++c) {
+                    for (int c = 0; c < CO; ++c) {
                         if (co0 + c >= a.Cout) break;
 #pragma unroll
                         for (int p = 0; p < kPX; ++p) {
@@ -322,7 +344,7 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                 // pooled max/min of this band (a full band only: u < Hp)
                 if (u < a.Hp) {
 #pragma unroll
-                    for (int c = 0; c < kCO; ++c) {
+                    for (int c = 0; c < CO; ++c) {
                         const int co = co0 + c;
                         if (co >= a.Cout) break;
 #pragma unroll
@@ -341,9 +363,9 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP ? 1 
                 __syncthreads();
                 float *S = sm, *SS = sm + COP * PG;  // [COP][PG] each
 #pragma unroll
-                for (int c = 0; c < kCO; ++c) {
-                    S[(ty * kCO + c) * PG + tx] = gs[c];
-                    SS[(ty * kCO + c) * PG + tx] = gss[c];
+                for (int c = 0; c < CO; ++c) {
+                    S[(ty * CO + c) * PG + tx] = gs[c];
+                    SS[(ty * CO + c) * PG + tx] = gss[c];
                 }
                 __syncthreads();
                 const int cpg = a.Cout / a.groups;
@@ -409,11 +431,13 @@ struct Layout {
     size_t smem;
 };
 
-Layout layout_for(const conv_epi_desc &d, int Wo) {
+// co: output channels per thread per pass (kCO, or 8 for gn_co's shapes);
+// nr: input rows staged at a time
+Layout layout_for(const conv_epi_desc &d, int Wo, int co = kCO, int nr = 3) {
     Layout L;
     L.PG = pow2ceil((Wo + kPX - 1) / kPX);
     if (L.PG > 64) L.PG = 64;
-    const int cg = (d.Cout + kCO - 1) / kCO;
+    const int cg = (d.Cout + co - 1) / co;
     L.CS = 256 / L.PG;
     if (L.CS > cg) L.CS = cg;
     L.TW = L.PG * kPX, L.XW = L.TW + 4;
@@ -422,8 +446,8 @@ Layout layout_for(const conv_epi_desc &d, int Wo) {
     // taps than a CTA's shared memory holds (many output channels, few pixel
     // groups); the channel passes then take the rest
     for (;;) {
-        L.COP = L.CS * kCO;
-        const size_t stage = (size_t)(kCI * 3 * L.XW + kCI * 9 * L.COP) * sizeof(float);
+        L.COP = L.CS * co;
+        const size_t stage = (size_t)(kCI * nr * L.XW + kCI * 9 * L.COP) * sizeof(float);
         const size_t red_min = (size_t)2 * L.CS * L.TW * sizeof(float);
         const size_t red_gn = (size_t)2 * L.COP * L.PG * sizeof(float);
         L.smem = stage;
@@ -435,9 +459,16 @@ Layout layout_for(const conv_epi_desc &d, int Wo) {
     return L;
 }
 
-template <int KIND, int PK>
+// the GroupNorm chain's channels per thread: 8 where 16 would leave the
+// CTA's channel slots (256 / pixel groups of them) partly empty
+int gn_co(const conv_epi_desc &d, int Wo) {
+    const Layout L = layout_for(d, Wo);
+    return L.PG * L.CS < 256 ? 8 : kCO;
+}
+
+template <int KIND, int PK, int CO = kCO>
 conv_epi_status launch(const SimtArgs &a, const Layout &L, int grid, cudaStream_t s) {
-    auto k = simt_conv_epi<KIND, PK>;
+    auto k = simt_conv_epi<KIND, PK, CO>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem));
     k<<<grid, L.PG * L.CS, L.smem, s>>>(a);
     CE_CUDA(cudaGetLastError());
@@ -595,6 +626,7 @@ conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float
     // input-channel step and one output-channel pass); otherwise one row per
     // CTA keeps more CTAs in flight (measured: 4 rows cost C3/C4 3-4%)
     a.rpc = (d.Cin <= kCI && d.Cout <= L.COP) ? kRowsPerCta : 1;
+    a.xrows = 3;
     conv_epi_status st;
     switch (e.kind) {
     case CONV_EPI_MIN_TANH2:
@@ -630,9 +662,31 @@ conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float
         a.gn = h->gn;
         a.Hp = h->gn.Hp, a.Wp = h->gn.Wp;
         if (h->gn.units != a.units) return CONV_EPI_ERR_INVALID_ARG;
-        if (e.pool_k == 4) st = launch<CONV_EPI_GN_SCALE_POOL_CLAMP, 4>(a, L, d.N * a.units, s);
-        else if (e.pool_k == 2) st = launch<CONV_EPI_GN_SCALE_POOL_CLAMP, 2>(a, L, d.N * a.units, s);
-        else st = launch<CONV_EPI_GN_SCALE_POOL_CLAMP, 1>(a, L, d.N * a.units, s);
+        constexpr int GN = CONV_EPI_GN_SCALE_POOL_CLAMP;
+        const int grid = d.N * a.units;
+        const int co = gn_co(d, h->Wo);
+        // a band's input rows staged once where one input-channel step, one
+        // channel pass and one pixel tile cover it, the layout stays the
+        // same and two CTAs still fit an SM's shared memory
+        {
+            const Layout L3 = layout_for(d, h->Wo, co), Lb = layout_for(d, h->Wo, co, e.pool_k + 2);
+            if (e.pool_k > 1 && d.Cin <= kCI && d.Cout <= Lb.COP && Lb.ntiles == 1 && Lb.CS == L3.CS &&
+                Lb.smem <= kBandSmemLimit)
+                a.xrows = e.pool_k + 2;
+        }
+        if (co == 8) {
+            const Layout L8 = layout_for(d, h->Wo, 8, a.xrows);
+            a.PG = L8.PG, a.CS = L8.CS, a.ntiles = L8.ntiles;
+            if (e.pool_k == 4) st = launch<GN, 4, 8>(a, L8, grid, s);
+            else if (e.pool_k == 2) st = launch<GN, 2, 8>(a, L8, grid, s);
+            else st = launch<GN, 1, 8>(a, L8, grid, s);
+        } else {
+            const Layout L16 = layout_for(d, h->Wo, kCO, a.xrows);
+            a.PG = L16.PG, a.CS = L16.CS, a.ntiles = L16.ntiles;
+            if (e.pool_k == 4) st = launch<GN, 4>(a, L16, grid, s);
+            else if (e.pool_k == 2) st = launch<GN, 2>(a, L16, grid, s);
+            else st = launch<GN, 1>(a, L16, grid, s);
+        }
         if (st) return st;
         h->last_launches = 1;
         st = gn_finalize(h, e, out, s, false);
