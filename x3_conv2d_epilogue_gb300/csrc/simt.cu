@@ -35,8 +35,8 @@ constexpr int kCO = 16;  // output channels per thread per pass
 constexpr int kPX = 4;   // consecutive output pixels per thread
 constexpr int kRowsPerCta = 4;  // output rows per CTA for the min and per-channel chains
 // dynamic shared memory per CTA: the 227 KB opt-in less the static group sums
-// and a margin
-constexpr size_t kSmemDynLimit = 227 * 1024 - 2 * 1024;
+// (5 KB) and a margin
+constexpr size_t kSmemDynLimit = 227 * 1024 - 6 * 1024;
 // a GroupNorm band staged at once, where its tiles keep two CTAs per SM
 constexpr size_t kBandSmemLimit = 110 * 1024;
 
@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
 
     // GroupNorm per-CTA group partial sums, in a fixed summation order
     __shared__ double gpart[2 * 64];
+    __shared__ double gred[2 * 256];  // per-thread partials of the group sums
     if (kGN) {
         for (int i = tid; i < 2 * 64; i += blockDim.x) gpart[i] = 0.0;
     }
@@ -368,14 +369,30 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                     SS[(ty * CO + c) * PG + tx] = gss[c];
                 }
                 __syncthreads();
+                // groups g0 .. g1 - 1 have channels in this pass; T threads
+                // a group each sum every T-th of its values (its channel rows
+                // of S are contiguous), then one thread a group adds the T
+                // partials in order: a fixed order with short fp64 chains
                 const int cpg = a.Cout / a.groups;
-                for (int g = tid; g < a.groups; g += blockDim.x) {
-                    const int c_lo = max(cobase, g * cpg), c_hi = min(min(cobase + COP, a.Cout), (g + 1) * cpg);
-                    double s = 0.0, ss = 0.0;
-                    for (int co = c_lo; co < c_hi; ++co)
-                        for (int q = 0; q < PG; ++q) s += S[(co - cobase) * PG + q], ss += SS[(co - cobase) * PG + q];
-                    gpart[2 * g] += s;
-                    gpart[2 * g + 1] += ss;
+                const int cend = min(cobase + COP, a.Cout);
+                const int g0 = cobase / cpg, g1 = (cend + cpg - 1) / cpg, ng = g1 - g0;
+                int T = 1;
+                while (2 * T * ng <= (int)blockDim.x && T < 64) T *= 2;
+                for (int i = tid; i < ng * T; i += blockDim.x) {
+                    const int g = g0 + i / T, k = i % T;
+                    const int c_lo = max(cobase, g * cpg), c_hi = min(cend, (g + 1) * cpg);
+                    const float *s0 = S + (c_lo - cobase) * PG, *ss0 = SS + (c_lo - cobase) * PG;
+                    const int nel = (c_hi - c_lo) * PG;
+                    double sv = 0.0, ssv = 0.0;
+                    for (int e = k; e < nel; e += T) sv += s0[e], ssv += ss0[e];
+                    gred[2 * i] = sv, gred[2 * i + 1] = ssv;
+                }
+                __syncthreads();
+                for (int gg = tid; gg < ng; gg += blockDim.x) {
+                    double sv = 0.0, ssv = 0.0;
+                    for (int k = 0; k < T; ++k) sv += gred[2 * (gg * T + k)], ssv += gred[2 * (gg * T + k) + 1];
+                    gpart[2 * (g0 + gg)] += sv;
+                    gpart[2 * (g0 + gg) + 1] += ssv;
                 }
             }
         }  // channel passes
