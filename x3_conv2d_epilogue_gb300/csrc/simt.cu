@@ -221,7 +221,26 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                             }
                         }
                     }
-                    if (!w_once || (row == row_lo && t == 0 && r == r0)) {
+                    if ((!w_once || (row == row_lo && t == 0 && r == r0)) && (blockDim.x & 3) == 0) {
+                        // the filter taps k = ci * 9 + tap of this step are
+                        // contiguous per output channel in w: a warp copies 8
+                        // channels x 4 consecutive taps (8 16-byte pieces of
+                        // w), into ws[k][co]; a thread keeps its tap lane kk
+                        const int KK = nci * 9, kk = tid & 3, step = blockDim.x >> 2;
+                        int co = (tid >> 2) % COP, kb = (tid >> 2) / COP;
+                        while (4 * kb < KK) {
+                            const int k = 4 * kb + kk, gco = cobase + co;
+                            if (k < KK) {
+                                const bool ok = gco < a.Cout;
+                                cp_async4(ws + k * COP + co, ok ? a.w + ((size_t)gco * a.Cin + ci0) * 9 + k : a.w,
+                                          ok ? 4 : 0);
+                            }
+                            co += step;
+                            while (co >= COP) co -= COP, ++kb;
+                        }
+                    } else if (!w_once || (row == row_lo && t == 0 && r == r0)) {
+                        // (blocks of fewer or an odd number of threads, on the
+                        // smallest shapes: one channel per thread, taps outer)
                         const int total = nci * 9 * COP;
                         int col = tid % COP, tap = (tid / COP) % 9, ci = tid / (9 * COP);
                         for (int i = tid; i < total; i += blockDim.x) {
