@@ -340,3 +340,17 @@ def test_channels_last_fp32_matches_nchw(case):
     check_fp32(got, oracle_run(wl, t)[0], case)
     if want_index:
         np.testing.assert_array_equal(idx, ref_idx)
+
+
+@pytest.mark.parametrize("case", ["c5s", "c5t", "c5_w37", "c5_k2", "c5_k1", "c5g1", "c5_cin20"])
+def test_fp32_groupnorm_values_do_not_depend_on_indices(case):
+    """The fp32 GroupNorm kernel tracks window indices only when index_out is
+    given; without it it keeps the extremes as values alone.  Both give the
+    same outputs bit for bit."""
+    import x3_conv2d_epilogue_gb300 as ce
+    wl = SMALL[case]
+    t = synth.make_inputs(wl, seed=5)
+    with_idx, _ = gpu_run(wl, t, ce.MODE_FP32, want_index=True)
+    without, _ = gpu_run(wl, t, ce.MODE_FP32, want_index=False)
+    np.testing.assert_array_equal(without.view(np.uint32), with_idx.view(np.uint32))
+    check_fp32(without, oracle_run(wl, t)[0], case)

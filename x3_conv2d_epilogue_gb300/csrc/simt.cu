@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
     // staged rows then start on 16-byte boundaries too (XW and wo0 are
     // multiples of 4)
     const bool xv4 = (a.W & 3) == 0;
+    // GroupNorm: window indices tracked and stored only when the caller asks
+    // for them (the finalize reads them only then)
+    const bool want_idx = a.idx != nullptr;
 
     // GroupNorm per-CTA group partial sums, in a fixed summation order
     __shared__ double gpart[2 * 64];
@@ -339,21 +342,42 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                     }
                 } else if (kGN) {
                     const bool prow = r < a.Hp * PK;
+                    if (want_idx) {
 #pragma unroll
-                    for (int c = 0; c < CO; ++c) {
-                        if (co0 + c >= a.Cout) break;
+                        for (int c = 0; c < CO; ++c) {
+                            if (co0 + c >= a.Cout) break;
 #pragma unroll
-                        for (int p = 0; p < kPX; ++p) {
-                            const int wo = wbase + p;
-                            if (wo >= a.Wo) continue;
-                            const float v = acc[c][p];
-                            gs[c] += v;
-                            gss[c] = fmaf(v, v, gss[c]);
-                            if (prow && wo < a.Wp * PK) {
-                                const int j = p / PK;
-                                const int off = (r - r0) * PK + (p % PK);
-                                if (amx[c][j] < 0 || v > pmx[c][j]) pmx[c][j] = v, amx[c][j] = off;
-                                if (amn[c][j] < 0 || v < pmn[c][j]) pmn[c][j] = v, amn[c][j] = off;
+                            for (int p = 0; p < kPX; ++p) {
+                                const int wo = wbase + p;
+                                if (wo >= a.Wo) continue;
+                                const float v = acc[c][p];
+                                gs[c] += v;
+                                gss[c] = fmaf(v, v, gss[c]);
+                                if (prow && wo < a.Wp * PK) {
+                                    const int j = p / PK;
+                                    const int off = (r - r0) * PK + (p % PK);
+                                    if (amx[c][j] < 0 || v > pmx[c][j]) pmx[c][j] = v, amx[c][j] = off;
+                                    if (amn[c][j] < 0 || v < pmn[c][j]) pmn[c][j] = v, amn[c][j] = off;
+                                }
+                            }
+                        }
+                    } else {
+                        // no indices asked for: the window extremes as values
+                        // only (the same values: conv outputs are finite)
+#pragma unroll
+                        for (int c = 0; c < CO; ++c) {
+                            if (co0 + c >= a.Cout) break;
+#pragma unroll
+                            for (int p = 0; p < kPX; ++p) {
+                                const int wo = wbase + p;
+                                if (wo >= a.Wo) continue;
+                                const float v = acc[c][p];
+                                gs[c] += v;
+                                gss[c] = fmaf(v, v, gss[c]);
+                                if (prow && wo < a.Wp * PK) {
+                                    pmx[c][p / PK] = fmaxf(pmx[c][p / PK], v);
+                                    pmn[c][p / PK] = fminf(pmn[c][p / PK], v);
+                                }
                             }
                         }
                     }
@@ -374,8 +398,7 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                             const size_t o = (((size_t)n * a.Cout + co) * a.Hp + u) * a.Wp + pw;
                             a.gn.pmax[o] = pmx[c][j];
                             a.gn.pmin[o] = pmn[c][j];
-                            a.gn.amax[o] = amx[c][j];
-                            a.gn.amin[o] = amn[c][j];
+                            if (want_idx) a.gn.amax[o] = amx[c][j], a.gn.amin[o] = amn[c][j];
                         }
                     }
                 }
