@@ -37,7 +37,8 @@ constexpr int kRowsPerCta = 4;  // output rows per CTA for the min and per-chann
 // dynamic shared memory per CTA: the 227 KB opt-in less the static group sums
 // (5 KB) and a margin
 constexpr size_t kSmemDynLimit = 227 * 1024 - 6 * 1024;
-// a GroupNorm band staged at once, where its tiles keep two CTAs per SM
+// a GroupNorm band staged at once, or the min and per-channel chains' ring
+// of input rows, where the CTA's tiles keep two CTAs per SM
 constexpr size_t kBandSmemLimit = 110 * 1024;
 
 struct SimtArgs {
@@ -47,7 +48,9 @@ struct SimtArgs {
     int units;           // CTAs per image
     int rpc;             // output rows per CTA (min and per-channel chains)
     int xrows;           // input rows staged at a time: 3 (one output row), or
-                         // PK + 2 (a GroupNorm band's rows, staged once)
+                         // PK + 2 (a GroupNorm band's rows, staged once), or
+                         // 4 (ring: a slot per input row, see below)
+    int ring;            // min and per-channel chains: input rows in a ring of 4
     int ntiles;          // pixel tiles of PG*4 columns along a row
     float scalar;        // MIN kinds
     const float *chan_scale;
@@ -132,6 +135,14 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
     // r0 .. r0 + PK + 1 are staged before the band's first row and serve all
     // of its rows (rows at or past H, below a short last band, are zeros)
     const bool band_once = kGN && NR > 3;
+    // min and per-channel chains with several rows per CTA, one input-channel
+    // step, one channel pass and one pixel tile (the host sets ring then,
+    // with xrows = 4): input row ir lives in slot ir & 3; the CTA's first row
+    // stages three rows, and each row then prefetches the one input row the
+    // next needs (into the slot of the row just finished) while it computes.
+    // The min chain's scratch then lies past the filter tile.
+    const bool ring = !kGN && a.ring && w_once;
+    float *red = ring ? ws + kCI * 9 * COP : sm;
     // input rows of whole 16-byte groups (x itself is 16-byte aligned): the
     // staged rows then start on 16-byte boundaries too (XW and wo0 are
     // multiples of 4)
@@ -188,42 +199,54 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                     // channels staged and used in this step (the tiles past
                     // them are never read)
                     const int nci = min(kCI, a.Cin - ci0);
-                    if (!band_once || r == r0) {
-                    __syncthreads();
-                    // staging by asynchronous copies (every copy of a thread
+                    // input rows ra .. ra + nrows - 1 of the step's channels
+                    // into their tile rows (ir - rs, or slot ir & 3 in the
+                    // ring), by asynchronous copies (every copy of a thread
                     // in flight at once, no register round trip), zero-filled
-                    // past W, Cin and Cout; element (or 4-float group) i of
-                    // each tile has its (channel, row or tap, column) stepped
-                    // by the block size without divisions
-                    if (xv4) {  // rows of whole 16-byte groups: one copy per 4 columns
-                        const int XW4 = XW >> 2, total = nci * NR * XW4;
-                        int col = tid % XW4, rr = (tid / XW4) % NR, ci = tid / (NR * XW4);
-                        for (int i = tid; i < total; i += blockDim.x) {
-                            const int gci = ci0 + ci, gw = wo0 + 4 * col, gr = rs + rr;
-                            const int nv = gr < a.H ? max(0, min(4, a.W - gw)) : 0;
-                            const float *src = nv ? a.x + (((size_t)n * a.Cin + gci) * a.H + gr) * a.W + gw : a.x;
-                            cp_async16(xs + 4 * i, src, 4 * nv);
-                            col += blockDim.x;
-                            while (col >= XW4) {
-                                col -= XW4;
-                                if (++rr == NR) rr = 0, ++ci;
+                    // past W and H; each copy's (channel, row, column) is
+                    // stepped by the block size without divisions
+                    auto stage_x = [&](int ra, int nrows) {
+                        if (xv4) {  // rows of whole 16-byte groups: one copy per 4 columns
+                            const int XW4 = XW >> 2, total = nci * nrows * XW4;
+                            int col = tid % XW4, rr = (tid / XW4) % nrows, ci = tid / (nrows * XW4);
+                            for (int i = tid; i < total; i += blockDim.x) {
+                                const int gci = ci0 + ci, gw = wo0 + 4 * col, gr = ra + rr;
+                                const int nv = gr < a.H ? max(0, min(4, a.W - gw)) : 0;
+                                const float *src = nv ? a.x + (((size_t)n * a.Cin + gci) * a.H + gr) * a.W + gw : a.x;
+                                const int srow = ring ? (gr & 3) : gr - rs;
+                                cp_async16(xs + ((ci * NR + srow) * XW4 + col) * 4, src, 4 * nv);
+                                col += blockDim.x;
+                                while (col >= XW4) {
+                                    col -= XW4;
+                                    if (++rr == nrows) rr = 0, ++ci;
+                                }
+                            }
+                        } else {
+                            const int total = nci * nrows * XW;
+                            int col = tid % XW, rr = (tid / XW) % nrows, ci = tid / (nrows * XW);
+                            for (int i = tid; i < total; i += blockDim.x) {
+                                const int gci = ci0 + ci, gw = wo0 + col, gr = ra + rr;
+                                const bool ok = gr < a.H && gw < a.W;
+                                const int srow = ring ? (gr & 3) : gr - rs;
+                                cp_async4(xs + (ci * NR + srow) * XW + col,
+                                          ok ? a.x + (((size_t)n * a.Cin + gci) * a.H + gr) * a.W + gw : a.x, ok ? 4 : 0);
+                                col += blockDim.x;
+                                while (col >= XW) {
+                                    col -= XW;
+                                    if (++rr == nrows) rr = 0, ++ci;
+                                }
                             }
                         }
-                    } else {
-                        const int total = nci * NR * XW;
-                        int col = tid % XW, rr = (tid / XW) % NR, ci = tid / (NR * XW);
-                        for (int i = tid; i < total; i += blockDim.x) {
-                            const int gci = ci0 + ci, gw = wo0 + col, gr = rs + rr;
-                            const bool ok = gr < a.H && gw < a.W;
-                            cp_async4(xs + i, ok ? a.x + (((size_t)n * a.Cin + gci) * a.H + gr) * a.W + gw : a.x,
-                                      ok ? 4 : 0);
-                            col += blockDim.x;
-                            while (col >= XW) {
-                                col -= XW;
-                                if (++rr == NR) rr = 0, ++ci;
-                            }
-                        }
+                    };
+                    // ring, after the CTA's first row: the prefetched row has
+                    // landed and every thread is past the previous row
+                    if (ring && row > row_lo) {
+                        cp_async_wait_all();
+                        __syncthreads();
                     }
+                    if (ring ? row == row_lo : (!band_once || r == r0)) {
+                    __syncthreads();
+                    stage_x(ring ? row : rs, ring ? 3 : NR);
                     if ((!w_once || (row == row_lo && t == 0 && r == r0)) && (blockDim.x & 3) == 0) {
                         // the filter taps k = ci * 9 + tap of this step are
                         // contiguous per output channel in w: a warp copies 8
@@ -260,10 +283,13 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                     cp_async_wait_all();
                     __syncthreads();
                     }
+                    // ring: the next row's new input row, in flight during this row
+                    if (ring && row + 1 < row_hi) stage_x(row + 3, 1);
                     for (int ci = 0; ci < nci; ++ci) {
 #pragma unroll
                         for (int kh = 0; kh < 3; ++kh) {
-                            const float *xr = xs + (ci * NR + (r - rs) + kh) * XW + tx * kPX;
+                            const int srow = ring ? ((r + kh) & 3) : (r - rs) + kh;
+                            const float *xr = xs + (ci * NR + srow) * XW + tx * kPX;
                             const float4 xa = *reinterpret_cast<const float4 *>(xr);
                             const float2 xb = *reinterpret_cast<const float2 *>(xr + 4);
                             // each input value twice, as the pair that meets two channels' taps
@@ -442,8 +468,8 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
         if (kMin) {
             // combine the CS channel slots: lowest value, then lowest channel
             __syncthreads();
-            float *rv = sm;
-            int *ri = reinterpret_cast<int *>(sm + CS * TW);
+            float *rv = red;
+            int *ri = reinterpret_cast<int *>(red + CS * TW);
 #pragma unroll
             for (int p = 0; p < kPX; ++p) rv[ty * TW + tx * kPX + p] = best[p], ri[ty * TW + tx * kPX + p] = bidx[p];
             __syncthreads();
@@ -686,23 +712,40 @@ conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float
     // CTA keeps more CTAs in flight (measured: 4 rows cost C3/C4 3-4%)
     a.rpc = (d.Cin <= kCI && d.Cout <= L.COP) ? kRowsPerCta : 1;
     a.xrows = 3;
+    a.ring = 0;
+    // the min and per-channel chains with several rows per CTA and one pixel
+    // tile keep the input rows in a ring of four slots (the layout unchanged,
+    // the filter staged once, and the tiles plus the min chain's scratch still
+    // two CTAs to an SM)
+    Layout LL = L;
+    if (e.kind != CONV_EPI_GN_SCALE_POOL_CLAMP && a.rpc > 1) {
+        const Layout Lr = layout_for(d, h->Wo, kCO, 4);
+        const int x4 = kCI * 4 * Lr.XW;
+        const bool w_once = d.Cin <= kCI && d.Cout <= Lr.COP && 2 * Lr.CS * Lr.TW <= x4 && 2 * Lr.COP * Lr.PG <= x4;
+        const size_t smem = (size_t)(x4 + kCI * 9 * Lr.COP + 2 * Lr.CS * Lr.TW) * sizeof(float);
+        if (w_once && Lr.ntiles == 1 && Lr.CS == L.CS && smem <= kBandSmemLimit) {
+            a.ring = 1, a.xrows = 4;
+            LL = Lr;
+            LL.smem = smem;
+        }
+    }
     conv_epi_status st;
     switch (e.kind) {
     case CONV_EPI_MIN_TANH2:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_MIN_TANH2, 1>(a, L, d.N * a.units, s);
+        st = launch<CONV_EPI_MIN_TANH2, 1>(a, LL, d.N * a.units, s);
         break;
     case CONV_EPI_SCALE_MIN:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_SCALE_MIN, 1>(a, L, d.N * a.units, s);
+        st = launch<CONV_EPI_SCALE_MIN, 1>(a, LL, d.N * a.units, s);
         break;
     case CONV_EPI_MUL_LRELU_GELU:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_MUL_LRELU_GELU, 1>(a, L, d.N * a.units, s);
+        st = launch<CONV_EPI_MUL_LRELU_GELU, 1>(a, LL, d.N * a.units, s);
         break;
     case CONV_EPI_NONE:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_NONE, 1>(a, L, d.N * a.units, s);
+        st = launch<CONV_EPI_NONE, 1>(a, LL, d.N * a.units, s);
         break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP: {
         if (simt_gn_two_pass(e)) {
