@@ -76,6 +76,11 @@ __device__ __forceinline__ float2 unpair(uint64_t v) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
     return r;
 }
+__device__ __forceinline__ uint64_t add_pair(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ uint64_t fma_pair(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -171,13 +176,16 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
         for (int cobase = 0; cobase < a.Cout; cobase += COP) {
             const int co0 = cobase + ty * CO;
             constexpr int WPT = kGN ? kPX / PK : 1;  // pooling windows per thread
-            float gs[CO], gss[CO];
+            // GroupNorm sums of y and y^2 for channels 2h, 2h + 1 as packed
+            // pairs (each half added in the same order as a scalar sum)
+            uint64_t gs2[CO / 2], gss2[CO / 2];
             float pmx[CO][WPT], pmn[CO][WPT];
             int amx[CO][WPT], amn[CO][WPT];
             if (kGN) {
 #pragma unroll
+                for (int h = 0; h < CO / 2; ++h) gs2[h] = gss2[h] = pair(0.0f, 0.0f);
+#pragma unroll
                 for (int c = 0; c < CO; ++c) {
-                    gs[c] = 0.0f, gss[c] = 0.0f;
 #pragma unroll
                     for (int j = 0; j < WPT; ++j) pmx[c][j] = -FLT_MAX, pmn[c][j] = FLT_MAX, amx[c][j] = -1, amn[c][j] = -1;
                 }
@@ -368,6 +376,16 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                     }
                 } else if (kGN) {
                     const bool prow = r < a.Hp * PK;
+                    // the sums over this row's pixels inside the row (the
+                    // channels past Cout have zero filters and bias: their
+                    // sums stay 0 and are never read)
+#pragma unroll
+                    for (int p = 0; p < kPX; ++p)
+                        if (wbase + p < a.Wo) {
+#pragma unroll
+                            for (int h = 0; h < CO / 2; ++h)
+                                gs2[h] = add_pair(gs2[h], acc2[h][p]), gss2[h] = fma_pair(acc2[h][p], acc2[h][p], gss2[h]);
+                        }
                     if (want_idx) {
 #pragma unroll
                         for (int c = 0; c < CO; ++c) {
@@ -377,8 +395,6 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                                 const int wo = wbase + p;
                                 if (wo >= a.Wo) continue;
                                 const float v = acc[c][p];
-                                gs[c] += v;
-                                gss[c] = fmaf(v, v, gss[c]);
                                 if (prow && wo < a.Wp * PK) {
                                     const int j = p / PK;
                                     const int off = (r - r0) * PK + (p % PK);
@@ -398,8 +414,6 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                                 const int wo = wbase + p;
                                 if (wo >= a.Wo) continue;
                                 const float v = acc[c][p];
-                                gs[c] += v;
-                                gss[c] = fmaf(v, v, gss[c]);
                                 if (prow && wo < a.Wp * PK) {
                                     pmx[c][p / PK] = fmaxf(pmx[c][p / PK], v);
                                     pmn[c][p / PK] = fminf(pmn[c][p / PK], v);
@@ -432,9 +446,10 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                 __syncthreads();
                 float *S = sm, *SS = sm + COP * PG;  // [COP][PG] each
 #pragma unroll
-                for (int c = 0; c < CO; ++c) {
-                    S[(ty * CO + c) * PG + tx] = gs[c];
-                    SS[(ty * CO + c) * PG + tx] = gss[c];
+                for (int h = 0; h < CO / 2; ++h) {
+                    const float2 sv = unpair(gs2[h]), qv = unpair(gss2[h]);
+                    S[(ty * CO + 2 * h) * PG + tx] = sv.x, S[(ty * CO + 2 * h + 1) * PG + tx] = sv.y;
+                    SS[(ty * CO + 2 * h) * PG + tx] = qv.x, SS[(ty * CO + 2 * h + 1) * PG + tx] = qv.y;
                 }
                 __syncthreads();
                 // groups g0 .. g1 - 1 have channels in this pass; T threads
