@@ -71,6 +71,9 @@ conv_epi_status check_epi(const conv_epi_desc &d, const conv_epi_epilogue_desc *
     }
 }
 
+// bytes of the fp32 kernel's packed filter (simt.cu)
+size_t simt_wpack_bytes(const conv_epi_desc &d);
+
 }  // namespace conv_epi
 
 namespace {
@@ -222,8 +225,11 @@ CONV_EPI_API conv_epi_status conv_epi_create(const conv_epi_desc *desc, conv_epi
     h->debug = dbg && dbg[0] == '1' && dbg[1] == '\0';
     cudaError_t e = cudaMalloc(&h->dev_err, 256);
     if (e == cudaSuccess) e = cudaMemset(h->dev_err, 0, 256);
-    if (e == cudaSuccess && desc->mode == CONV_EPI_MODE_TF32) {
-        h->wpack_bytes = conv_epi::tc_wpack_bytes(*desc);
+    // the packed filter: tf32 operands for the tensor-core kernel, or the fp32
+    // kernel's staging order
+    if (e == cudaSuccess) {
+        h->wpack_bytes = desc->mode == CONV_EPI_MODE_TF32 ? conv_epi::tc_wpack_bytes(*desc)
+                                                          : conv_epi::simt_wpack_bytes(*desc);
         e = cudaMalloc(&h->wpack, h->wpack_bytes);
     }
     // tf32 NCHW rows not a multiple of 4 floats: room for the padded copy of

@@ -51,6 +51,8 @@ struct SimtArgs {
                          // PK + 2 (a GroupNorm band's rows, staged once), or
                          // 4 (ring: a slot per input row, see below)
     int ring;            // min and per-channel chains: input rows in a ring of 4
+    const float *wpk;    // the filter packed as [pass][Cin * 9][COP] (zeros past
+                         // Cout), so a step's tile is one contiguous copy
     int ntiles;          // pixel tiles of PG*4 columns along a row
     float scalar;        // MIN kinds
     const float *chan_scale;
@@ -255,7 +257,14 @@ __global__ void __launch_bounds__(256, KIND == CONV_EPI_GN_SCALE_POOL_CLAMP && (
                     if (ring ? row == row_lo : (!band_once || r == r0)) {
                     __syncthreads();
                     stage_x(ring ? row : rs, ring ? 3 : NR);
-                    if ((!w_once || (row == row_lo && t == 0 && r == r0)) && (blockDim.x & 3) == 0) {
+                    if ((!w_once || (row == row_lo && t == 0 && r == r0)) && a.wpk) {
+                        // the step's [nci * 9][COP] tile is contiguous in the
+                        // packed filter (COP is a multiple of 8: whole
+                        // 16-byte pieces, 16-byte aligned)
+                        const int n4 = nci * 9 * COP / 4;
+                        const float *src = a.wpk + ((size_t)(cobase / COP) * a.Cin * 9 + ci0 * 9) * COP;
+                        for (int i = tid; i < n4; i += blockDim.x) cp_async16(ws + 4 * i, src + 4 * i, 16);
+                    } else if ((!w_once || (row == row_lo && t == 0 && r == r0)) && (blockDim.x & 3) == 0) {
                         // the filter taps k = ci * 9 + tap of this step are
                         // contiguous per output channel in w: a warp copies 8
                         // channels x 4 consecutive taps (8 16-byte pieces of
@@ -566,8 +575,35 @@ int gn_co(const conv_epi_desc &d, int Wo) {
     return L.PG * L.CS < 256 ? 8 : kCO;
 }
 
+// The filter in the order the conv kernel stages it: pass p (output
+// channels p * COP ..), then channel-tap q = ci * 9 + tap, then the pass's
+// COP channels (zeros past Cout), so one input-channel step of one pass is a
+// contiguous [nci * 9][COP] block.
+__global__ void __launch_bounds__(256) pack_filter(const float *__restrict__ w, float *__restrict__ wp, int Cout,
+                                                   int Cin, int COP, size_t total) {
+    const int K = Cin * 9;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int col = (int)(i % COP);
+        const size_t rq = i / COP;
+        const int q = (int)(rq % K), p = (int)(rq / K);
+        const int co = p * COP + col;
+        wp[i] = co < Cout ? w[(size_t)co * K + q] : 0.0f;
+    }
+}
+
+// wpack (bytes wbytes): the handle's buffer for the packed filter; where it
+// holds this layout's packing, the filter is packed first (one more launch,
+// counted by the caller) and the kernel stages from it
 template <int KIND, int PK, int CO = kCO>
-conv_epi_status launch(const SimtArgs &a, const Layout &L, int grid, cudaStream_t s) {
+conv_epi_status launch(SimtArgs a, const Layout &L, int grid, cudaStream_t s, float *wpack, size_t wbytes) {
+    const size_t total = (size_t)((a.Cout + L.COP - 1) / L.COP) * L.COP * a.Cin * 9;
+    a.wpk = nullptr;
+    if (wpack && total * sizeof(float) <= wbytes) {
+        const size_t blocks = (total + 255) / 256;
+        pack_filter<<<(unsigned)(blocks < 1024 ? blocks : 1024), 256, 0, s>>>(a.w, wpack, a.Cout, a.Cin, L.COP, total);
+        CE_CUDA(cudaGetLastError());
+        a.wpk = wpack;
+    }
     auto k = simt_conv_epi<KIND, PK, CO>;
     CE_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem));
     k<<<grid, L.PG * L.CS, L.smem, s>>>(a);
@@ -683,6 +719,18 @@ __global__ void __launch_bounds__(kNarrowThreads)
 
 }  // namespace
 
+// bytes of the packed filter for either channel count a thread may take
+size_t simt_wpack_bytes(const conv_epi_desc &d) {
+    const int Wo = d.W - 2;
+    size_t most = 0;
+    for (int co : {kCO, 8}) {
+        const Layout L = layout_for(d, Wo, co);
+        const size_t n = (size_t)((d.Cout + L.COP - 1) / L.COP) * L.COP * d.Cin * 9;
+        if (n > most) most = n;
+    }
+    return most * sizeof(float);
+}
+
 conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float *w, const float *b,
                                   const conv_epi_epilogue_desc &e, float *out, cudaStream_t s);
 
@@ -744,23 +792,24 @@ conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float
             LL.smem = smem;
         }
     }
+    const int packs = h->wpack ? 1 : 0;  // the filter-pack launch before the conv kernel
     conv_epi_status st;
     switch (e.kind) {
     case CONV_EPI_MIN_TANH2:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_MIN_TANH2, 1>(a, LL, d.N * a.units, s);
+        st = launch<CONV_EPI_MIN_TANH2, 1>(a, LL, d.N * a.units, s, h->wpack, h->wpack_bytes);
         break;
     case CONV_EPI_SCALE_MIN:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_SCALE_MIN, 1>(a, LL, d.N * a.units, s);
+        st = launch<CONV_EPI_SCALE_MIN, 1>(a, LL, d.N * a.units, s, h->wpack, h->wpack_bytes);
         break;
     case CONV_EPI_MUL_LRELU_GELU:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_MUL_LRELU_GELU, 1>(a, LL, d.N * a.units, s);
+        st = launch<CONV_EPI_MUL_LRELU_GELU, 1>(a, LL, d.N * a.units, s, h->wpack, h->wpack_bytes);
         break;
     case CONV_EPI_NONE:
         a.units = (h->Ho + a.rpc - 1) / a.rpc;
-        st = launch<CONV_EPI_NONE, 1>(a, LL, d.N * a.units, s);
+        st = launch<CONV_EPI_NONE, 1>(a, LL, d.N * a.units, s, h->wpack, h->wpack_bytes);
         break;
     case CONV_EPI_GN_SCALE_POOL_CLAMP: {
         if (simt_gn_two_pass(e)) {
@@ -794,26 +843,26 @@ conv_epi_status simt_forward_nchw(conv_epi_handle h, const float *x, const float
         if (co == 8) {
             const Layout L8 = layout_for(d, h->Wo, 8, a.xrows);
             a.PG = L8.PG, a.CS = L8.CS, a.ntiles = L8.ntiles;
-            if (e.pool_k == 4) st = launch<GN, 4, 8>(a, L8, grid, s);
-            else if (e.pool_k == 2) st = launch<GN, 2, 8>(a, L8, grid, s);
-            else st = launch<GN, 1, 8>(a, L8, grid, s);
+            if (e.pool_k == 4) st = launch<GN, 4, 8>(a, L8, grid, s, h->wpack, h->wpack_bytes);
+            else if (e.pool_k == 2) st = launch<GN, 2, 8>(a, L8, grid, s, h->wpack, h->wpack_bytes);
+            else st = launch<GN, 1, 8>(a, L8, grid, s, h->wpack, h->wpack_bytes);
         } else {
             const Layout L16 = layout_for(d, h->Wo, kCO, a.xrows);
             a.PG = L16.PG, a.CS = L16.CS, a.ntiles = L16.ntiles;
-            if (e.pool_k == 4) st = launch<GN, 4>(a, L16, grid, s);
-            else if (e.pool_k == 2) st = launch<GN, 2>(a, L16, grid, s);
-            else st = launch<GN, 1>(a, L16, grid, s);
+            if (e.pool_k == 4) st = launch<GN, 4>(a, L16, grid, s, h->wpack, h->wpack_bytes);
+            else if (e.pool_k == 2) st = launch<GN, 2>(a, L16, grid, s, h->wpack, h->wpack_bytes);
+            else st = launch<GN, 1>(a, L16, grid, s, h->wpack, h->wpack_bytes);
         }
         if (st) return st;
-        h->last_launches = 1;
+        h->last_launches = 1 + packs;
         st = gn_finalize(h, e, out, s, false);
-        if (st == CONV_EPI_OK) h->last_launches = 2;
+        if (st == CONV_EPI_OK) h->last_launches = 2 + packs;
         return st;
     }
     default:
         return CONV_EPI_ERR_INVALID_ARG;
     }
-    if (st == CONV_EPI_OK) h->last_launches = 1;
+    if (st == CONV_EPI_OK) h->last_launches = 1 + packs;
     return st;
 }
 
